@@ -1,0 +1,576 @@
+/*
+ * qoracle.c - the plain, slow, scalar CPU oracle for the ggml/GGUF
+ * block-quantized matrix-vector product.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or
+ * call this file: it is used by tests/, by the smoke check and by the CPU
+ * baseline leg of bench.py.  It shares no code, header, table or helper with
+ * the CUDA library.
+ *
+ * Build: gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared (see build.py).
+ * -ffp-contract=off forbids fused multiply-adds, so every float expression
+ * below rounds exactly as written.
+ *
+ * Sources (page titles and sections of the reference pages):
+ *   [rml]      "Quantization" (rayaq.ca/rml): The type table; Block layouts;
+ *              Unpacking the packed fields (Q4_K element-200 trace);
+ *              A worked example: Q4_0; Quantized dot products;
+ *              Kernels and references.
+ *   [sipllm]   "Quantization" (sipllm docs): On-disk block geometry;
+ *              Per-format dequant; The fused matmul.
+ *   [lesson21] "Building Q8_0 and Q4_0 Like ggml": Examples 1-2 (Q8_0 layout
+ *              and quantizer), 5-6 (Q4_0 scale, code rule, nibble order),
+ *              10 (Q8_0 x Q8_0 dot), 11 (Q4_0 x Q8_0 dot).
+ *   [candle]   "量化格式" (quantized formats, candle): GgmlDType table;
+ *              block structure table; "一些边界值" (special values);
+ *              VecDotType pairing table; vec_dot_unopt.
+ *
+ * Readings where the pages leave a step open (each is also listed in the
+ * design notes):
+ *   - Q8_K activation rule: the Q8_0 rule over 256 elements with d kept as
+ *     f32 (not rounded to f16), codes clamped to [-127, 127], and
+ *     bsums[k] = sum of codes 16k..16k+15.
+ *   - Q6_K element mapping: for e = 128h + 32k + l (h in 0..1, k in 0..3,
+ *     l in 0..31) the low 4 bits come from ql[64h + 32(k&1) + l] (low nibble
+ *     for k < 2, high nibble for k >= 2), the high 2 bits from
+ *     (qh[32h + l] >> 2k) & 3, and the sub-block scale is scales[e / 16].
+ *   - Q4_K sub-blocks 0..3: scale = scales[j] & 63, min = scales[j+4] & 63.
+ *   - NaN inputs to a quantizer are ignored by the amax and give code 0
+ *     (candle's special-value table).
+ *
+ * Parity pins: every function here is pinned by tests under tests/ against
+ * values the pages print, closed forms or brute force; the Q6_K element
+ * mapping and the Q8_K rule are pinned only by structural invariants (the
+ * pages do not define them) and are "parity unpinned" against ggml itself.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Type table ([rml] The type table; [candle] GgmlDType table).             */
+/* Numbers are the ggml element-type ids stored in GGUF tensor records.     */
+/* ------------------------------------------------------------------------ */
+enum {
+    OR_F32 = 0, OR_F16 = 1, OR_Q4_0 = 2, OR_Q8_0 = 8,
+    OR_Q4_K = 12, OR_Q6_K = 14, OR_Q8_K = 15
+};
+
+/* Returns 0 and fills (elems, bytes) for a known id, -1 otherwise. */
+int or_type_info(int type, int *elems, int *bytes) {
+    switch (type) {
+    case OR_F32:  *elems = 1;   *bytes = 4;   return 0;
+    case OR_F16:  *elems = 1;   *bytes = 2;   return 0;
+    case OR_Q4_0: *elems = 32;  *bytes = 18;  return 0;
+    case OR_Q8_0: *elems = 32;  *bytes = 34;  return 0;
+    case OR_Q4_K: *elems = 256; *bytes = 144; return 0;
+    case OR_Q6_K: *elems = 256; *bytes = 210; return 0;
+    case OR_Q8_K: *elems = 256; *bytes = 292; return 0;
+    default: return -1;
+    }
+}
+
+/* n elements take n / elems * bytes bytes; -1 if n is not whole blocks
+ * ([rml] The type table; [sipllm] type_nbytes). */
+int64_t or_type_nbytes(int type, int64_t n) {
+    int elems, bytes;
+    if (or_type_info(type, &elems, &bytes) != 0) return -1;
+    if (n < 0 || n % elems != 0) return -1;
+    return n / elems * bytes;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block layouts ([rml] Block layouts; [candle] block structure table).     */
+/* Plain structs whose bytes match the file format; sizes pinned below.     */
+/* ------------------------------------------------------------------------ */
+typedef struct { uint16_t d; int8_t qs[32]; } or_block_q8_0;
+typedef struct { uint16_t d; uint8_t qs[16]; } or_block_q4_0;
+typedef struct {
+    uint16_t d;
+    uint16_t dmin;
+    uint8_t scales[12];
+    uint8_t qs[128];
+} or_block_q4_k;
+typedef struct {
+    uint8_t ql[128];
+    uint8_t qh[64];
+    int8_t scales[16];
+    uint16_t d;
+} or_block_q6_k;
+typedef struct { float d; int8_t qs[256]; int16_t bsums[16]; } or_block_q8_k;
+
+_Static_assert(sizeof(or_block_q8_0) == 34, "Q8_0 block is 34 bytes");
+_Static_assert(sizeof(or_block_q4_0) == 18, "Q4_0 block is 18 bytes");
+_Static_assert(sizeof(or_block_q4_k) == 144, "Q4_K block is 144 bytes");
+_Static_assert(sizeof(or_block_q6_k) == 210, "Q6_K block is 210 bytes");
+_Static_assert(sizeof(or_block_q8_k) == 292, "Q8_K block is 292 bytes");
+
+/* ------------------------------------------------------------------------ */
+/* IEEE 754 binary16 codec, written from the format's definition:           */
+/* 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent 0 is   */
+/* zero/subnormal (value = m * 2^-24), exponent 31 is inf/NaN.  Encoding    */
+/* rounds to nearest, ties to even; overflow gives inf.                     */
+/* ------------------------------------------------------------------------ */
+float or_f16_to_f32(uint16_t h) {
+    int sign = h >> 15;
+    int e = (h >> 10) & 31;
+    int m = h & 1023;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24);
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25);
+    }
+    return (float)(sign ? -v : v);
+}
+
+/* Round a non-negative double to the nearest integer, ties to even. */
+static double or_round_half_even(double s) {
+    double fl = floor(s);
+    double diff = s - fl;
+    if (diff > 0.5) return fl + 1.0;
+    if (diff < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+uint16_t or_f32_to_f16(float f) {
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    if (isnan(f)) return (uint16_t)(sign | 0x7E00);
+    double a = fabs((double)f);
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7C00); /* 65504 + half ulp, tie goes up to 2^16 */
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: value = m * 2^-24, m rounded half to even */
+        double m = or_round_half_even(a * ldexp(1.0, 24));
+        return (uint16_t)(sign | (uint16_t)m); /* m == 1024 encodes the smallest normal */
+    }
+    int ex;
+    frexp(a, &ex);            /* a in [2^(ex-1), 2^ex) */
+    int E = ex - 1;           /* unbiased exponent, -14..15 */
+    double r = or_round_half_even(a * ldexp(1.0, 10 - E)); /* significand in [1024, 2048] */
+    if (r == 2048.0) { r = 1024.0; E += 1; }
+    if (E > 15) return (uint16_t)(sign | 0x7C00);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(r - 1024.0));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Code conversions shared by the quantizers.                               */
+/* ------------------------------------------------------------------------ */
+
+/* roundf result -> int8 code.  NaN gives 0 and out-of-range values
+ * saturate, as the special-value table of [candle] shows; for finite
+ * inputs the quantizers never leave [-127, 127]. */
+static int or_code_from_rounded(float r, int lo, int hi) {
+    if (isnan(r)) return 0;
+    if (r < (float)lo) return lo;
+    if (r > (float)hi) return hi;
+    return (int)r;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantizers                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Q8_0 ([lesson21] Example 2, [candle] BlockQ8_0::from_float): per block of
+ * 32, amax = largest |x| (NaN ignored), d = amax / 127 in f32, id = 1/d
+ * (0 when d == 0), store f16(d), code = roundf(x * id) with halves away
+ * from zero; codes use the unrounded id. Used for weights and activations. */
+void or_quantize_q8_0(const float *x, uint8_t *out, int64_t n) {
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const float *xb = x + b * 32;
+        float amax = 0.0f;
+        for (int j = 0; j < 32; ++j) {
+            float a = fabsf(xb[j]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+        or_block_q8_0 blk;
+        blk.d = or_f32_to_f16(d);
+        for (int j = 0; j < 32; ++j) {
+            float scaled = xb[j] * id;
+            blk.qs[j] = (int8_t)or_code_from_rounded(roundf(scaled), -128, 127);
+        }
+        memcpy(out + b * 34, &blk, 34);
+    }
+}
+
+/* Q4_0 ([lesson21] Example 5, [rml] A worked example: Q4_0): per block the
+ * FIRST element of strictly largest magnitude gives max (a later tie does
+ * not replace it), d = max / -8, id = 1/d (0 when d == 0), code =
+ * min(15, (int)(x*id + 8.5f)) with the multiply and the add rounded
+ * separately; byte j holds element j (low nibble) and j+16 (high nibble). */
+void or_quantize_q4_0(const float *x, uint8_t *out, int64_t n) {
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const float *xb = x + b * 32;
+        float amax = 0.0f, max = 0.0f;
+        for (int j = 0; j < 32; ++j) {
+            if (amax < fabsf(xb[j])) {
+                amax = fabsf(xb[j]);
+                max = xb[j];
+            }
+        }
+        float d = max / -8.0f;
+        float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+        int code[32];
+        for (int j = 0; j < 32; ++j) {
+            float scaled = xb[j] * id;
+            float shifted = scaled + 8.5f;
+            int c = (int)shifted; /* truncation toward zero; shifted >= 0 */
+            code[j] = c < 15 ? c : 15;
+        }
+        or_block_q4_0 blk;
+        blk.d = or_f32_to_f16(d);
+        for (int j = 0; j < 16; ++j)
+            blk.qs[j] = (uint8_t)(code[j] | (code[j + 16] << 4));
+        memcpy(out + b * 18, &blk, 18);
+    }
+}
+
+/* Q8_K activations ([candle] block table: f32 d, 256 codes, 16 bsums, each
+ * the sum of 16 codes; [rml] Quantized dot products: bsums serve the K-quant
+ * min term).  The rule itself is not printed; the reading used here is the
+ * Q8_0 rule over 256 elements with d kept in f32 and codes clamped to
+ * [-127, 127]. */
+void or_quantize_q8_k(const float *x, uint8_t *out, int64_t n) {
+    for (int64_t b = 0; b < n / 256; ++b) {
+        const float *xb = x + b * 256;
+        float amax = 0.0f;
+        for (int j = 0; j < 256; ++j) {
+            float a = fabsf(xb[j]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+        or_block_q8_k blk;
+        blk.d = d;
+        for (int j = 0; j < 256; ++j) {
+            float scaled = xb[j] * id;
+            blk.qs[j] = (int8_t)or_code_from_rounded(roundf(scaled), -127, 127);
+        }
+        for (int k = 0; k < 16; ++k) {
+            int s = 0;
+            for (int i = 0; i < 16; ++i) s += blk.qs[16 * k + i];
+            blk.bsums[k] = (int16_t)s;
+        }
+        memcpy(out + b * 292, &blk, 292);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Readable unpacking helpers (one per packed field).                       */
+/* ------------------------------------------------------------------------ */
+
+/* Q4_0 element e of a block: byte e mod 16, low nibble for e < 16, high
+ * nibble otherwise; the stored code c means c - 8 ([lesson21] Example 5). */
+static int q4_0_code(const or_block_q4_0 *b, int e) {
+    uint8_t byte = b->qs[e % 16];
+    return (e < 16) ? (byte & 0x0F) : (byte >> 4);
+}
+
+/* Q4_K sub-block j scale and min from the 12 packed bytes
+ * ([rml] Unpacking the packed fields; [candle] get_scale_min_k4 text):
+ * sub-blocks 0..3 keep both in the low 6 bits of bytes j (scale) and j+4
+ * (min); sub-blocks 4..7 keep their low 4 bits in byte j+4 (scale in the
+ * low nibble, min in the high nibble) and borrow the top 2 bits of byte
+ * j-4 (scale) and byte j (min). */
+static void q4_k_scale_min(const uint8_t s[12], int j, int *scale, int *min) {
+    if (j < 4) {
+        *scale = s[j] & 63;
+        *min = s[j + 4] & 63;
+    } else {
+        *scale = (s[j + 4] & 0x0F) | ((s[j - 4] >> 6) << 4);
+        *min = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+/* Q4_K element e: chunk e/64 of 32 bytes, low nibble for position < 32
+ * in the chunk, high nibble otherwise ([rml] element-200 trace). */
+static int q4_k_code(const or_block_q4_k *b, int e) {
+    int chunk = e / 64, p = e % 64;
+    if (p < 32) return b->qs[32 * chunk + p] & 0x0F;
+    return b->qs[32 * chunk + p - 32] >> 4;
+}
+
+/* Q6_K element e (reading stated in the file header): low 4 bits from ql,
+ * high 2 bits from qh; the stored q in 0..63 means q - 32 ([candle] block
+ * table: d * sc[j] * (q - 32)). */
+static int q6_k_code(const or_block_q6_k *b, int e) {
+    int h = e / 128, k = (e % 128) / 32, l = e % 32;
+    uint8_t lbyte = b->ql[64 * h + 32 * (k & 1) + l];
+    int lo4 = (k < 2) ? (lbyte & 0x0F) : (lbyte >> 4);
+    int hi2 = (b->qh[32 * h + l] >> (2 * k)) & 3;
+    return lo4 | (hi2 << 4);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantization ([sipllm] Per-format dequant; [candle] block table;      */
+/* [rml] Dequantization: memcpy each block into a local struct first).      */
+/* ------------------------------------------------------------------------ */
+static void dequant_block(int type, const uint8_t *src, float *dst) {
+    switch (type) {
+    case OR_Q8_0: {
+        or_block_q8_0 b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d);
+        for (int e = 0; e < 32; ++e) dst[e] = (float)b.qs[e] * d;
+        break;
+    }
+    case OR_Q4_0: {
+        or_block_q4_0 b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d);
+        for (int e = 0; e < 32; ++e) dst[e] = (float)(q4_0_code(&b, e) - 8) * d;
+        break;
+    }
+    case OR_Q4_K: {
+        or_block_q4_k b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d), dmin = or_f16_to_f32(b.dmin);
+        for (int e = 0; e < 256; ++e) {
+            int sc, m;
+            q4_k_scale_min(b.scales, e / 32, &sc, &m);
+            float scaled = d * (float)sc;      /* exact: 11 + 6 bits */
+            float value = scaled * (float)q4_k_code(&b, e); /* exact: 21 bits */
+            float offset = dmin * (float)m;    /* exact: 17 bits */
+            dst[e] = value - offset;           /* the only rounding */
+        }
+        break;
+    }
+    case OR_Q6_K: {
+        or_block_q6_k b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d);
+        for (int e = 0; e < 256; ++e) {
+            float scaled = d * (float)b.scales[e / 16];          /* exact: 11 + 7 bits */
+            dst[e] = scaled * (float)(q6_k_code(&b, e) - 32);    /* exact: 24 bits */
+        }
+        break;
+    }
+    case OR_Q8_K: {
+        or_block_q8_k b; memcpy(&b, src, sizeof b);
+        for (int e = 0; e < 256; ++e) dst[e] = (float)b.qs[e] * b.d;
+        break;
+    }
+    default:
+        break;
+    }
+}
+
+/* Dequantize n elements (whole blocks) of `type`. Returns 0, or -1 for an
+ * unsupported type or a length that is not whole blocks. */
+int or_dequantize(int type, const uint8_t *src, float *dst, int64_t n) {
+    int elems, bytes;
+    if (or_type_info(type, &elems, &bytes) != 0) return -1;
+    if (type == OR_F32 || type == OR_F16) return -1;
+    if (n % elems != 0) return -1;
+    for (int64_t b = 0; b < n / elems; ++b)
+        dequant_block(type, src + b * bytes, dst + b * elems);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Weight -> activation pairing ([rml] DotActivationType; [candle]          */
+/* VecDotType table): Q4_0 and Q8_0 pair with Q8_0, the K-quants with Q8_K. */
+/* ------------------------------------------------------------------------ */
+int or_act_type(int wtype) {
+    switch (wtype) {
+    case OR_Q4_0: case OR_Q8_0: return OR_Q8_0;
+    case OR_Q4_K: case OR_Q6_K: return OR_Q8_K;
+    default: return -1;
+    }
+}
+
+/* Number of int32 sums per (vector, row, block): Q4_K keeps the scale sum
+ * S_q and the min sum S_m apart, every other type has one sum S. */
+int or_isums_per_block(int wtype) { return wtype == OR_Q4_K ? 2 : 1; }
+
+/* ------------------------------------------------------------------------ */
+/* Per-block exact integer sums, element by element (the reference form of  */
+/* [rml] Kernels and references: each q decoded on its own, the K-quant min */
+/* term summed per element rather than through bsums).                      */
+/*                                                                          */
+/*   Q8_0: S = sum_i qw_i * qx_i                 ([lesson21] Example 10)    */
+/*   Q4_0: S = sum_i (code_i - 8) * qx_i         ([lesson21] Example 11)    */
+/*   Q4_K: S_q = sum_j sc_j * sum_{i in j} q_i * a_i,                       */
+/*         S_m = sum_j m_j * sum_{i in j} a_i    ([rml] Quantized dot)      */
+/*   Q6_K: S = sum_j sc_j * sum_{i in j} (q_i - 32) * a_i                   */
+/* ------------------------------------------------------------------------ */
+static void block_sums(int wtype, const uint8_t *wblk, const uint8_t *xblk, int32_t *out) {
+    switch (wtype) {
+    case OR_Q8_0: {
+        or_block_q8_0 w, x; memcpy(&w, wblk, 34); memcpy(&x, xblk, 34);
+        int32_t s = 0;
+        for (int i = 0; i < 32; ++i) s += (int32_t)w.qs[i] * (int32_t)x.qs[i];
+        out[0] = s;
+        break;
+    }
+    case OR_Q4_0: {
+        or_block_q4_0 w; or_block_q8_0 x; memcpy(&w, wblk, 18); memcpy(&x, xblk, 34);
+        int32_t s = 0;
+        for (int i = 0; i < 32; ++i) s += (int32_t)(q4_0_code(&w, i) - 8) * (int32_t)x.qs[i];
+        out[0] = s;
+        break;
+    }
+    case OR_Q4_K: {
+        or_block_q4_k w; or_block_q8_k x; memcpy(&w, wblk, 144); memcpy(&x, xblk, 292);
+        int32_t sq = 0, sm = 0;
+        for (int j = 0; j < 8; ++j) {
+            int sc, m;
+            q4_k_scale_min(w.scales, j, &sc, &m);
+            int32_t dot = 0, asum = 0;
+            for (int i = 32 * j; i < 32 * j + 32; ++i) {
+                dot += (int32_t)q4_k_code(&w, i) * (int32_t)x.qs[i];
+                asum += (int32_t)x.qs[i];
+            }
+            sq += sc * dot;
+            sm += m * asum;
+        }
+        out[0] = sq;
+        out[1] = sm;
+        break;
+    }
+    case OR_Q6_K: {
+        or_block_q6_k w; or_block_q8_k x; memcpy(&w, wblk, 210); memcpy(&x, xblk, 292);
+        int32_t s = 0;
+        for (int j = 0; j < 16; ++j) {
+            int32_t dot = 0;
+            for (int i = 16 * j; i < 16 * j + 16; ++i)
+                dot += (int32_t)(q6_k_code(&w, i) - 32) * (int32_t)x.qs[i];
+            s += (int32_t)w.scales[j] * dot;
+        }
+        out[0] = s;
+        break;
+    }
+    default:
+        break;
+    }
+}
+
+/* Block scales as doubles: (d_w, dmin_w, d_x). dmin_w is 0 except Q4_K. */
+static void block_scales(int wtype, const uint8_t *wblk, const uint8_t *xblk,
+                         double *dw, double *dmin, double *dx) {
+    *dmin = 0.0;
+    switch (wtype) {
+    case OR_Q8_0: { or_block_q8_0 w, x; memcpy(&w, wblk, 34); memcpy(&x, xblk, 34);
+        *dw = or_f16_to_f32(w.d); *dx = or_f16_to_f32(x.d); break; }
+    case OR_Q4_0: { or_block_q4_0 w; or_block_q8_0 x; memcpy(&w, wblk, 18); memcpy(&x, xblk, 34);
+        *dw = or_f16_to_f32(w.d); *dx = or_f16_to_f32(x.d); break; }
+    case OR_Q4_K: { or_block_q4_k w; or_block_q8_k x; memcpy(&w, wblk, 144); memcpy(&x, xblk, 292);
+        *dw = or_f16_to_f32(w.d); *dmin = or_f16_to_f32(w.dmin); *dx = x.d; break; }
+    case OR_Q6_K: { or_block_q6_k w; or_block_q8_k x; memcpy(&w, wblk, 210); memcpy(&x, xblk, 292);
+        *dw = or_f16_to_f32(w.d); *dx = x.d; break; }
+    default: *dw = 0.0; *dx = 0.0; break;
+    }
+}
+
+static int geometry(int wtype, int64_t n_in, int *wel, int *wby, int *xby) {
+    int at = or_act_type(wtype), xel;
+    if (at < 0) return -1;
+    if (or_type_info(wtype, wel, wby) != 0) return -1;
+    if (or_type_info(at, &xel, xby) != 0) return -1;
+    if (xel != *wel || n_in % *wel != 0) return -1;
+    return 0;
+}
+
+/* Per-(vector, row, block) sums, written to
+ * isums[((v * n_out + o) * nb + b) * k + t], k = or_isums_per_block(wtype).
+ * W is [n_out][n_in] in blocks of wtype; xq is [n_vec][n_in] in blocks of
+ * the paired activation type. Returns 0 or -1 on a bad type/shape. */
+int or_block_isums(int wtype, const uint8_t *W, const uint8_t *xq, int32_t *isums,
+                   int64_t n_out, int64_t n_in, int64_t n_vec) {
+    int wel, wby, xby;
+    if (geometry(wtype, n_in, &wel, &wby, &xby) != 0) return -1;
+    int64_t nb = n_in / wel;
+    int k = or_isums_per_block(wtype);
+    for (int64_t v = 0; v < n_vec; ++v)
+        for (int64_t o = 0; o < n_out; ++o)
+            for (int64_t b = 0; b < nb; ++b)
+                block_sums(wtype, W + (o * nb + b) * wby, xq + (v * nb + b) * xby,
+                           isums + ((v * n_out + o) * nb + b) * k);
+    return 0;
+}
+
+/* y[v * n_out + o] for rows o in [row0, row1), accumulated in f64 over the
+ * row's blocks ([lesson21] Example 10: integer sum per block times both
+ * scales):  Q8_0/Q4_0/Q6_K: T_b = d_w * d_x * S;
+ *           Q4_K:           T_b = d_x * (d_w * S_q - dmin_w * S_m). */
+int or_gemv(int wtype, const uint8_t *W, const uint8_t *xq, double *y,
+            int64_t n_out, int64_t n_in, int64_t n_vec, int64_t row0, int64_t row1) {
+    int wel, wby, xby;
+    if (geometry(wtype, n_in, &wel, &wby, &xby) != 0) return -1;
+    if (row0 < 0 || row1 > n_out || row0 > row1) return -1;
+    int64_t nb = n_in / wel;
+    for (int64_t v = 0; v < n_vec; ++v)
+        for (int64_t o = row0; o < row1; ++o) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t *wb = W + (o * nb + b) * wby;
+                const uint8_t *xb = xq + (v * nb + b) * xby;
+                int32_t s[2] = {0, 0};
+                double dw, dmin, dx;
+                block_sums(wtype, wb, xb, s);
+                block_scales(wtype, wb, xb, &dw, &dmin, &dx);
+                if (wtype == OR_Q4_K)
+                    acc += dx * (dw * (double)s[0] - dmin * (double)s[1]);
+                else
+                    acc += dw * dx * (double)s[0];
+            }
+            y[v * n_out + o] = acc;
+        }
+    return 0;
+}
+
+/* Exact value of one element as a double (no rounding at all), for the
+ * brute-force form below. */
+static double exact_weight(int wtype, const uint8_t *blk, int e) {
+    switch (wtype) {
+    case OR_Q8_0: { or_block_q8_0 b; memcpy(&b, blk, 34);
+        return (double)b.qs[e] * (double)or_f16_to_f32(b.d); }
+    case OR_Q4_0: { or_block_q4_0 b; memcpy(&b, blk, 18);
+        return (double)(q4_0_code(&b, e) - 8) * (double)or_f16_to_f32(b.d); }
+    case OR_Q4_K: { or_block_q4_k b; memcpy(&b, blk, 144);
+        int sc, m; q4_k_scale_min(b.scales, e / 32, &sc, &m);
+        return (double)or_f16_to_f32(b.d) * sc * q4_k_code(&b, e)
+             - (double)or_f16_to_f32(b.dmin) * m; }
+    case OR_Q6_K: { or_block_q6_k b; memcpy(&b, blk, 210);
+        return (double)or_f16_to_f32(b.d) * b.scales[e / 16] * (q6_k_code(&b, e) - 32); }
+    default: return 0.0;
+    }
+}
+
+static double exact_act(int atype, const uint8_t *blk, int e) {
+    if (atype == OR_Q8_0) { or_block_q8_0 b; memcpy(&b, blk, 34);
+        return (double)b.qs[e] * (double)or_f16_to_f32(b.d); }
+    or_block_q8_k b; memcpy(&b, blk, 292);
+    return (double)b.qs[e] * (double)b.d;
+}
+
+/* Second form ([sipllm] The fused matmul: dequantize one row, then dot):
+ * dequantize W and the quantized activations to exact doubles and take a
+ * plain f64 dot. Equal to or_gemv up to f64 rounding. */
+int or_gemv_dequant(int wtype, const uint8_t *W, const uint8_t *xq, double *y,
+                    int64_t n_out, int64_t n_in, int64_t n_vec) {
+    int wel, wby, xby;
+    if (geometry(wtype, n_in, &wel, &wby, &xby) != 0) return -1;
+    int at = or_act_type(wtype);
+    int64_t nb = n_in / wel;
+    for (int64_t v = 0; v < n_vec; ++v)
+        for (int64_t o = 0; o < n_out; ++o) {
+            double acc = 0.0;
+            for (int64_t i = 0; i < n_in; ++i) {
+                int64_t b = i / wel;
+                int e = (int)(i % wel);
+                acc += exact_weight(wtype, W + (o * nb + b) * wby, e)
+                     * exact_act(at, xq + (v * nb + b) * xby, e);
+            }
+            y[v * n_out + o] = acc;
+        }
+    return 0;
+}
+
+/* Returns 1 when the host stores integers little-endian, as the file
+ * format does (the struct decode above relies on it). */
+int or_host_is_little_endian(void) {
+    uint16_t probe = 1;
+    uint8_t first;
+    memcpy(&first, &probe, 1);
+    return first == 1;
+}

@@ -1,0 +1,352 @@
+"""Pins of the oracle against closed forms, library routines, brute force and
+structural invariants of the block formats (no GPU).
+
+Each check is chosen so that a plausible slip in the oracle (a dropped term,
+a wrong sign, index or shift, a transposed operand) fails at least one.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+RNG = np.random.default_rng(12345)
+
+
+# ------------------------------------------------------------- f16 codec
+def test_f16_decode_matches_numpy_for_all_bit_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want = bits.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_to_f32(int(b)) for b in bits], np.float32)
+    same = (got.view(np.uint32) == want.view(np.uint32)) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+
+
+def test_f16_encode_matches_numpy_round_to_nearest_even():
+    edge = [0.0, -0.0, 65504.0, 65519.99, 65520.0, 65536.0, 1e9, -1e9,
+            2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0000001, 3 * 2.0 ** -25, 2.0 ** -14,
+            2.0 ** -14 * (1 - 2.0 ** -11), 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11,
+            0.012204724, 1.0 / 127, float("inf"), float("-inf")]
+    rnd = np.concatenate([
+        RNG.standard_normal(20000).astype(np.float32),
+        (RNG.standard_normal(20000) * 1e-5).astype(np.float32),
+        (RNG.standard_normal(20000) * 3e4).astype(np.float32),
+        # exact ties between two f16 values in the normal and subnormal ranges
+        (np.arange(1, 2000) * 2.0 ** -25).astype(np.float32),
+        ((1024 + np.arange(0, 1024) + 0.5) * 2.0 ** -10).astype(np.float32),
+    ])
+    xs = np.concatenate([np.array(edge, np.float32), rnd])
+    with np.errstate(over="ignore"):
+        want = xs.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f32_to_f16(v) for v in xs], np.uint16)
+    assert np.array_equal(got, want)
+    assert oracle.f32_to_f16(float("nan")) & 0x7C00 == 0x7C00
+    assert oracle.f32_to_f16(float("nan")) & 0x3FF != 0
+
+
+# ------------------------------------------- exactness of dequantization
+def f32_round(fr: Fraction) -> float:
+    """Round an exact rational to the nearest f32 (ties to even), written
+    from the binary32 format (24-bit significand, normal range only)."""
+    if fr == 0:
+        return 0.0
+    sign = -1 if fr < 0 else 1
+    a = abs(fr)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    scaled = a / Fraction(2) ** (e - 23)          # in [2^23, 2^24)
+    fl = scaled.numerator // scaled.denominator
+    rem = scaled - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * float(fl * Fraction(2) ** (e - 23))
+
+
+def random_k_block(t):
+    b = bytearray(RNG.integers(0, 256, oracle.type_info(t)[1], dtype=np.uint8).tobytes())
+    d = np.float16(abs(RNG.standard_normal()) * 1e-3)
+    if t == oracle.Q4_K:
+        b[0:2] = d.tobytes()
+        b[2:4] = np.float16(abs(RNG.standard_normal()) * 1e-3).tobytes()
+    else:
+        b[208:210] = d.tobytes()
+    return bytes(b)
+
+
+def half(raw: bytes, off: int) -> Fraction:
+    return Fraction(float(np.frombuffer(raw[off:off + 2], np.float16)[0]))
+
+
+def test_dequant_is_the_correctly_rounded_exact_value():
+    # Q4_K: d*sc*q and dmin*m are exact in f32, so the value is the exact
+    # rational d*sc*q - dmin*m rounded once. The test decodes through the
+    # element-200 rule for every sub-block of the upper half and checks the
+    # lower half through the 6-bit low fields named by the candle page.
+    for _ in range(20):
+        raw = random_k_block(oracle.Q4_K)
+        vals = oracle.dequantize(oracle.Q4_K, np.frombuffer(raw, np.uint8), 256)
+        d, dmin, s, qs = half(raw, 0), half(raw, 2), raw[4:16], raw[16:]
+        for e in range(256):
+            j = e // 32
+            if j < 4:
+                sc, m = s[j] & 63, s[j + 4] & 63
+            else:
+                sc = (s[j + 4] & 0xF) | ((s[j - 4] >> 6) << 4)
+                m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4)
+            p = e % 64
+            q = qs[32 * (e // 64) + p] & 0xF if p < 32 else qs[32 * (e // 64) + p - 32] >> 4
+            exact = d * sc * q - dmin * m
+            assert float(vals[e]) == f32_round(exact)
+    # Q6_K, Q8_0, Q4_0: every product is exact, so dequantized values are
+    # exactly d * integer.
+    for _ in range(20):
+        raw = random_k_block(oracle.Q6_K)
+        vals = oracle.dequantize(oracle.Q6_K, np.frombuffer(raw, np.uint8), 256)
+        d = half(raw, 208)
+        sc = np.frombuffer(raw[192:208], np.int8)
+        for e in range(256):
+            ratio = Fraction(float(vals[e])) / (d * int(sc[e // 16])) if sc[e // 16] and d else None
+            if ratio is not None:
+                assert ratio.denominator == 1 and -32 <= ratio <= 31
+    for t, nbytes in ((oracle.Q8_0, 34), (oracle.Q4_0, 18)):
+        raw = bytearray(RNG.integers(0, 256, nbytes * 8, dtype=np.uint8).tobytes())
+        for b in range(8):
+            raw[nbytes * b:nbytes * b + 2] = np.float16(RNG.standard_normal()).tobytes()
+        vals = oracle.dequantize(t, np.frombuffer(bytes(raw), np.uint8), 256)
+        for b in range(8):
+            d = half(bytes(raw), nbytes * b)
+            for e in range(32):
+                r = Fraction(float(vals[32 * b + e])) / d
+                assert r.denominator == 1
+                assert (-128 <= r <= 127) if t == oracle.Q8_0 else (-8 <= r <= 7)
+
+
+# ----------------------------------------------- Q4_K packing structure
+def q4k_fields(raw):
+    """(scale[8], min[8]) observed through the oracle: d = 1, dmin = 0 gives
+    sc*q; d = 0, dmin = -1 gives +m; all nibbles 1."""
+    b = bytearray(raw)
+    b[16:] = bytes([0x11]) * 128
+    b[0:2] = np.float16(1).tobytes()
+    b[2:4] = np.float16(0).tobytes()
+    v = oracle.dequantize(oracle.Q4_K, np.frombuffer(bytes(b), np.uint8), 256)
+    sc = [int(v[32 * j]) for j in range(8)]
+    assert all((v[32 * j:32 * j + 32] == v[32 * j]).all() for j in range(8))
+    b[0:2] = np.float16(0).tobytes()
+    b[2:4] = np.float16(-1).tobytes()
+    v = oracle.dequantize(oracle.Q4_K, np.frombuffer(bytes(b), np.uint8), 256)
+    mn = [int(v[32 * j]) for j in range(8)]
+    return sc, mn
+
+
+def test_q4_k_scales_use_every_bit_once():
+    base = bytes(144)
+    sc0, mn0 = q4k_fields(base)
+    assert sc0 == [0] * 8 and mn0 == [0] * 8
+    hits = {}
+    for byte in range(12):
+        for bit in range(8):
+            b = bytearray(base)
+            b[4 + byte] = 1 << bit
+            sc, mn = q4k_fields(bytes(b))
+            changed = [("sc", j, v) for j, v in enumerate(sc) if v] + \
+                      [("m", j, v) for j, v in enumerate(mn) if v]
+            assert len(changed) == 1, (byte, bit, changed)
+            kind, j, v = changed[0]
+            assert v & (v - 1) == 0  # a single bit of a 6-bit field
+            hits[(kind, j, v.bit_length() - 1)] = (byte, bit)
+            # candle: sub-blocks 0..3 sit in the low 6 bits of bytes 0..7;
+            # sub-blocks 4..7 keep low 4 bits in bytes 8..11 and borrow the
+            # top 2 bits of bytes 0..7
+            if j < 4:
+                assert byte < 8 and bit < 6
+            elif v.bit_length() - 1 < 4:
+                assert byte >= 8
+            else:
+                assert byte < 8 and bit >= 6
+    assert len(hits) == 96  # 16 fields x 6 bits, each reached by one bit
+
+
+def test_q4_k_nibbles_are_a_bijection_in_element_order():
+    base = bytearray(144)
+    base[0:2] = np.float16(1).tobytes()
+    base[4:16] = bytes([1, 1, 1, 1, 0, 0, 0, 0, 0x01, 0x01, 0x01, 0x01])  # all scales 1, mins 0
+    seen = {}
+    for byte in range(128):
+        for hi in (0, 1):
+            b = bytearray(base)
+            b[16 + byte] = 0x10 if hi else 0x01
+            v = oracle.dequantize(oracle.Q4_K, np.frombuffer(bytes(b), np.uint8), 256)
+            nz = np.nonzero(v)[0]
+            assert len(nz) == 1 and v[nz[0]] == 1.0
+            seen[int(nz[0])] = (byte, hi)
+    assert sorted(seen) == list(range(256))
+    # element order inside a 64-element chunk: low nibbles of the chunk's 32
+    # bytes first, then high nibbles (the element-200 trace generalised)
+    assert seen[200] == (104, 0) and seen[232] == (104, 1) and seen[0] == (0, 0)
+
+
+# ----------------------------------------------- Q6_K packing structure
+def q6k_block(d=1.0, scales=None, ql=None, qh=None):
+    b = bytearray(210)
+    if ql is not None:
+        b[0:128] = ql
+    if qh is not None:
+        b[128:192] = qh
+    b[192:208] = np.array(scales if scales is not None else [1] * 16, np.int8).tobytes()
+    b[208:210] = np.float16(d).tobytes()
+    return np.frombuffer(bytes(b), np.uint8)
+
+
+def test_q6_k_every_bit_is_one_bit_of_one_element():
+    zero = oracle.dequantize(oracle.Q6_K, q6k_block(), 256)
+    assert (zero == -32).all()  # q = 0 means -32
+    owner = {}
+    for byte in range(192):
+        for bit in range(8):
+            raw = bytearray(192)
+            raw[byte] = 1 << bit
+            v = oracle.dequantize(oracle.Q6_K, q6k_block(ql=raw[:128], qh=raw[128:]), 256)
+            nz = np.nonzero(v != -32)[0]
+            assert len(nz) == 1, (byte, bit)
+            delta = int(v[nz[0]] + 32)
+            assert delta & (delta - 1) == 0
+            # ql gives the low 4 bits, qh the high 2 bits of q
+            assert (delta < 16) == (byte < 128)
+            owner.setdefault(int(nz[0]), set()).add(delta)
+    assert sorted(owner) == list(range(256))
+    assert all(s == {1, 2, 4, 8, 16, 32} for s in owner.values())
+
+
+def test_q6_k_scale_index_is_element_over_16_and_d_is_last():
+    for j in range(16):
+        sc = [0] * 16
+        sc[j] = -3
+        v = oracle.dequantize(oracle.Q6_K, q6k_block(d=0.5, scales=sc), 256)
+        nz = np.nonzero(v)[0]
+        assert list(nz) == list(range(16 * j, 16 * j + 16))
+        assert (v[nz] == np.float32(0.5 * -3 * -32)).all()
+
+
+# ------------------------------------------------------- Q8_K reading
+def test_q8_k_rule_and_bsums():
+    x = (RNG.standard_normal(256 * 6) * np.array([1, 1e-3, 50, 1, 1, 1]).repeat(256)).astype(np.float32)
+    x[256 * 4:256 * 5] = 0  # an all-zero block
+    q = oracle.quantize(oracle.Q8_K, x).reshape(6, 292)
+    for b in range(6):
+        xb = x[256 * b:256 * b + 256]
+        d = q[b, 0:4].copy().view(np.float32)[0]
+        qs = q[b, 4:260].copy().view(np.int8).astype(np.int32)
+        bs = q[b, 260:292].copy().view(np.int16).astype(np.int32)
+        amax = np.float32(np.max(np.abs(xb)))
+        assert d == amax / np.float32(127)            # f32 d, not rounded to f16
+        assert np.array_equal(bs, qs.reshape(16, 16).sum(axis=1))
+        if amax == 0:
+            assert (qs == 0).all()
+            continue
+        assert abs(qs[np.argmax(np.abs(xb))]) == 127
+        assert np.abs(qs).max() <= 127
+        # every code is the nearest integer to x/d up to the rounding of id
+        assert np.all(np.abs(qs - xb.astype(np.float64) / float(d)) <= 0.5 + 1e-4)
+
+
+def test_q8_0_codes_round_half_away_from_zero():
+    # x = k + 0.5 steps with d exactly 1: amax = 127 gives d = 1, id = 1
+    x = np.zeros(32, np.float32)
+    x[0] = 127
+    x[1:6] = [2.5, -2.5, 0.5, -0.5, 126.5]
+    q = oracle.quantize(oracle.Q8_0, x)
+    codes = q[2:].view(np.int8)
+    assert list(codes[:6]) == [127, 3, -3, 1, -1, 127]
+
+
+def test_zero_block_gives_zero():
+    # rml tests: ZeroActivationsGiveZero -- an all-zero row has d = 0, id = 0
+    for t in (oracle.Q8_0, oracle.Q8_K):
+        q = oracle.quantize(t, np.zeros(256, np.float32))
+        assert not q.any()
+    # Q4_0: d = 0 / -8 = -0.0 (f16 0x8000) and every code is 8, meaning 0
+    q = oracle.quantize(oracle.Q4_0, np.zeros(32, np.float32))
+    assert q.tobytes() == bytes([0x00, 0x80]) + bytes([0x88]) * 16
+    assert not oracle.dequantize(oracle.Q4_0, q, 32).any()
+    W = oracle.quantize(oracle.Q8_0, RNG.standard_normal(256).astype(np.float32))
+    xq = oracle.quantize(oracle.Q8_0, np.zeros(256, np.float32))
+    assert oracle.gemv(oracle.Q8_0, W, xq, 1, 256, 1)[0, 0] == 0.0
+
+
+# -------------------------------------------------- brute force on tiny inputs
+def random_weights(t, n_out, n_in):
+    if t in (oracle.Q8_0, oracle.Q4_0):
+        return oracle.quantize(t, (RNG.standard_normal(n_out * n_in) * 0.02).astype(np.float32))
+    nb = n_out * n_in // 256
+    return np.frombuffer(b"".join(random_k_block(t) for _ in range(nb)), np.uint8).copy()
+
+
+@pytest.mark.parametrize("t", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q6_K])
+def test_block_form_equals_dequantize_then_f64_dot(t):
+    for n_out, n_in, n_vec in ((1, 256, 1), (3, 512, 2), (8, 512, 3)):
+        W = random_weights(t, n_out, n_in)
+        x = RNG.standard_normal(n_vec * n_in).astype(np.float32)
+        xq = oracle.quantize(oracle.act_type(t), x)
+        y = oracle.gemv(t, W, xq, n_out, n_in, n_vec)
+        yb = oracle.gemv_dequant(t, W, xq, n_out, n_in, n_vec)
+        # scale for the bound: sum of |w_i * a_i|
+        wd = oracle.dequantize(t, W, n_out * n_in).reshape(n_out, n_in).astype(np.float64)
+        ad = oracle.dequantize(oracle.act_type(t), xq, n_vec * n_in).reshape(n_vec, n_in)
+        mag = np.abs(ad.astype(np.float64)) @ np.abs(wd).T
+        assert np.all(np.abs(y - yb) <= 1e-12 * mag + 1e-300)
+
+
+def test_block_isums_by_hand_for_one_q8_0_and_q4_0_block():
+    w = np.arange(-16, 16).astype(np.float32)     # Q8_0: d = 16/127
+    x = np.linspace(-1, 1, 32).astype(np.float32)
+    for t in (oracle.Q8_0, oracle.Q4_0):
+        qw, qx = oracle.quantize(t, w), oracle.quantize(oracle.Q8_0, x)
+        s = int(oracle.block_isums(t, qw, qx, 1, 32, 1)[0, 0, 0, 0])
+        cx = qx[2:].view(np.int8).astype(np.int64)
+        if t == oracle.Q8_0:
+            cw = qw[2:].view(np.int8).astype(np.int64)
+        else:
+            nib = np.concatenate([qw[2:] & 0xF, qw[2:] >> 4]).astype(np.int64)
+            cw = nib - 8
+        assert s == int(np.dot(cw, cx))
+
+
+def test_q4_k_min_term_equals_bsum_pairs():
+    # rml: the sub-block min term is min * sum(a), and sum(a) over 32
+    # activations is two of the stored 16-sums
+    W = random_weights(oracle.Q4_K, 2, 512)
+    xq = oracle.quantize(oracle.Q8_K, RNG.standard_normal(512).astype(np.float32))
+    sums = oracle.block_isums(oracle.Q4_K, W, xq, 2, 512, 1)
+    for o in range(2):
+        for b in range(2):
+            blk = W[(o * 2 + b) * 144:(o * 2 + b + 1) * 144].tobytes()
+            s = blk[4:16]
+            mins = [s[j + 4] & 63 if j < 4 else (s[j + 4] >> 4) | ((s[j] >> 6) << 4) for j in range(8)]
+            bs = xq[b * 292 + 260:b * 292 + 292].copy().view(np.int16).astype(np.int64)
+            assert sums[0, o, b, 1] == sum(mins[j] * (bs[2 * j] + bs[2 * j + 1]) for j in range(8))
+
+
+def test_int32_sums_stay_in_range_at_extremes():
+    # all codes at their extremes: Q6_K q = 0 (-32), scales -128, a = -127
+    W = q6k_block(d=1.0, scales=[-128] * 16)
+    xq = oracle.quantize(oracle.Q8_K, np.full(256, -1.0, np.float32))
+    s = oracle.block_isums(oracle.Q6_K, W, xq, 1, 256, 1)[0, 0, 0, 0]
+    assert s == 16 * (-128) * 16 * (-32) * (-127)
+
+
+# ------------------------------------------------------ sanity (unpinned)
+def test_round_trip_rmse_near_candle_table():
+    # candle's round-trip table on 262144 N(0,1) values: Q8_0 0.5365%,
+    # Q8K 0.6948%. Different random draws, so a loose statistical check.
+    x = RNG.standard_normal(262144).astype(np.float32)
+    for t, want in ((oracle.Q8_0, 0.5365), (oracle.Q8_K, 0.6948)):
+        y = oracle.dequantize(t, oracle.quantize(t, x), x.size)
+        e = (y.astype(np.float64) - x)
+        got = 100 * math.sqrt(np.sum(e ** 2) / np.sum(x.astype(np.float64) ** 2))
+        assert got == pytest.approx(want, rel=0.01)

@@ -1,0 +1,317 @@
+"""Pins of the oracle against values the reference pages print.
+
+Each test reads a fixture under tests/golden/ (the fixture names the page
+and section) and checks the oracle reproduces it. Nothing here touches the
+CUDA library.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from goldens import floats, hexbytes, ints, keyvals, rows
+from javarand import JavaRandom
+
+ORACLE_TYPES = {"Q4_0": oracle.Q4_0, "Q8_0": oracle.Q8_0, "Q4_K": oracle.Q4_K,
+                "Q6_K": oracle.Q6_K, "Q8_K": oracle.Q8_K}
+
+
+def lesson_block():
+    """x_i = (float)(((i * 7919) % 1001) - 500) / 337f, i = 0..31."""
+    i = np.arange(32)
+    return (((i * 7919) % 1001) - 500).astype(np.float32) / np.float32(337)
+
+
+def d_of(block: bytes) -> float:
+    return float(oracle.f16_to_f32(block[0] | (block[1] << 8)))
+
+
+# ---------------------------------------------------------------- type table
+def test_type_table():
+    seen = 0
+    for name, elems, nbytes, bpw in rows("type_table.txt"):
+        elems, nbytes, bpw = int(elems), int(nbytes), float(bpw)
+        assert nbytes * 8 / elems == pytest.approx(bpw, abs=5e-5)
+        if name in ORACLE_TYPES:
+            assert oracle.type_info(ORACLE_TYPES[name]) == (elems, nbytes)
+            assert oracle.type_nbytes(ORACLE_TYPES[name], 4096) == 4096 // elems * nbytes
+            seen += 1
+    assert seen == 5
+    assert oracle.type_info(99) is None
+
+
+def test_row_length_must_be_whole_blocks():
+    # "Building Q8_0 and Q4_0 Like ggml", Example 15: a row of 100 is rejected.
+    assert oracle.type_nbytes(oracle.Q4_0, 100) == -1
+    assert oracle.type_nbytes(oracle.Q4_K, 4096 + 32) == -1
+
+
+def test_tensor_sizes_example9():
+    g = keyvals("lesson21_seeded_examples.txt")
+    assert oracle.type_nbytes(oracle.Q8_0, 64 * 4096) == int(g["ex9_q8_0_bytes"])
+    assert oracle.type_nbytes(oracle.Q4_0, 64 * 4096) == int(g["ex9_q4_0_bytes"])
+    assert oracle.type_nbytes(oracle.Q8_0, 4096) == int(g["ex9_q8_0_stride"])
+    assert oracle.type_nbytes(oracle.Q4_0, 4096) == int(g["ex9_q4_0_stride"])
+
+
+# ------------------------------------------------------- candle Q8_0 block
+def test_candle_q8_0_block():
+    g = keyvals("candle_q8_0_block.txt")
+    x = (np.arange(32).astype(np.float32) - np.float32(15.5)) / np.float32(10)
+    b = oracle.quantize(oracle.Q8_0, x).tobytes()
+    assert b[:2] == hexbytes(g["d_bytes_hex"])
+    assert d_of(b) == pytest.approx(float(g["d"]), rel=1e-7)
+    assert list(np.frombuffer(b[2:], np.int8)) == ints(g["qs"])
+    back = oracle.dequantize(oracle.Q8_0, np.frombuffer(b, np.uint8), 32)
+    for got, want in zip(back[:4], floats(g["back_0_3"])):
+        assert float(got) == pytest.approx(want, rel=1e-7)
+
+
+# --------------------------------------------------- candle special values
+def test_candle_special_values():
+    for name, a, repl, shown_in, shown_out in rows("candle_special_values.txt", sep="|"):
+        i = np.arange(32).astype(np.float32)
+        x = np.float32(float(a)) * i / np.float32(31)
+        if repl != "-":
+            x[1] = np.float32(float(repl))
+        want_in = [float(t) for t in shown_in.split()]
+        for got, want in zip(x[:3], want_in):
+            if math.isnan(want) or math.isinf(want):
+                assert (math.isnan(got) and math.isnan(want)) or got == want
+            else:
+                assert float(got) == pytest.approx(want, rel=1e-6, abs=0), name
+        q = oracle.quantize(oracle.Q8_0, x)
+        out = oracle.dequantize(oracle.Q8_0, q, 32)
+        for got, want in zip(out[:3], [float(t) for t in shown_out.split()]):
+            if math.isnan(want):
+                assert math.isnan(got), name
+            elif math.isinf(want):
+                assert got == want, name
+            else:
+                assert float(got) == pytest.approx(want, rel=1e-7, abs=0), name
+
+
+# ------------------------------------------------------------ rml Q4_0 block
+def test_rml_q4_0_block():
+    g = keyvals("rml_q4_0_block.txt")
+    x = np.zeros(32, np.float32)
+    x[:4] = np.array(floats(g["x_0_3"]), np.float32)
+    b = oracle.quantize(oracle.Q4_0, x).tobytes()
+    want = hexbytes(g["first_bytes_hex"])
+    assert b[:len(want)] == want
+    back = oracle.dequantize(oracle.Q4_0, np.frombuffer(b, np.uint8), 32)
+    assert float(back[2]) == float(g["decoded_element_2"])
+    assert float(back[0]) == -2.0
+
+
+# ---------------------------------------------------- lesson 21 fixed blocks
+def test_lesson21_example2_q8_0():
+    g = keyvals("lesson21_fixed_blocks.txt")
+    x = lesson_block()
+    amax = float(np.max(np.abs(x)))
+    assert f"{amax:.6f}" == g["ex2_amax"]
+    b = oracle.quantize(oracle.Q8_0, x).tobytes()
+    bits = b[0] | (b[1] << 8)
+    assert f"{bits:04X}" == g["ex2_d_f16_bits"]
+    assert f"{d_of(b):.9f}" == g["ex2_d_f16"]
+    assert list(np.frombuffer(b[2:], np.int8)) == ints(g["ex2_qs"])
+
+
+def test_lesson21_example3_and_4():
+    g = keyvals("lesson21_fixed_blocks.txt")
+    x = lesson_block()
+    b = oracle.quantize(oracle.Q8_0, x)
+    assert b[:2].tobytes().hex() == g["ex4_d_hex"]
+    assert b[2:].tobytes().hex() == g["ex4_qs_hex"]
+    y = oracle.dequantize(oracle.Q8_0, b, 32)
+    assert float(y[0]) == pytest.approx(float(g["ex4_y0"]), rel=1e-7)
+    err = np.abs(y.astype(np.float64) - x)
+    assert f"{err.max():.6f}" == g["ex3_max_err_f16_d"]
+    rmse = 100 * math.sqrt(np.sum((y - x).astype(np.float64) ** 2) / np.sum(x.astype(np.float64) ** 2))
+    assert f"{rmse:.4f}" == g["ex3_rel_rmse_pct"]
+    # fixed point: quantizing the dequantized values reproduces the bytes
+    assert np.array_equal(oracle.quantize(oracle.Q8_0, y), b)
+
+
+def test_lesson21_example6_q4_0_vs_q8_0():
+    g = keyvals("lesson21_fixed_blocks.txt")
+    x = lesson_block()
+    y4 = oracle.dequantize(oracle.Q4_0, oracle.quantize(oracle.Q4_0, x), 32)
+    y8 = oracle.dequantize(oracle.Q8_0, oracle.quantize(oracle.Q8_0, x), 32)
+    assert [f"{v:.4f}" for v in y4[:4]] == g["ex6_q4_0_0_3"].split()
+    assert [f"{v:.4f}" for v in y8[:4]] == g["ex6_q8_0_0_3"].split()
+    for y, tag in ((y4, "q4_0"), (y8, "q8_0")):
+        e = (y.astype(np.float64) - x)
+        assert f"{np.abs(e).max():.4f}" == g[f"ex6_{tag}_max_err"]
+        rmse = 100 * math.sqrt(np.sum(e ** 2) / np.sum(x.astype(np.float64) ** 2))
+        assert f"{rmse:.3f}" == g[f"ex6_{tag}_rel_rmse_pct"]
+
+
+def test_lesson21_example14_hex():
+    g = keyvals("lesson21_fixed_blocks.txt")
+    i = np.arange(64)
+    x = (((i * 7919) % 1001) - 500).astype(np.float32) / np.float32(337)
+    x[40] = np.float32(9.5)
+    for blk in range(2):
+        xb = x[32 * blk:32 * blk + 32]
+        assert oracle.quantize(oracle.Q8_0, xb).tobytes().hex() == g[f"ex14_block{blk}_q8_0"]
+        assert oracle.quantize(oracle.Q4_0, xb).tobytes().hex() == g[f"ex14_block{blk}_q4_0"]
+
+
+def test_lesson21_example5_q4_0_signed_max_and_nibbles():
+    g = keyvals("lesson21_fixed_blocks.txt")
+    a = (np.arange(32).astype(np.float32) - np.float32(12)) / np.float32(4)
+    for x, tag in ((a, "a"), (-a, "b")):
+        q = oracle.quantize(oracle.Q4_0, x).tobytes()
+        assert f"{d_of(q):.4f}" == g[f"ex5_{tag}_d"]
+        assert f"{q[2]:02X}" == g["ex5_byte0"]
+        assert f"{q[3]:02X}" == g["ex5_byte1"]
+        assert q[2] & 0xF == int(g["ex5_code_0"])
+        assert q[2] >> 4 == int(g["ex5_code_16"])
+        back = oracle.dequantize(oracle.Q4_0, np.frombuffer(q, np.uint8), 32)
+        # the extreme value maps to code 0 (-8) and is stored up to f16 rounding of d
+        assert float(back[31]) == pytest.approx(float(g[f"ex5_{tag}_max"]), rel=1e-3)
+
+
+# --------------------------------------------- lesson 21 seeded Java examples
+def java_pairs(seed, n, scale_a=0.02):
+    r = JavaRandom(seed)
+    a = np.zeros(n, np.float32)
+    b = np.zeros(n, np.float32)
+    for i in range(n):
+        a[i] = np.float32(r.next_gaussian()) * np.float32(scale_a)
+        b[i] = np.float32(r.next_gaussian())
+    return a, b
+
+
+def java_outlier_weights(r, n):
+    w = np.zeros(n, np.float32)
+    for i in range(n):
+        g = np.float32(r.next_gaussian()) * np.float32(0.02)
+        w[i] = g * np.float32(10 if r.next_int(500) == 0 else 1)
+    return w
+
+
+def java_gaussians(r, n):
+    return np.array([np.float32(r.next_gaussian()) for _ in range(n)], np.float32)
+
+
+def f16_field(blocks: np.ndarray, nbytes: int, nblocks: int) -> np.ndarray:
+    raw = blocks.reshape(nblocks, nbytes)[:, :2].copy().view(np.uint16).reshape(-1)
+    return np.array([oracle.f16_to_f32(int(h)) for h in raw], np.float32)
+
+
+def test_lesson21_example10_q8_0_dot():
+    g = keyvals("lesson21_seeded_examples.txt")
+    n = 4096
+    a, b = java_pairs(22, n)
+    assert f"{np.dot(a.astype(np.float64), b.astype(np.float64)):.6f}" == g["ex10_exact"]
+    qa, qb = oracle.quantize(oracle.Q8_0, a), oracle.quantize(oracle.Q8_0, b)
+    s = oracle.block_isums(oracle.Q8_0, qa, qb, 1, n, 1).reshape(-1)
+    da, db = f16_field(qa, 34, n // 32), f16_field(qb, 34, n // 32)
+    # the page's float loop: sumf += sumi * (dx * dy), all in f32
+    sumf = np.float32(0)
+    for ib in range(n // 32):
+        sumf = np.float32(sumf + np.float32(np.float32(s[ib]) * np.float32(da[ib] * db[ib])))
+    assert f"{sumf:.6f}" == g["ex10_q8_0_dot"]
+    y = oracle.gemv(oracle.Q8_0, qa, qb, 1, n, 1)[0, 0]
+    assert y == pytest.approx(float(g["ex10_q8_0_dot"]), abs=5e-6)
+
+
+def test_lesson21_example11_q4_0_q8_0_dot():
+    g = keyvals("lesson21_seeded_examples.txt")
+    n = 4096
+    w, x = java_pairs(23, n)
+    assert f"{np.dot(w.astype(np.float64), x.astype(np.float64)):.6f}" == g["ex11_exact"]
+    qw, qx = oracle.quantize(oracle.Q4_0, w), oracle.quantize(oracle.Q8_0, x)
+    wdeq = oracle.dequantize(oracle.Q4_0, qw, n)
+    assert f"{np.dot(wdeq.astype(np.float64), x.astype(np.float64)):.6f}" == g["ex11_weight_only"]
+    s = oracle.block_isums(oracle.Q4_0, qw, qx, 1, n, 1).reshape(-1)
+    dw, dx = f16_field(qw, 18, n // 32), f16_field(qx, 34, n // 32)
+    sumf = np.float32(0)
+    for ib in range(n // 32):  # (sumi0 + sumi1) * dw * dx, left to right in f32
+        sumf = np.float32(sumf + np.float32(np.float32(np.float32(s[ib]) * dw[ib]) * dx[ib]))
+    assert f"{sumf:.6f}" == g["ex11_kernel"]
+    y = oracle.gemv(oracle.Q4_0, qw, qx, 1, n, 1)[0, 0]
+    assert y == pytest.approx(float(g["ex11_kernel"]), abs=5e-6)
+
+
+def rel_rmse_pct(y, x):
+    e = y.astype(np.float64) - x.astype(np.float64)
+    return 100 * math.sqrt(np.sum(e ** 2) / np.sum(x.astype(np.float64) ** 2))
+
+
+def test_lesson21_example12_error_table():
+    g = keyvals("lesson21_seeded_examples.txt")
+    x = java_outlier_weights(JavaRandom(24), 65536)
+    f16 = np.array([oracle.f16_to_f32(oracle.f32_to_f16(v)) for v in x], np.float32)
+    assert f"{rel_rmse_pct(f16, x):.4f}" == g["ex12_f16_rmse_pct"]
+    for t, key in ((oracle.Q8_0, "ex12_q8_0_rmse_pct"), (oracle.Q4_0, "ex12_q4_0_rmse_pct")):
+        y = oracle.dequantize(t, oracle.quantize(t, x), x.size)
+        assert f"{rel_rmse_pct(y, x):.4f}" == g[key]
+
+
+@pytest.mark.slow
+def test_lesson21_example13_output_error():
+    g = keyvals("lesson21_seeded_examples.txt")
+    rows_, cols = 256, 4096
+    r = JavaRandom(25)
+    w = java_outlier_weights(r, rows_ * cols)
+    x = java_gaussians(r, cols)
+    ref = w.reshape(rows_, cols).astype(np.float64) @ x.astype(np.float64)
+    qx = oracle.quantize(oracle.Q8_0, x)
+    for t, key in ((oracle.Q8_0, "ex13_q8_0_out_err_pct"), (oracle.Q4_0, "ex13_q4_0_out_err_pct")):
+        qw = oracle.quantize(t, w)
+        y = oracle.gemv(t, qw, qx, rows_, cols, 1)[0]
+        err = 100 * math.sqrt(np.sum((y - ref) ** 2) / np.sum(ref ** 2))
+        assert f"{err:.4f}" == g[key]
+
+
+@pytest.mark.slow
+def test_lesson21_example15_quantizer_report():
+    g = keyvals("lesson21_seeded_examples.txt")
+    rows_, cols = 512, 2048
+    r = JavaRandom(26)
+    w = java_outlier_weights(r, rows_ * cols)
+    x = java_gaussians(r, cols)
+    W = w.reshape(rows_, cols).astype(np.float64)
+    ref = W @ x.astype(np.float64)
+    for t, tag in ((oracle.Q8_0, "q8_0"), (oracle.Q4_0, "q4_0")):
+        q = oracle.quantize(t, w)
+        assert q.size == int(g[f"ex15_{tag}_bytes"])
+        wq = oracle.dequantize(t, q, w.size)
+        assert f"{rel_rmse_pct(wq, w):.3f}" == g[f"ex15_{tag}_weight_rmse_pct"]
+        yq = wq.reshape(rows_, cols).astype(np.float64) @ x.astype(np.float64)
+        err = 100 * math.sqrt(np.sum((yq - ref) ** 2) / np.sum(ref ** 2))
+        assert f"{err:.3f}" == g[f"ex15_{tag}_output_err_pct"]
+        # "stable": re-quantizing the dequantized tensor gives the same bytes
+        assert np.array_equal(oracle.quantize(t, wq), q)
+
+
+# ------------------------------------------------------- rml Q4_K trace
+def test_rml_q4_k_element_200_trace():
+    g = keyvals("rml_q4_k_trace.txt")
+    e = int(g["element"])
+    rng = np.random.default_rng(7)
+    blk = bytearray(rng.integers(0, 256, 144, dtype=np.uint8).tobytes())
+    d, dmin = 0.5, 0.25
+    blk[0:2] = np.float16(d).tobytes()
+    blk[2:4] = np.float16(dmin).tobytes()
+    s = blk[4:16]
+    qs = blk[16:144]
+    sc = (s[int(g["scale_low_byte"])] & 0xF) | ((s[int(g["scale_high_byte"])] >> 6) << 4)
+    mn = (s[int(g["min_low_byte"])] >> 4) | ((s[int(g["min_high_byte"])] >> 6) << 4)
+    q = qs[int(g["qs_byte"])] & 0xF
+    assert g["qs_nibble"] == "low" and e // 32 == int(g["sub_block"])
+    vals = oracle.dequantize(oracle.Q4_K, np.frombuffer(bytes(blk), np.uint8), 256)
+    assert float(vals[e]) == np.float32(d * sc * q - dmin * mn)
+    # changing any byte the trace does not name leaves element 200 unchanged
+    named = {0, 1, 2, 3, 4 + 10, 4 + 2, 4 + 6, 16 + 104}
+    for pos in range(144):
+        if pos in named:
+            continue
+        b2 = bytearray(blk)
+        b2[pos] ^= 0xFF
+        v2 = oracle.dequantize(oracle.Q4_K, np.frombuffer(bytes(b2), np.uint8), 256)
+        assert v2[e] == vals[e], pos
