@@ -1,0 +1,455 @@
+"""Benchmark of the block-quantized GEMV on GB300.
+
+Default workload (the headline): one decode step through a 32-layer
+Q4_K_M-style stack -- per layer Q4_K q/k/v/o 4096 x 4096, Q4_K gate/up
+11008 x 4096, Q6_K down 4096 x 11008 -- each matrix with a fresh activation
+vector (n_vec = 1). A step is the 224 qgemv calls (activation quantization
+to Q8_K + GEMV each); weights stay resident in HBM (4.01 GB, far above L2, so
+every step streams them from HBM). The metric is effective weight bandwidth:
+weight bytes streamed per second.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--n-vec V]
+
+Prints one JSON line (rank 0). Under torchrun every rank runs the whole
+workload on its own GPU (replicas: weak scaling); value sums all ranks' bytes
+over the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q4_K/Q6_K GEMV effective weight GB/s (% of GB300 HBM peak)"
+UNIT = "GB/s"
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    """Hash of the sources that make up the GEMV kernels (to tell whether a
+    committed ncu traffic figure still describes the current kernel)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ggml_block_quantized_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("gemv") or name == "qg_common.cuh":
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ the workload
+def build_workload(name, n_vec, device, keep_host_layers=2):
+    """Device-resident inputs for every qgemv call of one step.
+
+    Returns (calls, host_sample): calls is a list of dicts (type, n_out, n_in,
+    W, x, y) on the device; host_sample keeps the host arrays of the first
+    calls for the CPU baseline."""
+    import torch
+
+    import ggml_block_quantized_gb300 as qg
+    from ggml_block_quantized_gb300 import synth
+
+    calls, host_sample = [], []
+    if name == "layer_stack":
+        for layer in range(synth.N_LAYERS):
+            for m in range(len(synth.LAYER_MATRICES)):
+                mat = synth.layer_matrix(layer, m, n_vec)
+                c = dict(kind=mat["name"], type=mat["type"], n_out=mat["n_out"], n_in=mat["n_in"],
+                         W=torch.from_numpy(mat["w_blocks"]).to(device),
+                         x=torch.from_numpy(mat["x"]).to(device))
+                calls.append(c)
+                if layer < keep_host_layers:
+                    host_sample.append(dict(type=mat["type"], n_out=mat["n_out"], n_in=mat["n_in"],
+                                            W=mat["w_blocks"], x=mat["x"]))
+    else:
+        m = synth.single_matrix(name, n_vec=n_vec)
+        t = m["type"]
+        if "w_f32" in m:
+            W = qg.quantize_rows(t, torch.from_numpy(m["w_f32"]).to(device), m["n_out"])
+        else:
+            W = torch.from_numpy(m["w_blocks"]).to(device)
+        torch.cuda.synchronize()
+        # enough distinct copies of the weights that the rotation exceeds 4x L2
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        copies = max(1, int(np.ceil(4 * l2 / W.numel())))
+        x = torch.from_numpy(m["x"]).to(device)
+        for i in range(copies):
+            calls.append(dict(kind=name, type=t, n_out=m["n_out"], n_in=m["n_in"],
+                              W=W if i == 0 else W.clone(), x=x))
+        host_sample.append(dict(type=t, n_out=m["n_out"], n_in=m["n_in"], W=W.cpu().numpy(), x=m["x"]))
+    for c in calls:
+        c["y"] = torch.empty((n_vec, c["n_out"]), dtype=torch.float32, device=device)
+    return calls, host_sample
+
+
+def weight_bytes(calls):
+    return sum(c["W"].numel() for c in calls)
+
+
+# ------------------------------------------------------------ CPU baseline
+def time_oracle(sample, n_vec, budget_s=12.0):
+    """The oracle as it stands, rows split over the host cores; returns
+    (GB/s of weight bytes, cores, description)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    done_bytes, t_total, ncalls = 0, 0.0, 0
+    with ThreadPoolExecutor(max_workers=cores) as ex:
+        for c in sample:
+            t0 = time.perf_counter()
+            at = oracle.act_type(c["type"])
+            xq = oracle.quantize(at, c["x"])
+            y = np.zeros((n_vec, c["n_out"]))
+            chunks = np.linspace(0, c["n_out"], cores * 4 + 1).astype(int)
+            list(ex.map(lambda r: oracle.gemv(c["type"], c["W"], xq, c["n_out"], c["n_in"], n_vec,
+                                              rows=(int(r[0]), int(r[1])), out=y),
+                        zip(chunks[:-1], chunks[1:])))
+            t_total += time.perf_counter() - t0
+            done_bytes += c["W"].size
+            ncalls += 1
+            if t_total > budget_s:
+                break
+    return done_bytes / t_total / 1e9, cores, f"{ncalls} of the step's qgemv calls (first layers), n_vec={n_vec}"
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+    import ggml_block_quantized_gb300 as qg
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    calls, host_sample = build_workload(args.workload, args.n_vec, device)
+    wbytes = weight_bytes(calls)
+    ws = torch.empty(max(qg.qgemv_workspace_bytes(c["type"], c["n_in"], args.n_vec) for c in calls),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step():
+        for c in calls:
+            qg.qgemv(c["type"], c["W"], c["x"], c["n_out"], c["n_in"], args.n_vec, y=c["y"], workspace=ws,
+                     stream=stream)
+
+    def capture(fn):
+        with torch.cuda.stream(stream):
+            fn()  # eager warm-up on the capture stream
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    def time_graph(g, reps, sampler=None):
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if sampler:
+            sampler.start()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        return e0.elapsed_time(e1) / 1e3, clocks
+
+    g_step = capture(step)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_step.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    t, clocks = time_graph(g_step, args.steps, sampler)
+    if world > 1:
+        tt = torch.tensor([t], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t = float(tt.item())
+    value = wbytes * args.steps * world / t / 1e9
+    ms_per_step = t / args.steps * 1e3
+    assert qg.device_error() == 0, "a kernel reported a bounded-wait timeout"
+
+    # ---- per-kind breakdown (each kind's calls alone, graph-replayed)
+    breakdown = {}
+    kinds = sorted({(c["kind"] if c["kind"] not in ("q", "k", "v", "o") else "qkvo") for c in calls})
+    for kind in kinds:
+        sel = [c for c in calls if (c["kind"] == kind or (kind == "qkvo" and c["kind"] in ("q", "k", "v", "o")))]
+
+        def part(sel=sel):
+            for c in sel:
+                qg.qgemv(c["type"], c["W"], c["x"], c["n_out"], c["n_in"], args.n_vec, y=c["y"],
+                         workspace=ws, stream=stream)
+        g = capture(part)
+        reps = max(3, min(50, int(0.3 / max(1e-6, ms_per_step / 1e3 * len(sel) / len(calls)))))
+        tk, _ = time_graph(g, reps)
+        b = weight_bytes(sel)
+        c0 = sel[0]
+        breakdown[kind] = {"shape": f"{qg.TYPE_NAMES[c0['type']]} {c0['n_out']}x{c0['n_in']}",
+                           "calls_per_step": len(sel), "us_per_call": round(tk / reps / len(sel) * 1e6, 3),
+                           "GB_s": round(b * reps / tk / 1e9, 1)}
+        del g
+
+    # ---- roofline of the dominant kernel: the GEMV alone (activations
+    # pre-quantized), over the launches of the dominant weight type
+    peak, peak_kind = measured_peaks()
+    by_type = {}
+    for c in calls:
+        by_type[c["type"]] = by_type.get(c["type"], 0) + c["W"].numel()
+    dom_type = max(by_type, key=by_type.get)
+    dom = [c for c in calls if c["type"] == dom_type]
+    at = qg.qtype_act_type(dom_type)
+    for c in dom:
+        c["xq"] = qg.quantize_act(at, c["x"], args.n_vec)
+
+    def gemv_only():
+        for c in dom:
+            qg.qgemv_xq(c["type"], c["W"], c["xq"], c["n_out"], c["n_in"], args.n_vec, y=c["y"], stream=stream)
+    g = capture(gemv_only)
+    reps = 10
+    tg, _ = time_graph(g, reps)
+    del g
+    alg_bytes = sum(c["W"].numel() + c["xq"].numel() + 4 * args.n_vec * c["n_out"] for c in dom)
+    per_launch = alg_bytes / len(dom)
+    avg_dur = tg / reps / len(dom)
+    achieved = per_launch / avg_dur / 1e9
+    kernel_key = f"gemv_kernel<{qg.TYPE_NAMES[dom_type]},NV={args.n_vec}>"
+    roofline = {"bound": "hbm", "kernel": kernel_key, "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": committed_traffic(f"{kernel_key}@{args.workload}"),
+                "algorithmic_bytes_per_launch": int(per_launch), "avg_launch_us": round(avg_dur * 1e6, 3),
+                "launches": len(dom)}
+
+    # ---- end to end through the public API with host buffers: each step
+    # copies every x in from pinned host memory and every y back out
+    hx = [c["x"].cpu().pin_memory() for c in calls]
+    hy = [torch.empty(c["y"].shape, dtype=torch.float32).pin_memory() for c in calls]
+
+    def e2e_step():
+        for c, a, b in zip(calls, hx, hy):
+            c["x"].copy_(a, non_blocking=True)
+            qg.qgemv(c["type"], c["W"], c["x"], c["n_out"], c["n_in"], args.n_vec, y=c["y"], workspace=ws,
+                     stream=stream)
+            b.copy_(c["y"], non_blocking=True)
+    g = capture(e2e_step)
+    e2e_reps = max(3, args.steps // 4)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_reps):
+            g.replay()
+    torch.cuda.synchronize()
+    te = time.perf_counter() - t0
+    del g
+    h2d = sum(a.numel() * 4 for a in hx)
+    d2h = sum(b.numel() * 4 for b in hy)
+    e2e = {"value": round(wbytes * e2e_reps * world / te / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "timing": "host wall clock, CUDA-graph replay incl. copies + sync"}
+
+    cpu = None
+    if rank == 0:
+        v, cores, desc = time_oracle(host_sample, args.n_vec, budget_s=args.cpu_budget)
+        cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    launches_per_step = 2 * len(calls)  # quantize + GEMV per call
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "dtype_detail": "int8 x int8 -> int32 block sums, f32 block scales, f32 y",
+        "data": "synthetic (seeded random GGUF blocks; x ~ N(0,1))",
+        "config": {"workload": args.workload, "n_vec": args.n_vec, "calls_per_step": len(calls),
+                   "weight_bytes_per_step": wbytes,
+                   "l2": "inputs larger than L2 (weights rotate through distinct buffers > 4x L2)",
+                   "timing": "CUDA graph of one step, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_frac": round(value / world / peak, 4), "hbm_peak_gbs": peak,
+        "us_per_token": round(ms_per_step * 1e3, 2),
+        "breakdown": breakdown, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+    return line
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step one bounded
+    sample of the same workload; the metric is a rate, so a sample gives it."""
+    import numpy as _np  # noqa: F401
+
+    from ggml_block_quantized_gb300 import synth
+    import oracle
+    oracle.lib()
+    if args.workload == "layer_stack":
+        sample = [synth.layer_matrix(0, m, args.n_vec) for m in range(len(synth.LAYER_MATRICES))]
+        for s in sample:
+            s["W"] = s.pop("w_blocks")
+    else:
+        m = synth.single_matrix(args.workload, n_vec=args.n_vec)
+        W = oracle.quantize(m["type"], m["w_f32"]) if "w_f32" in m else m["w_blocks"]
+        sample = [dict(type=m["type"], n_out=m["n_out"], n_in=m["n_in"], W=W, x=m["x"])]
+    per_step_budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(sample[:1], args.n_vec, budget_s=per_step_budget)
+    rates = []
+    cores = 1
+    desc = ""
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, cores, desc = time_oracle(sample, args.n_vec, budget_s=per_step_budget)
+        rates.append(v)
+    wall = time.perf_counter() - t0
+    value = float(np.mean(rates))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded random GGUF blocks; x ~ N(0,1))",
+        "config": {"workload": args.workload, "n_vec": args.n_vec},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="layer_stack",
+                    choices=["layer_stack", "q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000"])
+    ap.add_argument("--n-vec", type=int, default=1)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,239 @@
+"""GB300 block-quantized matrix-vector product: thin Python binding.
+
+The work happens in the CUDA library libqgemv.so (the C ABI of
+include/qgemv.h); this module only marshals arguments: it checks dtypes,
+devices and sizes of torch tensors, allocates outputs with torch when the
+caller passes none, and calls the C entry points with raw device pointers and
+the current CUDA stream. There is no fallback: if the library is missing,
+importing this module raises.
+
+Element types are the ggml ids (Q4_0=2, Q8_0=8, Q4_K=12, Q6_K=14, Q8_K=15).
+"""
+import ctypes
+import os
+
+__all__ = [
+    "F32", "F16", "Q4_0", "Q8_0", "Q4_K", "Q6_K", "Q8_K", "MAX_NVEC", "QGError",
+    "library_path", "lib", "qtype_nbytes", "qtype_block", "qtype_act_type",
+    "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes",
+    "qgemv", "qgemv_xq", "qgemv_block_isums", "device_error", "EXPORTED_SYMBOLS",
+]
+
+F32, F16, Q4_0, Q8_0, Q4_K, Q6_K, Q8_K = 0, 1, 2, 8, 12, 14, 15
+MAX_NVEC = 8
+TYPE_NAMES = {F32: "F32", F16: "F16", Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K",
+              Q8_K: "Q8_K"}
+
+# every function declared in include/qgemv.h
+EXPORTED_SYMBOLS = (
+    "qtype_nbytes", "qtype_block", "qtype_act_type", "qg_status_string", "qg_last_cuda_error",
+    "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes", "qgemv",
+    "qgemv_xq", "qgemv_block_isums", "qg_device_error",
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "_build", "libqgemv.so")
+
+
+class QGError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib().qg_status_string(status).decode()
+        if status == -6:
+            msg += ": " + lib().qg_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """The loaded C library (built by build.py; raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"libqgemv.so not built ({path}); run ggml_block_quantized_gb300/build.py")
+        L = ctypes.CDLL(path)
+        i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        L.qtype_nbytes.argtypes, L.qtype_nbytes.restype = [i32, i64], i64
+        L.qtype_block.argtypes, L.qtype_block.restype = [i32, ctypes.POINTER(i32), ctypes.POINTER(i32)], i32
+        L.qtype_act_type.argtypes, L.qtype_act_type.restype = [i32], i32
+        L.qg_status_string.argtypes, L.qg_status_string.restype = [i32], ctypes.c_char_p
+        L.qg_last_cuda_error.argtypes, L.qg_last_cuda_error.restype = [], ctypes.c_char_p
+        L.quantize_act.argtypes, L.quantize_act.restype = [i32, vp, vp, i64, i64, vp], i32
+        L.quantize_rows.argtypes, L.quantize_rows.restype = [i32, vp, vp, i64, i64, vp], i32
+        L.dequantize_rows.argtypes, L.dequantize_rows.restype = [i32, vp, vp, i64, i64, vp], i32
+        L.qgemv_workspace_bytes.argtypes, L.qgemv_workspace_bytes.restype = [i32, i64, i64], sz
+        L.qgemv.argtypes, L.qgemv.restype = [i32, vp, vp, vp, i64, i64, i64, vp, sz, vp], i32
+        L.qgemv_xq.argtypes, L.qgemv_xq.restype = [i32, vp, vp, vp, i64, i64, i64, vp], i32
+        L.qgemv_block_isums.argtypes, L.qgemv_block_isums.restype = [i32, vp, vp, vp, i64, i64, i64, vp], i32
+        L.qg_device_error.argtypes, L.qg_device_error.restype = [ctypes.POINTER(ctypes.c_int32)], i32
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------ type table
+def qtype_nbytes(t: int, n: int) -> int:
+    return int(lib().qtype_nbytes(t, n))
+
+
+def qtype_block(t: int):
+    e, b = ctypes.c_int(), ctypes.c_int()
+    st = lib().qtype_block(t, ctypes.byref(e), ctypes.byref(b))
+    if st != 0:
+        raise QGError(st, "qtype_block")
+    return e.value, b.value
+
+
+def qtype_act_type(t: int) -> int:
+    return int(lib().qtype_act_type(t))
+
+
+# ------------------------------------------------------------ helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise QGError(st, where)
+
+
+def _dev_tensor(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _need(t, nbytes, name):
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes, needs {nbytes}")
+
+
+# ------------------------------------------------------------ quantizers
+def quantize_act(act_type: int, x, n_vec: int = 1, out=None, stream=None):
+    """x: f32 CUDA tensor of n_vec * n_in values -> uint8 blocks of act_type."""
+    torch = _torch()
+    _dev_tensor(x, torch.float32, "x")
+    n_in = x.numel() // n_vec
+    nbytes = qtype_nbytes(act_type, n_in)
+    if nbytes < 0 or n_in * n_vec != x.numel():
+        raise ValueError("x is not n_vec rows of whole blocks")
+    if out is None:
+        out = torch.empty(nbytes * n_vec, dtype=torch.uint8, device=x.device)
+    _dev_tensor(out, torch.uint8, "out")
+    _need(out, nbytes * n_vec, "out")
+    _check(lib().quantize_act(act_type, _ptr(x), _ptr(out), n_in, n_vec, _stream(stream)), "quantize_act")
+    return out
+
+
+def quantize_rows(t: int, x, n_rows: int, out=None, stream=None):
+    """Weights x (f32, n_rows * n_in) -> Q8_0 or Q4_0 blocks."""
+    torch = _torch()
+    _dev_tensor(x, torch.float32, "x")
+    n_in = x.numel() // n_rows
+    nbytes = qtype_nbytes(t, n_in)
+    if nbytes < 0 or n_in * n_rows != x.numel():
+        raise ValueError("x is not n_rows rows of whole blocks")
+    if out is None:
+        out = torch.empty(nbytes * n_rows, dtype=torch.uint8, device=x.device)
+    _dev_tensor(out, torch.uint8, "out")
+    _need(out, nbytes * n_rows, "out")
+    _check(lib().quantize_rows(t, _ptr(x), _ptr(out), n_rows, n_in, _stream(stream)), "quantize_rows")
+    return out
+
+
+def dequantize_rows(t: int, W, n_rows: int, n_in: int, out=None, stream=None):
+    torch = _torch()
+    _dev_tensor(W, torch.uint8, "W")
+    nbytes = qtype_nbytes(t, n_in)
+    if nbytes < 0:
+        raise ValueError("n_in is not whole blocks")
+    _need(W, nbytes * n_rows, "W")
+    if out is None:
+        out = torch.empty((n_rows, n_in), dtype=torch.float32, device=W.device)
+    _dev_tensor(out, torch.float32, "out")
+    _need(out, 4 * n_rows * n_in, "out")
+    _check(lib().dequantize_rows(t, _ptr(W), _ptr(out), n_rows, n_in, _stream(stream)), "dequantize_rows")
+    return out
+
+
+# ------------------------------------------------------------ product
+def qgemv_workspace_bytes(t: int, n_in: int, n_vec: int = 1) -> int:
+    return int(lib().qgemv_workspace_bytes(t, n_in, n_vec))
+
+
+def qgemv(t: int, W, x, n_out: int, n_in: int, n_vec: int = 1, y=None, workspace=None, stream=None):
+    """y[n_vec, n_out] = W . x for W in blocks of type t, x f32 [n_vec, n_in]."""
+    torch = _torch()
+    _dev_tensor(W, torch.uint8, "W")
+    _dev_tensor(x, torch.float32, "x")
+    _need(x, 4 * n_vec * n_in, "x")
+    if y is None:
+        y = torch.empty((n_vec, n_out), dtype=torch.float32, device=x.device)
+    _dev_tensor(y, torch.float32, "y")
+    _need(y, 4 * n_vec * n_out, "y")
+    need = qgemv_workspace_bytes(t, n_in, n_vec)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _dev_tensor(workspace, torch.uint8, "workspace")
+    _check(lib().qgemv(t, _ptr(W), _ptr(x), _ptr(y), n_out, n_in, n_vec, _ptr(workspace),
+                       workspace.numel(), _stream(stream)), "qgemv")
+    return y
+
+
+def qgemv_xq(t: int, W, xq, n_out: int, n_in: int, n_vec: int = 1, y=None, stream=None):
+    """y = W . x with x already quantized (quantize_act of the paired type)."""
+    torch = _torch()
+    _dev_tensor(W, torch.uint8, "W")
+    _dev_tensor(xq, torch.uint8, "xq")
+    if y is None:
+        y = torch.empty((n_vec, n_out), dtype=torch.float32, device=W.device)
+    _dev_tensor(y, torch.float32, "y")
+    _need(y, 4 * n_vec * n_out, "y")
+    _check(lib().qgemv_xq(t, _ptr(W), _ptr(xq), _ptr(y), n_out, n_in, n_vec, _stream(stream)), "qgemv_xq")
+    return y
+
+
+def qgemv_block_isums(t: int, W, xq, n_out: int, n_in: int, n_vec: int = 1, out=None, stream=None):
+    """Exact per-block int32 sums, shape [n_vec, n_out, nb, k] (k = 2 for Q4_K)."""
+    torch = _torch()
+    _dev_tensor(W, torch.uint8, "W")
+    _dev_tensor(xq, torch.uint8, "xq")
+    elems, _ = qtype_block(t)
+    k = 2 if t == Q4_K else 1
+    shape = (n_vec, n_out, n_in // elems, k)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.int32, device=W.device)
+    _dev_tensor(out, torch.int32, "out")
+    _check(lib().qgemv_block_isums(t, _ptr(W), _ptr(xq), _ptr(out), n_out, n_in, n_vec, _stream(stream)),
+           "qgemv_block_isums")
+    return out
+
+
+def device_error() -> int:
+    """Synchronize, read and clear the kernels' bounded-wait error word."""
+    v = ctypes.c_int32(0)
+    _check(lib().qg_device_error(ctypes.byref(v)), "qg_device_error")
+    return v.value

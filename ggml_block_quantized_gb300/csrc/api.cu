@@ -1,0 +1,412 @@
+// api.cu - the C ABI declared in include/qgemv.h: argument validation,
+// launch planning and kernel launches. Nothing here allocates device memory
+// or synchronizes (except qg_device_error, which says so).
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "gemv_launch.cuh"
+
+namespace qg {
+
+__global__ void quantize_q8_0_kernel(const float *, uint8_t *, int64_t);
+__global__ void quantize_q8_k_kernel(const float *, uint8_t *, int64_t);
+__global__ void quantize_q4_0_kernel(const float *, uint8_t *, int64_t);
+__global__ void dequant_q8_0_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q4_0_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q4_k_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q6_k_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q8_k_kernel(const uint8_t *, float *, int64_t);
+
+__device__ int32_t g_device_error = 0;
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e) {
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return QG_ERR_CUDA;
+}
+
+bool block_info(int type, int *elems, int *bytes) {
+    switch (type) {
+    case QG_F32: *elems = 1; *bytes = 4; return true;
+    case QG_F16: *elems = 1; *bytes = 2; return true;
+    case QG_Q4_0: *elems = 32; *bytes = 18; return true;
+    case QG_Q8_0: *elems = 32; *bytes = 34; return true;
+    case QG_Q4_K: *elems = 256; *bytes = 144; return true;
+    case QG_Q6_K: *elems = 256; *bytes = 210; return true;
+    case QG_Q8_K: *elems = 256; *bytes = 292; return true;
+    default: return false;
+    }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+    int device;
+    int sms;
+    int32_t *err;  // device address of g_device_error on this device
+};
+
+int current_device(DeviceInfo *info) {
+    static int sm_count[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int sms = (dev >= 0 && dev < 64) ? __atomic_load_n(&sm_count[dev], __ATOMIC_RELAXED) : 0;
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (dev >= 0 && dev < 64) __atomic_store_n(&sm_count[dev], sms, __ATOMIC_RELAXED);
+    }
+    static int32_t *err_addr[64] = {nullptr};
+    int32_t *err = (dev >= 0 && dev < 64) ? __atomic_load_n(&err_addr[dev], __ATOMIC_ACQUIRE) : nullptr;
+    if (!err) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_device_error);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (dev >= 0 && dev < 64) __atomic_store_n(&err_addr[dev], err, __ATOMIC_RELEASE);
+    }
+    info->device = dev;
+    info->sms = sms;
+    info->err = err;
+    return QG_OK;
+}
+
+int env_int(const char *name, int dflt, int lo, int hi) {
+    const char *s = std::getenv(name);
+    if (!s || !*s) return dflt;
+    int v = std::atoi(s);
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
+// Tuning of the GEMV launch (read once): CTAs resident per SM that the grid
+// aims at, and the shared-memory ring budget per CTA in KiB.
+int tune_ctas_per_sm() {
+    static const int v = env_int("QG_CTAS_PER_SM", 2, 1, 4);
+    return v;
+}
+int tune_ring_kib() {
+    static const int v = env_int("QG_RING_KIB", 64, 16, 200);
+    return v;
+}
+
+size_t act_smem_bytes(int type, int nb, int nv) {
+    switch (type) {
+    case QG_Q8_0: return TypeQ8_0::act_bytes(nb, nv);
+    case QG_Q4_0: return TypeQ4_0::act_bytes(nb, nv);
+    case QG_Q4_K: return TypeQ4_K::act_bytes(nb, nv);
+    case QG_Q6_K: return TypeQ6_K::act_bytes(nb, nv);
+    default: return 0;
+    }
+}
+
+size_t round16(size_t v) { return (v + 15) & ~size_t(15); }
+
+constexpr int kSmemTailPad = 16;  // unaligned word reads may touch up to 4 bytes past a stage
+
+// Stage geometry and grid of one GEMV launch. Returns QG_OK or QG_ERR_SHAPE.
+int plan_gemv(int type, int64_t n_out, int64_t n_in, int nv, int sms, GemvParams *p, GemvLaunch *l) {
+    int elems, bytes;
+    block_info(type, &elems, &bytes);
+    const int64_t nb = n_in / elems;
+    const int64_t row_bytes = nb * bytes;
+    const size_t act = round16(act_smem_bytes(type, static_cast<int>(nb), nv));
+    const size_t ring_target = static_cast<size_t>(tune_ring_kib()) * 1024;
+    for (int split = 1; split <= kConsumerWarps; split *= 2) {
+        const int R = kConsumerWarps / split;
+        const size_t stage = round16(static_cast<size_t>(R) * row_bytes + 15);
+        if (split < kConsumerWarps && stage > 20480) continue;  // prefer stages of <= 20 KiB
+        const size_t fixed = kHeaderBytes + act + kSmemTailPad;
+        if (fixed + 2 * stage > static_cast<size_t>(kSmemLimit)) continue;
+        int S = static_cast<int>(ring_target / stage);
+        S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+        while (S > 2 && fixed + S * stage > static_cast<size_t>(kSmemLimit)) --S;
+        const size_t smem = fixed + S * stage;
+        p->row_bytes = row_bytes;
+        p->w_total = row_bytes * n_out;
+        p->n_out = static_cast<int>(n_out);
+        p->nb = static_cast<int>(nb);
+        p->rows_per_stage = R;
+        p->split = split;
+        p->n_stages = S;
+        p->stage_bytes = static_cast<int>(stage);
+        p->act_bytes = static_cast<int>(act);
+        const int per_sm_fit = static_cast<int>((228 * 1024) / (smem + 1024));
+        int per_sm = tune_ctas_per_sm();
+        if (per_sm > per_sm_fit) per_sm = per_sm_fit < 1 ? 1 : per_sm_fit;
+        const int64_t tiles = (n_out + R - 1) / R;
+        const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+        l->grid = static_cast<int>(tiles < cap ? tiles : cap);
+        l->smem = static_cast<int>(smem);
+        return QG_OK;
+    }
+    return QG_ERR_SHAPE;
+}
+
+cudaError_t launch_gemv(int type, const GemvParams &p, int nv, bool isums, const GemvLaunch &l, int device,
+                        cudaStream_t s) {
+    switch (type) {
+    case QG_Q8_0: return launch_gemv_q8_0(p, nv, isums, l, device, s);
+    case QG_Q4_0: return launch_gemv_q4_0(p, nv, isums, l, device, s);
+    case QG_Q4_K: return launch_gemv_q4_k(p, nv, isums, l, device, s);
+    case QG_Q6_K: return launch_gemv_q6_k(p, nv, isums, l, device, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// Weight-type checks shared by the product entry points.
+int check_weight_type(int type) {
+    int e, b;
+    if (!block_info(type, &e, &b)) return QG_ERR_TYPE;
+    if (qtype_act_type(type) < 0) return QG_ERR_PAIR;
+    return QG_OK;
+}
+
+int check_gemv_shape(int type, int64_t n_out, int64_t n_in, int64_t n_vec) {
+    int elems, bytes;
+    block_info(type, &elems, &bytes);
+    if (n_out < 0 || n_in < 0 || n_out > INT32_MAX) return QG_ERR_SHAPE;
+    if (n_vec < 1 || n_vec > QG_MAX_NVEC) return QG_ERR_SHAPE;
+    if (n_in % elems != 0 || n_in / elems > INT32_MAX / 4) return QG_ERR_SHAPE;
+    return QG_OK;
+}
+
+int launch_quantize(int act_type, const float *x, void *xq, int64_t n_blocks, int sms, cudaStream_t s) {
+    if (n_blocks == 0) return QG_OK;
+    const int warps_per_cta = 8;
+    int64_t grid = (n_blocks + warps_per_cta - 1) / warps_per_cta;
+    if (grid > static_cast<int64_t>(sms) * 16) grid = static_cast<int64_t>(sms) * 16;
+    cudaError_t e;
+    if (act_type == QG_Q8_0)
+        e = launch_pdl(quantize_q8_0_kernel, static_cast<int>(grid), 32 * warps_per_cta, 0, s, x,
+                       static_cast<uint8_t *>(xq), n_blocks);
+    else if (act_type == QG_Q8_K)
+        e = launch_pdl(quantize_q8_k_kernel, static_cast<int>(grid), 32 * warps_per_cta, 0, s, x,
+                       static_cast<uint8_t *>(xq), n_blocks);
+    else
+        e = launch_pdl(quantize_q4_0_kernel, static_cast<int>(grid), 32 * warps_per_cta, 0, s, x,
+                       static_cast<uint8_t *>(xq), n_blocks);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
+// The product on quantized activations xq (shared by qgemv, qgemv_xq and
+// qgemv_block_isums). Arguments are already validated.
+int run_gemv(int type, const void *W, const void *xq, float *y, int32_t *isums, int64_t n_out, int64_t n_in,
+             int64_t n_vec, const DeviceInfo &dev, cudaStream_t s) {
+    GemvParams p = {};
+    GemvLaunch l = {};
+    int st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, &p, &l);
+    if (st != QG_OK) return st;
+    p.W = static_cast<const uint8_t *>(W);
+    p.xq = static_cast<const uint8_t *>(xq);
+    p.y = y;
+    p.isums = isums;
+    p.err = dev.err;
+    cudaError_t e = launch_gemv(type, p, static_cast<int>(n_vec), isums != nullptr, l, dev.device, s);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
+// Validation shared by qgemv_xq and qgemv_block_isums.
+int check_gemv_args(int type, const void *W, const void *xq, const void *out, int64_t n_out, int64_t n_in,
+                    int64_t n_vec) {
+    int st = check_weight_type(type);
+    if (st != QG_OK) return st;
+    st = check_gemv_shape(type, n_out, n_in, n_vec);
+    if (st != QG_OK) return st;
+    if (n_out > 0 && (!W || !out)) return QG_ERR_NULL;
+    if (n_out > 0 && n_in > 0 && !xq) return QG_ERR_NULL;
+    if ((W && !aligned16(W)) || (xq && !aligned16(xq)) || (out && !aligned16(out))) return QG_ERR_ALIGN;
+    return QG_OK;
+}
+
+}  // namespace
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+int64_t qtype_nbytes(int type, int64_t n) {
+    int elems, bytes;
+    if (!block_info(type, &elems, &bytes)) return -1;
+    if (n < 0 || n % elems != 0) return -1;
+    return n / elems * bytes;
+}
+
+int qtype_block(int type, int *elems, int *bytes) {
+    int e, b;
+    if (!block_info(type, &e, &b)) return QG_ERR_TYPE;
+    if (!elems || !bytes) return QG_ERR_NULL;
+    *elems = e;
+    *bytes = b;
+    return QG_OK;
+}
+
+int qtype_act_type(int weight_type) {
+    switch (weight_type) {
+    case QG_Q4_0:
+    case QG_Q8_0: return QG_Q8_0;
+    case QG_Q4_K:
+    case QG_Q6_K: return QG_Q8_K;
+    default: return QG_ERR_PAIR;
+    }
+}
+
+const char *qg_status_string(int status) {
+    switch (status) {
+    case QG_OK: return "ok";
+    case QG_ERR_TYPE: return "unknown or unsupported type";
+    case QG_ERR_SHAPE: return "bad shape (not whole blocks, or a size out of range)";
+    case QG_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case QG_ERR_NULL: return "required pointer is NULL";
+    case QG_ERR_PAIR: return "weight type has no activation pairing";
+    case QG_ERR_CUDA: return "CUDA error";
+    case QG_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+const char *qg_last_cuda_error(void) { return g_last_cuda_error; }
+
+int quantize_act(int act_type, const float *x, void *xq, int64_t n_in, int64_t n_vec, qg_stream_t stream) {
+    int elems, bytes;
+    if (!block_info(act_type, &elems, &bytes)) return QG_ERR_TYPE;
+    if (act_type != QG_Q8_0 && act_type != QG_Q8_K) return QG_ERR_TYPE;
+    if (n_in < 0 || n_vec < 0 || n_in % elems != 0) return QG_ERR_SHAPE;
+    const int64_t n_blocks = n_in / elems * n_vec;
+    if (n_blocks == 0) return QG_OK;
+    if (!x || !xq) return QG_ERR_NULL;
+    if (!aligned16(x) || !aligned16(xq)) return QG_ERR_ALIGN;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st != QG_OK) return st;
+    return launch_quantize(act_type, x, xq, n_blocks, dev.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int quantize_rows(int type, const float *x, void *out, int64_t n_rows, int64_t n_in, qg_stream_t stream) {
+    int elems, bytes;
+    if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
+    if (type != QG_Q8_0 && type != QG_Q4_0) return QG_ERR_TYPE;
+    if (n_in < 0 || n_rows < 0 || n_in % elems != 0) return QG_ERR_SHAPE;
+    const int64_t n_blocks = n_in / elems * n_rows;
+    if (n_blocks == 0) return QG_OK;
+    if (!x || !out) return QG_ERR_NULL;
+    if (!aligned16(x) || !aligned16(out)) return QG_ERR_ALIGN;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st != QG_OK) return st;
+    return launch_quantize(type, x, out, n_blocks, dev.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dequantize_rows(int type, const void *W, float *out, int64_t n_rows, int64_t n_in, qg_stream_t stream) {
+    int elems, bytes;
+    if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
+    if (type == QG_F32 || type == QG_F16) return QG_ERR_TYPE;
+    if (n_in < 0 || n_rows < 0 || n_in % elems != 0) return QG_ERR_SHAPE;
+    const int64_t groups = n_in / 8 * n_rows;
+    if (groups == 0) return QG_OK;
+    if (!W || !out) return QG_ERR_NULL;
+    if (!aligned16(W) || !aligned16(out)) return QG_ERR_ALIGN;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st != QG_OK) return st;
+    const int threads = 256;
+    int64_t grid = (groups + threads - 1) / threads;
+    if (grid > static_cast<int64_t>(dev.sms) * 16) grid = static_cast<int64_t>(dev.sms) * 16;
+    const uint8_t *w = static_cast<const uint8_t *>(W);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const unsigned g = static_cast<unsigned>(grid);
+    switch (type) {
+    case QG_Q8_0: dequant_q8_0_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q4_0: dequant_q4_0_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q4_K: dequant_q4_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q6_K: dequant_q6_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q8_K: dequant_q8_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    default: return QG_ERR_TYPE;
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+}
+
+size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec) {
+    if (check_weight_type(type) != QG_OK) return 0;
+    if (check_gemv_shape(type, 0, n_in, n_vec) != QG_OK) return 0;
+    const int64_t nb = qtype_nbytes(qtype_act_type(type), n_in);
+    return nb < 0 ? 0 : static_cast<size_t>(nb * n_vec);
+}
+
+int qgemv_xq(int type, const void *W, const void *xq, float *y, int64_t n_out, int64_t n_in, int64_t n_vec,
+             qg_stream_t stream) {
+    int st = check_gemv_args(type, W, xq, y, n_out, n_in, n_vec);
+    if (st != QG_OK) return st;
+    if (n_out == 0) return QG_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_in == 0) {  // the empty sum
+        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(n_out * n_vec) * sizeof(float), s);
+        return e == cudaSuccess ? QG_OK : cuda_fail(e);
+    }
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != QG_OK) return st;
+    return run_gemv(type, W, xq, y, nullptr, n_out, n_in, n_vec, dev, s);
+}
+
+int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, int64_t n_out, int64_t n_in,
+                      int64_t n_vec, qg_stream_t stream) {
+    int st = check_gemv_args(type, W, xq, isums, n_out, n_in, n_vec);
+    if (st != QG_OK) return st;
+    if (n_out == 0 || n_in == 0) return QG_OK;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != QG_OK) return st;
+    return run_gemv(type, W, xq, nullptr, isums, n_out, n_in, n_vec, dev,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in, int64_t n_vec,
+          void *workspace, size_t workspace_bytes, qg_stream_t stream) {
+    int st = check_gemv_args(type, W, x, y, n_out, n_in, n_vec);
+    if (st != QG_OK) return st;
+    if (n_out == 0) return QG_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_in == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(n_out * n_vec) * sizeof(float), s);
+        return e == cudaSuccess ? QG_OK : cuda_fail(e);
+    }
+    const size_t need = qgemv_workspace_bytes(type, n_in, n_vec);
+    if (!workspace || workspace_bytes < need) return QG_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return QG_ERR_ALIGN;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != QG_OK) return st;
+    // the product's shape limits are checked before anything is enqueued
+    GemvParams probe = {};
+    GemvLaunch pl = {};
+    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, &probe, &pl);
+    if (st != QG_OK) return st;
+    const int at = qtype_act_type(type);
+    int elems, bytes;
+    block_info(at, &elems, &bytes);
+    st = launch_quantize(at, x, workspace, n_in / elems * n_vec, dev.sms, s);
+    if (st != QG_OK) return st;
+    return run_gemv(type, W, workspace, y, nullptr, n_out, n_in, n_vec, dev, s);
+}
+
+int qg_device_error(int32_t *code) {
+    if (!code) return QG_ERR_NULL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    int32_t v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *code = v;
+    return QG_OK;
+}
+
+}  // extern "C"

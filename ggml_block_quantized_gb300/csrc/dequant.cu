@@ -1,0 +1,125 @@
+// dequant.cu - dequantize_rows: every element of a block-quantized matrix
+// to f32 ("Quantization" (sipllm), Per-format dequant; "量化格式" (candle),
+// block structure table; "Quantization" (rml), Unpacking the packed fields).
+//
+// Each thread writes 8 consecutive elements (two 16-byte streaming stores),
+// consecutive threads consecutive groups, so the f32 output -- the bulk of
+// the traffic, 4 bytes per element against 0.56..1.06 read -- is written
+// fully coalesced. Every product below is exact in f32 (a f16 d has 11
+// significant bits, the sub-block scales at most 7, the codes at most 6), so
+// the values are unique and equal the scalar definition bit for bit; the
+// explicit __fmul_rn/__fsub_rn only make the order visible.
+#include "qg_common.cuh"
+
+namespace qg {
+
+__device__ __forceinline__ void store8(float *dst, const float (&v)[8]) {
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    __stcs(d4, make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(d4 + 1, make_float4(v[4], v[5], v[6], v[7]));
+}
+
+__device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p) {
+    return static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t *>(p)));
+}
+
+// groups: total 8-element groups = n_rows * n_in / 8; W is the flat block stream.
+__global__ void dequant_q8_0_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 2) * 34;
+        const float d = f16_bits_to_f32(ldg_u16(blk));
+        const uint8_t *qs = blk + 2 + 8 * (g & 3);
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(static_cast<float>(static_cast<int8_t>(__ldg(qs + i))), d);
+        store8(out + g * 8, v);
+    }
+}
+
+__global__ void dequant_q4_0_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 2) * 18;
+        const float d = f16_bits_to_f32(ldg_u16(blk));
+        const int q = static_cast<int>(g & 3);       // elements 8q..8q+7 of the block
+        const uint8_t *qs = blk + 2 + 8 * (q & 1);   // bytes (8q..8q+7) mod 16
+        const int shift = q >= 2 ? 4 : 0;            // elements 16.. use the high nibble
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int code = (__ldg(qs + i) >> shift) & 0xF;
+            v[i] = __fmul_rn(static_cast<float>(code - 8), d);
+        }
+        store8(out + g * 8, v);
+    }
+}
+
+__global__ void dequant_q4_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 5) * 144;
+        const int e0 = 8 * static_cast<int>(g & 31);
+        const int j = e0 >> 5;                      // sub-block
+        const float d = f16_bits_to_f32(ldg_u16(blk));
+        const float dmin = f16_bits_to_f32(ldg_u16(blk + 2));
+        const uint8_t *s = blk + 4;
+        int sc, m;
+        if (j < 4) {
+            sc = __ldg(s + j) & 63;
+            m = __ldg(s + j + 4) & 63;
+        } else {
+            sc = (__ldg(s + j + 4) & 0xF) | ((__ldg(s + j - 4) >> 6) << 4);
+            m = (__ldg(s + j + 4) >> 4) | ((__ldg(s + j) >> 6) << 4);
+        }
+        const int p = e0 & 63;                       // position in the 64-element chunk
+        const uint8_t *qs = blk + 16 + 32 * (e0 >> 6) + (p & 31);
+        const int shift = p >= 32 ? 4 : 0;
+        const float dsc = __fmul_rn(d, static_cast<float>(sc));
+        const float off = __fmul_rn(dmin, static_cast<float>(m));
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = (__ldg(qs + i) >> shift) & 0xF;
+            v[i] = __fsub_rn(__fmul_rn(dsc, static_cast<float>(q)), off);
+        }
+        store8(out + g * 8, v);
+    }
+}
+
+__global__ void dequant_q6_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 5) * 210;
+        const int e0 = 8 * static_cast<int>(g & 31);
+        const int h = e0 >> 7, k = (e0 >> 5) & 3, l0 = e0 & 31;
+        const float d = f16_bits_to_f32(ldg_u16(blk + 208));
+        const int sc = static_cast<int8_t>(__ldg(blk + 192 + (e0 >> 4)));
+        const float dsc = __fmul_rn(d, static_cast<float>(sc));
+        const uint8_t *ql = blk + 64 * h + 32 * (k & 1) + l0;
+        const uint8_t *qh = blk + 128 + 32 * h + l0;
+        const int lshift = k >= 2 ? 4 : 0;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = ((__ldg(ql + i) >> lshift) & 0xF) | (((__ldg(qh + i) >> (2 * k)) & 3) << 4);
+            v[i] = __fmul_rn(dsc, static_cast<float>(q - 32));
+        }
+        store8(out + g * 8, v);
+    }
+}
+
+__global__ void dequant_q8_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 5) * 292;
+        const float d = __ldg(reinterpret_cast<const float *>(blk));
+        const int8_t *qs = reinterpret_cast<const int8_t *>(blk + 4 + 8 * (g & 31));
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(static_cast<float>(__ldg(qs + i)), d);
+        store8(out + g * 8, v);
+    }
+}
+
+}  // namespace qg

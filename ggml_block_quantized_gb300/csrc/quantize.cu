@@ -1,0 +1,137 @@
+// quantize.cu - activation and weight quantizers (byte-exact GGUF blocks).
+//
+// Q8_0 ("Building Q8_0 and Q4_0 Like ggml", Example 2; "量化格式" (candle),
+// BlockQ8_0::from_float): per 32 values amax = max |x| (NaN ignored),
+// d = amax / 127 (f32), id = 1/d or 0, stored d = f16(d), code =
+// roundf(x * id) with halves away from zero, from the unrounded id.
+// Q8_K: the same rule per 256 values with d kept in f32, codes clamped to
+// [-127, 127] and bsums[k] = sum of codes 16k..16k+15 (the library's reading;
+// the pages give only the block layout and the role of bsums).
+// Q4_0 ("Building Q8_0 and Q4_0 Like ggml", Example 5; "Quantization" (rml),
+// A worked example: Q4_0): the first value of strictly largest magnitude is
+// max, d = max / -8, id = 1/d or 0, code = min(15, (int)(x*id + 8.5f)) with
+// the multiply and the add rounded separately; byte j = code j | code j+16 << 4.
+//
+// One warp per block. The only float operations are the IEEE-rounded
+// division, reciprocal, multiply and add written below (the library is built
+// without fast-math, so '/' is correctly rounded), roundf and the f16
+// conversion, so the bytes equal the scalar definition's.
+#include "qg_common.cuh"
+
+namespace qg {
+
+__device__ __forceinline__ float warp_max_abs(float a) {
+    // fmaxf ignores NaN, as the scalar rule's comparison does
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+    return a;
+}
+
+// ---------------------------------------------------------------- Q8_0
+// out: n_blocks x 34 bytes. One warp per block, lane i owns element i.
+__global__ void quantize_q8_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
+                                     int64_t n_blocks) {
+    pdl_allow_dependents();
+    pdl_wait_prior_grids();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks;
+         b += warps) {
+        const float v = __ldg(x + b * 32 + lane);
+        const float amax = warp_max_abs(fabsf(v));
+        const float d = amax / 127.0f;
+        const float id = d != 0.0f ? 1.0f / d : 0.0f;
+        const int q = code_from_rounded(roundf(__fmul_rn(v, id)), -128, 127);
+        uint8_t *blk = out + b * 34;
+        blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+        if (lane == 0) {
+            const unsigned short h = __half_as_ushort(__float2half_rn(d));
+            blk[0] = static_cast<uint8_t>(h & 0xFF);
+            blk[1] = static_cast<uint8_t>(h >> 8);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- Q8_K
+// out: n_blocks x 292 bytes (f32 d | 256 int8 | 16 int16 bsums). One warp
+// per block, lane i owns elements 8i..8i+7.
+__global__ void quantize_q8_k_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
+                                     int64_t n_blocks) {
+    pdl_allow_dependents();
+    pdl_wait_prior_grids();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks;
+         b += warps) {
+        const float4 *src = reinterpret_cast<const float4 *>(x + b * 256 + 8 * lane);
+        const float4 u = __ldg(src), w = __ldg(src + 1);
+        const float v[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+        const float amax = warp_max_abs(a);
+        const float d = amax / 127.0f;
+        const float id = d != 0.0f ? 1.0f / d : 0.0f;
+        uint32_t packed[2] = {0u, 0u};
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = code_from_rounded(roundf(__fmul_rn(v[i], id)), -127, 127);
+            sum += q;
+            packed[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
+        }
+        // bsums[k] covers lanes 2k and 2k+1
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        uint8_t *blk = out + b * 292;
+        uint32_t *qs = reinterpret_cast<uint32_t *>(blk + 4 + 8 * lane);
+        qs[0] = packed[0];
+        qs[1] = packed[1];
+        if ((lane & 1) == 0) reinterpret_cast<int16_t *>(blk + 260)[lane >> 1] = static_cast<int16_t>(sum);
+        if (lane == 0) *reinterpret_cast<float *>(blk) = d;
+    }
+}
+
+// ---------------------------------------------------------------- Q4_0
+__global__ void quantize_q4_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
+                                     int64_t n_blocks) {
+    pdl_allow_dependents();
+    pdl_wait_prior_grids();
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks;
+         b += warps) {
+        const float v = __ldg(x + b * 32 + lane);
+        // First index of strictly largest |x| in scan order: reduce (|x|, index)
+        // keeping the larger magnitude and, on a tie, the smaller index. NaN
+        // never wins (the scalar test amax < |x| is false for NaN).
+        float best = (v != v) ? -1.0f : fabsf(v);
+        int idx = lane;
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, m);
+            const int oi = __shfl_xor_sync(0xffffffffu, idx, m);
+            if (ob > best || (ob == best && oi < idx)) {
+                best = ob;
+                idx = oi;
+            }
+        }
+        const float vmax = __shfl_sync(0xffffffffu, v, idx);
+        // an all-zero block keeps max = +0 (no element replaces it)
+        const float mx = best > 0.0f ? vmax : 0.0f;
+        const float d = mx / -8.0f;
+        const float id = d != 0.0f ? 1.0f / d : 0.0f;
+        const float t = __fadd_rn(__fmul_rn(v, id), 8.5f);
+        int code = static_cast<int>(t);  // truncation toward zero, t >= 0
+        code = code < 15 ? code : 15;
+        const int hi = __shfl_down_sync(0xffffffffu, code, 16);
+        uint8_t *blk = out + b * 18;
+        if (lane < 16) blk[2 + lane] = static_cast<uint8_t>(code | (hi << 4));
+        if (lane == 0) {
+            const unsigned short h = __half_as_ushort(__float2half_rn(d));
+            blk[0] = static_cast<uint8_t>(h & 0xFF);
+            blk[1] = static_cast<uint8_t>(h >> 8);
+        }
+    }
+}
+
+}  // namespace qg

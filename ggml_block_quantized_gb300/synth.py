@@ -1,0 +1,117 @@
+"""Seeded synthetic inputs for the block-quantized GEMV workloads.
+
+This module draws random numbers and packs them into arrays; it contains none
+of the method's arithmetic (no quantizer, no dequantizer, no dot product).
+Both the tests (which feed the oracle) and the benchmark use it, so both
+sides see identical bytes. All arrays are numpy, on the host.
+
+Workloads (names used across tests and bench.py):
+  q8_0_256x1024   Q8_0 weights from f32 N(0, 0.02), 256 x 1024, x ~ N(0, 1)
+  q4_0_4096       Q4_0 weights from f32 N(0, 0.02), 4096 x 4096, x ~ N(0, 1)
+  q4_k_4096       Q4_K random super-blocks, 4096 x 4096: d, dmin = f16 of
+                  |N(0,1)| * 1e-3, 12 uniform scale bytes, 128 uniform qs bytes
+  q6_k_32000      Q6_K random super-blocks, 32000 x 4096: ql and qh uniform
+                  bytes, scales int8 uniform in [-32, 31], d = f16 of
+                  |N(0,1)| * 1e-3 (stored last, at byte 208)
+  layer_stack     32 decoder layers, each Q4_K q/k/v/o 4096 x 4096, Q4_K
+                  gate/up 11008 x 4096, Q6_K down 4096 x 11008 (random blocks
+                  as above), a fresh x ~ N(0, 1) per matrix and vector
+Seeds: weights 1000 + workload index, activations 2000 + workload index; the
+layer stack derives per-(layer, matrix) streams from those.
+"""
+import numpy as np
+
+Q4_0, Q8_0, Q4_K, Q6_K = 2, 8, 12, 14
+BLOCK = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+
+WORKLOADS = ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000", "layer_stack"]
+
+# (name, type, n_out, n_in) of one decoder layer of the stack
+LAYER_MATRICES = [
+    ("q", Q4_K, 4096, 4096),
+    ("k", Q4_K, 4096, 4096),
+    ("v", Q4_K, 4096, 4096),
+    ("o", Q4_K, 4096, 4096),
+    ("gate", Q4_K, 11008, 4096),
+    ("up", Q4_K, 11008, 4096),
+    ("down", Q6_K, 4096, 11008),
+]
+N_LAYERS = 32
+
+
+def f32_normal(rng, n, std=1.0) -> np.ndarray:
+    x = rng.standard_normal(n, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
+
+
+def random_bytes(rng, n) -> np.ndarray:
+    return np.frombuffer(rng.bytes(n), dtype=np.uint8).copy()
+
+
+def _half_scales(rng, n) -> np.ndarray:
+    """n f16 values |N(0,1)| * 1e-3, as little-endian byte pairs [n, 2]."""
+    v = (np.abs(rng.standard_normal(n)) * 1e-3).astype(np.float16)
+    return v.view(np.uint8).reshape(n, 2)
+
+
+def k_blocks(wtype: int, n_blocks: int, rng) -> np.ndarray:
+    """Random Q4_K or Q6_K super-blocks (flat uint8, n_blocks * block bytes)."""
+    _, nbytes = BLOCK[wtype]
+    raw = random_bytes(rng, n_blocks * nbytes).reshape(n_blocks, nbytes)
+    if wtype == Q4_K:
+        raw[:, 0:2] = _half_scales(rng, n_blocks)
+        raw[:, 2:4] = _half_scales(rng, n_blocks)
+    elif wtype == Q6_K:
+        sc = rng.integers(-32, 32, size=(n_blocks, 16), dtype=np.int8)
+        raw[:, 192:208] = sc.view(np.uint8)
+        raw[:, 208:210] = _half_scales(rng, n_blocks)
+    else:
+        raise ValueError("k_blocks takes Q4_K or Q6_K")
+    return raw.reshape(-1)
+
+
+def workload_index(name: str) -> int:
+    return WORKLOADS.index(name) + 1
+
+
+def single_matrix(name: str, n_vec: int = 1, n_out: int = None, n_in: int = None):
+    """Inputs of one of the single-matrix workloads, optionally resized.
+
+    Returns dict(type, n_out, n_in, n_vec, x[f32 n_vec*n_in], and either
+    w_f32 (f32 weights to quantize, Q8_0/Q4_0) or w_blocks (uint8 blocks)).
+    """
+    idx = workload_index(name)
+    spec = {
+        "q8_0_256x1024": (Q8_0, 256, 1024),
+        "q4_0_4096": (Q4_0, 4096, 4096),
+        "q4_k_4096": (Q4_K, 4096, 4096),
+        "q6_k_32000": (Q6_K, 32000, 4096),
+    }[name]
+    t, d_out, d_in = spec
+    n_out = d_out if n_out is None else n_out
+    n_in = d_in if n_in is None else n_in
+    wr = np.random.default_rng(1000 + idx)
+    xr = np.random.default_rng(2000 + idx)
+    out = dict(type=t, n_out=n_out, n_in=n_in, n_vec=n_vec, x=f32_normal(xr, n_vec * n_in))
+    if t in (Q8_0, Q4_0):
+        out["w_f32"] = f32_normal(wr, n_out * n_in, std=0.02)
+    else:
+        out["w_blocks"] = k_blocks(t, n_out * n_in // 256, wr)
+    return out
+
+
+def layer_matrix(layer: int, m: int, n_vec: int = 1):
+    """Matrix m (index into LAYER_MATRICES) of decoder layer `layer`."""
+    name, t, n_out, n_in = LAYER_MATRICES[m]
+    idx = workload_index("layer_stack")
+    wr = np.random.default_rng([1000 + idx, layer, m])
+    xr = np.random.default_rng([2000 + idx, layer, m])
+    return dict(name=name, type=t, n_out=n_out, n_in=n_in, n_vec=n_vec,
+                w_blocks=k_blocks(t, n_out * n_in // 256, wr), x=f32_normal(xr, n_vec * n_in))
+
+
+def layer_stack_bytes() -> int:
+    per_layer = sum(n_out * n_in // 256 * BLOCK[t][1] for _, t, n_out, n_in in LAYER_MATRICES)
+    return per_layer * N_LAYERS

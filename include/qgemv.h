@@ -1,0 +1,196 @@
+/*
+ * qgemv.h - C ABI of the GB300 block-quantized matrix-vector product.
+ *
+ * y = W . x for W stored as byte-exact GGUF blocks (Q8_0, Q4_0, Q4_K,
+ * Q6_K), x quantized once per call to the activation blocks paired with the
+ * weight type (Q8_0 or Q8_K), exact int32 sums inside every block and float
+ * only for the block scales.
+ *
+ * Citations name the reference pages by title and section:
+ *   [rml]      "Quantization" (rayaq.ca/rml)
+ *   [sipllm]   "Quantization" (sipllm docs)
+ *   [lesson21] "Building Q8_0 and Q4_0 Like ggml" (codeloopback)
+ *   [candle]   "量化格式" (quantized formats, candle)
+ *
+ * Conventions for every call below
+ *   - Pointers named W, x, xq, y, out, isums, workspace are DEVICE pointers
+ *     (cudaMalloc / torch CUDA tensors) owned by the caller. The library
+ *     allocates nothing and keeps no reference after the call returns.
+ *   - Every device pointer must be 16-byte aligned (QG_ERR_ALIGN otherwise).
+ *   - W is [n_out][n_in] row-major: row o starts at byte o * qtype_nbytes(type,
+ *     n_in), rows and blocks follow each other with no padding ([lesson21]
+ *     Example 9). x is f32 [n_vec][n_in], y is f32 [n_vec][n_out]:
+ *     y[v * n_out + o] = sum_i W[o, i] * x[v, i].
+ *   - n_in must be a whole number of blocks (QG_ERR_SHAPE otherwise;
+ *     [lesson21] Example 15 rejects a row of 100). 1 <= n_vec <= QG_MAX_NVEC.
+ *   - All work is enqueued on `stream` (NULL = the legacy default stream);
+ *     no call synchronizes. Argument errors are returned before anything is
+ *     enqueued. A CUDA launch error is returned as QG_ERR_CUDA.
+ *   - Kernels launched by these calls use programmatic dependent launch: a
+ *     qgemv call may begin reading W while the previous call on the same
+ *     stream is still finishing. W must therefore not be written by the call
+ *     immediately before on the same stream (any other stream-ordered work
+ *     in between, such as a copy or an ordinary kernel, restores full
+ *     ordering). x, y and the workspace follow ordinary stream order.
+ *   - Inputs with NaN or inf are outside the contract of the product; the
+ *     quantizers map NaN to code 0 and let an infinite scale through, as
+ *     [candle] "一些边界值" (special values) shows.
+ */
+#ifndef GB300_QGEMV_H
+#define GB300_QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared opaquely so this header does not
+ * need the CUDA headers. */
+typedef struct CUstream_st *qg_stream_t;
+
+/* ggml element-type ids, the numbers a GGUF tensor record stores
+ * ([rml] The type table; [sipllm] On-disk block geometry). */
+enum qg_type {
+    QG_F32 = 0,
+    QG_F16 = 1,
+    QG_Q4_0 = 2,   /* 32 elements, 18 bytes: f16 d, 16 bytes of nibbles      */
+    QG_Q8_0 = 8,   /* 32 elements, 34 bytes: f16 d, 32 int8                  */
+    QG_Q4_K = 12,  /* 256 elements, 144 bytes: f16 d, f16 dmin, 12 B scales, 128 B qs */
+    QG_Q6_K = 14,  /* 256 elements, 210 bytes: 128 B ql, 64 B qh, 16 int8 scales, f16 d */
+    QG_Q8_K = 15   /* 256 elements, 292 bytes: f32 d, 256 int8, 16 int16 bsums (activations only) */
+};
+
+enum qg_status {
+    QG_OK = 0,
+    QG_ERR_TYPE = -1,      /* unknown or unsupported type id                  */
+    QG_ERR_SHAPE = -2,     /* n not whole blocks, a size out of range         */
+    QG_ERR_ALIGN = -3,     /* a device pointer not 16-byte aligned            */
+    QG_ERR_NULL = -4,      /* a required pointer is NULL                      */
+    QG_ERR_PAIR = -5,      /* the weight type has no activation pairing       */
+    QG_ERR_CUDA = -6,      /* a CUDA call failed (see qg_last_cuda_error)     */
+    QG_ERR_WORKSPACE = -7  /* workspace NULL or smaller than required         */
+};
+
+#define QG_MAX_NVEC 8
+
+/* ---- Type table ---------------------------------------------------------- */
+
+/* Bytes taken by n elements of `type`: n / block_elems * block_bytes
+ * ([rml] The type table; [sipllm] type_nbytes). Returns -1 for an unknown
+ * type or when n is negative or not a whole number of blocks. */
+int64_t qtype_nbytes(int type, int64_t n);
+
+/* Block geometry of `type` ([candle] GgmlDType table). Writes the elements
+ * and bytes of one block; returns QG_OK or QG_ERR_TYPE (outputs untouched).
+ * elems/bytes are host pointers and may not be NULL. */
+int qtype_block(int type, int *elems, int *bytes);
+
+/* Activation type paired with a weight type ([rml] DotActivationType;
+ * [candle] VecDotType table): Q4_0 and Q8_0 -> QG_Q8_0, Q4_K and Q6_K ->
+ * QG_Q8_K. Returns QG_ERR_PAIR for any other type. */
+int qtype_act_type(int weight_type);
+
+/* Static text for a status code. Never NULL. */
+const char *qg_status_string(int status);
+
+/* Text of the last CUDA error seen by this library on the calling thread
+ * ("" if none). */
+const char *qg_last_cuda_error(void);
+
+/* ---- Quantizers ---------------------------------------------------------- */
+
+/* Activation quantization, once per call ([rml] Quantization; [lesson21]
+ * Example 2; [candle] BlockQ8_0::from_float):
+ *   act_type QG_Q8_0: per 32 elements amax = max |x|, d = amax / 127 (f32),
+ *     id = 1/d (0 if d == 0), stored d = f16(d), code = roundf(x * id)
+ *     (halves away from zero, codes from the unrounded id).
+ *   act_type QG_Q8_K: the same rule per 256 elements with d stored as f32,
+ *     codes clamped to [-127, 127], and bsums[k] = sum of codes 16k..16k+15
+ *     ([candle] block table; the pages do not print the rule, this is the
+ *     library's stated reading).
+ * x: f32 [n_vec][n_in] (device). xq: n_vec * qtype_nbytes(act_type, n_in)
+ * bytes of byte-exact GGUF blocks (device). n_vec may be any positive count
+ * here. */
+int quantize_act(int act_type, const float *x, void *xq, int64_t n_in, int64_t n_vec,
+                 qg_stream_t stream);
+
+/* Weight quantization with ggml's reference rules, the bytes llama.cpp
+ * writes ([lesson21] Examples 2 and 5):
+ *   QG_Q8_0: as quantize_act(QG_Q8_0).
+ *   QG_Q4_0: per 32 elements the first element of strictly largest |x| gives
+ *     max, d = max / -8, id = 1/d (0 if d == 0), code = min(15, (int)(x*id +
+ *     8.5f)) with the multiply and add rounded separately; byte j holds
+ *     element j in its low nibble and element j+16 in its high nibble.
+ * x: f32 [n_rows][n_in]; out: n_rows * qtype_nbytes(type, n_in) bytes. */
+int quantize_rows(int type, const float *x, void *out, int64_t n_rows, int64_t n_in,
+                  qg_stream_t stream);
+
+/* ---- Dequantization ------------------------------------------------------ */
+
+/* Every element of n_rows rows to f32 ([sipllm] Per-format dequant; [candle]
+ * block table; [rml] Unpacking the packed fields):
+ *   Q8_0: q * d           Q4_0: (code - 8) * d
+ *   Q4_K: (d * sc_j) * q - dmin * m_j, j = e / 32, 6-bit sc/m unpacked as in
+ *         [rml]'s element-200 trace
+ *   Q6_K: (d * sc_j) * (q - 32), j = e / 16, q = 4 low bits from ql and 2
+ *         high bits from qh (element mapping: the library's stated reading)
+ *   Q8_K: q * d
+ * Every product is exact in f32, so results are unique (only Q4_K's
+ * subtraction rounds, to nearest even). W: n_rows * qtype_nbytes(type, n_in)
+ * bytes; out: f32 [n_rows][n_in]. */
+int dequantize_rows(int type, const void *W, float *out, int64_t n_rows, int64_t n_in,
+                    qg_stream_t stream);
+
+/* ---- Matrix-vector product ----------------------------------------------- */
+
+/* Bytes of workspace qgemv needs: the quantized activations,
+ * n_vec * qtype_nbytes(qtype_act_type(type), n_in). 0 on a bad argument. */
+size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec);
+
+/* y = W . x ([sipllm] The fused matmul; [rml] Quantized dot products;
+ * [lesson21] Examples 10-11): quantizes x once into `workspace` with
+ * quantize_act's rule for the paired activation type, then for every row
+ * and block forms the exact int32 block sum and adds
+ *   Q8_0, Q4_0, Q6_K: S * (d_w * d_x)
+ *   Q4_K:             d_x * (d_w * S_q - dmin_w * S_m)
+ * in f32. The f32 order of these few float operations is not fixed by the
+ * pages; results agree with an f64 accumulation to about 1e-5 relative.
+ * workspace: device buffer of at least qgemv_workspace_bytes(type, n_in,
+ * n_vec) bytes (workspace_bytes gives its size). Limits: n_out <=
+ * 2^31 - 1; n_vec * n_in must be small enough for the activations of one
+ * call to fit in one SM's shared memory next to two weight stages
+ * (QG_ERR_SHAPE otherwise; every shape with n_vec * n_in <= 65536 fits). */
+int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in,
+          int64_t n_vec, void *workspace, size_t workspace_bytes, qg_stream_t stream);
+
+/* The product on activations already quantized by quantize_act (byte-exact
+ * blocks of the paired type, [rml] VecDot takes quantized activations).
+ * Same limits and float step as qgemv. */
+int qgemv_xq(int type, const void *W, const void *xq, float *y, int64_t n_out, int64_t n_in,
+             int64_t n_vec, qg_stream_t stream);
+
+/* Diagnostic: the exact per-block int32 sums that qgemv_xq forms, written to
+ * isums[((v * n_out + o) * nb + b) * k + t], nb = n_in / block elements,
+ * k = 2 for Q4_K (t = 0: S_q = sum_j sc_j sum_{i in j} q_i a_i, t = 1:
+ * S_m = sum_j m_j (bsum_2j + bsum_2j+1)) and k = 1 otherwise (Q8_0:
+ * sum qw qx; Q4_0: sum (code - 8) qx; Q6_K: sum_j sc_j sum_{i in j}
+ * (q_i - 32) a_i) ([rml] Quantized dot products, Kernels and references).
+ * Runs the same device code as qgemv_xq. */
+int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, int64_t n_out,
+                      int64_t n_in, int64_t n_vec, qg_stream_t stream);
+
+/* ---- Device-side status -------------------------------------------------- */
+
+/* Every wait inside the kernels is bounded (about one second). A wait that
+ * runs out records a nonzero code in a device word and the kernel returns
+ * early. This call synchronizes the current device, writes the word to
+ * *code (host pointer), clears it and returns QG_OK (or QG_ERR_CUDA). */
+int qg_device_error(int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_QGEMV_H */

@@ -1,0 +1,355 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle.
+
+Bit-exact: activation blocks, weight blocks, dequantized f32 values and the
+per-block int32 sums. Tolerance on y (the float step per block is not fixed
+by the pages): |y - y_oracle| <= 1e-5 |y_oracle| + 1e-6 ||x_v|| ||w_o||, with
+y_oracle accumulated in f64 and w_o the dequantized row.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import ggml_block_quantized_gb300 as qg  # noqa: E402
+import oracle  # noqa: E402
+from ggml_block_quantized_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-5, 1e-6
+WTYPES = [qg.Q8_0, qg.Q4_0, qg.Q4_K, qg.Q6_K]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    assert qg.device_error() == 0
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def weights(t, n_out, n_in, rng):
+    """Host weight blocks: Q8_0/Q4_0 from the oracle's quantizer, K types random."""
+    if t in (qg.Q8_0, qg.Q4_0):
+        return oracle.quantize(t, synth.f32_normal(rng, n_out * n_in, 0.02))
+    return synth.k_blocks(t, n_out * n_in // 256, rng)
+
+
+def row_norms(t, W, rows, n_in):
+    rb = oracle.type_nbytes(t, n_in)
+    return np.array([np.linalg.norm(oracle.dequantize(t, W[r * rb:(r + 1) * rb], n_in).astype(np.float64))
+                     for r in rows])
+
+
+def check_y(t, W, x, y_gpu, n_out, n_in, n_vec, rows=None):
+    """y_gpu [n_vec, n_out] against the oracle on `rows` (all rows if None)."""
+    at = oracle.act_type(t)
+    xq = oracle.quantize(at, x)
+    rows = list(range(n_out)) if rows is None else sorted(set(rows))
+    y_ref = np.zeros((n_vec, n_out))
+    if len(rows) == n_out:
+        y_ref = oracle.gemv(t, W, xq, n_out, n_in, n_vec)
+    else:
+        for r in rows:
+            oracle.gemv(t, W, xq, n_out, n_in, n_vec, rows=(r, r + 1), out=y_ref)
+    wn = row_norms(t, W, rows, n_in)
+    xn = np.linalg.norm(x.reshape(n_vec, n_in).astype(np.float64), axis=1)
+    got = y_gpu[:, rows].astype(np.float64)
+    ref = y_ref[:, rows]
+    tol = REL * np.abs(ref) + ABS * xn[:, None] * wn[None, :]
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), (f"type {t}: {bad.sum()} of {bad.size} outside tolerance; worst "
+                           f"{np.max(np.abs(got - ref) / np.maximum(tol, 1e-30)):.3g} x tol")
+
+
+def sample_rows(n_out, rng, k=48):
+    base = [0, 1, n_out // 2, n_out - 2, n_out - 1]
+    return [r for r in base if 0 <= r < n_out] + list(rng.choice(n_out, size=min(k, n_out), replace=False))
+
+
+# ----------------------------------------------------------- quantizers
+SPECIAL = {
+    "zeros": lambda n: np.zeros(n, np.float32),
+    "neg_zero": lambda n: np.full(n, -0.0, np.float32),
+    "ties": lambda n: np.tile(np.concatenate([[127.0], np.arange(31) - 15 + 0.5]).astype(np.float32), n // 32),
+    "tiny": lambda n: (np.float32(3e-6) * np.arange(n, dtype=np.float32) / np.float32(31)),
+    "subnormal_d": lambda n: (np.float32(8e-6) * (np.arange(n) % 32).astype(np.float32) / np.float32(31)),
+    "huge": lambda n: (np.float32(9e6) * (np.arange(n) % 32).astype(np.float32) / np.float32(31)),
+    "equal_magnitudes": lambda n: np.tile(np.array([1.0, -1.0] * 16, np.float32), n // 32),
+}
+
+
+@pytest.mark.parametrize("at", [qg.Q8_0, qg.Q8_K])
+def test_quantize_act_bit_exact(at):
+    rng = np.random.default_rng(100 + at)
+    for n_in, n_vec in ((256, 1), (512, 3), (4096, 8), (11008, 2), (256 * 40, 5)):
+        x = synth.f32_normal(rng, n_in * n_vec) * np.float32(rng.uniform(0.01, 100))
+        got = host(qg.quantize_act(at, dev(x), n_vec))
+        assert np.array_equal(got, oracle.quantize(at, x)), (n_in, n_vec)
+    for name, fn in SPECIAL.items():
+        x = fn(512)
+        assert np.array_equal(host(qg.quantize_act(at, dev(x), 1)), oracle.quantize(at, x)), name
+    # NaN and inf elements (candle's special-value rows): NaN -> code 0, inf -> inf scale
+    for bad in (np.nan, np.inf, -np.inf):
+        x = synth.f32_normal(rng, 512)
+        x[[3, 300]] = bad
+        assert np.array_equal(host(qg.quantize_act(at, dev(x), 1)), oracle.quantize(at, x)), bad
+
+
+@pytest.mark.parametrize("t", [qg.Q8_0, qg.Q4_0])
+def test_quantize_rows_bit_exact(t):
+    rng = np.random.default_rng(200 + t)
+    # the lesson's fixed block with the 9.5 outlier, then random rows at the
+    # 4096 x 4096 workload size, then blocks with repeated extreme magnitudes
+    i = np.arange(64)
+    x = (((i * 7919) % 1001) - 500).astype(np.float32) / np.float32(337)
+    x[40] = np.float32(9.5)
+    assert np.array_equal(host(qg.quantize_rows(t, dev(x), 1)), oracle.quantize(t, x))
+    w = synth.single_matrix("q4_0_4096")["w_f32"]
+    assert np.array_equal(host(qg.quantize_rows(t, dev(w), 4096)), oracle.quantize(t, w))
+    for name, fn in SPECIAL.items():
+        x = fn(1024)
+        assert np.array_equal(host(qg.quantize_rows(t, dev(x), 4)), oracle.quantize(t, x)), name
+    # many exact halves: x * id + 8.5 lands on integers for a power-of-two max
+    x = (rng.integers(-16, 16, 32 * 64) / 2.0).astype(np.float32)
+    x[::32] = -8.0
+    assert np.array_equal(host(qg.quantize_rows(t, dev(x), 64)), oracle.quantize(t, x))
+
+
+# ------------------------------------------------------------- dequantize
+@pytest.mark.parametrize("t", [qg.Q8_0, qg.Q4_0, qg.Q4_K, qg.Q6_K, qg.Q8_K])
+def test_dequantize_bit_exact(t):
+    rng = np.random.default_rng(300 + t)
+    elems, nbytes = oracle.type_info(t)
+    for n_rows, n_in in ((1, elems), (3, 5 * elems), (37, 4096), (129, 11008 if elems == 256 else 1024)):
+        if t in (qg.Q4_K, qg.Q6_K):
+            W = synth.k_blocks(t, n_rows * n_in // 256, rng)
+        else:
+            W = synth.random_bytes(rng, n_rows * n_in // elems * nbytes).reshape(-1, nbytes)
+            if t == qg.Q8_K:
+                W[:, 0:4] = np.abs(rng.standard_normal((W.shape[0], 1))).astype(np.float32).view(np.uint8)
+            else:
+                W[:, 0:2] = rng.standard_normal((W.shape[0], 1)).astype(np.float16).view(np.uint8)
+            W = W.reshape(-1)
+        got = host(qg.dequantize_rows(t, dev(W), n_rows, n_in))
+        want = oracle.dequantize(t, W, n_rows * n_in).reshape(n_rows, n_in)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (n_rows, n_in)
+
+
+def test_dequantize_q4_k_workload_size():
+    m = synth.single_matrix("q4_k_4096")
+    got = host(qg.dequantize_rows(qg.Q4_K, dev(m["w_blocks"]), 4096, 4096))
+    want = oracle.dequantize(qg.Q4_K, m["w_blocks"], 4096 * 4096).reshape(4096, 4096)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+# ------------------------------------------------------- exact block sums
+SHAPES = {  # (n_out, n_in): one block; ragged rows; several stages and ring wrap-around
+    qg.Q8_0: [(1, 32), (37, 96), (300, 1024), (5000, 4096)],
+    qg.Q4_0: [(1, 32), (37, 96), (300, 1024), (5000, 4096)],
+    qg.Q4_K: [(1, 256), (37, 768), (300, 11008), (5000, 4096)],
+    qg.Q6_K: [(1, 256), (37, 768), (300, 11008), (3000, 4096)],
+}
+
+
+@pytest.mark.parametrize("t", WTYPES)
+def test_block_isums_bit_exact(t):
+    rng = np.random.default_rng(400 + t)
+    at = oracle.act_type(t)
+    for n_out, n_in in SHAPES[t]:
+        W = weights(t, n_out, n_in, rng)
+        Wd = dev(W)
+        for n_vec in ((1, 2, 5, 8) if n_out * n_in <= 300 * 11008 else (1, 8)):
+            x = synth.f32_normal(rng, n_vec * n_in)
+            xq = oracle.quantize(at, x)
+            got = host(qg.qgemv_block_isums(t, Wd, dev(xq), n_out, n_in, n_vec))
+            want = oracle.block_isums(t, W, xq, n_out, n_in, n_vec)
+            assert np.array_equal(got, want), (n_out, n_in, n_vec)
+
+
+def test_block_isums_at_extreme_codes():
+    # Q6_K scales at -128 and every q = 0 (-32) against activations of -127:
+    # the largest magnitudes the int32 sums see
+    rng = np.random.default_rng(5)
+    n_out, n_in = 9, 512
+    W = synth.k_blocks(qg.Q6_K, n_out * 2, rng).reshape(-1, 210)
+    W[:, :192] = 0
+    W[:, 192:208] = np.uint8(0x80)
+    W = W.reshape(-1)
+    x = np.full(n_in, -1.0, np.float32)
+    xq = oracle.quantize(qg.Q8_K, x)
+    got = host(qg.qgemv_block_isums(qg.Q6_K, dev(W), dev(xq), n_out, n_in, 1))
+    assert np.array_equal(got, oracle.block_isums(qg.Q6_K, W, xq, n_out, n_in, 1))
+    assert got[0, 0, 0, 0] == 16 * (-128) * 16 * (-32) * (-127)
+    # Q4_K with every scale/min byte 0xFF and every nibble 15
+    W = synth.k_blocks(qg.Q4_K, n_out * 2, rng).reshape(-1, 144)
+    W[:, 4:] = 0xFF
+    W = W.reshape(-1)
+    xq = oracle.quantize(qg.Q8_K, np.full(n_in, 1.0, np.float32))
+    got = host(qg.qgemv_block_isums(qg.Q4_K, dev(W), dev(xq), n_out, n_in, 1))
+    assert np.array_equal(got, oracle.block_isums(qg.Q4_K, W, xq, n_out, n_in, 1))
+
+
+# ------------------------------------------------------------ y tolerance
+@pytest.mark.parametrize("t", WTYPES)
+def test_qgemv_small_shapes_all_rows(t):
+    rng = np.random.default_rng(500 + t)
+    for n_out, n_in in SHAPES[t][:3]:
+        W = weights(t, n_out, n_in, rng)
+        for n_vec in (1, 3, 8):
+            x = synth.f32_normal(rng, n_vec * n_in)
+            y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
+            check_y(t, W, x, y, n_out, n_in, n_vec)
+
+
+@pytest.mark.parametrize("name", ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000"])
+@pytest.mark.parametrize("n_vec", [1, 8])
+def test_qgemv_workloads_full_size(name, n_vec):
+    m = synth.single_matrix(name, n_vec=n_vec)
+    t, n_out, n_in = m["type"], m["n_out"], m["n_in"]
+    rng = np.random.default_rng(600)
+    if "w_f32" in m:
+        Wd = qg.quantize_rows(t, dev(m["w_f32"]), n_out)
+        W = oracle.quantize(t, m["w_f32"])
+        assert np.array_equal(host(Wd), W)
+    else:
+        W = m["w_blocks"]
+        Wd = dev(W)
+    y = host(qg.qgemv(t, Wd, dev(m["x"]), n_out, n_in, n_vec))
+    rows = None if n_out * n_in * n_vec <= 4096 * 4096 else sample_rows(n_out, rng, 96)
+    check_y(t, W, m["x"], y, n_out, n_in, n_vec, rows)
+
+
+@pytest.mark.parametrize("m", range(len(synth.LAYER_MATRICES)))
+@pytest.mark.parametrize("n_vec", [1, 8])
+def test_qgemv_layer_stack_matrices(m, n_vec):
+    mat = synth.layer_matrix(0, m, n_vec)
+    t, n_out, n_in = mat["type"], mat["n_out"], mat["n_in"]
+    y = host(qg.qgemv(t, dev(mat["w_blocks"]), dev(mat["x"]), n_out, n_in, n_vec))
+    check_y(t, mat["w_blocks"], mat["x"], y, n_out, n_in, n_vec,
+            sample_rows(n_out, np.random.default_rng(m), 64))
+
+
+def test_qgemv_xq_equals_qgemv():
+    rng = np.random.default_rng(8)
+    for t in WTYPES:
+        n_out, n_in = 333, 1024
+        W = dev(weights(t, n_out, n_in, rng))
+        x = dev(synth.f32_normal(rng, 2 * n_in))
+        y1 = qg.qgemv(t, W, x, n_out, n_in, 2)
+        y2 = qg.qgemv_xq(t, W, qg.quantize_act(oracle.act_type(t), x, 2), n_out, n_in, 2)
+        assert torch.equal(y1, y2)
+
+
+# ---------------------------------------------------------------- edges
+def test_edges_empty_and_tails():
+    rng = np.random.default_rng(9)
+    # n_in = 0: the empty sum
+    y = torch.full((2, 5), 7.0, device="cuda")
+    qg.qgemv(qg.Q4_K, torch.zeros(16, dtype=torch.uint8, device="cuda"),
+             torch.zeros(16, dtype=torch.float32, device="cuda"), 5, 0, 2, y=y)
+    assert host(y).tolist() == [[0.0] * 5] * 2
+    # n_out = 0: nothing to do
+    qg.qgemv(qg.Q4_K, torch.zeros(16, dtype=torch.uint8, device="cuda"),
+             dev(synth.f32_normal(rng, 256)), 0, 256, 1, y=torch.zeros(4, device="cuda"))
+    # W byte lengths that end inside a 16-byte chunk (34, 630, 18*3 bytes)
+    for t, n_out, n_in in ((qg.Q8_0, 1, 32), (qg.Q6_K, 3, 256), (qg.Q4_0, 3, 32), (qg.Q6_K, 7, 2304)):
+        W = weights(t, n_out, n_in, rng)
+        assert W.size % 16 != 0
+        for n_vec in (1, 4):
+            x = synth.f32_normal(rng, n_vec * n_in)
+            y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
+            check_y(t, W, x, y, n_out, n_in, n_vec)
+
+
+def test_shape_limit_is_reported_not_launched():
+    # activations of 8 vectors x 65536 Q8_0 values cannot sit in one SM's shared memory
+    W = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(8 * 65536 * 2, dtype=torch.float32, device="cuda")
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv(qg.Q8_0, W, x, 1, 65536 * 2, 8)
+    assert e.value.status == -2
+
+
+# ----------------------------------------------- ordering, chaining, graphs
+def test_chained_calls_keep_stream_order():
+    """y of one call is x of the next; with programmatic dependent launch the
+    next call may start early, so compare with calls separated by syncs."""
+    rng = np.random.default_rng(10)
+    n = 4096
+    Ws = [dev(synth.k_blocks(qg.Q4_K, n * n // 256, rng)) for _ in range(6)]
+    x0 = dev(synth.f32_normal(rng, n))
+
+    def run(sync):
+        x = x0
+        ys = []
+        for W in Ws:
+            y = qg.qgemv(qg.Q4_K, W, x, n, n, 1)
+            y = y / (y.abs().max() + 1e-30)  # keep values O(1); an ordinary kernel in between
+            if sync:
+                torch.cuda.synchronize()
+            ys.append(y)
+            x = y.reshape(-1)
+        return torch.stack(ys)
+
+    a = run(False)
+    b = run(True)
+    assert torch.equal(a, b)
+
+    # back-to-back qgemv calls with nothing in between (x fixed, y reused as
+    # the next x without a separate kernel)
+    def run2(sync):
+        x = x0
+        outs = []
+        for W in Ws:
+            y = qg.qgemv(qg.Q4_K, W, x, n, n, 1)
+            if sync:
+                torch.cuda.synchronize()
+            outs.append(y)
+            x = y.reshape(-1)
+        return torch.stack(outs)
+
+    assert torch.equal(run2(False), run2(True))
+
+
+def test_graph_capture_replay_matches_eager():
+    rng = np.random.default_rng(11)
+    mats = [synth.layer_matrix(1, m, 1) for m in range(len(synth.LAYER_MATRICES))]
+    Ws = [dev(m["w_blocks"]) for m in mats]
+    xs = [dev(m["x"]) for m in mats]
+    ys = [torch.empty(m["n_out"], device="cuda") for m in mats]
+    wss = [torch.empty(qg.qgemv_workspace_bytes(m["type"], m["n_in"], 1), dtype=torch.uint8, device="cuda")
+           for m in mats]
+    s = torch.cuda.Stream()
+
+    def step():
+        for m, W, x, y, ws in zip(mats, Ws, xs, ys, wss):
+            qg.qgemv(m["type"], W, x, m["n_out"], m["n_in"], 1, y=y, workspace=ws, stream=s)
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    eager = [y.clone() for y in ys]
+    for y in ys:
+        y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, ys):
+        assert torch.equal(a, b)
+    del rng

@@ -1,0 +1,133 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/qgemv.h declares, and rejects bad arguments with status codes before
+it touches CUDA. No compute call runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ggml_block_quantized_gb300 as qg
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemv.h")
+
+OK, ERR_TYPE, ERR_SHAPE, ERR_ALIGN, ERR_NULL, ERR_PAIR, ERR_CUDA, ERR_WS = 0, -1, -2, -3, -4, -5, -6, -7
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    return qg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declarations_are_exported(L):
+    names = declared_functions()
+    assert len(names) == 13
+    assert sorted(qg.EXPORTED_SYMBOLS) == names
+    for n in names:
+        assert hasattr(L, n), n
+    # they are real dynamic symbols of the library
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", qg.library_path()], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+
+
+def test_type_table_matches_the_oracle(L):
+    for t in (qg.F32, qg.F16, qg.Q4_0, qg.Q8_0, qg.Q4_K, qg.Q6_K, qg.Q8_K):
+        assert qg.qtype_block(t) == oracle.type_info(t)
+        for n in (0, 256, 4096, 11008, 32 * 7, 100):
+            assert qg.qtype_nbytes(t, n) == oracle.type_nbytes(t, n)
+    with pytest.raises(qg.QGError):
+        qg.qtype_block(3)
+    assert qg.qtype_nbytes(99, 256) == -1
+    assert qg.qtype_nbytes(qg.Q8_0, -32) == -1
+
+
+def test_pairing(L):
+    assert qg.qtype_act_type(qg.Q4_0) == qg.Q8_0
+    assert qg.qtype_act_type(qg.Q8_0) == qg.Q8_0
+    assert qg.qtype_act_type(qg.Q4_K) == qg.Q8_K
+    assert qg.qtype_act_type(qg.Q6_K) == qg.Q8_K
+    for t in (qg.F32, qg.F16, qg.Q8_K, 7, 99):
+        assert qg.qtype_act_type(t) == ERR_PAIR
+
+
+def test_workspace_bytes(L):
+    assert qg.qgemv_workspace_bytes(qg.Q4_K, 4096, 1) == 16 * 292
+    assert qg.qgemv_workspace_bytes(qg.Q6_K, 11008, 8) == 8 * 43 * 292
+    assert qg.qgemv_workspace_bytes(qg.Q4_0, 4096, 2) == 2 * 128 * 34
+    assert qg.qgemv_workspace_bytes(qg.Q4_0, 100, 1) == 0
+    assert qg.qgemv_workspace_bytes(qg.Q4_0, 4096, 9) == 0
+    assert qg.qgemv_workspace_bytes(qg.Q8_K, 4096, 1) == 0
+
+
+def test_status_strings(L):
+    for s in range(-8, 1):
+        assert L.qg_status_string(s)
+
+
+# fake device addresses: validation must reject before any CUDA call
+A = ctypes.c_void_p(0x10000)
+A2 = ctypes.c_void_p(0x20000)
+A3 = ctypes.c_void_p(0x30000)
+MIS = ctypes.c_void_p(0x10008)
+NUL = None
+
+
+def test_qgemv_validation(L):
+    ws = ctypes.c_size_t(1 << 20)
+    g = lambda *a: L.qgemv(*a)
+    assert g(99, A, A2, A3, 16, 256, 1, A, ws, NUL) == ERR_TYPE
+    assert g(qg.Q8_K, A, A2, A3, 16, 256, 1, A, ws, NUL) == ERR_PAIR
+    assert g(qg.F32, A, A2, A3, 16, 256, 1, A, ws, NUL) == ERR_PAIR
+    assert g(qg.Q4_K, A, A2, A3, 16, 250, 1, A, ws, NUL) == ERR_SHAPE
+    assert g(qg.Q4_0, A, A2, A3, 16, 100, 1, A, ws, NUL) == ERR_SHAPE  # a row of 100 is rejected
+    assert g(qg.Q4_K, A, A2, A3, 16, 256, 0, A, ws, NUL) == ERR_SHAPE
+    assert g(qg.Q4_K, A, A2, A3, 16, 256, 9, A, ws, NUL) == ERR_SHAPE
+    assert g(qg.Q4_K, A, A2, A3, -1, 256, 1, A, ws, NUL) == ERR_SHAPE
+    assert g(qg.Q4_K, NUL, A2, A3, 16, 256, 1, A, ws, NUL) == ERR_NULL
+    assert g(qg.Q4_K, A, NUL, A3, 16, 256, 1, A, ws, NUL) == ERR_NULL
+    assert g(qg.Q4_K, A, A2, NUL, 16, 256, 1, A, ws, NUL) == ERR_NULL
+    assert g(qg.Q4_K, MIS, A2, A3, 16, 256, 1, A, ws, NUL) == ERR_ALIGN
+    assert g(qg.Q4_K, A, MIS, A3, 16, 256, 1, A, ws, NUL) == ERR_ALIGN
+    assert g(qg.Q4_K, A, A2, MIS, 16, 256, 1, A, ws, NUL) == ERR_ALIGN
+    assert g(qg.Q4_K, A, A2, A3, 16, 256, 1, NUL, ws, NUL) == ERR_WS
+    assert g(qg.Q4_K, A, A2, A3, 16, 256, 1, A, ctypes.c_size_t(291), NUL) == ERR_WS
+    assert g(qg.Q4_K, A, A2, A3, 16, 256, 1, MIS, ws, NUL) == ERR_ALIGN
+    # empty output: nothing to do, nothing enqueued
+    assert g(qg.Q4_K, A, A2, A3, 0, 256, 1, A, ws, NUL) == OK
+
+
+def test_other_entry_points_validate(L):
+    assert L.quantize_act(qg.Q4_0, A, A2, 256, 1, NUL) == ERR_TYPE
+    assert L.quantize_act(qg.Q8_K, A, A2, 100, 1, NUL) == ERR_SHAPE
+    assert L.quantize_act(qg.Q8_0, NUL, A2, 64, 1, NUL) == ERR_NULL
+    assert L.quantize_act(qg.Q8_0, MIS, A2, 64, 1, NUL) == ERR_ALIGN
+    assert L.quantize_act(qg.Q8_0, A, A2, 0, 1, NUL) == OK
+    assert L.quantize_rows(qg.Q4_K, A, A2, 1, 256, NUL) == ERR_TYPE
+    assert L.quantize_rows(qg.Q4_0, A, A2, 1, 33, NUL) == ERR_SHAPE
+    assert L.dequantize_rows(qg.F32, A, A2, 1, 256, NUL) == ERR_TYPE
+    assert L.dequantize_rows(qg.Q6_K, A, A2, 1, 255, NUL) == ERR_SHAPE
+    assert L.dequantize_rows(qg.Q6_K, A, MIS, 1, 256, NUL) == ERR_ALIGN
+    assert L.qgemv_xq(qg.Q6_K, A, NUL, A3, 4, 256, 1, NUL) == ERR_NULL
+    assert L.qgemv_block_isums(qg.Q6_K, A, A2, NUL, 4, 256, 1, NUL) == ERR_NULL
+    assert L.qgemv_block_isums(qg.Q4_0, A, A2, A3, 4, 256, 0, NUL) == ERR_SHAPE
+    assert L.qg_device_error(None) == ERR_NULL
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    monkeypatch.setattr(qg, "_lib", None)
+    monkeypatch.setattr(qg, "library_path", lambda: "/nonexistent/libqgemv.so")
+    with pytest.raises(ImportError):
+        qg.lib()
