@@ -24,9 +24,9 @@ namespace {
 
 thread_local char g_last_cuda_error[256] = "";
 
-int cuda_fail(cudaError_t e) {
-    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s", cudaGetErrorName(e),
-                  cudaGetErrorString(e));
+int cuda_fail(cudaError_t e, const char *where = "") {
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%s)", cudaGetErrorName(e),
+                  cudaGetErrorString(e), where);
     return QG_ERR_CUDA;
 }
 
@@ -48,29 +48,39 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DeviceInfo {
     int device;
     int sms;
-    int32_t *err;  // device address of g_device_error on this device
+    int smem_optin;  // opt-in dynamic shared memory per CTA (bytes)
+    int32_t *err;    // device address of g_device_error on this device
 };
 
 int current_device(DeviceInfo *info) {
     static int sm_count[64] = {0};
+    static int optin[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     int sms = (dev >= 0 && dev < 64) ? __atomic_load_n(&sm_count[dev], __ATOMIC_RELAXED) : 0;
-    if (sms == 0) {
+    int smem = (dev >= 0 && dev < 64) ? __atomic_load_n(&optin[dev], __ATOMIC_RELAXED) : 0;
+    if (sms == 0 || smem == 0) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return cuda_fail(e);
-        if (dev >= 0 && dev < 64) __atomic_store_n(&sm_count[dev], sms, __ATOMIC_RELAXED);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
+        e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
+        if (smem > kSmemLimit) smem = kSmemLimit;
+        if (dev >= 0 && dev < 64) {
+            __atomic_store_n(&sm_count[dev], sms, __ATOMIC_RELAXED);
+            __atomic_store_n(&optin[dev], smem, __ATOMIC_RELAXED);
+        }
     }
     static int32_t *err_addr[64] = {nullptr};
     int32_t *err = (dev >= 0 && dev < 64) ? __atomic_load_n(&err_addr[dev], __ATOMIC_ACQUIRE) : nullptr;
     if (!err) {
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&err), g_device_error);
-        if (e != cudaSuccess) return cuda_fail(e);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_device_error)");
         if (dev >= 0 && dev < 64) __atomic_store_n(&err_addr[dev], err, __ATOMIC_RELEASE);
     }
     info->device = dev;
     info->sms = sms;
+    info->smem_optin = smem;
     info->err = err;
     return QG_OK;
 }
@@ -108,7 +118,8 @@ size_t round16(size_t v) { return (v + 15) & ~size_t(15); }
 constexpr int kSmemTailPad = 16;  // unaligned word reads may touch up to 4 bytes past a stage
 
 // Stage geometry and grid of one GEMV launch. Returns QG_OK or QG_ERR_SHAPE.
-int plan_gemv(int type, int64_t n_out, int64_t n_in, int nv, int sms, GemvParams *p, GemvLaunch *l) {
+int plan_gemv(int type, int64_t n_out, int64_t n_in, int nv, int sms, int smem_limit, GemvParams *p,
+              GemvLaunch *l) {
     int elems, bytes;
     block_info(type, &elems, &bytes);
     const int64_t nb = n_in / elems;
@@ -120,10 +131,10 @@ int plan_gemv(int type, int64_t n_out, int64_t n_in, int nv, int sms, GemvParams
         const size_t stage = round16(static_cast<size_t>(R) * row_bytes + 15);
         if (split < kConsumerWarps && stage > 20480) continue;  // prefer stages of <= 20 KiB
         const size_t fixed = kHeaderBytes + act + kSmemTailPad;
-        if (fixed + 2 * stage > static_cast<size_t>(kSmemLimit)) continue;
+        if (fixed + 2 * stage > static_cast<size_t>(smem_limit)) continue;
         int S = static_cast<int>(ring_target / stage);
         S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
-        while (S > 2 && fixed + S * stage > static_cast<size_t>(kSmemLimit)) --S;
+        while (S > 2 && fixed + S * stage > static_cast<size_t>(smem_limit)) --S;
         const size_t smem = fixed + S * stage;
         p->row_bytes = row_bytes;
         p->w_total = row_bytes * n_out;
@@ -141,6 +152,7 @@ int plan_gemv(int type, int64_t n_out, int64_t n_in, int nv, int sms, GemvParams
         const int64_t cap = static_cast<int64_t>(sms) * per_sm;
         l->grid = static_cast<int>(tiles < cap ? tiles : cap);
         l->smem = static_cast<int>(smem);
+        l->smem_optin = smem_limit;
         return QG_OK;
     }
     return QG_ERR_SHAPE;
@@ -189,7 +201,7 @@ int launch_quantize(int act_type, const float *x, void *xq, int64_t n_blocks, in
     else
         e = launch_pdl(quantize_q4_0_kernel, static_cast<int>(grid), 32 * warps_per_cta, 0, s, x,
                        static_cast<uint8_t *>(xq), n_blocks);
-    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, "quantize launch");
 }
 
 // The product on quantized activations xq (shared by qgemv, qgemv_xq and
@@ -198,7 +210,7 @@ int run_gemv(int type, const void *W, const void *xq, float *y, int32_t *isums, 
              int64_t n_vec, const DeviceInfo &dev, cudaStream_t s) {
     GemvParams p = {};
     GemvLaunch l = {};
-    int st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, &p, &l);
+    int st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &p, &l);
     if (st != QG_OK) return st;
     p.W = static_cast<const uint8_t *>(W);
     p.xq = static_cast<const uint8_t *>(xq);
@@ -206,7 +218,13 @@ int run_gemv(int type, const void *W, const void *xq, float *y, int32_t *isums, 
     p.isums = isums;
     p.err = dev.err;
     cudaError_t e = launch_gemv(type, p, static_cast<int>(n_vec), isums != nullptr, l, dev.device, s);
-    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+    if (e != cudaSuccess) {
+        char where[160];
+        std::snprintf(where, sizeof where, "%s; grid %d block %d smem %d stages %d stage_bytes %d", g_launch_step,
+                      l.grid, kGemvThreads, l.smem, p.n_stages, p.stage_bytes);
+        return cuda_fail(e, where);
+    }
+    return QG_OK;
 }
 
 // Validation shared by qgemv_xq and qgemv_block_isums.
@@ -385,7 +403,7 @@ int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     // the product's shape limits are checked before anything is enqueued
     GemvParams probe = {};
     GemvLaunch pl = {};
-    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, &probe, &pl);
+    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
     if (st != QG_OK) return st;
     const int at = qtype_act_type(type);
     int elems, bytes;

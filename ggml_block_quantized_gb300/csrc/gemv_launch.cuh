@@ -14,15 +14,21 @@ namespace qg {
 struct GemvLaunch {
     int grid;
     int smem;
+    int smem_optin;  // the device's opt-in shared-memory limit per CTA
 };
 
-// Shared-memory opt-in, done once per (kernel, device).
-template <class K>
-inline cudaError_t ensure_smem_attr(K kernel, int device) {
+// Which CUDA call of a launch failed (for the error text).
+inline thread_local const char *g_launch_step = "";
+
+// Shared-memory opt-in, done once per (kernel, device). The flag is keyed by
+// the kernel's template arguments (every instance has the same C++ type).
+template <class T, int NV, bool ISUMS, class K>
+inline cudaError_t ensure_smem_attr(K kernel, int device, int bytes) {
     static std::atomic<uint64_t> done{0};
     const uint64_t bit = 1ull << (device & 63);
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    g_launch_step = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
@@ -39,6 +45,7 @@ inline cudaError_t launch_pdl(K kernel, int grid, int block, int smem, cudaStrea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    g_launch_step = "cudaLaunchKernelEx";
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
@@ -47,12 +54,12 @@ inline cudaError_t launch_gemv_nv(const GemvParams &p, bool isums, const GemvLau
                                   cudaStream_t s) {
     if (isums) {
         auto k = gemv_kernel<T, NV, true>;
-        cudaError_t e = ensure_smem_attr(k, device);
+        cudaError_t e = ensure_smem_attr<T, NV, true>(k, device, l.smem_optin);
         if (e != cudaSuccess) return e;
         return launch_pdl(k, l.grid, kGemvThreads, l.smem, s, p);
     }
     auto k = gemv_kernel<T, NV, false>;
-    cudaError_t e = ensure_smem_attr(k, device);
+    cudaError_t e = ensure_smem_attr<T, NV, false>(k, device, l.smem_optin);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, l.grid, kGemvThreads, l.smem, s, p);
 }

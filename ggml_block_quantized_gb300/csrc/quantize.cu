@@ -44,11 +44,8 @@ __global__ void quantize_q8_0_kernel(const float *__restrict__ x, uint8_t *__res
         const int q = code_from_rounded(roundf(__fmul_rn(v, id)), -128, 127);
         uint8_t *blk = out + b * 34;
         blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
-        if (lane == 0) {
-            const unsigned short h = __half_as_ushort(__float2half_rn(d));
-            blk[0] = static_cast<uint8_t>(h & 0xFF);
-            blk[1] = static_cast<uint8_t>(h >> 8);
-        }
+        // the f16 scale as one 16-bit store (blocks start 2-byte aligned)
+        if (lane == 0) *reinterpret_cast<unsigned short *>(blk) = __half_as_ushort(__float2half_rn(d));
     }
 }
 
@@ -126,11 +123,8 @@ __global__ void quantize_q4_0_kernel(const float *__restrict__ x, uint8_t *__res
         const int hi = __shfl_down_sync(0xffffffffu, code, 16);
         uint8_t *blk = out + b * 18;
         if (lane < 16) blk[2 + lane] = static_cast<uint8_t>(code | (hi << 4));
-        if (lane == 0) {
-            const unsigned short h = __half_as_ushort(__float2half_rn(d));
-            blk[0] = static_cast<uint8_t>(h & 0xFF);
-            blk[1] = static_cast<uint8_t>(h >> 8);
-        }
+        // the f16 scale as one 16-bit store (blocks start 2-byte aligned)
+        if (lane == 0) *reinterpret_cast<unsigned short *>(blk) = __half_as_ushort(__float2half_rn(d));
     }
 }
 
