@@ -16,7 +16,7 @@ __all__ = [
     "F32", "F16", "Q4_0", "Q8_0", "Q4_K", "Q6_K", "Q8_K", "MAX_NVEC", "QGError",
     "library_path", "lib", "qtype_nbytes", "qtype_block", "qtype_act_type",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes",
-    "qgemv", "qgemv_xq", "qgemv_block_isums", "device_error", "EXPORTED_SYMBOLS",
+    "qgemv", "qgemv_xq", "qgemv_block_isums", "qgemv_noalloc", "device_error", "EXPORTED_SYMBOLS",
 ]
 
 F32, F16, Q4_0, Q8_0, Q4_K, Q6_K, Q8_K = 0, 1, 2, 8, 12, 14, 15
@@ -28,7 +28,7 @@ TYPE_NAMES = {F32: "F32", F16: "F16", Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", 
 EXPORTED_SYMBOLS = (
     "qtype_nbytes", "qtype_block", "qtype_act_type", "qg_status_string", "qg_last_cuda_error",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes", "qgemv",
-    "qgemv_xq", "qgemv_block_isums", "qg_device_error",
+    "qgemv_xq", "qgemv_block_isums", "qg_device_error", "qgemv_noalloc",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -72,6 +72,7 @@ def lib():
         L.qgemv_xq.argtypes, L.qgemv_xq.restype = [i32, vp, vp, vp, i64, i64, i64, vp], i32
         L.qgemv_block_isums.argtypes, L.qgemv_block_isums.restype = [i32, vp, vp, vp, i64, i64, i64, vp], i32
         L.qg_device_error.argtypes, L.qg_device_error.restype = [ctypes.POINTER(ctypes.c_int32)], i32
+        L.qgemv_noalloc.argtypes, L.qgemv_noalloc.restype = [i32, vp, vp, vp, i64, i64, i64, vp], i32
         _lib = L
     return _lib
 
@@ -230,6 +231,25 @@ def qgemv_block_isums(t: int, W, xq, n_out: int, n_in: int, n_vec: int = 1, out=
     _check(lib().qgemv_block_isums(t, _ptr(W), _ptr(xq), _ptr(out), n_out, n_in, n_vec, _stream(stream)),
            "qgemv_block_isums")
     return out
+
+
+def qgemv_noalloc(t: int, W, x, n_out: int, n_in: int, n_vec: int = 1, y=None, stream=None):
+    """qgemv without a workspace: the library keeps the quantized activations
+    in its own fixed device array (256 KiB), for callers that cannot allocate
+    device memory where they run the product. Calls that may overlap on the
+    GPU share that array and must not run concurrently. Pass y to allocate
+    nothing from Python either."""
+    torch = _torch()
+    _dev_tensor(W, torch.uint8, "W")
+    _dev_tensor(x, torch.float32, "x")
+    _need(x, 4 * n_vec * n_in, "x")
+    if y is None:
+        y = torch.empty((n_vec, n_out), dtype=torch.float32, device=x.device)
+    _dev_tensor(y, torch.float32, "y")
+    _need(y, 4 * n_vec * n_out, "y")
+    _check(lib().qgemv_noalloc(t, _ptr(W), _ptr(x), _ptr(y), n_out, n_in, n_vec, _stream(stream)),
+           "qgemv_noalloc")
+    return y
 
 
 def device_error() -> int:

@@ -428,3 +428,76 @@ int qg_device_error(int32_t *code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// qgemv_noalloc: qgemv for callers that cannot hand the library a workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// product: a plugin or custom operator whose host framework owns every device
+// buffer and gives it none; a decode loop that must not call cudaMalloc or
+// cudaFree, because those calls can synchronize the whole device and stall
+// other streams; code being recorded by CUDA stream capture, where
+// allocation calls are not allowed. This entry point keeps the quantized
+// activations in a fixed array in the library's own device memory instead.
+//
+// The array is a file-scope __device__ variable of kNoAllocScratchBytes bytes;
+// every GPU that loads this library holds it until the process exits. In
+// host code its name is only a host-side handle, not a device address, so
+// the first call on each device (with that device current) asks the runtime
+// for the device address with cudaGetSymbolAddress and keeps it; later
+// calls on that device reuse it.
+// ---------------------------------------------------------------------------
+namespace qg {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256 * 1024;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device.
+int noalloc_scratch(int device, void **out) {
+    static void *addr[64] = {nullptr};
+    void *p = (device >= 0 && device < 64) ? __atomic_load_n(&addr[device], __ATOMIC_ACQUIRE) : nullptr;
+    if (!p) {
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_noalloc_scratch)");
+        if (device >= 0 && device < 64) __atomic_store_n(&addr[device], p, __ATOMIC_RELEASE);
+    }
+    *out = p;
+    return QG_OK;
+}
+
+}  // namespace
+}  // namespace qg
+
+extern "C" int qgemv_noalloc(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in,
+                             int64_t n_vec, qg_stream_t stream) {
+    int st = check_gemv_args(type, W, x, y, n_out, n_in, n_vec);
+    if (st != QG_OK) return st;
+    if (n_out == 0) return QG_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_in == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(n_out * n_vec) * sizeof(float), s);
+        return e == cudaSuccess ? QG_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    // the quantized activations must fit in the fixed array
+    if (qgemv_workspace_bytes(type, n_in, n_vec) > kNoAllocScratchBytes) return QG_ERR_WORKSPACE;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != QG_OK) return st;
+    GemvParams probe = {};
+    GemvLaunch pl = {};
+    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
+    if (st != QG_OK) return st;
+    void *scratch = nullptr;
+    st = noalloc_scratch(dev.device, &scratch);
+    if (st != QG_OK) return st;
+    // Every byte the product reads from the array is written by the
+    // quantization launched just before it, so nothing needs clearing.
+    const int at = qtype_act_type(type);
+    int elems, bytes;
+    block_info(at, &elems, &bytes);
+    st = launch_quantize(at, x, scratch, n_in / elems * n_vec, dev.sms, s);
+    if (st != QG_OK) return st;
+    return run_gemv(type, W, scratch, y, nullptr, n_out, n_in, n_vec, dev, s);
+}

@@ -181,6 +181,33 @@ int qgemv_xq(int type, const void *W, const void *xq, float *y, int64_t n_out, i
 int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, int64_t n_out,
                       int64_t n_in, int64_t n_vec, qg_stream_t stream);
 
+/* The product without a workspace, for callers that cannot allocate device
+ * memory where they run it: a plugin whose host framework owns every device
+ * buffer and passes it none, a decode loop that must not call cudaMalloc or
+ * cudaFree (they can synchronize the whole device), or code recorded by CUDA
+ * stream capture, where allocation is not allowed. The reference pages have
+ * no counterpart; this is a property of this library's interface.
+ *
+ * Same arguments, result and limits as qgemv without workspace and
+ * workspace_bytes. The quantized activations go to a fixed array of 256 KiB
+ * (262144 bytes) inside the library's device memory, which every GPU that
+ * loads the library holds until the process exits. Calls whose activations
+ * need more (qgemv_workspace_bytes(type, n_in, n_vec) > 262144) return
+ * QG_ERR_WORKSPACE and enqueue nothing. The call allocates nothing.
+ *
+ * All calls on a device share that array. Calls ordered on one stream are
+ * safe. Calls that may run at the same time on the GPU (different streams,
+ * or different host threads without ordering between them) race on it and
+ * give wrong results. The array keeps the previous call's contents; every
+ * byte a call reads is written earlier in the same call, so nothing needs
+ * clearing.
+ *
+ * The first call on each device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) and keeps it. Make that
+ * first call before any stream capture that includes this function. */
+int qgemv_noalloc(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in,
+                  int64_t n_vec, qg_stream_t stream);
+
 /* ---- Device-side status -------------------------------------------------- */
 
 /* Every wait inside the kernels is bounded (about one second). A wait that
