@@ -204,16 +204,25 @@ int launch_quantize(int act_type, const float *x, void *xq, int64_t n_blocks, in
     return e == cudaSuccess ? QG_OK : cuda_fail(e, "quantize launch");
 }
 
-// The product on quantized activations xq (shared by qgemv, qgemv_xq and
+// Activations of at most this many f32 bytes per call are quantized inside
+// the GEMV's prologue (every CTA reads x once); larger ones go through the
+// separate quantization launch into the workspace.
+constexpr int64_t kFusedQuantMaxBytes = 48 * 1024;
+
+bool fused_quantization(int64_t n_in, int64_t n_vec) { return 4 * n_in * n_vec <= kFusedQuantMaxBytes; }
+
+// The product on quantized activations xq, or on f32 x quantized in the
+// kernel when x is non-null (shared by qgemv, qgemv_xq, qgemv_noalloc and
 // qgemv_block_isums). Arguments are already validated.
 int run_gemv(int type, const void *W, const void *xq, float *y, int32_t *isums, int64_t n_out, int64_t n_in,
-             int64_t n_vec, const DeviceInfo &dev, cudaStream_t s) {
+             int64_t n_vec, const DeviceInfo &dev, cudaStream_t s, const float *x = nullptr) {
     GemvParams p = {};
     GemvLaunch l = {};
     int st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &p, &l);
     if (st != QG_OK) return st;
     p.W = static_cast<const uint8_t *>(W);
     p.xq = static_cast<const uint8_t *>(xq);
+    p.x = x;
     p.y = y;
     p.isums = isums;
     p.err = dev.err;
@@ -405,6 +414,8 @@ int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     GemvLaunch pl = {};
     st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
     if (st != QG_OK) return st;
+    if (fused_quantization(n_in, n_vec))  // one launch: x quantized in the GEMV's prologue
+        return run_gemv(type, W, nullptr, y, nullptr, n_out, n_in, n_vec, dev, s, x);
     const int at = qtype_act_type(type);
     int elems, bytes;
     block_info(at, &elems, &bytes);

@@ -21,7 +21,10 @@
 //    consumers wait for the previous grid before reading the activations.
 //  * Consumers first stage the activations (every vector, the whole row
 //    length) into shared memory in a per-type padded layout that makes the
-//    hot loop's 64/128-bit shared loads bank-conflict free, then for each
+//    hot loop's 128-bit shared loads bank-conflict free -- either copied from
+//    byte-exact Q8_0/Q8_K blocks or, for small activations, quantized from
+//    f32 x right there (the same rule, so the same bytes; it saves a
+//    dependent launch per call) -- then for each
 //    stage take one row per `split` warps. Lanes are grouped per block
 //    (kLanesPerBlock lanes share one block); each group forms the block's
 //    exact int32 sums with __dp4a, combines them with warp shuffles, and the
@@ -42,7 +45,8 @@ constexpr int kHeaderBytes = kRedOffset + 2 * kConsumerWarps * kMaxNvec * 4;
 
 struct GemvParams {
     const uint8_t *W;    // [n_out][row_bytes], 16-byte aligned
-    const uint8_t *xq;   // [n_vec][nb] activation blocks (byte-exact GGUF)
+    const uint8_t *xq;   // [n_vec][nb] activation blocks (byte-exact GGUF), or
+    const float *x;      // f32 activations [n_vec][n_in], quantized in the prologue when non-null
     float *y;            // [n_vec][n_out]
     int32_t *isums;      // [n_vec][n_out][nb][kSums] (diagnostic mode only)
     int32_t *err;        // device error word
@@ -147,7 +151,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
 
     // ---- consumers ----
     pdl_wait_prior_grids();  // activations may come from the previous kernel
-    T::stage_act(p.xq, act, p.nb, NV, threadIdx.x, kConsumerWarps * 32);
+    if (p.x)
+        T::stage_x(p.x, act, p.nb, NV, warp, kConsumerWarps, lane);
+    else
+        T::stage_act(p.xq, act, p.nb, NV, threadIdx.x, kConsumerWarps * 32);
     named_barrier(1, kConsumerWarps * 32);
 
     const int split = p.split;

@@ -1,6 +1,8 @@
 // gemv_types.cuh - per-type policies of the streaming GEMV kernel: how the
-// paired activation blocks are laid out in shared memory, and how a group of
-// lanes forms one weight block's exact int32 sums and float term.
+// paired activation blocks are laid out in shared memory (filled either from
+// byte-exact Q8_0/Q8_K blocks or by quantizing f32 x in the kernel's
+// prologue), and how a group of lanes forms one weight block's exact int32
+// sums and float terms.
 //
 // Block formats ("量化格式" (candle), block structure table; "Building Q8_0
 // and Q4_0 Like ggml", Examples 1 and 5; "Quantization" (rml), Unpacking the
@@ -22,8 +24,16 @@
 //   Q4_0: S = sum c * qx - 8 * sum qx
 //   Q4_K: S_q = sum_j sc_j * sum_{i in j} q_i a_i ; S_m = sum_j m_j (bsum_2j + bsum_2j+1)
 //   Q6_K: S = sum_j sc_j * sum_{i in j} q_i a_i - 32 * sum_j sc_j * bsum_j
-// Float step per block: Q8_0, Q4_0, Q6_K: S * (d_w * d_x); Q4_K:
-// d_x * (d_w * S_q - dmin * S_m).
+// Float step: Q8_0, Q4_0, Q6_K: S * (d_w * d_x); Q4_K: d_x * (d_w * S_q -
+// dmin * S_m). In the product, a block's lanes each apply the float step to
+// their own exact partial sums (no cross-lane sum per block); the
+// diagnostic mode adds the partials across the block's lanes first and
+// writes the whole-block sums.
+//
+// Activation quantization in the prologue follows the rule of quantize.cu
+// exactly (amax over the block, d = amax / 127 with IEEE division, id = 1/d
+// or 0, code = roundf(x * id)), so the codes are the bytes quantize_act
+// writes.
 #pragma once
 
 #include "qg_common.cuh"
@@ -38,6 +48,38 @@ __device__ __forceinline__ int group_sum(int v) {
     return v;
 }
 
+template <int G>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+    for (int m = 1; m < G; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// Codes of 8 values with the inverse scale id, packed 4 per word; returns
+// their sum.
+__device__ __forceinline__ int codes8(const float (&v)[8], float id, int lo, int hi, uint32_t (&w)[2]) {
+    w[0] = w[1] = 0u;
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int q = code_from_rounded(roundf(__fmul_rn(v[i], id)), lo, hi);
+        sum += q;
+        w[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
+    }
+    return sum;
+}
+
+__device__ __forceinline__ uint32_t pack16(int lo, int hi) {
+    return (static_cast<uint32_t>(lo) & 0xFFFFu) | (static_cast<uint32_t>(hi) << 16);
+}
+
 // ========================================================================
 // Q8_0-paired types (Q8_0, Q4_0): activations staged as 48-byte records
 // per (vector, block): qs[32] | f32 d_x | int32 sum(qs) | 8 pad bytes.
@@ -48,7 +90,7 @@ struct ActQ8_0 {
     static constexpr int kRecord = 48;
     static size_t bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * kRecord; }
 
-    // xq: [nv][nb] byte-exact Q8_0 blocks (34 B, 2-byte aligned each).
+    // From byte-exact Q8_0 blocks: xq [nv][nb] x 34 B (2-byte aligned each).
     __device__ static void stage(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         const int n = nb * nv;
         for (int i = tid; i < n; i += nthr) {
@@ -69,6 +111,40 @@ struct ActQ8_0 {
                 make_uint4(__float_as_uint(dx), static_cast<uint32_t>(asum), 0u, 0u);
         }
     }
+
+    // From f32 x [nv][nb * 32]: 4 lanes per 32-value block, 8 blocks per warp step.
+    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
+        const int n = nb * nv;
+        for (int base = warp * 8; base < n; base += nwarps * 8) {
+            const int i = base + (lane >> 2);
+            const int part = lane & 3;
+            const bool ok = i < n;
+            float v[8];
+            if (ok) {
+                load8(x + static_cast<size_t>(i) * 32 + 8 * part, v);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+            }
+            float a = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(v[k]));
+            a = group_max<4>(a);
+            const float d = a / 127.0f;
+            const float id = d != 0.0f ? 1.0f / d : 0.0f;
+            uint32_t w[2];
+            int sum = group_sum<4>(codes8(v, id, -128, 127, w));
+            if (ok) {
+                uint8_t *rec = act + static_cast<size_t>(i) * kRecord;
+                reinterpret_cast<uint2 *>(rec)[part] = make_uint2(w[0], w[1]);
+                if (part == 0) {
+                    const float dx = __half2float(__float2half_rn(d));  // the stored f16 scale
+                    reinterpret_cast<uint4 *>(rec)[2] =
+                        make_uint4(__float_as_uint(dx), static_cast<uint32_t>(sum), 0u, 0u);
+                }
+            }
+        }
+    }
 };
 
 struct TypeQ8_0 {
@@ -76,6 +152,9 @@ struct TypeQ8_0 {
     static size_t act_bytes(int nb, int nv) { return ActQ8_0::bytes(nb, nv); }
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
+    }
+    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
+        ActQ8_0::stage_x(x, act, nb, nv, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
@@ -102,7 +181,7 @@ struct TypeQ8_0 {
             if (ISUMS) {
                 if (active) isum_row[v * isum_vstride + b] = s;
             } else if (active) {
-                acc[v] += static_cast<float>(s) * (dw * dx);
+                acc[v] = fmaf(static_cast<float>(s), dw * dx, acc[v]);
             }
         }
     }
@@ -113,6 +192,9 @@ struct TypeQ4_0 {
     static size_t act_bytes(int nb, int nv) { return ActQ8_0::bytes(nb, nv); }
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
+    }
+    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
+        ActQ8_0::stage_x(x, act, nb, nv, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
@@ -146,144 +228,195 @@ struct TypeQ4_0 {
             if (ISUMS) {
                 if (active) isum_row[v * isum_vstride + b] = s;
             } else if (active) {
-                acc[v] += static_cast<float>(s) * (dw * __uint_as_float(ex.x));
+                acc[v] = fmaf(static_cast<float>(s), dw * __uint_as_float(ex.x), acc[v]);
             }
         }
     }
 };
 
 // ========================================================================
-// Q4_K. Four lanes per block, lane c takes the 64-element chunk c: the 32
-// bytes qs[32c..32c+31] hold sub-block 2c in their low nibbles and 2c+1 in
-// their high nibbles. Activations staged per (vector, block, chunk) as an
-// 80-byte record: a[64] | bsum(2c) | bsum(2c+1) | f32 d_x | pad, where
-// bsum(j) = bsums[2j] + bsums[2j+1] is the sum of sub-block j's 32 codes.
+// Q8_K from f32: one warp per 256-value block, lane l owns values
+// 8l..8l+7. Returns the codes (2 words), the 16-value sum of lanes
+// (2k, 2k+1) in every lane of the pair, and d.
+// ========================================================================
+__device__ __forceinline__ void quantize_q8_k_lane(const float *blk, int lane, uint32_t (&w)[2], int &sum16,
+                                                   float &d) {
+    float v[8];
+    load8(blk + 8 * lane, v);
+    float a = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(v[k]));
+    a = group_max<32>(a);
+    d = a / 127.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    const int s = codes8(v, id, -127, 127, w);
+    sum16 = s + __shfl_xor_sync(0xffffffffu, s, 1);
+}
+
+// ========================================================================
+// Q4_K. Two lanes per block: lane h takes half h (values 128h..128h+127,
+// sub-blocks 4h..4h+3, qs bytes 64h..64h+63). Activations staged per
+// (vector, block, half) as a 144-byte record:
+//   codes[128] | int16 bsum32[4] (sub-blocks 4h..4h+3) | f32 d_x | pad
+// where bsum32(j) = bsums[2j] + bsums[2j+1]. A 144-byte stride (36 words)
+// puts 8 consecutive records' 128-bit loads in 8 disjoint bank quads.
 // ========================================================================
 struct TypeQ4_K {
-    static constexpr int kBlockElems = 256, kBlockBytes = 144, kLanesPerBlock = 4, kSums = 2;
-    static constexpr int kRecord = 80;
-    static size_t act_bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * 4 * kRecord; }
+    static constexpr int kBlockElems = 256, kBlockBytes = 144, kLanesPerBlock = 2, kSums = 2;
+    static constexpr int kRecord = 144;
+    static size_t act_bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * 2 * kRecord; }
 
-    // xq: [nv][nb] byte-exact Q8_K blocks (292 B, 4-byte aligned).
+    // From byte-exact Q8_K blocks (292 B, 4-byte aligned): 9 16-byte units per record.
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
-        const int n = nb * nv * 4;
-        for (int i = tid; i < n; i += nthr) {
-            const int blk = i >> 2, c = i & 3;
+        const int n = nb * nv * 2 * 9;
+        for (int u = tid; u < n; u += nthr) {
+            const int r = u / 9, part = u % 9;
+            const int blk = r >> 1, h = r & 1;
             const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + static_cast<size_t>(blk) * 292);
-            uint4 *rec = reinterpret_cast<uint4 *>(act + static_cast<size_t>(i) * kRecord);
+            uint4 *rec = reinterpret_cast<uint4 *>(act + static_cast<size_t>(r) * kRecord);
+            if (part < 8) {
+                const int w = 1 + 32 * h + 4 * part;  // codes start at byte 4
+                rec[part] = make_uint4(__ldg(src + w), __ldg(src + w + 1), __ldg(src + w + 2), __ldg(src + w + 3));
+            } else {
+                // bsums (int16) at byte 260 = word 65; sub-block 4h+t needs bsums[8h+2t], [8h+2t+1]
+                int s[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int w = 1 + 16 * c + 4 * j;  // qs start at byte 4
-                rec[j] = make_uint4(__ldg(src + w), __ldg(src + w + 1), __ldg(src + w + 2), __ldg(src + w + 3));
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t pr = __ldg(src + 65 + 4 * h + t);
+                    s[t] = static_cast<int>(static_cast<int16_t>(pr & 0xFFFFu)) +
+                           static_cast<int>(static_cast<int16_t>(pr >> 16));
+                }
+                rec[8] = make_uint4(pack16(s[0], s[1]), pack16(s[2], s[3]), __ldg(src), 0u);
             }
-            // bsums (int16) at byte 260 = word 65: sub-blocks 2c, 2c+1 need bsums[4c..4c+3]
-            const uint32_t p0 = __ldg(src + 65 + 2 * c), p1 = __ldg(src + 66 + 2 * c);
-            const int bs0 = static_cast<int>(static_cast<int16_t>(p0 & 0xFFFFu)) +
-                            static_cast<int>(static_cast<int16_t>(p0 >> 16));
-            const int bs1 = static_cast<int>(static_cast<int16_t>(p1 & 0xFFFFu)) +
-                            static_cast<int>(static_cast<int16_t>(p1 >> 16));
-            rec[4] = make_uint4(static_cast<uint32_t>(bs0), static_cast<uint32_t>(bs1), __ldg(src), 0u);
+        }
+    }
+
+    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
+        const int n = nb * nv;
+        const int h = lane >> 4;
+        for (int i = warp; i < n; i += nwarps) {
+            uint32_t w[2];
+            int s16;
+            float d;
+            quantize_q8_k_lane(x + static_cast<size_t>(i) * 256, lane, w, s16, d);
+            const int s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 2);  // sub-block lane/4
+            uint8_t *rec = act + (static_cast<size_t>(i) * 2 + h) * kRecord;
+            reinterpret_cast<uint2 *>(rec)[lane & 15] = make_uint2(w[0], w[1]);
+            if ((lane & 3) == 0) reinterpret_cast<int16_t *>(rec + 128)[(lane >> 2) & 3] = static_cast<int16_t>(s32);
+            if ((lane & 15) == 0) reinterpret_cast<uint2 *>(rec + 136)[0] = make_uint2(__float_as_uint(d), 0u);
         }
     }
 
     template <int NV, bool ISUMS>
-    __device__ static void item(const uint8_t *rowp, int b, int c, bool active, const uint8_t *act, int nb,
+    __device__ static void item(const uint8_t *rowp, int b, int h, bool active, const uint8_t *act, int nb,
                                 float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
         const uint8_t *blk = rowp + b * kBlockBytes;  // 16-byte aligned (144 = 9 x 16)
         const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
         const float dw = f16_bits_to_f32(hdr.x);
         const float dmin = f16_bits_to_f32(hdr.x >> 16);
-        // scales[0..3] = hdr.y, scales[4..7] = hdr.z, scales[8..11] = hdr.w.
-        // Sub-block j < 4: sc = s[j] & 63, m = s[j+4] & 63. j >= 4 (jj = j-4):
-        // sc = (s[j+4] & 15) | (s[jj] >> 6) << 4, m = (s[j+4] >> 4) | (s[j] >> 6) << 4.
-        int sc[2], mn[2];
+        // 6-bit scales and mins of sub-blocks 4h..4h+3, one per byte.
+        // scales[0..3] = hdr.y, [4..7] = hdr.z, [8..11] = hdr.w. Half 0: sc = s[j] & 63,
+        // m = s[j+4] & 63. Half 1 (j = 4 + t): sc = (s[8+t] & 15) | (s[t] >> 6) << 4,
+        // m = (s[8+t] >> 4) | (s[4+t] >> 6) << 4.
+        const uint32_t SC = h == 0 ? (hdr.y & 0x3F3F3F3Fu)
+                                   : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
+        const uint32_t M = h == 0 ? (hdr.z & 0x3F3F3F3Fu)
+                                  : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
+        uint32_t q[16];
+        const uint4 *qp = reinterpret_cast<const uint4 *>(blk + 16 + 64 * h);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int j = 2 * c + h;
-            const int jj = j & 3;
-            const uint32_t y8 = (hdr.y >> (8 * jj)) & 0xFFu;
-            const uint32_t z8 = (hdr.z >> (8 * jj)) & 0xFFu;
-            const uint32_t w8 = (hdr.w >> (8 * jj)) & 0xFFu;
-            if (j < 4) {
-                sc[h] = static_cast<int>(y8 & 63u);
-                mn[h] = static_cast<int>(z8 & 63u);
-            } else {
-                sc[h] = static_cast<int>((w8 & 15u) | ((y8 >> 6) << 4));
-                mn[h] = static_cast<int>((w8 >> 4) | ((z8 >> 6) << 4));
-            }
+        for (int j = 0; j < 4; ++j) {
+            const uint4 t = qp[j];
+            q[4 * j] = t.x; q[4 * j + 1] = t.y; q[4 * j + 2] = t.z; q[4 * j + 3] = t.w;
         }
-        const uint4 qa = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * c);
-        const uint4 qb = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * c);
-        const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const int sc0 = SC & 0xFF, sc1 = (SC >> 8) & 0xFF, sc2 = (SC >> 16) & 0xFF, sc3 = SC >> 24;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const uint4 *rec = reinterpret_cast<const uint4 *>(
-                act + ((static_cast<size_t>(v) * nb + b) * 4 + c) * kRecord);
-            const uint4 a0 = rec[0], a1 = rec[1], a2 = rec[2], a3 = rec[3], ex = rec[4];
-            const uint32_t a[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
-                                    a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
-            int lo = 0, hi = 0;
+                act + ((static_cast<size_t>(v) * nb + b) * 2 + h) * kRecord);
+            uint32_t a[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 t = rec[j];
+                a[4 * j] = t.x; a[4 * j + 1] = t.y; a[4 * j + 2] = t.z; a[4 * j + 3] = t.w;
+            }
+            const uint4 ex = rec[8];
+            int d0 = 0, d1 = 0, d2 = 0, d3 = 0;  // d1, d3 carry a factor 16
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                lo = dp4a(q[i] & 0x0F0F0F0Fu, a[i], lo);
-                hi = dp4a((q[i] >> 4) & 0x0F0F0F0Fu, a[8 + i], hi);
+                d0 = dp4a(q[i] & 0x0F0F0F0Fu, a[i], d0);
+                d1 = dp4a_us(q[i] & 0xF0F0F0F0u, a[8 + i], d1);
+                d2 = dp4a(q[8 + i] & 0x0F0F0F0Fu, a[16 + i], d2);
+                d3 = dp4a_us(q[8 + i] & 0xF0F0F0F0u, a[24 + i], d3);
             }
-            int sq = sc[0] * lo + sc[1] * hi;
-            int sm = mn[0] * static_cast<int>(ex.x) + mn[1] * static_cast<int>(ex.y);
-            sq = group_sum<4>(sq);
-            sm = group_sum<4>(sm);
+            int sq = ((sc0 * d0 + sc2 * d2) * 16 + sc1 * d1 + sc3 * d3) >> 4;  // exact: divisible by 16
+            int sm = dp2a_hi_su(ex.y, M, dp2a_lo_su(ex.x, M, 0));
             if (ISUMS) {
-                if (active && c == 0) {
+                sq = group_sum<2>(sq);
+                sm = group_sum<2>(sm);
+                if (active && h == 0) {
                     isum_row[v * isum_vstride + 2 * b] = sq;
                     isum_row[v * isum_vstride + 2 * b + 1] = sm;
                 }
-            } else if (active && c == 0) {
+            } else if (active) {
                 const float dx = __uint_as_float(ex.z);
-                acc[v] += dx * (dw * static_cast<float>(sq) - dmin * static_cast<float>(sm));
+                acc[v] = fmaf(dx * dw, static_cast<float>(sq), acc[v]);
+                acc[v] = fmaf(-(dx * dmin), static_cast<float>(sm), acc[v]);
             }
         }
     }
 };
 
 // ========================================================================
-// Q6_K. Eight lanes per block: lane (h, lq) = (sub >> 2, sub & 3) takes
-// l = 8lq..8lq+7 of half h for all four k, i.e. 8 elements of each of the
-// sub-blocks j_k = 8h + 2k + (lq >> 1). Activations staged as
-//   qs records [nv][nb] x 320 B: segment s = 4h + k (elements 128h + 32k ..
-//     +31) at 40 s, so a lane's 8-byte loads are conflict free;
-//   extras [nv][nb] x 48 B: int16 bsums permuted so that position
-//     8h + 4p + k holds bsums[8h + 2k + p], then f32 d_x at byte 32.
-// The -32 offset of q is applied through the bsums: lanes with even lq
-// subtract 32 * sum_k sc_k * bsum(j_k) for their four sub-blocks.
+// Q6_K. Four lanes per block: lane sub = 2h + p takes half h and the 16
+// positions l = 16p..16p+15 of each of the four 32-value rows k, i.e. the
+// 16-value sub-blocks j_k = 8h + 2k + p (k = 0..3). Activations staged per
+// (vector, block, sub) as an 80-byte record:
+//   codes[64] (k-th 16 bytes = values 128h + 32k + 16p ..) |
+//   int16 bsums[j_0..j_3] | f32 d_x | pad
+// An 80-byte stride (20 words) puts 8 consecutive records' 128-bit loads in
+// 8 disjoint bank quads. The -32 offset of q is applied through the bsums.
 // ========================================================================
 struct TypeQ6_K {
-    static constexpr int kBlockElems = 256, kBlockBytes = 210, kLanesPerBlock = 8, kSums = 1;
-    static constexpr int kQsRecord = 320, kExRecord = 48;
-    static size_t act_bytes(int nb, int nv) {
-        return static_cast<size_t>(nv) * nb * (kQsRecord + kExRecord);
-    }
+    static constexpr int kBlockElems = 256, kBlockBytes = 210, kLanesPerBlock = 4, kSums = 1;
+    static constexpr int kRecord = 80;
+    static size_t act_bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * 4 * kRecord; }
 
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
-        const int nblk = nb * nv;
-        uint8_t *ex = act + static_cast<size_t>(nblk) * kQsRecord;
-        for (int i = tid; i < nblk * 9; i += nthr) {
-            const int blk = i / 9, s = i % 9;
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + static_cast<size_t>(blk) * 292);
-            if (s < 8) {
-                uint2 *dst = reinterpret_cast<uint2 *>(act + static_cast<size_t>(blk) * kQsRecord + 40 * s);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    dst[j] = make_uint2(__ldg(src + 1 + 8 * s + 2 * j), __ldg(src + 2 + 8 * s + 2 * j));
+        const int n = nb * nv * 4 * 5;
+        for (int u = tid; u < n; u += nthr) {
+            const int r = u / 5, part = u % 5;
+            const int blk = r >> 2, sub = r & 3, h = sub >> 1, p = sub & 1;
+            const uint8_t *src = xq + static_cast<size_t>(blk) * 292;
+            uint4 *rec = reinterpret_cast<uint4 *>(act + static_cast<size_t>(r) * kRecord);
+            if (part < 4) {
+                const uint32_t *w = reinterpret_cast<const uint32_t *>(src + 4 + 128 * h + 32 * part + 16 * p);
+                rec[part] = make_uint4(__ldg(w), __ldg(w + 1), __ldg(w + 2), __ldg(w + 3));
             } else {
-                const int16_t *bs = reinterpret_cast<const int16_t *>(xq + static_cast<size_t>(blk) * 292 + 260);
-                int16_t *dst = reinterpret_cast<int16_t *>(ex + static_cast<size_t>(blk) * kExRecord);
-                for (int h = 0; h < 2; ++h)
-                    for (int par = 0; par < 2; ++par)
-                        for (int k = 0; k < 4; ++k) dst[8 * h + 4 * par + k] = __ldg(bs + 8 * h + 2 * k + par);
-                reinterpret_cast<uint32_t *>(dst)[8] = __ldg(src);  // d_x
-                reinterpret_cast<uint32_t *>(dst)[9] = 0u;
-                reinterpret_cast<uint2 *>(dst)[5] = make_uint2(0u, 0u);
+                const int16_t *bs = reinterpret_cast<const int16_t *>(src + 260);
+                int s[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) s[k] = __ldg(bs + 8 * h + 2 * k + p);
+                rec[4] = make_uint4(pack16(s[0], s[1]), pack16(s[2], s[3]),
+                                    __ldg(reinterpret_cast<const uint32_t *>(src)), 0u);
             }
+        }
+    }
+
+    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
+        const int n = nb * nv;
+        // lane l holds values 8l..8l+7: h = l/16, k = (l%16)/4, p = (l%4)/2
+        const int h = lane >> 4, k = (lane >> 2) & 3, p = (lane >> 1) & 1;
+        const int sub = 2 * h + p;
+        for (int i = warp; i < n; i += nwarps) {
+            uint32_t w[2];
+            int s16;
+            float d;
+            quantize_q8_k_lane(x + static_cast<size_t>(i) * 256, lane, w, s16, d);
+            uint8_t *rec = act + (static_cast<size_t>(i) * 4 + sub) * kRecord;
+            reinterpret_cast<uint2 *>(rec + 16 * k)[lane & 1] = make_uint2(w[0], w[1]);
+            if ((lane & 1) == 0) reinterpret_cast<int16_t *>(rec + 64)[k] = static_cast<int16_t>(s16);
+            if (k == 0 && (lane & 1) == 0) reinterpret_cast<uint2 *>(rec + 72)[0] = make_uint2(__float_as_uint(d), 0u);
         }
     }
 
@@ -291,52 +424,45 @@ struct TypeQ6_K {
     __device__ static void item(const uint8_t *rowp, int b, int sub, bool active, const uint8_t *act, int nb,
                                 float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
         const uint8_t *blk = rowp + b * kBlockBytes;  // 2-byte aligned
-        const int h = sub >> 2, lq = sub & 3, par = lq >> 1;
-        uint32_t ql0[2], ql1[2], qh[2], scw[2];
-        lds_words_a2<2>(blk + 64 * h + 8 * lq, ql0);
-        lds_words_a2<2>(blk + 64 * h + 32 + 8 * lq, ql1);
-        lds_words_a2<2>(blk + 128 + 32 * h + 8 * lq, qh);
+        const int h = sub >> 1, p = sub & 1;
+        uint32_t ql0[4], ql1[4], qh[4], scw[2];
+        lds_words_a2<4>(blk + 64 * h + 16 * p, ql0);
+        lds_words_a2<4>(blk + 64 * h + 32 + 16 * p, ql1);
+        lds_words_a2<4>(blk + 128 + 32 * h + 16 * p, qh);
         lds_words_a2<2>(blk + 192 + 8 * h, scw);  // scales[8h .. 8h+7]
         const float dw = f16_bits_to_f32(lds_u16(blk + 208));
-        int sc[4];
+        // scales of sub-blocks 8h + 2k + p, k = 0..3, as 4 signed bytes
+        const uint32_t SC = __byte_perm(scw[0], scw[1], p ? 0x7531u : 0x6420u);
+        const int sc0 = sbyte(SC, 0), sc1 = sbyte(SC, 1), sc2 = sbyte(SC, 2), sc3 = sbyte(SC, 3);
+        uint32_t qv[4][4];  // q (0..63) of the lane's 16 values of row k, 4 per word
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sc[k] = sbyte(scw[k >> 1], 2 * (k & 1) + par);
-        // q (0..63) of the lane's 8 elements for each k, 4 per word
-        uint32_t qv[4][2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             qv[0][i] = (ql0[i] & 0x0F0F0F0Fu) | ((qh[i] << 4) & 0x30303030u);
             qv[1][i] = (ql1[i] & 0x0F0F0F0Fu) | ((qh[i] << 2) & 0x30303030u);
             qv[2][i] = ((ql0[i] >> 4) & 0x0F0F0F0Fu) | (qh[i] & 0x30303030u);
             qv[3][i] = ((ql1[i] >> 4) & 0x0F0F0F0Fu) | ((qh[i] >> 2) & 0x30303030u);
         }
-        const uint8_t *exbase = act + static_cast<size_t>(NV) * nb * kQsRecord;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const size_t r = static_cast<size_t>(v) * nb + b;
-            const uint8_t *rq = act + r * kQsRecord + 8 * lq;
-            int part = 0;
+            const uint4 *rec = reinterpret_cast<const uint4 *>(
+                act + ((static_cast<size_t>(v) * nb + b) * 4 + sub) * kRecord);
+            int dk[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint2 a = *reinterpret_cast<const uint2 *>(rq + 40 * (4 * h + k));
-                const int dk = dp4a(qv[k][1], a.y, dp4a(qv[k][0], a.x, 0));
-                part += sc[k] * dk;
+                const uint4 a = rec[k];
+                int s = dp4a(qv[k][0], a.x, 0);
+                s = dp4a(qv[k][1], a.y, s);
+                s = dp4a(qv[k][2], a.z, s);
+                dk[k] = dp4a(qv[k][3], a.w, s);
             }
-            const uint8_t *re = exbase + r * kExRecord;
-            if ((lq & 1) == 0) {
-                const uint2 bw = *reinterpret_cast<const uint2 *>(re + 8 * (2 * h + par));
-                const int bsum = sc[0] * static_cast<int>(static_cast<int16_t>(bw.x & 0xFFFFu)) +
-                                 sc[1] * static_cast<int>(static_cast<int16_t>(bw.x >> 16)) +
-                                 sc[2] * static_cast<int>(static_cast<int16_t>(bw.y & 0xFFFFu)) +
-                                 sc[3] * static_cast<int>(static_cast<int16_t>(bw.y >> 16));
-                part -= 32 * bsum;
-            }
-            part = group_sum<8>(part);
+            const uint4 ex = rec[4];
+            int s = sc0 * dk[0] + sc1 * dk[1] + sc2 * dk[2] + sc3 * dk[3];
+            s -= 32 * dp2a_hi_ss(ex.y, SC, dp2a_lo_ss(ex.x, SC, 0));
             if (ISUMS) {
-                if (active && sub == 0) isum_row[v * isum_vstride + b] = part;
-            } else if (active && sub == 0) {
-                const float dx = *reinterpret_cast<const float *>(re + 32);
-                acc[v] += static_cast<float>(part) * (dw * dx);
+                s = group_sum<4>(s);
+                if (active && sub == 0) isum_row[v * isum_vstride + b] = s;
+            } else if (active) {
+                acc[v] = fmaf(static_cast<float>(s), dw * __uint_as_float(ex.z), acc[v]);
             }
         }
     }
