@@ -2,11 +2,15 @@
 
 Default workload (the headline): one decode step through a 32-layer
 Q4_K_M-style stack -- per layer Q4_K q/k/v/o 4096 x 4096, Q4_K gate/up
-11008 x 4096, Q6_K down 4096 x 11008 -- each matrix with a fresh activation
-vector (n_vec = 1). A step is the 224 qgemv calls (activation quantization
-to Q8_K + GEMV each); weights stay resident in HBM (4.01 GB, far above L2, so
-every step streams them from HBM). The metric is effective weight bandwidth:
-weight bytes streamed per second.
+11008 x 4096, Q6_K down 4096 x 11008 -- each matrix with its own fresh
+activation vector (n_vec = 1; no chaining between matrices). A step is the
+224 matrix-vector products with their activation quantization to Q8_K. The
+products are independent, so the step runs them as batched calls
+(qgemv_batched: one launch for the 192 Q4_K matrices of row length 4096,
+one for the 32 Q6_K matrices of row length 11008); the same step with one
+qgemv call per matrix is reported beside it ("per_call"). Weights stay
+resident in HBM (4.01 GB, far above L2, so every step streams them from HBM).
+The metric is effective weight bandwidth: weight bytes streamed per second.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--n-vec V]
@@ -218,14 +222,29 @@ def run_ours(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     calls, host_sample = build_workload(args.workload, args.n_vec, device)
     wbytes = weight_bytes(calls)
-    ws = torch.empty(max(qg.qgemv_workspace_bytes(c["type"], c["n_in"], args.n_vec) for c in calls),
+    nv = args.n_vec
+    ws = torch.empty(max(qg.qgemv_workspace_bytes(c["type"], c["n_in"], nv) for c in calls),
                      dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device)
 
-    def step():
-        for c in calls:
-            qg.qgemv(c["type"], c["W"], c["x"], c["n_out"], c["n_in"], args.n_vec, y=c["y"], workspace=ws,
-                     stream=stream)
+    # Batched plans: matrices grouped by (type, n_in), at most MAX_BATCH a launch.
+    groups = {}
+    for c in calls:
+        groups.setdefault((c["type"], c["n_in"]), []).append(c)
+    plans = []
+    for (t, n_in), cs in sorted(groups.items()):
+        for i in range(0, len(cs), qg.MAX_BATCH):
+            part = cs[i:i + qg.MAX_BATCH]
+            plans.append((t, part, qg.BatchPlan(t, [(c["W"], c["x"], c["y"], c["n_out"]) for c in part], n_in, nv)))
+    batched = args.workload == "layer_stack"
+
+    def step_batched():
+        for _, _, plan in plans:
+            plan.run(stream)
+
+    def step_calls(sel=None):
+        for c in (calls if sel is None else sel):
+            qg.qgemv(c["type"], c["W"], c["x"], c["n_out"], c["n_in"], nv, y=c["y"], workspace=ws, stream=stream)
 
     def capture(fn):
         with torch.cuda.stream(stream):
@@ -256,6 +275,7 @@ def run_ours(args, rank, world, local_rank):
         clocks = sampler.stop() if sampler else None
         return e0.elapsed_time(e1) / 1e3, clocks
 
+    step = step_batched if batched else step_calls
     g_step = capture(step)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -270,18 +290,26 @@ def run_ours(args, rank, world, local_rank):
     value = wbytes * args.steps * world / t / 1e9
     ms_per_step = t / args.steps * 1e3
     assert qg.device_error() == 0, "a kernel reported a bounded-wait timeout"
+    fused = 4 * nv * max(c["n_in"] for c in calls) <= 48 * 1024
+    launches_per_step = (len(plans) if batched else len(calls)) * (1 if fused else 2)
+    del g_step
 
-    # ---- per-kind breakdown (each kind's calls alone, graph-replayed)
+    # ---- one qgemv call per matrix (stream-ordered, each call may depend on the previous)
+    per_call = None
+    if batched:
+        g = capture(step_calls)
+        reps = max(3, args.steps // 4)
+        tc, _ = time_graph(g, reps)
+        del g
+        per_call = {"value": round(wbytes * reps / tc / 1e9, 1), "unit": UNIT,
+                    "ms_per_step": round(tc / reps * 1e3, 4), "launches_per_step": len(calls) * (1 if fused else 2)}
+
+    # ---- per-kind breakdown: each kind's calls alone, one qgemv call each
     breakdown = {}
     kinds = sorted({(c["kind"] if c["kind"] not in ("q", "k", "v", "o") else "qkvo") for c in calls})
     for kind in kinds:
         sel = [c for c in calls if (c["kind"] == kind or (kind == "qkvo" and c["kind"] in ("q", "k", "v", "o")))]
-
-        def part(sel=sel):
-            for c in sel:
-                qg.qgemv(c["type"], c["W"], c["x"], c["n_out"], c["n_in"], args.n_vec, y=c["y"],
-                         workspace=ws, stream=stream)
-        g = capture(part)
+        g = capture(lambda sel=sel: step_calls(sel))
         reps = max(3, min(50, int(0.3 / max(1e-6, ms_per_step / 1e3 * len(sel) / len(calls)))))
         tk, _ = time_graph(g, reps)
         b = weight_bytes(sel)
@@ -291,35 +319,33 @@ def run_ours(args, rank, world, local_rank):
                            "GB_s": round(b * reps / tk / 1e9, 1)}
         del g
 
-    # ---- roofline of the dominant kernel: the GEMV alone (activations
-    # pre-quantized), over the launches of the dominant weight type
+    # ---- roofline of the dominant kernel: the launch that streams the most
+    # weight bytes, timed alone; algorithmic bytes = its weights + f32
+    # activations read + f32 outputs written
     peak, peak_kind = measured_peaks()
-    by_type = {}
-    for c in calls:
-        by_type[c["type"]] = by_type.get(c["type"], 0) + c["W"].numel()
-    dom_type = max(by_type, key=by_type.get)
-    dom = [c for c in calls if c["type"] == dom_type]
-    at = qg.qtype_act_type(dom_type)
-    for c in dom:
-        c["xq"] = qg.quantize_act(at, c["x"], args.n_vec)
-
-    def gemv_only():
-        for c in dom:
-            qg.qgemv_xq(c["type"], c["W"], c["xq"], c["n_out"], c["n_in"], args.n_vec, y=c["y"], stream=stream)
-    g = capture(gemv_only)
+    if batched:
+        dom_t, dom_calls, dom_plan = max(plans, key=lambda pl: weight_bytes(pl[1]))
+        g = capture(lambda: dom_plan.run(stream))
+        launches = 1
+    else:
+        dom_t = calls[0]["type"]
+        dom_calls = calls
+        g = capture(step_calls)
+        launches = len(calls)
     reps = 10
     tg, _ = time_graph(g, reps)
     del g
-    alg_bytes = sum(c["W"].numel() + c["xq"].numel() + 4 * args.n_vec * c["n_out"] for c in dom)
-    per_launch = alg_bytes / len(dom)
-    avg_dur = tg / reps / len(dom)
+    alg_bytes = sum(c["W"].numel() + 4 * nv * (c["n_in"] + c["n_out"]) for c in dom_calls)
+    per_launch = alg_bytes / launches
+    avg_dur = tg / reps / launches
     achieved = per_launch / avg_dur / 1e9
-    kernel_key = f"gemv_kernel<{qg.TYPE_NAMES[dom_type]},NV={args.n_vec}>"
-    roofline = {"bound": "hbm", "kernel": kernel_key, "achieved": round(achieved, 1), "peak": peak,
-                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+    kernel_key = f"gemv_kernel<{qg.TYPE_NAMES[dom_t]},NV={nv}>"
+    roofline = {"bound": "hbm", "kernel": kernel_key + (" batched" if batched else ""),
+                "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
                 "traffic": committed_traffic(f"{kernel_key}@{args.workload}"),
                 "algorithmic_bytes_per_launch": int(per_launch), "avg_launch_us": round(avg_dur * 1e6, 3),
-                "launches": len(dom)}
+                "launches": launches}
 
     # ---- end to end through the public API with host buffers: each step
     # copies every x in from pinned host memory and every y back out
@@ -327,10 +353,10 @@ def run_ours(args, rank, world, local_rank):
     hy = [torch.empty(c["y"].shape, dtype=torch.float32).pin_memory() for c in calls]
 
     def e2e_step():
-        for c, a, b in zip(calls, hx, hy):
+        for c, a in zip(calls, hx):
             c["x"].copy_(a, non_blocking=True)
-            qg.qgemv(c["type"], c["W"], c["x"], c["n_out"], c["n_in"], args.n_vec, y=c["y"], workspace=ws,
-                     stream=stream)
+        step()
+        for c, b in zip(calls, hy):
             b.copy_(c["y"], non_blocking=True)
     g = capture(e2e_step)
     e2e_reps = max(3, args.steps // 4)
@@ -351,24 +377,24 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0:
-        v, cores, desc = time_oracle(host_sample, args.n_vec, budget_s=args.cpu_budget)
+        v, cores, desc = time_oracle(host_sample, nv, budget_s=args.cpu_budget)
         cpu = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
 
-    launches_per_step = 2 * len(calls)  # quantize + GEMV per call
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "dtype_detail": "int8 x int8 -> int32 block sums, f32 block scales, f32 y",
         "data": "synthetic (seeded random GGUF blocks; x ~ N(0,1))",
-        "config": {"workload": args.workload, "n_vec": args.n_vec, "calls_per_step": len(calls),
+        "config": {"workload": args.workload, "n_vec": nv, "gemvs_per_step": len(calls),
+                   "api": "qgemv_batched (one launch per type and row length)" if batched else "qgemv per matrix",
                    "weight_bytes_per_step": wbytes,
                    "l2": "inputs larger than L2 (weights rotate through distinct buffers > 4x L2)",
                    "timing": "CUDA graph of one step, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
         "hbm_frac": round(value / world / peak, 4), "hbm_peak_gbs": peak,
         "us_per_token": round(ms_per_step * 1e3, 2),
-        "breakdown": breakdown, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "per_call": per_call, "breakdown": breakdown, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
     return line

@@ -16,7 +16,8 @@ __all__ = [
     "F32", "F16", "Q4_0", "Q8_0", "Q4_K", "Q6_K", "Q8_K", "MAX_NVEC", "QGError",
     "library_path", "lib", "qtype_nbytes", "qtype_block", "qtype_act_type",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes",
-    "qgemv", "qgemv_xq", "qgemv_block_isums", "qgemv_noalloc", "device_error", "EXPORTED_SYMBOLS",
+    "qgemv", "qgemv_xq", "qgemv_block_isums", "qgemv_noalloc", "qgemv_batched",
+    "qgemv_batched_workspace_bytes", "BatchPlan", "device_error", "EXPORTED_SYMBOLS", "MAX_BATCH",
 ]
 
 F32, F16, Q4_0, Q8_0, Q4_K, Q6_K, Q8_K = 0, 1, 2, 8, 12, 14, 15
@@ -29,7 +30,14 @@ EXPORTED_SYMBOLS = (
     "qtype_nbytes", "qtype_block", "qtype_act_type", "qg_status_string", "qg_last_cuda_error",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes", "qgemv",
     "qgemv_xq", "qgemv_block_isums", "qg_device_error", "qgemv_noalloc",
+    "qgemv_batched_workspace_bytes", "qgemv_batched",
 )
+MAX_BATCH = 256
+
+
+class GemvMat(ctypes.Structure):
+    """qg_gemv_mat: one matrix of a batched call."""
+    _fields_ = [("W", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("n_out", ctypes.c_int64)]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -73,6 +81,10 @@ def lib():
         L.qgemv_block_isums.argtypes, L.qgemv_block_isums.restype = [i32, vp, vp, vp, i64, i64, i64, vp], i32
         L.qg_device_error.argtypes, L.qg_device_error.restype = [ctypes.POINTER(ctypes.c_int32)], i32
         L.qgemv_noalloc.argtypes, L.qgemv_noalloc.restype = [i32, vp, vp, vp, i64, i64, i64, vp], i32
+        L.qgemv_batched_workspace_bytes.argtypes = [i32, i64, i64, i32]
+        L.qgemv_batched_workspace_bytes.restype = sz
+        L.qgemv_batched.argtypes = [i32, ctypes.POINTER(GemvMat), i32, i64, i64, vp, sz, vp]
+        L.qgemv_batched.restype = i32
         _lib = L
     return _lib
 
@@ -250,6 +262,47 @@ def qgemv_noalloc(t: int, W, x, n_out: int, n_in: int, n_vec: int = 1, y=None, s
     _check(lib().qgemv_noalloc(t, _ptr(W), _ptr(x), _ptr(y), n_out, n_in, n_vec, _stream(stream)),
            "qgemv_noalloc")
     return y
+
+
+def qgemv_batched_workspace_bytes(t: int, n_in: int, n_vec: int, n_mats: int) -> int:
+    return int(lib().qgemv_batched_workspace_bytes(t, n_in, n_vec, n_mats))
+
+
+class BatchPlan:
+    """A prepared batched call: the matrix table is built once from tensors
+    (W uint8, x f32 [n_vec, n_in], y f32 [n_vec, n_out]) and reused; run()
+    only issues the C call."""
+
+    def __init__(self, t: int, mats, n_in: int, n_vec: int = 1, workspace=None):
+        torch = _torch()
+        if not 1 <= len(mats) <= MAX_BATCH:
+            raise ValueError(f"1..{MAX_BATCH} matrices per batch")
+        self.t, self.n_in, self.n_vec = t, n_in, n_vec
+        self.keep = []
+        self.table = (GemvMat * len(mats))()
+        for i, (W, x, y, n_out) in enumerate(mats):
+            _dev_tensor(W, torch.uint8, "W")
+            _dev_tensor(x, torch.float32, "x")
+            _dev_tensor(y, torch.float32, "y")
+            _need(x, 4 * n_vec * n_in, "x")
+            _need(y, 4 * n_vec * n_out, "y")
+            self.table[i] = GemvMat(W.data_ptr(), x.data_ptr(), y.data_ptr(), n_out)
+            self.keep += [W, x, y]
+        need = qgemv_batched_workspace_bytes(t, n_in, n_vec, len(mats))
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=mats[0][0].device)
+        _dev_tensor(workspace, torch.uint8, "workspace")
+        self.workspace = workspace
+
+    def run(self, stream=None):
+        _check(lib().qgemv_batched(self.t, self.table, len(self.table), self.n_in, self.n_vec,
+                                   _ptr(self.workspace), self.workspace.numel(), _stream(stream)), "qgemv_batched")
+
+
+def qgemv_batched(t: int, mats, n_in: int, n_vec: int = 1, workspace=None, stream=None):
+    """y_i = W_i . x_i for independent matrices [(W, x, y, n_out), ...] of one
+    type, row length and vector count, in one launch."""
+    BatchPlan(t, mats, n_in, n_vec, workspace).run(stream)
 
 
 def device_error() -> int:

@@ -9,9 +9,10 @@
 
 namespace qg {
 
-__global__ void quantize_q8_0_kernel(const float *, uint8_t *, int64_t);
-__global__ void quantize_q8_k_kernel(const float *, uint8_t *, int64_t);
-__global__ void quantize_q4_0_kernel(const float *, uint8_t *, int64_t);
+cudaError_t launch_quantize_kernel(int type, int grid, int block, cudaStream_t s, const float *x, uint8_t *out,
+                                   int64_t n_blocks);
+cudaError_t launch_quantize_batched_kernel(int type, int grid, int block, cudaStream_t s, const QuantTable &t,
+                                           uint8_t *out, int n_mats, int64_t blocks_per_mat);
 __global__ void dequant_q8_0_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q4_0_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q4_k_kernel(const uint8_t *, float *, int64_t);
@@ -95,11 +96,11 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 // Tuning of the GEMV launch (read once): CTAs resident per SM that the grid
 // aims at, and the shared-memory ring budget per CTA in KiB.
 int tune_ctas_per_sm() {
-    static const int v = env_int("QG_CTAS_PER_SM", 2, 1, 4);
+    static const int v = env_int("QG_CTAS_PER_SM", 1, 1, 4);
     return v;
 }
 int tune_ring_kib() {
-    static const int v = env_int("QG_RING_KIB", 64, 16, 200);
+    static const int v = env_int("QG_RING_KIB", 96, 16, 200);
     return v;
 }
 
@@ -117,38 +118,41 @@ size_t round16(size_t v) { return (v + 15) & ~size_t(15); }
 
 constexpr int kSmemTailPad = 16;  // unaligned word reads may touch up to 4 bytes past a stage
 
-// Stage geometry and grid of one GEMV launch. Returns QG_OK or QG_ERR_SHAPE.
-int plan_gemv(int type, int64_t n_out, int64_t n_in, int nv, int sms, int smem_limit, GemvParams *p,
-              GemvLaunch *l) {
+// Stage geometry and grid of one GEMV launch. x_bytes is the shared-memory
+// copy of f32 x for in-kernel quantization (0 otherwise). Returns QG_OK or
+// QG_ERR_SHAPE when the activations do not fit next to two stages.
+int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int smem_limit, size_t x_bytes,
+              GemvParams *p, GemvLaunch *l) {
     int elems, bytes;
     block_info(type, &elems, &bytes);
     const int64_t nb = n_in / elems;
     const int64_t row_bytes = nb * bytes;
     const size_t act = round16(act_smem_bytes(type, static_cast<int>(nb), nv));
+    const size_t xb = round16(x_bytes);
     const size_t ring_target = static_cast<size_t>(tune_ring_kib()) * 1024;
     for (int split = 1; split <= kConsumerWarps; split *= 2) {
-        const int R = kConsumerWarps / split;
+        const int R = (kConsumerWarps / split) * kRowsPerWarp;
         const size_t stage = round16(static_cast<size_t>(R) * row_bytes + 15);
-        if (split < kConsumerWarps && stage > 20480) continue;  // prefer stages of <= 20 KiB
-        const size_t fixed = kHeaderBytes + act + kSmemTailPad;
+        if (split < kConsumerWarps && stage > 40960) continue;  // prefer stages of <= 40 KiB
+        const size_t fixed = kHeaderBytes + act + xb + kSmemTailPad;
         if (fixed + 2 * stage > static_cast<size_t>(smem_limit)) continue;
         int S = static_cast<int>(ring_target / stage);
         S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
         while (S > 2 && fixed + S * stage > static_cast<size_t>(smem_limit)) --S;
         const size_t smem = fixed + S * stage;
         p->row_bytes = row_bytes;
-        p->w_total = row_bytes * n_out;
-        p->n_out = static_cast<int>(n_out);
+        p->total_rows = total_rows;
         p->nb = static_cast<int>(nb);
         p->rows_per_stage = R;
         p->split = split;
         p->n_stages = S;
         p->stage_bytes = static_cast<int>(stage);
         p->act_bytes = static_cast<int>(act);
+        p->x_bytes = static_cast<int>(xb);
         const int per_sm_fit = static_cast<int>((228 * 1024) / (smem + 1024));
         int per_sm = tune_ctas_per_sm();
         if (per_sm > per_sm_fit) per_sm = per_sm_fit < 1 ? 1 : per_sm_fit;
-        const int64_t tiles = (n_out + R - 1) / R;
+        const int64_t tiles = (total_rows + R - 1) / R;
         const int64_t cap = static_cast<int64_t>(sms) * per_sm;
         l->grid = static_cast<int>(tiles < cap ? tiles : cap);
         l->smem = static_cast<int>(smem);
@@ -158,13 +162,13 @@ int plan_gemv(int type, int64_t n_out, int64_t n_in, int nv, int sms, int smem_l
     return QG_ERR_SHAPE;
 }
 
-cudaError_t launch_gemv(int type, const GemvParams &p, int nv, bool isums, const GemvLaunch &l, int device,
-                        cudaStream_t s) {
+cudaError_t launch_gemv(int type, const GemvParams &p, const GemvMat *mats, int n, int nv, bool isums,
+                        const GemvLaunch &l, int device, cudaStream_t s) {
     switch (type) {
-    case QG_Q8_0: return launch_gemv_q8_0(p, nv, isums, l, device, s);
-    case QG_Q4_0: return launch_gemv_q4_0(p, nv, isums, l, device, s);
-    case QG_Q4_K: return launch_gemv_q4_k(p, nv, isums, l, device, s);
-    case QG_Q6_K: return launch_gemv_q6_k(p, nv, isums, l, device, s);
+    case QG_Q8_0: return launch_gemv_q8_0(p, mats, n, nv, isums, l, device, s);
+    case QG_Q4_0: return launch_gemv_q4_0(p, mats, n, nv, isums, l, device, s);
+    case QG_Q4_K: return launch_gemv_q4_k(p, mats, n, nv, isums, l, device, s);
+    case QG_Q6_K: return launch_gemv_q6_k(p, mats, n, nv, isums, l, device, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -191,17 +195,24 @@ int launch_quantize(int act_type, const float *x, void *xq, int64_t n_blocks, in
     const int warps_per_cta = 8;
     int64_t grid = (n_blocks + warps_per_cta - 1) / warps_per_cta;
     if (grid > static_cast<int64_t>(sms) * 16) grid = static_cast<int64_t>(sms) * 16;
-    cudaError_t e;
-    if (act_type == QG_Q8_0)
-        e = launch_pdl(quantize_q8_0_kernel, static_cast<int>(grid), 32 * warps_per_cta, 0, s, x,
-                       static_cast<uint8_t *>(xq), n_blocks);
-    else if (act_type == QG_Q8_K)
-        e = launch_pdl(quantize_q8_k_kernel, static_cast<int>(grid), 32 * warps_per_cta, 0, s, x,
-                       static_cast<uint8_t *>(xq), n_blocks);
-    else
-        e = launch_pdl(quantize_q4_0_kernel, static_cast<int>(grid), 32 * warps_per_cta, 0, s, x,
-                       static_cast<uint8_t *>(xq), n_blocks);
+    uint8_t *out = static_cast<uint8_t *>(xq);
+    const int g = static_cast<int>(grid), blk = 32 * warps_per_cta;
+    const cudaError_t e = launch_quantize_kernel(act_type, g, blk, s, x, out, n_blocks);
     return e == cudaSuccess ? QG_OK : cuda_fail(e, "quantize launch");
+}
+
+// Activations of n matrices (xs[m], blocks_per_mat blocks each) into xq.
+int launch_quantize_batched(int act_type, const QuantTable &t, int n, void *xq, int64_t blocks_per_mat, int sms,
+                            cudaStream_t s) {
+    const int64_t n_blocks = blocks_per_mat * n;
+    if (n_blocks == 0) return QG_OK;
+    const int warps_per_cta = 8;
+    int64_t grid = (n_blocks + warps_per_cta - 1) / warps_per_cta;
+    if (grid > static_cast<int64_t>(sms) * 16) grid = static_cast<int64_t>(sms) * 16;
+    uint8_t *out = static_cast<uint8_t *>(xq);
+    const int g = static_cast<int>(grid), blk = 32 * warps_per_cta;
+    const cudaError_t e = launch_quantize_batched_kernel(act_type, g, blk, s, t, out, n, blocks_per_mat);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, "batched quantize launch");
 }
 
 // Activations of at most this many f32 bytes per call are quantized inside
@@ -211,22 +222,24 @@ constexpr int64_t kFusedQuantMaxBytes = 48 * 1024;
 
 bool fused_quantization(int64_t n_in, int64_t n_vec) { return 4 * n_in * n_vec <= kFusedQuantMaxBytes; }
 
-// The product on quantized activations xq, or on f32 x quantized in the
-// kernel when x is non-null (shared by qgemv, qgemv_xq, qgemv_noalloc and
-// qgemv_block_isums). Arguments are already validated.
-int run_gemv(int type, const void *W, const void *xq, float *y, int32_t *isums, int64_t n_out, int64_t n_in,
-             int64_t n_vec, const DeviceInfo &dev, cudaStream_t s, const float *x = nullptr) {
+// The product over `n` matrices of one type, row length and vector count
+// (activations from mats[i].x quantized in the kernel when x_bytes > 0, else
+// from mats[i].xq). Arguments are already validated.
+int run_gemv_mats(int type, GemvMat *mats, int n, int64_t n_in, int64_t n_vec, size_t x_bytes, bool isums,
+                  const DeviceInfo &dev, cudaStream_t s) {
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        mats[i].row_base = total;
+        total += mats[i].n_out;
+    }
+    if (total == 0) return QG_OK;
     GemvParams p = {};
     GemvLaunch l = {};
-    int st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &p, &l);
+    int st = plan_gemv(type, total, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, x_bytes, &p, &l);
     if (st != QG_OK) return st;
-    p.W = static_cast<const uint8_t *>(W);
-    p.xq = static_cast<const uint8_t *>(xq);
-    p.x = x;
-    p.y = y;
-    p.isums = isums;
     p.err = dev.err;
-    cudaError_t e = launch_gemv(type, p, static_cast<int>(n_vec), isums != nullptr, l, dev.device, s);
+    p.n_mats = n;
+    cudaError_t e = launch_gemv(type, p, mats, n, static_cast<int>(n_vec), isums, l, dev.device, s);
     if (e != cudaSuccess) {
         char where[160];
         std::snprintf(where, sizeof where, "%s; grid %d block %d smem %d stages %d stage_bytes %d", g_launch_step,
@@ -234,6 +247,22 @@ int run_gemv(int type, const void *W, const void *xq, float *y, int32_t *isums, 
         return cuda_fail(e, where);
     }
     return QG_OK;
+}
+
+// One matrix: activations from xq, or from f32 x quantized in the kernel when
+// x is non-null (shared by qgemv, qgemv_xq, qgemv_noalloc and
+// qgemv_block_isums).
+int run_gemv(int type, const void *W, const void *xq, float *y, int32_t *isums, int64_t n_out, int64_t n_in,
+             int64_t n_vec, const DeviceInfo &dev, cudaStream_t s, const float *x = nullptr) {
+    GemvMat m = {};
+    m.W = static_cast<const uint8_t *>(W);
+    m.x = x;
+    m.xq = static_cast<const uint8_t *>(xq);
+    m.y = y;
+    m.isums = isums;
+    m.n_out = static_cast<int>(n_out);
+    const size_t x_bytes = x ? static_cast<size_t>(4 * n_in * n_vec) : 0;
+    return run_gemv_mats(type, &m, 1, n_in, n_vec, x_bytes, isums != nullptr, dev, s);
 }
 
 // Validation shared by qgemv_xq and qgemv_block_isums.
@@ -412,9 +441,11 @@ int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     // the product's shape limits are checked before anything is enqueued
     GemvParams probe = {};
     GemvLaunch pl = {};
-    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
+    const bool fused = fused_quantization(n_in, n_vec);
+    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
+                   fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &probe, &pl);
     if (st != QG_OK) return st;
-    if (fused_quantization(n_in, n_vec))  // one launch: x quantized in the GEMV's prologue
+    if (fused)  // one launch: x quantized in the GEMV's prologue
         return run_gemv(type, W, nullptr, y, nullptr, n_out, n_in, n_vec, dev, s, x);
     const int at = qtype_act_type(type);
     int elems, bytes;
@@ -422,6 +453,70 @@ int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     st = launch_quantize(at, x, workspace, n_in / elems * n_vec, dev.sms, s);
     if (st != QG_OK) return st;
     return run_gemv(type, W, workspace, y, nullptr, n_out, n_in, n_vec, dev, s);
+}
+
+size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int n_mats) {
+    if (n_mats < 1 || n_mats > QG_MAX_BATCH) return 0;
+    const size_t one = qgemv_workspace_bytes(type, n_in, n_vec);
+    if (one == 0) return 0;
+    return fused_quantization(n_in, n_vec) ? 16 : one * static_cast<size_t>(n_mats);
+}
+
+int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, int64_t n_vec, void *workspace,
+                  size_t workspace_bytes, qg_stream_t stream) {
+    int st = check_weight_type(type);
+    if (st != QG_OK) return st;
+    if (!mats) return QG_ERR_NULL;
+    if (n_mats < 1 || n_mats > QG_MAX_BATCH) return QG_ERR_SHAPE;
+    for (int i = 0; i < n_mats; ++i) {
+        st = check_gemv_args(type, mats[i].W, mats[i].x, mats[i].y, mats[i].n_out, n_in, n_vec);
+        if (st != QG_OK) return st;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_in == 0) {
+        for (int i = 0; i < n_mats; ++i) {
+            if (mats[i].n_out == 0) continue;
+            cudaError_t e = cudaMemsetAsync(mats[i].y, 0, static_cast<size_t>(mats[i].n_out * n_vec) * sizeof(float), s);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+        }
+        return QG_OK;
+    }
+    const bool fused = fused_quantization(n_in, n_vec);
+    const size_t need = qgemv_batched_workspace_bytes(type, n_in, n_vec, n_mats);
+    if (!fused && (!workspace || workspace_bytes < need)) return QG_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return QG_ERR_ALIGN;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != QG_OK) return st;
+    int64_t total = 0;
+    for (int i = 0; i < n_mats; ++i) total += mats[i].n_out;
+    if (total == 0) return QG_OK;
+    GemvParams probe = {};
+    GemvLaunch pl = {};
+    st = plan_gemv(type, total, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
+                   fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &probe, &pl);
+    if (st != QG_OK) return st;
+    GemvMat gm[QG_MAX_BATCH];
+    const int at = qtype_act_type(type);
+    int elems, bytes;
+    block_info(at, &elems, &bytes);
+    const int64_t blocks_per_mat = n_in / elems * n_vec;
+    if (!fused) {
+        QuantTable t = {};
+        for (int i = 0; i < n_mats; ++i) t.x[i] = mats[i].x;
+        st = launch_quantize_batched(at, t, n_mats, workspace, blocks_per_mat, dev.sms, s);
+        if (st != QG_OK) return st;
+    }
+    for (int i = 0; i < n_mats; ++i) {
+        gm[i] = GemvMat{};
+        gm[i].W = static_cast<const uint8_t *>(mats[i].W);
+        gm[i].x = fused ? mats[i].x : nullptr;
+        gm[i].xq = fused ? nullptr : static_cast<const uint8_t *>(workspace) + i * blocks_per_mat * bytes;
+        gm[i].y = mats[i].y;
+        gm[i].n_out = static_cast<int>(mats[i].n_out);
+    }
+    return run_gemv_mats(type, gm, n_mats, n_in, n_vec, fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, false,
+                         dev, s);
 }
 
 int qg_device_error(int32_t *code) {
@@ -498,7 +593,7 @@ extern "C" int qgemv_noalloc(int type, const void *W, const float *x, float *y, 
     if (st != QG_OK) return st;
     GemvParams probe = {};
     GemvLaunch pl = {};
-    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
+    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, 0, &probe, &pl);
     if (st != QG_OK) return st;
     void *scratch = nullptr;
     st = noalloc_scratch(dev.device, &scratch);

@@ -17,8 +17,6 @@ struct GemvLaunch {
     int smem_optin;  // the device's opt-in shared-memory limit per CTA
 };
 
-// Which CUDA call of a launch failed (for the error text).
-inline thread_local const char *g_launch_step = "";
 
 // Shared-memory opt-in, done once per (kernel, device). The flag is keyed by
 // the kernel's template arguments (every instance has the same C++ type).
@@ -33,61 +31,54 @@ inline cudaError_t ensure_smem_attr(K kernel, int device, int bytes) {
     return e;
 }
 
-template <class K, class... Args>
-inline cudaError_t launch_pdl(K kernel, int grid, int block, int smem, cudaStream_t stream, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(block));
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    g_launch_step = "cudaLaunchKernelEx";
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
+template <class T, int NV, bool ISUMS, int MAXB>
+inline cudaError_t launch_gemv_inst(const GemvParams &p, const GemvBatch<MAXB> &b, const GemvLaunch &l,
+                                    int device, cudaStream_t s) {
+    auto k = gemv_kernel<T, NV, ISUMS, MAXB>;
+    cudaError_t e = ensure_smem_attr<T, NV, ISUMS>(k, device, l.smem_optin);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k, l.grid, kGemvThreads, l.smem, s, p, b);
 }
 
 template <class T, int NV>
-inline cudaError_t launch_gemv_nv(const GemvParams &p, bool isums, const GemvLaunch &l, int device,
-                                  cudaStream_t s) {
-    if (isums) {
-        auto k = gemv_kernel<T, NV, true>;
-        cudaError_t e = ensure_smem_attr<T, NV, true>(k, device, l.smem_optin);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(k, l.grid, kGemvThreads, l.smem, s, p);
+inline cudaError_t launch_gemv_nv(const GemvParams &p, const GemvMat *mats, int n, bool isums, const GemvLaunch &l,
+                                  int device, cudaStream_t s) {
+    if (n == 1) {
+        GemvBatch<1> b;
+        b.m[0] = mats[0];
+        return isums ? launch_gemv_inst<T, NV, true, 1>(p, b, l, device, s)
+                     : launch_gemv_inst<T, NV, false, 1>(p, b, l, device, s);
     }
-    auto k = gemv_kernel<T, NV, false>;
-    cudaError_t e = ensure_smem_attr<T, NV, false>(k, device, l.smem_optin);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k, l.grid, kGemvThreads, l.smem, s, p);
+    if (isums || n > kMaxBatch) return cudaErrorInvalidValue;
+    GemvBatch<kMaxBatch> b = {};
+    for (int i = 0; i < n; ++i) b.m[i] = mats[i];
+    return launch_gemv_inst<T, NV, false, kMaxBatch>(p, b, l, device, s);
 }
 
 template <class T>
-inline cudaError_t launch_gemv_type(const GemvParams &p, int nv, bool isums, const GemvLaunch &l, int device,
-                                    cudaStream_t s) {
+inline cudaError_t launch_gemv_type(const GemvParams &p, const GemvMat *mats, int n, int nv, bool isums,
+                                    const GemvLaunch &l, int device, cudaStream_t s) {
     switch (nv) {
-    case 1: return launch_gemv_nv<T, 1>(p, isums, l, device, s);
-    case 2: return launch_gemv_nv<T, 2>(p, isums, l, device, s);
-    case 3: return launch_gemv_nv<T, 3>(p, isums, l, device, s);
-    case 4: return launch_gemv_nv<T, 4>(p, isums, l, device, s);
-    case 5: return launch_gemv_nv<T, 5>(p, isums, l, device, s);
-    case 6: return launch_gemv_nv<T, 6>(p, isums, l, device, s);
-    case 7: return launch_gemv_nv<T, 7>(p, isums, l, device, s);
-    case 8: return launch_gemv_nv<T, 8>(p, isums, l, device, s);
+    case 1: return launch_gemv_nv<T, 1>(p, mats, n, isums, l, device, s);
+    case 2: return launch_gemv_nv<T, 2>(p, mats, n, isums, l, device, s);
+    case 3: return launch_gemv_nv<T, 3>(p, mats, n, isums, l, device, s);
+    case 4: return launch_gemv_nv<T, 4>(p, mats, n, isums, l, device, s);
+    case 5: return launch_gemv_nv<T, 5>(p, mats, n, isums, l, device, s);
+    case 6: return launch_gemv_nv<T, 6>(p, mats, n, isums, l, device, s);
+    case 7: return launch_gemv_nv<T, 7>(p, mats, n, isums, l, device, s);
+    case 8: return launch_gemv_nv<T, 8>(p, mats, n, isums, l, device, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 // One definition per weight type, each in its own translation unit.
-cudaError_t launch_gemv_q8_0(const GemvParams &p, int nv, bool isums, const GemvLaunch &l, int device,
-                             cudaStream_t s);
-cudaError_t launch_gemv_q4_0(const GemvParams &p, int nv, bool isums, const GemvLaunch &l, int device,
-                             cudaStream_t s);
-cudaError_t launch_gemv_q4_k(const GemvParams &p, int nv, bool isums, const GemvLaunch &l, int device,
-                             cudaStream_t s);
-cudaError_t launch_gemv_q6_k(const GemvParams &p, int nv, bool isums, const GemvLaunch &l, int device,
-                             cudaStream_t s);
+#define QG_DECLARE_GEMV_LAUNCH(name)                                                                       \
+    cudaError_t name(const GemvParams &p, const GemvMat *mats, int n, int nv, bool isums, const GemvLaunch &l, \
+                     int device, cudaStream_t s);
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q8_0)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_0)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_k)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q6_k)
+#undef QG_DECLARE_GEMV_LAUNCH
 
 }  // namespace qg

@@ -6,10 +6,13 @@
 // and Q4_0 Like ggml", Examples 10-11).
 //
 // Design (one CTA = 1 producer warp + 8 consumer warps):
-//  * Each CTA owns a contiguous range of rows, i.e. one contiguous byte range
-//    of W. The producer's lane 0 streams it into a ring of shared-memory
+//  * A launch covers one matrix or a batch of independent matrices with the
+//    same type, row length and vector count; their rows are numbered
+//    consecutively ("global rows"). Each CTA owns a balanced contiguous range
+//    of global rows; within one matrix that is one contiguous byte range of
+//    its W. The producer's lane 0 streams it into a ring of shared-memory
 //    stages with 1-D bulk async copies (the TMA engine's non-tensor form),
-//    each stage a whole number of rows. A stage copies the 16-byte aligned
+//    each stage a whole number of rows of one matrix. A stage copies the 16-byte aligned
 //    window that covers its rows, so rows of any byte length (Q6_K rows of
 //    9030 bytes start 2-byte aligned) need no special case; the last < 16
 //    bytes of W, which no aligned window may cover without reading past the
@@ -25,7 +28,9 @@
 //    byte-exact Q8_0/Q8_K blocks or, for small activations, quantized from
 //    f32 x right there (the same rule, so the same bytes; it saves a
 //    dependent launch per call) -- then for each
-//    stage take one row per `split` warps. Lanes are grouped per block
+//    stage take kRowsPerWarp rows per `split` warps, interleaved. When a
+//    CTA's stages move on to the next matrix of a batch, the consumers
+//    stage that matrix's activations. Lanes are grouped per block
 //    (kLanesPerBlock lanes share one block); each group forms the block's
 //    exact int32 sums with __dp4a, combines them with warp shuffles, and the
 //    group leader applies the block's float scales.
@@ -38,40 +43,86 @@ namespace qg {
 constexpr int kConsumerWarps = 8;
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 16;
-// Shared-memory header: 2 x kMaxStages mbarriers (256 B), then the
-// cross-warp partial sums [2][kConsumerWarps][kMaxNvec] floats (512 B).
+constexpr int kRowsPerWarp = 2;  // rows a warp group takes per stage, processed interleaved
+constexpr int kMaxBatch = 256;   // matrices per batched launch (their table is a kernel parameter)
+// Shared-memory header: kMaxStages full + kMaxStages empty mbarriers, then
+// the cross-warp partial sums [2][kConsumerWarps][kRowsPerWarp][kMaxNvec]
+// floats (split > 1).
 constexpr int kRedOffset = 2 * 8 * kMaxStages;
-constexpr int kHeaderBytes = kRedOffset + 2 * kConsumerWarps * kMaxNvec * 4;
+constexpr int kHeaderBytes = ((kRedOffset + 2 * kConsumerWarps * kRowsPerWarp * kMaxNvec * 4) + 127) & ~127;
 
-struct GemvParams {
+// One matrix of a launch.
+struct GemvMat {
     const uint8_t *W;    // [n_out][row_bytes], 16-byte aligned
-    const uint8_t *xq;   // [n_vec][nb] activation blocks (byte-exact GGUF), or
-    const float *x;      // f32 activations [n_vec][n_in], quantized in the prologue when non-null
+    const float *x;      // f32 activations [n_vec][n_in], quantized in the kernel; or null and
+    const uint8_t *xq;   // byte-exact activation blocks [n_vec][nb] (Q8_0 or Q8_K)
     float *y;            // [n_vec][n_out]
     int32_t *isums;      // [n_vec][n_out][nb][kSums] (diagnostic mode only)
-    int32_t *err;        // device error word
-    int64_t row_bytes;
-    int64_t w_total;     // n_out * row_bytes
+    int64_t row_base;    // global row of this matrix's row 0
     int n_out;
+    int pad;
+};
+
+template <int MAXB>
+struct GemvBatch {
+    GemvMat m[MAXB];
+};
+
+// Geometry shared by every matrix of a launch.
+struct GemvParams {
+    int32_t *err;        // device error word
+    int64_t row_bytes;   // bytes of one row (n_in / block elems * block bytes)
+    int64_t total_rows;  // sum of n_out over the matrices
+    int n_mats;
     int nb;              // blocks per row
-    int rows_per_stage;  // kConsumerWarps / split
+    int rows_per_stage;  // (kConsumerWarps / split) * kRowsPerWarp
     int split;           // consumer warps per row: 1, 2, 4 or 8
     int n_stages;        // ring depth (2..kMaxStages)
     int stage_bytes;     // bytes per ring slot, multiple of 16
     int act_bytes;       // bytes of staged activations, multiple of 16
+    int x_bytes;         // bytes of f32 x staged in shared memory (n_vec * n_in * 4), 0 without x
 };
+
+// Walks a CTA's global rows [g, g1) as stages of at most R rows that never
+// cross a matrix boundary. Producer and consumers run the same walk.
+struct StageWalk {
+    int64_t g, g1;
+    int m;
+
+    template <int MAXB>
+    __device__ __forceinline__ bool next(const GemvBatch<MAXB> &b, int n_mats, int R, int &mat, int &r, int &rows) {
+        if (g >= g1) return false;
+        while (m + 1 < n_mats && b.m[m + 1].row_base <= g) ++m;
+        mat = m;
+        r = static_cast<int>(g - b.m[m].row_base);
+        int64_t left = b.m[m].n_out - r;
+        if (g1 - g < left) left = g1 - g;
+        rows = static_cast<int>(left < R ? left : R);
+        g += rows;
+        return true;
+    }
+};
+
+__device__ __forceinline__ StageWalk cta_rows(const GemvParams &p) {
+    StageWalk w;
+    w.g = static_cast<int64_t>(blockIdx.x) * p.total_rows / gridDim.x;
+    w.g1 = static_cast<int64_t>(blockIdx.x + 1) * p.total_rows / gridDim.x;
+    w.m = 0;
+    return w;
+}
 
 // ------------------------------------------------------------------------
 // Producer: lane 0 of the last warp.
 // ------------------------------------------------------------------------
-__device__ __forceinline__ void gemv_producer(const GemvParams &p, uint8_t *ring, uint32_t bar_full0,
-                                              uint32_t bar_empty0, int r0, int r1, int n_iter) {
+template <int MAXB>
+__device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBatch<MAXB> &b, uint8_t *ring,
+                                              uint32_t bar_full0, uint32_t bar_empty0) {
     const uint64_t policy = l2_evict_first_policy();
-    const int R = p.rows_per_stage;
     const int S = p.n_stages;
-    const int64_t lim = p.w_total & ~int64_t(15);
+    StageWalk walk = cta_rows(p);
+    int mat, r, rows;
     int issued = 0;
-    for (int k = 0; k < n_iter; ++k) {
+    for (int k = 0; walk.next(b, p.n_mats, p.rows_per_stage, mat, r, rows); ++k) {
         const int slot = k % S;
         if (k >= S) {
             const uint32_t parity = static_cast<uint32_t>((k / S) & 1) ^ 1u;
@@ -80,9 +131,9 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, uint8_t *ring
                 break;
             }
         }
-        const int row = r0 + k * R;
-        const int rows = min(R, r1 - row);
-        const int64_t start = static_cast<int64_t>(row) * p.row_bytes;
+        const uint8_t *W = b.m[mat].W;
+        const int64_t lim = (static_cast<int64_t>(b.m[mat].n_out) * p.row_bytes) & ~int64_t(15);
+        const int64_t start = static_cast<int64_t>(r) * p.row_bytes;
         const int64_t end = start + static_cast<int64_t>(rows) * p.row_bytes;
         const int64_t a0 = start & ~int64_t(15);
         int64_t a1 = (end + 15) & ~int64_t(15);
@@ -90,9 +141,9 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, uint8_t *ring
         const uint32_t bulk = a1 > a0 ? static_cast<uint32_t>(a1 - a0) : 0u;
         uint8_t *buf = ring + static_cast<size_t>(slot) * p.stage_bytes;
         // bytes past the last 16-byte boundary of W: plain loads
-        for (int64_t i = a0 + bulk; i < end; ++i) buf[i - a0] = __ldg(p.W + i);
+        for (int64_t i = a0 + bulk; i < end; ++i) buf[i - a0] = __ldg(W + i);
         mbar_arrive_expect_tx(bar_full0 + 8 * slot, bulk);
-        if (bulk) bulk_copy_g2s(smem_addr(buf), p.W + a0, bulk, bar_full0 + 8 * slot, policy);
+        if (bulk) bulk_copy_g2s(smem_addr(buf), W + a0, bulk, bar_full0 + 8 * slot, policy);
         ++issued;
     }
     // Do not leave while copies into this CTA's shared memory are in flight.
@@ -112,26 +163,47 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Activations of matrix `mat` into shared memory (all consumer threads).
+template <class T, int NV>
+__device__ __forceinline__ void stage_activations(const GemvParams &p, const GemvMat &mt, uint8_t *act,
+                                                  float *xbuf, int warp, int lane) {
+    if (mt.x) {
+        // Copy x into shared memory through the load/store path (16 bytes a
+        // thread per instruction, all in flight at once) -- not through the
+        // bulk-copy engine, whose queue also carries weight prefetches --
+        // then quantize from there.
+        const int n16 = p.x_bytes / 16;
+        const uint32_t xs = smem_addr(xbuf);
+        for (int i = threadIdx.x; i < n16; i += kConsumerWarps * 32) cp_async_16(xs + 16 * i, mt.x + 4 * i);
+        cp_async_wait_all();
+        named_barrier(1, kConsumerWarps * 32);
+        T::stage_x(xbuf, act, p.nb, NV, warp, kConsumerWarps, lane);
+    } else {
+        T::stage_act(mt.xq, act, p.nb, NV, threadIdx.x, kConsumerWarps * 32);
+    }
+    named_barrier(1, kConsumerWarps * 32);
+}
+
 // ------------------------------------------------------------------------
 // The kernel. T is the per-type policy (gemv_types.cuh), NV the number of
-// vectors, ISUMS selects the diagnostic output of the exact block sums.
+// vectors, ISUMS selects the diagnostic output of the exact block sums,
+// MAXB the capacity of the matrix table.
 // ------------------------------------------------------------------------
-template <class T, int NV, bool ISUMS>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams p) {
+template <class T, int NV, bool ISUMS, int MAXB>
+__global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
+    gemv_kernel(const GemvParams p, const GemvBatch<MAXB> b) {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t bar_full0 = smem_addr(smem);
     const uint32_t bar_empty0 = bar_full0 + 8 * kMaxStages;
     uint8_t *act = smem + kHeaderBytes;
-    uint8_t *ring = act + p.act_bytes;
-    float *red = reinterpret_cast<float *>(smem + kRedOffset);  // [2][8][NV] partials (split > 1)
+    float *xbuf = reinterpret_cast<float *>(act + p.act_bytes);
+    uint8_t *ring = act + p.act_bytes + p.x_bytes;
+    float *red = reinterpret_cast<float *>(smem + kRedOffset);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.n_out / gridDim.x);
-    const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.n_out / gridDim.x);
     const int R = p.rows_per_stage;
     const int S = p.n_stages;
-    const int n_iter = (r1 - r0 + R - 1) / R;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -145,75 +217,102 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvParams 
     pdl_allow_dependents();
 
     if (warp == kConsumerWarps) {
-        if (lane == 0) gemv_producer(p, ring, bar_full0, bar_empty0, r0, r1, n_iter);
+        if (lane == 0) gemv_producer(p, b, ring, bar_full0, bar_empty0);
         return;
     }
 
     // ---- consumers ----
     pdl_wait_prior_grids();  // activations may come from the previous kernel
-    if (p.x)
-        T::stage_x(p.x, act, p.nb, NV, warp, kConsumerWarps, lane);
-    else
-        T::stage_act(p.xq, act, p.nb, NV, threadIdx.x, kConsumerWarps * 32);
-    named_barrier(1, kConsumerWarps * 32);
+    bool failed = false;
 
     const int split = p.split;
-    const int row_in_stage = warp / split;
+    const int groups = kConsumerWarps / split;
+    const int grp = warp / split;
     const int part = warp % split;
     const int b0 = part * p.nb / split;
     const int b1 = (part + 1) * p.nb / split;
     const int items = (b1 - b0) * T::kLanesPerBlock;
-    const int64_t isum_vstride = static_cast<int64_t>(p.n_out) * p.nb * T::kSums;
-    bool failed = false;
 
-    for (int k = 0; k < n_iter; ++k) {
+    StageWalk walk = cta_rows(p);
+    int cur = -1;
+    int mat, r, rows;
+    for (int k = 0; walk.next(b, p.n_mats, R, mat, r, rows); ++k) {
+        const GemvMat &mt = b.m[mat];
+        if (mat != cur) {  // this CTA reaches a new matrix: stage its activations
+            if (cur >= 0) named_barrier(1, kConsumerWarps * 32);
+            stage_activations<T, NV>(p, mt, act, xbuf, warp, lane);
+            cur = mat;
+        }
         const int slot = k % S;
         if (!failed && !mbar_wait_bounded(bar_full0 + 8 * slot, static_cast<uint32_t>((k / S) & 1))) {
             record_error(p.err, kErrConsumerWait);
             failed = true;
         }
-        const int row_first = r0 + k * R;
-        const int rows = min(R, r1 - row_first);
-        if (row_in_stage < rows) {
-            const int row = row_first + row_in_stage;
-            const int64_t start = static_cast<int64_t>(row_first) * p.row_bytes;
-            const uint8_t *rowp = ring + static_cast<size_t>(slot) * p.stage_bytes + (start & 15) +
-                                  static_cast<int64_t>(row_in_stage) * p.row_bytes;
-            float acc[NV];
+        const int64_t start = static_cast<int64_t>(r) * p.row_bytes;
+        const uint8_t *stage = ring + static_cast<size_t>(slot) * p.stage_bytes + (start & 15);
+        const int64_t isum_vstride = static_cast<int64_t>(mt.n_out) * p.nb * T::kSums;
+        // this warp group's rows in the stage: grp + groups * i
+        const uint8_t *rowp[kRowsPerWarp];
+        bool has[kRowsPerWarp];
+        int32_t *isum_row[kRowsPerWarp];
 #pragma unroll
-            for (int v = 0; v < NV; ++v) acc[v] = 0.0f;
-            int32_t *isum_row = ISUMS ? p.isums + static_cast<int64_t>(row) * p.nb * T::kSums : nullptr;
-            if (!failed) {
-                for (int it = lane; it < ((items + 31) & ~31); it += 32) {
-                    const bool active = it < items;
-                    const int b = active ? b0 + it / T::kLanesPerBlock : b1 - 1;
-                    const int sub = it % T::kLanesPerBlock;
-                    T::template item<NV, ISUMS>(rowp, b, sub, active, act, p.nb, acc, isum_row,
-                                                isum_vstride);
-                }
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int ris = grp + groups * i;
+            has[i] = ris < rows;
+            rowp[i] = stage + static_cast<int64_t>(has[i] ? ris : 0) * p.row_bytes;
+            isum_row[i] = ISUMS ? mt.isums + static_cast<int64_t>(r + (has[i] ? ris : 0)) * p.nb * T::kSums
+                                : nullptr;
+        }
+        float acc[kRowsPerWarp][NV];
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) acc[i][v] = 0.0f;
+        if (!failed && has[0]) {
+            for (int it = lane; it < ((items + 31) & ~31); it += 32) {
+                const bool active = it < items;
+                const int blk = active ? b0 + it / T::kLanesPerBlock : b1 - 1;
+                const int sub = it % T::kLanesPerBlock;
+#pragma unroll
+                for (int i = 0; i < kRowsPerWarp; ++i)
+                    T::template item<NV, ISUMS>(rowp[i], blk, sub, active && has[i], act, p.nb, acc[i],
+                                                isum_row[i], isum_vstride);
             }
-            if (!ISUMS) {
+        }
+        if (!ISUMS && has[0]) {
 #pragma unroll
-                for (int v = 0; v < NV; ++v) acc[v] = warp_sum(acc[v]);
-                if (split == 1) {
-                    if (lane == 0 && !failed) {
+            for (int i = 0; i < kRowsPerWarp; ++i)
 #pragma unroll
-                        for (int v = 0; v < NV; ++v) p.y[static_cast<int64_t>(v) * p.n_out + row] = acc[v];
+                for (int v = 0; v < NV; ++v) acc[i][v] = warp_sum(acc[i][v]);
+            if (split == 1) {
+                if (lane == 0 && !failed) {
+#pragma unroll
+                    for (int i = 0; i < kRowsPerWarp; ++i) {
+                        if (!has[i]) continue;
+                        const int row = r + grp + groups * i;
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) mt.y[static_cast<int64_t>(v) * mt.n_out + row] = acc[i][v];
                     }
-                } else {
-                    float *r = red + ((k & 1) * kConsumerWarps + warp) * NV;
-                    if (lane == 0) {
+                }
+            } else {
+                float *rp = red + (((k & 1) * kConsumerWarps + warp) * kRowsPerWarp) * NV;
+                if (lane == 0) {
 #pragma unroll
-                        for (int v = 0; v < NV; ++v) r[v] = acc[v];
-                    }
-                    named_barrier(2 + row_in_stage, split * 32);
-                    if (part == 0 && lane == 0 && !failed) {
-                        const float *g = red + ((k & 1) * kConsumerWarps + warp) * NV;
+                    for (int i = 0; i < kRowsPerWarp; ++i)
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) rp[i * NV + v] = acc[i][v];
+                }
+                named_barrier(2 + grp, split * 32);
+                if (part == 0 && lane == 0 && !failed) {
+#pragma unroll
+                    for (int i = 0; i < kRowsPerWarp; ++i) {
+                        if (!has[i]) continue;
+                        const int row = r + grp + groups * i;
 #pragma unroll
                         for (int v = 0; v < NV; ++v) {
-                            float s = 0.0f;
-                            for (int q = 0; q < split; ++q) s += g[q * NV + v];
-                            p.y[static_cast<int64_t>(v) * p.n_out + row] = s;
+                            float sum = 0.0f;
+                            for (int q = 0; q < split; ++q) sum += rp[(q * kRowsPerWarp + i) * NV + v];
+                            mt.y[static_cast<int64_t>(v) * mt.n_out + row] = sum;
                         }
                     }
                 }

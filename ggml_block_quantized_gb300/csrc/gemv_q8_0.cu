@@ -1,12 +1,13 @@
 // gemv_q8_0.cu - template instances of the streaming GEMV kernel for Q8_0
-// weights (n_vec = 1..8, product and exact-block-sum outputs).
+// weights (n_vec = 1..8; single matrix with product or exact-block-sum output, batches
+// of up to kMaxBatch matrices with product output).
 #include "gemv_launch.cuh"
 
 namespace qg {
 
-cudaError_t launch_gemv_q8_0(const GemvParams &p, int nv, bool isums, const GemvLaunch &l, int device,
-                             cudaStream_t s) {
-    return launch_gemv_type<TypeQ8_0>(p, nv, isums, l, device, s);
+cudaError_t launch_gemv_q8_0(const GemvParams &p, const GemvMat *mats, int n, int nv, bool isums, const GemvLaunch &l,
+                             int device, cudaStream_t s) {
+    return launch_gemv_type<TypeQ8_0>(p, mats, n, nv, isums, l, device, s);
 }
 
 }  // namespace qg

@@ -55,9 +55,10 @@ __device__ __forceinline__ float group_max(float v) {
     return v;
 }
 
+// Eight f32 values from shared memory (the bulk-copied activations).
 __device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    const float4 a = reinterpret_cast<const float4 *>(p)[0];
+    const float4 b = reinterpret_cast<const float4 *>(p)[1];
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
@@ -112,7 +113,7 @@ struct ActQ8_0 {
         }
     }
 
-    // From f32 x [nv][nb * 32]: 4 lanes per 32-value block, 8 blocks per warp step.
+    // From f32 x [nv][nb * 32] in shared memory: 4 lanes per 32-value block, 8 blocks per warp step.
     __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
         const int n = nb * nv;
         for (int base = warp * 8; base < n; base += nwarps * 8) {

@@ -8,12 +8,18 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/qgemv.h"
+#include "qgemv.h"  // include/ is on the include path
 
 namespace qg {
 
 // ---------------------------------------------------------------- limits
 constexpr int kMaxNvec = QG_MAX_NVEC;
+constexpr int kQuantTableMax = 256;  // matrices per batched quantization launch
+
+// Activation pointers of a batched quantization launch (a kernel parameter).
+struct QuantTable {
+    const float *x[kQuantTableMax];
+};
 constexpr int kSmemLimit = 227 * 1024;  // opt-in dynamic shared memory per CTA
 
 // Device-side error word: 0 = fine; the first failing wait records its code.
@@ -105,6 +111,21 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// The same copy with the default L2 policy.
+__device__ __forceinline__ void bulk_copy_g2s_plain(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through the load/store unit.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 // L2 policy: weights are streamed once, so let them be evicted first.
@@ -201,6 +222,28 @@ __device__ __forceinline__ int code_from_rounded(float r, int lo, int hi) {
     if (r != r) return 0;
     r = fminf(fmaxf(r, static_cast<float>(lo)), static_cast<float>(hi));
     return static_cast<int>(r);
+}
+
+// Which CUDA call of a launch failed (for the error text).
+inline thread_local const char *g_launch_step = "";
+
+// Launch with programmatic dependent launch enabled: the kernel may start
+// while the previous kernel on the stream finishes; it orders itself with
+// griddepcontrol.wait before touching anything that kernel may write.
+template <class K, class... Args>
+inline cudaError_t launch_pdl(K kernel, int grid, int block, int smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    g_launch_step = "cudaLaunchKernelEx";
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace qg

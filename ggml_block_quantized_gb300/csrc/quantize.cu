@@ -28,103 +28,136 @@ __device__ __forceinline__ float warp_max_abs(float a) {
 }
 
 // ---------------------------------------------------------------- Q8_0
-// out: n_blocks x 34 bytes. One warp per block, lane i owns element i.
-__global__ void quantize_q8_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
-                                     int64_t n_blocks) {
-    pdl_allow_dependents();
-    pdl_wait_prior_grids();
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks;
-         b += warps) {
-        const float v = __ldg(x + b * 32 + lane);
-        const float amax = warp_max_abs(fabsf(v));
-        const float d = amax / 127.0f;
-        const float id = d != 0.0f ? 1.0f / d : 0.0f;
-        const int q = code_from_rounded(roundf(__fmul_rn(v, id)), -128, 127);
-        uint8_t *blk = out + b * 34;
-        blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
-        // the f16 scale as one 16-bit store (blocks start 2-byte aligned)
-        if (lane == 0) *reinterpret_cast<unsigned short *>(blk) = __half_as_ushort(__float2half_rn(d));
-    }
+// One 32-value block, lane i owns value i. ob: 34 bytes.
+__device__ __forceinline__ void q8_0_block(const float *xb, uint8_t *ob, int lane) {
+    const float v = __ldg(xb + lane);
+    const float amax = warp_max_abs(fabsf(v));
+    const float d = amax / 127.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    const int q = code_from_rounded(roundf(__fmul_rn(v, id)), -128, 127);
+    ob[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+    // the f16 scale as one 16-bit store (blocks start 2-byte aligned)
+    if (lane == 0) *reinterpret_cast<unsigned short *>(ob) = __half_as_ushort(__float2half_rn(d));
 }
 
 // ---------------------------------------------------------------- Q8_K
-// out: n_blocks x 292 bytes (f32 d | 256 int8 | 16 int16 bsums). One warp
-// per block, lane i owns elements 8i..8i+7.
-__global__ void quantize_q8_k_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
-                                     int64_t n_blocks) {
-    pdl_allow_dependents();
-    pdl_wait_prior_grids();
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks;
-         b += warps) {
-        const float4 *src = reinterpret_cast<const float4 *>(x + b * 256 + 8 * lane);
-        const float4 u = __ldg(src), w = __ldg(src + 1);
-        const float v[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
-        float a = 0.0f;
+// One 256-value block, lane i owns values 8i..8i+7. ob: 292 bytes
+// (f32 d | 256 int8 | 16 int16 bsums).
+__device__ __forceinline__ void q8_k_block(const float *xb, uint8_t *ob, int lane) {
+    const float4 *src = reinterpret_cast<const float4 *>(xb + 8 * lane);
+    const float4 u = __ldg(src), w = __ldg(src + 1);
+    const float v[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+    float a = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
-        const float amax = warp_max_abs(a);
-        const float d = amax / 127.0f;
-        const float id = d != 0.0f ? 1.0f / d : 0.0f;
-        uint32_t packed[2] = {0u, 0u};
-        int sum = 0;
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+    const float amax = warp_max_abs(a);
+    const float d = amax / 127.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    uint32_t packed[2] = {0u, 0u};
+    int sum = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int q = code_from_rounded(roundf(__fmul_rn(v[i], id)), -127, 127);
-            sum += q;
-            packed[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
-        }
-        // bsums[k] covers lanes 2k and 2k+1
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        uint8_t *blk = out + b * 292;
-        uint32_t *qs = reinterpret_cast<uint32_t *>(blk + 4 + 8 * lane);
-        qs[0] = packed[0];
-        qs[1] = packed[1];
-        if ((lane & 1) == 0) reinterpret_cast<int16_t *>(blk + 260)[lane >> 1] = static_cast<int16_t>(sum);
-        if (lane == 0) *reinterpret_cast<float *>(blk) = d;
+    for (int i = 0; i < 8; ++i) {
+        const int q = code_from_rounded(roundf(__fmul_rn(v[i], id)), -127, 127);
+        sum += q;
+        packed[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
     }
+    // bsums[k] covers lanes 2k and 2k+1
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    uint32_t *qs = reinterpret_cast<uint32_t *>(ob + 4 + 8 * lane);
+    qs[0] = packed[0];
+    qs[1] = packed[1];
+    if ((lane & 1) == 0) reinterpret_cast<int16_t *>(ob + 260)[lane >> 1] = static_cast<int16_t>(sum);
+    if (lane == 0) *reinterpret_cast<float *>(ob) = d;
 }
 
 // ---------------------------------------------------------------- Q4_0
-__global__ void quantize_q4_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ out,
-                                     int64_t n_blocks) {
+// One 32-value block, lane i owns value i. ob: 18 bytes.
+__device__ __forceinline__ void q4_0_block(const float *xb, uint8_t *ob, int lane) {
+    const float v = __ldg(xb + lane);
+    // First index of strictly largest |x| in scan order: reduce (|x|, index)
+    // keeping the larger magnitude and, on a tie, the smaller index. NaN
+    // never wins (the scalar test amax < |x| is false for NaN).
+    float best = (v != v) ? -1.0f : fabsf(v);
+    int idx = lane;
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+        const float ob_ = __shfl_xor_sync(0xffffffffu, best, m);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, m);
+        if (ob_ > best || (ob_ == best && oi < idx)) {
+            best = ob_;
+            idx = oi;
+        }
+    }
+    const float vmax = __shfl_sync(0xffffffffu, v, idx);
+    // an all-zero block keeps max = +0 (no element replaces it)
+    const float mx = best > 0.0f ? vmax : 0.0f;
+    const float d = mx / -8.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    const float t = __fadd_rn(__fmul_rn(v, id), 8.5f);
+    int code = static_cast<int>(t);  // truncation toward zero, t >= 0
+    code = code < 15 ? code : 15;
+    const int hi = __shfl_down_sync(0xffffffffu, code, 16);
+    if (lane < 16) ob[2 + lane] = static_cast<uint8_t>(code | (hi << 4));
+    if (lane == 0) *reinterpret_cast<unsigned short *>(ob) = __half_as_ushort(__float2half_rn(d));
+}
+
+template <int TYPE>
+__device__ __forceinline__ void quantize_block(const float *xb, uint8_t *ob, int lane) {
+    if (TYPE == QG_Q8_0) q8_0_block(xb, ob, lane);
+    else if (TYPE == QG_Q8_K) q8_k_block(xb, ob, lane);
+    else q4_0_block(xb, ob, lane);
+}
+
+// One warp per block over n_blocks consecutive blocks.
+template <int TYPE>
+__global__ void quantize_kernel(const float *__restrict__ x, uint8_t *__restrict__ out, int64_t n_blocks) {
     pdl_allow_dependents();
     pdl_wait_prior_grids();
+    constexpr int elems = TYPE == QG_Q8_K ? 256 : 32;
+    constexpr int bytes = TYPE == QG_Q8_K ? 292 : (TYPE == QG_Q8_0 ? 34 : 18);
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks;
+         b += warps)
+        quantize_block<TYPE>(x + b * elems, out + b * bytes, lane);
+}
+
+// Batches: the activations of matrix m (blocks_per_mat blocks, from t.x[m])
+// go to out + m * blocks_per_mat * block bytes.
+template <int TYPE>
+__global__ void quantize_batched_kernel(const QuantTable t, uint8_t *__restrict__ out, int n_mats,
+                                        int64_t blocks_per_mat) {
+    pdl_allow_dependents();
+    pdl_wait_prior_grids();
+    constexpr int elems = TYPE == QG_Q8_K ? 256 : 32;
+    constexpr int bytes = TYPE == QG_Q8_K ? 292 : 34;
+    const int lane = threadIdx.x & 31;
+    const int64_t n_blocks = blocks_per_mat * n_mats;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks;
          b += warps) {
-        const float v = __ldg(x + b * 32 + lane);
-        // First index of strictly largest |x| in scan order: reduce (|x|, index)
-        // keeping the larger magnitude and, on a tie, the smaller index. NaN
-        // never wins (the scalar test amax < |x| is false for NaN).
-        float best = (v != v) ? -1.0f : fabsf(v);
-        int idx = lane;
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, m);
-            const int oi = __shfl_xor_sync(0xffffffffu, idx, m);
-            if (ob > best || (ob == best && oi < idx)) {
-                best = ob;
-                idx = oi;
-            }
-        }
-        const float vmax = __shfl_sync(0xffffffffu, v, idx);
-        // an all-zero block keeps max = +0 (no element replaces it)
-        const float mx = best > 0.0f ? vmax : 0.0f;
-        const float d = mx / -8.0f;
-        const float id = d != 0.0f ? 1.0f / d : 0.0f;
-        const float t = __fadd_rn(__fmul_rn(v, id), 8.5f);
-        int code = static_cast<int>(t);  // truncation toward zero, t >= 0
-        code = code < 15 ? code : 15;
-        const int hi = __shfl_down_sync(0xffffffffu, code, 16);
-        uint8_t *blk = out + b * 18;
-        if (lane < 16) blk[2 + lane] = static_cast<uint8_t>(code | (hi << 4));
-        // the f16 scale as one 16-bit store (blocks start 2-byte aligned)
-        if (lane == 0) *reinterpret_cast<unsigned short *>(blk) = __half_as_ushort(__float2half_rn(d));
+        const int64_t m = b / blocks_per_mat, i = b % blocks_per_mat;
+        quantize_block<TYPE>(t.x[m] + i * elems, out + b * bytes, lane);
+    }
+}
+
+// Launches (kernels are launched from the translation unit that defines them).
+cudaError_t launch_quantize_kernel(int type, int grid, int block, cudaStream_t s, const float *x, uint8_t *out,
+                                   int64_t n_blocks) {
+    switch (type) {
+    case QG_Q8_0: return launch_pdl(quantize_kernel<QG_Q8_0>, grid, block, 0, s, x, out, n_blocks);
+    case QG_Q8_K: return launch_pdl(quantize_kernel<QG_Q8_K>, grid, block, 0, s, x, out, n_blocks);
+    case QG_Q4_0: return launch_pdl(quantize_kernel<QG_Q4_0>, grid, block, 0, s, x, out, n_blocks);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_quantize_batched_kernel(int type, int grid, int block, cudaStream_t s, const QuantTable &t,
+                                           uint8_t *out, int n_mats, int64_t blocks_per_mat) {
+    switch (type) {
+    case QG_Q8_0: return launch_pdl(quantize_batched_kernel<QG_Q8_0>, grid, block, 0, s, t, out, n_mats, blocks_per_mat);
+    case QG_Q8_K: return launch_pdl(quantize_batched_kernel<QG_Q8_K>, grid, block, 0, s, t, out, n_mats, blocks_per_mat);
+    default: return cudaErrorInvalidValue;
     }
 }
 

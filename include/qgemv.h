@@ -208,6 +208,36 @@ int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, i
 int qgemv_noalloc(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in,
                   int64_t n_vec, qg_stream_t stream);
 
+/* ---- Batches of independent products -------------------------------------- */
+
+#define QG_MAX_BATCH 256
+
+/* One matrix of a batched call (host struct; device pointers inside). */
+typedef struct {
+    const void *W;   /* weight blocks [n_out][n_in], 16-byte aligned */
+    const float *x;  /* f32 activations [n_vec][n_in], 16-byte aligned */
+    float *y;        /* f32 output [n_vec][n_out], 16-byte aligned */
+    int64_t n_out;   /* rows of this matrix (0 allowed) */
+} qg_gemv_mat;
+
+/* Workspace bytes qgemv_batched needs for n_mats matrices: 16 when the
+ * activations are small enough to be quantized inside the product (4 *
+ * n_in * n_vec <= 48 KiB), else the quantized activations of every matrix,
+ * n_mats * qgemv_workspace_bytes(type, n_in, n_vec). 0 on a bad argument. */
+size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int n_mats);
+
+/* y_i = W_i . x_i for n_mats independent matrices of one type, row length
+ * n_in and vector count n_vec, in one launch ([sipllm] The fused matmul,
+ * applied to several matrices; [rml] Quantized dot products; [candle]
+ * vec_dot_4 reuses one activation load across rows). Same arithmetic,
+ * result and limits as qgemv for each matrix. The matrices must be
+ * independent: no y_i may alias any W_j or x_j of the same call. The rows of
+ * all matrices are spread over the GPU's SMs as one stream, so a batch of
+ * small matrices runs at the bandwidth of one large one. mats is a host
+ * array read during the call (1 <= n_mats <= QG_MAX_BATCH). */
+int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, int64_t n_vec, void *workspace,
+                  size_t workspace_bytes, qg_stream_t stream);
+
 /* ---- Device-side status -------------------------------------------------- */
 
 /* Every wait inside the kernels is bounded (about one second). A wait that

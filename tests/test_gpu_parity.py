@@ -353,3 +353,77 @@ def test_graph_capture_replay_matches_eager():
     for a, b in zip(eager, ys):
         assert torch.equal(a, b)
     del rng
+
+
+# ------------------------------------------------------------- batched calls
+def batch_inputs(t, n_outs, n_in, n_vec, rng):
+    mats, host_w, host_x = [], [], []
+    for n_out in n_outs:
+        W = weights(t, n_out, n_in, rng) if n_out else np.zeros(16, np.uint8)
+        x = synth.f32_normal(rng, n_vec * n_in)
+        mats.append((dev(W), dev(x), torch.full((n_vec, max(n_out, 1)), np.nan, device="cuda"), n_out))
+        host_w.append(W)
+        host_x.append(x)
+    return mats, host_w, host_x
+
+
+@pytest.mark.parametrize("t", WTYPES)
+@pytest.mark.parametrize("n_vec", [1, 3, 8])
+def test_batched_equals_single_calls(t, n_vec):
+    """One launch over several independent matrices gives, per matrix, the
+    same bits as one qgemv call each (n_vec 8 takes the path that quantizes
+    all activations into the workspace first)."""
+    rng = np.random.default_rng(900 + t + n_vec)
+    n_in = 4096 if n_vec == 8 else (1024 if t in (qg.Q8_0, qg.Q4_0) else 2048)
+    n_outs = [300, 0, 1, 2000, 77, 513]
+    mats, host_w, host_x = batch_inputs(t, n_outs, n_in, n_vec, rng)
+    qg.qgemv_batched(t, mats, n_in, n_vec)
+    for (W, x, y, n_out), Wh, xh in zip(mats, host_w, host_x):
+        if n_out == 0:
+            continue
+        ref = qg.qgemv(t, W, x, n_out, n_in, n_vec)
+        assert torch.equal(y[:, :n_out], ref), n_out
+    # and against the oracle on one matrix
+    W, x, y, n_out = mats[3]
+    check_y(t, host_w[3], host_x[3], host(y), n_out, n_in, n_vec, sample_rows(n_out, rng, 64))
+
+
+def test_batched_layer_and_many_small_matrices():
+    rng = np.random.default_rng(901)
+    # the Q4_K matrices of one decoder layer
+    mats = []
+    ref = []
+    for m in range(6):
+        mat = synth.layer_matrix(2, m, 1)
+        W, x = dev(mat["w_blocks"]), dev(mat["x"])
+        y = torch.empty((1, mat["n_out"]), device="cuda")
+        mats.append((W, x, y, mat["n_out"]))
+        ref.append(qg.qgemv(qg.Q4_K, W, x, mat["n_out"], 4096, 1))
+    qg.qgemv_batched(qg.Q4_K, mats, 4096, 1)
+    for (W, x, y, n), r in zip(mats, ref):
+        assert torch.equal(y, r)
+    # 256 tiny matrices: every CTA crosses many matrix boundaries
+    mats, host_w, host_x = batch_inputs(qg.Q6_K, [int(v) for v in rng.integers(1, 7, 256)], 512, 2, rng)
+    qg.qgemv_batched(qg.Q6_K, mats, 512, 2)
+    for (W, x, y, n_out), Wh, xh in zip(mats, host_w, host_x):
+        check_y(qg.Q6_K, Wh, xh, host(y)[:, :n_out], n_out, 512, 2)
+
+
+def test_batched_graph_capture():
+    rng = np.random.default_rng(902)
+    mats, _, _ = batch_inputs(qg.Q4_K, [4096, 4096, 11008], 4096, 1, rng)
+    plan = qg.BatchPlan(qg.Q4_K, mats, 4096, 1)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        plan.run(s)
+    torch.cuda.synchronize()
+    eager = [y.clone() for (_, _, y, _) in mats]
+    for (_, _, y, _) in mats:
+        y.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        plan.run(s)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, (_, _, y, _) in zip(eager, mats):
+        assert torch.equal(a, y)

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declarations_are_exported(L):
     names = declared_functions()
-    assert len(names) == 14
+    assert len(names) == 16
     assert sorted(qg.EXPORTED_SYMBOLS) == names
     for n in names:
         assert hasattr(L, n), n
@@ -124,6 +124,28 @@ def test_other_entry_points_validate(L):
     assert L.qgemv_block_isums(qg.Q6_K, A, A2, NUL, 4, 256, 1, NUL) == ERR_NULL
     assert L.qgemv_block_isums(qg.Q4_0, A, A2, A3, 4, 256, 0, NUL) == ERR_SHAPE
     assert L.qg_device_error(None) == ERR_NULL
+
+
+def test_batched_validation(L):
+    Mat = qg.GemvMat
+    ws = ctypes.c_size_t(1 << 20)
+    one = (Mat * 1)(Mat(0x10000, 0x20000, 0x30000, 16))
+    assert L.qgemv_batched(99, one, 1, 256, 1, A, ws, NUL) == ERR_TYPE
+    assert L.qgemv_batched(qg.Q8_K, one, 1, 256, 1, A, ws, NUL) == ERR_PAIR
+    assert L.qgemv_batched(qg.Q4_K, None, 1, 256, 1, A, ws, NUL) == ERR_NULL
+    assert L.qgemv_batched(qg.Q4_K, one, 0, 256, 1, A, ws, NUL) == ERR_SHAPE
+    assert L.qgemv_batched(qg.Q4_K, one, 257, 256, 1, A, ws, NUL) == ERR_SHAPE
+    assert L.qgemv_batched(qg.Q4_K, one, 1, 250, 1, A, ws, NUL) == ERR_SHAPE
+    bad = (Mat * 2)(Mat(0x10000, 0x20000, 0x30000, 16), Mat(0x10000, 0x20008, 0x30000, 16))
+    assert L.qgemv_batched(qg.Q4_K, bad, 2, 256, 1, A, ws, NUL) == ERR_ALIGN
+    nul = (Mat * 2)(Mat(0x10000, 0x20000, 0x30000, 16), Mat(0x10000, 0, 0x30000, 16))
+    assert L.qgemv_batched(qg.Q4_K, nul, 2, 256, 1, A, ws, NUL) == ERR_NULL
+    # large activations need the quantized copies in the workspace
+    assert qg.qgemv_batched_workspace_bytes(qg.Q4_K, 4096, 8, 3) == 3 * 8 * 16 * 292
+    assert qg.qgemv_batched_workspace_bytes(qg.Q4_K, 4096, 1, 3) == 16
+    assert qg.qgemv_batched_workspace_bytes(qg.Q4_K, 4096, 1, 0) == 0
+    big = (Mat * 2)(Mat(0x10000, 0x20000, 0x30000, 16), Mat(0x10000, 0x20000, 0x30000, 16))
+    assert L.qgemv_batched(qg.Q4_K, big, 2, 4096, 8, A, ctypes.c_size_t(100), NUL) == ERR_WS
 
 
 def test_missing_library_fails_loudly(monkeypatch):
