@@ -135,7 +135,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ the workload
-def build_workload(name, n_vec, device, keep_host_layers=2):
+def build_workload(name, n_vec, device, keep_host_layers=2, n_layers=None):
     """Device-resident inputs for every qgemv call of one step.
 
     Returns (calls, host_sample): calls is a list of dicts (type, n_out, n_in,
@@ -148,7 +148,7 @@ def build_workload(name, n_vec, device, keep_host_layers=2):
 
     calls, host_sample = [], []
     if name == "layer_stack":
-        for layer in range(synth.N_LAYERS):
+        for layer in range(synth.N_LAYERS if n_layers is None else n_layers):
             for m in range(len(synth.LAYER_MATRICES)):
                 mat = synth.layer_matrix(layer, m, n_vec)
                 c = dict(kind=mat["name"], type=mat["type"], n_out=mat["n_out"], n_in=mat["n_in"],
@@ -220,7 +220,7 @@ def run_ours(args, rank, world, local_rank):
     __graft_entry__.build()
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
-    calls, host_sample = build_workload(args.workload, args.n_vec, device)
+    calls, host_sample = build_workload(args.workload, args.n_vec, device, n_layers=args.layers)
     wbytes = weight_bytes(calls)
     nv = args.n_vec
     ws = torch.empty(max(qg.qgemv_workspace_bytes(c["type"], c["n_in"], nv) for c in calls),
@@ -386,7 +386,8 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "dtype_detail": "int8 x int8 -> int32 block sums, f32 block scales, f32 y",
         "data": "synthetic (seeded random GGUF blocks; x ~ N(0,1))",
-        "config": {"workload": args.workload, "n_vec": nv, "gemvs_per_step": len(calls),
+        "config": {"workload": args.workload + ("" if args.layers in (None, 32) else f"[{args.layers} layers]"),
+                   "n_vec": nv, "gemvs_per_step": len(calls),
                    "api": "qgemv_batched (one launch per type and row length)" if batched else "qgemv per matrix",
                    "weight_bytes_per_step": wbytes,
                    "l2": "inputs larger than L2 (weights rotate through distinct buffers > 4x L2)",
@@ -451,6 +452,8 @@ def main():
                     choices=["layer_stack", "q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000"])
     ap.add_argument("--n-vec", type=int, default=1)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decoder layers of the stack (default 32; fewer only for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
