@@ -96,7 +96,7 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 // Tuning of the GEMV launch (read once): CTAs resident per SM that the grid
 // aims at, and the shared-memory ring budget per CTA in KiB.
 int tune_ctas_per_sm() {
-    static const int v = env_int("QG_CTAS_PER_SM", 1, 1, 4);
+    static const int v = env_int("QG_CTAS_PER_SM", 2, 1, 4);
     return v;
 }
 int tune_ring_kib() {
@@ -118,9 +118,25 @@ size_t round16(size_t v) { return (v + 15) & ~size_t(15); }
 
 constexpr int kSmemTailPad = 16;  // unaligned word reads may touch up to 4 bytes past a stage
 
-// Stage geometry and grid of one GEMV launch. x_bytes is the shared-memory
-// copy of f32 x for in-kernel quantization (0 otherwise). Returns QG_OK or
-// QG_ERR_SHAPE when the activations do not fit next to two stages.
+// Lanes of one activation block's f32 values (bytes) and lanes per weight
+// block, per type.
+int act_block_f32_bytes(int type) { return (type == QG_Q8_0 || type == QG_Q4_0) ? 128 : 1024; }
+int lanes_per_block(int type) {
+    switch (type) {
+    case QG_Q4_K: return TypeQ4_K::kLanesPerBlock;
+    case QG_Q6_K: return TypeQ6_K::kLanesPerBlock;
+    default: return 1;
+    }
+}
+
+// Stage geometry and grid of one GEMV launch. x_bytes is the f32 x of the
+// launch's vectors for in-kernel quantization (0 otherwise); it is staged
+// whole when that fits, else in chunks of whole activation blocks. Among the
+// configurations whose shared memory lets the tuned number of CTAs share an
+// SM (more resident warps hide more latency), the plan keeps the lanes of
+// each warp's item loop fullest, then prefers x staged whole (one round trip
+// per matrix), then the larger ring. Returns QG_ERR_SHAPE when the
+// activations do not fit next to two stages even with one CTA per SM.
 int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int smem_limit, size_t x_bytes,
               GemvParams *p, GemvLaunch *l) {
     int elems, bytes;
@@ -128,35 +144,72 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
     const int64_t nb = n_in / elems;
     const int64_t row_bytes = nb * bytes;
     const size_t act = round16(act_smem_bytes(type, static_cast<int>(nb), nv));
-    const size_t xb = round16(x_bytes);
     const size_t ring_target = static_cast<size_t>(tune_ring_kib()) * 1024;
-    for (int split = 1; split <= kConsumerWarps; split *= 2) {
-        const int R = (kConsumerWarps / split) * kRowsPerWarp;
-        const size_t stage = round16(static_cast<size_t>(R) * row_bytes + 15);
-        if (split < kConsumerWarps && stage > 40960) continue;  // prefer stages of <= 40 KiB
-        const size_t fixed = kHeaderBytes + act + xb + kSmemTailPad;
-        if (fixed + 2 * stage > static_cast<size_t>(smem_limit)) continue;
-        int S = static_cast<int>(ring_target / stage);
-        S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
-        while (S > 2 && fixed + S * stage > static_cast<size_t>(smem_limit)) --S;
-        const size_t smem = fixed + S * stage;
-        p->row_bytes = row_bytes;
-        p->total_rows = total_rows;
-        p->nb = static_cast<int>(nb);
-        p->rows_per_stage = R;
-        p->split = split;
-        p->n_stages = S;
-        p->stage_bytes = static_cast<int>(stage);
-        p->act_bytes = static_cast<int>(act);
-        p->x_bytes = static_cast<int>(xb);
-        const int per_sm_fit = static_cast<int>((228 * 1024) / (smem + 1024));
-        int per_sm = tune_ctas_per_sm();
-        if (per_sm > per_sm_fit) per_sm = per_sm_fit < 1 ? 1 : per_sm_fit;
-        const int64_t tiles = (total_rows + R - 1) / R;
+    const size_t sm_smem = 228 * 1024, cta_reserve = 1024;  // per-SM shared memory, per-CTA driver share
+    const size_t blk_f32 = static_cast<size_t>(act_block_f32_bytes(type));
+    size_t xb_opts[4] = {round16(x_bytes), 16384, 8192, 4096};
+    const int n_xb = x_bytes ? 4 : 1;
+    const int lpb = lanes_per_block(type);
+    for (int per_sm = tune_ctas_per_sm(); per_sm >= 1; --per_sm) {
+        size_t budget = sm_smem / per_sm - cta_reserve;
+        if (budget > static_cast<size_t>(smem_limit)) budget = static_cast<size_t>(smem_limit);
+        bool found = false;
+        double best_score = -1.0;
+        GemvParams bp = {};
+        size_t best_smem = 0;
+        for (int xi = 0; xi < n_xb; ++xi) {
+            size_t xb = xb_opts[xi];
+            if (x_bytes) {
+                if (xb > round16(x_bytes)) continue;
+                xb = xb / blk_f32 * blk_f32;  // whole activation blocks
+                if (xb == 0) continue;
+            }
+            const size_t fixed0 = kHeaderBytes + act + xb + kSmemTailPad;
+            for (int split = 1; split <= kConsumerWarps; split *= 2) {
+                const int R = (kConsumerWarps / split) * kRowsPerWarp;
+                const size_t stage = round16(static_cast<size_t>(R) * row_bytes + 15);
+                if (split < kConsumerWarps && stage > 40960) continue;  // stages of <= 40 KiB
+                // partial sums of split rows: [S][warps][rows per warp][nv] floats
+                auto red_bytes = [&](int S) {
+                    return split > 1 ? round16(static_cast<size_t>(S) * kConsumerWarps * kRowsPerWarp * nv * 4) : 0;
+                };
+                if (fixed0 + red_bytes(2) + 2 * stage > budget) continue;
+                int S = static_cast<int>(ring_target / stage);
+                S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+                while (S > 2 && fixed0 + red_bytes(S) + S * stage > budget) --S;
+                // lane use of the busiest warp's flattened item loop (two rows)
+                const int64_t items = (nb + split - 1) / split * lpb * kRowsPerWarp;
+                const double eff = static_cast<double>(nb * lpb * kRowsPerWarp) / split /
+                                   (32.0 * static_cast<double>((items + 31) / 32));
+                // fuller lanes first; then fewer warps per row (each stage does
+                // more work per warp); then x staged whole; then the larger ring
+                const double score = static_cast<int>(eff * 20.0 + 0.5) * 100.0 - split * 10.0 +
+                                     (xi == 0 ? 5.0 : 0.0) + static_cast<double>(S * stage) / (4.0 * 1024 * 1024);
+                if (score > best_score) {
+                    best_score = score;
+                    found = true;
+                    bp.row_bytes = row_bytes;
+                    bp.total_rows = total_rows;
+                    bp.nb = static_cast<int>(nb);
+                    bp.rows_per_stage = R;
+                    bp.split = split;
+                    bp.n_stages = S;
+                    bp.stage_bytes = static_cast<int>(stage);
+                    bp.act_bytes = static_cast<int>(act);
+                    bp.x_bytes = static_cast<int>(xb);
+                    bp.red_bytes = static_cast<int>(red_bytes(S));
+                    best_smem = fixed0 + red_bytes(S) + S * stage;
+                }
+            }
+        }
+        if (!found) continue;
+        *p = bp;
+        const int64_t tiles = (total_rows + bp.rows_per_stage - 1) / bp.rows_per_stage;
         const int64_t cap = static_cast<int64_t>(sms) * per_sm;
         l->grid = static_cast<int>(tiles < cap ? tiles : cap);
-        l->smem = static_cast<int>(smem);
+        l->smem = static_cast<int>(best_smem);
         l->smem_optin = smem_limit;
+        l->sms = sms;
         return QG_OK;
     }
     return QG_ERR_SHAPE;

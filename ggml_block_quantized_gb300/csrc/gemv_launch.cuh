@@ -15,6 +15,7 @@ struct GemvLaunch {
     int grid;
     int smem;
     int smem_optin;  // the device's opt-in shared-memory limit per CTA
+    int sms;         // SMs of the device
 };
 
 
@@ -31,13 +32,32 @@ inline cudaError_t ensure_smem_attr(K kernel, int device, int bytes) {
     return e;
 }
 
+// CTAs of kernel k that one SM holds with `smem` bytes of shared memory,
+// cached per (kernel, device) for the last shared-memory size asked.
+template <class T, int NV, bool ISUMS, class K>
+inline int resident_ctas(K kernel, int device, int smem) {
+    static thread_local int cache_dev = -1, cache_smem = -1, cache_n = 0;
+    if (cache_dev == device && cache_smem == smem) return cache_n;
+    int n = 0;
+    g_launch_step = "cudaOccupancyMaxActiveBlocksPerMultiprocessor";
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kGemvThreads, smem) != cudaSuccess) n = 1;
+    cache_dev = device;
+    cache_smem = smem;
+    cache_n = n < 1 ? 1 : n;
+    return cache_n;
+}
+
 template <class T, int NV, bool ISUMS, int MAXB>
 inline cudaError_t launch_gemv_inst(const GemvParams &p, const GemvBatch<MAXB> &b, const GemvLaunch &l,
                                     int device, cudaStream_t s) {
     auto k = gemv_kernel<T, NV, ISUMS, MAXB>;
     cudaError_t e = ensure_smem_attr<T, NV, ISUMS>(k, device, l.smem_optin);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, l.grid, kGemvThreads, l.smem, s, p, b);
+    // never more CTAs than fit at once: every CTA streams a fixed row range
+    int grid = l.grid;
+    const int cap = resident_ctas<T, NV, ISUMS>(k, device, l.smem) * l.sms;
+    if (grid > cap) grid = cap;
+    return launch_pdl(k, grid, kGemvThreads, l.smem, s, p, b);
 }
 
 template <class T, int NV>

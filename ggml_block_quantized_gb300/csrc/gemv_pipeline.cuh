@@ -43,13 +43,12 @@ namespace qg {
 constexpr int kConsumerWarps = 8;
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 16;
-constexpr int kRowsPerWarp = 2;  // rows a warp group takes per stage, processed interleaved
+constexpr int kRowsPerWarp = 2;  // rows a warp group takes per stage (its items are flattened over them)
 constexpr int kMaxBatch = 256;   // matrices per batched launch (their table is a kernel parameter)
-// Shared-memory header: kMaxStages full + kMaxStages empty mbarriers, then
-// the cross-warp partial sums [2][kConsumerWarps][kRowsPerWarp][kMaxNvec]
-// floats (split > 1).
-constexpr int kRedOffset = 2 * 8 * kMaxStages;
-constexpr int kHeaderBytes = ((kRedOffset + 2 * kConsumerWarps * kRowsPerWarp * kMaxNvec * 4) + 127) & ~127;
+// Shared memory: header (kMaxStages full + kMaxStages empty mbarriers) |
+// staged activations | f32 x buffer | cross-warp partial sums (split > 1:
+// [n_stages][kConsumerWarps][kRowsPerWarp][NV] floats) | ring of stages.
+constexpr int kHeaderBytes = 2 * 8 * kMaxStages;
 
 // One matrix of a launch.
 struct GemvMat {
@@ -80,7 +79,8 @@ struct GemvParams {
     int n_stages;        // ring depth (2..kMaxStages)
     int stage_bytes;     // bytes per ring slot, multiple of 16
     int act_bytes;       // bytes of staged activations, multiple of 16
-    int x_bytes;         // bytes of f32 x staged in shared memory (n_vec * n_in * 4), 0 without x
+    int x_bytes;         // bytes of the f32 x buffer (whole activation blocks), 0 without x
+    int red_bytes;       // bytes of the cross-warp partial sums (split > 1), else 0
 };
 
 // Walks a CTA's global rows [g, g1) as stages of at most R rows that never
@@ -112,25 +112,56 @@ __device__ __forceinline__ StageWalk cta_rows(const GemvParams &p) {
 }
 
 // ------------------------------------------------------------------------
-// Producer: lane 0 of the last warp.
+// Producer: lane 0 of the last warp. Besides streaming the stages it
+// finishes rows split across warps (split > 1): once a stage is consumed it
+// adds the warps' partial sums of each row in a fixed order and writes y, so
+// the consumer warps of a row never wait for one another.
 // ------------------------------------------------------------------------
-template <int MAXB>
+struct StageInfo {
+    int mat, r, rows;
+};
+
+template <int MAXB, int NV>
+__device__ __forceinline__ void finish_split_rows(const GemvParams &p, const GemvBatch<MAXB> &b, const float *red,
+                                                  int slot, const StageInfo &st) {
+    const int split = p.split;
+    const int groups = kConsumerWarps / split;
+    const GemvMat &mt = b.m[st.mat];
+    for (int ris = 0; ris < st.rows; ++ris) {
+        const int grp = ris % groups, i = ris / groups;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            float sum = 0.0f;
+            for (int q = 0; q < split; ++q)
+                sum += red[((slot * kConsumerWarps + grp * split + q) * kRowsPerWarp + i) * NV + v];
+            mt.y[static_cast<int64_t>(v) * mt.n_out + st.r + ris] = sum;
+        }
+    }
+}
+
+template <int MAXB, int NV, bool ISUMS>
 __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBatch<MAXB> &b, uint8_t *ring,
-                                              uint32_t bar_full0, uint32_t bar_empty0) {
+                                              const float *red, uint32_t bar_full0, uint32_t bar_empty0) {
     const uint64_t policy = l2_evict_first_policy();
     const int S = p.n_stages;
+    const bool reduce = !ISUMS && p.split > 1;
+    StageInfo info[kMaxStages];
     StageWalk walk = cta_rows(p);
     int mat, r, rows;
     int issued = 0;
+    bool ok = true;
     for (int k = 0; walk.next(b, p.n_mats, p.rows_per_stage, mat, r, rows); ++k) {
         const int slot = k % S;
         if (k >= S) {
             const uint32_t parity = static_cast<uint32_t>((k / S) & 1) ^ 1u;
             if (!mbar_wait_bounded(bar_empty0 + 8 * slot, parity)) {
                 record_error(p.err, kErrProducerWait);
+                ok = false;
                 break;
             }
+            if (reduce) finish_split_rows<MAXB, NV>(p, b, red, slot, info[slot]);
         }
+        info[slot] = StageInfo{mat, r, rows};
         const uint8_t *W = b.m[mat].W;
         const int64_t lim = (static_cast<int64_t>(b.m[mat].n_out) * p.row_bytes) & ~int64_t(15);
         const int64_t start = static_cast<int64_t>(r) * p.row_bytes;
@@ -146,13 +177,23 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBat
         if (bulk) bulk_copy_g2s(smem_addr(buf), W + a0, bulk, bar_full0 + 8 * slot, policy);
         ++issued;
     }
-    // Do not leave while copies into this CTA's shared memory are in flight.
+    // Do not leave while copies into this CTA's shared memory are in flight,
+    // then finish the last stages' split rows once they are consumed.
     for (int k = max(0, issued - S); k < issued; ++k) {
         const int slot = k % S;
         if (!mbar_wait_bounded(bar_full0 + 8 * slot, static_cast<uint32_t>((k / S) & 1))) {
             record_error(p.err, kErrDrainWait);
-            break;
+            return;
         }
+    }
+    if (!reduce || !ok) return;
+    for (int k = max(0, issued - S); k < issued; ++k) {
+        const int slot = k % S;
+        if (!mbar_wait_bounded(bar_empty0 + 8 * slot, static_cast<uint32_t>((k / S) & 1))) {
+            record_error(p.err, kErrDrainWait);
+            return;
+        }
+        finish_split_rows<MAXB, NV>(p, b, red, slot, info[slot]);
     }
 }
 
@@ -163,21 +204,30 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Activations of matrix `mat` into shared memory (all consumer threads).
+// Activations of one matrix into shared memory (all consumer threads). f32
+// x goes through a shared buffer of p.x_bytes, one chunk of whole
+// activation blocks at a time.
 template <class T, int NV>
 __device__ __forceinline__ void stage_activations(const GemvParams &p, const GemvMat &mt, uint8_t *act,
                                                   float *xbuf, int warp, int lane) {
     if (mt.x) {
-        // Copy x into shared memory through the load/store path (16 bytes a
-        // thread per instruction, all in flight at once) -- not through the
-        // bulk-copy engine, whose queue also carries weight prefetches --
-        // then quantize from there.
-        const int n16 = p.x_bytes / 16;
+        // Copy x through the load/store path (16 bytes a thread per
+        // instruction, all in flight at once) -- not through the bulk-copy
+        // engine, whose queue also carries weight prefetches -- then quantize
+        // from shared memory.
+        const int blocks = p.nb * NV;
+        const int chunk = p.x_bytes / (4 * T::kActValues);
         const uint32_t xs = smem_addr(xbuf);
-        for (int i = threadIdx.x; i < n16; i += kConsumerWarps * 32) cp_async_16(xs + 16 * i, mt.x + 4 * i);
-        cp_async_wait_all();
-        named_barrier(1, kConsumerWarps * 32);
-        T::stage_x(xbuf, act, p.nb, NV, warp, kConsumerWarps, lane);
+        for (int g0 = 0; g0 < blocks; g0 += chunk) {
+            const int count = min(chunk, blocks - g0);
+            const float *src = mt.x + static_cast<size_t>(g0) * T::kActValues;
+            const int n16 = count * T::kActValues / 4;
+            if (g0 > 0) named_barrier(1, kConsumerWarps * 32);  // the previous chunk is consumed
+            for (int i = threadIdx.x; i < n16; i += kConsumerWarps * 32) cp_async_16(xs + 16 * i, src + 4 * i);
+            cp_async_wait_all();
+            named_barrier(1, kConsumerWarps * 32);
+            T::stage_x(xs, act, g0, count, warp, kConsumerWarps, lane);
+        }
     } else {
         T::stage_act(mt.xq, act, p.nb, NV, threadIdx.x, kConsumerWarps * 32);
     }
@@ -197,8 +247,8 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     const uint32_t bar_empty0 = bar_full0 + 8 * kMaxStages;
     uint8_t *act = smem + kHeaderBytes;
     float *xbuf = reinterpret_cast<float *>(act + p.act_bytes);
-    uint8_t *ring = act + p.act_bytes + p.x_bytes;
-    float *red = reinterpret_cast<float *>(smem + kRedOffset);
+    float *red = reinterpret_cast<float *>(act + p.act_bytes + p.x_bytes);
+    uint8_t *ring = act + p.act_bytes + p.x_bytes + p.red_bytes;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -217,7 +267,7 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     pdl_allow_dependents();
 
     if (warp == kConsumerWarps) {
-        if (lane == 0) gemv_producer(p, b, ring, bar_full0, bar_empty0);
+        if (lane == 0) gemv_producer<MAXB, NV, ISUMS>(p, b, ring, red, bar_full0, bar_empty0);
         return;
     }
 
@@ -269,14 +319,28 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
 #pragma unroll
             for (int v = 0; v < NV; ++v) acc[i][v] = 0.0f;
         if (!failed && has[0]) {
-            for (int it = lane; it < ((items + 31) & ~31); it += 32) {
-                const bool active = it < items;
-                const int blk = active ? b0 + it / T::kLanesPerBlock : b1 - 1;
-                const int sub = it % T::kLanesPerBlock;
+            // The warp's items over its rows, flattened (row i, item j), so
+            // the lanes stay busy whatever the row length.
+            const int n_rows = has[1] ? 2 : 1;
+            const int total = items * n_rows;
+            const uint32_t rowa0 = smem_addr(rowp[0]), rowa1 = smem_addr(rowp[1]);
+            const uint32_t acta = smem_addr(act);
+            for (int f = lane; f < ((total + 31) & ~31); f += 32) {
+                const bool active = f < total;
+                const int i = active && f >= items ? 1 : 0;
+                const int j = active ? f - i * items : 0;
+                const int blk = b0 + j / T::kLanesPerBlock;
+                const int sub = j % T::kLanesPerBlock;
+                float part[NV];
 #pragma unroll
-                for (int i = 0; i < kRowsPerWarp; ++i)
-                    T::template item<NV, ISUMS>(rowp[i], blk, sub, active && has[i], act, p.nb, acc[i],
-                                                isum_row[i], isum_vstride);
+                for (int v = 0; v < NV; ++v) part[v] = 0.0f;
+                T::template item<NV, ISUMS>(i ? rowa1 : rowa0, blk, sub, active, acta, p.nb, part,
+                                            i ? isum_row[1] : isum_row[0], isum_vstride);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    acc[0][v] += i ? 0.0f : part[v];
+                    acc[1][v] += i ? part[v] : 0.0f;
+                }
             }
         }
         if (!ISUMS && has[0]) {
@@ -294,28 +358,13 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
                         for (int v = 0; v < NV; ++v) mt.y[static_cast<int64_t>(v) * mt.n_out + row] = acc[i][v];
                     }
                 }
-            } else {
-                float *rp = red + (((k & 1) * kConsumerWarps + warp) * kRowsPerWarp) * NV;
-                if (lane == 0) {
+            } else if (lane == 0) {
+                // partial sums of this warp's part of its rows; the producer adds them up
+                float *rp = red + ((slot * kConsumerWarps + warp) * kRowsPerWarp) * NV;
 #pragma unroll
-                    for (int i = 0; i < kRowsPerWarp; ++i)
+                for (int i = 0; i < kRowsPerWarp; ++i)
 #pragma unroll
-                        for (int v = 0; v < NV; ++v) rp[i * NV + v] = acc[i][v];
-                }
-                named_barrier(2 + grp, split * 32);
-                if (part == 0 && lane == 0 && !failed) {
-#pragma unroll
-                    for (int i = 0; i < kRowsPerWarp; ++i) {
-                        if (!has[i]) continue;
-                        const int row = r + grp + groups * i;
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            float sum = 0.0f;
-                            for (int q = 0; q < split; ++q) sum += rp[(q * kRowsPerWarp + i) * NV + v];
-                            mt.y[static_cast<int64_t>(v) * mt.n_out + row] = sum;
-                        }
-                    }
-                }
+                    for (int v = 0; v < NV; ++v) rp[i * NV + v] = acc[i][v];
             }
         }
         __syncwarp();

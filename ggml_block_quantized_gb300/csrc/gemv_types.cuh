@@ -55,12 +55,11 @@ __device__ __forceinline__ float group_max(float v) {
     return v;
 }
 
-// Eight f32 values from shared memory (the bulk-copied activations).
-__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
-    const float4 a = reinterpret_cast<const float4 *>(p)[0];
-    const float4 b = reinterpret_cast<const float4 *>(p)[1];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+// Eight f32 values at a shared-memory address (the staged activations).
+__device__ __forceinline__ void load8(uint32_t a, float (&v)[8]) {
+    const uint4 x = ld_s128(a), y = ld_s128(a + 16);
+    v[0] = __uint_as_float(x.x); v[1] = __uint_as_float(x.y); v[2] = __uint_as_float(x.z); v[3] = __uint_as_float(x.w);
+    v[4] = __uint_as_float(y.x); v[5] = __uint_as_float(y.y); v[6] = __uint_as_float(y.z); v[7] = __uint_as_float(y.w);
 }
 
 // Codes of 8 values with the inverse scale id, packed 4 per word; returns
@@ -82,13 +81,25 @@ __device__ __forceinline__ uint32_t pack16(int lo, int hi) {
 }
 
 // ========================================================================
+// Staging interfaces shared by all types:
+//   stage_act(xq, act, nb, nv, tid, nthr): records from byte-exact blocks.
+//   stage_x(xs, act, g0, count, warp, nwarps, lane): records for activation
+//     blocks g0 .. g0+count-1 (block index g = v * nb + b) from their f32
+//     values at shared address xs (value 0 of block g0).
+// Item interface: item<NV, ISUMS>(rowa, b, sub, active, acta, nb, acc,
+//   isum_row, isum_vstride) adds the block's float terms of one weight row
+//   (shared address rowa) to acc[v], or writes its exact sums.
+// ========================================================================
+
+// ------------------------------------------------------------------------
 // Q8_0-paired types (Q8_0, Q4_0): activations staged as 48-byte records
 // per (vector, block): qs[32] | f32 d_x | int32 sum(qs) | 8 pad bytes.
 // Record stride 48 B makes 8 consecutive blocks' 128-bit loads hit 8
 // disjoint bank quads.
-// ========================================================================
+// ------------------------------------------------------------------------
 struct ActQ8_0 {
     static constexpr int kRecord = 48;
+    static constexpr int kValues = 32;  // f32 values per activation block
     static size_t bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * kRecord; }
 
     // From byte-exact Q8_0 blocks: xq [nv][nb] x 34 B (2-byte aligned each).
@@ -113,16 +124,15 @@ struct ActQ8_0 {
         }
     }
 
-    // From f32 x [nv][nb * 32] in shared memory: 4 lanes per 32-value block, 8 blocks per warp step.
-    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
-        const int n = nb * nv;
-        for (int base = warp * 8; base < n; base += nwarps * 8) {
+    // From f32 values in shared memory: 4 lanes per 32-value block, 8 blocks per warp step.
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        for (int base = warp * 8; base < count; base += nwarps * 8) {
             const int i = base + (lane >> 2);
             const int part = lane & 3;
-            const bool ok = i < n;
+            const bool ok = i < count;
             float v[8];
             if (ok) {
-                load8(x + static_cast<size_t>(i) * 32 + 8 * part, v);
+                load8(xs + 4u * (32u * i + 8u * part), v);
             } else {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) v[k] = 0.0f;
@@ -136,7 +146,7 @@ struct ActQ8_0 {
             uint32_t w[2];
             int sum = group_sum<4>(codes8(v, id, -128, 127, w));
             if (ok) {
-                uint8_t *rec = act + static_cast<size_t>(i) * kRecord;
+                uint8_t *rec = act + static_cast<size_t>(g0 + i) * kRecord;
                 reinterpret_cast<uint2 *>(rec)[part] = make_uint2(w[0], w[1]);
                 if (part == 0) {
                     const float dx = __half2float(__float2half_rn(d));  // the stored f16 scale
@@ -150,27 +160,27 @@ struct ActQ8_0 {
 
 struct TypeQ8_0 {
     static constexpr int kBlockElems = 32, kBlockBytes = 34, kLanesPerBlock = 1, kSums = 1;
+    static constexpr int kActValues = ActQ8_0::kValues;
     static size_t act_bytes(int nb, int nv) { return ActQ8_0::bytes(nb, nv); }
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
-        ActQ8_0::stage_x(x, act, nb, nv, warp, nwarps, lane);
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        ActQ8_0::stage_x(xs, act, g0, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
-    __device__ static void item(const uint8_t *rowp, int b, int /*sub*/, bool active, const uint8_t *act,
-                                int nb, float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
-        const uint8_t *blk = rowp + b * kBlockBytes;
-        const float dw = f16_bits_to_f32(lds_u16(blk));
+    __device__ static void item(uint32_t rowa, int b, int /*sub*/, bool active, uint32_t acta, int nb,
+                                float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;
+        const float dw = f16_bits_to_f32(ld_s16(blk));
         uint32_t w[8];
-        lds_words_a2<8>(blk + 2, w);
+        ld_words_a2<8>(blk + 2, w);
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const uint8_t *rec = act + (static_cast<size_t>(v) * nb + b) * ActQ8_0::kRecord;
-            const uint4 a0 = reinterpret_cast<const uint4 *>(rec)[0];
-            const uint4 a1 = reinterpret_cast<const uint4 *>(rec)[1];
-            const float dx = reinterpret_cast<const float *>(rec)[8];
+            const uint32_t rec = acta + (static_cast<uint32_t>(v) * nb + b) * ActQ8_0::kRecord;
+            const uint4 a0 = ld_s128(rec), a1 = ld_s128(rec + 16);
+            const float dx = __uint_as_float(ld_s32(rec + 32));
             int s = dp4a(w[0], a0.x, 0);
             s = dp4a(w[1], a0.y, s);
             s = dp4a(w[2], a0.z, s);
@@ -190,21 +200,22 @@ struct TypeQ8_0 {
 
 struct TypeQ4_0 {
     static constexpr int kBlockElems = 32, kBlockBytes = 18, kLanesPerBlock = 1, kSums = 1;
+    static constexpr int kActValues = ActQ8_0::kValues;
     static size_t act_bytes(int nb, int nv) { return ActQ8_0::bytes(nb, nv); }
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
-        ActQ8_0::stage_x(x, act, nb, nv, warp, nwarps, lane);
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        ActQ8_0::stage_x(xs, act, g0, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
-    __device__ static void item(const uint8_t *rowp, int b, int /*sub*/, bool active, const uint8_t *act,
-                                int nb, float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
-        const uint8_t *blk = rowp + b * kBlockBytes;
-        const float dw = f16_bits_to_f32(lds_u16(blk));
+    __device__ static void item(uint32_t rowa, int b, int /*sub*/, bool active, uint32_t acta, int nb,
+                                float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;
+        const float dw = f16_bits_to_f32(ld_s16(blk));
         uint32_t q[4];
-        lds_words_a2<4>(blk + 2, q);
+        ld_words_a2<4>(blk + 2, q);
         uint32_t lo[4], hi[4];  // codes of elements 4i.. and 16+4i..
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -213,10 +224,8 @@ struct TypeQ4_0 {
         }
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const uint8_t *rec = act + (static_cast<size_t>(v) * nb + b) * ActQ8_0::kRecord;
-            const uint4 a0 = reinterpret_cast<const uint4 *>(rec)[0];
-            const uint4 a1 = reinterpret_cast<const uint4 *>(rec)[1];
-            const uint4 ex = reinterpret_cast<const uint4 *>(rec)[2];
+            const uint32_t rec = acta + (static_cast<uint32_t>(v) * nb + b) * ActQ8_0::kRecord;
+            const uint4 a0 = ld_s128(rec), a1 = ld_s128(rec + 16), ex = ld_s128(rec + 32);
             int s = dp4a(lo[0], a0.x, 0);
             s = dp4a(lo[1], a0.y, s);
             s = dp4a(lo[2], a0.z, s);
@@ -235,15 +244,14 @@ struct TypeQ4_0 {
     }
 };
 
-// ========================================================================
-// Q8_K from f32: one warp per 256-value block, lane l owns values
-// 8l..8l+7. Returns the codes (2 words), the 16-value sum of lanes
+// ------------------------------------------------------------------------
+// Q8_K from f32 in shared memory: one warp per 256-value block, lane l owns
+// values 8l..8l+7. Returns the codes (2 words), the 16-value sum of lanes
 // (2k, 2k+1) in every lane of the pair, and d.
-// ========================================================================
-__device__ __forceinline__ void quantize_q8_k_lane(const float *blk, int lane, uint32_t (&w)[2], int &sum16,
-                                                   float &d) {
+// ------------------------------------------------------------------------
+__device__ __forceinline__ void quantize_q8_k_lane(uint32_t blk, int lane, uint32_t (&w)[2], int &sum16, float &d) {
     float v[8];
-    load8(blk + 8 * lane, v);
+    load8(blk + 32u * lane, v);
     float a = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(v[k]));
@@ -254,16 +262,17 @@ __device__ __forceinline__ void quantize_q8_k_lane(const float *blk, int lane, u
     sum16 = s + __shfl_xor_sync(0xffffffffu, s, 1);
 }
 
-// ========================================================================
+// ------------------------------------------------------------------------
 // Q4_K. Two lanes per block: lane h takes half h (values 128h..128h+127,
 // sub-blocks 4h..4h+3, qs bytes 64h..64h+63). Activations staged per
 // (vector, block, half) as a 144-byte record:
 //   codes[128] | int16 bsum32[4] (sub-blocks 4h..4h+3) | f32 d_x | pad
 // where bsum32(j) = bsums[2j] + bsums[2j+1]. A 144-byte stride (36 words)
 // puts 8 consecutive records' 128-bit loads in 8 disjoint bank quads.
-// ========================================================================
+// ------------------------------------------------------------------------
 struct TypeQ4_K {
     static constexpr int kBlockElems = 256, kBlockBytes = 144, kLanesPerBlock = 2, kSums = 2;
+    static constexpr int kActValues = 256;
     static constexpr int kRecord = 144;
     static size_t act_bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * 2 * kRecord; }
 
@@ -292,16 +301,15 @@ struct TypeQ4_K {
         }
     }
 
-    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
-        const int n = nb * nv;
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
         const int h = lane >> 4;
-        for (int i = warp; i < n; i += nwarps) {
+        for (int i = warp; i < count; i += nwarps) {
             uint32_t w[2];
             int s16;
             float d;
-            quantize_q8_k_lane(x + static_cast<size_t>(i) * 256, lane, w, s16, d);
+            quantize_q8_k_lane(xs + 1024u * i, lane, w, s16, d);
             const int s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 2);  // sub-block lane/4
-            uint8_t *rec = act + (static_cast<size_t>(i) * 2 + h) * kRecord;
+            uint8_t *rec = act + (static_cast<size_t>(g0 + i) * 2 + h) * kRecord;
             reinterpret_cast<uint2 *>(rec)[lane & 15] = make_uint2(w[0], w[1]);
             if ((lane & 3) == 0) reinterpret_cast<int16_t *>(rec + 128)[(lane >> 2) & 3] = static_cast<int16_t>(s32);
             if ((lane & 15) == 0) reinterpret_cast<uint2 *>(rec + 136)[0] = make_uint2(__float_as_uint(d), 0u);
@@ -309,10 +317,10 @@ struct TypeQ4_K {
     }
 
     template <int NV, bool ISUMS>
-    __device__ static void item(const uint8_t *rowp, int b, int h, bool active, const uint8_t *act, int nb,
+    __device__ static void item(uint32_t rowa, int b, int h, bool active, uint32_t acta, int nb,
                                 float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
-        const uint8_t *blk = rowp + b * kBlockBytes;  // 16-byte aligned (144 = 9 x 16)
-        const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;  // 16-byte aligned
+        const uint4 hdr = ld_s128(blk);
         const float dw = f16_bits_to_f32(hdr.x);
         const float dmin = f16_bits_to_f32(hdr.x >> 16);
         // 6-bit scales and mins of sub-blocks 4h..4h+3, one per byte.
@@ -324,24 +332,23 @@ struct TypeQ4_K {
         const uint32_t M = h == 0 ? (hdr.z & 0x3F3F3F3Fu)
                                   : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
         uint32_t q[16];
-        const uint4 *qp = reinterpret_cast<const uint4 *>(blk + 16 + 64 * h);
+        const uint32_t qa = blk + 16u + 64u * h;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint4 t = qp[j];
+            const uint4 t = ld_s128(qa + 16u * j);
             q[4 * j] = t.x; q[4 * j + 1] = t.y; q[4 * j + 2] = t.z; q[4 * j + 3] = t.w;
         }
         const int sc0 = SC & 0xFF, sc1 = (SC >> 8) & 0xFF, sc2 = (SC >> 16) & 0xFF, sc3 = SC >> 24;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const uint4 *rec = reinterpret_cast<const uint4 *>(
-                act + ((static_cast<size_t>(v) * nb + b) * 2 + h) * kRecord);
+            const uint32_t rec = acta + ((static_cast<uint32_t>(v) * nb + b) * 2 + h) * kRecord;
             uint32_t a[32];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint4 t = rec[j];
+                const uint4 t = ld_s128(rec + 16u * j);
                 a[4 * j] = t.x; a[4 * j + 1] = t.y; a[4 * j + 2] = t.z; a[4 * j + 3] = t.w;
             }
-            const uint4 ex = rec[8];
+            const uint4 ex = ld_s128(rec + 128);
             int d0 = 0, d1 = 0, d2 = 0, d3 = 0;  // d1, d3 carry a factor 16
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -368,7 +375,7 @@ struct TypeQ4_K {
     }
 };
 
-// ========================================================================
+// ------------------------------------------------------------------------
 // Q6_K. Four lanes per block: lane sub = 2h + p takes half h and the 16
 // positions l = 16p..16p+15 of each of the four 32-value rows k, i.e. the
 // 16-value sub-blocks j_k = 8h + 2k + p (k = 0..3). Activations staged per
@@ -377,9 +384,10 @@ struct TypeQ4_K {
 //   int16 bsums[j_0..j_3] | f32 d_x | pad
 // An 80-byte stride (20 words) puts 8 consecutive records' 128-bit loads in
 // 8 disjoint bank quads. The -32 offset of q is applied through the bsums.
-// ========================================================================
+// ------------------------------------------------------------------------
 struct TypeQ6_K {
     static constexpr int kBlockElems = 256, kBlockBytes = 210, kLanesPerBlock = 4, kSums = 1;
+    static constexpr int kActValues = 256;
     static constexpr int kRecord = 80;
     static size_t act_bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * 4 * kRecord; }
 
@@ -404,17 +412,16 @@ struct TypeQ6_K {
         }
     }
 
-    __device__ static void stage_x(const float *x, uint8_t *act, int nb, int nv, int warp, int nwarps, int lane) {
-        const int n = nb * nv;
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
         // lane l holds values 8l..8l+7: h = l/16, k = (l%16)/4, p = (l%4)/2
         const int h = lane >> 4, k = (lane >> 2) & 3, p = (lane >> 1) & 1;
         const int sub = 2 * h + p;
-        for (int i = warp; i < n; i += nwarps) {
+        for (int i = warp; i < count; i += nwarps) {
             uint32_t w[2];
             int s16;
             float d;
-            quantize_q8_k_lane(x + static_cast<size_t>(i) * 256, lane, w, s16, d);
-            uint8_t *rec = act + (static_cast<size_t>(i) * 4 + sub) * kRecord;
+            quantize_q8_k_lane(xs + 1024u * i, lane, w, s16, d);
+            uint8_t *rec = act + (static_cast<size_t>(g0 + i) * 4 + sub) * kRecord;
             reinterpret_cast<uint2 *>(rec + 16 * k)[lane & 1] = make_uint2(w[0], w[1]);
             if ((lane & 1) == 0) reinterpret_cast<int16_t *>(rec + 64)[k] = static_cast<int16_t>(s16);
             if (k == 0 && (lane & 1) == 0) reinterpret_cast<uint2 *>(rec + 72)[0] = make_uint2(__float_as_uint(d), 0u);
@@ -422,16 +429,16 @@ struct TypeQ6_K {
     }
 
     template <int NV, bool ISUMS>
-    __device__ static void item(const uint8_t *rowp, int b, int sub, bool active, const uint8_t *act, int nb,
+    __device__ static void item(uint32_t rowa, int b, int sub, bool active, uint32_t acta, int nb,
                                 float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
-        const uint8_t *blk = rowp + b * kBlockBytes;  // 2-byte aligned
-        const int h = sub >> 1, p = sub & 1;
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;  // 2-byte aligned
+        const uint32_t h = static_cast<uint32_t>(sub) >> 1, p = static_cast<uint32_t>(sub) & 1u;
         uint32_t ql0[4], ql1[4], qh[4], scw[2];
-        lds_words_a2<4>(blk + 64 * h + 16 * p, ql0);
-        lds_words_a2<4>(blk + 64 * h + 32 + 16 * p, ql1);
-        lds_words_a2<4>(blk + 128 + 32 * h + 16 * p, qh);
-        lds_words_a2<2>(blk + 192 + 8 * h, scw);  // scales[8h .. 8h+7]
-        const float dw = f16_bits_to_f32(lds_u16(blk + 208));
+        ld_words_a2<4>(blk + 64u * h + 16u * p, ql0);
+        ld_words_a2<4>(blk + 64u * h + 32u + 16u * p, ql1);
+        ld_words_a2<4>(blk + 128u + 32u * h + 16u * p, qh);
+        ld_words_a2<2>(blk + 192u + 8u * h, scw);  // scales[8h .. 8h+7]
+        const float dw = f16_bits_to_f32(ld_s16(blk + 208u));
         // scales of sub-blocks 8h + 2k + p, k = 0..3, as 4 signed bytes
         const uint32_t SC = __byte_perm(scw[0], scw[1], p ? 0x7531u : 0x6420u);
         const int sc0 = sbyte(SC, 0), sc1 = sbyte(SC, 1), sc2 = sbyte(SC, 2), sc3 = sbyte(SC, 3);
@@ -445,18 +452,17 @@ struct TypeQ6_K {
         }
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const uint4 *rec = reinterpret_cast<const uint4 *>(
-                act + ((static_cast<size_t>(v) * nb + b) * 4 + sub) * kRecord);
+            const uint32_t rec = acta + ((static_cast<uint32_t>(v) * nb + b) * 4 + sub) * kRecord;
             int dk[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint4 a = rec[k];
+                const uint4 a = ld_s128(rec + 16u * k);
                 int s = dp4a(qv[k][0], a.x, 0);
                 s = dp4a(qv[k][1], a.y, s);
                 s = dp4a(qv[k][2], a.z, s);
                 dk[k] = dp4a(qv[k][3], a.w, s);
             }
-            const uint4 ex = rec[4];
+            const uint4 ex = ld_s128(rec + 64u);
             int s = sc0 * dk[0] + sc1 * dk[1] + sc2 * dk[2] + sc3 * dk[3];
             s -= 32 * dp2a_hi_ss(ex.y, SC, dp2a_lo_ss(ex.x, SC, 0));
             if (ISUMS) {

@@ -149,6 +149,40 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 }
 
 // ------------------------------------------------ shared-memory word reads
+// Loads from 32-bit shared-memory addresses (no generic-address arithmetic).
+__device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_s16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_s64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 ld_s128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+// N consecutive 32-bit words starting at a 2-byte-aligned shared address.
+template <int N>
+__device__ __forceinline__ void ld_words_a2(uint32_t a, uint32_t (&out)[N]) {
+    const uint32_t base = a & ~3u;
+    const uint32_t sh = (a & 3u) * 8u;  // 0 or 16
+    uint32_t raw[N + 1];
+#pragma unroll
+    for (int i = 0; i <= N; ++i) raw[i] = ld_s32(base + 4 * i);
+#pragma unroll
+    for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+}
+
 // Four bytes starting at a 2-byte-aligned shared-memory address.
 __device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t *p) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
