@@ -104,6 +104,32 @@ int tune_ring_kib() {
     return v;
 }
 
+// Vectors from which Q4_K / Q6_K products run on the tensor cores.
+int tune_mma_min_nvec() {
+    static const int v = env_int("QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1);
+    return v;
+}
+
+// Tensor-core plan overrides: activation source (0 = automatic; 1 = a
+// shared-memory panel even where registers would do; 8 = the biased-int8
+// panel) and an upper bound on blocks per chunk of the panel kernel (0 =
+// none).
+int tune_mma_panel() {
+    static const int v = env_int("QG_MMA_PANEL", 0, 0, 16);
+    return v;
+}
+int tune_mma_kb() {
+    static const int v = env_int("QG_MMA_KB", 0, 0, 4096);
+    return v;
+}
+
+bool mma_type(int type) { return type == QG_Q4_K || type == QG_Q6_K; }
+
+// Whether a product (not the exact-block-sum diagnostic) takes the tensor-core
+// kernel; it reads activations from the workspace, so such calls never
+// quantize x inside the GEMV prologue.
+bool mma_preferred(int type, int64_t n_vec) { return mma_type(type) && n_vec >= tune_mma_min_nvec(); }
+
 size_t act_smem_bytes(int type, int nb, int nv) {
     switch (type) {
     case QG_Q8_0: return TypeQ8_0::act_bytes(nb, nv);
@@ -215,6 +241,130 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
     return QG_ERR_SHAPE;
 }
 
+// Geometry of a tensor-core launch. A stage is 16 rows in 4 groups of 4
+// whose starts are 32 modulo 128 bytes apart (one bulk copy per group when
+// the stage spans whole rows). When a whole row has at most 16 blocks, it is
+// one stage and 8 consumer warps keep their activation fragments in
+// registers (nothing but the ring in shared memory). Otherwise 16 warps read
+// them from a shared-memory panel (f16 when it fits, else biased int8), the
+// row is split into chunks of kb blocks, and among the shapes that fit the
+// plan keeps the warps busiest, then a ring of at least 3 stages, then the
+// f16 panel, then the longer chunk. Partial-output buffers are doubled when
+// that keeps the ring as deep. Returns QG_ERR_SHAPE when nothing fits (the
+// caller then uses the __dp4a kernel).
+namespace {
+
+// Slot layout for kb blocks per chunk of a row of nb blocks of `bytes` each.
+void mma_slot_layout(int nb, int kb, int bytes, int *rpitch, int *gpitch) {
+    const bool contig = kb == nb;
+    const int64_t row = static_cast<int64_t>(nb) * bytes;
+    *rpitch = contig ? static_cast<int>(row) : static_cast<int>(round16(static_cast<size_t>(kb) * bytes + 32));
+    int gp = contig ? static_cast<int>(round16(static_cast<size_t>(4 * row + 32))) : 4 * *rpitch;
+    *gpitch = (gp + 95) / 128 * 128 + 32;  // the smallest value >= gp that is 32 mod 128
+}
+
+// Ring depth and partial-buffer count for `stage` bytes per slot next to
+// `fixed` bytes; false when not even two stages fit.
+bool mma_ring(int64_t smem_limit, int64_t fixed, int64_t stage, int nw, int *S, int *red_slots) {
+    const int64_t red = mma_red_bytes(nw);
+    if (fixed + 2 * (stage + red) > smem_limit) return false;
+    int64_t s1 = (smem_limit - fixed) / (stage + red);
+    int64_t s2 = (smem_limit - fixed) / (stage + 2 * red);
+    if (s1 > kMmaMaxStages) s1 = kMmaMaxStages;
+    if (s2 > kMmaMaxStages) s2 = kMmaMaxStages;
+    const bool dbl = s2 >= 2 && s2 >= (s1 < 3 ? s1 : 3);
+    *S = static_cast<int>(dbl ? s2 : s1);
+    *red_slots = dbl ? 2 * *S : *S;
+    return true;
+}
+
+}  // namespace
+
+int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, int smem_limit, MmaParams *p,
+                  MmaLaunch *l) {
+    int elems, bytes;
+    block_info(type, &elems, &bytes);
+    const int64_t nb64 = n_in / elems;
+    if (nb64 < 1 || nb64 > 4096 || total_tiles < 1) return QG_ERR_SHAPE;
+    const int nb = static_cast<int>(nb64);
+    MmaParams bp = {};
+    MmaLaunch bl = {};
+    bp.row_bytes = nb64 * bytes;
+    bp.total_tiles = total_tiles;
+    bp.nb = nb;
+    bp.nv = nv;
+    bool found = false;
+    const int force = tune_mma_panel();  // 0 automatic, 1 a panel, 8 the int8 panel
+    if (force == 0 && nb <= 16) {
+        int rp, gp, S, R;
+        mma_slot_layout(nb, nb, bytes, &rp, &gp);
+        if (mma_ring(smem_limit, kMmaHeaderBytes, 4 * static_cast<int64_t>(gp), 8, &S, &R)) {
+            bp.kb = nb;
+            bp.n_chunks = 1;
+            bp.rpitch = rp;
+            bp.gpitch = gp;
+            bp.contig = 1;
+            bp.stage_bytes = 4 * gp;
+            bp.n_stages = S;
+            bp.red_slots = R;
+            bp.rec_bytes = 0;
+            bp.panel_bytes = 0;
+            bl.smem = kMmaHeaderBytes + S * bp.stage_bytes + R * mma_red_bytes(8);
+            bl.mode = kMmaRegs;
+            bl.warps = 8;
+            found = true;
+        }
+    }
+    if (!found) {
+        constexpr int W = 16;
+        long best = -1;
+        const int cands[6] = {nb, 32, 24, 16, 8, 4};
+        for (int f = 0; f < 2; ++f) {
+            const bool b16 = f == 0;
+            if (b16 && force == 8) continue;
+            const int rec = mma_rec_bytes(b16);
+            const int64_t panel = static_cast<int64_t>(nb) * rec;
+            for (int ci = 0; ci < 6; ++ci) {
+                const int kb = cands[ci];
+                if (kb > nb || (ci > 0 && kb == nb)) continue;
+                if (tune_mma_kb() > 0 && kb > tune_mma_kb()) continue;
+                int rp, gp, S, R;
+                mma_slot_layout(nb, kb, bytes, &rp, &gp);
+                const int64_t stage = 4 * static_cast<int64_t>(gp);
+                const int64_t fixed = kMmaHeaderBytes + panel;
+                if (!mma_ring(smem_limit, fixed, stage, W, &S, &R)) continue;
+                const int n_chunks = (nb + kb - 1) / kb;
+                const int last = nb - (n_chunks - 1) * kb;
+                const int64_t slots = static_cast<int64_t>(n_chunks - 1) * ((kb + W - 1) / W * W) + (last + W - 1) / W * W;
+                const long eff = static_cast<long>(50.0 * nb / slots + 0.5);
+                const long score = eff * 100000 + (S >= 3 ? 10000 : 0) + (b16 ? 1000 : 0) + kb;
+                if (score <= best) continue;
+                best = score;
+                bp.kb = kb;
+                bp.n_chunks = n_chunks;
+                bp.rpitch = rp;
+                bp.gpitch = gp;
+                bp.contig = kb == nb ? 1 : 0;
+                bp.stage_bytes = static_cast<int>(stage);
+                bp.n_stages = S;
+                bp.red_slots = R;
+                bp.rec_bytes = rec;
+                bp.panel_bytes = static_cast<int>(panel);
+                bl.smem = static_cast<int>(fixed + S * stage + static_cast<int64_t>(R) * mma_red_bytes(W));
+                bl.mode = b16 ? kMmaPanel16 : kMmaPanel8;
+                bl.warps = W;
+                found = true;
+            }
+        }
+    }
+    if (!found) return QG_ERR_SHAPE;
+    *p = bp;
+    bl.grid = static_cast<int>(total_tiles < sms ? total_tiles : sms);
+    bl.smem_optin = smem_limit;
+    *l = bl;
+    return QG_OK;
+}
+
 cudaError_t launch_gemv(int type, const GemvParams &p, const GemvMat *mats, int n, int nv, bool isums,
                         const GemvLaunch &l, int device, cudaStream_t s) {
     switch (type) {
@@ -286,6 +436,34 @@ int run_gemv_mats(int type, GemvMat *mats, int n, int64_t n_in, int64_t n_vec, s
         total += mats[i].n_out;
     }
     if (total == 0) return QG_OK;
+    if (!isums && x_bytes == 0 && mma_preferred(type, n_vec)) {
+        // several vectors: the tensor-core kernel, when its shapes fit
+        MmaMat mm[QG_MAX_BATCH];
+        int64_t tiles = 0;
+        for (int i = 0; i < n; ++i) {
+            mm[i] = MmaMat{};
+            mm[i].W = mats[i].W;
+            mm[i].xq = mats[i].xq;
+            mm[i].y = mats[i].y;
+            mm[i].n_out = mats[i].n_out;
+            mm[i].tile_base = tiles;
+            tiles += (mats[i].n_out + kMmaTileRows - 1) / kMmaTileRows;
+        }
+        MmaParams mp = {};
+        MmaLaunch ml = {};
+        if (plan_gemv_mma(type, tiles, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &mp, &ml) == QG_OK) {
+            mp.err = dev.err;
+            mp.n_mats = n;
+            cudaError_t e = launch_gemv_mma(type, mp, mm, n, ml, dev.device, s);
+            if (e != cudaSuccess) {
+                char where[160];
+                std::snprintf(where, sizeof where, "%s; tensor-core grid %d block %d smem %d stages %d", g_launch_step,
+                              ml.grid, (ml.warps + 1) * 32, ml.smem, mp.n_stages);
+                return cuda_fail(e, where);
+            }
+            return QG_OK;
+        }
+    }
     GemvParams p = {};
     GemvLaunch l = {};
     int st = plan_gemv(type, total, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, x_bytes, &p, &l);
@@ -494,7 +672,7 @@ int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     // the product's shape limits are checked before anything is enqueued
     GemvParams probe = {};
     GemvLaunch pl = {};
-    const bool fused = fused_quantization(n_in, n_vec);
+    const bool fused = fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec);
     st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
                    fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &probe, &pl);
     if (st != QG_OK) return st;
@@ -512,7 +690,7 @@ size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int 
     if (n_mats < 1 || n_mats > QG_MAX_BATCH) return 0;
     const size_t one = qgemv_workspace_bytes(type, n_in, n_vec);
     if (one == 0) return 0;
-    return fused_quantization(n_in, n_vec) ? 16 : one * static_cast<size_t>(n_mats);
+    return fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec) ? 16 : one * static_cast<size_t>(n_mats);
 }
 
 int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, int64_t n_vec, void *workspace,
@@ -534,7 +712,7 @@ int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, i
         }
         return QG_OK;
     }
-    const bool fused = fused_quantization(n_in, n_vec);
+    const bool fused = fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec);
     const size_t need = qgemv_batched_workspace_bytes(type, n_in, n_vec, n_mats);
     if (!fused && (!workspace || workspace_bytes < need)) return QG_ERR_WORKSPACE;
     if (workspace && !aligned16(workspace)) return QG_ERR_ALIGN;

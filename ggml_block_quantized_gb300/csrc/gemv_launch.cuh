@@ -6,6 +6,7 @@
 
 #include <atomic>
 
+#include "gemv_mma_launch.cuh"
 #include "gemv_pipeline.cuh"
 #include "gemv_types.cuh"
 

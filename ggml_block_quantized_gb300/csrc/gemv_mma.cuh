@@ -1,0 +1,891 @@
+// gemv_mma.cuh - the block-quantized GEMV for several vectors on the tensor
+// cores: Y[v][o] = sum over the blocks of row o of (exact sub-block sums) x
+// (block scales), for Q4_K and Q6_K weights with Q8_K activations
+// ("Quantization" (rml), Quantized dot products, K-quants; "How to Read
+// ggml/GGUF" (sh), block layouts).
+//
+// Why tensor cores here. With n_vec vectors every weight code meets n_vec
+// activation codes: the product is the dense contraction
+// [16 rows x n_in] x [n_in x 8 vectors] per tile of rows, and the __dp4a form
+// spends n_vec multiply instructions and activation loads per weight word.
+// mma.sync m16n8k16 (f16 in, f32 accumulate) takes 16 rows x 16 codes x 8
+// vectors per instruction. It stays exact:
+//  * a weight code q (4 or 6 bits, unsigned) enters as the f16 whose bit
+//    pattern is q -- the subnormal q * 2^-24 -- built from the block bytes
+//    by one mask (Q4_K's high nibbles give 16q * 2^-24);
+//  * an activation code (-127..127) is an exact f16;
+//  * every product and every partial sum of one sub-block is an integer
+//    times 2^-24 below 2^0, exact in the f32 accumulator;
+// so the accumulator of a sub-block (32 codes for Q4_K, 16 for Q6_K) is its
+// exact int32 sum times 2^-24 (times 16 for Q4_K odd sub-blocks). The
+// sub-block scales are then applied in f32 (an exact small integer times the
+// accumulator), the minimum / offset terms come from one more small mma over
+// the Q8_K block sums (bsums), and only d_w, dmin_w and d_x are inexact
+// floats -- the same arithmetic as the scalar definition up to f32 rounding.
+//
+// Structure (one CTA = 1 producer warp + NW consumer warps, one CTA per SM):
+//  * Work unit: a tile of 16 consecutive rows of one matrix. A CTA owns a
+//    balanced contiguous range of the launch's tiles (matrices of a batch
+//    numbered consecutively). Each tile is streamed as one or more chunks of
+//    kb blocks of its 16 rows ("stages").
+//  * The producer warp copies each stage into a ring slot with 1-D bulk
+//    async copies (TMA engine, non-tensor form). A slot holds 4 groups of 4
+//    stage rows, group q at q * gpitch, row j of a group at j * rpitch. When
+//    a stage spans whole rows, a group's 4 rows are contiguous in W and
+//    travel as one copy (4 requests a stage; each bulk request costs the
+//    issuing thread on the order of 100 cycles); otherwise each row segment
+//    is its own copy. gpitch is 32 modulo 128 bytes and the mma rows are
+//    mapped to stage rows so that the 4 rows read by one 16-lane phase of a
+//    64-bit load lie in 4 different groups: their banks are distinct. A copy
+//    takes the 16-byte aligned window covering its bytes; bytes of W past its
+//    last 16-byte boundary are copied with plain loads.
+//  * Activations: at the start of each matrix the consumers rebuild a panel
+//    in shared memory from the Q8_K blocks -- per block the B fragments of
+//    every mma in lane order (f16, or biased int8 when f16 does not fit),
+//    the bsums operands of the correction mma, d_x and the block sums.
+//  * Consumers (NW warps): warp w takes blocks w, w+NW, ... of each stage's
+//    chunk for all 16 rows and accumulates the tile's partial outputs in
+//    registers across the chunks. After the tile's last chunk every warp
+//    stores its partials and counts itself in; the last warp to arrive adds
+//    the NW partials in a fixed warp order (deterministic) and writes y. With
+//    the partial buffers doubled it first releases the ring slot, so the
+//    refill does not wait.
+//  * Full/empty mbarriers with bounded waits (about 1 s), as in the __dp4a
+//    kernel; programmatic dependent launch: the producer streams W while the
+//    previous kernel finishes, the consumers wait for it before reading the
+//    activations.
+#pragma once
+
+#include "qg_common.cuh"
+
+namespace qg {
+
+// Where a warp's activation (B) fragments come from: a panel in shared
+// memory built per matrix (f16, or biased int8 when f16 does not fit), or
+// registers -- when every stage spans whole rows of at most 2 * NW blocks,
+// warp w always takes blocks w and w + NW, so it loads their fragments once
+// per matrix and shared memory holds only the ring.
+enum MmaBMode : int { kMmaPanel16 = 0, kMmaPanel8 = 1, kMmaRegs = 2 };
+constexpr int kMmaTileRows = 16;
+constexpr int kMmaMaxStages = 8;
+constexpr int kMmaHeaderBytes = 2 * 8 * kMmaMaxStages + 4 * 2 * kMmaMaxStages;  // mbarriers, partial-buffer counters
+constexpr int kMmaRecords = 8;              // fragment records per block
+constexpr int kMmaTailBytes = 256 + 32 + 32;  // per block: correction operands, d_x[8], block sums[8]
+// Bytes of one partial-output buffer: every consumer lane's 4 partial outputs.
+__host__ __device__ constexpr int mma_red_bytes(int nw) { return nw * 32 * 16; }
+constexpr int kMmaNvec = 8;                 // vectors per mma (the n of m16n8k16)
+
+// Panel bytes per weight block: fragment records (lane order, 16 bytes a lane
+// in f16, 8 in biased int8) then the tail.
+__host__ __device__ constexpr int mma_rec_bytes(bool b16) { return kMmaRecords * 32 * (b16 ? 16 : 8) + kMmaTailBytes; }
+__host__ __device__ constexpr int mma_frag_bytes(bool b16) { return kMmaRecords * 32 * (b16 ? 16 : 8); }
+
+struct MmaMat {
+    const uint8_t *W;   // [n_out][row_bytes], 16-byte aligned
+    const uint8_t *xq;  // byte-exact Q8_K blocks [n_vec][nb]
+    float *y;           // [n_vec][n_out]
+    int64_t tile_base;  // launch-wide index of this matrix's first tile
+    int n_out;
+    int pad;
+};
+
+template <int MAXB>
+struct MmaBatch {
+    MmaMat m[MAXB];
+};
+
+struct MmaParams {
+    int32_t *err;         // device error word
+    int64_t row_bytes;    // bytes of one row
+    int64_t total_tiles;  // tiles of all matrices
+    int n_mats;
+    int nb;               // blocks per row
+    int nv;               // vectors (1..8)
+    int kb;               // blocks per chunk
+    int n_chunks;         // chunks per row: ceil(nb / kb)
+    int rpitch;           // bytes between the rows of a group in a slot
+    int gpitch;           // bytes between the 4 row groups of a slot (32 mod 128)
+    int contig;           // 1: a stage spans whole rows (one copy per group)
+    int stage_bytes;      // 4 * gpitch
+    int n_stages;         // ring depth (2..kMmaMaxStages)
+    int red_slots;        // partial-output buffers: n_stages, or 2 * n_stages (then the
+                          // warp that adds a tile's partials releases the slot first)
+    int rec_bytes;        // panel bytes per block
+    int panel_bytes;      // nb * rec_bytes
+};
+
+struct MmaStage {
+    int mat, tile, kc;
+    bool last;  // the tile's last chunk
+};
+
+// Stage row of mma row r (0..15): rows r and r+4... of one 16-lane load
+// phase (r = 0..3, 4..7, 8..11, 12..15) fall in the 4 different groups.
+__device__ __forceinline__ int mma_stage_row(int r) { return 4 * (r & 3) + ((r >> 2) & 1) + 2 * (r >> 3); }
+
+// Walks a CTA's tiles, each as n_chunks stages. Producer and consumers run
+// the same walk.
+struct MmaWalk {
+    int64_t t, t1;
+    int m, kc;
+    int64_t base, next_base;  // tile_base of matrices m and m+1 (cached: the table is kernel parameters)
+
+    template <int MAXB>
+    __device__ __forceinline__ bool next(const MmaBatch<MAXB> &b, const MmaParams &p, MmaStage &s) {
+        if (t >= t1) return false;
+        while (t >= next_base) {
+            ++m;
+            base = next_base;
+            next_base = m + 1 < p.n_mats ? b.m[m + 1].tile_base : INT64_MAX;
+        }
+        s.mat = m;
+        s.tile = static_cast<int>(t - base);
+        s.kc = kc;
+        s.last = kc == p.n_chunks - 1;
+        if (++kc == p.n_chunks) {
+            kc = 0;
+            ++t;
+        }
+        return true;
+    }
+};
+
+template <int MAXB>
+__device__ __forceinline__ MmaWalk mma_cta_walk(const MmaParams &p, const MmaBatch<MAXB> &b) {
+    MmaWalk w;
+    w.t = static_cast<int64_t>(blockIdx.x) * p.total_tiles / gridDim.x;
+    w.t1 = static_cast<int64_t>(blockIdx.x + 1) * p.total_tiles / gridDim.x;
+    w.m = 0;
+    w.kc = 0;
+    w.base = 0;
+    w.next_base = p.n_mats > 1 ? b.m[1].tile_base : INT64_MAX;
+    return w;
+}
+
+// ------------------------------------------------------------ mma wrappers
+// D += A (16x16, rows g and g+8 of lane 4g+t hold columns 2t,2t+1 and
+// 2t+8,2t+9) x B (16x8, column g holds rows 2t,2t+1 and 2t+8,2t+9), f16 in,
+// f32 accumulate; d[0..3] = D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1].
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// The k = 8 form: a0/a1 = rows g/g+8, columns 2t,2t+1; b0 = rows 2t,2t+1 of column g.
+__device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Two f16 lanes minus 1152 each (exact for the integers used here).
+__device__ __forceinline__ uint32_t hsub1152(uint32_t h) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+
+// Packed two-lane f32 arithmetic (one instruction for both lanes).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 ra, ra, rb, rc;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// The B fragments of record r for this lane: b[0], b[1] for the record's
+// first mma, b[2], b[3] for its second.
+template <bool B16>
+__device__ __forceinline__ void mma_load_b(uint32_t rec, int r, int lane, uint32_t (&b)[4]) {
+    if (B16) {
+        const uint4 v = ld_s128(rec + static_cast<uint32_t>((r * 32 + lane) * 16));
+        b[0] = v.x;
+        b[1] = v.y;
+        b[2] = v.z;
+        b[3] = v.w;
+    } else {
+        // biased bytes c = a + 128 -> f16 (1024 + c) by placing 0x64 above
+        // each byte, then subtract 1152
+        const uint2 v = ld_s64(rec + static_cast<uint32_t>((r * 32 + lane) * 8));
+        b[0] = hsub1152(__byte_perm(v.x, 0x64646464u, 0x4140));
+        b[1] = hsub1152(__byte_perm(v.x, 0x64646464u, 0x4342));
+        b[2] = hsub1152(__byte_perm(v.y, 0x64646464u, 0x4140));
+        b[3] = hsub1152(__byte_perm(v.y, 0x64646464u, 0x4342));
+    }
+}
+
+__device__ __forceinline__ uint32_t mma_pack(unsigned short lo, unsigned short hi) {
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// A warp's B operands for one weight block: the fragments of record r
+// (b(r, .)), the correction operand of the lane and d_x / block sums of
+// vectors 2t, 2t+1 -- read from the shared-memory panel ...
+template <bool B16>
+struct MmaSmemB {
+    uint32_t rec;
+    int lane;
+    __device__ __forceinline__ void b(int r, uint32_t (&bf)[4]) const { mma_load_b<B16>(rec, r, lane, bf); }
+    __device__ __forceinline__ uint32_t corr32() const { return ld_s32(rec + mma_frag_bytes(B16) + 8 * lane); }
+    __device__ __forceinline__ uint2 corr64() const { return ld_s64(rec + mma_frag_bytes(B16) + 8 * lane); }
+    __device__ __forceinline__ uint2 dxw(int t) const { return ld_s64(rec + mma_frag_bytes(B16) + 256 + 8 * t); }
+    __device__ __forceinline__ uint2 bsw(int t) const { return ld_s64(rec + mma_frag_bytes(B16) + 288 + 8 * t); }
+};
+
+// ... or held in registers (f16 fragments).
+struct MmaRegB {
+    const uint32_t (&r)[kMmaRecords][4];
+    uint2 corr, dx, bs;
+    __device__ __forceinline__ void b(int i, uint32_t (&bf)[4]) const {
+        bf[0] = r[i][0];
+        bf[1] = r[i][1];
+        bf[2] = r[i][2];
+        bf[3] = r[i][3];
+    }
+    __device__ __forceinline__ uint32_t corr32() const { return corr.x; }
+    __device__ __forceinline__ uint2 corr64() const { return corr; }
+    __device__ __forceinline__ uint2 dxw(int) const { return dx; }
+    __device__ __forceinline__ uint2 bsw(int) const { return bs; }
+};
+
+// ------------------------------------------------------------------ Q4_K
+// Block: f16 d, f16 dmin, 12 bytes of packed 6-bit scales and mins, 128 bytes
+// of nibbles (element 64c + l: low nibble of qs[32c + l], element 64c+32+l:
+// high nibble). Sub-block j = 2c + n (n = nibble) has scale sc_j, min m_j.
+// Lane (g, t) reads 8 bytes qs[32c + 8t ..] of rows g and g+8; mma (j, u)
+// takes its words u: f16 lanes of bytes 0,2 (k-slots 2t, 2t+1) and 1,3
+// (slots 2t+8, 2t+9). The panel's record j holds the matching activation
+// codes 32j + 8t + {0,2,1,3, 4,6,5,7} of vector g.
+struct MmaQ4_K {
+    static constexpr int kBlockBytes = 144;
+
+    // Element offsets (within the block) of the two 4-code runs of record r
+    // for lane t; the run is permuted to slots {0,2,1,3}.
+    __device__ static int run0(int r, int t) { return 32 * r + 8 * t; }
+    __device__ static int run1(int r, int t) { return 32 * r + 8 * t + 4; }
+
+    // Correction operand of lane (g, t): the 32-code sums of sub-blocks 2t
+    // and 2t+1 of vector g (k = 8 mma over the 8 sub-blocks).
+    __device__ static void corr(const int16_t *bs, int t, float (&c)[4]) {
+        c[0] = static_cast<float>(bs[4 * t] + bs[4 * t + 1]);
+        c[1] = static_cast<float>(bs[4 * t + 2] + bs[4 * t + 3]);
+        c[2] = 0.0f;
+        c[3] = 0.0f;
+    }
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        const uint4 ha = ld_s128(ra), hb = ld_s128(rb);
+        // scales (bytes 0..3: sub-blocks 0..3, 4..7: sub-blocks 4..7) and mins
+        const uint32_t sca0 = ha.y & 0x3F3F3F3Fu, sca1 = (ha.w & 0x0F0F0F0Fu) | ((ha.y >> 2) & 0x30303030u);
+        const uint32_t scb0 = hb.y & 0x3F3F3F3Fu, scb1 = (hb.w & 0x0F0F0F0Fu) | ((hb.y >> 2) & 0x30303030u);
+        const uint32_t ma0 = ha.z & 0x3F3F3F3Fu, ma1 = ((ha.w >> 4) & 0x0F0F0F0Fu) | ((ha.z >> 2) & 0x30303030u);
+        const uint32_t mb0 = hb.z & 0x3F3F3F3Fu, mb1 = ((hb.w >> 4) & 0x0F0F0F0Fu) | ((hb.z >> 2) & 0x30303030u);
+        // min term: sum_j m_j * bsum32_j (m as subnormal f16 bits: m * 2^-24)
+        const uint32_t msel = (t & 1) ? 0x4342u : 0x4140u;
+        float m2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_1688(m2, __byte_perm(t < 2 ? ma0 : ma1, 0u, msel), __byte_perm(t < 2 ? mb0 : mb1, 0u, msel), B.corr32());
+        float2 Ta = make_float2(0.0f, 0.0f), Tb = make_float2(0.0f, 0.0f);  // rows g, g+8
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint2 wa = ld_s64(ra + 16 + 32 * c + 8 * t), wb = ld_s64(rb + 16 + 32 * c + 8 * t);
+            const uint32_t sa0 = wa.x >> 8, sa1 = wa.y >> 8, sb0 = wb.x >> 8, sb1 = wb.y >> 8;
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const int j = 2 * c + n;
+                const uint32_t M = n ? 0x00F000F0u : 0x000F000Fu;
+                uint32_t bf[4];
+                B.b(j, bf);
+                float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                mma_16816(C, wa.x & M, wb.x & M, sa0 & M, sb0 & M, bf[0], bf[1]);
+                mma_16816(C, wa.y & M, wb.y & M, sa1 & M, sb1 & M, bf[2], bf[3]);
+                // the two rows' scales of sub-block j: byte j&3 placed in the
+                // mantissa of 2^23 (even j) or 2^19 (odd j: the high nibbles
+                // carry a factor 16), then the power of two subtracted
+                const uint32_t swa = j < 4 ? sca0 : sca1, swb = j < 4 ? scb0 : scb1;
+                const uint32_t hi = n ? 0x49000000u : 0x4B000000u;
+                const float off = n ? -524288.0f : -8388608.0f;
+                const float2 f = fadd2(make_float2(__uint_as_float(__byte_perm(swa, hi, 0x7540u | (j & 3))),
+                                                   __uint_as_float(__byte_perm(swb, hi, 0x7540u | (j & 3)))),
+                                       make_float2(off, off));
+                Ta = ffma2(make_float2(f.x, f.x), make_float2(C[0], C[1]), Ta);
+                Tb = ffma2(make_float2(f.y, f.y), make_float2(C[2], C[3]), Tb);
+            }
+        }
+        // block value = d_x * 2^24 * (d * T - dmin * m2)
+        const float da = f16_bits_to_f32(ha.x) * 16777216.0f, dma = f16_bits_to_f32(ha.x >> 16) * -16777216.0f;
+        const float db = f16_bits_to_f32(hb.x) * 16777216.0f, dmb = f16_bits_to_f32(hb.x >> 16) * -16777216.0f;
+        const uint2 dxw = B.dxw(t);
+        const float2 dx = make_float2(__uint_as_float(dxw.x), __uint_as_float(dxw.y));
+        const float2 ua = ffma2(make_float2(da, da), Ta, make_float2(dma * m2[0], dma * m2[1]));
+        const float2 ub = ffma2(make_float2(db, db), Tb, make_float2(dmb * m2[2], dmb * m2[3]));
+        float2 acc01 = ffma2(dx, ua, make_float2(acc[0], acc[1]));
+        float2 acc23 = ffma2(dx, ub, make_float2(acc[2], acc[3]));
+        acc[0] = acc01.x;
+        acc[1] = acc01.y;
+        acc[2] = acc23.x;
+        acc[3] = acc23.y;
+    }
+};
+
+// ------------------------------------------------------------------ Q6_K
+// Block: ql[128], qh[64], int8 scales[16], f16 d (the 210 bytes start
+// 2-byte aligned). Element e = 128h + 32k + 16m + lam (sub-block
+// j = 8h + 2k + m = e / 16): low 4 bits from nibble k>>1 of
+// ql[64h + 32(k&1) + 16m + lam], high 2 bits from bits 2k of
+// qh[32h + 16m + lam]; value d * sc_j * (q - 32). Lane (g, t) takes
+// lam = 4t..4t+3 of every sub-block: bytes 0,2 -> k-slots 2t, 2t+1, bytes
+// 1,3 -> slots 2t+8, 2t+9. Record i of the panel holds activation codes
+// 32i + 4t + {0,2,1,3} (sub-block 2i) and 32i + 16 + 4t + {0,2,1,3}
+// (sub-block 2i+1) of vector g.
+struct MmaQ6_K {
+    static constexpr int kBlockBytes = 210;
+
+    __device__ static int run0(int r, int t) { return 32 * r + 4 * t; }
+    __device__ static int run1(int r, int t) { return 32 * r + 16 + 4 * t; }
+
+    // Correction operand of lane (g, t): bsums 2t, 2t+1, 2t+8, 2t+9 of
+    // vector g (k = 16 mma over the 16 sub-blocks).
+    __device__ static void corr(const int16_t *bs, int t, float (&c)[4]) {
+        c[0] = static_cast<float>(bs[2 * t]);
+        c[1] = static_cast<float>(bs[2 * t + 1]);
+        c[2] = static_cast<float>(bs[2 * t + 8]);
+        c[3] = static_cast<float>(bs[2 * t + 9]);
+    }
+
+    // The two f16 lanes (bytes 0,2 when odd == 0, bytes 1,3 otherwise) of
+    // codes q = low nibble(s) | 2 high bits << 4, as subnormal bits.
+    __device__ __forceinline__ static uint32_t codes(uint32_t ql, uint32_t qh, int k, int odd) {
+        const int n = k >> 1;
+        const uint32_t lo = (ql >> (8 * odd + 4 * n)) & 0x000F000Fu;
+        const uint32_t hi = ((qh >> (8 * odd + 2 * k)) & 0x00030003u) << 4;
+        return lo | hi;
+    }
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        // scales as biased bytes sc + 128
+        uint32_t swa[4], swb[4];
+        ld_words_a2<4>(ra + 192, swa);
+        ld_words_a2<4>(rb + 192, swb);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            swa[i] ^= 0x80808080u;
+            swb[i] ^= 0x80808080u;
+        }
+        // offset term: sum_j (sc_j + 128) * bsum16_j (subnormal bits)
+        const uint32_t ssel = (t & 1) ? 0x4342u : 0x4140u;
+        const uint2 cw = B.corr64();
+        float mq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_16816(mq, __byte_perm(t < 2 ? swa[0] : swa[1], 0u, ssel), __byte_perm(t < 2 ? swb[0] : swb[1], 0u, ssel),
+                  __byte_perm(t < 2 ? swa[2] : swa[3], 0u, ssel), __byte_perm(t < 2 ? swb[2] : swb[3], 0u, ssel),
+                  cw.x, cw.y);
+        float2 Ta = make_float2(0.0f, 0.0f), Tb = make_float2(0.0f, 0.0f);  // rows g, g+8
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t qla[2][2], qlb[2][2], qha[2], qhb[2];  // [m][k & 1], [m]
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                uint32_t w[1];
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    ld_words_a2<1>(ra + 64 * h + 32 * kk + 16 * m + 4 * t, w);
+                    qla[m][kk] = w[0];
+                    ld_words_a2<1>(rb + 64 * h + 32 * kk + 16 * m + 4 * t, w);
+                    qlb[m][kk] = w[0];
+                }
+                ld_words_a2<1>(ra + 128 + 32 * h + 16 * m + 4 * t, w);
+                qha[m] = w[0];
+                ld_words_a2<1>(rb + 128 + 32 * h + 16 * m + 4 * t, w);
+                qhb[m] = w[0];
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t bf[4];
+                B.b(4 * h + k, bf);
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int j = 8 * h + 2 * k + m;
+                    float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    mma_16816(C, codes(qla[m][k & 1], qha[m], k, 0), codes(qlb[m][k & 1], qhb[m], k, 0),
+                              codes(qla[m][k & 1], qha[m], k, 1), codes(qlb[m][k & 1], qhb[m], k, 1), bf[2 * m],
+                              bf[2 * m + 1]);
+                    const float2 f = fadd2(
+                        make_float2(__uint_as_float(__byte_perm(swa[j >> 2], 0x4B000000u, 0x7540u | (j & 3))),
+                                    __uint_as_float(__byte_perm(swb[j >> 2], 0x4B000000u, 0x7540u | (j & 3)))),
+                        make_float2(-8388736.0f, -8388736.0f));
+                    Ta = ffma2(make_float2(f.x, f.x), make_float2(C[0], C[1]), Ta);
+                    Tb = ffma2(make_float2(f.y, f.y), make_float2(C[2], C[3]), Tb);
+                }
+            }
+        }
+        // block value = d * d_x * 2^24 * (T - 32 mq + 2^-12 * block sum)
+        const float da = f16_bits_to_f32(ld_s16(ra + 208)) * 16777216.0f;
+        const float db = f16_bits_to_f32(ld_s16(rb + 208)) * 16777216.0f;
+        const uint2 dxw = B.dxw(t);
+        const uint2 bsw = B.bsw(t);
+        const float dx0 = __uint_as_float(dxw.x), dx1 = __uint_as_float(dxw.y);
+        const float2 bs = make_float2(__uint_as_float(bsw.x), __uint_as_float(bsw.y));
+        const float2 q4 = make_float2(0.000244140625f, 0.000244140625f), m32 = make_float2(-32.0f, -32.0f);
+        const float2 ea = ffma2(q4, bs, ffma2(m32, make_float2(mq[0], mq[1]), Ta));
+        const float2 eb = ffma2(q4, bs, ffma2(m32, make_float2(mq[2], mq[3]), Tb));
+        const float2 acc01 = ffma2(make_float2(da * dx0, da * dx1), ea, make_float2(acc[0], acc[1]));
+        const float2 acc23 = ffma2(make_float2(db * dx0, db * dx1), eb, make_float2(acc[2], acc[3]));
+        acc[0] = acc01.x;
+        acc[1] = acc01.y;
+        acc[2] = acc23.x;
+        acc[3] = acc23.y;
+    }
+};
+
+// ------------------------------------------------------------------ panel
+// Activations of one matrix (Q8_K blocks [nv][nb] at xq) into the panel:
+// per block, fragment record r of lane (g, t) = codes of vector g at the
+// type's two 4-code runs, each permuted to slots {0,2,1,3}; then per lane
+// the correction operand (f16), d_x[8] and the block sums[8] (f32). Vectors
+// g >= nv are zero. All consumer threads take part.
+template <class T, bool B16>
+__device__ __forceinline__ void mma_build_panel(const MmaParams &p, const uint8_t *xq, uint8_t *pan, int tid,
+                                                int nthr) {
+    const int nb = p.nb, nv = p.nv;
+    const int n_rec = nb * kMmaRecords * 32;
+    constexpr int kBatch = 8;  // records whose loads are in flight together
+    for (int u0 = tid; u0 < n_rec; u0 += kBatch * nthr) {
+        uint32_t w0[kBatch], w1[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int u = u0 + i * nthr;
+            const int b = u / (kMmaRecords * 32), r = (u / 32) % kMmaRecords, L = u % 32;
+            const int g = L >> 2, t = L & 3;
+            w0[i] = w1[i] = 0u;
+            if (u < n_rec && g < nv) {
+                const uint8_t *qs = xq + (static_cast<size_t>(g) * nb + b) * 292 + 4;
+                w0[i] = __ldg(reinterpret_cast<const uint32_t *>(qs + T::run0(r, t)));
+                w1[i] = __ldg(reinterpret_cast<const uint32_t *>(qs + T::run1(r, t)));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int u = u0 + i * nthr;
+            if (u >= n_rec) break;
+            const int b = u / (kMmaRecords * 32), r = (u / 32) % kMmaRecords, L = u % 32;
+            const uint32_t x0 = __byte_perm(w0[i], 0u, 0x3120), x1 = __byte_perm(w1[i], 0u, 0x3120);
+            uint8_t *dst = pan + static_cast<size_t>(b) * p.rec_bytes;
+            if (B16) {
+                uint4 o;
+                o.x = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x0, 0))), __half_as_ushort(__int2half_rn(sbyte(x0, 1))));
+                o.y = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x0, 2))), __half_as_ushort(__int2half_rn(sbyte(x0, 3))));
+                o.z = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x1, 0))), __half_as_ushort(__int2half_rn(sbyte(x1, 1))));
+                o.w = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x1, 2))), __half_as_ushort(__int2half_rn(sbyte(x1, 3))));
+                reinterpret_cast<uint4 *>(dst)[r * 32 + L] = o;
+            } else {
+                reinterpret_cast<uint2 *>(dst)[r * 32 + L] = make_uint2(x0 ^ 0x80808080u, x1 ^ 0x80808080u);
+            }
+        }
+    }
+    // per (block, vector): the correction operands of the vector's 4 lanes,
+    // d_x and the block sum
+    for (int u = tid; u < nb * kMmaNvec; u += nthr) {
+        const int b = u / kMmaNvec, v = u % kMmaNvec;
+        int16_t bs[16];
+        float dx = 0.0f;
+        if (v < nv) {
+            const uint8_t *blk = xq + (static_cast<size_t>(v) * nb + b) * 292;
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = __ldg(reinterpret_cast<const uint32_t *>(blk + 260) + i);
+            dx = __ldg(reinterpret_cast<const float *>(blk));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                bs[2 * i] = static_cast<int16_t>(w[i] & 0xFFFFu);
+                bs[2 * i + 1] = static_cast<int16_t>(w[i] >> 16);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bs[i] = 0;
+        }
+        uint8_t *tail = pan + static_cast<size_t>(b) * p.rec_bytes + mma_frag_bytes(B16);
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sum += bs[i];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            float c[4];
+            T::corr(bs, t, c);
+            reinterpret_cast<uint2 *>(tail)[4 * v + t] =
+                make_uint2(mma_pack(__half_as_ushort(__float2half_rn(c[0])), __half_as_ushort(__float2half_rn(c[1]))),
+                           mma_pack(__half_as_ushort(__float2half_rn(c[2])), __half_as_ushort(__float2half_rn(c[3]))));
+        }
+        reinterpret_cast<float *>(tail + 256)[v] = dx;
+        reinterpret_cast<float *>(tail + 288)[v] = static_cast<float>(sum);
+    }
+}
+
+// The B operands of one weight block `blk` of the matrix whose activations
+// are xq, into registers (the panel's contents for this lane: fragments as
+// f16, the correction operand, d_x and block sums of vectors 2t, 2t+1).
+template <class T>
+__device__ __forceinline__ void mma_load_regs(const uint8_t *xq, int nb, int nv, int blk, int lane,
+                                              uint32_t (&r)[kMmaRecords][4], uint2 &corr, uint2 &dx, uint2 &bs) {
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t w0[kMmaRecords], w1[kMmaRecords];
+    const uint8_t *qs = xq + (static_cast<size_t>(g) * nb + blk) * 292 + 4;
+#pragma unroll
+    for (int i = 0; i < kMmaRecords; ++i) {
+        w0[i] = g < nv ? __ldg(reinterpret_cast<const uint32_t *>(qs + T::run0(i, t))) : 0u;
+        w1[i] = g < nv ? __ldg(reinterpret_cast<const uint32_t *>(qs + T::run1(i, t))) : 0u;
+    }
+    int16_t bsv[16];
+    if (g < nv) {
+        const uint32_t *bw = reinterpret_cast<const uint32_t *>(xq + (static_cast<size_t>(g) * nb + blk) * 292 + 260);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = __ldg(bw + i);
+            bsv[2 * i] = static_cast<int16_t>(w & 0xFFFFu);
+            bsv[2 * i + 1] = static_cast<int16_t>(w >> 16);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) bsv[i] = 0;
+    }
+    float dxv[2] = {0.0f, 0.0f}, bsum[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int v = 2 * t + u;
+        if (v < nv) {
+            const uint8_t *vb = xq + (static_cast<size_t>(v) * nb + blk) * 292;
+            dxv[u] = __ldg(reinterpret_cast<const float *>(vb));
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(vb + 260) + i);
+                sum += static_cast<int16_t>(w & 0xFFFFu) + static_cast<int16_t>(w >> 16);
+            }
+            bsum[u] = static_cast<float>(sum);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kMmaRecords; ++i) {
+        // slots {0,2,1,3} of each run, biased bytes -> f16 (1024 + c) -> minus 1152
+        const uint32_t x0 = __byte_perm(w0[i], 0u, 0x3120) ^ 0x80808080u;
+        const uint32_t x1 = __byte_perm(w1[i], 0u, 0x3120) ^ 0x80808080u;
+        r[i][0] = hsub1152(__byte_perm(x0, 0x64646464u, 0x4140));
+        r[i][1] = hsub1152(__byte_perm(x0, 0x64646464u, 0x4342));
+        r[i][2] = hsub1152(__byte_perm(x1, 0x64646464u, 0x4140));
+        r[i][3] = hsub1152(__byte_perm(x1, 0x64646464u, 0x4342));
+    }
+    float c[4];
+    T::corr(bsv, t, c);
+    corr = make_uint2(mma_pack(__half_as_ushort(__float2half_rn(c[0])), __half_as_ushort(__float2half_rn(c[1]))),
+                      mma_pack(__half_as_ushort(__float2half_rn(c[2])), __half_as_ushort(__float2half_rn(c[3]))));
+    dx = make_uint2(__float_as_uint(dxv[0]), __float_as_uint(dxv[1]));
+    bs = make_uint2(__float_as_uint(bsum[0]), __float_as_uint(bsum[1]));
+}
+
+// ------------------------------------------------------------------ producer
+// The whole producer warp runs this: lane 0 waits for free slots and issues
+// the copies; after each tile's last stage is consumed all lanes add the
+// consumer warps' partial outputs (fixed order) and store y.
+// The tile's output: the NW warps' partials of buffer ri added in warp
+// order, stored to y (lane (g, t) holds rows g and g+8, vectors 2t, 2t+1 of
+// the mma tile, i.e. stage rows mma_stage_row(g), mma_stage_row(g + 8)).
+template <int NW>
+__device__ __forceinline__ void mma_finish_tile(const MmaParams &p, const float4 *red, int ri, float *y, int n_out,
+                                                int tile, int lane) {
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const float4 v = red[(ri * NW + w) * 32 + lane];
+        s[0] += v.x;
+        s[1] += v.y;
+        s[2] += v.z;
+        s[3] += v.w;
+    }
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int row = tile * kMmaTileRows + mma_stage_row(g + (q >= 2 ? 8 : 0));
+        const int v = 2 * t + (q & 1);
+        if (row < n_out && v < p.nv) y[static_cast<int64_t>(v) * n_out + row] = s[q];
+    }
+}
+
+// One stage's copies for the whole producer warp: lane q copies row group q
+// (whole rows) or lane i row segment i. mma_plan_copy works out this lane's
+// window (it does not touch the slot, so it runs before the slot is free);
+// mma_issue_copy stores the bytes past W's last 16-byte boundary, announces
+// the stage's bytes on its barrier and issues the copy.
+struct MmaCopy {
+    int64_t a0, a1, e;  // window [a0, a1) of W by bulk copy, [a1, e) by plain loads
+    uint32_t dst;       // slot offset of the window
+    uint32_t total;     // bytes by bulk copy, whole stage (every lane)
+};
+
+template <class T>
+__device__ __forceinline__ MmaCopy mma_plan_copy(const MmaParams &p, int n_out, const MmaStage &st, int lane) {
+    const int rows = min(kMmaTileRows, n_out - st.tile * kMmaTileRows);
+    const int64_t row0 = static_cast<int64_t>(st.tile) * kMmaTileRows;
+    MmaCopy c;
+    int64_t s;
+    bool mine;
+    if (p.contig) {
+        mine = 4 * lane < rows;
+        s = (row0 + 4 * lane) * p.row_bytes;
+        c.e = s + static_cast<int64_t>(min(4, rows - 4 * lane)) * p.row_bytes;
+        c.dst = static_cast<uint32_t>(lane * p.gpitch);
+    } else {
+        mine = lane < rows;
+        const int kbt = min(p.kb, p.nb - st.kc * p.kb);
+        s = (row0 + lane) * p.row_bytes + static_cast<int64_t>(st.kc) * p.kb * T::kBlockBytes;
+        c.e = s + static_cast<int64_t>(kbt) * T::kBlockBytes;
+        c.dst = static_cast<uint32_t>((lane >> 2) * p.gpitch + (lane & 3) * p.rpitch);
+    }
+    c.a0 = c.a1 = c.e = mine ? c.e : 0;
+    if (mine) {
+        const int64_t lim = (static_cast<int64_t>(n_out) * p.row_bytes) & ~int64_t(15);
+        c.a0 = s & ~int64_t(15);
+        c.a1 = (c.e + 15) & ~int64_t(15);
+        if (c.a1 > lim) c.a1 = lim;
+        if (c.a1 < c.a0) c.a1 = c.a0;
+    }
+    uint32_t total = static_cast<uint32_t>(c.a1 - c.a0);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    c.total = total;
+    return c;
+}
+
+__device__ __forceinline__ void mma_issue_copy(const MmaCopy &c, const uint8_t *W, uint8_t *buf, uint32_t bar,
+                                               uint64_t policy, int lane) {
+    uint8_t *dst = buf + c.dst;
+    for (int64_t x = c.a1; x < c.e; ++x) dst[x - c.a0] = __ldg(W + x);  // rare: W's last < 16 bytes
+    __syncwarp();  // the plain stores come before the arrival that publishes the stage
+    if (lane == 0) mbar_arrive_expect_tx(bar, c.total);
+    __syncwarp();
+    if (c.a1 > c.a0) bulk_copy_g2s(smem_addr(dst), W + c.a0, static_cast<uint32_t>(c.a1 - c.a0), bar, policy);
+}
+
+template <class T, int MAXB>
+__device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<MAXB> &b, uint8_t *ring,
+                                             uint32_t full0, uint32_t empty0, int lane) {
+    const uint64_t policy = l2_evict_first_policy();
+    const int S = p.n_stages;
+    int cur = -1;
+    const uint8_t *W = nullptr;
+    int n_out = 0;
+    MmaWalk walk = mma_cta_walk(p, b);
+    MmaStage st;
+    int issued = 0;
+    // slot = k mod S and phase = (k / S) & 1, kept incrementally
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int k = 0; walk.next(b, p, st); ++k) {
+        if (st.mat != cur) {  // the matrix's fields, read from the parameter table once
+            cur = st.mat;
+            W = b.m[cur].W;
+            n_out = b.m[cur].n_out;
+        }
+        const MmaCopy cp = mma_plan_copy<T>(p, n_out, st, lane);  // before the slot is free
+        if (k >= S) {
+            bool got = true;
+            if (lane == 0) got = mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1u);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            if (!got) {
+                if (lane == 0) record_error(p.err, kErrProducerWait);
+                break;
+            }
+        }
+        mma_issue_copy(cp, W, ring + static_cast<size_t>(slot) * p.stage_bytes, full0 + 8 * slot, policy, lane);
+        ++issued;
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+    // Leave no copy in flight into this CTA's shared memory.
+    for (int k = max(0, issued - S); k < issued; ++k) {
+        const int slot = k % S;
+        bool got = true;
+        if (lane == 0) got = mbar_wait_bounded(full0 + 8 * slot, static_cast<uint32_t>((k / S) & 1));
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+            if (lane == 0) record_error(p.err, kErrDrainWait);
+            return;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+// Shared memory: mbarriers | panel | partial outputs [red_slots][warps][32]
+// float4 | ring of n_stages stages.
+template <class T, int BMODE, int NW, int MAXB>
+__global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaParams p, const MmaBatch<MAXB> b) {
+    constexpr bool B16 = BMODE == kMmaPanel16;
+    constexpr bool REGS = BMODE == kMmaRegs;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t full0 = smem_addr(smem);
+    const uint32_t empty0 = full0 + 8 * kMmaMaxStages;
+    uint8_t *pan = smem + kMmaHeaderBytes;
+    float4 *red = reinterpret_cast<float4 *>(pan + p.panel_bytes);
+    int *red_count = reinterpret_cast<int *>(smem + 2 * 8 * kMmaMaxStages);  // per partial buffer
+    uint8_t *ring = pan + p.panel_bytes + p.red_slots * mma_red_bytes(NW);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.n_stages;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, NW);
+        }
+        for (int r = 0; r < 2 * kMmaMaxStages; ++r) red_count[r] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_allow_dependents();
+
+    if (warp == NW) {
+        mma_producer<T, MAXB>(p, b, ring, full0, empty0, lane);
+        return;
+    }
+
+    // ---- consumers ----
+    pdl_wait_prior_grids();  // the activations may come from the previous kernel
+    const int g = lane >> 2;
+    const int sra = mma_stage_row(g), srb = mma_stage_row(g + 8);
+    const uint32_t pan_a = smem_addr(pan), ring_a = smem_addr(ring);
+    bool failed = false;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    MmaWalk walk = mma_cta_walk(p, b);
+    MmaStage st;
+    int cur = -1;
+    float *y = nullptr;
+    int n_out = 0;
+    uint32_t breg[2][kMmaRecords][4];  // REGS: fragments of blocks warp and warp + NW
+    uint2 bcorr[2], bdx[2], bbs[2];
+    // slot = k mod S, its phase (k / S) & 1 and the partial buffer k mod red_slots, kept incrementally
+    int slot = 0, ri = 0;
+    uint32_t phase = 0;
+    for (int k = 0; walk.next(b, p, st); ++k) {
+        if (st.mat != cur) {  // a new matrix: its activations
+            if (REGS) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (warp + i * NW < p.nb)
+                        mma_load_regs<T>(b.m[st.mat].xq, p.nb, p.nv, warp + i * NW, lane, breg[i], bcorr[i], bdx[i],
+                                         bbs[i]);
+            } else {
+                if (cur >= 0) named_barrier(1, NW * 32);
+                mma_build_panel<T, B16>(p, b.m[st.mat].xq, pan, threadIdx.x, NW * 32);
+                named_barrier(1, NW * 32);
+            }
+            y = b.m[st.mat].y;
+            n_out = b.m[st.mat].n_out;
+            cur = st.mat;
+        }
+        if (!failed) {
+            // every lane waits (each needs the acquire); the warp agrees on
+            // the outcome, since mma.sync needs all 32 lanes
+            const bool got = mbar_wait_bounded(full0 + 8 * slot, phase);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) record_error(p.err, kErrConsumerWait);
+                failed = true;
+            }
+        }
+        if (!failed) {
+            const uint32_t sb = ring_a + static_cast<uint32_t>(slot * p.stage_bytes);
+            // row sr of the stage: group sr/4 at sr/4 * gpitch, row sr%4 of it at
+            // (sr%4) * rpitch, plus the copy's offset from its 16-byte window
+            const int64_t row0 = static_cast<int64_t>(st.tile) * kMmaTileRows;
+            const int64_t koff = static_cast<int64_t>(st.kc) * p.kb * T::kBlockBytes;
+            const int64_t ca = (p.contig ? row0 + (sra & ~3) : row0 + sra) * p.row_bytes + koff;
+            const int64_t cb = (p.contig ? row0 + (srb & ~3) : row0 + srb) * p.row_bytes + koff;
+            const uint32_t ra = sb + static_cast<uint32_t>((sra >> 2) * p.gpitch + (sra & 3) * p.rpitch) +
+                                static_cast<uint32_t>(ca & 15);
+            const uint32_t rb = sb + static_cast<uint32_t>((srb >> 2) * p.gpitch + (srb & 3) * p.rpitch) +
+                                static_cast<uint32_t>(cb & 15);
+            const int kbt = min(p.kb, p.nb - st.kc * p.kb);
+            const uint32_t rec0 = pan_a + static_cast<uint32_t>(st.kc * p.kb * p.rec_bytes);
+            if (REGS) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int kb = warp + i * NW;
+                    if (kb < kbt)
+                        T::tile_block(ra + kb * T::kBlockBytes, rb + kb * T::kBlockBytes,
+                                      MmaRegB{breg[i], bcorr[i], bdx[i], bbs[i]}, lane, acc);
+                }
+            } else {
+                for (int kb = warp; kb < kbt; kb += NW)
+                    T::tile_block(ra + kb * T::kBlockBytes, rb + kb * T::kBlockBytes,
+                                  MmaSmemB<B16>{rec0 + static_cast<uint32_t>(kb * p.rec_bytes), lane}, lane, acc);
+            }
+        }
+        bool last_warp = false;
+        if (st.last) {
+            // this warp's share of the tile; the last of the NW warps adds them up
+            red[(ri * NW + warp) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(red_count + ri, 1) == NW - 1;
+            }
+            last_warp = __shfl_sync(0xffffffffu, last, 0);
+            if (last_warp) {
+                __threadfence_block();
+                const bool doubled = p.red_slots > S;
+                if (doubled && lane == 0) mbar_arrive(empty0 + 8 * slot);  // the slot is free already
+                if (!failed) mma_finish_tile<NW>(p, red, ri, y, n_out, st.tile, lane);
+                __syncwarp();
+                if (lane == 0) {
+                    red_count[ri] = 0;
+                    if (!doubled) mbar_arrive(empty0 + 8 * slot);
+                }
+            }
+        }
+        if (!(st.last && last_warp)) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+        }
+        if (++ri == p.red_slots) ri = 0;
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
+}  // namespace qg
+
+namespace qg {
+
+// Host side: grid, shared memory and instance of one launch.
+struct MmaLaunch {
+    int grid;
+    int smem;
+    int smem_optin;  // the device's opt-in shared-memory limit per CTA
+    int mode;        // MmaBMode
+    int warps;       // consumer warps (8 with registers, 16 with a panel)
+};
+
+}  // namespace qg

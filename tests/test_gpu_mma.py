@@ -1,0 +1,123 @@
+"""The tensor-core GEMV (Q4_K / Q6_K weights, three or more vectors) against
+the oracle, through the C ABI.
+
+The kernel tiles 16 rows and streams each tile as chunks of whole blocks, so
+the shapes here cover a ragged last tile (n_out not a multiple of 16), rows of
+one block, chunks that do not divide the row (Q6_K with 43 blocks per row),
+W whose end is not 16-byte aligned (Q6_K rows of 9030 bytes: the last bytes
+come through plain loads), both activation-panel formats (f16 when it fits in
+shared memory, biased int8 for long rows) and every vector count from 3 to 8.
+The bar is the parity tolerance of the other product tests,
+|y - y_oracle| <= 1e-5 |y_oracle| + 1e-6 ||x_v|| ||w_o||.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import ggml_block_quantized_gb300 as qg  # noqa: E402
+import oracle  # noqa: E402
+from ggml_block_quantized_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+K_TYPES = [qg.Q4_K, qg.Q6_K]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def check_y(t, W, x, y, n_out, n_in, n_vec, rows=None):
+    xq = oracle.quantize(oracle.act_type(t), x)
+    if rows is None:
+        ref = oracle.gemv(t, W, xq, n_out, n_in, n_vec)
+        rows = np.arange(n_out)
+    else:
+        ref = np.zeros((n_vec, n_out))
+        for r in rows:
+            oracle.gemv(t, W, xq, n_out, n_in, n_vec, rows=(int(r), int(r) + 1), out=ref)
+    wn = np.linalg.norm(oracle.dequantize(t, W, n_out * n_in).reshape(n_out, n_in).astype(np.float64), axis=1)
+    xn = np.linalg.norm(x.reshape(n_vec, n_in).astype(np.float64), axis=1)
+    got = y.reshape(n_vec, n_out)[:, rows].astype(np.float64)
+    want = ref[:, rows]
+    tol = 1e-5 * np.abs(want) + 1e-6 * xn[:, None] * wn[None, rows]
+    bad = np.abs(got - want) > tol
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside tolerance; worst {np.abs(got - want).max()}"
+
+
+# (n_out, n_in): ragged tiles, one-block rows, multi-chunk rows, unaligned W end
+SHAPES = [(33, 256), (40, 768), (100, 2816), (16, 4096), (257, 4096), (17, 11008), (31, 11008)]
+
+
+@pytest.mark.parametrize("t", K_TYPES)
+def test_mma_shapes_all_rows(t):
+    rng = np.random.default_rng(4100 + t)
+    for n_out, n_in in SHAPES:
+        W = synth.k_blocks(t, n_out * n_in // 256, rng)
+        for n_vec in (3, 5, 8):
+            x = synth.f32_normal(rng, n_vec * n_in)
+            y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
+            check_y(t, W, x, y, n_out, n_in, n_vec)
+
+
+@pytest.mark.parametrize("t", K_TYPES)
+def test_mma_every_vector_count(t):
+    rng = np.random.default_rng(4200 + t)
+    n_out, n_in = 48, 2048
+    W = synth.k_blocks(t, n_out * n_in // 256, rng)
+    for n_vec in range(3, 9):
+        x = synth.f32_normal(rng, n_vec * n_in)
+        y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
+        check_y(t, W, x, y, n_out, n_in, n_vec)
+
+
+@pytest.mark.parametrize("t", K_TYPES)
+def test_mma_is_deterministic(t):
+    rng = np.random.default_rng(4300 + t)
+    n_out, n_in, n_vec = 1000, 11008 if t == qg.Q6_K else 4096, 8
+    Wd = dev(synth.k_blocks(t, n_out * n_in // 256, rng))
+    xd = dev(synth.f32_normal(rng, n_vec * n_in))
+    a = host(qg.qgemv(t, Wd, xd, n_out, n_in, n_vec))
+    b = host(qg.qgemv(t, Wd, xd, n_out, n_in, n_vec))
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("t", K_TYPES)
+def test_mma_batched_equals_single_calls(t):
+    """A batch of matrices of ragged sizes in one launch gives, per matrix,
+    the same bits as one call each (a tile's sum does not depend on which
+    CTA computes it)."""
+    rng = np.random.default_rng(4400 + t)
+    n_in, n_vec = (11008, 8) if t == qg.Q6_K else (4096, 8)
+    n_outs = [1, 15, 16, 17, 100, 700, 4096]
+    mats, hw, hx = [], [], []
+    for n_out in n_outs:
+        W = synth.k_blocks(t, n_out * n_in // 256, rng)
+        x = synth.f32_normal(rng, n_vec * n_in)
+        hw.append(W)
+        hx.append(x)
+        mats.append((dev(W), dev(x), torch.full((n_vec, n_out), np.nan, device="cuda"), n_out))
+    qg.qgemv_batched(t, mats, n_in, n_vec)
+    torch.cuda.synchronize()
+    for (W, x, y, n_out), w_host, x_host in zip(mats, hw, hx):
+        ref = qg.qgemv(t, W, x, n_out, n_in, n_vec)
+        got = host(y)
+        assert np.array_equal(got.view(np.uint32), host(ref).view(np.uint32)), n_out
+    W, x, y, n_out = mats[-2]
+    check_y(t, hw[-2], hx[-2], host(y), n_out, n_in, n_vec)
+    assert qg.device_error() == 0
