@@ -48,27 +48,33 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash():
-    """Hash of the sources that make up the GEMV kernels (to tell whether a
+def kernel_family(kernel_desc):
+    """'mma' for the tensor-core kernel, 'dp4a' for the streaming __dp4a one."""
+    return "mma" if kernel_desc.startswith("gemv_mma") else "dp4a"
+
+
+def kernel_source_hash(family):
+    """Hash of the sources of one GEMV kernel family (to tell whether a
     committed ncu traffic figure still describes the current kernel)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ggml_block_quantized_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("gemv") or name == "qg_common.cuh":
+        mine = name.startswith("gemv_mma") if family == "mma" else (name.startswith("gemv") and not name.startswith("gemv_mma"))
+        if mine or name == "qg_common.cuh":
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel_key):
+def committed_traffic(kernel_key, family):
     """dram bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of the kernel's family; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(kernel_key)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash(family):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -352,11 +358,13 @@ def run_ours(args, rank, world, local_rank):
     per_launch = alg_bytes / launches
     avg_dur = tg / reps / launches
     achieved = per_launch / avg_dur / 1e9
-    kernel_key = f"gemv_kernel<{qg.TYPE_NAMES[dom_t]},NV={nv}>"
-    roofline = {"bound": "hbm", "kernel": kernel_key + (" batched" if batched else ""),
+    rows = sum(c["n_out"] for c in dom_calls) if batched else dom_calls[0]["n_out"]
+    desc = qg.kernel_info(dom_t, rows, dom_calls[0]["n_in"], nv, len(dom_calls) if batched else 1)
+    kernel_key = desc.split(" ")[0]
+    roofline = {"bound": "hbm", "kernel": desc + (" (batched launch)" if batched else ""),
                 "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": committed_traffic(f"{kernel_key}@{args.workload}"),
+                "traffic": committed_traffic(f"{kernel_key}@{args.workload}", kernel_family(desc)),
                 "algorithmic_bytes_per_launch": int(per_launch), "avg_launch_us": round(avg_dur * 1e6, 3),
                 "launches": launches}
 

@@ -17,7 +17,8 @@ __all__ = [
     "library_path", "lib", "qtype_nbytes", "qtype_block", "qtype_act_type",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes",
     "qgemv", "qgemv_xq", "qgemv_block_isums", "qgemv_noalloc", "qgemv_batched",
-    "qgemv_batched_workspace_bytes", "BatchPlan", "device_error", "EXPORTED_SYMBOLS", "MAX_BATCH",
+    "qgemv_batched_workspace_bytes", "BatchPlan", "device_error", "kernel_info", "EXPORTED_SYMBOLS",
+    "MAX_BATCH",
 ]
 
 F32, F16, Q4_0, Q8_0, Q4_K, Q6_K, Q8_K = 0, 1, 2, 8, 12, 14, 15
@@ -30,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "qtype_nbytes", "qtype_block", "qtype_act_type", "qg_status_string", "qg_last_cuda_error",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes", "qgemv",
     "qgemv_xq", "qgemv_block_isums", "qg_device_error", "qgemv_noalloc",
-    "qgemv_batched_workspace_bytes", "qgemv_batched",
+    "qgemv_batched_workspace_bytes", "qgemv_batched", "qgemv_kernel_info",
 )
 MAX_BATCH = 256
 
@@ -85,6 +86,8 @@ def lib():
         L.qgemv_batched_workspace_bytes.restype = sz
         L.qgemv_batched.argtypes = [i32, ctypes.POINTER(GemvMat), i32, i64, i64, vp, sz, vp]
         L.qgemv_batched.restype = i32
+        L.qgemv_kernel_info.argtypes = [i32, i64, i64, i64, i32]
+        L.qgemv_kernel_info.restype = ctypes.c_char_p
         _lib = L
     return _lib
 
@@ -303,6 +306,11 @@ def qgemv_batched(t: int, mats, n_in: int, n_vec: int = 1, workspace=None, strea
     """y_i = W_i . x_i for independent matrices [(W, x, y, n_out), ...] of one
     type, row length and vector count, in one launch."""
     BatchPlan(t, mats, n_in, n_vec, workspace).run(stream)
+
+
+def kernel_info(t: int, total_rows: int, n_in: int, n_vec: int = 1, n_mats: int = 1) -> str:
+    """Which kernel and plan a product would use on the current device."""
+    return lib().qgemv_kernel_info(t, total_rows, n_in, n_vec, n_mats).decode()
 
 
 def device_error() -> int:

@@ -195,9 +195,9 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
                 const int R = (kConsumerWarps / split) * kRowsPerWarp;
                 const size_t stage = round16(static_cast<size_t>(R) * row_bytes + 15);
                 if (split < kConsumerWarps && stage > 40960) continue;  // stages of <= 40 KiB
-                // partial sums of split rows: [S][warps][rows per warp][nv] floats
+                // partial sums of split rows, double-buffered: [2S][warps][rows per warp][nv] floats
                 auto red_bytes = [&](int S) {
-                    return split > 1 ? round16(static_cast<size_t>(S) * kConsumerWarps * kRowsPerWarp * nv * 4) : 0;
+                    return split > 1 ? round16(static_cast<size_t>(2 * S) * kConsumerWarps * kRowsPerWarp * nv * 4) : 0;
                 };
                 if (fixed0 + red_bytes(2) + 2 * stage > budget) continue;
                 int S = static_cast<int>(ring_target / stage);
@@ -418,12 +418,28 @@ int launch_quantize_batched(int act_type, const QuantTable &t, int n, void *xq, 
     return e == cudaSuccess ? QG_OK : cuda_fail(e, "batched quantize launch");
 }
 
-// Activations of at most this many f32 bytes per call are quantized inside
-// the GEMV's prologue (every CTA reads x once); larger ones go through the
-// separate quantization launch into the workspace.
-constexpr int64_t kFusedQuantMaxBytes = 48 * 1024;
+// Activations of at most this many f32 bytes per call (QG_FUSED_QUANT_KIB,
+// default 48 KiB) are quantized inside the GEMV's prologue (every CTA reads
+// x once); larger ones go through the separate quantization launch into the
+// workspace.
+int64_t fused_quant_max_bytes() {
+    static const int64_t v = static_cast<int64_t>(env_int("QG_FUSED_QUANT_KIB", 48, 0, 1024)) * 1024;
+    return v;
+}
 
-bool fused_quantization(int64_t n_in, int64_t n_vec) { return 4 * n_in * n_vec <= kFusedQuantMaxBytes; }
+bool fused_quantization(int64_t n_in, int64_t n_vec) { return 4 * n_in * n_vec <= fused_quant_max_bytes(); }
+
+// A single product quantizes x inside the GEMV only when its matrix is small
+// enough (<= 32 MiB of blocks) for the prologue that every CTA then runs to
+// matter more than the separate launch; for larger matrices every CTA streams
+// enough rows that the quantization launch, overlapped with the GEMV's weight
+// prefetch, is the cheaper way.
+constexpr int64_t kFusedMaxWeightBytes = 32ll << 20;
+
+bool fused_single(int type, int64_t n_out, int64_t n_in, int64_t n_vec) {
+    return fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec) &&
+           qtype_nbytes(type, n_in) * n_out <= kFusedMaxWeightBytes;
+}
 
 // The product over `n` matrices of one type, row length and vector count
 // (activations from mats[i].x quantized in the kernel when x_bytes > 0, else
@@ -672,7 +688,7 @@ int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     // the product's shape limits are checked before anything is enqueued
     GemvParams probe = {};
     GemvLaunch pl = {};
-    const bool fused = fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec);
+    const bool fused = fused_single(type, n_out, n_in, n_vec);
     st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
                    fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &probe, &pl);
     if (st != QG_OK) return st;
@@ -748,6 +764,43 @@ int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, i
     }
     return run_gemv_mats(type, gm, n_mats, n_in, n_vec, fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, false,
                          dev, s);
+}
+
+const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_t n_vec, int n_mats) {
+    static thread_local char buf[160];
+    buf[0] = 0;
+    if (check_weight_type(type) != QG_OK || check_gemv_shape(type, total_rows, n_in, n_vec) != QG_OK) return buf;
+    if (n_mats < 1 || n_mats > QG_MAX_BATCH || total_rows < 1 || n_in < 1) return buf;
+    DeviceInfo dev;
+    if (current_device(&dev) != QG_OK) {
+        std::snprintf(buf, sizeof buf, "cuda: %s", g_last_cuda_error);
+        return buf;
+    }
+    const char *tn = type == QG_Q4_K ? "Q4_K" : type == QG_Q6_K ? "Q6_K" : type == QG_Q8_0 ? "Q8_0" : "Q4_0";
+    if (mma_preferred(type, n_vec)) {
+        // tiles: a batch of equal matrices is assumed for the tile count
+        const int64_t per = total_rows / n_mats;
+        const int64_t tiles = n_mats * ((per + kMmaTileRows - 1) / kMmaTileRows);
+        MmaParams mp = {};
+        MmaLaunch ml = {};
+        if (plan_gemv_mma(type, tiles, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &mp, &ml) == QG_OK) {
+            const char *mode = ml.mode == kMmaRegs ? "regs" : ml.mode == kMmaPanel16 ? "panel16" : "panel8";
+            std::snprintf(buf, sizeof buf, "gemv_mma_kernel<%s,%s,%dw> grid=%d stages=%d kb=%d smem=%d", tn, mode,
+                          ml.warps, ml.grid, mp.n_stages, mp.kb, ml.smem);
+            return buf;
+        }
+    }
+    const bool fused = n_mats == 1 ? fused_single(type, total_rows, n_in, n_vec)
+                                   : fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec);
+    GemvParams gp = {};
+    GemvLaunch gl = {};
+    if (plan_gemv(type, total_rows, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
+                  fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &gp, &gl) != QG_OK)
+        return buf;
+    std::snprintf(buf, sizeof buf, "gemv_kernel<%s,NV=%d> grid=%d stages=%d split=%d rows_per_stage=%d smem=%d%s", tn,
+                  static_cast<int>(n_vec), gl.grid, gp.n_stages, gp.split, gp.rows_per_stage, gl.smem,
+                  fused ? " fused-quantize" : "");
+    return buf;
 }
 
 int qg_device_error(int32_t *code) {

@@ -47,7 +47,7 @@ constexpr int kRowsPerWarp = 2;  // rows a warp group takes per stage (its items
 constexpr int kMaxBatch = 256;   // matrices per batched launch (their table is a kernel parameter)
 // Shared memory: header (kMaxStages full + kMaxStages empty mbarriers) |
 // staged activations | f32 x buffer | cross-warp partial sums (split > 1:
-// [n_stages][kConsumerWarps][kRowsPerWarp][NV] floats) | ring of stages.
+// [2 * n_stages][kConsumerWarps][kRowsPerWarp][NV] floats) | ring of stages.
 constexpr int kHeaderBytes = 2 * 8 * kMaxStages;
 
 // One matrix of a launch.
@@ -88,14 +88,21 @@ struct GemvParams {
 struct StageWalk {
     int64_t g, g1;
     int m;
+    int n_out;                // rows of matrix m
+    int64_t base, next_base;  // row_base of matrices m and m+1 (cached: the table is kernel parameters)
 
     template <int MAXB>
     __device__ __forceinline__ bool next(const GemvBatch<MAXB> &b, int n_mats, int R, int &mat, int &r, int &rows) {
         if (g >= g1) return false;
-        while (m + 1 < n_mats && b.m[m + 1].row_base <= g) ++m;
+        while (g >= next_base) {
+            ++m;
+            base = next_base;
+            n_out = b.m[m].n_out;
+            next_base = m + 1 < n_mats ? b.m[m + 1].row_base : INT64_MAX;
+        }
         mat = m;
-        r = static_cast<int>(g - b.m[m].row_base);
-        int64_t left = b.m[m].n_out - r;
+        r = static_cast<int>(g - base);
+        int64_t left = n_out - r;
         if (g1 - g < left) left = g1 - g;
         rows = static_cast<int>(left < R ? left : R);
         g += rows;
@@ -103,97 +110,136 @@ struct StageWalk {
     }
 };
 
-__device__ __forceinline__ StageWalk cta_rows(const GemvParams &p) {
+template <int MAXB>
+__device__ __forceinline__ StageWalk cta_rows(const GemvParams &p, const GemvBatch<MAXB> &b) {
     StageWalk w;
     w.g = static_cast<int64_t>(blockIdx.x) * p.total_rows / gridDim.x;
     w.g1 = static_cast<int64_t>(blockIdx.x + 1) * p.total_rows / gridDim.x;
     w.m = 0;
+    w.n_out = b.m[0].n_out;
+    w.base = 0;
+    w.next_base = p.n_mats > 1 ? b.m[1].row_base : INT64_MAX;
     return w;
 }
 
 // ------------------------------------------------------------------------
-// Producer: lane 0 of the last warp. Besides streaming the stages it
-// finishes rows split across warps (split > 1): once a stage is consumed it
-// adds the warps' partial sums of each row in a fixed order and writes y, so
-// the consumer warps of a row never wait for one another.
+// Producer: the last warp. Lane 0 waits for free slots and streams the
+// stages. Besides that the warp finishes rows split across consumer warps
+// (split > 1): once a stage is consumed its lanes add the warps' partial sums
+// of each row in a fixed order and write y, so the consumer warps of a row
+// never wait for one another. The partial sums are double-buffered (buffer
+// k mod 2S for stage k), so the warp adds them up after issuing the copy
+// that refills the slot: the refill does not wait for the additions.
 // ------------------------------------------------------------------------
 struct StageInfo {
-    int mat, r, rows;
+    float *y;
+    int n_out, r, rows;
 };
 
-template <int MAXB, int NV>
-__device__ __forceinline__ void finish_split_rows(const GemvParams &p, const GemvBatch<MAXB> &b, const float *red,
-                                                  int slot, const StageInfo &st) {
+template <int NV>
+__device__ __forceinline__ void finish_split_rows(const GemvParams &p, const float *red, int ri, const StageInfo &st,
+                                                  int lane) {
     const int split = p.split;
-    const int groups = kConsumerWarps / split;
-    const GemvMat &mt = b.m[st.mat];
-    for (int ris = 0; ris < st.rows; ++ris) {
-        const int grp = ris % groups, i = ris / groups;
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            float sum = 0.0f;
-            for (int q = 0; q < split; ++q)
-                sum += red[((slot * kConsumerWarps + grp * split + q) * kRowsPerWarp + i) * NV + v];
-            mt.y[static_cast<int64_t>(v) * mt.n_out + st.r + ris] = sum;
-        }
+    const int gshift = 3 - (split == 1 ? 0 : split == 2 ? 1 : split == 4 ? 2 : 3);  // log2(kConsumerWarps / split)
+    for (int o = lane; o < st.rows * NV; o += 32) {
+        const int ris = o / NV, v = o % NV;
+        const int grp = ris & ((1 << gshift) - 1), i = ris >> gshift;
+        float sum = 0.0f;
+        for (int q = 0; q < split; ++q) sum += red[((ri * kConsumerWarps + grp * split + q) * kRowsPerWarp + i) * NV + v];
+        st.y[static_cast<int64_t>(v) * st.n_out + st.r + ris] = sum;
     }
 }
 
 template <int MAXB, int NV, bool ISUMS>
 __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBatch<MAXB> &b, uint8_t *ring,
-                                              const float *red, uint32_t bar_full0, uint32_t bar_empty0) {
+                                              const float *red, uint32_t bar_full0, uint32_t bar_empty0, int lane) {
     const uint64_t policy = l2_evict_first_policy();
     const int S = p.n_stages;
     const bool reduce = !ISUMS && p.split > 1;
     StageInfo info[kMaxStages];
-    StageWalk walk = cta_rows(p);
+    StageWalk walk = cta_rows(p, b);
     int mat, r, rows;
     int issued = 0;
     bool ok = true;
+    // slot = k mod S, phase = (k / S) & 1 and rprev = (k - S) mod 2S (the partial-sum
+    // buffer of the stage the slot held before), kept incrementally
+    int slot = 0, rprev = 0;
+    uint32_t phase = 0;
+    int cur = -1;
+    const uint8_t *W = nullptr;
+    float *y = nullptr;
+    int n_out = 0;
+    int64_t lim = 0;
     for (int k = 0; walk.next(b, p.n_mats, p.rows_per_stage, mat, r, rows); ++k) {
-        const int slot = k % S;
         if (k >= S) {
-            const uint32_t parity = static_cast<uint32_t>((k / S) & 1) ^ 1u;
-            if (!mbar_wait_bounded(bar_empty0 + 8 * slot, parity)) {
-                record_error(p.err, kErrProducerWait);
+            const uint32_t parity = phase ^ 1u;
+            bool got = true;
+            if (lane == 0) got = mbar_wait_bounded(bar_empty0 + 8 * slot, parity);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            __syncwarp();
+            if (!got) {
+                if (lane == 0) record_error(p.err, kErrProducerWait);
                 ok = false;
                 break;
             }
-            if (reduce) finish_split_rows<MAXB, NV>(p, b, red, slot, info[slot]);
         }
-        info[slot] = StageInfo{mat, r, rows};
-        const uint8_t *W = b.m[mat].W;
-        const int64_t lim = (static_cast<int64_t>(b.m[mat].n_out) * p.row_bytes) & ~int64_t(15);
-        const int64_t start = static_cast<int64_t>(r) * p.row_bytes;
-        const int64_t end = start + static_cast<int64_t>(rows) * p.row_bytes;
-        const int64_t a0 = start & ~int64_t(15);
-        int64_t a1 = (end + 15) & ~int64_t(15);
-        if (a1 > lim) a1 = lim;
-        const uint32_t bulk = a1 > a0 ? static_cast<uint32_t>(a1 - a0) : 0u;
-        uint8_t *buf = ring + static_cast<size_t>(slot) * p.stage_bytes;
-        // bytes past the last 16-byte boundary of W: plain loads
-        for (int64_t i = a0 + bulk; i < end; ++i) buf[i - a0] = __ldg(W + i);
-        mbar_arrive_expect_tx(bar_full0 + 8 * slot, bulk);
-        if (bulk) bulk_copy_g2s(smem_addr(buf), W + a0, bulk, bar_full0 + 8 * slot, policy);
+        if (mat != cur) {  // the matrix's fields, read from the parameter table once
+            cur = mat;
+            W = b.m[mat].W;
+            y = b.m[mat].y;
+            n_out = b.m[mat].n_out;
+            lim = (static_cast<int64_t>(n_out) * p.row_bytes) & ~int64_t(15);
+        }
+        const StageInfo prev = info[slot];
+        info[slot] = StageInfo{y, n_out, r, rows};
+        if (lane == 0) {
+            const int64_t start = static_cast<int64_t>(r) * p.row_bytes;
+            const int64_t end = start + static_cast<int64_t>(rows) * p.row_bytes;
+            const int64_t a0 = start & ~int64_t(15);
+            int64_t a1 = (end + 15) & ~int64_t(15);
+            if (a1 > lim) a1 = lim;
+            const uint32_t bulk = a1 > a0 ? static_cast<uint32_t>(a1 - a0) : 0u;
+            uint8_t *buf = ring + static_cast<size_t>(slot) * p.stage_bytes;
+            // bytes past the last 16-byte boundary of W: plain loads
+            for (int64_t i = a0 + bulk; i < end; ++i) buf[i - a0] = __ldg(W + i);
+            mbar_arrive_expect_tx(bar_full0 + 8 * slot, bulk);
+            if (bulk) bulk_copy_g2s(smem_addr(buf), W + a0, bulk, bar_full0 + 8 * slot, policy);
+        }
+        // the partial sums of stage k - S (buffer (k - S) mod 2S; stage k uses k mod 2S)
+        if (reduce && k >= S) {
+            finish_split_rows<NV>(p, red, rprev, prev, lane);
+            if (++rprev == 2 * S) rprev = 0;
+        }
         ++issued;
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
     }
     // Do not leave while copies into this CTA's shared memory are in flight,
     // then finish the last stages' split rows once they are consumed.
     for (int k = max(0, issued - S); k < issued; ++k) {
         const int slot = k % S;
-        if (!mbar_wait_bounded(bar_full0 + 8 * slot, static_cast<uint32_t>((k / S) & 1))) {
-            record_error(p.err, kErrDrainWait);
+        bool got = true;
+        if (lane == 0) got = mbar_wait_bounded(bar_full0 + 8 * slot, static_cast<uint32_t>((k / S) & 1));
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+            if (lane == 0) record_error(p.err, kErrDrainWait);
             return;
         }
     }
     if (!reduce || !ok) return;
     for (int k = max(0, issued - S); k < issued; ++k) {
         const int slot = k % S;
-        if (!mbar_wait_bounded(bar_empty0 + 8 * slot, static_cast<uint32_t>((k / S) & 1))) {
-            record_error(p.err, kErrDrainWait);
+        bool got = true;
+        if (lane == 0) got = mbar_wait_bounded(bar_empty0 + 8 * slot, static_cast<uint32_t>((k / S) & 1));
+        got = __shfl_sync(0xffffffffu, got, 0);
+        __syncwarp();
+        if (!got) {
+            if (lane == 0) record_error(p.err, kErrDrainWait);
             return;
         }
-        finish_split_rows<MAXB, NV>(p, b, red, slot, info[slot]);
+        finish_split_rows<NV>(p, red, k % (2 * S), info[slot], lane);
     }
 }
 
@@ -267,7 +313,7 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     pdl_allow_dependents();
 
     if (warp == kConsumerWarps) {
-        if (lane == 0) gemv_producer<MAXB, NV, ISUMS>(p, b, ring, red, bar_full0, bar_empty0);
+        gemv_producer<MAXB, NV, ISUMS>(p, b, ring, red, bar_full0, bar_empty0, lane);
         return;
     }
 
@@ -281,26 +327,37 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     const int part = warp % split;
     const int b0 = part * p.nb / split;
     const int b1 = (part + 1) * p.nb / split;
-    const int items = (b1 - b0) * T::kLanesPerBlock;
+    const int nbw = b1 - b0;  // blocks of each of this warp's rows
+    constexpr int kBlocksPerIter = 32 / T::kLanesPerBlock;
+    const int sub = lane % T::kLanesPerBlock;  // the lane's part of a block
+    const int lane_blk = lane / T::kLanesPerBlock;
+    const uint32_t acta = smem_addr(act);
 
-    StageWalk walk = cta_rows(p);
+    StageWalk walk = cta_rows(p, b);
     int cur = -1;
     int mat, r, rows;
+    float *y = nullptr;          // the current matrix's fields, read from the parameter table once
+    int32_t *isums = nullptr;
+    int n_out = 0;
+    // slot = k mod S, its phase (k / S) & 1 and the partial-sum buffer k mod 2S, kept incrementally
+    int slot = 0, ri = 0;
+    uint32_t phase = 0;
     for (int k = 0; walk.next(b, p.n_mats, R, mat, r, rows); ++k) {
-        const GemvMat &mt = b.m[mat];
         if (mat != cur) {  // this CTA reaches a new matrix: stage its activations
             if (cur >= 0) named_barrier(1, kConsumerWarps * 32);
-            stage_activations<T, NV>(p, mt, act, xbuf, warp, lane);
+            stage_activations<T, NV>(p, b.m[mat], act, xbuf, warp, lane);
             cur = mat;
+            y = b.m[mat].y;
+            isums = b.m[mat].isums;
+            n_out = b.m[mat].n_out;
         }
-        const int slot = k % S;
-        if (!failed && !mbar_wait_bounded(bar_full0 + 8 * slot, static_cast<uint32_t>((k / S) & 1))) {
+        if (!failed && !mbar_wait_bounded(bar_full0 + 8 * slot, phase)) {
             record_error(p.err, kErrConsumerWait);
             failed = true;
         }
         const int64_t start = static_cast<int64_t>(r) * p.row_bytes;
         const uint8_t *stage = ring + static_cast<size_t>(slot) * p.stage_bytes + (start & 15);
-        const int64_t isum_vstride = static_cast<int64_t>(mt.n_out) * p.nb * T::kSums;
+        const int64_t isum_vstride = static_cast<int64_t>(n_out) * p.nb * T::kSums;
         // this warp group's rows in the stage: grp + groups * i
         const uint8_t *rowp[kRowsPerWarp];
         bool has[kRowsPerWarp];
@@ -310,7 +367,7 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
             const int ris = grp + groups * i;
             has[i] = ris < rows;
             rowp[i] = stage + static_cast<int64_t>(has[i] ? ris : 0) * p.row_bytes;
-            isum_row[i] = ISUMS ? mt.isums + static_cast<int64_t>(r + (has[i] ? ris : 0)) * p.nb * T::kSums
+            isum_row[i] = ISUMS ? isums + static_cast<int64_t>(r + (has[i] ? ris : 0)) * p.nb * T::kSums
                                 : nullptr;
         }
         float acc[kRowsPerWarp][NV];
@@ -319,27 +376,26 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
 #pragma unroll
             for (int v = 0; v < NV; ++v) acc[i][v] = 0.0f;
         if (!failed && has[0]) {
-            // The warp's items over its rows, flattened (row i, item j), so
-            // the lanes stay busy whatever the row length.
-            const int n_rows = has[1] ? 2 : 1;
-            const int total = items * n_rows;
+            // The warp's blocks over its rows, flattened (virtual block vb:
+            // row vb / nbw, block vb % nbw), so the lanes stay busy whatever
+            // the row length. A lane always takes the same part `sub` of its
+            // blocks (32 is a multiple of the lanes per block).
+            const int tot = nbw * (has[1] ? 2 : 1);
+            const int lim = (tot + kBlocksPerIter - 1) / kBlocksPerIter * kBlocksPerIter;
             const uint32_t rowa0 = smem_addr(rowp[0]), rowa1 = smem_addr(rowp[1]);
-            const uint32_t acta = smem_addr(act);
-            for (int f = lane; f < ((total + 31) & ~31); f += 32) {
-                const bool active = f < total;
-                const int i = active && f >= items ? 1 : 0;
-                const int j = active ? f - i * items : 0;
-                const int blk = b0 + j / T::kLanesPerBlock;
-                const int sub = j % T::kLanesPerBlock;
+            for (int vb = lane_blk; vb < lim; vb += kBlocksPerIter) {
+                const bool active = vb < tot;
+                const bool second = active && vb >= nbw;
+                const int blk = b0 + (active ? (second ? vb - nbw : vb) : 0);
                 float part[NV];
 #pragma unroll
                 for (int v = 0; v < NV; ++v) part[v] = 0.0f;
-                T::template item<NV, ISUMS>(i ? rowa1 : rowa0, blk, sub, active, acta, p.nb, part,
-                                            i ? isum_row[1] : isum_row[0], isum_vstride);
+                T::template item<NV, ISUMS>(second ? rowa1 : rowa0, blk, sub, active, acta, p.nb, part,
+                                            second ? isum_row[1] : isum_row[0], isum_vstride);
 #pragma unroll
                 for (int v = 0; v < NV; ++v) {
-                    acc[0][v] += i ? 0.0f : part[v];
-                    acc[1][v] += i ? part[v] : 0.0f;
+                    acc[0][v] += second ? 0.0f : part[v];
+                    acc[1][v] += second ? part[v] : 0.0f;
                 }
             }
         }
@@ -355,12 +411,12 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
                         if (!has[i]) continue;
                         const int row = r + grp + groups * i;
 #pragma unroll
-                        for (int v = 0; v < NV; ++v) mt.y[static_cast<int64_t>(v) * mt.n_out + row] = acc[i][v];
+                        for (int v = 0; v < NV; ++v) y[static_cast<int64_t>(v) * n_out + row] = acc[i][v];
                     }
                 }
             } else if (lane == 0) {
                 // partial sums of this warp's part of its rows; the producer adds them up
-                float *rp = red + ((slot * kConsumerWarps + warp) * kRowsPerWarp) * NV;
+                float *rp = red + ((ri * kConsumerWarps + warp) * kRowsPerWarp) * NV;
 #pragma unroll
                 for (int i = 0; i < kRowsPerWarp; ++i)
 #pragma unroll
@@ -369,6 +425,11 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty0 + 8 * slot);
+        if (++ri == 2 * S) ri = 0;
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
     }
 }
 

@@ -157,6 +157,12 @@ size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec);
  *   Q4_K:             d_x * (d_w * S_q - dmin_w * S_m)
  * in f32. The f32 order of these few float operations is not fixed by the
  * pages; results agree with an f64 accumulation to about 1e-5 relative.
+ * For Q4_K and Q6_K with n_vec >= 3 the sums are formed on the tensor cores
+ * (mma.sync, f16 operands that hold the integer codes exactly, f32
+ * accumulation per sub-block, which is exact) and the sub-block scales are
+ * applied in f32 per sub-block -- the same tolerance holds. The vector count
+ * from which this path is taken can be changed with the environment
+ * variable QG_MMA_MIN_NVEC (read once per process).
  * workspace: device buffer of at least qgemv_workspace_bytes(type, n_in,
  * n_vec) bytes (workspace_bytes gives its size). Limits: n_out <=
  * 2^31 - 1; n_vec * n_in must be small enough for the activations of one
@@ -177,7 +183,9 @@ int qgemv_xq(int type, const void *W, const void *xq, float *y, int64_t n_out, i
  * S_m = sum_j m_j (bsum_2j + bsum_2j+1)) and k = 1 otherwise (Q8_0:
  * sum qw qx; Q4_0: sum (code - 8) qx; Q6_K: sum_j sc_j sum_{i in j}
  * (q_i - 32) a_i) ([rml] Quantized dot products, Kernels and references).
- * Runs the same device code as qgemv_xq. */
+ * Runs the __dp4a kernel that qgemv_xq runs for Q8_0, Q4_0 and for fewer
+ * than 3 vectors (the tensor-core kernel accumulates the same exact sums,
+ * scaled by 2^-24, but does not write them out). */
 int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, int64_t n_out,
                       int64_t n_in, int64_t n_vec, qg_stream_t stream);
 
@@ -222,7 +230,8 @@ typedef struct {
 
 /* Workspace bytes qgemv_batched needs for n_mats matrices: 16 when the
  * activations are small enough to be quantized inside the product (4 *
- * n_in * n_vec <= 48 KiB), else the quantized activations of every matrix,
+ * n_in * n_vec <= 48 KiB, and not a tensor-core product: Q4_K or Q6_K with
+ * n_vec >= 3), else the quantized activations of every matrix,
  * n_mats * qgemv_workspace_bytes(type, n_in, n_vec). 0 on a bad argument. */
 size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int n_mats);
 
@@ -237,6 +246,17 @@ size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int 
  * array read during the call (1 <= n_mats <= QG_MAX_BATCH). */
 int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, int64_t n_vec, void *workspace,
                   size_t workspace_bytes, qg_stream_t stream);
+
+/* ---- Introspection --------------------------------------------------------- */
+
+/* Which kernel and launch plan a product over n_mats matrices with
+ * total_rows rows in all (row length n_in, n_vec vectors) would use on the
+ * current device, as one line of text for logs and benchmarks, e.g.
+ * "gemv_mma_kernel<Q4_K,regs,8w> grid=152 stages=5 smem=226048". The string
+ * belongs to the library (per host thread, overwritten by the next call).
+ * Returns "" on a bad argument or when the shape has no plan; "cuda: ..." on
+ * a CUDA error. Launches nothing. */
+const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_t n_vec, int n_mats);
 
 /* ---- Device-side status -------------------------------------------------- */
 

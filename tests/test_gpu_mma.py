@@ -121,3 +121,13 @@ def test_mma_batched_equals_single_calls(t):
     W, x, y, n_out = mats[-2]
     check_y(t, hw[-2], hx[-2], host(y), n_out, n_in, n_vec)
     assert qg.device_error() == 0
+
+
+def test_kernel_choice_is_reported():
+    """The tensor-core kernel is the one planned for Q4_K/Q6_K from 3 vectors,
+    the __dp4a kernel below that and for Q8_0/Q4_0."""
+    assert qg.kernel_info(qg.Q4_K, 4096, 4096, 8).startswith("gemv_mma_kernel<Q4_K,regs,8w>")
+    assert qg.kernel_info(qg.Q6_K, 4096, 11008, 8).startswith("gemv_mma_kernel<Q6_K,panel8,16w>")
+    assert qg.kernel_info(qg.Q4_K, 4096, 4096, 3).startswith("gemv_mma_kernel<")
+    assert qg.kernel_info(qg.Q4_K, 4096, 4096, 2).startswith("gemv_kernel<Q4_K,NV=2>")
+    assert qg.kernel_info(qg.Q4_0, 4096, 4096, 8).startswith("gemv_kernel<Q4_0,NV=8>")

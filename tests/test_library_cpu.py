@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declarations_are_exported(L):
     names = declared_functions()
-    assert len(names) == 16
+    assert len(names) == 17
     assert sorted(qg.EXPORTED_SYMBOLS) == names
     for n in names:
         assert hasattr(L, n), n
@@ -124,6 +124,11 @@ def test_other_entry_points_validate(L):
     assert L.qgemv_block_isums(qg.Q6_K, A, A2, NUL, 4, 256, 1, NUL) == ERR_NULL
     assert L.qgemv_block_isums(qg.Q4_0, A, A2, A3, 4, 256, 0, NUL) == ERR_SHAPE
     assert L.qg_device_error(None) == ERR_NULL
+    # bad arguments give an empty description before any CUDA call
+    assert L.qgemv_kernel_info(qg.Q8_K, 16, 256, 1, 1) == b""
+    assert L.qgemv_kernel_info(qg.Q4_K, 16, 250, 1, 1) == b""
+    assert L.qgemv_kernel_info(qg.Q4_K, 16, 256, 9, 1) == b""
+    assert L.qgemv_kernel_info(qg.Q4_K, 16, 256, 1, 0) == b""
 
 
 def test_batched_validation(L):
