@@ -130,12 +130,12 @@ bool mma_type(int type) { return type == QG_Q4_K || type == QG_Q6_K; }
 // quantize x inside the GEMV prologue.
 bool mma_preferred(int type, int64_t n_vec) { return mma_type(type) && n_vec >= tune_mma_min_nvec(); }
 
-size_t act_smem_bytes(int type, int nb, int nv) {
+size_t act_smem_bytes(int type, int lpb, int nb, int nv) {
     switch (type) {
     case QG_Q8_0: return TypeQ8_0::act_bytes(nb, nv);
     case QG_Q4_0: return TypeQ4_0::act_bytes(nb, nv);
     case QG_Q4_K: return TypeQ4_K::act_bytes(nb, nv);
-    case QG_Q6_K: return TypeQ6_K::act_bytes(nb, nv);
+    case QG_Q6_K: return lpb == TypeQ6_K4::kLanesPerBlock ? TypeQ6_K4::act_bytes(nb, nv) : TypeQ6_K::act_bytes(nb, nv);
     default: return 0;
     }
 }
@@ -147,11 +147,14 @@ constexpr int kSmemTailPad = 16;  // unaligned word reads may touch up to 4 byte
 // Lanes of one activation block's f32 values (bytes) and lanes per weight
 // block, per type.
 int act_block_f32_bytes(int type) { return (type == QG_Q8_0 || type == QG_Q4_0) ? 128 : 1024; }
-int lanes_per_block(int type) {
+// The item variants a type offers (lanes per weight block); Q6_K has a
+// two-lane item (fewer instructions per code) and a four-lane one (its
+// 8-block iterations fill better for some row lengths).
+int item_lpbs(int type, int (&out)[2]) {
     switch (type) {
-    case QG_Q4_K: return TypeQ4_K::kLanesPerBlock;
-    case QG_Q6_K: return TypeQ6_K::kLanesPerBlock;
-    default: return 1;
+    case QG_Q4_K: out[0] = TypeQ4_K::kLanesPerBlock; return 1;
+    case QG_Q6_K: out[0] = TypeQ6_K::kLanesPerBlock; out[1] = TypeQ6_K4::kLanesPerBlock; return 2;
+    default: out[0] = 1; return 1;
     }
 }
 
@@ -169,13 +172,13 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
     block_info(type, &elems, &bytes);
     const int64_t nb = n_in / elems;
     const int64_t row_bytes = nb * bytes;
-    const size_t act = round16(act_smem_bytes(type, static_cast<int>(nb), nv));
     const size_t ring_target = static_cast<size_t>(tune_ring_kib()) * 1024;
     const size_t sm_smem = 228 * 1024, cta_reserve = 1024;  // per-SM shared memory, per-CTA driver share
     const size_t blk_f32 = static_cast<size_t>(act_block_f32_bytes(type));
     size_t xb_opts[4] = {round16(x_bytes), 16384, 8192, 4096};
     const int n_xb = x_bytes ? 4 : 1;
-    const int lpb = lanes_per_block(type);
+    int lpbs[2] = {1, 1};
+    const int n_lpb = item_lpbs(type, lpbs);
     for (int per_sm = tune_ctas_per_sm(); per_sm >= 1; --per_sm) {
         size_t budget = sm_smem / per_sm - cta_reserve;
         if (budget > static_cast<size_t>(smem_limit)) budget = static_cast<size_t>(smem_limit);
@@ -183,6 +186,10 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
         double best_score = -1.0;
         GemvParams bp = {};
         size_t best_smem = 0;
+        int best_lpb = lpbs[0];
+        for (int li = 0; li < n_lpb; ++li) {
+        const int lpb = lpbs[li];
+        const size_t act = round16(act_smem_bytes(type, lpb, static_cast<int>(nb), nv));
         for (int xi = 0; xi < n_xb; ++xi) {
             size_t xb = xb_opts[xi];
             if (x_bytes) {
@@ -208,12 +215,15 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
                 const double eff = static_cast<double>(nb * lpb * kRowsPerWarp) / split /
                                    (32.0 * static_cast<double>((items + 31) / 32));
                 // fuller lanes first; then fewer warps per row (each stage does
-                // more work per warp); then x staged whole; then the larger ring
-                const double score = static_cast<int>(eff * 20.0 + 0.5) * 100.0 - split * 10.0 +
+                // more work per warp); then the item with fewer lanes per
+                // block (fewer instructions per code); then x staged whole;
+                // then the larger ring
+                const double score = static_cast<int>(eff * 20.0 + 0.5) * 100.0 - split * 10.0 - li * 6.0 +
                                      (xi == 0 ? 5.0 : 0.0) + static_cast<double>(S * stage) / (4.0 * 1024 * 1024);
                 if (score > best_score) {
                     best_score = score;
                     found = true;
+                    best_lpb = lpb;
                     bp.row_bytes = row_bytes;
                     bp.total_rows = total_rows;
                     bp.nb = static_cast<int>(nb);
@@ -228,6 +238,7 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
                 }
             }
         }
+        }
         if (!found) continue;
         *p = bp;
         const int64_t tiles = (total_rows + bp.rows_per_stage - 1) / bp.rows_per_stage;
@@ -236,6 +247,7 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
         l->smem = static_cast<int>(best_smem);
         l->smem_optin = smem_limit;
         l->sms = sms;
+        l->lpb = best_lpb;
         return QG_OK;
     }
     return QG_ERR_SHAPE;
@@ -797,8 +809,8 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
     if (plan_gemv(type, total_rows, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
                   fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &gp, &gl) != QG_OK)
         return buf;
-    std::snprintf(buf, sizeof buf, "gemv_kernel<%s,NV=%d> grid=%d stages=%d split=%d rows_per_stage=%d smem=%d%s", tn,
-                  static_cast<int>(n_vec), gl.grid, gp.n_stages, gp.split, gp.rows_per_stage, gl.smem,
+    std::snprintf(buf, sizeof buf, "gemv_kernel<%s,NV=%d> grid=%d stages=%d split=%d rows_per_stage=%d lanes_per_block=%d smem=%d%s",
+                  tn, static_cast<int>(n_vec), gl.grid, gp.n_stages, gp.split, gp.rows_per_stage, gl.lpb, gl.smem,
                   fused ? " fused-quantize" : "");
     return buf;
 }

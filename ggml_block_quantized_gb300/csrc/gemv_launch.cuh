@@ -17,6 +17,7 @@ struct GemvLaunch {
     int smem;
     int smem_optin;  // the device's opt-in shared-memory limit per CTA
     int sms;         // SMs of the device
+    int lpb;         // lanes per weight block of the chosen item (Q6_K: 2 or 4)
 };
 
 
@@ -100,6 +101,7 @@ QG_DECLARE_GEMV_LAUNCH(launch_gemv_q8_0)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_0)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_k)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q6_k)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q6_k4)
 #undef QG_DECLARE_GEMV_LAUNCH
 
 }  // namespace qg

@@ -129,7 +129,8 @@ __device__ __forceinline__ StageWalk cta_rows(const GemvParams &p, const GemvBat
 // of each row in a fixed order and write y, so the consumer warps of a row
 // never wait for one another. The partial sums are double-buffered (buffer
 // k mod 2S for stage k), so the warp adds them up after issuing the copy
-// that refills the slot: the refill does not wait for the additions.
+// that refills the slot: the refill does not wait for the additions. With
+// no split rows to finish, lane 0 runs alone.
 // ------------------------------------------------------------------------
 struct StageInfo {
     float *y;
@@ -156,6 +157,9 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBat
     const uint64_t policy = l2_evict_first_policy();
     const int S = p.n_stages;
     const bool reduce = !ISUMS && p.split > 1;
+    // without split rows to finish, lane 0 alone runs the loop
+    if (!reduce && lane != 0) return;
+    const unsigned lanes = reduce ? 0xffffffffu : 1u;
     StageInfo info[kMaxStages];
     StageWalk walk = cta_rows(p, b);
     int mat, r, rows;
@@ -175,8 +179,8 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBat
             const uint32_t parity = phase ^ 1u;
             bool got = true;
             if (lane == 0) got = mbar_wait_bounded(bar_empty0 + 8 * slot, parity);
-            got = __shfl_sync(0xffffffffu, got, 0);
-            __syncwarp();
+            got = __shfl_sync(lanes, got, 0);
+            __syncwarp(lanes);
             if (!got) {
                 if (lane == 0) record_error(p.err, kErrProducerWait);
                 ok = false;
@@ -222,7 +226,7 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBat
         const int slot = k % S;
         bool got = true;
         if (lane == 0) got = mbar_wait_bounded(bar_full0 + 8 * slot, static_cast<uint32_t>((k / S) & 1));
-        got = __shfl_sync(0xffffffffu, got, 0);
+        got = __shfl_sync(lanes, got, 0);
         if (!got) {
             if (lane == 0) record_error(p.err, kErrDrainWait);
             return;
@@ -233,8 +237,8 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBat
         const int slot = k % S;
         bool got = true;
         if (lane == 0) got = mbar_wait_bounded(bar_empty0 + 8 * slot, static_cast<uint32_t>((k / S) & 1));
-        got = __shfl_sync(0xffffffffu, got, 0);
-        __syncwarp();
+        got = __shfl_sync(lanes, got, 0);
+        __syncwarp(lanes);
         if (!got) {
             if (lane == 0) record_error(p.err, kErrDrainWait);
             return;

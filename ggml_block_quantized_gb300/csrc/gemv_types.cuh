@@ -376,8 +376,112 @@ struct TypeQ4_K {
 };
 
 // ------------------------------------------------------------------------
-// Q6_K. Four lanes per block: lane sub = 2h + p takes half h and the 16
-// positions l = 16p..16p+15 of each of the four 32-value rows k, i.e. the
+// Q6_K. Two lanes per block: lane sub = h takes half h, i.e. the four
+// 32-value rows k of ql[64h..64h+63] / qh[32h..32h+31] and the 16-value
+// sub-blocks j = 8h + 2k + m (m = 0, 1). Its ql and qh runs are contiguous,
+// so the 2-byte aligned block costs one extra word load and one funnel shift
+// per word of the run. Activations staged per (vector, block, half) as a
+// 176-byte record (codes 128h.. in order | int16 bsums 8h..8h+7 | f32 d_x).
+// The -32 offset of q is applied through the bsums.
+// ------------------------------------------------------------------------
+struct TypeQ6_K {
+    static constexpr int kBlockElems = 256, kBlockBytes = 210, kLanesPerBlock = 2, kSums = 1;
+    static constexpr int kActValues = 256;
+    // 176-byte records (44 words): 8 consecutive records' 128-bit loads fall
+    // in 8 disjoint bank quads. Layout: codes 128h..128h+127 of the block in
+    // order | bsums 8h..8h+7 (int16) at +128 | f32 d at +144.
+    static constexpr int kRecord = 176;
+    static size_t act_bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * 2 * kRecord; }
+
+    // From byte-exact Q8_K blocks (292 B, 4-byte aligned): 8 16-byte units of
+    // codes, then the bsums with d.
+    __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
+        const int n = nb * nv * 2 * 9;
+        for (int u = tid; u < n; u += nthr) {
+            const int r = u / 9, part = u % 9;
+            const int blk = r >> 1, h = r & 1;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + static_cast<size_t>(blk) * 292);
+            uint4 *rec = reinterpret_cast<uint4 *>(act + static_cast<size_t>(r) * kRecord);
+            if (part < 8) {
+                const int w = 1 + 32 * h + 4 * part;  // codes start at byte 4
+                rec[part] = make_uint4(__ldg(src + w), __ldg(src + w + 1), __ldg(src + w + 2), __ldg(src + w + 3));
+            } else {
+                const int w = 65 + 4 * h;  // bsums (int16) start at byte 260
+                rec[8] = make_uint4(__ldg(src + w), __ldg(src + w + 1), __ldg(src + w + 2), __ldg(src + w + 3));
+                reinterpret_cast<uint32_t *>(rec + 9)[0] = __ldg(src);
+            }
+        }
+    }
+
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        // lane l holds values 8l..8l+7: half h = l/16
+        const int h = lane >> 4;
+        for (int i = warp; i < count; i += nwarps) {
+            uint32_t w[2];
+            int s16;
+            float d;
+            quantize_q8_k_lane(xs + 1024u * i, lane, w, s16, d);
+            uint8_t *rec = act + (static_cast<size_t>(g0 + i) * 2 + h) * kRecord;
+            reinterpret_cast<uint2 *>(rec)[lane & 15] = make_uint2(w[0], w[1]);
+            if ((lane & 1) == 0) reinterpret_cast<int16_t *>(rec + 128)[(lane & 15) >> 1] = static_cast<int16_t>(s16);
+            if ((lane & 15) == 0) reinterpret_cast<float *>(rec + 144)[0] = d;
+        }
+    }
+
+    // Lane part h: element e = 128h + 32k + 16m + lam (sub-block j = 8h + 2k + m)
+    // takes its low 4 bits from nibble k>>1 of ql[64h + 32(k&1) + 16m + lam] and
+    // its high 2 bits from bits 2k of qh[32h + 16m + lam].
+    template <int NV, bool ISUMS>
+    __device__ static void item(uint32_t rowa, int b, int sub, bool active, uint32_t acta, int nb,
+                                float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;  // 2-byte aligned
+        const uint32_t h = static_cast<uint32_t>(sub);
+        uint32_t ql[16], qh[8], scw[2];
+        ld_words_a2<16>(blk + 64u * h, ql);         // words 0..7: k = 0, 2; words 8..15: k = 1, 3
+        ld_words_a2<8>(blk + 128u + 32u * h, qh);   // bits 2k..2k+1 of each byte: k
+        ld_words_a2<2>(blk + 192u + 8u * h, scw);   // scales 8h..8h+7: byte 2k + m of the pair
+        const float dw = f16_bits_to_f32(ld_s16(blk + 208u));
+        uint32_t q[4][8];  // codes 0..63 of row k, words w = 0..7 (m = w / 4)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            q[0][w] = (ql[w] & 0x0F0F0F0Fu) | ((qh[w] << 4) & 0x30303030u);
+            q[1][w] = (ql[8 + w] & 0x0F0F0F0Fu) | ((qh[w] << 2) & 0x30303030u);
+            q[2][w] = ((ql[w] >> 4) & 0x0F0F0F0Fu) | (qh[w] & 0x30303030u);
+            q[3][w] = ((ql[8 + w] >> 4) & 0x0F0F0F0Fu) | ((qh[w] >> 2) & 0x30303030u);
+        }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const uint32_t rec = acta + ((static_cast<uint32_t>(v) * nb + b) * 2 + h) * kRecord;
+            int s = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 a0 = ld_s128(rec + 32u * k), a1 = ld_s128(rec + 32u * k + 16u);
+                const int d0 = dp4a(q[k][3], a0.w, dp4a(q[k][2], a0.z, dp4a(q[k][1], a0.y, dp4a(q[k][0], a0.x, 0))));
+                const int d1 = dp4a(q[k][7], a1.w, dp4a(q[k][6], a1.z, dp4a(q[k][5], a1.y, dp4a(q[k][4], a1.x, 0))));
+                s += sbyte(scw[k >> 1], 2 * (k & 1)) * d0 + sbyte(scw[k >> 1], 2 * (k & 1) + 1) * d1;
+            }
+            // the q - 32 offset: 32 * sum_j sc_j * bsum_j (int16 pairs times scale byte pairs)
+            const uint4 bs = ld_s128(rec + 128u);
+            int t = dp2a_lo_ss(bs.x, scw[0], 0);
+            t = dp2a_hi_ss(bs.y, scw[0], t);
+            t = dp2a_lo_ss(bs.z, scw[1], t);
+            t = dp2a_hi_ss(bs.w, scw[1], t);
+            s -= 32 * t;
+            if (ISUMS) {
+                s = group_sum<2>(s);
+                if (active && h == 0) isum_row[v * isum_vstride + b] = s;
+            } else if (active) {
+                acc[v] = fmaf(static_cast<float>(s), dw * __uint_as_float(ld_s32(rec + 144u)), acc[v]);
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------------
+// Q6_K, four lanes per block (for rows whose block count leaves the
+// two-lane item's 16-block iterations partly empty): lane sub = 2h + p takes
+// half h and the 16 positions l = 16p..16p+15 of each of the four 32-value
+// rows k, i.e. the
 // 16-value sub-blocks j_k = 8h + 2k + p (k = 0..3). Activations staged per
 // (vector, block, sub) as an 80-byte record:
 //   codes[64] (k-th 16 bytes = values 128h + 32k + 16p ..) |
@@ -385,7 +489,7 @@ struct TypeQ4_K {
 // An 80-byte stride (20 words) puts 8 consecutive records' 128-bit loads in
 // 8 disjoint bank quads. The -32 offset of q is applied through the bsums.
 // ------------------------------------------------------------------------
-struct TypeQ6_K {
+struct TypeQ6_K4 {
     static constexpr int kBlockElems = 256, kBlockBytes = 210, kLanesPerBlock = 4, kSums = 1;
     static constexpr int kActValues = 256;
     static constexpr int kRecord = 80;

@@ -131,3 +131,8 @@ def test_kernel_choice_is_reported():
     assert qg.kernel_info(qg.Q4_K, 4096, 4096, 3).startswith("gemv_mma_kernel<")
     assert qg.kernel_info(qg.Q4_K, 4096, 4096, 2).startswith("gemv_kernel<Q4_K,NV=2>")
     assert qg.kernel_info(qg.Q4_0, 4096, 4096, 8).startswith("gemv_kernel<Q4_0,NV=8>")
+    # the __dp4a kernel's two Q6_K items: two lanes per block where their
+    # 16-block iterations fill (16 blocks a row), four where they would not
+    # (43 blocks a row); the parity tests cover both row lengths
+    assert "lanes_per_block=2" in qg.kernel_info(qg.Q6_K, 32000, 4096, 1)
+    assert "lanes_per_block=4" in qg.kernel_info(qg.Q6_K, 4096, 11008, 1, 32)
