@@ -307,10 +307,11 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
     bp.nv = nv;
     bool found = false;
     const int force = tune_mma_panel();  // 0 automatic, 1 a panel, 8 the int8 panel
-    if (force == 0 && nb <= 16) {
+    constexpr int rw = 8;  // consumer warps of the register kernel: blocks w and w + 8 each
+    if (force == 0 && nb <= 2 * rw) {
         int rp, gp, S, R;
         mma_slot_layout(nb, nb, bytes, &rp, &gp);
-        if (mma_ring(smem_limit, kMmaHeaderBytes, 4 * static_cast<int64_t>(gp), 8, &S, &R)) {
+        if (mma_ring(smem_limit, kMmaHeaderBytes, 4 * static_cast<int64_t>(gp), rw, &S, &R)) {
             bp.kb = nb;
             bp.n_chunks = 1;
             bp.rpitch = rp;
@@ -321,9 +322,9 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
             bp.red_slots = R;
             bp.rec_bytes = 0;
             bp.panel_bytes = 0;
-            bl.smem = kMmaHeaderBytes + S * bp.stage_bytes + R * mma_red_bytes(8);
+            bl.smem = kMmaHeaderBytes + S * bp.stage_bytes + R * mma_red_bytes(rw);
             bl.mode = kMmaRegs;
-            bl.warps = 8;
+            bl.warps = rw;
             found = true;
         }
     }

@@ -780,8 +780,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaPar
     int cur = -1;
     float *y = nullptr;
     int n_out = 0;
-    uint32_t breg[2][kMmaRecords][4];  // REGS: fragments of blocks warp and warp + NW
-    uint2 bcorr[2], bdx[2], bbs[2];
+    constexpr int RB = 2;  // REGS: blocks a warp keeps (warp, warp + NW)
+    uint32_t breg[RB][kMmaRecords][4];
+    uint2 bcorr[RB], bdx[RB], bbs[RB];
     // slot = k mod S, its phase (k / S) & 1 and the partial buffer k mod red_slots, kept incrementally
     int slot = 0, ri = 0;
     uint32_t phase = 0;
@@ -789,7 +790,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaPar
         if (st.mat != cur) {  // a new matrix: its activations
             if (REGS) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                for (int i = 0; i < RB; ++i)
                     if (warp + i * NW < p.nb)
                         mma_load_regs<T>(b.m[st.mat].xq, p.nb, p.nv, warp + i * NW, lane, breg[i], bcorr[i], bdx[i],
                                          bbs[i]);
@@ -827,7 +828,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaPar
             const uint32_t rec0 = pan_a + static_cast<uint32_t>(st.kc * p.kb * p.rec_bytes);
             if (REGS) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 0; i < RB; ++i) {
                     const int kb = warp + i * NW;
                     if (kb < kbt)
                         T::tile_block(ra + kb * T::kBlockBytes, rb + kb * T::kBlockBytes,
