@@ -8,10 +8,10 @@ library (ggml_block_quantized_gb300) never imports, links or calls it, and
 the two share no code.
 
 Every function follows a passage of the reference pages; the citations sit
-beside each C function in qoracle.c. The Q6_K element mapping and the Q8_K
-activation rule are readings of the pages (they do not define them) and are
-"parity unpinned" against ggml itself: they are pinned only by structural
-invariants in the tests.
+beside each C function in qoracle.c. The Q6_K element mapping, the Q8_K
+activation rule and the s field of Q8_1 are readings of the pages (they do
+not define them) and are "parity unpinned" against ggml itself: they are
+pinned only by structural invariants in the tests.
 """
 import ctypes
 import os
@@ -20,9 +20,9 @@ import numpy as np
 
 from . import build as _build
 
-F32, F16, Q4_0, Q8_0, Q4_K, Q6_K, Q8_K = 0, 1, 2, 8, 12, 14, 15
-TYPE_NAMES = {F32: "F32", F16: "F16", Q4_0: "Q4_0", Q8_0: "Q8_0",
-              Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K"}
+F32, F16, Q4_0, Q4_1, Q5_0, Q8_0, Q8_1, Q4_K, Q6_K, Q8_K = 0, 1, 2, 3, 6, 8, 9, 12, 14, 15
+TYPE_NAMES = {F32: "F32", F16: "F16", Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0",
+              Q8_0: "Q8_0", Q8_1: "Q8_1", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K"}
 
 _lib = None
 
@@ -42,7 +42,8 @@ def lib():
         L.or_f16_to_f32.restype = f32
         L.or_f32_to_f16.argtypes = [f32]
         L.or_f32_to_f16.restype = u16
-        for name in ("or_quantize_q8_0", "or_quantize_q4_0", "or_quantize_q8_k"):
+        for name in ("or_quantize_q8_0", "or_quantize_q4_0", "or_quantize_q8_k",
+                     "or_quantize_q4_1", "or_quantize_q5_0", "or_quantize_q8_1"):
             getattr(L, name).argtypes = [vp, vp, i64]
             getattr(L, name).restype = None
         L.or_dequantize.argtypes = [i32, vp, vp, i64]
@@ -97,14 +98,16 @@ def f32_to_f16(x) -> int:
 
 def quantize(t: int, x: np.ndarray) -> np.ndarray:
     """Quantize a float32 array (length a whole number of blocks) to the
-    byte-exact blocks of type t (Q8_0, Q4_0 or Q8_K). Returns uint8 bytes."""
+    byte-exact blocks of type t (Q8_0, Q4_0, Q4_1, Q5_0, Q8_1 or Q8_K).
+    Returns uint8 bytes."""
     x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
     nbytes = type_nbytes(t, x.size)
     if nbytes < 0:
         raise ValueError(f"length {x.size} is not whole blocks of type {t}")
     out = np.zeros(nbytes, dtype=np.uint8)
     fn = {Q8_0: lib().or_quantize_q8_0, Q4_0: lib().or_quantize_q4_0,
-          Q8_K: lib().or_quantize_q8_k}.get(t)
+          Q4_1: lib().or_quantize_q4_1, Q5_0: lib().or_quantize_q5_0,
+          Q8_1: lib().or_quantize_q8_1, Q8_K: lib().or_quantize_q8_k}.get(t)
     if fn is None:
         raise ValueError(f"the oracle has no quantizer for type {t}")
     fn(_ptr(x), _ptr(out), x.size)

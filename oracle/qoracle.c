@@ -20,7 +20,9 @@
  *              Per-format dequant; The fused matmul.
  *   [lesson21] "Building Q8_0 and Q4_0 Like ggml": Examples 1-2 (Q8_0 layout
  *              and quantizer), 5-6 (Q4_0 scale, code rule, nibble order),
- *              10 (Q8_0 x Q8_0 dot), 11 (Q4_0 x Q8_0 dot).
+ *              7 (Q4_1 min/max rule and layout), 8 (Q5_0 rule, qh packing
+ *              and decode), 10 (Q8_0 x Q8_0 dot), 11 (Q4_0 x Q8_0 dot),
+ *              14 (byte-exact blocks of all four formats).
  *   [candle]   "量化格式" (quantized formats, candle): GgmlDType table;
  *              block structure table; "一些边界值" (special values);
  *              VecDotType pairing table; vec_dot_unopt.
@@ -37,11 +39,18 @@
  *   - Q4_K sub-blocks 0..3: scale = scales[j] & 63, min = scales[j+4] & 63.
  *   - NaN inputs to a quantizer are ignored by the amax and give code 0
  *     (candle's special-value table).
+ *   - Q8_1 activations (paired with Q4_1 by [candle]'s VecDotType table;
+ *     the byte layout is not printed): f16 d, f16 s, 32 int8 codes
+ *     (36 bytes), where d and the codes follow the Q8_0 rule and
+ *     s = f16(d * sum of the codes) in f32 with the unrounded d. The
+ *     Q4_1 x Q8_1 block term is d_w * d_x * S + m_w * s_x (S = sum of
+ *     code * q_x), so it carries s's f16 rounding.
  *
  * Parity pins: every function here is pinned by tests under tests/ against
  * values the pages print, closed forms or brute force; the Q6_K element
- * mapping and the Q8_K rule are pinned only by structural invariants (the
- * pages do not define them) and are "parity unpinned" against ggml itself.
+ * mapping, the Q8_K rule and Q8_1's s field are pinned only by structural
+ * invariants (the pages do not define them) and are "parity unpinned"
+ * against ggml itself.
  */
 #include <math.h>
 #include <stdint.h>
@@ -52,7 +61,7 @@
 /* Numbers are the ggml element-type ids stored in GGUF tensor records.     */
 /* ------------------------------------------------------------------------ */
 enum {
-    OR_F32 = 0, OR_F16 = 1, OR_Q4_0 = 2, OR_Q8_0 = 8,
+    OR_F32 = 0, OR_F16 = 1, OR_Q4_0 = 2, OR_Q4_1 = 3, OR_Q5_0 = 6, OR_Q8_0 = 8, OR_Q8_1 = 9,
     OR_Q4_K = 12, OR_Q6_K = 14, OR_Q8_K = 15
 };
 
@@ -62,6 +71,9 @@ int or_type_info(int type, int *elems, int *bytes) {
     case OR_F32:  *elems = 1;   *bytes = 4;   return 0;
     case OR_F16:  *elems = 1;   *bytes = 2;   return 0;
     case OR_Q4_0: *elems = 32;  *bytes = 18;  return 0;
+    case OR_Q4_1: *elems = 32;  *bytes = 20;  return 0;
+    case OR_Q5_0: *elems = 32;  *bytes = 22;  return 0;
+    case OR_Q8_1: *elems = 32;  *bytes = 36;  return 0;
     case OR_Q8_0: *elems = 32;  *bytes = 34;  return 0;
     case OR_Q4_K: *elems = 256; *bytes = 144; return 0;
     case OR_Q6_K: *elems = 256; *bytes = 210; return 0;
@@ -85,6 +97,9 @@ int64_t or_type_nbytes(int type, int64_t n) {
 /* ------------------------------------------------------------------------ */
 typedef struct { uint16_t d; int8_t qs[32]; } or_block_q8_0;
 typedef struct { uint16_t d; uint8_t qs[16]; } or_block_q4_0;
+typedef struct { uint16_t d, m; uint8_t qs[16]; } or_block_q4_1;
+typedef struct { uint16_t d; uint8_t qh[4]; uint8_t qs[16]; } or_block_q5_0;
+typedef struct { uint16_t d, s; int8_t qs[32]; } or_block_q8_1;
 typedef struct {
     uint16_t d;
     uint16_t dmin;
@@ -101,6 +116,9 @@ typedef struct { float d; int8_t qs[256]; int16_t bsums[16]; } or_block_q8_k;
 
 _Static_assert(sizeof(or_block_q8_0) == 34, "Q8_0 block is 34 bytes");
 _Static_assert(sizeof(or_block_q4_0) == 18, "Q4_0 block is 18 bytes");
+_Static_assert(sizeof(or_block_q4_1) == 20, "Q4_1 block is 20 bytes");
+_Static_assert(sizeof(or_block_q5_0) == 22, "Q5_0 block is 22 bytes");
+_Static_assert(sizeof(or_block_q8_1) == 36, "Q8_1 block is 36 bytes");
 _Static_assert(sizeof(or_block_q4_k) == 144, "Q4_K block is 144 bytes");
 _Static_assert(sizeof(or_block_q6_k) == 210, "Q6_K block is 210 bytes");
 _Static_assert(sizeof(or_block_q8_k) == 292, "Q8_K block is 292 bytes");
@@ -228,6 +246,98 @@ void or_quantize_q4_0(const float *x, uint8_t *out, int64_t n) {
     }
 }
 
+/* Q4_1 ([lesson21] Example 7): per block of 32, min and max of the values,
+ * d = (max - min) / 15, id = 1/d (0 when d == 0), store f16(d) and
+ * f16(min), code = min(15, (int)((x - min) * id + 0.5f)) with the
+ * subtraction, the multiply and the add each rounded in f32, using the
+ * unrounded min; nibbles in Q4_0's order (byte j: element j low, j+16 high). */
+void or_quantize_q4_1(const float *x, uint8_t *out, int64_t n) {
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const float *xb = x + b * 32;
+        float mn = 3.4028234663852886e38f, mx = -3.4028234663852886e38f;
+        for (int j = 0; j < 32; ++j) {
+            if (xb[j] < mn) mn = xb[j];
+            if (xb[j] > mx) mx = xb[j];
+        }
+        float d = (mx - mn) / 15.0f;
+        float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+        int code[32];
+        for (int j = 0; j < 32; ++j) {
+            float diff = xb[j] - mn;
+            float scaled = diff * id;
+            float shifted = scaled + 0.5f;
+            int c = isnan(shifted) ? 0 : (int)shifted; /* truncation toward zero; shifted >= 0 */
+            code[j] = c < 15 ? c : 15;
+        }
+        or_block_q4_1 blk;
+        blk.d = or_f32_to_f16(d);
+        blk.m = or_f32_to_f16(mn);
+        for (int j = 0; j < 16; ++j)
+            blk.qs[j] = (uint8_t)(code[j] | (code[j + 16] << 4));
+        memcpy(out + b * 20, &blk, 20);
+    }
+}
+
+/* Q5_0 ([lesson21] Example 8): the Q4_0 rule with 5-bit codes -- the first
+ * element of strictly largest magnitude gives max, d = max / -16, id = 1/d
+ * (0 when d == 0), code = min(31, (int)(x * id + 16.5f)) with the multiply
+ * and the add rounded separately. The low 4 bits go into nibbles as in
+ * Q4_0; bit j of the 32-bit little-endian word qh is bit 4 of code j. */
+void or_quantize_q5_0(const float *x, uint8_t *out, int64_t n) {
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const float *xb = x + b * 32;
+        float amax = 0.0f, max = 0.0f;
+        for (int j = 0; j < 32; ++j) {
+            if (amax < fabsf(xb[j])) {
+                amax = fabsf(xb[j]);
+                max = xb[j];
+            }
+        }
+        float d = max / -16.0f;
+        float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+        int code[32];
+        for (int j = 0; j < 32; ++j) {
+            float scaled = xb[j] * id;
+            float shifted = scaled + 16.5f;
+            int c = isnan(shifted) ? 0 : (int)shifted;
+            code[j] = c < 31 ? c : 31;
+        }
+        or_block_q5_0 blk;
+        blk.d = or_f32_to_f16(d);
+        uint32_t qh = 0;
+        for (int j = 0; j < 32; ++j) qh |= (uint32_t)((code[j] >> 4) & 1) << j;
+        for (int i = 0; i < 4; ++i) blk.qh[i] = (uint8_t)(qh >> (8 * i));
+        for (int j = 0; j < 16; ++j)
+            blk.qs[j] = (uint8_t)((code[j] & 0x0F) | ((code[j + 16] & 0x0F) << 4));
+        memcpy(out + b * 22, &blk, 22);
+    }
+}
+
+/* Q8_1 activations (the reading stated at the top of this file): the Q8_0
+ * rule, plus s = f16(d * sum of codes) with the f32 d. */
+void or_quantize_q8_1(const float *x, uint8_t *out, int64_t n) {
+    for (int64_t b = 0; b < n / 32; ++b) {
+        const float *xb = x + b * 32;
+        float amax = 0.0f;
+        for (int j = 0; j < 32; ++j) {
+            float a = fabsf(xb[j]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+        or_block_q8_1 blk;
+        int sum = 0;
+        for (int j = 0; j < 32; ++j) {
+            float scaled = xb[j] * id;
+            blk.qs[j] = (int8_t)or_code_from_rounded(roundf(scaled), -128, 127);
+            sum += blk.qs[j];
+        }
+        blk.d = or_f32_to_f16(d);
+        blk.s = or_f32_to_f16((float)sum * d);
+        memcpy(out + b * 36, &blk, 36);
+    }
+}
+
 /* Q8_K activations ([candle] block table: f32 d, 256 codes, 16 bsums, each
  * the sum of 16 codes; [rml] Quantized dot products: bsums serve the K-quant
  * min term).  The rule itself is not printed; the reading used here is the
@@ -265,6 +375,23 @@ void or_quantize_q8_k(const float *x, uint8_t *out, int64_t n) {
 /* Q4_0 element e of a block: byte e mod 16, low nibble for e < 16, high
  * nibble otherwise; the stored code c means c - 8 ([lesson21] Example 5). */
 static int q4_0_code(const or_block_q4_0 *b, int e) {
+    uint8_t byte = b->qs[e % 16];
+    return (e < 16) ? (byte & 0x0F) : (byte >> 4);
+}
+
+/* Q5_0 element e: low 4 bits as in Q4_0, bit 4 = bit e of qh (the
+ * decoder of [lesson21] Example 8 rebuilds it from bit j and bit j + 16);
+ * the stored code c means c - 16. */
+static int q5_0_code(const or_block_q5_0 *b, int e) {
+    uint32_t qh = (uint32_t)b->qh[0] | ((uint32_t)b->qh[1] << 8) | ((uint32_t)b->qh[2] << 16) |
+                  ((uint32_t)b->qh[3] << 24);
+    uint8_t byte = b->qs[e % 16];
+    int lo4 = (e < 16) ? (byte & 0x0F) : (byte >> 4);
+    return lo4 | (int)(((qh >> e) & 1u) << 4);
+}
+
+/* Q4_1 element e: the nibble in Q4_0's order; its value is code * d + m. */
+static int q4_1_code(const or_block_q4_1 *b, int e) {
     uint8_t byte = b->qs[e % 16];
     return (e < 16) ? (byte & 0x0F) : (byte >> 4);
 }
@@ -322,6 +449,27 @@ static void dequant_block(int type, const uint8_t *src, float *dst) {
         for (int e = 0; e < 32; ++e) dst[e] = (float)(q4_0_code(&b, e) - 8) * d;
         break;
     }
+    case OR_Q4_1: {
+        or_block_q4_1 b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d), m = or_f16_to_f32(b.m);
+        for (int e = 0; e < 32; ++e) {
+            float value = (float)q4_1_code(&b, e) * d; /* exact: 11 + 4 bits */
+            dst[e] = value + m;                         /* the only rounding */
+        }
+        break;
+    }
+    case OR_Q5_0: {
+        or_block_q5_0 b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d);
+        for (int e = 0; e < 32; ++e) dst[e] = (float)(q5_0_code(&b, e) - 16) * d;
+        break;
+    }
+    case OR_Q8_1: {
+        or_block_q8_1 b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d);
+        for (int e = 0; e < 32; ++e) dst[e] = (float)b.qs[e] * d;
+        break;
+    }
     case OR_Q4_K: {
         or_block_q4_k b; memcpy(&b, src, sizeof b);
         float d = or_f16_to_f32(b.d), dmin = or_f16_to_f32(b.dmin);
@@ -368,11 +516,13 @@ int or_dequantize(int type, const uint8_t *src, float *dst, int64_t n) {
 
 /* ------------------------------------------------------------------------ */
 /* Weight -> activation pairing ([rml] DotActivationType; [candle]          */
-/* VecDotType table): Q4_0 and Q8_0 pair with Q8_0, the K-quants with Q8_K. */
+/* VecDotType table): Q4_0, Q5_0 and Q8_0 pair with Q8_0, Q4_1 with Q8_1,   */
+/* the K-quants with Q8_K.                                                  */
 /* ------------------------------------------------------------------------ */
 int or_act_type(int wtype) {
     switch (wtype) {
-    case OR_Q4_0: case OR_Q8_0: return OR_Q8_0;
+    case OR_Q4_0: case OR_Q5_0: case OR_Q8_0: return OR_Q8_0;
+    case OR_Q4_1: return OR_Q8_1;
     case OR_Q4_K: case OR_Q6_K: return OR_Q8_K;
     default: return -1;
     }
@@ -389,6 +539,8 @@ int or_isums_per_block(int wtype) { return wtype == OR_Q4_K ? 2 : 1; }
 /*                                                                          */
 /*   Q8_0: S = sum_i qw_i * qx_i                 ([lesson21] Example 10)    */
 /*   Q4_0: S = sum_i (code_i - 8) * qx_i         ([lesson21] Example 11)    */
+/*   Q5_0: S = sum_i (code_i - 16) * qx_i        ([lesson21] Example 8)     */
+/*   Q4_1: S = sum_i code_i * qx_i (the min m enters with s_x, below)       */
 /*   Q4_K: S_q = sum_j sc_j * sum_{i in j} q_i * a_i,                       */
 /*         S_m = sum_j m_j * sum_{i in j} a_i    ([rml] Quantized dot)      */
 /*   Q6_K: S = sum_j sc_j * sum_{i in j} (q_i - 32) * a_i                   */
@@ -406,6 +558,20 @@ static void block_sums(int wtype, const uint8_t *wblk, const uint8_t *xblk, int3
         or_block_q4_0 w; or_block_q8_0 x; memcpy(&w, wblk, 18); memcpy(&x, xblk, 34);
         int32_t s = 0;
         for (int i = 0; i < 32; ++i) s += (int32_t)(q4_0_code(&w, i) - 8) * (int32_t)x.qs[i];
+        out[0] = s;
+        break;
+    }
+    case OR_Q5_0: {
+        or_block_q5_0 w; or_block_q8_0 x; memcpy(&w, wblk, 22); memcpy(&x, xblk, 34);
+        int32_t s = 0;
+        for (int i = 0; i < 32; ++i) s += (int32_t)(q5_0_code(&w, i) - 16) * (int32_t)x.qs[i];
+        out[0] = s;
+        break;
+    }
+    case OR_Q4_1: {
+        or_block_q4_1 w; or_block_q8_1 x; memcpy(&w, wblk, 20); memcpy(&x, xblk, 36);
+        int32_t s = 0;
+        for (int i = 0; i < 32; ++i) s += (int32_t)q4_1_code(&w, i) * (int32_t)x.qs[i];
         out[0] = s;
         break;
     }
@@ -444,11 +610,18 @@ static void block_sums(int wtype, const uint8_t *wblk, const uint8_t *xblk, int3
     }
 }
 
-/* Block scales as doubles: (d_w, dmin_w, d_x). dmin_w is 0 except Q4_K. */
+/* Block scales as doubles: (d_w, dmin_w, d_x) and the additive term off
+ * (Q4_1: m_w * s_x, else 0). dmin_w is 0 except Q4_K. */
 static void block_scales(int wtype, const uint8_t *wblk, const uint8_t *xblk,
-                         double *dw, double *dmin, double *dx) {
+                         double *dw, double *dmin, double *dx, double *off) {
     *dmin = 0.0;
+    *off = 0.0;
     switch (wtype) {
+    case OR_Q5_0: { or_block_q5_0 w; or_block_q8_0 x; memcpy(&w, wblk, 22); memcpy(&x, xblk, 34);
+        *dw = or_f16_to_f32(w.d); *dx = or_f16_to_f32(x.d); break; }
+    case OR_Q4_1: { or_block_q4_1 w; or_block_q8_1 x; memcpy(&w, wblk, 20); memcpy(&x, xblk, 36);
+        *dw = or_f16_to_f32(w.d); *dx = or_f16_to_f32(x.d);
+        *off = (double)or_f16_to_f32(w.m) * (double)or_f16_to_f32(x.s); break; }
     case OR_Q8_0: { or_block_q8_0 w, x; memcpy(&w, wblk, 34); memcpy(&x, xblk, 34);
         *dw = or_f16_to_f32(w.d); *dx = or_f16_to_f32(x.d); break; }
     case OR_Q4_0: { or_block_q4_0 w; or_block_q8_0 x; memcpy(&w, wblk, 18); memcpy(&x, xblk, 34);
@@ -490,8 +663,9 @@ int or_block_isums(int wtype, const uint8_t *W, const uint8_t *xq, int32_t *isum
 
 /* y[v * n_out + o] for rows o in [row0, row1), accumulated in f64 over the
  * row's blocks ([lesson21] Example 10: integer sum per block times both
- * scales):  Q8_0/Q4_0/Q6_K: T_b = d_w * d_x * S;
- *           Q4_K:           T_b = d_x * (d_w * S_q - dmin_w * S_m). */
+ * scales):  Q8_0/Q4_0/Q5_0/Q6_K: T_b = d_w * d_x * S;
+ *           Q4_1:                T_b = d_w * d_x * S + m_w * s_x;
+ *           Q4_K:                T_b = d_x * (d_w * S_q - dmin_w * S_m). */
 int or_gemv(int wtype, const uint8_t *W, const uint8_t *xq, double *y,
             int64_t n_out, int64_t n_in, int64_t n_vec, int64_t row0, int64_t row1) {
     int wel, wby, xby;
@@ -505,13 +679,13 @@ int or_gemv(int wtype, const uint8_t *W, const uint8_t *xq, double *y,
                 const uint8_t *wb = W + (o * nb + b) * wby;
                 const uint8_t *xb = xq + (v * nb + b) * xby;
                 int32_t s[2] = {0, 0};
-                double dw, dmin, dx;
+                double dw, dmin, dx, off;
                 block_sums(wtype, wb, xb, s);
-                block_scales(wtype, wb, xb, &dw, &dmin, &dx);
+                block_scales(wtype, wb, xb, &dw, &dmin, &dx, &off);
                 if (wtype == OR_Q4_K)
                     acc += dx * (dw * (double)s[0] - dmin * (double)s[1]);
                 else
-                    acc += dw * dx * (double)s[0];
+                    acc += dw * dx * (double)s[0] + off;
             }
             y[v * n_out + o] = acc;
         }
@@ -526,6 +700,10 @@ static double exact_weight(int wtype, const uint8_t *blk, int e) {
         return (double)b.qs[e] * (double)or_f16_to_f32(b.d); }
     case OR_Q4_0: { or_block_q4_0 b; memcpy(&b, blk, 18);
         return (double)(q4_0_code(&b, e) - 8) * (double)or_f16_to_f32(b.d); }
+    case OR_Q5_0: { or_block_q5_0 b; memcpy(&b, blk, 22);
+        return (double)(q5_0_code(&b, e) - 16) * (double)or_f16_to_f32(b.d); }
+    case OR_Q4_1: { or_block_q4_1 b; memcpy(&b, blk, 20);
+        return (double)q4_1_code(&b, e) * (double)or_f16_to_f32(b.d) + (double)or_f16_to_f32(b.m); }
     case OR_Q4_K: { or_block_q4_k b; memcpy(&b, blk, 144);
         int sc, m; q4_k_scale_min(b.scales, e / 32, &sc, &m);
         return (double)or_f16_to_f32(b.d) * sc * q4_k_code(&b, e)
@@ -539,13 +717,17 @@ static double exact_weight(int wtype, const uint8_t *blk, int e) {
 static double exact_act(int atype, const uint8_t *blk, int e) {
     if (atype == OR_Q8_0) { or_block_q8_0 b; memcpy(&b, blk, 34);
         return (double)b.qs[e] * (double)or_f16_to_f32(b.d); }
+    if (atype == OR_Q8_1) { or_block_q8_1 b; memcpy(&b, blk, 36);
+        return (double)b.qs[e] * (double)or_f16_to_f32(b.d); }
     or_block_q8_k b; memcpy(&b, blk, 292);
     return (double)b.qs[e] * (double)b.d;
 }
 
 /* Second form ([sipllm] The fused matmul: dequantize one row, then dot):
  * dequantize W and the quantized activations to exact doubles and take a
- * plain f64 dot. Equal to or_gemv up to f64 rounding. */
+ * plain f64 dot. Equal to or_gemv up to f64 rounding, except for Q4_1,
+ * whose block form takes the min term through the f16-rounded s_x: there
+ * the two differ by sum_b m_w * (s_x - d_x * sum of codes). */
 int or_gemv_dequant(int wtype, const uint8_t *W, const uint8_t *xq, double *y,
                     int64_t n_out, int64_t n_in, int64_t n_vec) {
     int wel, wby, xby;

@@ -124,6 +124,72 @@ def test_dequant_is_the_correctly_rounded_exact_value():
                 r = Fraction(float(vals[32 * b + e])) / d
                 assert r.denominator == 1
                 assert (-128 <= r <= 127) if t == oracle.Q8_0 else (-8 <= r <= 7)
+    # Q5_0 and Q8_1: d times an integer in [-16, 15] / [-128, 127];
+    # Q4_1: code * d is exact in f32 (15 bits), so the value is the exact
+    # code * d + m rounded once.
+    for t, nbytes in ((oracle.Q5_0, 22), (oracle.Q8_1, 36), (oracle.Q4_1, 20)):
+        raw = bytearray(RNG.integers(0, 256, nbytes * 8, dtype=np.uint8).tobytes())
+        for b in range(8):
+            raw[nbytes * b:nbytes * b + 2] = np.float16(RNG.standard_normal()).tobytes()
+            if t == oracle.Q4_1:
+                raw[nbytes * b + 2:nbytes * b + 4] = np.float16(RNG.standard_normal()).tobytes()
+        raw = bytes(raw)
+        vals = oracle.dequantize(t, np.frombuffer(raw, np.uint8), 256)
+        for b in range(8):
+            blk = raw[nbytes * b:nbytes * (b + 1)]
+            d = half(blk, 0)
+            for e in range(32):
+                if t == oracle.Q4_1:
+                    byte = blk[4 + e % 16]
+                    code = byte & 0xF if e < 16 else byte >> 4
+                    assert float(vals[32 * b + e]) == f32_round(code * d + half(blk, 2))
+                    continue
+                r = Fraction(float(vals[32 * b + e])) / d
+                assert r.denominator == 1
+                assert (-16 <= r <= 15) if t == oracle.Q5_0 else (-128 <= r <= 127)
+
+
+def test_q5_0_every_bit_is_one_bit_of_one_element():
+    # "Building Q8_0 and Q4_0 Like ggml", Example 8: bit j of the 32-bit qh
+    # word is bit 4 of code j; the low 4 bits sit in nibbles as in Q4_0
+    # (byte j: element j low, element j + 16 high). Setting one bit of a zero
+    # block (codes 0, value -16 d) raises exactly one element by its weight.
+    base = bytearray(22)
+    base[0:2] = np.float16(1.0).tobytes()
+    v0 = oracle.dequantize(oracle.Q5_0, np.frombuffer(bytes(base), np.uint8), 32)
+    assert np.all(v0 == -16.0)
+    for bit in range(8 * 20):
+        raw = bytearray(base)
+        raw[2 + bit // 8] |= 1 << (bit % 8)
+        v = oracle.dequantize(oracle.Q5_0, np.frombuffer(bytes(raw), np.uint8), 32) - v0
+        hit = np.nonzero(v)[0]
+        assert hit.size == 1
+        if bit < 32:                                   # qh, little-endian word
+            assert hit[0] == bit and v[hit[0]] == 16
+        else:
+            j, k = divmod(bit - 32, 8)
+            assert hit[0] == (j if k < 4 else j + 16)
+            assert v[hit[0]] == 1 << (k % 4)
+
+
+def test_q8_1_is_q8_0_plus_the_scaled_code_sum():
+    # "量化格式" (candle): Q8_1 is the activation format of the _1 types and
+    # carries the block's sum beside Q8_0's d and codes. The codes and d must
+    # be Q8_0's bytes, and s the f16 of d times the code sum.
+    x = RNG.standard_normal(32 * 64).astype(np.float32)
+    x[::97] *= 50
+    q1 = oracle.quantize(oracle.Q8_1, x).reshape(64, 36)
+    q0 = oracle.quantize(oracle.Q8_0, x).reshape(64, 34)
+    assert np.array_equal(q1[:, 0:2], q0[:, 0:2])
+    assert np.array_equal(q1[:, 4:], q0[:, 2:])
+    for b in range(64):
+        d = float(np.frombuffer(q0[b, 0:2].tobytes(), np.float16)[0])
+        s = float(np.frombuffer(q1[b, 2:4].tobytes(), np.float16)[0])
+        tot = int(q1[b, 4:].view(np.int8).astype(np.int64).sum())
+        # s was rounded from the f32 d, which is within 2^-11 of the f16 d
+        assert abs(s - d * tot) <= (2.0 ** -10) * abs(d * tot) + 1e-7
+    assert np.array_equal(oracle.dequantize(oracle.Q8_1, q1.reshape(-1), x.size),
+                          oracle.dequantize(oracle.Q8_0, q0.reshape(-1), x.size))
 
 
 # ----------------------------------------------- Q4_K packing structure
@@ -277,17 +343,26 @@ def test_zero_block_gives_zero():
     W = oracle.quantize(oracle.Q8_0, RNG.standard_normal(256).astype(np.float32))
     xq = oracle.quantize(oracle.Q8_0, np.zeros(256, np.float32))
     assert oracle.gemv(oracle.Q8_0, W, xq, 1, 256, 1)[0, 0] == 0.0
+    # Q5_0: d = -0.0, every code 16 (all fifth bits set, nibbles 0)
+    q = oracle.quantize(oracle.Q5_0, np.zeros(32, np.float32))
+    assert q.tobytes() == bytes([0x00, 0x80]) + bytes([0xFF]) * 4 + bytes(16)
+    assert not oracle.dequantize(oracle.Q5_0, q, 32).any()
+    # Q4_1: d = 0, m = 0, codes 0; a constant block keeps its value in m
+    assert not oracle.quantize(oracle.Q4_1, np.zeros(32, np.float32)).any()
+    q = oracle.quantize(oracle.Q4_1, np.full(32, 0.75, np.float32))
+    assert np.all(oracle.dequantize(oracle.Q4_1, q, 32) == 0.75)
+    assert not oracle.quantize(oracle.Q8_1, np.zeros(32, np.float32)).any()
 
 
 # -------------------------------------------------- brute force on tiny inputs
 def random_weights(t, n_out, n_in):
-    if t in (oracle.Q8_0, oracle.Q4_0):
+    if t in (oracle.Q8_0, oracle.Q4_0, oracle.Q5_0, oracle.Q4_1):
         return oracle.quantize(t, (RNG.standard_normal(n_out * n_in) * 0.02).astype(np.float32))
     nb = n_out * n_in // 256
     return np.frombuffer(b"".join(random_k_block(t) for _ in range(nb)), np.uint8).copy()
 
 
-@pytest.mark.parametrize("t", [oracle.Q8_0, oracle.Q4_0, oracle.Q4_K, oracle.Q6_K])
+@pytest.mark.parametrize("t", [oracle.Q8_0, oracle.Q4_0, oracle.Q5_0, oracle.Q4_K, oracle.Q6_K])
 def test_block_form_equals_dequantize_then_f64_dot(t):
     for n_out, n_in, n_vec in ((1, 256, 1), (3, 512, 2), (8, 512, 3)):
         W = random_weights(t, n_out, n_in)
@@ -300,6 +375,32 @@ def test_block_form_equals_dequantize_then_f64_dot(t):
         ad = oracle.dequantize(oracle.act_type(t), xq, n_vec * n_in).reshape(n_vec, n_in)
         mag = np.abs(ad.astype(np.float64)) @ np.abs(wd).T
         assert np.all(np.abs(y - yb) <= 1e-12 * mag + 1e-300)
+
+
+def test_q4_1_block_form_differs_only_by_the_rounded_activation_sum():
+    # Q4_1 against Q8_1: each block's dot splits into d_w d_x sum(code q)
+    # plus m_w times the activation sum; the block form takes that sum as the
+    # stored f16 s. So block form minus the exact f64 dot is, per block,
+    # m_w (s - d_x sum q), and |s - d_x sum q| <= 2^-10 |d_x sum q| (f16
+    # rounding of a value computed from the f32 d).
+    n_out, n_in, n_vec = 5, 512, 3
+    W = random_weights(oracle.Q4_1, n_out, n_in)
+    x = (RNG.standard_normal(n_vec * n_in) + 0.3).astype(np.float32)
+    xq = oracle.quantize(oracle.Q8_1, x)
+    y = oracle.gemv(oracle.Q4_1, W, xq, n_out, n_in, n_vec)
+    yb = oracle.gemv_dequant(oracle.Q4_1, W, xq, n_out, n_in, n_vec)
+    nb = n_in // 32
+    Wb = W.reshape(n_out, nb, 20)
+    Xb = xq.reshape(n_vec, nb, 36)
+    m = np.frombuffer(Wb[:, :, 2:4].tobytes(), np.float16).astype(np.float64).reshape(n_out, nb)
+    dx = np.frombuffer(Xb[:, :, 0:2].tobytes(), np.float16).astype(np.float64).reshape(n_vec, nb)
+    sx = np.frombuffer(Xb[:, :, 2:4].tobytes(), np.float16).astype(np.float64).reshape(n_vec, nb)
+    cs = Xb[:, :, 4:].view(np.int8).astype(np.float64).sum(axis=2)
+    corr = (sx - dx * cs) @ m.T                                    # [n_vec, n_out]
+    assert np.allclose(y, yb + corr, rtol=1e-12, atol=1e-12)
+    bound = (2.0 ** -10) * (np.abs(dx * cs) @ np.abs(m).T)
+    assert np.all(np.abs(y - yb) <= bound + 1e-12)
+    assert np.any(corr != 0)
 
 
 def test_block_isums_by_hand_for_one_q8_0_and_q4_0_block():
@@ -315,6 +416,15 @@ def test_block_isums_by_hand_for_one_q8_0_and_q4_0_block():
             nib = np.concatenate([qw[2:] & 0xF, qw[2:] >> 4]).astype(np.int64)
             cw = nib - 8
         assert s == int(np.dot(cw, cx))
+    # Q5_0 codes minus 16 against Q8_0; Q4_1 raw codes against Q8_1
+    qw, qx = oracle.quantize(oracle.Q5_0, w), oracle.quantize(oracle.Q8_0, x)
+    qh = int.from_bytes(qw[2:6].tobytes(), "little")
+    nib = np.concatenate([qw[6:] & 0xF, qw[6:] >> 4]).astype(np.int64)
+    cw = nib + 16 * np.array([(qh >> j) & 1 for j in range(32)]) - 16
+    assert int(oracle.block_isums(oracle.Q5_0, qw, qx, 1, 32, 1)[0, 0, 0, 0]) == int(np.dot(cw, qx[2:].view(np.int8)))
+    qw, qx = oracle.quantize(oracle.Q4_1, w), oracle.quantize(oracle.Q8_1, x)
+    nib = np.concatenate([qw[4:] & 0xF, qw[4:] >> 4]).astype(np.int64)
+    assert int(oracle.block_isums(oracle.Q4_1, qw, qx, 1, 32, 1)[0, 0, 0, 0]) == int(np.dot(nib, qx[4:].view(np.int8)))
 
 
 def test_q4_k_min_term_equals_bsum_pairs():

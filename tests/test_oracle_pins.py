@@ -13,8 +13,9 @@ import oracle
 from goldens import floats, hexbytes, ints, keyvals, rows
 from javarand import JavaRandom
 
-ORACLE_TYPES = {"Q4_0": oracle.Q4_0, "Q8_0": oracle.Q8_0, "Q4_K": oracle.Q4_K,
-                "Q6_K": oracle.Q6_K, "Q8_K": oracle.Q8_K}
+ORACLE_TYPES = {"Q4_0": oracle.Q4_0, "Q4_1": oracle.Q4_1, "Q5_0": oracle.Q5_0,
+                "Q8_0": oracle.Q8_0, "Q4_K": oracle.Q4_K, "Q6_K": oracle.Q6_K,
+                "Q8_K": oracle.Q8_K}
 
 
 def lesson_block():
@@ -37,8 +38,19 @@ def test_type_table():
             assert oracle.type_info(ORACLE_TYPES[name]) == (elems, nbytes)
             assert oracle.type_nbytes(ORACLE_TYPES[name], 4096) == 4096 // elems * nbytes
             seen += 1
-    assert seen == 5
+    assert seen == 7
     assert oracle.type_info(99) is None
+
+
+def test_activation_pairing_follows_the_vec_dot_type_table():
+    # "量化格式" (candle), the VecDotType table: Q4_0/Q5_0/Q8_0 pair with
+    # Q8_0, Q4_1 with Q8_1, the K-quants with Q8K.
+    assert oracle.act_type(oracle.Q4_0) == oracle.Q8_0
+    assert oracle.act_type(oracle.Q5_0) == oracle.Q8_0
+    assert oracle.act_type(oracle.Q8_0) == oracle.Q8_0
+    assert oracle.act_type(oracle.Q4_1) == oracle.Q8_1
+    assert oracle.act_type(oracle.Q4_K) == oracle.Q8_K
+    assert oracle.act_type(oracle.Q6_K) == oracle.Q8_K
 
 
 def test_row_length_must_be_whole_blocks():
@@ -157,6 +169,50 @@ def test_lesson21_example14_hex():
         xb = x[32 * blk:32 * blk + 32]
         assert oracle.quantize(oracle.Q8_0, xb).tobytes().hex() == g[f"ex14_block{blk}_q8_0"]
         assert oracle.quantize(oracle.Q4_0, xb).tobytes().hex() == g[f"ex14_block{blk}_q4_0"]
+        assert oracle.quantize(oracle.Q4_1, xb).tobytes().hex() == g[f"ex14_block{blk}_q4_1"]
+        assert oracle.quantize(oracle.Q5_0, xb).tobytes().hex() == g[f"ex14_block{blk}_q5_0"]
+
+
+def page_rel_rmse_pct(y, x):
+    """The lesson's error measure: the difference taken in f32, squared and
+    summed in f64, over the f32 squares of x summed in f64."""
+    e = (y.astype(np.float32) - x.astype(np.float32)).astype(np.float64)
+    p = (x.astype(np.float32) * x.astype(np.float32)).astype(np.float64)
+    return 100 * math.sqrt(np.sum(e ** 2) / np.sum(p))
+
+
+def test_lesson21_example7_q4_1():
+    g = keyvals("lesson21_fixed_blocks.txt")
+    centered = lesson_block()
+    shifted = np.float32(2) + np.abs(centered)
+    for x, tag in ((centered, "centered"), (shifted, "shifted")):
+        lo, hi = float(x.min()), float(x.max())
+        assert [f"{lo:.3f}", f"{hi:.3f}"] == g[f"ex7_{tag}_range"].split()
+        q = oracle.quantize(oracle.Q4_1, x).tobytes()
+        # the printed d and m are the f32 values before f16 storage
+        d = np.float32(np.float32(hi) - np.float32(lo)) / np.float32(15)
+        assert f"{d:.4f}" == g[f"ex7_{tag}_d"]
+        assert f"{lo:.4f}" == g[f"ex7_{tag}_m"]
+        assert q[0] | (q[1] << 8) == oracle.f32_to_f16(d)
+        assert q[2] | (q[3] << 8) == oracle.f32_to_f16(lo)
+        y = oracle.dequantize(oracle.Q4_1, np.frombuffer(q, np.uint8), 32)
+        assert f"{page_rel_rmse_pct(y, x):.3f}" == g[f"ex7_{tag}_rmse_pct"]
+
+
+def test_lesson21_example8_q5_0():
+    g = keyvals("lesson21_fixed_blocks.txt")
+    x = lesson_block()
+    q = oracle.quantize(oracle.Q5_0, x).tobytes()
+    assert len(q) == 22
+    mx = x[np.argmax(np.abs(x))]                   # first of largest magnitude
+    assert f"{mx:.4f}" == g["ex8_max"]
+    assert f"{mx / np.float32(-16):.5f}" == g["ex8_d"]
+    qh = int.from_bytes(q[2:6], "little")
+    assert format(qh, "032b") == g["ex8_qh_bits"]
+    y = oracle.dequantize(oracle.Q5_0, np.frombuffer(q, np.uint8), 32)
+    assert f"{page_rel_rmse_pct(y, x):.3f}" == g["ex8_rmse_pct"]
+    # the same block is the first Q5_0 line of Example 14
+    assert q.hex() == g["ex14_block0_q5_0"]
 
 
 def test_lesson21_example5_q4_0_signed_max_and_nibbles():
@@ -247,9 +303,14 @@ def test_lesson21_example12_error_table():
     x = java_outlier_weights(JavaRandom(24), 65536)
     f16 = np.array([oracle.f16_to_f32(oracle.f32_to_f16(v)) for v in x], np.float32)
     assert f"{rel_rmse_pct(f16, x):.4f}" == g["ex12_f16_rmse_pct"]
-    for t, key in ((oracle.Q8_0, "ex12_q8_0_rmse_pct"), (oracle.Q4_0, "ex12_q4_0_rmse_pct")):
+    for t, key in ((oracle.Q8_0, "ex12_q8_0_rmse_pct"), (oracle.Q4_0, "ex12_q4_0_rmse_pct"),
+                   (oracle.Q5_0, "ex12_q5_0_rmse_pct"), (oracle.Q4_1, "ex12_q4_1_rmse_pct")):
         y = oracle.dequantize(t, oracle.quantize(t, x), x.size)
         assert f"{rel_rmse_pct(y, x):.4f}" == g[key]
+    for t, key in ((oracle.Q5_0, "ex12_q5_0_snr_db"), (oracle.Q4_1, "ex12_q4_1_snr_db")):
+        y = oracle.dequantize(t, oracle.quantize(t, x), x.size)
+        e = np.sum((y.astype(np.float64) - x) ** 2)
+        assert f"{10 * math.log10(np.sum(x.astype(np.float64) ** 2) / e):.2f}" == g[key]
 
 
 @pytest.mark.slow
