@@ -7,13 +7,14 @@ caller passes none, and calls the C entry points with raw device pointers and
 the current CUDA stream. There is no fallback: if the library is missing,
 importing this module raises.
 
-Element types are the ggml ids (Q4_0=2, Q8_0=8, Q4_K=12, Q6_K=14, Q8_K=15).
+Element types are the ggml ids (Q4_0=2, Q4_1=3, Q5_0=6, Q8_0=8, Q8_1=9,
+Q4_K=12, Q6_K=14, Q8_K=15).
 """
 import ctypes
 import os
 
 __all__ = [
-    "F32", "F16", "Q4_0", "Q8_0", "Q4_K", "Q6_K", "Q8_K", "MAX_NVEC", "QGError",
+    "F32", "F16", "Q4_0", "Q4_1", "Q5_0", "Q8_0", "Q8_1", "Q4_K", "Q6_K", "Q8_K", "MAX_NVEC", "QGError",
     "library_path", "lib", "qtype_nbytes", "qtype_block", "qtype_act_type",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes",
     "qgemv", "qgemv_xq", "qgemv_block_isums", "qgemv_noalloc", "qgemv_batched",
@@ -21,10 +22,10 @@ __all__ = [
     "MAX_BATCH",
 ]
 
-F32, F16, Q4_0, Q8_0, Q4_K, Q6_K, Q8_K = 0, 1, 2, 8, 12, 14, 15
+F32, F16, Q4_0, Q4_1, Q5_0, Q8_0, Q8_1, Q4_K, Q6_K, Q8_K = 0, 1, 2, 3, 6, 8, 9, 12, 14, 15
 MAX_NVEC = 8
-TYPE_NAMES = {F32: "F32", F16: "F16", Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K",
-              Q8_K: "Q8_K"}
+TYPE_NAMES = {F32: "F32", F16: "F16", Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0", Q8_0: "Q8_0",
+              Q8_1: "Q8_1", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K"}
 
 # every function declared in include/qgemv.h
 EXPORTED_SYMBOLS = (
@@ -165,7 +166,7 @@ def quantize_act(act_type: int, x, n_vec: int = 1, out=None, stream=None):
 
 
 def quantize_rows(t: int, x, n_rows: int, out=None, stream=None):
-    """Weights x (f32, n_rows * n_in) -> Q8_0 or Q4_0 blocks."""
+    """Weights x (f32, n_rows * n_in) -> Q8_0, Q4_0, Q4_1 or Q5_0 blocks."""
     torch = _torch()
     _dev_tensor(x, torch.float32, "x")
     n_in = x.numel() // n_rows

@@ -15,6 +15,9 @@ cudaError_t launch_quantize_batched_kernel(int type, int grid, int block, cudaSt
                                            uint8_t *out, int n_mats, int64_t blocks_per_mat);
 __global__ void dequant_q8_0_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q4_0_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q4_1_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q5_0_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q8_1_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q4_k_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q6_k_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q8_k_kernel(const uint8_t *, float *, int64_t);
@@ -36,7 +39,10 @@ bool block_info(int type, int *elems, int *bytes) {
     case QG_F32: *elems = 1; *bytes = 4; return true;
     case QG_F16: *elems = 1; *bytes = 2; return true;
     case QG_Q4_0: *elems = 32; *bytes = 18; return true;
+    case QG_Q4_1: *elems = 32; *bytes = 20; return true;
+    case QG_Q5_0: *elems = 32; *bytes = 22; return true;
     case QG_Q8_0: *elems = 32; *bytes = 34; return true;
+    case QG_Q8_1: *elems = 32; *bytes = 36; return true;
     case QG_Q4_K: *elems = 256; *bytes = 144; return true;
     case QG_Q6_K: *elems = 256; *bytes = 210; return true;
     case QG_Q8_K: *elems = 256; *bytes = 292; return true;
@@ -134,6 +140,8 @@ size_t act_smem_bytes(int type, int lpb, int nb, int nv) {
     switch (type) {
     case QG_Q8_0: return TypeQ8_0::act_bytes(nb, nv);
     case QG_Q4_0: return TypeQ4_0::act_bytes(nb, nv);
+    case QG_Q4_1: return TypeQ4_1::act_bytes(nb, nv);
+    case QG_Q5_0: return TypeQ5_0::act_bytes(nb, nv);
     case QG_Q4_K: return TypeQ4_K::act_bytes(nb, nv);
     case QG_Q6_K: return lpb == TypeQ6_K4::kLanesPerBlock ? TypeQ6_K4::act_bytes(nb, nv) : TypeQ6_K::act_bytes(nb, nv);
     default: return 0;
@@ -146,7 +154,7 @@ constexpr int kSmemTailPad = 16;  // unaligned word reads may touch up to 4 byte
 
 // Lanes of one activation block's f32 values (bytes) and lanes per weight
 // block, per type.
-int act_block_f32_bytes(int type) { return (type == QG_Q8_0 || type == QG_Q4_0) ? 128 : 1024; }
+int act_block_f32_bytes(int type) { return (type == QG_Q4_K || type == QG_Q6_K) ? 1024 : 128; }
 // The item variants a type offers (lanes per weight block); Q6_K has a
 // two-lane item (fewer instructions per code) and a four-lane one (its
 // 8-block iterations fill better for some row lengths).
@@ -383,6 +391,8 @@ cudaError_t launch_gemv(int type, const GemvParams &p, const GemvMat *mats, int 
     switch (type) {
     case QG_Q8_0: return launch_gemv_q8_0(p, mats, n, nv, isums, l, device, s);
     case QG_Q4_0: return launch_gemv_q4_0(p, mats, n, nv, isums, l, device, s);
+    case QG_Q4_1: return launch_gemv_q4_1(p, mats, n, nv, isums, l, device, s);
+    case QG_Q5_0: return launch_gemv_q5_0(p, mats, n, nv, isums, l, device, s);
     case QG_Q4_K: return launch_gemv_q4_k(p, mats, n, nv, isums, l, device, s);
     case QG_Q6_K: return launch_gemv_q6_k(p, mats, n, nv, isums, l, device, s);
     default: return cudaErrorInvalidValue;
@@ -564,7 +574,9 @@ int qtype_block(int type, int *elems, int *bytes) {
 int qtype_act_type(int weight_type) {
     switch (weight_type) {
     case QG_Q4_0:
+    case QG_Q5_0:
     case QG_Q8_0: return QG_Q8_0;
+    case QG_Q4_1: return QG_Q8_1;
     case QG_Q4_K:
     case QG_Q6_K: return QG_Q8_K;
     default: return QG_ERR_PAIR;
@@ -590,7 +602,7 @@ const char *qg_last_cuda_error(void) { return g_last_cuda_error; }
 int quantize_act(int act_type, const float *x, void *xq, int64_t n_in, int64_t n_vec, qg_stream_t stream) {
     int elems, bytes;
     if (!block_info(act_type, &elems, &bytes)) return QG_ERR_TYPE;
-    if (act_type != QG_Q8_0 && act_type != QG_Q8_K) return QG_ERR_TYPE;
+    if (act_type != QG_Q8_0 && act_type != QG_Q8_1 && act_type != QG_Q8_K) return QG_ERR_TYPE;
     if (n_in < 0 || n_vec < 0 || n_in % elems != 0) return QG_ERR_SHAPE;
     const int64_t n_blocks = n_in / elems * n_vec;
     if (n_blocks == 0) return QG_OK;
@@ -605,7 +617,7 @@ int quantize_act(int act_type, const float *x, void *xq, int64_t n_in, int64_t n
 int quantize_rows(int type, const float *x, void *out, int64_t n_rows, int64_t n_in, qg_stream_t stream) {
     int elems, bytes;
     if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
-    if (type != QG_Q8_0 && type != QG_Q4_0) return QG_ERR_TYPE;
+    if (type != QG_Q8_0 && type != QG_Q4_0 && type != QG_Q4_1 && type != QG_Q5_0) return QG_ERR_TYPE;
     if (n_in < 0 || n_rows < 0 || n_in % elems != 0) return QG_ERR_SHAPE;
     const int64_t n_blocks = n_in / elems * n_rows;
     if (n_blocks == 0) return QG_OK;
@@ -638,6 +650,9 @@ int dequantize_rows(int type, const void *W, float *out, int64_t n_rows, int64_t
     switch (type) {
     case QG_Q8_0: dequant_q8_0_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
     case QG_Q4_0: dequant_q4_0_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q4_1: dequant_q4_1_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q5_0: dequant_q5_0_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q8_1: dequant_q8_1_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
     case QG_Q4_K: dequant_q4_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
     case QG_Q6_K: dequant_q6_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
     case QG_Q8_K: dequant_q8_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
@@ -789,7 +804,8 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
         std::snprintf(buf, sizeof buf, "cuda: %s", g_last_cuda_error);
         return buf;
     }
-    const char *tn = type == QG_Q4_K ? "Q4_K" : type == QG_Q6_K ? "Q6_K" : type == QG_Q8_0 ? "Q8_0" : "Q4_0";
+    const char *tn = type == QG_Q4_K ? "Q4_K" : type == QG_Q6_K ? "Q6_K" : type == QG_Q8_0 ? "Q8_0"
+                   : type == QG_Q4_1 ? "Q4_1" : type == QG_Q5_0 ? "Q5_0" : "Q4_0";
     if (mma_preferred(type, n_vec)) {
         // tiles: a batch of equal matrices is assumed for the tile count
         const int64_t per = total_rows / n_mats;

@@ -55,6 +55,61 @@ __global__ void dequant_q4_0_kernel(const uint8_t *__restrict__ W, float *__rest
     }
 }
 
+// Q4_1: code * d is exact (4 + 11 bits), so code * d + m rounds once.
+__global__ void dequant_q4_1_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 2) * 20;
+        const float d = f16_bits_to_f32(ldg_u16(blk));
+        const float m = f16_bits_to_f32(ldg_u16(blk + 2));
+        const int q = static_cast<int>(g & 3);
+        const uint8_t *qs = blk + 4 + 8 * (q & 1);
+        const int shift = q >= 2 ? 4 : 0;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int code = (__ldg(qs + i) >> shift) & 0xF;
+            v[i] = __fadd_rn(__fmul_rn(static_cast<float>(code), d), m);
+        }
+        store8(out + g * 8, v);
+    }
+}
+
+// Q5_0: 5-bit code = nibble | bit e of qh << 4, value (code - 16) * d.
+__global__ void dequant_q5_0_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 2) * 22;
+        const float d = f16_bits_to_f32(ldg_u16(blk));
+        const uint32_t qh = ldg_u16(blk + 2) | (ldg_u16(blk + 4) << 16);
+        const int q = static_cast<int>(g & 3);
+        const uint8_t *qs = blk + 6 + 8 * (q & 1);
+        const int shift = q >= 2 ? 4 : 0;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = 8 * q + i;
+            const int code = ((__ldg(qs + i) >> shift) & 0xF) | (((qh >> e) & 1u) << 4);
+            v[i] = __fmul_rn(static_cast<float>(code - 16), d);
+        }
+        store8(out + g * 8, v);
+    }
+}
+
+// Q8_1: q * d (s is not part of the values).
+__global__ void dequant_q8_1_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 2) * 36;
+        const float d = f16_bits_to_f32(ldg_u16(blk));
+        const uint8_t *qs = blk + 4 + 8 * (g & 3);
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(static_cast<float>(static_cast<int8_t>(__ldg(qs + i))), d);
+        store8(out + g * 8, v);
+    }
+}
+
 __global__ void dequant_q4_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {

@@ -99,6 +99,8 @@ inline cudaError_t launch_gemv_type(const GemvParams &p, const GemvMat *mats, in
                      int device, cudaStream_t s);
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q8_0)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_0)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_1)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q5_0)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_k)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q6_k)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q6_k4)

@@ -9,6 +9,10 @@
 // packed fields):
 //   Q8_0  34 B: f16 d, int8 qs[32]                          value q * d
 //   Q4_0  18 B: f16 d, qs[16]; byte j = elem j | elem j+16 << 4, value (c - 8) * d
+//   Q4_1  20 B: f16 d, f16 m, qs[16] as Q4_0; value c * d + m
+//   Q5_0  22 B: f16 d, u32 qh (LE), qs[16] as Q4_0 for the low 4 bits; bit j of
+//               qh is bit 4 of code j; value (c - 16) * d
+//   Q8_1  36 B: f16 d, f16 s = f16(d * sum of codes), int8 qs[32] (activations)
 //   Q4_K 144 B: f16 d, f16 dmin, scales[12] (8 x 6-bit scale, 8 x 6-bit min),
 //               qs[128]; elem e in chunk e/64: low nibble of qs[32(e/64) + e%64]
 //               for e%64 < 32, else high nibble of qs[32(e/64) + e%64 - 32];
@@ -22,10 +26,12 @@
 // Exact block sums (the int32 part of every product):
 //   Q8_0: S = sum qw * qx
 //   Q4_0: S = sum c * qx - 8 * sum qx
+//   Q5_0: S = sum c * qx - 16 * sum qx
+//   Q4_1: S = sum c * qx  (the min enters as m_w * s_x)
 //   Q4_K: S_q = sum_j sc_j * sum_{i in j} q_i a_i ; S_m = sum_j m_j (bsum_2j + bsum_2j+1)
 //   Q6_K: S = sum_j sc_j * sum_{i in j} q_i a_i - 32 * sum_j sc_j * bsum_j
-// Float step: Q8_0, Q4_0, Q6_K: S * (d_w * d_x); Q4_K: d_x * (d_w * S_q -
-// dmin * S_m). In the product, a block's lanes each apply the float step to
+// Float step: Q8_0, Q4_0, Q5_0, Q6_K: S * (d_w * d_x); Q4_1: S * (d_w * d_x)
+// + m_w * s_x; Q4_K: d_x * (d_w * S_q - dmin * S_m). In the product, a block's lanes each apply the float step to
 // their own exact partial sums (no cross-lane sum per block); the
 // diagnostic mode adds the partials across the block's lanes first and
 // writes the whole-block sums.
@@ -239,6 +245,177 @@ struct TypeQ4_0 {
                 if (active) isum_row[v * isum_vstride + b] = s;
             } else if (active) {
                 acc[v] = fmaf(static_cast<float>(s), dw * __uint_as_float(ex.x), acc[v]);
+            }
+        }
+    }
+};
+
+// Bit 4 of each byte of a word from 4 consecutive bits of x (x < 16): the
+// multiplier places bit k at bit 8k + 4 (the shifted copies 7 bits apart
+// never overlap, so nothing carries).
+__device__ __forceinline__ uint32_t fifth_bits(uint32_t x4) { return (x4 * 0x02040810u) & 0x10101010u; }
+
+// Q5_0 (weights, paired with Q8_0): 22-byte blocks, 2-byte aligned.
+struct TypeQ5_0 {
+    static constexpr int kBlockElems = 32, kBlockBytes = 22, kLanesPerBlock = 1, kSums = 1;
+    static constexpr int kActValues = ActQ8_0::kValues;
+    static size_t act_bytes(int nb, int nv) { return ActQ8_0::bytes(nb, nv); }
+    __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
+        ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
+    }
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        ActQ8_0::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    }
+
+    template <int NV, bool ISUMS>
+    __device__ static void item(uint32_t rowa, int b, int /*sub*/, bool active, uint32_t acta, int nb,
+                                float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;
+        const float dw = f16_bits_to_f32(ld_s16(blk));
+        uint32_t w[5];  // qh, then the 16 nibble bytes
+        ld_words_a2<5>(blk + 2, w);
+        const uint32_t qh = w[0];
+        uint32_t lo[4], hi[4];  // 5-bit codes of elements 4i.. and 16+4i..
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo[i] = (w[1 + i] & 0x0F0F0F0Fu) | fifth_bits((qh >> (4 * i)) & 0xFu);
+            hi[i] = ((w[1 + i] >> 4) & 0x0F0F0F0Fu) | fifth_bits((qh >> (16 + 4 * i)) & 0xFu);
+        }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const uint32_t rec = acta + (static_cast<uint32_t>(v) * nb + b) * ActQ8_0::kRecord;
+            const uint4 a0 = ld_s128(rec), a1 = ld_s128(rec + 16), ex = ld_s128(rec + 32);
+            int s = dp4a(lo[0], a0.x, 0);
+            s = dp4a(lo[1], a0.y, s);
+            s = dp4a(lo[2], a0.z, s);
+            s = dp4a(lo[3], a0.w, s);
+            s = dp4a(hi[0], a1.x, s);
+            s = dp4a(hi[1], a1.y, s);
+            s = dp4a(hi[2], a1.z, s);
+            s = dp4a(hi[3], a1.w, s);
+            s -= 16 * static_cast<int>(ex.y);
+            if (ISUMS) {
+                if (active) isum_row[v * isum_vstride + b] = s;
+            } else if (active) {
+                acc[v] = fmaf(static_cast<float>(s), dw * __uint_as_float(ex.x), acc[v]);
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------------
+// Q8_1-paired type (Q4_1): the Q8_0 record with s_x in the third word of its
+// tail: qs[32] | f32 d_x | int32 sum(qs) | f32 s_x | 4 pad bytes.
+// ------------------------------------------------------------------------
+struct ActQ8_1 {
+    static constexpr int kRecord = ActQ8_0::kRecord;
+    static constexpr int kValues = 32;
+    static size_t bytes(int nb, int nv) { return static_cast<size_t>(nv) * nb * kRecord; }
+
+    // From byte-exact Q8_1 blocks: xq [nv][nb] x 36 B (4-byte aligned each).
+    __device__ static void stage(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
+        const int n = nb * nv;
+        for (int i = tid; i < n; i += nthr) {
+            const uint32_t *blk = reinterpret_cast<const uint32_t *>(xq + static_cast<size_t>(i) * 36);
+            const uint32_t ds = __ldg(blk);
+            uint32_t w[8];
+            int asum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                w[j] = __ldg(blk + 1 + j);
+                asum = dp4a(w[j], 0x01010101u, asum);
+            }
+            uint8_t *rec = act + static_cast<size_t>(i) * kRecord;
+            reinterpret_cast<uint4 *>(rec)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4 *>(rec)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            reinterpret_cast<uint4 *>(rec)[2] =
+                make_uint4(__float_as_uint(f16_bits_to_f32(ds)), static_cast<uint32_t>(asum),
+                           __float_as_uint(f16_bits_to_f32(ds >> 16)), 0u);
+        }
+    }
+
+    // From f32 values in shared memory (the Q8_0 rule, then s = f16(sum * d)
+    // from the f32 d): 4 lanes per block, 8 blocks per warp step.
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        for (int base = warp * 8; base < count; base += nwarps * 8) {
+            const int i = base + (lane >> 2);
+            const int part = lane & 3;
+            const bool ok = i < count;
+            float v[8];
+            if (ok) {
+                load8(xs + 4u * (32u * i + 8u * part), v);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+            }
+            float a = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(v[k]));
+            a = group_max<4>(a);
+            const float d = a / 127.0f;
+            const float id = d != 0.0f ? 1.0f / d : 0.0f;
+            uint32_t w[2];
+            const int sum = group_sum<4>(codes8(v, id, -128, 127, w));
+            if (ok) {
+                uint8_t *rec = act + static_cast<size_t>(g0 + i) * kRecord;
+                reinterpret_cast<uint2 *>(rec)[part] = make_uint2(w[0], w[1]);
+                if (part == 0) {
+                    const float dx = __half2float(__float2half_rn(d));
+                    const float sx = __half2float(__float2half_rn(__fmul_rn(static_cast<float>(sum), d)));
+                    reinterpret_cast<uint4 *>(rec)[2] = make_uint4(__float_as_uint(dx), static_cast<uint32_t>(sum),
+                                                                   __float_as_uint(sx), 0u);
+                }
+            }
+        }
+    }
+};
+
+// Q4_1 (weights, paired with Q8_1): 20-byte blocks. Rows start at multiples
+// of 20 bytes from a 16-byte aligned W and stages keep the address modulo
+// 16, so every block is 4-byte aligned in shared memory.
+struct TypeQ4_1 {
+    static constexpr int kBlockElems = 32, kBlockBytes = 20, kLanesPerBlock = 1, kSums = 1;
+    static constexpr int kActValues = ActQ8_1::kValues;
+    static size_t act_bytes(int nb, int nv) { return ActQ8_1::bytes(nb, nv); }
+    __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
+        ActQ8_1::stage(xq, act, nb, nv, tid, nthr);
+    }
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        ActQ8_1::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    }
+
+    template <int NV, bool ISUMS>
+    __device__ static void item(uint32_t rowa, int b, int /*sub*/, bool active, uint32_t acta, int nb,
+                                float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;
+        const uint32_t dm = ld_s32(blk);
+        const float dw = f16_bits_to_f32(dm), mw = f16_bits_to_f32(dm >> 16);
+        uint32_t qw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qw[i] = ld_s32(blk + 4 + 4 * i);
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo[i] = qw[i] & 0x0F0F0F0Fu;
+            hi[i] = (qw[i] >> 4) & 0x0F0F0F0Fu;
+        }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const uint32_t rec = acta + (static_cast<uint32_t>(v) * nb + b) * ActQ8_1::kRecord;
+            const uint4 a0 = ld_s128(rec), a1 = ld_s128(rec + 16), ex = ld_s128(rec + 32);
+            int s = dp4a(lo[0], a0.x, 0);
+            s = dp4a(lo[1], a0.y, s);
+            s = dp4a(lo[2], a0.z, s);
+            s = dp4a(lo[3], a0.w, s);
+            s = dp4a(hi[0], a1.x, s);
+            s = dp4a(hi[1], a1.y, s);
+            s = dp4a(hi[2], a1.z, s);
+            s = dp4a(hi[3], a1.w, s);
+            if (ISUMS) {
+                if (active) isum_row[v * isum_vstride + b] = s;
+            } else if (active) {
+                acc[v] = fmaf(static_cast<float>(s), dw * __uint_as_float(ex.x), acc[v]);
+                acc[v] = fmaf(mw, __uint_as_float(ex.z), acc[v]);
             }
         }
     }

@@ -16,15 +16,20 @@ Workloads (names used across tests and bench.py):
   layer_stack     32 decoder layers, each Q4_K q/k/v/o 4096 x 4096, Q4_K
                   gate/up 11008 x 4096, Q6_K down 4096 x 11008 (random blocks
                   as above), a fresh x ~ N(0, 1) per matrix and vector
+  q4_1_4096       Q4_1 weights from f32 N(0, 0.02) + 0.01, 4096 x 4096, x ~ N(0, 1)
+  q5_0_4096       Q5_0 weights from f32 N(0, 0.02), 4096 x 4096, x ~ N(0, 1)
 Seeds: weights 1000 + workload index, activations 2000 + workload index; the
 layer stack derives per-(layer, matrix) streams from those.
 """
 import numpy as np
 
-Q4_0, Q8_0, Q4_K, Q6_K = 2, 8, 12, 14
-BLOCK = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+Q4_0, Q4_1, Q5_0, Q8_0, Q4_K, Q6_K = 2, 3, 6, 8, 12, 14
+BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q5_0: (32, 22), Q8_0: (32, 34), Q4_K: (256, 144),
+         Q6_K: (256, 210)}
+FROM_F32 = (Q8_0, Q4_0, Q4_1, Q5_0)  # workloads that quantize f32 weights
 
-WORKLOADS = ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000", "layer_stack"]
+WORKLOADS = ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000", "layer_stack",
+             "q4_1_4096", "q5_0_4096"]
 
 # (name, type, n_out, n_in) of one decoder layer of the stack
 LAYER_MATRICES = [
@@ -72,6 +77,17 @@ def k_blocks(wtype: int, n_blocks: int, rng) -> np.ndarray:
     return raw.reshape(-1)
 
 
+def legacy_blocks(wtype: int, n_blocks: int, rng) -> np.ndarray:
+    """Random 32-element blocks with every code and bit pattern: uniform
+    bytes, then d (and Q4_1's m) = f16 of N(0,1) * 1e-2 (d of either sign)."""
+    _, nbytes = BLOCK[wtype]
+    raw = random_bytes(rng, n_blocks * nbytes).reshape(n_blocks, nbytes)
+    raw[:, 0:2] = (rng.standard_normal(n_blocks) * 1e-2).astype(np.float16).view(np.uint8).reshape(n_blocks, 2)
+    if wtype == Q4_1:
+        raw[:, 2:4] = (rng.standard_normal(n_blocks) * 1e-2).astype(np.float16).view(np.uint8).reshape(n_blocks, 2)
+    return raw.reshape(-1)
+
+
 def workload_index(name: str) -> int:
     return WORKLOADS.index(name) + 1
 
@@ -80,7 +96,8 @@ def single_matrix(name: str, n_vec: int = 1, n_out: int = None, n_in: int = None
     """Inputs of one of the single-matrix workloads, optionally resized.
 
     Returns dict(type, n_out, n_in, n_vec, x[f32 n_vec*n_in], and either
-    w_f32 (f32 weights to quantize, Q8_0/Q4_0) or w_blocks (uint8 blocks)).
+    w_f32 (f32 weights to quantize, Q8_0/Q4_0/Q4_1/Q5_0) or w_blocks (uint8
+    blocks)).
     """
     idx = workload_index(name)
     spec = {
@@ -88,6 +105,8 @@ def single_matrix(name: str, n_vec: int = 1, n_out: int = None, n_in: int = None
         "q4_0_4096": (Q4_0, 4096, 4096),
         "q4_k_4096": (Q4_K, 4096, 4096),
         "q6_k_32000": (Q6_K, 32000, 4096),
+        "q4_1_4096": (Q4_1, 4096, 4096),
+        "q5_0_4096": (Q5_0, 4096, 4096),
     }[name]
     t, d_out, d_in = spec
     n_out = d_out if n_out is None else n_out
@@ -95,8 +114,10 @@ def single_matrix(name: str, n_vec: int = 1, n_out: int = None, n_in: int = None
     wr = np.random.default_rng(1000 + idx)
     xr = np.random.default_rng(2000 + idx)
     out = dict(type=t, n_out=n_out, n_in=n_in, n_vec=n_vec, x=f32_normal(xr, n_vec * n_in))
-    if t in (Q8_0, Q4_0):
+    if t in FROM_F32:
         out["w_f32"] = f32_normal(wr, n_out * n_in, std=0.02)
+        if t == Q4_1:  # off-centre rows, where the min of Q4_1 matters
+            out["w_f32"] += np.float32(0.01)
     else:
         out["w_blocks"] = k_blocks(t, n_out * n_in // 256, wr)
     return out

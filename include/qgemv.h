@@ -1,10 +1,10 @@
 /*
  * qgemv.h - C ABI of the GB300 block-quantized matrix-vector product.
  *
- * y = W . x for W stored as byte-exact GGUF blocks (Q8_0, Q4_0, Q4_K,
- * Q6_K), x quantized once per call to the activation blocks paired with the
- * weight type (Q8_0 or Q8_K), exact int32 sums inside every block and float
- * only for the block scales.
+ * y = W . x for W stored as byte-exact GGUF blocks (Q8_0, Q4_0, Q4_1, Q5_0,
+ * Q4_K, Q6_K), x quantized once per call to the activation blocks paired
+ * with the weight type (Q8_0, Q8_1 or Q8_K), exact int32 sums inside every
+ * block and float only for the block scales.
  *
  * Citations name the reference pages by title and section:
  *   [rml]      "Quantization" (rayaq.ca/rml)
@@ -56,7 +56,10 @@ enum qg_type {
     QG_F32 = 0,
     QG_F16 = 1,
     QG_Q4_0 = 2,   /* 32 elements, 18 bytes: f16 d, 16 bytes of nibbles      */
+    QG_Q4_1 = 3,   /* 32 elements, 20 bytes: f16 d, f16 m, 16 bytes of nibbles */
+    QG_Q5_0 = 6,   /* 32 elements, 22 bytes: f16 d, u32 qh (fifth bits), 16 bytes of nibbles */
     QG_Q8_0 = 8,   /* 32 elements, 34 bytes: f16 d, 32 int8                  */
+    QG_Q8_1 = 9,   /* 32 elements, 36 bytes: f16 d, f16 s, 32 int8 (activations only) */
     QG_Q4_K = 12,  /* 256 elements, 144 bytes: f16 d, f16 dmin, 12 B scales, 128 B qs */
     QG_Q6_K = 14,  /* 256 elements, 210 bytes: 128 B ql, 64 B qh, 16 int8 scales, f16 d */
     QG_Q8_K = 15   /* 256 elements, 292 bytes: f32 d, 256 int8, 16 int16 bsums (activations only) */
@@ -88,8 +91,9 @@ int64_t qtype_nbytes(int type, int64_t n);
 int qtype_block(int type, int *elems, int *bytes);
 
 /* Activation type paired with a weight type ([rml] DotActivationType;
- * [candle] VecDotType table): Q4_0 and Q8_0 -> QG_Q8_0, Q4_K and Q6_K ->
- * QG_Q8_K. Returns QG_ERR_PAIR for any other type. */
+ * [candle] VecDotType table): Q4_0, Q5_0 and Q8_0 -> QG_Q8_0, Q4_1 ->
+ * QG_Q8_1, Q4_K and Q6_K -> QG_Q8_K. Returns QG_ERR_PAIR for any other
+ * type. */
 int qtype_act_type(int weight_type);
 
 /* Static text for a status code. Never NULL. */
@@ -106,6 +110,10 @@ const char *qg_last_cuda_error(void);
  *   act_type QG_Q8_0: per 32 elements amax = max |x|, d = amax / 127 (f32),
  *     id = 1/d (0 if d == 0), stored d = f16(d), code = roundf(x * id)
  *     (halves away from zero, codes from the unrounded id).
+ *   act_type QG_Q8_1: the Q8_0 rule, plus s = f16(sum of the codes * d)
+ *     computed in f32 from the unrounded d, a NaN s (only a block holding
+ *     inf gives one) stored as 0x7E00 (the pages pair Q8_1 with Q4_1 but
+ *     print neither its layout nor this rule: the library's reading).
  *   act_type QG_Q8_K: the same rule per 256 elements with d stored as f32,
  *     codes clamped to [-127, 127], and bsums[k] = sum of codes 16k..16k+15
  *     ([candle] block table; the pages do not print the rule, this is the
@@ -117,12 +125,19 @@ int quantize_act(int act_type, const float *x, void *xq, int64_t n_in, int64_t n
                  qg_stream_t stream);
 
 /* Weight quantization with ggml's reference rules, the bytes llama.cpp
- * writes ([lesson21] Examples 2 and 5):
+ * writes ([lesson21] Examples 2, 5, 7, 8 and 14):
  *   QG_Q8_0: as quantize_act(QG_Q8_0).
  *   QG_Q4_0: per 32 elements the first element of strictly largest |x| gives
  *     max, d = max / -8, id = 1/d (0 if d == 0), code = min(15, (int)(x*id +
  *     8.5f)) with the multiply and add rounded separately; byte j holds
  *     element j in its low nibble and element j+16 in its high nibble.
+ *   QG_Q4_1: per 32 elements min and max, d = (max - min) / 15, id = 1/d (0
+ *     if d == 0), stored f16(d) and f16(min), code = min(15, (int)((x - min)
+ *     * id + 0.5f)) with each step rounded in f32 from the unrounded min;
+ *     nibbles as Q4_0.
+ *   QG_Q5_0: Q4_0's signed max, d = max / -16, code = min(31, (int)(x * id +
+ *     16.5f)); the low 4 bits in nibbles as Q4_0, bit 4 of code j in bit j of
+ *     the little-endian 32-bit word qh.
  * x: f32 [n_rows][n_in]; out: n_rows * qtype_nbytes(type, n_in) bytes. */
 int quantize_rows(int type, const float *x, void *out, int64_t n_rows, int64_t n_in,
                   qg_stream_t stream);
@@ -131,7 +146,8 @@ int quantize_rows(int type, const float *x, void *out, int64_t n_rows, int64_t n
 
 /* Every element of n_rows rows to f32 ([sipllm] Per-format dequant; [candle]
  * block table; [rml] Unpacking the packed fields):
- *   Q8_0: q * d           Q4_0: (code - 8) * d
+ *   Q8_0, Q8_1: q * d     Q4_0: (code - 8) * d     Q5_0: (code - 16) * d
+ *   Q4_1: code * d + m (the product is exact; the sum rounds once)
  *   Q4_K: (d * sc_j) * q - dmin * m_j, j = e / 32, 6-bit sc/m unpacked as in
  *         [rml]'s element-200 trace
  *   Q6_K: (d * sc_j) * (q - 32), j = e / 16, q = 4 low bits from ql and 2
@@ -153,8 +169,9 @@ size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec);
  * [lesson21] Examples 10-11): quantizes x once into `workspace` with
  * quantize_act's rule for the paired activation type, then for every row
  * and block forms the exact int32 block sum and adds
- *   Q8_0, Q4_0, Q6_K: S * (d_w * d_x)
- *   Q4_K:             d_x * (d_w * S_q - dmin_w * S_m)
+ *   Q8_0, Q4_0, Q5_0, Q6_K: S * (d_w * d_x)
+ *   Q4_1:                   S * (d_w * d_x) + m_w * s_x
+ *   Q4_K:                   d_x * (d_w * S_q - dmin_w * S_m)
  * in f32. The f32 order of these few float operations is not fixed by the
  * pages; results agree with an f64 accumulation to about 1e-5 relative.
  * For Q4_K and Q6_K with n_vec >= 3 the sums are formed on the tensor cores
@@ -181,9 +198,11 @@ int qgemv_xq(int type, const void *W, const void *xq, float *y, int64_t n_out, i
  * isums[((v * n_out + o) * nb + b) * k + t], nb = n_in / block elements,
  * k = 2 for Q4_K (t = 0: S_q = sum_j sc_j sum_{i in j} q_i a_i, t = 1:
  * S_m = sum_j m_j (bsum_2j + bsum_2j+1)) and k = 1 otherwise (Q8_0:
- * sum qw qx; Q4_0: sum (code - 8) qx; Q6_K: sum_j sc_j sum_{i in j}
- * (q_i - 32) a_i) ([rml] Quantized dot products, Kernels and references).
- * Runs the __dp4a kernel that qgemv_xq runs for Q8_0, Q4_0 and for fewer
+ * sum qw qx; Q4_0: sum (code - 8) qx; Q5_0: sum (code - 16) qx; Q4_1:
+ * sum code qx, its min term m_w s_x being float; Q6_K: sum_j sc_j
+ * sum_{i in j} (q_i - 32) a_i) ([rml] Quantized dot products, Kernels and
+ * references). Runs the __dp4a kernel that qgemv_xq runs for the 32-element
+ * types and for fewer
  * than 3 vectors (the tensor-core kernel accumulates the same exact sums,
  * scaled by 2^-24, but does not write them out). */
 int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, int64_t n_out,

@@ -42,7 +42,8 @@
  *   - Q8_1 activations (paired with Q4_1 by [candle]'s VecDotType table;
  *     the byte layout is not printed): f16 d, f16 s, 32 int8 codes
  *     (36 bytes), where d and the codes follow the Q8_0 rule and
- *     s = f16(d * sum of the codes) in f32 with the unrounded d. The
+ *     s = f16(d * sum of the codes) in f32 with the unrounded d (a NaN s,
+ *     which only a block holding inf produces, is stored as 0x7E00). The
  *     Q4_1 x Q8_1 block term is d_w * d_x * S + m_w * s_x (S = sum of
  *     code * q_x), so it carries s's f16 rounding.
  *
@@ -314,7 +315,8 @@ void or_quantize_q5_0(const float *x, uint8_t *out, int64_t n) {
 }
 
 /* Q8_1 activations (the reading stated at the top of this file): the Q8_0
- * rule, plus s = f16(d * sum of codes) with the f32 d. */
+ * rule, plus s = f16(d * sum of codes) with the f32 d; a NaN s (only from a
+ * block holding inf) is stored as 0x7E00. */
 void or_quantize_q8_1(const float *x, uint8_t *out, int64_t n) {
     for (int64_t b = 0; b < n / 32; ++b) {
         const float *xb = x + b * 32;
@@ -333,7 +335,10 @@ void or_quantize_q8_1(const float *x, uint8_t *out, int64_t n) {
             sum += blk.qs[j];
         }
         blk.d = or_f32_to_f16(d);
-        blk.s = or_f32_to_f16((float)sum * d);
+        float sv = (float)sum * d;
+        /* a block holding inf has d = inf, codes 0 and s = 0 * inf: store
+         * the one quiet NaN 0x7E00 whatever sign the host's NaN carries */
+        blk.s = isnan(sv) ? (uint16_t)0x7E00 : or_f32_to_f16(sv);
         memcpy(out + b * 36, &blk, 36);
     }
 }

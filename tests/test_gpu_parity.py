@@ -17,7 +17,8 @@ from ggml_block_quantized_gb300 import synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 REL, ABS = 1e-5, 1e-6
-WTYPES = [qg.Q8_0, qg.Q4_0, qg.Q4_K, qg.Q6_K]
+WTYPES = [qg.Q8_0, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q4_K, qg.Q6_K]
+LEGACY = (qg.Q8_0, qg.Q4_0, qg.Q4_1, qg.Q5_0)  # 32-element blocks
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,9 +42,13 @@ def host(t):
 
 
 def weights(t, n_out, n_in, rng):
-    """Host weight blocks: Q8_0/Q4_0 from the oracle's quantizer, K types random."""
-    if t in (qg.Q8_0, qg.Q4_0):
-        return oracle.quantize(t, synth.f32_normal(rng, n_out * n_in, 0.02))
+    """Host weight blocks: 32-element types from the oracle's quantizer (Q4_1
+    from off-centre values), K types random."""
+    if t in LEGACY:
+        w = synth.f32_normal(rng, n_out * n_in, 0.02)
+        if t == qg.Q4_1:
+            w += np.float32(0.01)
+        return oracle.quantize(t, w)
     return synth.k_blocks(t, n_out * n_in // 256, rng)
 
 
@@ -91,7 +96,7 @@ SPECIAL = {
 }
 
 
-@pytest.mark.parametrize("at", [qg.Q8_0, qg.Q8_K])
+@pytest.mark.parametrize("at", [qg.Q8_0, qg.Q8_1, qg.Q8_K])
 def test_quantize_act_bit_exact(at):
     rng = np.random.default_rng(100 + at)
     for n_in, n_vec in ((256, 1), (512, 3), (4096, 8), (11008, 2), (256 * 40, 5)):
@@ -108,7 +113,7 @@ def test_quantize_act_bit_exact(at):
         assert np.array_equal(host(qg.quantize_act(at, dev(x), 1)), oracle.quantize(at, x)), bad
 
 
-@pytest.mark.parametrize("t", [qg.Q8_0, qg.Q4_0])
+@pytest.mark.parametrize("t", LEGACY)
 def test_quantize_rows_bit_exact(t):
     rng = np.random.default_rng(200 + t)
     # the lesson's fixed block with the 9.5 outlier, then random rows at the
@@ -126,10 +131,19 @@ def test_quantize_rows_bit_exact(t):
     x = (rng.integers(-16, 16, 32 * 64) / 2.0).astype(np.float32)
     x[::32] = -8.0
     assert np.array_equal(host(qg.quantize_rows(t, dev(x), 64)), oracle.quantize(t, x))
+    if t in (qg.Q4_1, qg.Q5_0):
+        # off-centre blocks (Q4_1's min at work) and NaN / inf elements, which
+        # both sides define: NaN is skipped by min/max and gives code 0
+        x = synth.f32_normal(rng, 32 * 64) + np.float32(3)
+        assert np.array_equal(host(qg.quantize_rows(t, dev(x), 64)), oracle.quantize(t, x))
+        for bad in (np.nan, np.inf, -np.inf):
+            x = synth.f32_normal(rng, 32 * 8)
+            x[[3, 100, 101]] = bad
+            assert np.array_equal(host(qg.quantize_rows(t, dev(x), 8)), oracle.quantize(t, x)), bad
 
 
 # ------------------------------------------------------------- dequantize
-@pytest.mark.parametrize("t", [qg.Q8_0, qg.Q4_0, qg.Q4_K, qg.Q6_K, qg.Q8_K])
+@pytest.mark.parametrize("t", [qg.Q8_0, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q8_1, qg.Q4_K, qg.Q6_K, qg.Q8_K])
 def test_dequantize_bit_exact(t):
     rng = np.random.default_rng(300 + t)
     elems, nbytes = oracle.type_info(t)
@@ -142,6 +156,8 @@ def test_dequantize_bit_exact(t):
                 W[:, 0:4] = np.abs(rng.standard_normal((W.shape[0], 1))).astype(np.float32).view(np.uint8)
             else:
                 W[:, 0:2] = rng.standard_normal((W.shape[0], 1)).astype(np.float16).view(np.uint8)
+            if t == qg.Q4_1:  # the min: finite f16 (random bytes could be NaN)
+                W[:, 2:4] = rng.standard_normal((W.shape[0], 1)).astype(np.float16).view(np.uint8)
             W = W.reshape(-1)
         got = host(qg.dequantize_rows(t, dev(W), n_rows, n_in))
         want = oracle.dequantize(t, W, n_rows * n_in).reshape(n_rows, n_in)
@@ -159,6 +175,8 @@ def test_dequantize_q4_k_workload_size():
 SHAPES = {  # (n_out, n_in): one block; ragged rows; several stages and ring wrap-around
     qg.Q8_0: [(1, 32), (37, 96), (300, 1024), (5000, 4096)],
     qg.Q4_0: [(1, 32), (37, 96), (300, 1024), (5000, 4096)],
+    qg.Q4_1: [(1, 32), (37, 96), (300, 1024), (5000, 4096)],
+    qg.Q5_0: [(1, 32), (37, 96), (300, 1024), (5000, 4096)],
     qg.Q4_K: [(1, 256), (37, 768), (300, 11008), (5000, 4096)],
     qg.Q6_K: [(1, 256), (37, 768), (300, 11008), (3000, 4096)],
 }
@@ -177,6 +195,24 @@ def test_block_isums_bit_exact(t):
             got = host(qg.qgemv_block_isums(t, Wd, dev(xq), n_out, n_in, n_vec))
             want = oracle.block_isums(t, W, xq, n_out, n_in, n_vec)
             assert np.array_equal(got, want), (n_out, n_in, n_vec)
+
+
+@pytest.mark.parametrize("t", [qg.Q4_1, qg.Q5_0])
+def test_every_code_and_bit_pattern(t):
+    """Blocks of uniform random bytes (every nibble, every fifth bit, d of
+    either sign, Q4_1's min of either sign): exact sums bit for bit and y
+    within tolerance, all rows."""
+    rng = np.random.default_rng(450 + t)
+    at = oracle.act_type(t)
+    for n_out, n_in in ((5, 32), (67, 1024), (1000, 4096)):
+        W = synth.legacy_blocks(t, n_out * n_in // 32, rng)
+        for n_vec in (1, 2, 3, 8):
+            x = synth.f32_normal(rng, n_vec * n_in)
+            xq = oracle.quantize(at, x)
+            got = host(qg.qgemv_block_isums(t, dev(W), dev(xq), n_out, n_in, n_vec))
+            assert np.array_equal(got, oracle.block_isums(t, W, xq, n_out, n_in, n_vec)), (n_out, n_in, n_vec)
+            y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
+            check_y(t, W, x, y, n_out, n_in, n_vec)
 
 
 def test_block_isums_at_extreme_codes():
@@ -214,7 +250,8 @@ def test_qgemv_small_shapes_all_rows(t):
             check_y(t, W, x, y, n_out, n_in, n_vec)
 
 
-@pytest.mark.parametrize("name", ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000"])
+@pytest.mark.parametrize("name", ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000", "q4_1_4096",
+                                  "q5_0_4096"])
 @pytest.mark.parametrize("n_vec", [1, 8])
 def test_qgemv_workloads_full_size(name, n_vec):
     m = synth.single_matrix(name, n_vec=n_vec)
@@ -265,7 +302,8 @@ def test_edges_empty_and_tails():
     qg.qgemv(qg.Q4_K, torch.zeros(16, dtype=torch.uint8, device="cuda"),
              dev(synth.f32_normal(rng, 256)), 0, 256, 1, y=torch.zeros(4, device="cuda"))
     # W byte lengths that end inside a 16-byte chunk (34, 630, 18*3 bytes)
-    for t, n_out, n_in in ((qg.Q8_0, 1, 32), (qg.Q6_K, 3, 256), (qg.Q4_0, 3, 32), (qg.Q6_K, 7, 2304)):
+    for t, n_out, n_in in ((qg.Q8_0, 1, 32), (qg.Q6_K, 3, 256), (qg.Q4_0, 3, 32), (qg.Q6_K, 7, 2304),
+                           (qg.Q4_1, 1, 32), (qg.Q5_0, 3, 32), (qg.Q5_0, 5, 96)):
         W = weights(t, n_out, n_in, rng)
         assert W.size % 16 != 0
         for n_vec in (1, 4):
@@ -374,7 +412,7 @@ def test_batched_equals_single_calls(t, n_vec):
     same bits as one qgemv call each (n_vec 8 takes the path that quantizes
     all activations into the workspace first)."""
     rng = np.random.default_rng(900 + t + n_vec)
-    n_in = 4096 if n_vec == 8 else (1024 if t in (qg.Q8_0, qg.Q4_0) else 2048)
+    n_in = 4096 if n_vec == 8 else (1024 if t in LEGACY else 2048)
     n_outs = [300, 0, 1, 2000, 77, 513]
     mats, host_w, host_x = batch_inputs(t, n_outs, n_in, n_vec, rng)
     qg.qgemv_batched(t, mats, n_in, n_vec)

@@ -44,12 +44,12 @@ def test_header_declarations_are_exported(L):
 
 
 def test_type_table_matches_the_oracle(L):
-    for t in (qg.F32, qg.F16, qg.Q4_0, qg.Q8_0, qg.Q4_K, qg.Q6_K, qg.Q8_K):
+    for t in (qg.F32, qg.F16, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q8_0, qg.Q8_1, qg.Q4_K, qg.Q6_K, qg.Q8_K):
         assert qg.qtype_block(t) == oracle.type_info(t)
         for n in (0, 256, 4096, 11008, 32 * 7, 100):
             assert qg.qtype_nbytes(t, n) == oracle.type_nbytes(t, n)
     with pytest.raises(qg.QGError):
-        qg.qtype_block(3)
+        qg.qtype_block(7)
     assert qg.qtype_nbytes(99, 256) == -1
     assert qg.qtype_nbytes(qg.Q8_0, -32) == -1
 
@@ -59,7 +59,9 @@ def test_pairing(L):
     assert qg.qtype_act_type(qg.Q8_0) == qg.Q8_0
     assert qg.qtype_act_type(qg.Q4_K) == qg.Q8_K
     assert qg.qtype_act_type(qg.Q6_K) == qg.Q8_K
-    for t in (qg.F32, qg.F16, qg.Q8_K, 7, 99):
+    assert qg.qtype_act_type(qg.Q5_0) == qg.Q8_0
+    assert qg.qtype_act_type(qg.Q4_1) == qg.Q8_1
+    for t in (qg.F32, qg.F16, qg.Q8_K, qg.Q8_1, 7, 99):
         assert qg.qtype_act_type(t) == ERR_PAIR
 
 
@@ -70,6 +72,8 @@ def test_workspace_bytes(L):
     assert qg.qgemv_workspace_bytes(qg.Q4_0, 100, 1) == 0
     assert qg.qgemv_workspace_bytes(qg.Q4_0, 4096, 9) == 0
     assert qg.qgemv_workspace_bytes(qg.Q8_K, 4096, 1) == 0
+    assert qg.qgemv_workspace_bytes(qg.Q4_1, 4096, 2) == 2 * 128 * 36
+    assert qg.qgemv_workspace_bytes(qg.Q5_0, 4096, 3) == 3 * 128 * 34
 
 
 def test_status_strings(L):
@@ -117,6 +121,10 @@ def test_other_entry_points_validate(L):
     assert L.quantize_act(qg.Q8_0, A, A2, 0, 1, NUL) == OK
     assert L.quantize_rows(qg.Q4_K, A, A2, 1, 256, NUL) == ERR_TYPE
     assert L.quantize_rows(qg.Q4_0, A, A2, 1, 33, NUL) == ERR_SHAPE
+    assert L.quantize_rows(qg.Q8_1, A, A2, 1, 32, NUL) == ERR_TYPE   # activations only
+    assert L.quantize_act(qg.Q4_1, A, A2, 32, 1, NUL) == ERR_TYPE
+    assert L.quantize_act(qg.Q8_1, A, A2, 33, 1, NUL) == ERR_SHAPE
+    assert L.quantize_rows(qg.Q5_0, A, A2, 1, 48, NUL) == ERR_SHAPE
     assert L.dequantize_rows(qg.F32, A, A2, 1, 256, NUL) == ERR_TYPE
     assert L.dequantize_rows(qg.Q6_K, A, A2, 1, 255, NUL) == ERR_SHAPE
     assert L.dequantize_rows(qg.Q6_K, A, MIS, 1, 256, NUL) == ERR_ALIGN

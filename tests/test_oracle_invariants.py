@@ -190,6 +190,12 @@ def test_q8_1_is_q8_0_plus_the_scaled_code_sum():
         assert abs(s - d * tot) <= (2.0 ** -10) * abs(d * tot) + 1e-7
     assert np.array_equal(oracle.dequantize(oracle.Q8_1, q1.reshape(-1), x.size),
                           oracle.dequantize(oracle.Q8_0, q0.reshape(-1), x.size))
+    # a block holding inf: d = inf, every code 0, s = 0 * inf stored as the
+    # one quiet NaN 0x7E00, whatever sign the host gives that NaN
+    x = np.ones(32, np.float32)
+    x[5] = np.inf
+    q = oracle.quantize(oracle.Q8_1, x).tobytes()
+    assert q[0:4] == bytes([0x00, 0x7C, 0x00, 0x7E]) and not any(q[4:])
 
 
 # ----------------------------------------------- Q4_K packing structure
