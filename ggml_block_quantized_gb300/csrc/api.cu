@@ -207,7 +207,8 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
             }
             const size_t fixed0 = kHeaderBytes + act + xb + kSmemTailPad;
             for (int split = 1; split <= kConsumerWarps; split *= 2) {
-                const int R = (kConsumerWarps / split) * kRowsPerWarp;
+            for (int rpw = kRowsPerWarp; rpw >= 1; --rpw) {  // rows a warp group takes per stage
+                const int R = (kConsumerWarps / split) * rpw;
                 const size_t stage = round16(static_cast<size_t>(R) * row_bytes + 15);
                 if (split < kConsumerWarps && stage > 40960) continue;  // stages of <= 40 KiB
                 // partial sums of split rows, double-buffered: [2S][warps][rows per warp][nv] floats
@@ -219,15 +220,18 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
                 S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
                 while (S > 2 && fixed0 + red_bytes(S) + S * stage > budget) --S;
                 // lane use of the busiest warp's flattened item loop (two rows)
-                const int64_t items = (nb + split - 1) / split * lpb * kRowsPerWarp;
-                const double eff = static_cast<double>(nb * lpb * kRowsPerWarp) / split /
+                const int64_t items = (nb + split - 1) / split * lpb * rpw;
+                const double eff = static_cast<double>(nb * lpb * rpw) / split /
                                    (32.0 * static_cast<double>((items + 31) / 32));
                 // fuller lanes first; then fewer warps per row (each stage does
-                // more work per warp); then the item with fewer lanes per
-                // block (fewer instructions per code); then x staged whole;
-                // then the larger ring
-                const double score = static_cast<int>(eff * 20.0 + 0.5) * 100.0 - split * 10.0 - li * 6.0 +
-                                     (xi == 0 ? 5.0 : 0.0) + static_cast<double>(S * stage) / (4.0 * 1024 * 1024);
+                // more work per warp, and no partial sums to add up); then two
+                // rows per warp group over one (the per-stage work is shared by
+                // more blocks); then the item with fewer lanes per block (fewer
+                // instructions per code); then x staged whole; then the larger
+                // ring
+                const double score = static_cast<int>(eff * 20.0 + 0.5) * 100.0 - split * 10.0 -
+                                     (kRowsPerWarp - rpw) * 3.0 - li * 6.0 + (xi == 0 ? 5.0 : 0.0) +
+                                     static_cast<double>(S * stage) / (4.0 * 1024 * 1024);
                 if (score > best_score) {
                     best_score = score;
                     found = true;
@@ -244,6 +248,7 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
                     bp.red_bytes = static_cast<int>(red_bytes(S));
                     best_smem = fixed0 + red_bytes(S) + S * stage;
                 }
+            }
             }
         }
         }

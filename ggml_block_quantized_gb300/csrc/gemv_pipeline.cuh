@@ -43,7 +43,7 @@ namespace qg {
 constexpr int kConsumerWarps = 8;
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 16;
-constexpr int kRowsPerWarp = 2;  // rows a warp group takes per stage (its items are flattened over them)
+constexpr int kRowsPerWarp = 2;  // most rows a warp group takes per stage (its items are flattened over them)
 constexpr int kMaxBatch = 256;   // matrices per batched launch (their table is a kernel parameter)
 // Shared memory: header (kMaxStages full + kMaxStages empty mbarriers) |
 // staged activations | f32 x buffer | cross-warp partial sums (split > 1:
@@ -74,7 +74,7 @@ struct GemvParams {
     int64_t total_rows;  // sum of n_out over the matrices
     int n_mats;
     int nb;              // blocks per row
-    int rows_per_stage;  // (kConsumerWarps / split) * kRowsPerWarp
+    int rows_per_stage;  // (kConsumerWarps / split) * (1 or kRowsPerWarp)
     int split;           // consumer warps per row: 1, 2, 4 or 8
     int n_stages;        // ring depth (2..kMaxStages)
     int stage_bytes;     // bytes per ring slot, multiple of 16
@@ -406,8 +406,10 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
         if (!ISUMS && has[0]) {
 #pragma unroll
             for (int i = 0; i < kRowsPerWarp; ++i)
+                if (i == 0 || has[i]) {  // warp-uniform: stages of one row per warp group leave row 1 empty
 #pragma unroll
-                for (int v = 0; v < NV; ++v) acc[i][v] = warp_sum(acc[i][v]);
+                    for (int v = 0; v < NV; ++v) acc[i][v] = warp_sum(acc[i][v]);
+                }
             if (split == 1) {
                 if (lane == 0 && !failed) {
 #pragma unroll
