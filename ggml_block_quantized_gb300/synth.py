@@ -23,9 +23,11 @@ layer stack derives per-(layer, matrix) streams from those.
 """
 import numpy as np
 
-Q4_0, Q4_1, Q5_0, Q8_0, Q4_K, Q6_K = 2, 3, 6, 8, 12, 14
-BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q5_0: (32, 22), Q8_0: (32, 34), Q4_K: (256, 144),
-         Q6_K: (256, 210)}
+Q4_0, Q4_1, Q5_0, Q8_0 = 2, 3, 6, 8
+Q2_K, Q3_K, Q4_K, Q5_K, Q6_K = 10, 11, 12, 13, 14
+BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q5_0: (32, 22), Q8_0: (32, 34), Q2_K: (256, 84),
+         Q3_K: (256, 110), Q4_K: (256, 144), Q5_K: (256, 176), Q6_K: (256, 210)}
+K_TYPES = (Q2_K, Q3_K, Q4_K, Q5_K, Q6_K)
 FROM_F32 = (Q8_0, Q4_0, Q4_1, Q5_0)  # workloads that quantize f32 weights
 
 WORKLOADS = ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000", "layer_stack",
@@ -62,18 +64,25 @@ def _half_scales(rng, n) -> np.ndarray:
 
 
 def k_blocks(wtype: int, n_blocks: int, rng) -> np.ndarray:
-    """Random Q4_K or Q6_K super-blocks (flat uint8, n_blocks * block bytes)."""
+    """Random K-quant super-blocks (flat uint8, n_blocks * block bytes):
+    uniform bytes, then the f16 d (and dmin) set to |N(0,1)| * 1e-3 and, for
+    Q6_K, the int8 scales drawn uniform in [-32, 31]."""
     _, nbytes = BLOCK[wtype]
     raw = random_bytes(rng, n_blocks * nbytes).reshape(n_blocks, nbytes)
-    if wtype == Q4_K:
+    if wtype in (Q4_K, Q5_K):
         raw[:, 0:2] = _half_scales(rng, n_blocks)
         raw[:, 2:4] = _half_scales(rng, n_blocks)
+    elif wtype == Q2_K:
+        raw[:, 80:82] = _half_scales(rng, n_blocks)
+        raw[:, 82:84] = _half_scales(rng, n_blocks)
+    elif wtype == Q3_K:
+        raw[:, 108:110] = _half_scales(rng, n_blocks)
     elif wtype == Q6_K:
         sc = rng.integers(-32, 32, size=(n_blocks, 16), dtype=np.int8)
         raw[:, 192:208] = sc.view(np.uint8)
         raw[:, 208:210] = _half_scales(rng, n_blocks)
     else:
-        raise ValueError("k_blocks takes Q4_K or Q6_K")
+        raise ValueError("k_blocks takes a K-quant weight type")
     return raw.reshape(-1)
 
 

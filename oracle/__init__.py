@@ -9,9 +9,10 @@ the two share no code.
 
 Every function follows a passage of the reference pages; the citations sit
 beside each C function in qoracle.c. The Q6_K element mapping, the Q8_K
-activation rule and the s field of Q8_1 are readings of the pages (they do
-not define them) and are "parity unpinned" against ggml itself: they are
-pinned only by structural invariants in the tests.
+activation rule, the s field of Q8_1 and the Q2_K/Q3_K/Q5_K layouts are
+readings of the pages (they do not define them) and are "parity unpinned"
+against ggml itself: they are pinned only by structural invariants in the
+tests.
 """
 import ctypes
 import os
@@ -20,9 +21,11 @@ import numpy as np
 
 from . import build as _build
 
-F32, F16, Q4_0, Q4_1, Q5_0, Q8_0, Q8_1, Q4_K, Q6_K, Q8_K = 0, 1, 2, 3, 6, 8, 9, 12, 14, 15
+F32, F16, Q4_0, Q4_1, Q5_0, Q8_0, Q8_1 = 0, 1, 2, 3, 6, 8, 9
+Q2_K, Q3_K, Q4_K, Q5_K, Q6_K, Q8_K = 10, 11, 12, 13, 14, 15
 TYPE_NAMES = {F32: "F32", F16: "F16", Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0",
-              Q8_0: "Q8_0", Q8_1: "Q8_1", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K"}
+              Q8_0: "Q8_0", Q8_1: "Q8_1", Q2_K: "Q2_K", Q3_K: "Q3_K", Q4_K: "Q4_K",
+              Q5_K: "Q5_K", Q6_K: "Q6_K", Q8_K: "Q8_K"}
 
 _lib = None
 
@@ -128,7 +131,7 @@ def dequantize(t: int, data: np.ndarray, n: int) -> np.ndarray:
 def block_isums(wtype: int, W: np.ndarray, xq: np.ndarray, n_out: int, n_in: int,
                 n_vec: int) -> np.ndarray:
     """Per-(vector, row, block) exact int32 sums; shape [n_vec, n_out, nb, k]
-    with k = 2 (S_q, S_m) for Q4_K and 1 otherwise."""
+    with k = 2 (S_q, S_m) for Q2_K, Q4_K and Q5_K and 1 otherwise."""
     elems, _ = type_info(wtype)
     nb = n_in // elems
     k = isums_per_block(wtype)

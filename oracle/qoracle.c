@@ -37,6 +37,16 @@
  *     for k < 2, high nibble for k >= 2), the high 2 bits from
  *     (qh[32h + l] >> 2k) & 3, and the sub-block scale is scales[e / 16].
  *   - Q4_K sub-blocks 0..3: scale = scales[j] & 63, min = scales[j+4] & 63.
+ *   - Q2_K, Q3_K and Q5_K (the pages give their sizes and, for Q5_K, that
+ *     it carries dmin and Q4_K's packed 6-bit scales and mins): the ggml
+ *     file layouts, written out at q2_k_code, q3_k_code and q5_k_code below.
+ *     Element e = 128n + 32j + 16h + l of Q2_K/Q3_K takes bits 2j..2j+1 of
+ *     qs[32n + 16h + l] and lies in the 16-element sub-block e / 16; Q3_K's
+ *     third bit is bit 4n + j of hmask[16h + l] (set means the 2-bit value
+ *     as is, clear means 4 less) and its sixteen 6-bit scales, stored
+ *     biased by 32, keep their low 4 bits in the nibbles of bytes 0..7 and
+ *     their high 2 bits in bytes 8..11; Q5_K is Q4_K plus a fifth bit, bit j
+ *     of qh[e % 32] for sub-block j = e / 32.
  *   - NaN inputs to a quantizer are ignored by the amax and give code 0
  *     (candle's special-value table).
  *   - Q8_1 activations (paired with Q4_1 by [candle]'s VecDotType table;
@@ -49,9 +59,10 @@
  *
  * Parity pins: every function here is pinned by tests under tests/ against
  * values the pages print, closed forms or brute force; the Q6_K element
- * mapping, the Q8_K rule and Q8_1's s field are pinned only by structural
- * invariants (the pages do not define them) and are "parity unpinned"
- * against ggml itself.
+ * mapping, the Q8_K rule, Q8_1's s field and the Q2_K/Q3_K/Q5_K layouts
+ * are pinned only by structural invariants (and Q5_K also by its reduction
+ * to the pinned Q4_K): the pages do not define them, so they are "parity
+ * unpinned" against ggml itself.
  */
 #include <math.h>
 #include <stdint.h>
@@ -63,7 +74,7 @@
 /* ------------------------------------------------------------------------ */
 enum {
     OR_F32 = 0, OR_F16 = 1, OR_Q4_0 = 2, OR_Q4_1 = 3, OR_Q5_0 = 6, OR_Q8_0 = 8, OR_Q8_1 = 9,
-    OR_Q4_K = 12, OR_Q6_K = 14, OR_Q8_K = 15
+    OR_Q2_K = 10, OR_Q3_K = 11, OR_Q4_K = 12, OR_Q5_K = 13, OR_Q6_K = 14, OR_Q8_K = 15
 };
 
 /* Returns 0 and fills (elems, bytes) for a known id, -1 otherwise. */
@@ -76,7 +87,10 @@ int or_type_info(int type, int *elems, int *bytes) {
     case OR_Q5_0: *elems = 32;  *bytes = 22;  return 0;
     case OR_Q8_1: *elems = 32;  *bytes = 36;  return 0;
     case OR_Q8_0: *elems = 32;  *bytes = 34;  return 0;
+    case OR_Q2_K: *elems = 256; *bytes = 84;  return 0;
+    case OR_Q3_K: *elems = 256; *bytes = 110; return 0;
     case OR_Q4_K: *elems = 256; *bytes = 144; return 0;
+    case OR_Q5_K: *elems = 256; *bytes = 176; return 0;
     case OR_Q6_K: *elems = 256; *bytes = 210; return 0;
     case OR_Q8_K: *elems = 256; *bytes = 292; return 0;
     default: return -1;
@@ -113,6 +127,25 @@ typedef struct {
     int8_t scales[16];
     uint16_t d;
 } or_block_q6_k;
+typedef struct {
+    uint8_t scales[16];  /* low nibble: scale, high nibble: min */
+    uint8_t qs[64];
+    uint16_t d;
+    uint16_t dmin;
+} or_block_q2_k;
+typedef struct {
+    uint8_t hmask[32];
+    uint8_t qs[64];
+    uint8_t scales[12];
+    uint16_t d;
+} or_block_q3_k;
+typedef struct {
+    uint16_t d;
+    uint16_t dmin;
+    uint8_t scales[12];
+    uint8_t qh[32];
+    uint8_t qs[128];
+} or_block_q5_k;
 typedef struct { float d; int8_t qs[256]; int16_t bsums[16]; } or_block_q8_k;
 
 _Static_assert(sizeof(or_block_q8_0) == 34, "Q8_0 block is 34 bytes");
@@ -122,6 +155,9 @@ _Static_assert(sizeof(or_block_q5_0) == 22, "Q5_0 block is 22 bytes");
 _Static_assert(sizeof(or_block_q8_1) == 36, "Q8_1 block is 36 bytes");
 _Static_assert(sizeof(or_block_q4_k) == 144, "Q4_K block is 144 bytes");
 _Static_assert(sizeof(or_block_q6_k) == 210, "Q6_K block is 210 bytes");
+_Static_assert(sizeof(or_block_q2_k) == 84, "Q2_K block is 84 bytes");
+_Static_assert(sizeof(or_block_q3_k) == 110, "Q3_K block is 110 bytes");
+_Static_assert(sizeof(or_block_q5_k) == 176, "Q5_K block is 176 bytes");
 _Static_assert(sizeof(or_block_q8_k) == 292, "Q8_K block is 292 bytes");
 
 /* ------------------------------------------------------------------------ */
@@ -436,6 +472,41 @@ static int q6_k_code(const or_block_q6_k *b, int e) {
     return lo4 | (hi2 << 4);
 }
 
+/* Q5_K element e: Q4_K's nibble plus a fifth bit, bit j of qh[e % 32] for
+ * the 32-element sub-block j = e / 32 (reading in the file header). */
+static int q5_k_code(const or_block_q5_k *b, int e) {
+    int chunk = e / 64, p = e % 64, j = e / 32;
+    int lo4 = (p < 32) ? (b->qs[32 * chunk + p] & 0x0F) : (b->qs[32 * chunk + p - 32] >> 4);
+    int bit = (b->qh[e % 32] >> j) & 1;
+    return lo4 | (bit << 4);
+}
+
+/* Q2_K element e = 128n + 32j + 16h + l: bits 2j..2j+1 of qs[32n + 16h + l]
+ * (reading in the file header); its sub-block e / 16 has scale
+ * scales[e/16] & 15 and min scales[e/16] >> 4. */
+static int q2_k_code(const or_block_q2_k *b, int e) {
+    int n = e / 128, j = (e % 128) / 32, h = (e % 32) / 16, l = e % 16;
+    return (b->qs[32 * n + 16 * h + l] >> (2 * j)) & 3;
+}
+
+/* Q3_K element e = 128n + 32j + 16h + l: the 2-bit value as in Q2_K, less 4
+ * when bit 4n + j of hmask[16h + l] is clear; the result is in -4..3. */
+static int q3_k_code(const or_block_q3_k *b, int e) {
+    int n = e / 128, j = (e % 128) / 32, h = (e % 32) / 16, l = e % 16;
+    int q2 = (b->qs[32 * n + 16 * h + l] >> (2 * j)) & 3;
+    int high = (b->hmask[16 * h + l] >> (4 * n + j)) & 1;
+    return q2 - (high ? 0 : 4);
+}
+
+/* Q3_K sub-block scale j (0..15), unbiased to -32..31: low 4 bits in the
+ * low nibble of byte j (j < 8) or the high nibble of byte j - 8, high 2
+ * bits at bits 2(j/4)..2(j/4)+1 of byte 8 + j % 4. */
+static int q3_k_scale(const uint8_t s[12], int j) {
+    int lo4 = (j < 8) ? (s[j] & 0x0F) : (s[j - 8] >> 4);
+    int hi2 = (s[8 + j % 4] >> (2 * (j / 4))) & 3;
+    return (lo4 | (hi2 << 4)) - 32;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Dequantization ([sipllm] Per-format dequant; [candle] block table;      */
 /* [rml] Dequantization: memcpy each block into a local struct first).      */
@@ -488,6 +559,39 @@ static void dequant_block(int type, const uint8_t *src, float *dst) {
         }
         break;
     }
+    case OR_Q5_K: {
+        or_block_q5_k b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d), dmin = or_f16_to_f32(b.dmin);
+        for (int e = 0; e < 256; ++e) {
+            int sc, m;
+            q4_k_scale_min(b.scales, e / 32, &sc, &m);
+            float scaled = d * (float)sc;      /* exact: 11 + 6 bits */
+            float value = scaled * (float)q5_k_code(&b, e); /* exact: 22 bits */
+            float offset = dmin * (float)m;    /* exact: 17 bits */
+            dst[e] = value - offset;           /* the only rounding */
+        }
+        break;
+    }
+    case OR_Q2_K: {
+        or_block_q2_k b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d), dmin = or_f16_to_f32(b.dmin);
+        for (int e = 0; e < 256; ++e) {
+            int sc = b.scales[e / 16] & 0x0F, m = b.scales[e / 16] >> 4;
+            float value = (d * (float)sc) * (float)q2_k_code(&b, e); /* exact: 17 bits */
+            float offset = dmin * (float)m;                          /* exact: 15 bits */
+            dst[e] = value - offset;                                 /* the only rounding */
+        }
+        break;
+    }
+    case OR_Q3_K: {
+        or_block_q3_k b; memcpy(&b, src, sizeof b);
+        float d = or_f16_to_f32(b.d);
+        for (int e = 0; e < 256; ++e) {
+            float scaled = d * (float)q3_k_scale(b.scales, e / 16); /* exact: 11 + 6 bits */
+            dst[e] = scaled * (float)q3_k_code(&b, e);               /* exact: 20 bits */
+        }
+        break;
+    }
     case OR_Q6_K: {
         or_block_q6_k b; memcpy(&b, src, sizeof b);
         float d = or_f16_to_f32(b.d);
@@ -528,14 +632,17 @@ int or_act_type(int wtype) {
     switch (wtype) {
     case OR_Q4_0: case OR_Q5_0: case OR_Q8_0: return OR_Q8_0;
     case OR_Q4_1: return OR_Q8_1;
-    case OR_Q4_K: case OR_Q6_K: return OR_Q8_K;
+    case OR_Q2_K: case OR_Q3_K: case OR_Q4_K: case OR_Q5_K: case OR_Q6_K: return OR_Q8_K;
     default: return -1;
     }
 }
 
-/* Number of int32 sums per (vector, row, block): Q4_K keeps the scale sum
- * S_q and the min sum S_m apart, every other type has one sum S. */
-int or_isums_per_block(int wtype) { return wtype == OR_Q4_K ? 2 : 1; }
+/* Number of int32 sums per (vector, row, block): the types with a dmin
+ * (Q2_K, Q4_K, Q5_K) keep the scale sum S_q and the min sum S_m apart,
+ * every other type has one sum S. */
+int or_isums_per_block(int wtype) {
+    return (wtype == OR_Q2_K || wtype == OR_Q4_K || wtype == OR_Q5_K) ? 2 : 1;
+}
 
 /* ------------------------------------------------------------------------ */
 /* Per-block exact integer sums, element by element (the reference form of  */
@@ -549,6 +656,9 @@ int or_isums_per_block(int wtype) { return wtype == OR_Q4_K ? 2 : 1; }
 /*   Q4_K: S_q = sum_j sc_j * sum_{i in j} q_i * a_i,                       */
 /*         S_m = sum_j m_j * sum_{i in j} a_i    ([rml] Quantized dot)      */
 /*   Q6_K: S = sum_j sc_j * sum_{i in j} (q_i - 32) * a_i                   */
+/*   Q5_K: as Q4_K with the 5-bit q; Q2_K: as Q4_K over 16-element          */
+/*         sub-blocks; Q3_K: S = sum_j sc_j * sum_{i in j} q_i * a_i with   */
+/*         q in -4..3 and sc in -32..31                                     */
 /* ------------------------------------------------------------------------ */
 static void block_sums(int wtype, const uint8_t *wblk, const uint8_t *xblk, int32_t *out) {
     switch (wtype) {
@@ -598,6 +708,52 @@ static void block_sums(int wtype, const uint8_t *wblk, const uint8_t *xblk, int3
         out[1] = sm;
         break;
     }
+    case OR_Q5_K: {
+        or_block_q5_k w; or_block_q8_k x; memcpy(&w, wblk, 176); memcpy(&x, xblk, 292);
+        int32_t sq = 0, sm = 0;
+        for (int j = 0; j < 8; ++j) {
+            int sc, m;
+            q4_k_scale_min(w.scales, j, &sc, &m);
+            int32_t dot = 0, asum = 0;
+            for (int i = 32 * j; i < 32 * j + 32; ++i) {
+                dot += (int32_t)q5_k_code(&w, i) * (int32_t)x.qs[i];
+                asum += (int32_t)x.qs[i];
+            }
+            sq += sc * dot;
+            sm += m * asum;
+        }
+        out[0] = sq;
+        out[1] = sm;
+        break;
+    }
+    case OR_Q2_K: {
+        or_block_q2_k w; or_block_q8_k x; memcpy(&w, wblk, 84); memcpy(&x, xblk, 292);
+        int32_t sq = 0, sm = 0;
+        for (int j = 0; j < 16; ++j) {
+            int32_t dot = 0, asum = 0;
+            for (int i = 16 * j; i < 16 * j + 16; ++i) {
+                dot += (int32_t)q2_k_code(&w, i) * (int32_t)x.qs[i];
+                asum += (int32_t)x.qs[i];
+            }
+            sq += (w.scales[j] & 0x0F) * dot;
+            sm += (w.scales[j] >> 4) * asum;
+        }
+        out[0] = sq;
+        out[1] = sm;
+        break;
+    }
+    case OR_Q3_K: {
+        or_block_q3_k w; or_block_q8_k x; memcpy(&w, wblk, 110); memcpy(&x, xblk, 292);
+        int32_t s = 0;
+        for (int j = 0; j < 16; ++j) {
+            int32_t dot = 0;
+            for (int i = 16 * j; i < 16 * j + 16; ++i)
+                dot += (int32_t)q3_k_code(&w, i) * (int32_t)x.qs[i];
+            s += q3_k_scale(w.scales, j) * dot;
+        }
+        out[0] = s;
+        break;
+    }
     case OR_Q6_K: {
         or_block_q6_k w; or_block_q8_k x; memcpy(&w, wblk, 210); memcpy(&x, xblk, 292);
         int32_t s = 0;
@@ -616,7 +772,7 @@ static void block_sums(int wtype, const uint8_t *wblk, const uint8_t *xblk, int3
 }
 
 /* Block scales as doubles: (d_w, dmin_w, d_x) and the additive term off
- * (Q4_1: m_w * s_x, else 0). dmin_w is 0 except Q4_K. */
+ * (Q4_1: m_w * s_x, else 0). dmin_w is 0 except Q2_K, Q4_K and Q5_K. */
 static void block_scales(int wtype, const uint8_t *wblk, const uint8_t *xblk,
                          double *dw, double *dmin, double *dx, double *off) {
     *dmin = 0.0;
@@ -634,6 +790,12 @@ static void block_scales(int wtype, const uint8_t *wblk, const uint8_t *xblk,
     case OR_Q4_K: { or_block_q4_k w; or_block_q8_k x; memcpy(&w, wblk, 144); memcpy(&x, xblk, 292);
         *dw = or_f16_to_f32(w.d); *dmin = or_f16_to_f32(w.dmin); *dx = x.d; break; }
     case OR_Q6_K: { or_block_q6_k w; or_block_q8_k x; memcpy(&w, wblk, 210); memcpy(&x, xblk, 292);
+        *dw = or_f16_to_f32(w.d); *dx = x.d; break; }
+    case OR_Q5_K: { or_block_q5_k w; or_block_q8_k x; memcpy(&w, wblk, 176); memcpy(&x, xblk, 292);
+        *dw = or_f16_to_f32(w.d); *dmin = or_f16_to_f32(w.dmin); *dx = x.d; break; }
+    case OR_Q2_K: { or_block_q2_k w; or_block_q8_k x; memcpy(&w, wblk, 84); memcpy(&x, xblk, 292);
+        *dw = or_f16_to_f32(w.d); *dmin = or_f16_to_f32(w.dmin); *dx = x.d; break; }
+    case OR_Q3_K: { or_block_q3_k w; or_block_q8_k x; memcpy(&w, wblk, 110); memcpy(&x, xblk, 292);
         *dw = or_f16_to_f32(w.d); *dx = x.d; break; }
     default: *dw = 0.0; *dx = 0.0; break;
     }
@@ -668,9 +830,9 @@ int or_block_isums(int wtype, const uint8_t *W, const uint8_t *xq, int32_t *isum
 
 /* y[v * n_out + o] for rows o in [row0, row1), accumulated in f64 over the
  * row's blocks ([lesson21] Example 10: integer sum per block times both
- * scales):  Q8_0/Q4_0/Q5_0/Q6_K: T_b = d_w * d_x * S;
- *           Q4_1:                T_b = d_w * d_x * S + m_w * s_x;
- *           Q4_K:                T_b = d_x * (d_w * S_q - dmin_w * S_m). */
+ * scales):  Q8_0/Q4_0/Q5_0/Q3_K/Q6_K: T_b = d_w * d_x * S;
+ *           Q4_1:                     T_b = d_w * d_x * S + m_w * s_x;
+ *           Q2_K/Q4_K/Q5_K:           T_b = d_x * (d_w * S_q - dmin_w * S_m). */
 int or_gemv(int wtype, const uint8_t *W, const uint8_t *xq, double *y,
             int64_t n_out, int64_t n_in, int64_t n_vec, int64_t row0, int64_t row1) {
     int wel, wby, xby;
@@ -687,7 +849,7 @@ int or_gemv(int wtype, const uint8_t *W, const uint8_t *xq, double *y,
                 double dw, dmin, dx, off;
                 block_sums(wtype, wb, xb, s);
                 block_scales(wtype, wb, xb, &dw, &dmin, &dx, &off);
-                if (wtype == OR_Q4_K)
+                if (or_isums_per_block(wtype) == 2)
                     acc += dx * (dw * (double)s[0] - dmin * (double)s[1]);
                 else
                     acc += dw * dx * (double)s[0] + off;
@@ -715,6 +877,16 @@ static double exact_weight(int wtype, const uint8_t *blk, int e) {
              - (double)or_f16_to_f32(b.dmin) * m; }
     case OR_Q6_K: { or_block_q6_k b; memcpy(&b, blk, 210);
         return (double)or_f16_to_f32(b.d) * b.scales[e / 16] * (q6_k_code(&b, e) - 32); }
+    case OR_Q5_K: { or_block_q5_k b; memcpy(&b, blk, 176);
+        int sc, m; q4_k_scale_min(b.scales, e / 32, &sc, &m);
+        return (double)or_f16_to_f32(b.d) * sc * q5_k_code(&b, e)
+             - (double)or_f16_to_f32(b.dmin) * m; }
+    case OR_Q2_K: { or_block_q2_k b; memcpy(&b, blk, 84);
+        int sc = b.scales[e / 16] & 0x0F, m = b.scales[e / 16] >> 4;
+        return (double)or_f16_to_f32(b.d) * sc * q2_k_code(&b, e)
+             - (double)or_f16_to_f32(b.dmin) * m; }
+    case OR_Q3_K: { or_block_q3_k b; memcpy(&b, blk, 110);
+        return (double)or_f16_to_f32(b.d) * q3_k_scale(b.scales, e / 16) * q3_k_code(&b, e); }
     default: return 0.0;
     }
 }

@@ -365,10 +365,14 @@ def random_weights(t, n_out, n_in):
     if t in (oracle.Q8_0, oracle.Q4_0, oracle.Q5_0, oracle.Q4_1):
         return oracle.quantize(t, (RNG.standard_normal(n_out * n_in) * 0.02).astype(np.float32))
     nb = n_out * n_in // 256
+    if t in (oracle.Q2_K, oracle.Q3_K, oracle.Q5_K):
+        from ggml_block_quantized_gb300 import synth
+        return synth.k_blocks(t, nb, RNG)
     return np.frombuffer(b"".join(random_k_block(t) for _ in range(nb)), np.uint8).copy()
 
 
-@pytest.mark.parametrize("t", [oracle.Q8_0, oracle.Q4_0, oracle.Q5_0, oracle.Q4_K, oracle.Q6_K])
+@pytest.mark.parametrize("t", [oracle.Q8_0, oracle.Q4_0, oracle.Q5_0, oracle.Q2_K, oracle.Q3_K,
+                               oracle.Q4_K, oracle.Q5_K, oracle.Q6_K])
 def test_block_form_equals_dequantize_then_f64_dot(t):
     for n_out, n_in, n_vec in ((1, 256, 1), (3, 512, 2), (8, 512, 3)):
         W = random_weights(t, n_out, n_in)
@@ -466,3 +470,158 @@ def test_round_trip_rmse_near_candle_table():
         e = (y.astype(np.float64) - x)
         got = 100 * math.sqrt(np.sum(e ** 2) / np.sum(x.astype(np.float64) ** 2))
         assert got == pytest.approx(want, rel=0.01)
+
+
+# ------------------------------------------- Q2_K / Q3_K / Q5_K structure
+# The pages give these types' sizes (and, for Q5_K, that it carries dmin and
+# Q4_K's packed scales); the element layouts are readings. They are pinned
+# here by structure: every bit is one bit of one element or one field, the
+# scale of an element is that of its 16- or 32-element sub-block, Q5_K
+# reduces to the pinned Q4_K, and the block form equals brute force.
+def k_block(t, d=1.0, dmin=0.0):
+    raw = bytearray(oracle.type_info(t)[1])
+    if t == oracle.Q2_K:
+        raw[80:82] = np.float16(d).tobytes()
+        raw[82:84] = np.float16(dmin).tobytes()
+    elif t == oracle.Q3_K:
+        raw[108:110] = np.float16(d).tobytes()
+    elif t == oracle.Q5_K:
+        raw[0:2] = np.float16(d).tobytes()
+        raw[2:4] = np.float16(dmin).tobytes()
+    return raw
+
+
+def deq(t, raw):
+    return oracle.dequantize(t, np.frombuffer(bytes(raw), np.uint8), 256).astype(np.float64)
+
+
+def test_q5_k_reduces_to_q4_k():
+    # qh all zero: the same d, dmin, scales and qs decode exactly as Q4_K
+    # (whose element-200 trace the rml page prints); a set qh bit adds
+    # exactly 16 * d * sc of the element's 32-element sub-block
+    for _ in range(10):
+        q4 = bytearray(RNG.integers(0, 256, 144, dtype=np.uint8).tobytes())
+        q4[0:2] = np.float16(abs(RNG.standard_normal()) * 1e-2).tobytes()
+        q4[2:4] = np.float16(abs(RNG.standard_normal()) * 1e-2).tobytes()
+        q5 = bytearray(176)
+        q5[0:16] = q4[0:16]
+        q5[48:176] = q4[16:144]
+        v4 = oracle.dequantize(oracle.Q4_K, np.frombuffer(bytes(q4), np.uint8), 256)
+        assert np.array_equal(oracle.dequantize(oracle.Q5_K, np.frombuffer(bytes(q5), np.uint8), 256), v4)
+    blk = k_block(oracle.Q5_K, d=1.0)
+    blk[4:16] = bytes([5, 6, 7, 8, 0, 0, 0, 0, 0x21, 0x43, 0x65, 0x87])  # sub-block scales 5..8, then 1..7 and 8 low nibbles
+    base = deq(oracle.Q5_K, blk)
+    seen = set()
+    for byte in range(32):
+        for bit in range(8):
+            raw = bytearray(blk)
+            raw[16 + byte] |= 1 << bit
+            dv = deq(oracle.Q5_K, raw) - base
+            hit = np.nonzero(dv)[0]
+            assert hit.size == 1
+            e = int(hit[0])
+            seen.add(e)
+            sc = [5, 6, 7, 8, 1, 3, 5, 7][e // 32]
+            assert dv[e] == 16 * sc
+    assert seen == set(range(256))
+
+
+@pytest.mark.parametrize("t", [oracle.Q2_K, oracle.Q3_K])
+def test_q2_k_q3_k_every_code_bit_is_one_bit_of_one_element(t):
+    blk = k_block(t, d=1.0, dmin=0.0)
+    if t == oracle.Q2_K:
+        blk[0:16] = bytes([1] * 16)      # every scale 1, every min 0
+        qs_off, qs_len = 16, 64
+    else:
+        blk[96:104] = bytes([0x11] * 8)  # low 4 bits 1 for every scale
+        blk[104:108] = bytes([0xAA] * 4)  # high 2 bits 2: biased 33, i.e. scale 1
+        qs_off, qs_len = 32, 64
+    base = deq(t, blk)
+    weight_of = {}
+    for byte in range(qs_len):
+        for bit in range(8):
+            raw = bytearray(blk)
+            raw[qs_off + byte] ^= 1 << bit
+            dv = deq(t, raw) - base
+            hit = np.nonzero(dv)[0]
+            assert hit.size == 1, (byte, bit)
+            e = int(hit[0])
+            assert abs(dv[e]) == (1 << (bit % 2)), (byte, bit)  # bits come in 2-bit fields
+            weight_of.setdefault(e, []).append(bit % 2)
+    assert sorted(weight_of) == list(range(256))
+    assert all(sorted(v) == [0, 1] for v in weight_of.values())
+    if t == oracle.Q3_K:
+        # the 256 hmask bits: one per element, each moving it by 4
+        hit_all = set()
+        for byte in range(32):
+            for bit in range(8):
+                raw = bytearray(blk)
+                raw[byte] ^= 1 << bit
+                dv = deq(t, raw) - base
+                hit = np.nonzero(dv)[0]
+                assert hit.size == 1 and abs(dv[hit[0]]) == 4
+                hit_all.add(int(hit[0]))
+        assert hit_all == set(range(256))
+        # all code bits and hmask bits clear: -4 times the scale everywhere
+        assert np.all(base == -4.0)
+
+
+@pytest.mark.parametrize("t", [oracle.Q2_K, oracle.Q3_K])
+def test_q2_k_q3_k_scales_cover_16_element_sub_blocks(t):
+    # every code 1 (Q3_K: 2-bit value 1 with its hmask bit set), d = 1; each
+    # scale bit then moves exactly the 16 elements of one sub-block, and the
+    # sub-blocks are 16 consecutive elements each
+    blk = k_block(t, d=1.0, dmin=0.5)
+    if t == oracle.Q2_K:
+        blk[16:80] = bytes([0x55] * 64)
+        scale_bytes = range(0, 16)
+    else:
+        blk[32:96] = bytes([0x55] * 64)
+        blk[0:32] = bytes([0xFF] * 32)
+        scale_bytes = range(96, 108)
+    base = deq(t, blk)
+    owners = {}
+    for byte in scale_bytes:
+        for bit in range(8):
+            raw = bytearray(blk)
+            raw[byte] ^= 1 << bit
+            dv = deq(t, raw) - base
+            hit = np.nonzero(dv)[0]
+            assert hit.size == 16, (byte, bit)
+            j = int(hit[0]) // 16
+            assert list(hit) == list(range(16 * j, 16 * j + 16))
+            assert np.all(dv[hit] == dv[hit[0]])
+            owners.setdefault(j, []).append(abs(dv[hit[0]]))
+    assert sorted(owners) == list(range(16))
+    if t == oracle.Q2_K:   # 4 scale bits (x code 1) and 4 min bits (x dmin 0.5) per sub-block
+        assert all(sorted(v) == [0.5, 1, 1, 2, 2, 4, 4, 8] for v in owners.values())
+    else:                  # 6 scale bits per sub-block, code 1
+        assert all(sorted(v) == [1, 2, 4, 8, 16, 32] for v in owners.values())
+
+
+@pytest.mark.parametrize("t", [oracle.Q2_K, oracle.Q3_K, oracle.Q5_K])
+def test_new_k_types_dequant_rounds_once(t):
+    # every product is exact in f32, so values are the exact rationals rounded
+    # once: compare with the brute-force form's exact doubles through f32
+    W = random_weights(t, 4, 512)
+    xq = oracle.quantize(oracle.Q8_K, np.zeros(512, np.float32))
+    vals = oracle.dequantize(t, W, 4 * 512)
+    # the exact value of each element is the brute-force form's dot with a
+    # one-hot activation: build it through gemv_dequant on unit activations
+    unit = np.zeros(256, np.float32)
+    unit[0] = 127.0                    # Q8_K: d = 1, code 127 -> a_0 = 127 exactly
+    xu = oracle.quantize(oracle.Q8_K, unit)
+    for blk in range(8):
+        w = W[blk * oracle.type_info(t)[1]:(blk + 1) * oracle.type_info(t)[1]]
+        exact = oracle.gemv_dequant(t, w, xu, 1, 256, 1)[0, 0] / 127.0
+        assert float(vals[blk * 256]) == f32_round(Fraction(exact))
+    del xq
+
+
+def test_q3_k_int32_extremes():
+    blk = k_block(oracle.Q3_K, d=1.0)
+    blk[96:108] = bytes(12)                 # every biased scale 0 -> -32
+    # codes: 2-bit value 0 with hmask clear -> -4 everywhere
+    xq = oracle.quantize(oracle.Q8_K, np.full(256, -1.0, np.float32))
+    s = oracle.block_isums(oracle.Q3_K, np.frombuffer(bytes(blk), np.uint8), xq, 1, 256, 1)[0, 0, 0, 0]
+    assert s == 16 * (-32) * 16 * (-4) * (-127)

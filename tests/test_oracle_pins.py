@@ -14,7 +14,8 @@ from goldens import floats, hexbytes, ints, keyvals, rows
 from javarand import JavaRandom
 
 ORACLE_TYPES = {"Q4_0": oracle.Q4_0, "Q4_1": oracle.Q4_1, "Q5_0": oracle.Q5_0,
-                "Q8_0": oracle.Q8_0, "Q4_K": oracle.Q4_K, "Q6_K": oracle.Q6_K,
+                "Q8_0": oracle.Q8_0, "Q2_K": oracle.Q2_K, "Q3_K": oracle.Q3_K,
+                "Q4_K": oracle.Q4_K, "Q5_K": oracle.Q5_K, "Q6_K": oracle.Q6_K,
                 "Q8_K": oracle.Q8_K}
 
 
@@ -38,7 +39,7 @@ def test_type_table():
             assert oracle.type_info(ORACLE_TYPES[name]) == (elems, nbytes)
             assert oracle.type_nbytes(ORACLE_TYPES[name], 4096) == 4096 // elems * nbytes
             seen += 1
-    assert seen == 7
+    assert seen == 10
     assert oracle.type_info(99) is None
 
 
@@ -49,8 +50,8 @@ def test_activation_pairing_follows_the_vec_dot_type_table():
     assert oracle.act_type(oracle.Q5_0) == oracle.Q8_0
     assert oracle.act_type(oracle.Q8_0) == oracle.Q8_0
     assert oracle.act_type(oracle.Q4_1) == oracle.Q8_1
-    assert oracle.act_type(oracle.Q4_K) == oracle.Q8_K
-    assert oracle.act_type(oracle.Q6_K) == oracle.Q8_K
+    for t in (oracle.Q2_K, oracle.Q3_K, oracle.Q4_K, oracle.Q5_K, oracle.Q6_K):
+        assert oracle.act_type(t) == oracle.Q8_K
 
 
 def test_row_length_must_be_whole_blocks():
