@@ -469,7 +469,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="layer_stack",
                     choices=["layer_stack", "q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000",
-                             "q4_1_4096", "q5_0_4096"])
+                             "q4_1_32000", "q5_0_32000", "q2_k_32000", "q3_k_32000", "q5_k_32000"])
     ap.add_argument("--n-vec", type=int, default=1)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
     ap.add_argument("--layers", type=int, default=None,

@@ -8,13 +8,14 @@ the current CUDA stream. There is no fallback: if the library is missing,
 importing this module raises.
 
 Element types are the ggml ids (Q4_0=2, Q4_1=3, Q5_0=6, Q8_0=8, Q8_1=9,
-Q4_K=12, Q6_K=14, Q8_K=15).
+Q2_K=10, Q3_K=11, Q4_K=12, Q5_K=13, Q6_K=14, Q8_K=15).
 """
 import ctypes
 import os
 
 __all__ = [
-    "F32", "F16", "Q4_0", "Q4_1", "Q5_0", "Q8_0", "Q8_1", "Q4_K", "Q6_K", "Q8_K", "MAX_NVEC", "QGError",
+    "F32", "F16", "Q4_0", "Q4_1", "Q5_0", "Q8_0", "Q8_1", "Q2_K", "Q3_K", "Q4_K", "Q5_K", "Q6_K", "Q8_K",
+    "MAX_NVEC", "QGError",
     "library_path", "lib", "qtype_nbytes", "qtype_block", "qtype_act_type",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes",
     "qgemv", "qgemv_xq", "qgemv_block_isums", "qgemv_noalloc", "qgemv_batched",
@@ -22,10 +23,12 @@ __all__ = [
     "MAX_BATCH",
 ]
 
-F32, F16, Q4_0, Q4_1, Q5_0, Q8_0, Q8_1, Q4_K, Q6_K, Q8_K = 0, 1, 2, 3, 6, 8, 9, 12, 14, 15
+F32, F16, Q4_0, Q4_1, Q5_0, Q8_0, Q8_1 = 0, 1, 2, 3, 6, 8, 9
+Q2_K, Q3_K, Q4_K, Q5_K, Q6_K, Q8_K = 10, 11, 12, 13, 14, 15
 MAX_NVEC = 8
 TYPE_NAMES = {F32: "F32", F16: "F16", Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0", Q8_0: "Q8_0",
-              Q8_1: "Q8_1", Q4_K: "Q4_K", Q6_K: "Q6_K", Q8_K: "Q8_K"}
+              Q8_1: "Q8_1", Q2_K: "Q2_K", Q3_K: "Q3_K", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K",
+              Q8_K: "Q8_K"}
 
 # every function declared in include/qgemv.h
 EXPORTED_SYMBOLS = (
@@ -234,12 +237,12 @@ def qgemv_xq(t: int, W, xq, n_out: int, n_in: int, n_vec: int = 1, y=None, strea
 
 
 def qgemv_block_isums(t: int, W, xq, n_out: int, n_in: int, n_vec: int = 1, out=None, stream=None):
-    """Exact per-block int32 sums, shape [n_vec, n_out, nb, k] (k = 2 for Q4_K)."""
+    """Exact per-block int32 sums, shape [n_vec, n_out, nb, k] (k = 2 for Q2_K, Q4_K, Q5_K)."""
     torch = _torch()
     _dev_tensor(W, torch.uint8, "W")
     _dev_tensor(xq, torch.uint8, "xq")
     elems, _ = qtype_block(t)
-    k = 2 if t == Q4_K else 1
+    k = 2 if t in (Q2_K, Q4_K, Q5_K) else 1
     shape = (n_vec, n_out, n_in // elems, k)
     if out is None:
         out = torch.empty(shape, dtype=torch.int32, device=W.device)

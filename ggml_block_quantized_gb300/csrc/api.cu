@@ -20,6 +20,9 @@ __global__ void dequant_q5_0_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q8_1_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q4_k_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q6_k_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q2_k_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q3_k_kernel(const uint8_t *, float *, int64_t);
+__global__ void dequant_q5_k_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q8_k_kernel(const uint8_t *, float *, int64_t);
 
 __device__ int32_t g_device_error = 0;
@@ -43,7 +46,10 @@ bool block_info(int type, int *elems, int *bytes) {
     case QG_Q5_0: *elems = 32; *bytes = 22; return true;
     case QG_Q8_0: *elems = 32; *bytes = 34; return true;
     case QG_Q8_1: *elems = 32; *bytes = 36; return true;
+    case QG_Q2_K: *elems = 256; *bytes = 84; return true;
+    case QG_Q3_K: *elems = 256; *bytes = 110; return true;
     case QG_Q4_K: *elems = 256; *bytes = 144; return true;
+    case QG_Q5_K: *elems = 256; *bytes = 176; return true;
     case QG_Q6_K: *elems = 256; *bytes = 210; return true;
     case QG_Q8_K: *elems = 256; *bytes = 292; return true;
     default: return false;
@@ -143,6 +149,9 @@ size_t act_smem_bytes(int type, int lpb, int nb, int nv) {
     case QG_Q4_1: return TypeQ4_1::act_bytes(nb, nv);
     case QG_Q5_0: return TypeQ5_0::act_bytes(nb, nv);
     case QG_Q4_K: return TypeQ4_K::act_bytes(nb, nv);
+    case QG_Q5_K: return TypeQ5_K::act_bytes(nb, nv);
+    case QG_Q2_K: return TypeQ2_K::act_bytes(nb, nv);
+    case QG_Q3_K: return TypeQ3_K::act_bytes(nb, nv);
     case QG_Q6_K: return lpb == TypeQ6_K4::kLanesPerBlock ? TypeQ6_K4::act_bytes(nb, nv) : TypeQ6_K::act_bytes(nb, nv);
     default: return 0;
     }
@@ -154,13 +163,20 @@ constexpr int kSmemTailPad = 16;  // unaligned word reads may touch up to 4 byte
 
 // Lanes of one activation block's f32 values (bytes) and lanes per weight
 // block, per type.
-int act_block_f32_bytes(int type) { return (type == QG_Q4_K || type == QG_Q6_K) ? 1024 : 128; }
+int act_block_f32_bytes(int type) {
+    int elems = 0, bytes = 0;
+    block_info(type, &elems, &bytes);
+    return 4 * elems;
+}
 // The item variants a type offers (lanes per weight block); Q6_K has a
 // two-lane item (fewer instructions per code) and a four-lane one (its
 // 8-block iterations fill better for some row lengths).
 int item_lpbs(int type, int (&out)[2]) {
     switch (type) {
     case QG_Q4_K: out[0] = TypeQ4_K::kLanesPerBlock; return 1;
+    case QG_Q5_K: out[0] = TypeQ5_K::kLanesPerBlock; return 1;
+    case QG_Q2_K: out[0] = TypeQ2_K::kLanesPerBlock; return 1;
+    case QG_Q3_K: out[0] = TypeQ3_K::kLanesPerBlock; return 1;
     case QG_Q6_K: out[0] = TypeQ6_K::kLanesPerBlock; out[1] = TypeQ6_K4::kLanesPerBlock; return 2;
     default: out[0] = 1; return 1;
     }
@@ -399,6 +415,9 @@ cudaError_t launch_gemv(int type, const GemvParams &p, const GemvMat *mats, int 
     case QG_Q4_1: return launch_gemv_q4_1(p, mats, n, nv, isums, l, device, s);
     case QG_Q5_0: return launch_gemv_q5_0(p, mats, n, nv, isums, l, device, s);
     case QG_Q4_K: return launch_gemv_q4_k(p, mats, n, nv, isums, l, device, s);
+    case QG_Q5_K: return launch_gemv_q5_k(p, mats, n, nv, isums, l, device, s);
+    case QG_Q2_K: return launch_gemv_q2_k(p, mats, n, nv, isums, l, device, s);
+    case QG_Q3_K: return launch_gemv_q3_k(p, mats, n, nv, isums, l, device, s);
     case QG_Q6_K: return launch_gemv_q6_k(p, mats, n, nv, isums, l, device, s);
     default: return cudaErrorInvalidValue;
     }
@@ -582,7 +601,10 @@ int qtype_act_type(int weight_type) {
     case QG_Q5_0:
     case QG_Q8_0: return QG_Q8_0;
     case QG_Q4_1: return QG_Q8_1;
+    case QG_Q2_K:
+    case QG_Q3_K:
     case QG_Q4_K:
+    case QG_Q5_K:
     case QG_Q6_K: return QG_Q8_K;
     default: return QG_ERR_PAIR;
     }
@@ -660,6 +682,9 @@ int dequantize_rows(int type, const void *W, float *out, int64_t n_rows, int64_t
     case QG_Q8_1: dequant_q8_1_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
     case QG_Q4_K: dequant_q4_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
     case QG_Q6_K: dequant_q6_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q2_K: dequant_q2_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q3_K: dequant_q3_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q5_K: dequant_q5_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
     case QG_Q8_K: dequant_q8_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
     default: return QG_ERR_TYPE;
     }
@@ -810,7 +835,8 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
         return buf;
     }
     const char *tn = type == QG_Q4_K ? "Q4_K" : type == QG_Q6_K ? "Q6_K" : type == QG_Q8_0 ? "Q8_0"
-                   : type == QG_Q4_1 ? "Q4_1" : type == QG_Q5_0 ? "Q5_0" : "Q4_0";
+                   : type == QG_Q4_1 ? "Q4_1" : type == QG_Q5_0 ? "Q5_0" : type == QG_Q2_K ? "Q2_K"
+                   : type == QG_Q3_K ? "Q3_K" : type == QG_Q5_K ? "Q5_K" : "Q4_0";
     if (mma_preferred(type, n_vec)) {
         // tiles: a batch of equal matrices is assumed for the tile count
         const int64_t per = total_rows / n_mats;

@@ -164,6 +164,91 @@ __global__ void dequant_q6_k_kernel(const uint8_t *__restrict__ W, float *__rest
     }
 }
 
+// Q5_K: Q4_K's scales, mins and nibbles plus bit j of qh[e % 32] as bit 4
+// of the code (sub-block j = e / 32).
+__global__ void dequant_q5_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 5) * 176;
+        const int e0 = 8 * static_cast<int>(g & 31);
+        const int j = e0 >> 5;
+        const float d = f16_bits_to_f32(ldg_u16(blk));
+        const float dmin = f16_bits_to_f32(ldg_u16(blk + 2));
+        const uint8_t *s = blk + 4;
+        int sc, m;
+        if (j < 4) {
+            sc = __ldg(s + j) & 63;
+            m = __ldg(s + j + 4) & 63;
+        } else {
+            sc = (__ldg(s + j + 4) & 0xF) | ((__ldg(s + j - 4) >> 6) << 4);
+            m = (__ldg(s + j + 4) >> 4) | ((__ldg(s + j) >> 6) << 4);
+        }
+        const float dsc = __fmul_rn(d, static_cast<float>(sc));
+        const float off = __fmul_rn(dmin, static_cast<float>(m));
+        const uint8_t *qs = blk + 48 + 32 * (j >> 1) + (e0 & 31);
+        const uint8_t *qh = blk + 16 + (e0 & 31);
+        const int shift = (j & 1) ? 4 : 0;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = ((__ldg(qs + i) >> shift) & 0xF) | (((__ldg(qh + i) >> j) & 1) << 4);
+            v[i] = __fsub_rn(__fmul_rn(dsc, static_cast<float>(q)), off);
+        }
+        store8(out + g * 8, v);
+    }
+}
+
+// Q2_K: element e = 128n + 32j + 16h + l takes bits 2j of qs[32n + 16h + l];
+// sub-block e / 16 has scale scales[e/16] & 15 and min scales[e/16] >> 4.
+__global__ void dequant_q2_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 5) * 84;
+        const int e0 = 8 * static_cast<int>(g & 31);
+        const int n = e0 >> 7, j = (e0 >> 5) & 3, h = (e0 >> 4) & 1, l0 = e0 & 15;
+        const int sm = __ldg(blk + (e0 >> 4));
+        const float d = f16_bits_to_f32(ldg_u16(blk + 80));
+        const float dmin = f16_bits_to_f32(ldg_u16(blk + 82));
+        const float dsc = __fmul_rn(d, static_cast<float>(sm & 0xF));
+        const float off = __fmul_rn(dmin, static_cast<float>(sm >> 4));
+        const uint8_t *qs = blk + 16 + 32 * n + 16 * h + l0;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = (__ldg(qs + i) >> (2 * j)) & 3;
+            v[i] = __fsub_rn(__fmul_rn(dsc, static_cast<float>(q)), off);
+        }
+        store8(out + g * 8, v);
+    }
+}
+
+// Q3_K: the Q2_K 2-bit value less 4 when bit 4n + j of hmask[16h + l] is
+// clear; scale = 6-bit field - 32 (low 4 bits in nibble (e/16) / 8 of byte
+// (e/16) % 8, high 2 bits at bits 2((e/16) / 4) of byte 8 + (e/16) % 4).
+__global__ void dequant_q3_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const uint8_t *blk = W + (g >> 5) * 110;
+        const int e0 = 8 * static_cast<int>(g & 31);
+        const int n = e0 >> 7, j = (e0 >> 5) & 3, h = (e0 >> 4) & 1, l0 = e0 & 15;
+        const int sb = e0 >> 4;
+        const int lo4 = (__ldg(blk + 96 + (sb & 7)) >> (4 * (sb >> 3))) & 0xF;
+        const int hi2 = (__ldg(blk + 104 + (sb & 3)) >> (2 * (sb >> 2))) & 3;
+        const float d = f16_bits_to_f32(ldg_u16(blk + 108));
+        const float dsc = __fmul_rn(d, static_cast<float>((lo4 | (hi2 << 4)) - 32));
+        const uint8_t *qs = blk + 32 + 32 * n + 16 * h + l0;
+        const uint8_t *hm = blk + 16 * h + l0;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q2 = (__ldg(qs + i) >> (2 * j)) & 3;
+            const int hb = (__ldg(hm + i) >> (4 * n + j)) & 1;
+            v[i] = __fmul_rn(dsc, static_cast<float>(q2 - (hb ? 0 : 4)));
+        }
+        store8(out + g * 8, v);
+    }
+}
+
 __global__ void dequant_q8_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {

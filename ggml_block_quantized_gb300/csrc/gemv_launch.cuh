@@ -102,6 +102,9 @@ QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_0)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_1)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q5_0)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q4_k)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q2_k)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q3_k)
+QG_DECLARE_GEMV_LAUNCH(launch_gemv_q5_k)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q6_k)
 QG_DECLARE_GEMV_LAUNCH(launch_gemv_q6_k4)
 #undef QG_DECLARE_GEMV_LAUNCH

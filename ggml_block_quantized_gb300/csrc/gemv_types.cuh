@@ -756,4 +756,262 @@ struct TypeQ6_K4 {
     }
 };
 
+// ------------------------------------------------------------------------
+// Q5_K (176-byte blocks, 16-byte aligned: f16 d, f16 dmin, scales[12] as
+// Q4_K, qh[32], qs[128]). Two lanes per block as Q4_K, same activation
+// record. The fifth bit of value l of sub-block j is bit j of qh[l]; it is
+// merged into bit 4 of the code bytes (low- and high-nibble sub-blocks
+// alike, so no factor 16 here).
+// ------------------------------------------------------------------------
+struct TypeQ5_K {
+    static constexpr int kBlockElems = 256, kBlockBytes = 176, kLanesPerBlock = 2, kSums = 2;
+    static constexpr int kActValues = 256;
+    static constexpr int kRecord = TypeQ4_K::kRecord;
+    static size_t act_bytes(int nb, int nv) { return TypeQ4_K::act_bytes(nb, nv); }
+    __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
+        TypeQ4_K::stage_act(xq, act, nb, nv, tid, nthr);
+    }
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        TypeQ4_K::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    }
+
+    template <int NV, bool ISUMS>
+    __device__ static void item(uint32_t rowa, int b, int h, bool active, uint32_t acta, int nb,
+                                float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;  // 16-byte aligned
+        const uint4 hdr = ld_s128(blk);
+        const float dw = f16_bits_to_f32(hdr.x);
+        const float dmin = f16_bits_to_f32(hdr.x >> 16);
+        const uint32_t SC = h == 0 ? (hdr.y & 0x3F3F3F3Fu)
+                                   : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
+        const uint32_t M = h == 0 ? (hdr.z & 0x3F3F3F3Fu)
+                                  : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
+        // fifth bits of sub-blocks 4h..4h+3: bits 0..3 of each qh byte after the shift
+        uint32_t qh[8];
+        {
+            const uint4 t0 = ld_s128(blk + 16u), t1 = ld_s128(blk + 32u);
+            const uint32_t w[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) qh[i] = (w[i] >> (4 * h)) & 0x0F0F0F0Fu;
+        }
+        uint32_t c[4][8];  // 5-bit codes of sub-block 4h + s, 4 per word
+        const uint32_t qa = blk + 48u + 64u * h;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 t = ld_s128(qa + 16u * j);
+            const uint32_t q[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = 4 * (j & 1) + u;      // word of the 32-value run
+                const int s0 = 2 * (j >> 1);        // low-nibble sub-block of this run
+                c[s0][i] = (q[u] & 0x0F0F0F0Fu) | ((qh[i] << (4 - s0)) & 0x10101010u);
+                c[s0 + 1][i] = ((q[u] >> 4) & 0x0F0F0F0Fu) | ((qh[i] << (3 - s0)) & 0x10101010u);
+            }
+        }
+        const int sc0 = SC & 0xFF, sc1 = (SC >> 8) & 0xFF, sc2 = (SC >> 16) & 0xFF, sc3 = SC >> 24;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const uint32_t rec = acta + ((static_cast<uint32_t>(v) * nb + b) * 2 + h) * kRecord;
+            int d[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint4 a0 = ld_s128(rec + 32u * s), a1 = ld_s128(rec + 32u * s + 16u);
+                int t = dp4a(c[s][0], a0.x, 0);
+                t = dp4a(c[s][1], a0.y, t);
+                t = dp4a(c[s][2], a0.z, t);
+                t = dp4a(c[s][3], a0.w, t);
+                t = dp4a(c[s][4], a1.x, t);
+                t = dp4a(c[s][5], a1.y, t);
+                t = dp4a(c[s][6], a1.z, t);
+                d[s] = dp4a(c[s][7], a1.w, t);
+            }
+            const uint4 ex = ld_s128(rec + 128);
+            int sq = sc0 * d[0] + sc1 * d[1] + sc2 * d[2] + sc3 * d[3];
+            int sm = dp2a_hi_su(ex.y, M, dp2a_lo_su(ex.x, M, 0));
+            if (ISUMS) {
+                sq = group_sum<2>(sq);
+                sm = group_sum<2>(sm);
+                if (active && h == 0) {
+                    isum_row[v * isum_vstride + 2 * b] = sq;
+                    isum_row[v * isum_vstride + 2 * b + 1] = sm;
+                }
+            } else if (active) {
+                const float dx = __uint_as_float(ex.z);
+                acc[v] = fmaf(dx * dw, static_cast<float>(sq), acc[v]);
+                acc[v] = fmaf(-(dx * dmin), static_cast<float>(sm), acc[v]);
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------------
+// Q2_K (84-byte blocks, 4-byte aligned: scales[16] (scale | min << 4),
+// qs[64], f16 d, f16 dmin). Two lanes per block: lane h takes values
+// 128h..128h+127, i.e. qs[32h..32h+31] and the 16-value sub-blocks 8h..8h+7.
+// Value 32j + 16hh + l of the half is bits 2j..2j+1 of byte 16hh + l of the
+// lane's qs run, so word i of the run (hh = i / 4) holds, at shift 2j, the
+// four codes that meet activation word 8j + i of the Q6_K-style record.
+// ------------------------------------------------------------------------
+struct TypeQ2_K {
+    static constexpr int kBlockElems = 256, kBlockBytes = 84, kLanesPerBlock = 2, kSums = 2;
+    static constexpr int kActValues = 256;
+    static constexpr int kRecord = TypeQ6_K::kRecord;
+    static size_t act_bytes(int nb, int nv) { return TypeQ6_K::act_bytes(nb, nv); }
+    __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
+        TypeQ6_K::stage_act(xq, act, nb, nv, tid, nthr);
+    }
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        TypeQ6_K::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    }
+
+    template <int NV, bool ISUMS>
+    __device__ static void item(uint32_t rowa, int b, int h, bool active, uint32_t acta, int nb,
+                                float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;  // 4-byte aligned
+        uint32_t q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = ld_s32(blk + 16u + 32u * h + 4u * i);
+        const uint32_t sw0 = ld_s32(blk + 8u * h), sw1 = ld_s32(blk + 8u * h + 4u);
+        const uint32_t dd = ld_s32(blk + 80u);
+        const float dw = f16_bits_to_f32(dd), dmin = f16_bits_to_f32(dd >> 16);
+        const uint32_t M0 = (sw0 >> 4) & 0x0F0F0F0Fu, M1 = (sw1 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t S0 = sw0 & 0x0F0F0F0Fu, S1 = sw1 & 0x0F0F0F0Fu;
+        int sc[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            sc[k] = (S0 >> (8 * k)) & 0xFF;
+            sc[4 + k] = (S1 >> (8 * k)) & 0xFF;
+        }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const uint32_t rec = acta + ((static_cast<uint32_t>(v) * nb + b) * 2 + h) * kRecord;
+            int sq = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 a0 = ld_s128(rec + 32u * j), a1 = ld_s128(rec + 32u * j + 16u);
+                // sub-blocks 2j (words 0..3) and 2j + 1 (words 4..7)
+                int t0 = dp4a((q[0] >> (2 * j)) & 0x03030303u, a0.x, 0);
+                t0 = dp4a((q[1] >> (2 * j)) & 0x03030303u, a0.y, t0);
+                t0 = dp4a((q[2] >> (2 * j)) & 0x03030303u, a0.z, t0);
+                t0 = dp4a((q[3] >> (2 * j)) & 0x03030303u, a0.w, t0);
+                int t1 = dp4a((q[4] >> (2 * j)) & 0x03030303u, a1.x, 0);
+                t1 = dp4a((q[5] >> (2 * j)) & 0x03030303u, a1.y, t1);
+                t1 = dp4a((q[6] >> (2 * j)) & 0x03030303u, a1.z, t1);
+                t1 = dp4a((q[7] >> (2 * j)) & 0x03030303u, a1.w, t1);
+                sq += sc[2 * j] * t0 + sc[2 * j + 1] * t1;
+            }
+            // min term: sum over the 8 sub-blocks of m * bsum16
+            const uint4 ex = ld_s128(rec + 128u);
+            int sm = dp2a_lo_su(ex.x, M0, 0);
+            sm = dp2a_hi_su(ex.y, M0, sm);
+            sm = dp2a_lo_su(ex.z, M1, sm);
+            sm = dp2a_hi_su(ex.w, M1, sm);
+            if (ISUMS) {
+                sq = group_sum<2>(sq);
+                sm = group_sum<2>(sm);
+                if (active && h == 0) {
+                    isum_row[v * isum_vstride + 2 * b] = sq;
+                    isum_row[v * isum_vstride + 2 * b + 1] = sm;
+                }
+            } else if (active) {
+                const float dx = __uint_as_float(ld_s32(rec + 144u));
+                acc[v] = fmaf(dx * dw, static_cast<float>(sq), acc[v]);
+                acc[v] = fmaf(-(dx * dmin), static_cast<float>(sm), acc[v]);
+            }
+        }
+    }
+};
+
+// Six-bit fields of each byte (0..63) minus 32, as signed bytes: b ^ 32
+// flips the field's top bit, then that bit is copied into bits 6..7 (the
+// product with 6 stays inside its byte).
+__device__ __forceinline__ uint32_t bias32_to_s8x4(uint32_t b) {
+    const uint32_t x = b ^ 0x20202020u;
+    return x | ((x & 0x20202020u) * 6u);
+}
+
+// ------------------------------------------------------------------------
+// Q3_K (110-byte blocks, 2-byte aligned: hmask[32], qs[64], scales[12],
+// f16 d). Two lanes per block: lane h takes values 128h..128h+127 (qs bytes
+// 32h.., bit 4h + j of hmask, sub-blocks 8h..8h+7). Codes enter as
+// c = q2 + 4 * hbit in 0..7 (value c - 4); the -4 goes through the bsums.
+// Sub-block scale = 6-bit field - 32: low 4 bits in nibble h of bytes
+// 0..7, high 2 bits at bits 4h + 2(sb / 4) of byte 8 + sb % 4.
+// ------------------------------------------------------------------------
+struct TypeQ3_K {
+    static constexpr int kBlockElems = 256, kBlockBytes = 110, kLanesPerBlock = 2, kSums = 1;
+    static constexpr int kActValues = 256;
+    static constexpr int kRecord = TypeQ6_K::kRecord;
+    static size_t act_bytes(int nb, int nv) { return TypeQ6_K::act_bytes(nb, nv); }
+    __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
+        TypeQ6_K::stage_act(xq, act, nb, nv, tid, nthr);
+    }
+    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+        TypeQ6_K::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    }
+
+    template <int NV, bool ISUMS>
+    __device__ static void item(uint32_t rowa, int b, int h, bool active, uint32_t acta, int nb,
+                                float (&acc)[NV], int32_t *isum_row, int64_t isum_vstride) {
+        const uint32_t blk = rowa + static_cast<uint32_t>(b) * kBlockBytes;  // 2-byte aligned
+        uint32_t hm[8], q[8], sw[3];
+        ld_words_a2<8>(blk, hm);
+        ld_words_a2<8>(blk + 32u + 32u * h, q);
+        ld_words_a2<3>(blk + 96u, sw);
+        const float dw = f16_bits_to_f32(ld_s16(blk + 108u));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hm[i] = (hm[i] >> (4 * h)) & 0x0F0F0F0Fu;  // bit j: row j of this half
+        // biased 6-bit scales of sub-blocks 8h..8h+3 and 8h+4..8h+7
+        const uint32_t lo0 = (sw[0] >> (4 * h)) & 0x0F0F0F0Fu, lo1 = (sw[1] >> (4 * h)) & 0x0F0F0F0Fu;
+        const uint32_t B0 = lo0 | (((sw[2] >> (4 * h)) & 0x03030303u) << 4);
+        const uint32_t B1 = lo1 | (((sw[2] >> (4 * h + 2)) & 0x03030303u) << 4);
+        const uint32_t SC0 = bias32_to_s8x4(B0), SC1 = bias32_to_s8x4(B1);
+        int sc[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            sc[k] = sbyte(SC0, k);
+            sc[4 + k] = sbyte(SC1, k);
+        }
+        uint32_t c[4][8];  // codes q2 + 4 hbit of row j, word i
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                c[j][i] = ((q[i] >> (2 * j)) & 0x03030303u) | (j <= 2 ? ((hm[i] << (2 - j)) & 0x04040404u)
+                                                                      : ((hm[i] >> 1) & 0x04040404u));
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const uint32_t rec = acta + ((static_cast<uint32_t>(v) * nb + b) * 2 + h) * kRecord;
+            int s = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 a0 = ld_s128(rec + 32u * j), a1 = ld_s128(rec + 32u * j + 16u);
+                int t0 = dp4a(c[j][0], a0.x, 0);
+                t0 = dp4a(c[j][1], a0.y, t0);
+                t0 = dp4a(c[j][2], a0.z, t0);
+                t0 = dp4a(c[j][3], a0.w, t0);
+                int t1 = dp4a(c[j][4], a1.x, 0);
+                t1 = dp4a(c[j][5], a1.y, t1);
+                t1 = dp4a(c[j][6], a1.z, t1);
+                t1 = dp4a(c[j][7], a1.w, t1);
+                s += sc[2 * j] * t0 + sc[2 * j + 1] * t1;
+            }
+            // the -4 offset: 4 * sum over sub-blocks of sc * bsum16
+            const uint4 ex = ld_s128(rec + 128u);
+            int t = dp2a_lo_ss(ex.x, SC0, 0);
+            t = dp2a_hi_ss(ex.y, SC0, t);
+            t = dp2a_lo_ss(ex.z, SC1, t);
+            t = dp2a_hi_ss(ex.w, SC1, t);
+            s -= 4 * t;
+            if (ISUMS) {
+                s = group_sum<2>(s);
+                if (active && h == 0) isum_row[v * isum_vstride + b] = s;
+            } else if (active) {
+                acc[v] = fmaf(static_cast<float>(s), dw * __uint_as_float(ld_s32(rec + 144u)), acc[v]);
+            }
+        }
+    }
+};
+
+
 }  // namespace qg

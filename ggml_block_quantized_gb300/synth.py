@@ -16,8 +16,12 @@ Workloads (names used across tests and bench.py):
   layer_stack     32 decoder layers, each Q4_K q/k/v/o 4096 x 4096, Q4_K
                   gate/up 11008 x 4096, Q6_K down 4096 x 11008 (random blocks
                   as above), a fresh x ~ N(0, 1) per matrix and vector
-  q4_1_4096       Q4_1 weights from f32 N(0, 0.02) + 0.01, 4096 x 4096, x ~ N(0, 1)
-  q5_0_4096       Q5_0 weights from f32 N(0, 0.02), 4096 x 4096, x ~ N(0, 1)
+  q4_1_32000      Q4_1 weights from f32 N(0, 0.02) + 0.01, 32000 x 4096, x ~ N(0, 1)
+  q5_0_32000      Q5_0 weights from f32 N(0, 0.02), 32000 x 4096, x ~ N(0, 1)
+  q2_k_32000, q3_k_32000, q5_k_32000
+                  random Q2_K / Q3_K / Q5_K super-blocks (k_blocks), 32000 x 4096
+                  (the output-projection shape of the Q6_K workload: large
+                  enough that one call streams at the kernel's rate)
 Seeds: weights 1000 + workload index, activations 2000 + workload index; the
 layer stack derives per-(layer, matrix) streams from those.
 """
@@ -31,7 +35,7 @@ K_TYPES = (Q2_K, Q3_K, Q4_K, Q5_K, Q6_K)
 FROM_F32 = (Q8_0, Q4_0, Q4_1, Q5_0)  # workloads that quantize f32 weights
 
 WORKLOADS = ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000", "layer_stack",
-             "q4_1_4096", "q5_0_4096"]
+             "q4_1_32000", "q5_0_32000", "q2_k_32000", "q3_k_32000", "q5_k_32000"]
 
 # (name, type, n_out, n_in) of one decoder layer of the stack
 LAYER_MATRICES = [
@@ -114,8 +118,11 @@ def single_matrix(name: str, n_vec: int = 1, n_out: int = None, n_in: int = None
         "q4_0_4096": (Q4_0, 4096, 4096),
         "q4_k_4096": (Q4_K, 4096, 4096),
         "q6_k_32000": (Q6_K, 32000, 4096),
-        "q4_1_4096": (Q4_1, 4096, 4096),
-        "q5_0_4096": (Q5_0, 4096, 4096),
+        "q4_1_32000": (Q4_1, 32000, 4096),
+        "q5_0_32000": (Q5_0, 32000, 4096),
+        "q2_k_32000": (Q2_K, 32000, 4096),
+        "q3_k_32000": (Q3_K, 32000, 4096),
+        "q5_k_32000": (Q5_K, 32000, 4096),
     }[name]
     t, d_out, d_in = spec
     n_out = d_out if n_out is None else n_out

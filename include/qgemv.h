@@ -2,9 +2,9 @@
  * qgemv.h - C ABI of the GB300 block-quantized matrix-vector product.
  *
  * y = W . x for W stored as byte-exact GGUF blocks (Q8_0, Q4_0, Q4_1, Q5_0,
- * Q4_K, Q6_K), x quantized once per call to the activation blocks paired
- * with the weight type (Q8_0, Q8_1 or Q8_K), exact int32 sums inside every
- * block and float only for the block scales.
+ * Q2_K, Q3_K, Q4_K, Q5_K, Q6_K), x quantized once per call to the activation
+ * blocks paired with the weight type (Q8_0, Q8_1 or Q8_K), exact int32 sums
+ * inside every block and float only for the block scales.
  *
  * Citations name the reference pages by title and section:
  *   [rml]      "Quantization" (rayaq.ca/rml)
@@ -60,7 +60,10 @@ enum qg_type {
     QG_Q5_0 = 6,   /* 32 elements, 22 bytes: f16 d, u32 qh (fifth bits), 16 bytes of nibbles */
     QG_Q8_0 = 8,   /* 32 elements, 34 bytes: f16 d, 32 int8                  */
     QG_Q8_1 = 9,   /* 32 elements, 36 bytes: f16 d, f16 s, 32 int8 (activations only) */
+    QG_Q2_K = 10,  /* 256 elements, 84 bytes: 16 B scales|mins, 64 B qs, f16 d, f16 dmin */
+    QG_Q3_K = 11,  /* 256 elements, 110 bytes: 32 B hmask, 64 B qs, 12 B scales, f16 d */
     QG_Q4_K = 12,  /* 256 elements, 144 bytes: f16 d, f16 dmin, 12 B scales, 128 B qs */
+    QG_Q5_K = 13,  /* 256 elements, 176 bytes: f16 d, f16 dmin, 12 B scales, 32 B qh, 128 B qs */
     QG_Q6_K = 14,  /* 256 elements, 210 bytes: 128 B ql, 64 B qh, 16 int8 scales, f16 d */
     QG_Q8_K = 15   /* 256 elements, 292 bytes: f32 d, 256 int8, 16 int16 bsums (activations only) */
 };
@@ -92,8 +95,8 @@ int qtype_block(int type, int *elems, int *bytes);
 
 /* Activation type paired with a weight type ([rml] DotActivationType;
  * [candle] VecDotType table): Q4_0, Q5_0 and Q8_0 -> QG_Q8_0, Q4_1 ->
- * QG_Q8_1, Q4_K and Q6_K -> QG_Q8_K. Returns QG_ERR_PAIR for any other
- * type. */
+ * QG_Q8_1, the K-quants Q2_K..Q6_K -> QG_Q8_K. Returns QG_ERR_PAIR for any
+ * other type. */
 int qtype_act_type(int weight_type);
 
 /* Static text for a status code. Never NULL. */
@@ -152,9 +155,20 @@ int quantize_rows(int type, const float *x, void *out, int64_t n_rows, int64_t n
  *         [rml]'s element-200 trace
  *   Q6_K: (d * sc_j) * (q - 32), j = e / 16, q = 4 low bits from ql and 2
  *         high bits from qh (element mapping: the library's stated reading)
+ *   Q5_K: as Q4_K with q = nibble | (bit j of qh[e % 32]) << 4
+ *   Q2_K: (d * sc_j) * q - dmin * m_j, j = e / 16, sc/m the low/high nibble
+ *         of scales[j], q = bits 2k..2k+1 of qs[32n + 16h + l] for
+ *         e = 128n + 32k + 16h + l
+ *   Q3_K: (d * (sc_j - 32)) * (q - 4 * (1 - hbit)), j = e / 16, q as Q2_K,
+ *         hbit = bit 4n + k of hmask[16h + l], sc_j the 6-bit field whose
+ *         low 4 bits are nibble j / 8 of byte j % 8 and high 2 bits are bits
+ *         2(j / 4) of byte 8 + j % 4
+ *   (the Q2_K, Q3_K and Q5_K layouts are ggml's, which the pages do not
+ *   print: the library's stated reading)
  *   Q8_K: q * d
- * Every product is exact in f32, so results are unique (only Q4_K's
- * subtraction rounds, to nearest even). W: n_rows * qtype_nbytes(type, n_in)
+ * Every product is exact in f32, so results are unique (only the
+ * subtraction of Q2_K, Q4_K and Q5_K and the addition of Q4_1 round, to
+ * nearest even). W: n_rows * qtype_nbytes(type, n_in)
  * bytes; out: f32 [n_rows][n_in]. */
 int dequantize_rows(int type, const void *W, float *out, int64_t n_rows, int64_t n_in,
                     qg_stream_t stream);
@@ -169,9 +183,9 @@ size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec);
  * [lesson21] Examples 10-11): quantizes x once into `workspace` with
  * quantize_act's rule for the paired activation type, then for every row
  * and block forms the exact int32 block sum and adds
- *   Q8_0, Q4_0, Q5_0, Q6_K: S * (d_w * d_x)
- *   Q4_1:                   S * (d_w * d_x) + m_w * s_x
- *   Q4_K:                   d_x * (d_w * S_q - dmin_w * S_m)
+ *   Q8_0, Q4_0, Q5_0, Q3_K, Q6_K: S * (d_w * d_x)
+ *   Q4_1:                         S * (d_w * d_x) + m_w * s_x
+ *   Q2_K, Q4_K, Q5_K:             d_x * (d_w * S_q - dmin_w * S_m)
  * in f32. The f32 order of these few float operations is not fixed by the
  * pages; results agree with an f64 accumulation to about 1e-5 relative.
  * For Q4_K and Q6_K with n_vec >= 3 the sums are formed on the tensor cores
@@ -196,8 +210,9 @@ int qgemv_xq(int type, const void *W, const void *xq, float *y, int64_t n_out, i
 
 /* Diagnostic: the exact per-block int32 sums that qgemv_xq forms, written to
  * isums[((v * n_out + o) * nb + b) * k + t], nb = n_in / block elements,
- * k = 2 for Q4_K (t = 0: S_q = sum_j sc_j sum_{i in j} q_i a_i, t = 1:
- * S_m = sum_j m_j (bsum_2j + bsum_2j+1)) and k = 1 otherwise (Q8_0:
+ * k = 2 for Q2_K, Q4_K and Q5_K (t = 0: S_q = sum_j sc_j sum_{i in j}
+ * q_i a_i, t = 1: S_m = sum_j m_j (sum of a over sub-block j)) and k = 1
+ * otherwise (Q3_K: sum_j sc_j sum_{i in j} q_i a_i with signed q; Q8_0:
  * sum qw qx; Q4_0: sum (code - 8) qx; Q5_0: sum (code - 16) qx; Q4_1:
  * sum code qx, its min term m_w s_x being float; Q6_K: sum_j sc_j
  * sum_{i in j} (q_i - 32) a_i) ([rml] Quantized dot products, Kernels and

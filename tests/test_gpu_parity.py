@@ -17,7 +17,7 @@ from ggml_block_quantized_gb300 import synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 REL, ABS = 1e-5, 1e-6
-WTYPES = [qg.Q8_0, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q4_K, qg.Q6_K]
+WTYPES = [qg.Q8_0, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q2_K, qg.Q3_K, qg.Q4_K, qg.Q5_K, qg.Q6_K]
 LEGACY = (qg.Q8_0, qg.Q4_0, qg.Q4_1, qg.Q5_0)  # 32-element blocks
 
 
@@ -143,12 +143,13 @@ def test_quantize_rows_bit_exact(t):
 
 
 # ------------------------------------------------------------- dequantize
-@pytest.mark.parametrize("t", [qg.Q8_0, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q8_1, qg.Q4_K, qg.Q6_K, qg.Q8_K])
+@pytest.mark.parametrize("t", [qg.Q8_0, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q8_1, qg.Q2_K, qg.Q3_K, qg.Q4_K,
+                               qg.Q5_K, qg.Q6_K, qg.Q8_K])
 def test_dequantize_bit_exact(t):
     rng = np.random.default_rng(300 + t)
     elems, nbytes = oracle.type_info(t)
     for n_rows, n_in in ((1, elems), (3, 5 * elems), (37, 4096), (129, 11008 if elems == 256 else 1024)):
-        if t in (qg.Q4_K, qg.Q6_K):
+        if t in synth.K_TYPES:
             W = synth.k_blocks(t, n_rows * n_in // 256, rng)
         else:
             W = synth.random_bytes(rng, n_rows * n_in // elems * nbytes).reshape(-1, nbytes)
@@ -178,6 +179,9 @@ SHAPES = {  # (n_out, n_in): one block; ragged rows; several stages and ring wra
     qg.Q4_1: [(1, 32), (37, 96), (300, 1024), (5000, 4096)],
     qg.Q5_0: [(1, 32), (37, 96), (300, 1024), (5000, 4096)],
     qg.Q4_K: [(1, 256), (37, 768), (300, 11008), (5000, 4096)],
+    qg.Q2_K: [(1, 256), (37, 768), (300, 11008), (5000, 4096)],
+    qg.Q3_K: [(1, 256), (37, 768), (300, 11008), (3000, 4096)],
+    qg.Q5_K: [(1, 256), (37, 768), (300, 11008), (5000, 4096)],
     qg.Q6_K: [(1, 256), (37, 768), (300, 11008), (3000, 4096)],
 }
 
@@ -250,8 +254,8 @@ def test_qgemv_small_shapes_all_rows(t):
             check_y(t, W, x, y, n_out, n_in, n_vec)
 
 
-@pytest.mark.parametrize("name", ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000", "q4_1_4096",
-                                  "q5_0_4096"])
+@pytest.mark.parametrize("name", ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000", "q4_1_32000",
+                                  "q5_0_32000", "q2_k_32000", "q3_k_32000", "q5_k_32000"])
 @pytest.mark.parametrize("n_vec", [1, 8])
 def test_qgemv_workloads_full_size(name, n_vec):
     m = synth.single_matrix(name, n_vec=n_vec)
@@ -303,7 +307,8 @@ def test_edges_empty_and_tails():
              dev(synth.f32_normal(rng, 256)), 0, 256, 1, y=torch.zeros(4, device="cuda"))
     # W byte lengths that end inside a 16-byte chunk (34, 630, 18*3 bytes)
     for t, n_out, n_in in ((qg.Q8_0, 1, 32), (qg.Q6_K, 3, 256), (qg.Q4_0, 3, 32), (qg.Q6_K, 7, 2304),
-                           (qg.Q4_1, 1, 32), (qg.Q5_0, 3, 32), (qg.Q5_0, 5, 96)):
+                           (qg.Q4_1, 1, 32), (qg.Q5_0, 3, 32), (qg.Q5_0, 5, 96), (qg.Q3_K, 1, 256),
+                           (qg.Q3_K, 3, 768), (qg.Q2_K, 1, 256)):
         W = weights(t, n_out, n_in, rng)
         assert W.size % 16 != 0
         for n_vec in (1, 4):

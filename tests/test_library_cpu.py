@@ -44,7 +44,8 @@ def test_header_declarations_are_exported(L):
 
 
 def test_type_table_matches_the_oracle(L):
-    for t in (qg.F32, qg.F16, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q8_0, qg.Q8_1, qg.Q4_K, qg.Q6_K, qg.Q8_K):
+    for t in (qg.F32, qg.F16, qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q8_0, qg.Q8_1, qg.Q2_K, qg.Q3_K, qg.Q4_K,
+              qg.Q5_K, qg.Q6_K, qg.Q8_K):
         assert qg.qtype_block(t) == oracle.type_info(t)
         for n in (0, 256, 4096, 11008, 32 * 7, 100):
             assert qg.qtype_nbytes(t, n) == oracle.type_nbytes(t, n)
@@ -61,6 +62,8 @@ def test_pairing(L):
     assert qg.qtype_act_type(qg.Q6_K) == qg.Q8_K
     assert qg.qtype_act_type(qg.Q5_0) == qg.Q8_0
     assert qg.qtype_act_type(qg.Q4_1) == qg.Q8_1
+    for t in (qg.Q2_K, qg.Q3_K, qg.Q5_K):
+        assert qg.qtype_act_type(t) == qg.Q8_K
     for t in (qg.F32, qg.F16, qg.Q8_K, qg.Q8_1, 7, 99):
         assert qg.qtype_act_type(t) == ERR_PAIR
 
