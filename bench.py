@@ -49,7 +49,10 @@ def measured_peaks():
 
 
 def kernel_family(kernel_desc):
-    """'mma' for the tensor-core kernel, 'dp4a' for the streaming __dp4a one."""
+    """'tc' for the tcgen05 kernel, 'mma' for the mma.sync tensor-core kernel,
+    'dp4a' for the streaming __dp4a one."""
+    if kernel_desc.startswith("gemv_tc"):
+        return "tc"
     return "mma" if kernel_desc.startswith("gemv_mma") else "dp4a"
 
 
@@ -59,7 +62,10 @@ def kernel_source_hash(family):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ggml_block_quantized_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        mine = name.startswith("gemv_mma") if family == "mma" else (name.startswith("gemv") and not name.startswith("gemv_mma"))
+        if family in ("mma", "tc"):
+            mine = name.startswith("gemv_" + family)
+        else:
+            mine = name.startswith("gemv") and not name.startswith(("gemv_mma", "gemv_tc"))
         if mine or name == "qg_common.cuh":
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + f.read())

@@ -35,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "qtype_nbytes", "qtype_block", "qtype_act_type", "qg_status_string", "qg_last_cuda_error",
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes", "qgemv",
     "qgemv_xq", "qgemv_block_isums", "qg_device_error", "qgemv_noalloc",
-    "qgemv_batched_workspace_bytes", "qgemv_batched", "qgemv_kernel_info",
+    "qgemv_batched_workspace_bytes", "qgemv_batched", "qgemv_kernel_info", "qg_tune",
 )
 MAX_BATCH = 256
 
@@ -92,6 +92,7 @@ def lib():
         L.qgemv_batched.restype = i32
         L.qgemv_kernel_info.argtypes = [i32, i64, i64, i64, i32]
         L.qgemv_kernel_info.restype = ctypes.c_char_p
+        L.qg_tune.argtypes, L.qg_tune.restype = [ctypes.c_char_p, i32, ctypes.POINTER(i32)], i32
         _lib = L
     return _lib
 
@@ -315,6 +316,14 @@ def qgemv_batched(t: int, mats, n_in: int, n_vec: int = 1, workspace=None, strea
 def kernel_info(t: int, total_rows: int, n_in: int, n_vec: int = 1, n_mats: int = 1) -> str:
     """Which kernel and plan a product would use on the current device."""
     return lib().qgemv_kernel_info(t, total_rows, n_in, n_vec, n_mats).decode()
+
+
+def tune(name: str, value: int) -> int:
+    """Set a tuning knob (an environment variable name such as "QG_TC") for
+    the rest of the process; returns its previous value."""
+    prev = ctypes.c_int32(0)
+    _check(lib().qg_tune(name.encode(), int(value), ctypes.byref(prev)), "qg_tune")
+    return prev.value
 
 
 def device_error() -> int:

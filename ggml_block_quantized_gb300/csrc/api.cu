@@ -5,7 +5,10 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <atomic>
+
 #include "gemv_launch.cuh"
+#include "gemv_tc.cuh"
 
 namespace qg {
 
@@ -24,6 +27,8 @@ __global__ void dequant_q2_k_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q3_k_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q5_k_kernel(const uint8_t *, float *, int64_t);
 __global__ void dequant_q8_k_kernel(const uint8_t *, float *, int64_t);
+cudaError_t launch_gemv_tc_q4_k(const TcParams &p, const TcMat *mats, int n, int grid, int smem, int smem_optin,
+                                int device, cudaStream_t s);
 
 __device__ int32_t g_device_error = 0;
 
@@ -105,35 +110,58 @@ int env_int(const char *name, int dflt, int lo, int hi) {
     return v < lo ? lo : (v > hi ? hi : v);
 }
 
-// Tuning of the GEMV launch (read once): CTAs resident per SM that the grid
-// aims at, and the shared-memory ring budget per CTA in KiB.
-int tune_ctas_per_sm() {
-    static const int v = env_int("QG_CTAS_PER_SM", 2, 1, 4);
-    return v;
-}
-int tune_ring_kib() {
-    static const int v = env_int("QG_RING_KIB", 96, 16, 200);
-    return v;
+// Tuning knobs. Each is read once from the environment variable of the same
+// name (defaults are the measured best) and can be set for the rest of the
+// process with qg_tune():
+//  QG_CTAS_PER_SM, QG_RING_KIB: CTAs per SM the __dp4a GEMV grid aims at, and
+//    its shared-memory ring budget per CTA in KiB;
+//  QG_MMA_MIN_NVEC: vectors from which Q4_K / Q6_K products run on the
+//    tensor cores;
+//  QG_MMA_PANEL, QG_MMA_KB: mma.sync plan overrides (activation source: 0
+//    automatic, 1 a shared-memory panel, 8 the biased-int8 panel; an upper
+//    bound on blocks per chunk, 0 none);
+//  QG_FUSED_QUANT_KIB: f32 activations up to this size are quantized inside
+//    the GEMV's prologue;
+//  QG_TC: the tcgen05 Q4_K kernel for three or more vectors -- 0 never (the
+//    default: the mma.sync kernel measured faster on this GPU), 1 whenever its
+//    shared memory fits (rows of 8 or 16 blocks).
+enum KnobId {
+    kKnobCtasPerSm,
+    kKnobRingKib,
+    kKnobMmaMinNvec,
+    kKnobMmaPanel,
+    kKnobMmaKb,
+    kKnobFusedQuantKib,
+    kKnobTc,
+    kKnobCount
+};
+struct KnobDef {
+    const char *name;
+    int dflt, lo, hi;
+};
+constexpr KnobDef kKnobs[kKnobCount] = {
+    {"QG_CTAS_PER_SM", 2, 1, 4},          {"QG_RING_KIB", 96, 16, 200}, {"QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1},
+    {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 48, 0, 1024},
+    {"QG_TC", 0, 0, 1}};
+std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
+
+int knob(KnobId k) {
+    int v = g_knob_val[k].load(std::memory_order_relaxed);
+    if (v == 0) {
+        int expected = 0;
+        const int env = env_int(kKnobs[k].name, kKnobs[k].dflt, kKnobs[k].lo, kKnobs[k].hi) + 1;
+        g_knob_val[k].compare_exchange_strong(expected, env, std::memory_order_relaxed);
+        v = g_knob_val[k].load(std::memory_order_relaxed);
+    }
+    return v - 1;
 }
 
-// Vectors from which Q4_K / Q6_K products run on the tensor cores.
-int tune_mma_min_nvec() {
-    static const int v = env_int("QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1);
-    return v;
-}
-
-// Tensor-core plan overrides: activation source (0 = automatic; 1 = a
-// shared-memory panel even where registers would do; 8 = the biased-int8
-// panel) and an upper bound on blocks per chunk of the panel kernel (0 =
-// none).
-int tune_mma_panel() {
-    static const int v = env_int("QG_MMA_PANEL", 0, 0, 16);
-    return v;
-}
-int tune_mma_kb() {
-    static const int v = env_int("QG_MMA_KB", 0, 0, 4096);
-    return v;
-}
+int tune_ctas_per_sm() { return knob(kKnobCtasPerSm); }
+int tune_ring_kib() { return knob(kKnobRingKib); }
+int tune_mma_min_nvec() { return knob(kKnobMmaMinNvec); }
+int tune_mma_panel() { return knob(kKnobMmaPanel); }
+int tune_mma_kb() { return knob(kKnobMmaKb); }
+int tune_tc() { return knob(kKnobTc); }
 
 bool mma_type(int type) { return type == QG_Q4_K || type == QG_Q6_K; }
 
@@ -407,6 +435,31 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
     return QG_OK;
 }
 
+// Plan of the tcgen05 Q4_K kernel: ring depth next to the activation panel,
+// grid. False when the knob is off or the shapes rule it out: rows of 8 or 16
+// blocks only (whole rows travel per stage; blocks go to the mma in groups of
+// eight), or fewer than two stages of shared memory.
+bool plan_gemv_tc(int type, int64_t tiles, int64_t n_in, int nv, int n_mats, int sms, int smem_limit, TcParams *p,
+                  int *grid, int *smem) {
+    const int mode = tune_tc();
+    if (type != QG_Q4_K || mode == 0 || n_mats < 1 || n_mats > kTcMaxBatch || tiles < 1) return false;
+    const int64_t nb = n_in / 256;
+    if (nb != kTcGroupBlocks && nb != 2 * kTcGroupBlocks) return false;
+    const int64_t fixed = tc_smem_bytes(static_cast<int>(nb), 0);
+    int64_t S = (smem_limit - fixed) / tc_stage_bytes(static_cast<int>(nb));
+    if (S > kTcMaxStages) S = kTcMaxStages;
+    if (S < 2) return false;
+    *p = TcParams{};
+    p->total_tiles = tiles;
+    p->n_mats = n_mats;
+    p->nb = static_cast<int>(nb);
+    p->nv = nv;
+    p->n_stages = static_cast<int>(S);
+    *grid = static_cast<int>(tiles < sms ? tiles : sms);
+    *smem = tc_smem_bytes(static_cast<int>(nb), static_cast<int>(S));
+    return true;
+}
+
 cudaError_t launch_gemv(int type, const GemvParams &p, const GemvMat *mats, int n, int nv, bool isums,
                         const GemvLaunch &l, int device, cudaStream_t s) {
     switch (type) {
@@ -469,10 +522,7 @@ int launch_quantize_batched(int act_type, const QuantTable &t, int n, void *xq, 
 // default 48 KiB) are quantized inside the GEMV's prologue (every CTA reads
 // x once); larger ones go through the separate quantization launch into the
 // workspace.
-int64_t fused_quant_max_bytes() {
-    static const int64_t v = static_cast<int64_t>(env_int("QG_FUSED_QUANT_KIB", 48, 0, 1024)) * 1024;
-    return v;
-}
+int64_t fused_quant_max_bytes() { return static_cast<int64_t>(knob(kKnobFusedQuantKib)) * 1024; }
 
 bool fused_quantization(int64_t n_in, int64_t n_vec) { return 4 * n_in * n_vec <= fused_quant_max_bytes(); }
 
@@ -500,7 +550,35 @@ int run_gemv_mats(int type, GemvMat *mats, int n, int64_t n_in, int64_t n_vec, s
     }
     if (total == 0) return QG_OK;
     if (!isums && x_bytes == 0 && mma_preferred(type, n_vec)) {
-        // several vectors: the tensor-core kernel, when its shapes fit
+        // several vectors: the tcgen05 kernel (Q4_K, launches of many 16-row
+        // tiles), else the mma.sync kernel, when their shapes fit
+        int64_t tiles16 = 0;
+        for (int i = 0; i < n; ++i) tiles16 += (mats[i].n_out + kTcRows - 1) / kTcRows;
+        TcParams tp = {};
+        int tgrid = 0, tsmem = 0;
+        if (plan_gemv_tc(type, tiles16, n_in, static_cast<int>(n_vec), n, dev.sms, dev.smem_optin, &tp, &tgrid,
+                         &tsmem)) {
+            TcMat tm[kTcMaxBatch];
+            int64_t base = 0;
+            for (int i = 0; i < n; ++i) {
+                tm[i] = TcMat{};
+                tm[i].W = mats[i].W;
+                tm[i].xq = mats[i].xq;
+                tm[i].y = mats[i].y;
+                tm[i].n_out = mats[i].n_out;
+                tm[i].tile_base = base;
+                base += (mats[i].n_out + kTcRows - 1) / kTcRows;
+            }
+            tp.err = dev.err;
+            cudaError_t e = launch_gemv_tc_q4_k(tp, tm, n, tgrid, tsmem, dev.smem_optin, dev.device, s);
+            if (e != cudaSuccess) {
+                char where[160];
+                std::snprintf(where, sizeof where, "%s; tcgen05 grid %d block %d smem %d stages %d", g_launch_step,
+                              tgrid, kTcThreads, tsmem, tp.n_stages);
+                return cuda_fail(e, where);
+            }
+            return QG_OK;
+        }
         MmaMat mm[QG_MAX_BATCH];
         int64_t tiles = 0;
         for (int i = 0; i < n; ++i) {
@@ -625,6 +703,19 @@ const char *qg_status_string(int status) {
 }
 
 const char *qg_last_cuda_error(void) { return g_last_cuda_error; }
+
+int qg_tune(const char *name, int value, int *previous) {
+    if (!name) return QG_ERR_NULL;
+    for (int k = 0; k < kKnobCount; ++k) {
+        if (std::strcmp(name, kKnobs[k].name) != 0) continue;
+        const int old = knob(static_cast<KnobId>(k));
+        const int v = value < kKnobs[k].lo ? kKnobs[k].lo : (value > kKnobs[k].hi ? kKnobs[k].hi : value);
+        g_knob_val[k].store(v + 1, std::memory_order_relaxed);
+        if (previous) *previous = old;
+        return QG_OK;
+    }
+    return QG_ERR_TYPE;
+}
 
 int quantize_act(int act_type, const float *x, void *xq, int64_t n_in, int64_t n_vec, qg_stream_t stream) {
     int elems, bytes;
@@ -840,6 +931,14 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
     if (mma_preferred(type, n_vec)) {
         // tiles: a batch of equal matrices is assumed for the tile count
         const int64_t per = total_rows / n_mats;
+        TcParams tp = {};
+        int tgrid = 0, tsmem = 0;
+        if (plan_gemv_tc(type, n_mats * ((per + kTcRows - 1) / kTcRows), n_in, static_cast<int>(n_vec), n_mats,
+                         dev.sms, dev.smem_optin, &tp, &tgrid, &tsmem)) {
+            std::snprintf(buf, sizeof buf, "gemv_tc_kernel<%s,tcgen05> grid=%d stages=%d tile_rows=%d smem=%d", tn,
+                          tgrid, tp.n_stages, kTcRows, tsmem);
+            return buf;
+        }
         const int64_t tiles = n_mats * ((per + kMmaTileRows - 1) / kMmaTileRows);
         MmaParams mp = {};
         MmaLaunch ml = {};

@@ -292,6 +292,18 @@ int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, i
  * a CUDA error. Launches nothing. */
 const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_t n_vec, int n_mats);
 
+/* Sets a tuning knob for the rest of the process (the pages have no
+ * counterpart; the knobs choose between kernels that compute the same
+ * product). name is one of the environment variables the library reads once
+ * at first use: QG_CTAS_PER_SM, QG_RING_KIB, QG_MMA_MIN_NVEC, QG_MMA_PANEL,
+ * QG_MMA_KB, QG_FUSED_QUANT_KIB, QG_TC (the tcgen05 Q4_K kernel for three or
+ * more vectors, rows of 2048 or 4096 elements: 0 never, the default; 1
+ * whenever it fits). value is clamped to the knob's range; the old
+ * value goes to *previous when that is not NULL. Returns QG_OK, QG_ERR_NULL
+ * or QG_ERR_TYPE (unknown name). Host-only; affects launches planned after
+ * it returns. */
+int qg_tune(const char *name, int value, int *previous);
+
 /* ---- Device-side status -------------------------------------------------- */
 
 /* Every wait inside the kernels is bounded (about one second). A wait that

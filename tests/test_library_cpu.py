@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declarations_are_exported(L):
     names = declared_functions()
-    assert len(names) == 17
+    assert len(names) == 18
     assert sorted(qg.EXPORTED_SYMBOLS) == names
     for n in names:
         assert hasattr(L, n), n
@@ -140,6 +140,20 @@ def test_other_entry_points_validate(L):
     assert L.qgemv_kernel_info(qg.Q4_K, 16, 250, 1, 1) == b""
     assert L.qgemv_kernel_info(qg.Q4_K, 16, 256, 9, 1) == b""
     assert L.qgemv_kernel_info(qg.Q4_K, 16, 256, 1, 0) == b""
+
+
+def test_tune_knobs(L):
+    """qg_tune sets a knob for the process, returns the old value, clamps to
+    the knob's range and rejects unknown names (no CUDA call involved)."""
+    prev = ctypes.c_int32(-1)
+    assert L.qg_tune(None, 1, None) == ERR_NULL
+    assert L.qg_tune(b"QG_NO_SUCH_KNOB", 1, None) == ERR_TYPE
+    assert L.qg_tune(b"QG_TC", 1, ctypes.byref(prev)) == OK
+    old = prev.value
+    assert old in (0, 1)
+    assert L.qg_tune(b"QG_TC", 7, ctypes.byref(prev)) == OK and prev.value == 1
+    assert L.qg_tune(b"QG_TC", old, ctypes.byref(prev)) == OK and prev.value == 1  # clamped to 1
+    assert qg.tune("QG_MMA_MIN_NVEC", 3) in range(1, 10)
 
 
 def test_batched_validation(L):
