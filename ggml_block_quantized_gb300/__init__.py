@@ -36,6 +36,7 @@ EXPORTED_SYMBOLS = (
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes", "qgemv",
     "qgemv_xq", "qgemv_block_isums", "qg_device_error", "qgemv_noalloc",
     "qgemv_batched_workspace_bytes", "qgemv_batched", "qgemv_kernel_info", "qg_tune",
+    "qgemm_workspace_bytes", "qgemm", "qgemm_f16",
 )
 MAX_BATCH = 256
 
@@ -93,6 +94,9 @@ def lib():
         L.qgemv_kernel_info.argtypes = [i32, i64, i64, i64, i32]
         L.qgemv_kernel_info.restype = ctypes.c_char_p
         L.qg_tune.argtypes, L.qg_tune.restype = [ctypes.c_char_p, i32, ctypes.POINTER(i32)], i32
+        L.qgemm_workspace_bytes.argtypes, L.qgemm_workspace_bytes.restype = [i32, i64, i64, i64], sz
+        L.qgemm.argtypes, L.qgemm.restype = [i32, vp, vp, vp, i64, i64, i64, vp, sz, vp], i32
+        L.qgemm_f16.argtypes, L.qgemm_f16.restype = [vp, vp, vp, i64, i64, i64, vp], i32
         _lib = L
     return _lib
 
@@ -311,6 +315,48 @@ def qgemv_batched(t: int, mats, n_in: int, n_vec: int = 1, workspace=None, strea
     """y_i = W_i . x_i for independent matrices [(W, x, y, n_out), ...] of one
     type, row length and vector count, in one launch."""
     BatchPlan(t, mats, n_in, n_vec, workspace).run(stream)
+
+
+def qgemm_workspace_bytes(t: int, n_out: int, n_in: int, n_tok: int) -> int:
+    return lib().qgemm_workspace_bytes(t, n_out, n_in, n_tok)
+
+
+def qgemm(t: int, W, x, n_out: int, n_in: int, n_tok: int, y=None, workspace=None, stream=None):
+    """Prefill product y[n_tok, n_out] = x . W^T for W in blocks of type t and
+    f32 x [n_tok, n_in]: W dequantized and x rounded to f16, one tensor-core
+    GEMM with f32 accumulation."""
+    torch = _torch()
+    _dev_tensor(W, torch.uint8, "W")
+    _dev_tensor(x, torch.float32, "x")
+    _need(x, 4 * n_tok * n_in, "x")
+    if y is None:
+        y = torch.empty((n_tok, n_out), dtype=torch.float32, device=x.device)
+    _dev_tensor(y, torch.float32, "y")
+    _need(y, 4 * n_tok * n_out, "y")
+    need = qgemm_workspace_bytes(t, n_out, n_in, n_tok)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _dev_tensor(workspace, torch.uint8, "workspace")
+    _check(lib().qgemm(t, _ptr(W), _ptr(x), _ptr(y), n_out, n_in, n_tok, _ptr(workspace), workspace.numel(),
+                       _stream(stream)), "qgemm")
+    return y
+
+
+def qgemm_f16(A, B, n_out: int, n_tok: int, K: int, y=None, stream=None):
+    """Dense GEMM y[n_tok, n_out] = B . A^T for f16 A [n_out, K] and B
+    [n_tok, K] (torch.float16 tensors, or uint8 views of f16 bytes), f32 out."""
+    torch = _torch()
+    for name, t_ in (("A", A), ("B", B)):
+        if t_.dtype not in (torch.float16, torch.uint8) or not t_.is_cuda or not t_.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA float16 (or uint8) tensor")
+    _need(A, 2 * n_out * K, "A")
+    _need(B, 2 * n_tok * K, "B")
+    if y is None:
+        y = torch.empty((n_tok, n_out), dtype=torch.float32, device=A.device)
+    _dev_tensor(y, torch.float32, "y")
+    _need(y, 4 * n_tok * n_out, "y")
+    _check(lib().qgemm_f16(_ptr(A), _ptr(B), _ptr(y), n_out, n_tok, K, _stream(stream)), "qgemm_f16")
+    return y
 
 
 def kernel_info(t: int, total_rows: int, n_in: int, n_vec: int = 1, n_mats: int = 1) -> str:

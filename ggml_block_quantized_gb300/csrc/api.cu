@@ -16,17 +16,15 @@ cudaError_t launch_quantize_kernel(int type, int grid, int block, cudaStream_t s
                                    int64_t n_blocks);
 cudaError_t launch_quantize_batched_kernel(int type, int grid, int block, cudaStream_t s, const QuantTable &t,
                                            uint8_t *out, int n_mats, int64_t blocks_per_mat);
-__global__ void dequant_q8_0_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q4_0_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q4_1_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q5_0_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q8_1_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q4_k_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q6_k_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q2_k_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q3_k_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q5_k_kernel(const uint8_t *, float *, int64_t);
-__global__ void dequant_q8_k_kernel(const uint8_t *, float *, int64_t);
+// dequant.cu: every element of `groups` 8-element groups of the block stream
+// w to O (f32 for dequantize_rows, f16 for the prefill GEMM's operand).
+template <class O>
+cudaError_t launch_dequant(int type, const uint8_t *w, O *out, int64_t groups, unsigned grid, int threads,
+                           cudaStream_t s);
+// gemm_tc.cu: f32 -> f16 and the tcgen05 f16 GEMM of the prefill product.
+cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, cudaStream_t s);
+cudaError_t launch_gemm_f16_tc(const __half *A, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
+                               int32_t *err, int sms, int device, cudaStream_t s);
 cudaError_t launch_gemv_tc_q4_k(const TcParams &p, const TcMat *mats, int n, int grid, int smem, int smem_optin,
                                 int device, cudaStream_t s);
 
@@ -765,22 +763,8 @@ int dequantize_rows(int type, const void *W, float *out, int64_t n_rows, int64_t
     const uint8_t *w = static_cast<const uint8_t *>(W);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const unsigned g = static_cast<unsigned>(grid);
-    switch (type) {
-    case QG_Q8_0: dequant_q8_0_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q4_0: dequant_q4_0_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q4_1: dequant_q4_1_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q5_0: dequant_q5_0_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q8_1: dequant_q8_1_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q4_K: dequant_q4_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q6_K: dequant_q6_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q2_K: dequant_q2_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q3_K: dequant_q3_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q5_K: dequant_q5_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    case QG_Q8_K: dequant_q8_k_kernel<<<g, threads, 0, s>>>(w, out, groups); break;
-    default: return QG_ERR_TYPE;
-    }
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? QG_OK : cuda_fail(e);
+    cudaError_t e = launch_dequant(type, w, out, groups, g, threads, s);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, "dequantize launch");
 }
 
 size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec) {
@@ -913,6 +897,75 @@ int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, i
     }
     return run_gemv_mats(type, gm, n_mats, n_in, n_vec, fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, false,
                          dev, s);
+}
+
+size_t qgemm_workspace_bytes(int type, int64_t n_out, int64_t n_in, int64_t n_tok) {
+    if (check_weight_type(type) != QG_OK) return 0;
+    int elems, bytes;
+    block_info(type, &elems, &bytes);
+    if (n_out < 0 || n_in < 0 || n_tok < 0 || n_out > INT32_MAX || n_tok > INT32_MAX || n_in % elems != 0) return 0;
+    const size_t a = (static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255);
+    const size_t b = (static_cast<size_t>(2 * n_tok * n_in) + 255) & ~size_t(255);
+    return a + b > 0 ? a + b : 16;
+}
+
+int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in, int64_t n_tok,
+          void *workspace, size_t workspace_bytes, qg_stream_t stream) {
+    int st = check_weight_type(type);
+    if (st != QG_OK) return st;
+    int elems, bytes;
+    block_info(type, &elems, &bytes);
+    if (n_out < 0 || n_in < 0 || n_tok < 0 || n_out > INT32_MAX || n_tok > INT32_MAX || n_in % elems != 0 ||
+        n_in > INT32_MAX)
+        return QG_ERR_SHAPE;
+    if (n_out == 0 || n_tok == 0) return QG_OK;
+    if (!y) return QG_ERR_NULL;
+    if (!aligned16(y)) return QG_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n_in == 0) {  // the empty sum
+        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(n_out * n_tok) * sizeof(float), s);
+        return e == cudaSuccess ? QG_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (!W || !x || !workspace) return QG_ERR_NULL;
+    if (!aligned16(W) || !aligned16(x) || !aligned16(workspace)) return QG_ERR_ALIGN;
+    if (workspace_bytes < qgemm_workspace_bytes(type, n_out, n_in, n_tok)) return QG_ERR_WORKSPACE;
+    DeviceInfo dev;
+    st = current_device(&dev);
+    if (st != QG_OK) return st;
+    __half *A = static_cast<__half *>(workspace);
+    __half *B = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) +
+                                           ((static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255)));
+    const int64_t groups = n_out * n_in / 8;
+    int64_t grid = (groups + 255) / 256;
+    if (grid > static_cast<int64_t>(dev.sms) * 16) grid = static_cast<int64_t>(dev.sms) * 16;
+    cudaError_t e = launch_dequant(type, static_cast<const uint8_t *>(W), A, groups, static_cast<unsigned>(grid), 256, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill: dequantize to f16");
+    e = launch_f32_to_f16(x, B, n_tok * n_in, dev.sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill: x to f16");
+    e = launch_gemm_f16_tc(A, B, y, n_out, n_tok, n_in, dev.err, dev.sms, dev.device, s);
+    if (e != cudaSuccess) return cuda_fail(e, g_launch_step);
+    return QG_OK;
+}
+
+int qgemm_f16(const void *A, const void *B, float *y, int64_t n_out, int64_t n_tok, int64_t K, qg_stream_t stream) {
+    if (n_out < 0 || n_tok < 0 || K < 0 || n_out > INT32_MAX || n_tok > INT32_MAX || K > INT32_MAX || K % 8 != 0)
+        return QG_ERR_SHAPE;
+    if (n_out == 0 || n_tok == 0) return QG_OK;
+    if (!y) return QG_ERR_NULL;
+    if (!aligned16(y)) return QG_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, static_cast<size_t>(n_out * n_tok) * sizeof(float), s);
+        return e == cudaSuccess ? QG_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (!A || !B) return QG_ERR_NULL;
+    if (!aligned16(A) || !aligned16(B)) return QG_ERR_ALIGN;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st != QG_OK) return st;
+    cudaError_t e = launch_gemm_f16_tc(static_cast<const __half *>(A), static_cast<const __half *>(B), y, n_out, n_tok, K,
+                                       dev.err, dev.sms, dev.device, s);
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, g_launch_step);
 }
 
 const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_t n_vec, int n_mats) {

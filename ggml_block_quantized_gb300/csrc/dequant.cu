@@ -19,12 +19,28 @@ __device__ __forceinline__ void store8(float *dst, const float (&v)[8]) {
     __stcs(d4 + 1, make_float4(v[4], v[5], v[6], v[7]));
 }
 
+// The same 8 values rounded to f16 (round to nearest even), one 16-byte
+// store: the operand form of the prefill GEMM.
+__device__ __forceinline__ void store8(__half *dst, const float (&v)[8]) {
+    uint4 o;
+    o.x = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[0]))) |
+          (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[1]))) << 16);
+    o.y = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[2]))) |
+          (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[3]))) << 16);
+    o.z = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[4]))) |
+          (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[5]))) << 16);
+    o.w = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[6]))) |
+          (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(v[7]))) << 16);
+    __stcs(reinterpret_cast<uint4 *>(dst), o);
+}
+
 __device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p) {
     return static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t *>(p)));
 }
 
 // groups: total 8-element groups = n_rows * n_in / 8; W is the flat block stream.
-__global__ void dequant_q8_0_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q8_0_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 2) * 34;
@@ -37,7 +53,8 @@ __global__ void dequant_q8_0_kernel(const uint8_t *__restrict__ W, float *__rest
     }
 }
 
-__global__ void dequant_q4_0_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q4_0_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 2) * 18;
@@ -56,7 +73,8 @@ __global__ void dequant_q4_0_kernel(const uint8_t *__restrict__ W, float *__rest
 }
 
 // Q4_1: code * d is exact (4 + 11 bits), so code * d + m rounds once.
-__global__ void dequant_q4_1_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q4_1_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 2) * 20;
@@ -76,7 +94,8 @@ __global__ void dequant_q4_1_kernel(const uint8_t *__restrict__ W, float *__rest
 }
 
 // Q5_0: 5-bit code = nibble | bit e of qh << 4, value (code - 16) * d.
-__global__ void dequant_q5_0_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q5_0_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 2) * 22;
@@ -97,7 +116,8 @@ __global__ void dequant_q5_0_kernel(const uint8_t *__restrict__ W, float *__rest
 }
 
 // Q8_1: q * d (s is not part of the values).
-__global__ void dequant_q8_1_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q8_1_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 2) * 36;
@@ -110,7 +130,8 @@ __global__ void dequant_q8_1_kernel(const uint8_t *__restrict__ W, float *__rest
     }
 }
 
-__global__ void dequant_q4_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q4_k_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 5) * 144;
@@ -142,7 +163,8 @@ __global__ void dequant_q4_k_kernel(const uint8_t *__restrict__ W, float *__rest
     }
 }
 
-__global__ void dequant_q6_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q6_k_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 5) * 210;
@@ -166,7 +188,8 @@ __global__ void dequant_q6_k_kernel(const uint8_t *__restrict__ W, float *__rest
 
 // Q5_K: Q4_K's scales, mins and nibbles plus bit j of qh[e % 32] as bit 4
 // of the code (sub-block j = e / 32).
-__global__ void dequant_q5_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q5_k_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 5) * 176;
@@ -200,7 +223,8 @@ __global__ void dequant_q5_k_kernel(const uint8_t *__restrict__ W, float *__rest
 
 // Q2_K: element e = 128n + 32j + 16h + l takes bits 2j of qs[32n + 16h + l];
 // sub-block e / 16 has scale scales[e/16] & 15 and min scales[e/16] >> 4.
-__global__ void dequant_q2_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q2_k_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 5) * 84;
@@ -225,7 +249,8 @@ __global__ void dequant_q2_k_kernel(const uint8_t *__restrict__ W, float *__rest
 // Q3_K: the Q2_K 2-bit value less 4 when bit 4n + j of hmask[16h + l] is
 // clear; scale = 6-bit field - 32 (low 4 bits in nibble (e/16) / 8 of byte
 // (e/16) % 8, high 2 bits at bits 2((e/16) / 4) of byte 8 + (e/16) % 4).
-__global__ void dequant_q3_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q3_k_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 5) * 110;
@@ -249,7 +274,8 @@ __global__ void dequant_q3_k_kernel(const uint8_t *__restrict__ W, float *__rest
     }
 }
 
-__global__ void dequant_q8_k_kernel(const uint8_t *__restrict__ W, float *__restrict__ out, int64_t groups) {
+template <class O>
+__global__ void dequant_q8_k_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const uint8_t *blk = W + (g >> 5) * 292;
@@ -261,5 +287,30 @@ __global__ void dequant_q8_k_kernel(const uint8_t *__restrict__ W, float *__rest
         store8(out + g * 8, v);
     }
 }
+
+
+// One dequantization launch over `groups` 8-element groups (kernel
+// templates are launched from the translation unit that defines them).
+template <class O>
+cudaError_t launch_dequant(int type, const uint8_t *w, O *out, int64_t groups, unsigned g, int threads,
+                           cudaStream_t s) {
+    switch (type) {
+    case QG_Q8_0: dequant_q8_0_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q4_0: dequant_q4_0_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q4_1: dequant_q4_1_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q5_0: dequant_q5_0_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q8_1: dequant_q8_1_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q4_K: dequant_q4_k_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q6_K: dequant_q6_k_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q2_K: dequant_q2_k_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q3_K: dequant_q3_k_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q5_K: dequant_q5_k_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    case QG_Q8_K: dequant_q8_k_kernel<O><<<g, threads, 0, s>>>(w, out, groups); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+template cudaError_t launch_dequant<float>(int, const uint8_t *, float *, int64_t, unsigned, int, cudaStream_t);
+template cudaError_t launch_dequant<__half>(int, const uint8_t *, __half *, int64_t, unsigned, int, cudaStream_t);
 
 }  // namespace qg

@@ -64,7 +64,7 @@
 // leaves the converters waiting for the mmas of the group before last.
 #pragma once
 
-#include "qg_common.cuh"
+#include "tc_common.cuh"
 
 namespace qg {
 
@@ -130,37 +130,6 @@ struct TcParams {
     int n_stages;  // ring depth (2..kTcMaxStages)
 };
 
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ void tc_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Generic-proxy shared-memory writes made visible to the tensor cores.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// 32 lanes x 32 columns from this warp's 32 registers each.
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
 // Eight mmas over consecutive k-steps s = 0..7 into one accumulator: A at
 // a_t + 8 s columns, B at descriptor b0 (steps 0..3) or b4 (steps 4..7),
 // advanced by 32 bytes a step within a 128-byte swizzle row; the first step
@@ -212,58 +181,8 @@ __device__ __forceinline__ void tc_ld16x2_wait(uint32_t ta, uint32_t tb, uint32_
         : "memory");
 }
 
-// The mbarrier completes (one arrival) when every earlier tcgen05 operation
-// of this thread has.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t r;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-    return r;
-}
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-// Instruction descriptor of kind::f16: f32 D, f16 A and B, both K-major,
-// N = 64, M = 128.
-constexpr uint32_t kTcIdesc = (1u << 4) | (static_cast<uint32_t>(kTcN >> 3) << 17) |
-                              (static_cast<uint32_t>(kTcM >> 4) << 24);
-
-// Shared-memory descriptor of a 128-byte-swizzled K-major operand: start
-// address, the byte offset between groups of 8 rows (one atom here),
-// version 1, swizzle mode 2 (128 bytes).
-__device__ __forceinline__ uint64_t tc_smem_desc(uint32_t start, uint32_t group_stride) {
-    return static_cast<uint64_t>((start >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
-           (static_cast<uint64_t>((group_stride >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
-           (static_cast<uint64_t>(2) << 61);
-}
-
-// Bounded wait that also gives up once another thread of the CTA has set
-// the abort flag. It polls without a suspend hint: a thread suspended on an
-// mbarrier that tcgen05.commit completes was measured to wake up a thousand
-// cycles or more after the phase completed, which stalls the mma pipeline.
-__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const volatile int *abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1; i < kWaitLimitPolls; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-        }
-    }
-    return false;
-}
+// Instruction descriptor: N = 64, M = 128.
+constexpr uint32_t kTcIdesc = tc_idesc_f16(kTcM, kTcN);
 
 // Walks a CTA's tiles. Every role runs the same walk.
 struct TcWalk {

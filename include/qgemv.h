@@ -281,6 +281,43 @@ size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int 
 int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, int64_t n_vec, void *workspace,
                   size_t workspace_bytes, qg_stream_t stream);
 
+/* ---- Prefill: many tokens ------------------------------------------------ */
+
+/* Workspace bytes qgemm needs: the f16 copy of W (2 * n_out * n_in) and of x
+ * (2 * n_tok * n_in), each rounded up to 256 bytes. 0 on a bad argument. */
+size_t qgemm_workspace_bytes(int type, int64_t n_out, int64_t n_in, int64_t n_tok);
+
+/* The product for many tokens at once (prefill): y[t][o] = sum_i
+ * W[o][i] * x[t][i] for t < n_tok, with W of any weight type above
+ * ([sipllm] The fused matmul: matmul_quant dequantizes a row to f32 and dots
+ * it with f32 x; here the whole product is one dense GEMM). Steps, all on
+ * `stream`: dequantize W to f16 (round to nearest even) into the workspace,
+ * round x to f16 into the workspace, then a tcgen05 tensor-core GEMM with
+ * f32 accumulation. The result differs from the f32 product by the f16
+ * rounding of each weight and activation (at most 2^-11 relative each) and
+ * the f32 accumulation: |y - y_exact| <= (2^-10 + n_in 2^-24) sum_i
+ * |W[o][i] x[t][i]| (values beyond f16's range, 65504, become inf).
+ * Unlike qgemv, x is not quantized to Q8 blocks.
+ * W: blocks [n_out][n_in] (device, 16-byte aligned); x: f32 [n_tok][n_in];
+ * y: f32 [n_tok][n_out]; workspace: qgemm_workspace_bytes, 16-byte aligned.
+ * n_in must be a multiple of the block size; 0 <= n_out, n_tok < 2^31.
+ * n_in == 0 writes zeros. Returns QG_OK or an error before anything is
+ * enqueued (QG_ERR_TYPE, QG_ERR_PAIR, QG_ERR_SHAPE, QG_ERR_NULL,
+ * QG_ERR_ALIGN, QG_ERR_WORKSPACE), or QG_ERR_CUDA if a launch fails. */
+int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in, int64_t n_tok,
+          void *workspace, size_t workspace_bytes, qg_stream_t stream);
+
+/* The dense GEMM step of qgemm on its own, for callers that keep f16
+ * operands (for instance weights dequantized once and reused across prefill
+ * calls): y[t][o] = sum_k A[o][k] * B[t][k] with A f16 [n_out][K] and B f16
+ * [n_tok][K] (row-major, device, 16-byte aligned; K a multiple of 8, 0 <= K,
+ * n_out, n_tok < 2^31), y f32 [n_tok][n_out], f32 accumulation on the
+ * tcgen05 tensor cores. qgemm's workspace holds its A (offset 0) and B
+ * (offset 2 * n_out * K rounded up to 256 bytes) in this form. K == 0
+ * writes zeros. Returns QG_OK, QG_ERR_SHAPE, QG_ERR_NULL, QG_ERR_ALIGN or
+ * QG_ERR_CUDA. */
+int qgemm_f16(const void *A, const void *B, float *y, int64_t n_out, int64_t n_tok, int64_t K, qg_stream_t stream);
+
 /* ---- Introspection --------------------------------------------------------- */
 
 /* Which kernel and launch plan a product over n_mats matrices with

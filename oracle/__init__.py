@@ -168,5 +168,15 @@ def gemv_dequant(wtype: int, W: np.ndarray, xq: np.ndarray, n_out: int, n_in: in
     return out
 
 
+def gemm_float(wtype: int, W: np.ndarray, x: np.ndarray, n_out: int, n_in: int, n_tok: int) -> np.ndarray:
+    """The float product of [sipllm] "The fused matmul" (matmul_quant):
+    each row of W dequantized to f32 (the exact values of dequantize), dotted
+    with the f32 activations, here in f64 (numpy's matmul as the dot).
+    x is f32 [n_tok, n_in] (not quantized); returns y [n_tok, n_out]."""
+    w = dequantize(wtype, W, n_out * n_in).reshape(n_out, n_in).astype(np.float64)
+    xs = np.asarray(x, dtype=np.float32).reshape(n_tok, n_in).astype(np.float64)
+    return xs @ w.T
+
+
 def host_is_little_endian() -> bool:
     return bool(lib().or_host_is_little_endian())

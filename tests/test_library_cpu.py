@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declarations_are_exported(L):
     names = declared_functions()
-    assert len(names) == 18
+    assert len(names) == 21
     assert sorted(qg.EXPORTED_SYMBOLS) == names
     for n in names:
         assert hasattr(L, n), n
@@ -114,6 +114,36 @@ def test_qgemv_validation(L):
     assert g(qg.Q4_K, A, A2, A3, 16, 256, 1, MIS, ws, NUL) == ERR_ALIGN
     # empty output: nothing to do, nothing enqueued
     assert g(qg.Q4_K, A, A2, A3, 0, 256, 1, A, ws, NUL) == OK
+
+
+def test_prefill_validation(L):
+    """qgemm / qgemm_f16 reject bad arguments before any CUDA call."""
+    need = L.qgemm_workspace_bytes(qg.Q4_K, 64, 512, 10)
+    assert need == (2 * 64 * 512 + 255) // 256 * 256 + (2 * 10 * 512 + 255) // 256 * 256
+    assert L.qgemm_workspace_bytes(qg.Q4_K, 64, 500, 10) == 0
+    assert L.qgemm_workspace_bytes(99, 64, 512, 10) == 0
+    ws = ctypes.c_size_t(need)
+    g = lambda *a: L.qgemm(*a)
+    assert g(99, A, A2, A3, 64, 512, 10, A, ws, NUL) == ERR_TYPE
+    assert g(qg.Q8_K, A, A2, A3, 64, 512, 10, A, ws, NUL) == ERR_PAIR
+    assert g(qg.Q4_K, A, A2, A3, 64, 500, 10, A, ws, NUL) == ERR_SHAPE
+    assert g(qg.Q4_K, A, A2, A3, -1, 512, 10, A, ws, NUL) == ERR_SHAPE
+    assert g(qg.Q4_K, A, A2, A3, 64, 512, -1, A, ws, NUL) == ERR_SHAPE
+    assert g(qg.Q4_K, NUL, A2, A3, 64, 512, 10, A, ws, NUL) == ERR_NULL
+    assert g(qg.Q4_K, A, A2, NUL, 64, 512, 10, A, ws, NUL) == ERR_NULL
+    assert g(qg.Q4_K, A, A2, A3, 64, 512, 10, NUL, ws, NUL) == ERR_NULL
+    assert g(qg.Q4_K, MIS, A2, A3, 64, 512, 10, A, ws, NUL) == ERR_ALIGN
+    assert g(qg.Q4_K, A, A2, MIS, 64, 512, 10, A, ws, NUL) == ERR_ALIGN
+    assert g(qg.Q4_K, A, A2, A3, 64, 512, 10, A, ctypes.c_size_t(need - 1), NUL) == ERR_WS
+    assert g(qg.Q4_K, A, A2, A3, 0, 512, 10, A, ws, NUL) == OK  # nothing to do
+    assert g(qg.Q4_K, A, A2, A3, 64, 512, 0, A, ws, NUL) == OK
+    f = lambda *a: L.qgemm_f16(*a)
+    assert f(A, A2, A3, 64, 10, 500, NUL) == ERR_SHAPE  # K not a multiple of 8
+    assert f(A, A2, A3, -1, 10, 512, NUL) == ERR_SHAPE
+    assert f(NUL, A2, A3, 64, 10, 512, NUL) == ERR_NULL
+    assert f(A, A2, NUL, 64, 10, 512, NUL) == ERR_NULL
+    assert f(A, MIS, A3, 64, 10, 512, NUL) == ERR_ALIGN
+    assert f(A, A2, A3, 0, 10, 512, NUL) == OK
 
 
 def test_other_entry_points_validate(L):
