@@ -89,6 +89,23 @@ def test_gemm_several_tiles_per_cta(t):
     assert qg.device_error() == 0
 
 
+def test_gemm_wide_token_tiles():
+    """Enough tokens that 256-token tiles still give every SM a tile (the
+    wide-tile kernel: N = 256 mmas, 512 tensor-memory columns), with a
+    ragged last token tile."""
+    rng = np.random.default_rng(7600)
+    t, n_out, n_in, n_tok = qg.Q4_K, 4096, 2048, 1300
+    W = weights(t, n_out, n_in, rng)
+    x = synth.f32_normal(rng, n_tok * n_in)
+    y = host(qg.qgemm(t, dev(W), dev(x), n_out, n_in, n_tok))
+    rows = np.unique(np.concatenate([rng.integers(0, n_out, 40), [0, n_out - 1]]))
+    toks = np.unique(np.concatenate([rng.integers(0, n_tok, 12), [0, 255, 256, 1279, 1280, n_tok - 1]]))
+    Wr = W.reshape(n_out, -1)[rows].reshape(-1)
+    xs = x.reshape(n_tok, n_in)[toks].reshape(-1)
+    check(t, Wr, xs, y[np.ix_(toks, rows)], len(rows), n_in, len(toks))
+    assert qg.device_error() == 0
+
+
 def test_gemm_is_deterministic_and_edges():
     rng = np.random.default_rng(7500)
     t, n_out, n_in, n_tok = qg.Q4_K, 300, 1024, 200
