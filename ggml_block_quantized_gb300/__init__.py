@@ -36,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes", "qgemv",
     "qgemv_xq", "qgemv_block_isums", "qg_device_error", "qgemv_noalloc",
     "qgemv_batched_workspace_bytes", "qgemv_batched", "qgemv_kernel_info", "qg_tune",
-    "qgemm_workspace_bytes", "qgemm", "qgemm_f16",
+    "qgemm_workspace_bytes", "qgemm", "qgemm_f16", "qg_selftest_bounded_wait",
 )
 MAX_BATCH = 256
 
@@ -97,6 +97,7 @@ def lib():
         L.qgemm_workspace_bytes.argtypes, L.qgemm_workspace_bytes.restype = [i32, i64, i64, i64], sz
         L.qgemm.argtypes, L.qgemm.restype = [i32, vp, vp, vp, i64, i64, i64, vp, sz, vp], i32
         L.qgemm_f16.argtypes, L.qgemm_f16.restype = [vp, vp, vp, i64, i64, i64, vp], i32
+        L.qg_selftest_bounded_wait.argtypes, L.qg_selftest_bounded_wait.restype = [vp], i32
         _lib = L
     return _lib
 
@@ -370,6 +371,12 @@ def tune(name: str, value: int) -> int:
     prev = ctypes.c_int32(0)
     _check(lib().qg_tune(name.encode(), int(value), ctypes.byref(prev)), "qg_tune")
     return prev.value
+
+
+def selftest_bounded_wait(stream=None):
+    """Enqueue the bounded-wait self-test kernel (a wait that runs out after
+    about one second); read its code with device_error()."""
+    _check(lib().qg_selftest_bounded_wait(_stream(stream)), "qg_selftest_bounded_wait")
 
 
 def device_error() -> int:

@@ -30,6 +30,18 @@ cudaError_t launch_gemv_tc_q4_k(const TcParams &p, const TcMat *mats, int n, int
 
 __device__ int32_t g_device_error = 0;
 
+// One thread waits, with the product kernels' bounded wait, on an mbarrier
+// that nothing arrives on; the wait gives up after about one second and the
+// kernel records the consumer-wait code and returns.
+__global__ void selftest_wait_kernel(int32_t *err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!mbar_wait_bounded(b, 0u)) record_error(err, kErrConsumerWait);
+}
+
 namespace {
 
 thread_local char g_last_cuda_error[256] = "";
@@ -1027,6 +1039,15 @@ int qg_device_error(int32_t *code) {
     if (e != cudaSuccess) return cuda_fail(e);
     *code = v;
     return QG_OK;
+}
+
+int qg_selftest_bounded_wait(qg_stream_t stream) {
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st != QG_OK) return st;
+    selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev.err);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, "self-test launch");
 }
 
 }  // extern "C"

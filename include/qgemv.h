@@ -349,6 +349,15 @@ int qg_tune(const char *name, int value, int *previous);
  * *code (host pointer), clears it and returns QG_OK (or QG_ERR_CUDA). */
 int qg_device_error(int32_t *code);
 
+/* Self-test of that mechanism (the pages have no counterpart): enqueues on
+ * `stream` one single-thread kernel that waits, with the same bounded wait
+ * the product kernels use, on an mbarrier that nothing completes. After
+ * about one second the wait gives up, the kernel records the code a
+ * consumer wait records (2) and returns; no fault, no trap, and the context
+ * stays usable. Read the code with qg_device_error. Returns QG_OK or
+ * QG_ERR_CUDA. */
+int qg_selftest_bounded_wait(qg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declarations_are_exported(L):
     names = declared_functions()
-    assert len(names) == 21
+    assert len(names) == 22
     assert sorted(qg.EXPORTED_SYMBOLS) == names
     for n in names:
         assert hasattr(L, n), n
