@@ -132,6 +132,9 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 //    bound on blocks per chunk, 0 none);
 //  QG_FUSED_QUANT_KIB: f32 activations up to this size are quantized inside
 //    the GEMV's prologue;
+//  QG_FUSED_MAX_MIB: ... for a single matrix of at most this many MiB of
+//    blocks (larger ones take the separate quantization launch; the default
+//    sets no limit: in-kernel quantization measured faster at every size);
 //  QG_TC: the tcgen05 Q4_K kernel for three or more vectors -- 0 never (the
 //    default: the mma.sync kernel measured faster on this GPU), 1 whenever its
 //    shared memory fits (rows of 8 or 16 blocks).
@@ -143,6 +146,7 @@ enum KnobId {
     kKnobMmaKb,
     kKnobFusedQuantKib,
     kKnobTc,
+    kKnobFusedMaxMib,
     kKnobCount
 };
 struct KnobDef {
@@ -152,7 +156,7 @@ struct KnobDef {
 constexpr KnobDef kKnobs[kKnobCount] = {
     {"QG_CTAS_PER_SM", 2, 1, 4},          {"QG_RING_KIB", 96, 16, 200}, {"QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1},
     {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 48, 0, 1024},
-    {"QG_TC", 0, 0, 1}};
+    {"QG_TC", 0, 0, 1},                   {"QG_FUSED_MAX_MIB", 1 << 20, 0, 1 << 20}};
 std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
 
 int knob(KnobId k) {
@@ -199,13 +203,6 @@ size_t round16(size_t v) { return (v + 15) & ~size_t(15); }
 
 constexpr int kSmemTailPad = 16;  // unaligned word reads may touch up to 4 bytes past a stage
 
-// Lanes of one activation block's f32 values (bytes) and lanes per weight
-// block, per type.
-int act_block_f32_bytes(int type) {
-    int elems = 0, bytes = 0;
-    block_info(type, &elems, &bytes);
-    return 4 * elems;
-}
 // The item variants a type offers (lanes per weight block); Q6_K has a
 // two-lane item (fewer instructions per code) and a four-lane one (its
 // 8-block iterations fill better for some row lengths).
@@ -220,25 +217,21 @@ int item_lpbs(int type, int (&out)[2]) {
     }
 }
 
-// Stage geometry and grid of one GEMV launch. x_bytes is the f32 x of the
-// launch's vectors for in-kernel quantization (0 otherwise); it is staged
-// whole when that fits, else in chunks of whole activation blocks. Among the
-// configurations whose shared memory lets the tuned number of CTAs share an
-// SM (more resident warps hide more latency), the plan keeps the lanes of
-// each warp's item loop fullest, then prefers x staged whole (one round trip
-// per matrix), then the larger ring. Returns QG_ERR_SHAPE when the
-// activations do not fit next to two stages even with one CTA per SM.
-int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int smem_limit, size_t x_bytes,
-              GemvParams *p, GemvLaunch *l) {
+// Stage geometry and grid of one GEMV launch. Among the configurations whose
+// shared memory lets the tuned number of CTAs share an SM (more resident
+// warps hide more latency), the plan keeps the lanes of each warp's item
+// loop fullest, then the larger ring. (In-kernel quantization of f32 x needs
+// no shared memory of its own: each warp loads the blocks it quantizes.)
+// Returns QG_ERR_SHAPE when the activations do not fit next to two stages
+// even with one CTA per SM.
+int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int smem_limit, GemvParams *p,
+              GemvLaunch *l) {
     int elems, bytes;
     block_info(type, &elems, &bytes);
     const int64_t nb = n_in / elems;
     const int64_t row_bytes = nb * bytes;
     const size_t ring_target = static_cast<size_t>(tune_ring_kib()) * 1024;
     const size_t sm_smem = 228 * 1024, cta_reserve = 1024;  // per-SM shared memory, per-CTA driver share
-    const size_t blk_f32 = static_cast<size_t>(act_block_f32_bytes(type));
-    size_t xb_opts[4] = {round16(x_bytes), 16384, 8192, 4096};
-    const int n_xb = x_bytes ? 4 : 1;
     int lpbs[2] = {1, 1};
     const int n_lpb = item_lpbs(type, lpbs);
     for (int per_sm = tune_ctas_per_sm(); per_sm >= 1; --per_sm) {
@@ -252,14 +245,8 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
         for (int li = 0; li < n_lpb; ++li) {
         const int lpb = lpbs[li];
         const size_t act = round16(act_smem_bytes(type, lpb, static_cast<int>(nb), nv));
-        for (int xi = 0; xi < n_xb; ++xi) {
-            size_t xb = xb_opts[xi];
-            if (x_bytes) {
-                if (xb > round16(x_bytes)) continue;
-                xb = xb / blk_f32 * blk_f32;  // whole activation blocks
-                if (xb == 0) continue;
-            }
-            const size_t fixed0 = kHeaderBytes + act + xb + kSmemTailPad;
+        {
+            const size_t fixed0 = kHeaderBytes + act + kSmemTailPad;
             for (int split = 1; split <= kConsumerWarps; split *= 2) {
             for (int rpw = kRowsPerWarp; rpw >= 1; --rpw) {  // rows a warp group takes per stage
                 const int R = (kConsumerWarps / split) * rpw;
@@ -281,10 +268,9 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
                 // more work per warp, and no partial sums to add up); then two
                 // rows per warp group over one (the per-stage work is shared by
                 // more blocks); then the item with fewer lanes per block (fewer
-                // instructions per code); then x staged whole; then the larger
-                // ring
+                // instructions per code); then the larger ring
                 const double score = static_cast<int>(eff * 20.0 + 0.5) * 100.0 - split * 10.0 -
-                                     (kRowsPerWarp - rpw) * 3.0 - li * 6.0 + (xi == 0 ? 5.0 : 0.0) +
+                                     (kRowsPerWarp - rpw) * 3.0 - li * 6.0 +
                                      static_cast<double>(S * stage) / (4.0 * 1024 * 1024);
                 if (score > best_score) {
                     best_score = score;
@@ -295,10 +281,10 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
                     bp.nb = static_cast<int>(nb);
                     bp.rows_per_stage = R;
                     bp.split = split;
+                    bp.split_log2 = split == 1 ? 0 : split == 2 ? 1 : split == 4 ? 2 : 3;
                     bp.n_stages = S;
                     bp.stage_bytes = static_cast<int>(stage);
                     bp.act_bytes = static_cast<int>(act);
-                    bp.x_bytes = static_cast<int>(xb);
                     bp.red_bytes = static_cast<int>(red_bytes(S));
                     best_smem = fixed0 + red_bytes(S) + S * stage;
                 }
@@ -536,16 +522,12 @@ int64_t fused_quant_max_bytes() { return static_cast<int64_t>(knob(kKnobFusedQua
 
 bool fused_quantization(int64_t n_in, int64_t n_vec) { return 4 * n_in * n_vec <= fused_quant_max_bytes(); }
 
-// A single product quantizes x inside the GEMV only when its matrix is small
-// enough (<= 32 MiB of blocks) for the prologue that every CTA then runs to
-// matter more than the separate launch; for larger matrices every CTA streams
-// enough rows that the quantization launch, overlapped with the GEMV's weight
-// prefetch, is the cheaper way.
-constexpr int64_t kFusedMaxWeightBytes = 32ll << 20;
-
+// A single product quantizes x inside the GEMV when its matrix is at most
+// QG_FUSED_MAX_MIB of blocks (by default any matrix); above that the separate
+// quantization launch, overlapped with the GEMV's weight prefetch, is taken.
 bool fused_single(int type, int64_t n_out, int64_t n_in, int64_t n_vec) {
     return fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec) &&
-           qtype_nbytes(type, n_in) * n_out <= kFusedMaxWeightBytes;
+           qtype_nbytes(type, n_in) * n_out <= (static_cast<int64_t>(knob(kKnobFusedMaxMib)) << 20);
 }
 
 // The product over `n` matrices of one type, row length and vector count
@@ -617,7 +599,7 @@ int run_gemv_mats(int type, GemvMat *mats, int n, int64_t n_in, int64_t n_vec, s
     }
     GemvParams p = {};
     GemvLaunch l = {};
-    int st = plan_gemv(type, total, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, x_bytes, &p, &l);
+    int st = plan_gemv(type, total, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &p, &l);
     if (st != QG_OK) return st;
     p.err = dev.err;
     p.n_mats = n;
@@ -834,8 +816,7 @@ int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     GemvParams probe = {};
     GemvLaunch pl = {};
     const bool fused = fused_single(type, n_out, n_in, n_vec);
-    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
-                   fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &probe, &pl);
+    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
     if (st != QG_OK) return st;
     if (fused)  // one launch: x quantized in the GEMV's prologue
         return run_gemv(type, W, nullptr, y, nullptr, n_out, n_in, n_vec, dev, s, x);
@@ -885,8 +866,7 @@ int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, i
     if (total == 0) return QG_OK;
     GemvParams probe = {};
     GemvLaunch pl = {};
-    st = plan_gemv(type, total, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
-                   fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &probe, &pl);
+    st = plan_gemv(type, total, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
     if (st != QG_OK) return st;
     GemvMat gm[QG_MAX_BATCH];
     const int at = qtype_act_type(type);
@@ -1018,8 +998,7 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
                                    : fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec);
     GemvParams gp = {};
     GemvLaunch gl = {};
-    if (plan_gemv(type, total_rows, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin,
-                  fused ? static_cast<size_t>(4 * n_in * n_vec) : 0, &gp, &gl) != QG_OK)
+    if (plan_gemv(type, total_rows, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &gp, &gl) != QG_OK)
         return buf;
     std::snprintf(buf, sizeof buf, "gemv_kernel<%s,NV=%d> grid=%d stages=%d split=%d rows_per_stage=%d lanes_per_block=%d smem=%d%s",
                   tn, static_cast<int>(n_vec), gl.grid, gp.n_stages, gp.split, gp.rows_per_stage, gl.lpb, gl.smem,
@@ -1110,7 +1089,7 @@ extern "C" int qgemv_noalloc(int type, const void *W, const float *x, float *y, 
     if (st != QG_OK) return st;
     GemvParams probe = {};
     GemvLaunch pl = {};
-    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, 0, &probe, &pl);
+    st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
     if (st != QG_OK) return st;
     void *scratch = nullptr;
     st = noalloc_scratch(dev.device, &scratch);

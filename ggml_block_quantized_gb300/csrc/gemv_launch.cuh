@@ -59,7 +59,10 @@ inline cudaError_t launch_gemv_inst(const GemvParams &p, const GemvBatch<MAXB> &
     int grid = l.grid;
     const int cap = resident_ctas<T, NV, ISUMS>(k, device, l.smem) * l.sms;
     if (grid > cap) grid = cap;
-    return launch_pdl(k, grid, kGemvThreads, l.smem, s, p, b);
+    GemvParams q = p;  // the CTAs' row ranges for the final grid
+    q.rows_q = p.total_rows / grid;
+    q.rows_r = static_cast<int>(p.total_rows % grid);
+    return launch_pdl(k, grid, kGemvThreads, l.smem, s, q, b);
 }
 
 template <class T, int NV>

@@ -46,7 +46,7 @@ constexpr int kMaxStages = 16;
 constexpr int kRowsPerWarp = 2;  // most rows a warp group takes per stage (its items are flattened over them)
 constexpr int kMaxBatch = 256;   // matrices per batched launch (their table is a kernel parameter)
 // Shared memory: header (kMaxStages full + kMaxStages empty mbarriers) |
-// staged activations | f32 x buffer | cross-warp partial sums (split > 1:
+// staged activations | cross-warp partial sums (split > 1:
 // [2 * n_stages][kConsumerWarps][kRowsPerWarp][NV] floats) | ring of stages.
 constexpr int kHeaderBytes = 2 * 8 * kMaxStages;
 
@@ -72,14 +72,16 @@ struct GemvParams {
     int32_t *err;        // device error word
     int64_t row_bytes;   // bytes of one row (n_in / block elems * block bytes)
     int64_t total_rows;  // sum of n_out over the matrices
+    int64_t rows_q;      // total_rows / gridDim.x and total_rows % gridDim.x: CTA b starts at global
+    int rows_r;          // row b * rows_q + b * rows_r / gridDim.x (no 64-bit division in the kernel)
     int n_mats;
     int nb;              // blocks per row
     int rows_per_stage;  // (kConsumerWarps / split) * (1 or kRowsPerWarp)
     int split;           // consumer warps per row: 1, 2, 4 or 8
+    int split_log2;      // log2(split)
     int n_stages;        // ring depth (2..kMaxStages)
     int stage_bytes;     // bytes per ring slot, multiple of 16
     int act_bytes;       // bytes of staged activations, multiple of 16
-    int x_bytes;         // bytes of the f32 x buffer (whole activation blocks), 0 without x
     int red_bytes;       // bytes of the cross-warp partial sums (split > 1), else 0
 };
 
@@ -94,7 +96,7 @@ struct StageWalk {
     template <int MAXB>
     __device__ __forceinline__ bool next(const GemvBatch<MAXB> &b, int n_mats, int R, int &mat, int &r, int &rows) {
         if (g >= g1) return false;
-        while (g >= next_base) {
+        while (MAXB > 1 && g >= next_base) {  // (one matrix: a constant index, no local copy of the table)
             ++m;
             base = next_base;
             n_out = b.m[m].n_out;
@@ -110,15 +112,21 @@ struct StageWalk {
     }
 };
 
+// CTA b's rows: [floor(b * total / grid), floor((b + 1) * total / grid)),
+// formed as b * q + floor(b * r / grid) with total = q * grid + r.
+__device__ __forceinline__ int64_t cta_row_start(const GemvParams &p, unsigned b) {
+    return static_cast<int64_t>(b) * p.rows_q + (b * static_cast<unsigned>(p.rows_r)) / gridDim.x;
+}
+
 template <int MAXB>
 __device__ __forceinline__ StageWalk cta_rows(const GemvParams &p, const GemvBatch<MAXB> &b) {
     StageWalk w;
-    w.g = static_cast<int64_t>(blockIdx.x) * p.total_rows / gridDim.x;
-    w.g1 = static_cast<int64_t>(blockIdx.x + 1) * p.total_rows / gridDim.x;
+    w.g = cta_row_start(p, blockIdx.x);
+    w.g1 = cta_row_start(p, blockIdx.x + 1);
     w.m = 0;
     w.n_out = b.m[0].n_out;
     w.base = 0;
-    w.next_base = p.n_mats > 1 ? b.m[1].row_base : INT64_MAX;
+    w.next_base = MAXB > 1 && p.n_mats > 1 ? b.m[MAXB > 1 ? 1 : 0].row_base : INT64_MAX;
     return w;
 }
 
@@ -141,7 +149,7 @@ template <int NV>
 __device__ __forceinline__ void finish_split_rows(const GemvParams &p, const float *red, int ri, const StageInfo &st,
                                                   int lane) {
     const int split = p.split;
-    const int gshift = 3 - (split == 1 ? 0 : split == 2 ? 1 : split == 4 ? 2 : 3);  // log2(kConsumerWarps / split)
+    const int gshift = 3 - p.split_log2;  // log2(kConsumerWarps / split)
     for (int o = lane; o < st.rows * NV; o += 32) {
         const int ris = o / NV, v = o % NV;
         const int grp = ris & ((1 << gshift) - 1), i = ris >> gshift;
@@ -189,13 +197,18 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBat
         }
         if (mat != cur) {  // the matrix's fields, read from the parameter table once
             cur = mat;
-            W = b.m[mat].W;
-            y = b.m[mat].y;
-            n_out = b.m[mat].n_out;
+            const GemvMat &mt = b.m[MAXB == 1 ? 0 : mat];
+            W = mt.W;
+            y = mt.y;
+            n_out = mt.n_out;
             lim = (static_cast<int64_t>(n_out) * p.row_bytes) & ~int64_t(15);
         }
-        const StageInfo prev = info[slot];
-        info[slot] = StageInfo{y, n_out, r, rows};
+        // the stage info is kept (in local memory) only when split rows need it
+        StageInfo prev = {};
+        if (reduce) {
+            prev = info[slot];
+            info[slot] = StageInfo{y, n_out, r, rows};
+        }
         if (lane == 0) {
             const int64_t start = static_cast<int64_t>(r) * p.row_bytes;
             const int64_t end = start + static_cast<int64_t>(rows) * p.row_bytes;
@@ -254,30 +267,14 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Activations of one matrix into shared memory (all consumer threads). f32
-// x goes through a shared buffer of p.x_bytes, one chunk of whole
-// activation blocks at a time.
+// Activations of one matrix into shared memory (all consumer threads): f32
+// x quantized straight from global memory (each warp loads the blocks it
+// quantizes, two at a time), or records copied from byte-exact blocks.
 template <class T, int NV>
-__device__ __forceinline__ void stage_activations(const GemvParams &p, const GemvMat &mt, uint8_t *act,
-                                                  float *xbuf, int warp, int lane) {
+__device__ __forceinline__ void stage_activations(const GemvParams &p, const GemvMat &mt, uint8_t *act, int warp,
+                                                  int lane) {
     if (mt.x) {
-        // Copy x through the load/store path (16 bytes a thread per
-        // instruction, all in flight at once) -- not through the bulk-copy
-        // engine, whose queue also carries weight prefetches -- then quantize
-        // from shared memory.
-        const int blocks = p.nb * NV;
-        const int chunk = p.x_bytes / (4 * T::kActValues);
-        const uint32_t xs = smem_addr(xbuf);
-        for (int g0 = 0; g0 < blocks; g0 += chunk) {
-            const int count = min(chunk, blocks - g0);
-            const float *src = mt.x + static_cast<size_t>(g0) * T::kActValues;
-            const int n16 = count * T::kActValues / 4;
-            if (g0 > 0) named_barrier(1, kConsumerWarps * 32);  // the previous chunk is consumed
-            for (int i = threadIdx.x; i < n16; i += kConsumerWarps * 32) cp_async_16(xs + 16 * i, src + 4 * i);
-            cp_async_wait_all();
-            named_barrier(1, kConsumerWarps * 32);
-            T::stage_x(xs, act, g0, count, warp, kConsumerWarps, lane);
-        }
+        T::stage_x(mt.x, act, p.nb * NV, warp, kConsumerWarps, lane);
     } else {
         T::stage_act(mt.xq, act, p.nb, NV, threadIdx.x, kConsumerWarps * 32);
     }
@@ -296,9 +293,8 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     const uint32_t bar_full0 = smem_addr(smem);
     const uint32_t bar_empty0 = bar_full0 + 8 * kMaxStages;
     uint8_t *act = smem + kHeaderBytes;
-    float *xbuf = reinterpret_cast<float *>(act + p.act_bytes);
-    float *red = reinterpret_cast<float *>(act + p.act_bytes + p.x_bytes);
-    uint8_t *ring = act + p.act_bytes + p.x_bytes + p.red_bytes;
+    float *red = reinterpret_cast<float *>(act + p.act_bytes);
+    uint8_t *ring = act + p.act_bytes + p.red_bytes;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -322,15 +318,16 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     }
 
     // ---- consumers ----
-    pdl_wait_prior_grids();  // activations may come from the previous kernel
+    // Everything up to the first activation read is independent of the
+    // previous kernel and runs before waiting for it.
     bool failed = false;
 
     const int split = p.split;
-    const int groups = kConsumerWarps / split;
-    const int grp = warp / split;
-    const int part = warp % split;
-    const int b0 = part * p.nb / split;
-    const int b1 = (part + 1) * p.nb / split;
+    const int groups = kConsumerWarps >> p.split_log2;
+    const int grp = warp >> p.split_log2;
+    const int part = warp & (split - 1);
+    const int b0 = (part * p.nb) >> p.split_log2;
+    const int b1 = ((part + 1) * p.nb) >> p.split_log2;
     const int nbw = b1 - b0;  // blocks of each of this warp's rows
     constexpr int kBlocksPerIter = 32 / T::kLanesPerBlock;
     const int sub = lane % T::kLanesPerBlock;  // the lane's part of a block
@@ -349,11 +346,13 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     for (int k = 0; walk.next(b, p.n_mats, R, mat, r, rows); ++k) {
         if (mat != cur) {  // this CTA reaches a new matrix: stage its activations
             if (cur >= 0) named_barrier(1, kConsumerWarps * 32);
-            stage_activations<T, NV>(p, b.m[mat], act, xbuf, warp, lane);
+            else pdl_wait_prior_grids();  // activations may come from the previous kernel
+            stage_activations<T, NV>(p, b.m[MAXB == 1 ? 0 : mat], act, warp, lane);
             cur = mat;
-            y = b.m[mat].y;
-            isums = b.m[mat].isums;
-            n_out = b.m[mat].n_out;
+            const GemvMat &mt = b.m[MAXB == 1 ? 0 : mat];  // constant index: no local copy of the table
+            y = mt.y;
+            isums = mt.isums;
+            n_out = mt.n_out;
         }
         if (!failed && !mbar_wait_bounded(bar_full0 + 8 * slot, phase)) {
             record_error(p.err, kErrConsumerWait);

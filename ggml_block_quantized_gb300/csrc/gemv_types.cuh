@@ -61,11 +61,14 @@ __device__ __forceinline__ float group_max(float v) {
     return v;
 }
 
-// Eight f32 values at a shared-memory address (the staged activations).
-__device__ __forceinline__ void load8(uint32_t a, float (&v)[8]) {
-    const uint4 x = ld_s128(a), y = ld_s128(a + 16);
-    v[0] = __uint_as_float(x.x); v[1] = __uint_as_float(x.y); v[2] = __uint_as_float(x.z); v[3] = __uint_as_float(x.w);
-    v[4] = __uint_as_float(y.x); v[5] = __uint_as_float(y.y); v[6] = __uint_as_float(y.z); v[7] = __uint_as_float(y.w);
+// Eight consecutive f32 values of x from global memory (16-byte aligned),
+// cached in L2 only: x may have been written by the kernel this one waited
+// for.
+__device__ __forceinline__ void load8g(const float *p, float (&v)[8]) {
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 // Codes of 8 values with the inverse scale id, packed 4 per word; returns
@@ -86,12 +89,98 @@ __device__ __forceinline__ uint32_t pack16(int lo, int hi) {
     return (static_cast<uint32_t>(lo) & 0xFFFFu) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// Q8_0-rule quantization of 32-value blocks 0..count-1 of f32 x (global
+// memory) inside the GEMV prologue: 4 lanes per block (lane l takes values
+// 8(l%4)..+7 of block base + l/4), 8 blocks per warp step, two steps at a
+// time so that their load round trips and reduction chains overlap.
+// emit(i, ok, part, w, sum, d) stores one lane's part of block i (ok: i < count).
+template <int LO, class Emit>
+__device__ __forceinline__ void stage_x_q8_0(const float *x, int count, int warp, int nwarps, int lane, Emit emit) {
+    const int part = lane & 3;
+    for (int base = warp * 8; base < count; base += 2 * nwarps * 8) {
+        int idx[2];
+        bool ok[2];
+        float v[2][8];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            idx[n] = base + n * nwarps * 8 + (lane >> 2);
+            ok[n] = idx[n] < count;
+            if (ok[n]) {
+                load8g(x + 32 * static_cast<size_t>(idx[n]) + 8 * part, v[n]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[n][k] = 0.0f;
+            }
+        }
+        float a[2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            a[n] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a[n] = fmaxf(a[n], fabsf(v[n][k]));
+        }
+#pragma unroll
+        for (int m = 1; m < 4; m <<= 1)
+#pragma unroll
+            for (int n = 0; n < 2; ++n) a[n] = fmaxf(a[n], __shfl_xor_sync(0xffffffffu, a[n], m));
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const float d = a[n] / 127.0f;
+            const float id = d != 0.0f ? 1.0f / d : 0.0f;
+            uint32_t w[2];
+            const int sum = group_sum<4>(codes8(v[n], id, LO, 127, w));
+            emit(idx[n], ok[n], part, w, sum, d);
+        }
+    }
+}
+
+// Q8_K quantization of 256-value blocks 0..count-1 of f32 x (global memory):
+// one warp per block, lane l owning values 8l..8l+7, two blocks at a time.
+// emit(i, w, sum16, d) stores block i's part of lane l: its codes (2 words),
+// the 16-value sum of lanes (2k, 2k+1) (in both lanes of the pair) and d.
+// emit is called by all lanes of the warp together (it may shuffle).
+template <class Emit>
+__device__ __forceinline__ void stage_x_q8_k(const float *x, int count, int warp, int nwarps, int lane, Emit emit) {
+    for (int i = warp; i < count; i += 2 * nwarps) {
+        const int j = i + nwarps;
+        const bool two = j < count;  // warp-uniform
+        float v[2][8];
+        load8g(x + 256 * static_cast<size_t>(i) + 8 * lane, v[0]);
+        if (two) {
+            load8g(x + 256 * static_cast<size_t>(j) + 8 * lane, v[1]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[1][k] = 0.0f;
+        }
+        float a[2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            a[n] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) a[n] = fmaxf(a[n], fabsf(v[n][k]));
+        }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+            for (int n = 0; n < 2; ++n) a[n] = fmaxf(a[n], __shfl_xor_sync(0xffffffffu, a[n], m));
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const float d = a[n] / 127.0f;
+            const float id = d != 0.0f ? 1.0f / d : 0.0f;
+            uint32_t w[2];
+            const int s = codes8(v[n], id, -127, 127, w);
+            const int sum16 = s + __shfl_xor_sync(0xffffffffu, s, 1);
+            if (n == 0 || two) emit(n == 0 ? i : j, w, sum16, d);
+        }
+    }
+}
+
 // ========================================================================
 // Staging interfaces shared by all types:
 //   stage_act(xq, act, nb, nv, tid, nthr): records from byte-exact blocks.
-//   stage_x(xs, act, g0, count, warp, nwarps, lane): records for activation
-//     blocks g0 .. g0+count-1 (block index g = v * nb + b) from their f32
-//     values at shared address xs (value 0 of block g0).
+//   stage_x(x, act, count, warp, nwarps, lane): records for activation
+//     blocks 0 .. count-1 (block index g = v * nb + b) quantized from their
+//     f32 values in global memory (x = value 0 of block 0).
 // Item interface: item<NV, ISUMS>(rowa, b, sub, active, acta, nb, acc,
 //   isum_row, isum_vstride) adds the block's float terms of one weight row
 //   (shared address rowa) to acc[v], or writes its exact sums.
@@ -130,37 +219,19 @@ struct ActQ8_0 {
         }
     }
 
-    // From f32 values in shared memory: 4 lanes per 32-value block, 8 blocks per warp step.
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        for (int base = warp * 8; base < count; base += nwarps * 8) {
-            const int i = base + (lane >> 2);
-            const int part = lane & 3;
-            const bool ok = i < count;
-            float v[8];
-            if (ok) {
-                load8(xs + 4u * (32u * i + 8u * part), v);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = 0.0f;
-            }
-            float a = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(v[k]));
-            a = group_max<4>(a);
-            const float d = a / 127.0f;
-            const float id = d != 0.0f ? 1.0f / d : 0.0f;
-            uint32_t w[2];
-            int sum = group_sum<4>(codes8(v, id, -128, 127, w));
-            if (ok) {
-                uint8_t *rec = act + static_cast<size_t>(g0 + i) * kRecord;
-                reinterpret_cast<uint2 *>(rec)[part] = make_uint2(w[0], w[1]);
-                if (part == 0) {
-                    const float dx = __half2float(__float2half_rn(d));  // the stored f16 scale
-                    reinterpret_cast<uint4 *>(rec)[2] =
-                        make_uint4(__float_as_uint(dx), static_cast<uint32_t>(sum), 0u, 0u);
-                }
-            }
-        }
+    // From f32 x: 4 lanes per 32-value block (the Q8_0 rule).
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        stage_x_q8_0<-128>(x, count, warp, nwarps, lane,
+                           [&](int i, bool ok, int part, const uint32_t (&w)[2], int sum, float d) {
+                               if (!ok) return;
+                               uint8_t *rec = act + static_cast<size_t>(i) * kRecord;
+                               reinterpret_cast<uint2 *>(rec)[part] = make_uint2(w[0], w[1]);
+                               if (part == 0) {
+                                   const float dx = __half2float(__float2half_rn(d));  // the stored f16 scale
+                                   reinterpret_cast<uint4 *>(rec)[2] =
+                                       make_uint4(__float_as_uint(dx), static_cast<uint32_t>(sum), 0u, 0u);
+                               }
+                           });
     }
 };
 
@@ -171,8 +242,8 @@ struct TypeQ8_0 {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        ActQ8_0::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
@@ -211,8 +282,8 @@ struct TypeQ4_0 {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        ActQ8_0::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
@@ -263,8 +334,8 @@ struct TypeQ5_0 {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        ActQ8_0::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
@@ -334,39 +405,22 @@ struct ActQ8_1 {
         }
     }
 
-    // From f32 values in shared memory (the Q8_0 rule, then s = f16(sum * d)
-    // from the f32 d): 4 lanes per block, 8 blocks per warp step.
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        for (int base = warp * 8; base < count; base += nwarps * 8) {
-            const int i = base + (lane >> 2);
-            const int part = lane & 3;
-            const bool ok = i < count;
-            float v[8];
-            if (ok) {
-                load8(xs + 4u * (32u * i + 8u * part), v);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = 0.0f;
-            }
-            float a = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(v[k]));
-            a = group_max<4>(a);
-            const float d = a / 127.0f;
-            const float id = d != 0.0f ? 1.0f / d : 0.0f;
-            uint32_t w[2];
-            const int sum = group_sum<4>(codes8(v, id, -128, 127, w));
-            if (ok) {
-                uint8_t *rec = act + static_cast<size_t>(g0 + i) * kRecord;
-                reinterpret_cast<uint2 *>(rec)[part] = make_uint2(w[0], w[1]);
-                if (part == 0) {
-                    const float dx = __half2float(__float2half_rn(d));
-                    const float sx = __half2float(__float2half_rn(__fmul_rn(static_cast<float>(sum), d)));
-                    reinterpret_cast<uint4 *>(rec)[2] = make_uint4(__float_as_uint(dx), static_cast<uint32_t>(sum),
-                                                                   __float_as_uint(sx), 0u);
-                }
-            }
-        }
+    // From f32 x (the Q8_0 rule, then s = f16(sum * d) from the f32 d): 4
+    // lanes per block.
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        stage_x_q8_0<-128>(x, count, warp, nwarps, lane,
+                           [&](int i, bool ok, int part, const uint32_t (&w)[2], int sum, float d) {
+                               if (!ok) return;
+                               uint8_t *rec = act + static_cast<size_t>(i) * kRecord;
+                               reinterpret_cast<uint2 *>(rec)[part] = make_uint2(w[0], w[1]);
+                               if (part == 0) {
+                                   const float dx = __half2float(__float2half_rn(d));
+                                   const float sx =
+                                       __half2float(__float2half_rn(__fmul_rn(static_cast<float>(sum), d)));
+                                   reinterpret_cast<uint4 *>(rec)[2] = make_uint4(
+                                       __float_as_uint(dx), static_cast<uint32_t>(sum), __float_as_uint(sx), 0u);
+                               }
+                           });
     }
 };
 
@@ -380,8 +434,8 @@ struct TypeQ4_1 {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_1::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        ActQ8_1::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        ActQ8_1::stage_x(x, act, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
@@ -421,23 +475,6 @@ struct TypeQ4_1 {
     }
 };
 
-// ------------------------------------------------------------------------
-// Q8_K from f32 in shared memory: one warp per 256-value block, lane l owns
-// values 8l..8l+7. Returns the codes (2 words), the 16-value sum of lanes
-// (2k, 2k+1) in every lane of the pair, and d.
-// ------------------------------------------------------------------------
-__device__ __forceinline__ void quantize_q8_k_lane(uint32_t blk, int lane, uint32_t (&w)[2], int &sum16, float &d) {
-    float v[8];
-    load8(blk + 32u * lane, v);
-    float a = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) a = fmaxf(a, fabsf(v[k]));
-    a = group_max<32>(a);
-    d = a / 127.0f;
-    const float id = d != 0.0f ? 1.0f / d : 0.0f;
-    const int s = codes8(v, id, -127, 127, w);
-    sum16 = s + __shfl_xor_sync(0xffffffffu, s, 1);
-}
 
 // ------------------------------------------------------------------------
 // Q4_K. Two lanes per block: lane h takes half h (values 128h..128h+127,
@@ -478,19 +515,15 @@ struct TypeQ4_K {
         }
     }
 
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
         const int h = lane >> 4;
-        for (int i = warp; i < count; i += nwarps) {
-            uint32_t w[2];
-            int s16;
-            float d;
-            quantize_q8_k_lane(xs + 1024u * i, lane, w, s16, d);
+        stage_x_q8_k(x, count, warp, nwarps, lane, [&](int i, const uint32_t (&w)[2], int s16, float d) {
             const int s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 2);  // sub-block lane/4
-            uint8_t *rec = act + (static_cast<size_t>(g0 + i) * 2 + h) * kRecord;
+            uint8_t *rec = act + (static_cast<size_t>(i) * 2 + h) * kRecord;
             reinterpret_cast<uint2 *>(rec)[lane & 15] = make_uint2(w[0], w[1]);
             if ((lane & 3) == 0) reinterpret_cast<int16_t *>(rec + 128)[(lane >> 2) & 3] = static_cast<int16_t>(s32);
             if ((lane & 15) == 0) reinterpret_cast<uint2 *>(rec + 136)[0] = make_uint2(__float_as_uint(d), 0u);
-        }
+        });
     }
 
     template <int NV, bool ISUMS>
@@ -590,19 +623,15 @@ struct TypeQ6_K {
         }
     }
 
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
         // lane l holds values 8l..8l+7: half h = l/16
         const int h = lane >> 4;
-        for (int i = warp; i < count; i += nwarps) {
-            uint32_t w[2];
-            int s16;
-            float d;
-            quantize_q8_k_lane(xs + 1024u * i, lane, w, s16, d);
-            uint8_t *rec = act + (static_cast<size_t>(g0 + i) * 2 + h) * kRecord;
+        stage_x_q8_k(x, count, warp, nwarps, lane, [&](int i, const uint32_t (&w)[2], int s16, float d) {
+            uint8_t *rec = act + (static_cast<size_t>(i) * 2 + h) * kRecord;
             reinterpret_cast<uint2 *>(rec)[lane & 15] = make_uint2(w[0], w[1]);
             if ((lane & 1) == 0) reinterpret_cast<int16_t *>(rec + 128)[(lane & 15) >> 1] = static_cast<int16_t>(s16);
             if ((lane & 15) == 0) reinterpret_cast<float *>(rec + 144)[0] = d;
-        }
+        });
     }
 
     // Lane part h: element e = 128h + 32k + 16m + lam (sub-block j = 8h + 2k + m)
@@ -693,20 +722,16 @@ struct TypeQ6_K4 {
         }
     }
 
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
         // lane l holds values 8l..8l+7: h = l/16, k = (l%16)/4, p = (l%4)/2
         const int h = lane >> 4, k = (lane >> 2) & 3, p = (lane >> 1) & 1;
         const int sub = 2 * h + p;
-        for (int i = warp; i < count; i += nwarps) {
-            uint32_t w[2];
-            int s16;
-            float d;
-            quantize_q8_k_lane(xs + 1024u * i, lane, w, s16, d);
-            uint8_t *rec = act + (static_cast<size_t>(g0 + i) * 4 + sub) * kRecord;
+        stage_x_q8_k(x, count, warp, nwarps, lane, [&](int i, const uint32_t (&w)[2], int s16, float d) {
+            uint8_t *rec = act + (static_cast<size_t>(i) * 4 + sub) * kRecord;
             reinterpret_cast<uint2 *>(rec + 16 * k)[lane & 1] = make_uint2(w[0], w[1]);
             if ((lane & 1) == 0) reinterpret_cast<int16_t *>(rec + 64)[k] = static_cast<int16_t>(s16);
             if (k == 0 && (lane & 1) == 0) reinterpret_cast<uint2 *>(rec + 72)[0] = make_uint2(__float_as_uint(d), 0u);
-        }
+        });
     }
 
     template <int NV, bool ISUMS>
@@ -771,8 +796,8 @@ struct TypeQ5_K {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         TypeQ4_K::stage_act(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        TypeQ4_K::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        TypeQ4_K::stage_x(x, act, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
@@ -860,8 +885,8 @@ struct TypeQ2_K {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         TypeQ6_K::stage_act(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        TypeQ6_K::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        TypeQ6_K::stage_x(x, act, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>
@@ -946,8 +971,8 @@ struct TypeQ3_K {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         TypeQ6_K::stage_act(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(uint32_t xs, uint8_t *act, int g0, int count, int warp, int nwarps, int lane) {
-        TypeQ6_K::stage_x(xs, act, g0, count, warp, nwarps, lane);
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+        TypeQ6_K::stage_x(x, act, count, warp, nwarps, lane);
     }
 
     template <int NV, bool ISUMS>

@@ -333,7 +333,9 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
  * counterpart; the knobs choose between kernels that compute the same
  * product). name is one of the environment variables the library reads once
  * at first use: QG_CTAS_PER_SM, QG_RING_KIB, QG_MMA_MIN_NVEC, QG_MMA_PANEL,
- * QG_MMA_KB, QG_FUSED_QUANT_KIB, QG_TC (the tcgen05 Q4_K kernel for three or
+ * QG_MMA_KB, QG_FUSED_QUANT_KIB (f32 x of at most this many KiB is quantized
+ * inside the GEMV), QG_FUSED_MAX_MIB (... for a single matrix of at most this
+ * many MiB of blocks; default: no limit), QG_TC (the tcgen05 Q4_K kernel for three or
  * more vectors, rows of 2048 or 4096 elements: 0 never, the default; 1
  * whenever it fits). value is clamped to the knob's range; the old
  * value goes to *previous when that is not NULL. Returns QG_OK, QG_ERR_NULL

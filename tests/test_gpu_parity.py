@@ -283,15 +283,40 @@ def test_qgemv_layer_stack_matrices(m, n_vec):
             sample_rows(n_out, np.random.default_rng(m), 64))
 
 
-def test_qgemv_xq_equals_qgemv():
+@pytest.mark.parametrize("t", WTYPES)
+def test_qgemv_xq_equals_qgemv(t):
+    """x quantized inside the GEMV's prologue (each warp quantizing two
+    blocks at a time, with a ragged last pair) gives the same bits as the
+    separate quantization launch: on normal x and on the quantizer's special
+    patterns, at block counts that leave warps with one block or none."""
     rng = np.random.default_rng(8)
-    for t in WTYPES:
-        n_out, n_in = 333, 1024
+    cases = [(333, 1024, 2), (70, 1280, 3), (19, 256, 8), (40, 2560, 1)]
+    for n_out, n_in, n_vec in cases:
         W = dev(weights(t, n_out, n_in, rng))
-        x = dev(synth.f32_normal(rng, 2 * n_in))
-        y1 = qg.qgemv(t, W, x, n_out, n_in, 2)
-        y2 = qg.qgemv_xq(t, W, qg.quantize_act(oracle.act_type(t), x, 2), n_out, n_in, 2)
-        assert torch.equal(y1, y2)
+        xs = [synth.f32_normal(rng, n_vec * n_in)] + [f(n_vec * n_in) for f in SPECIAL.values()]
+        for xh in xs:
+            x = dev(xh)
+            y1 = qg.qgemv(t, W, x, n_out, n_in, n_vec)
+            y2 = qg.qgemv_xq(t, W, qg.quantize_act(oracle.act_type(t), x, n_vec), n_out, n_in, n_vec)
+            assert torch.equal(y1.view(torch.int32), y2.view(torch.int32)), (n_out, n_in, n_vec)
+
+
+def test_fused_limit_knob_keeps_results():
+    """QG_FUSED_MAX_MIB moves a single call between in-kernel quantization and
+    the separate launch; the product is the same bits either way."""
+    t, n_out, n_in = qg.Q4_K, 3000, 4096
+    rng = np.random.default_rng(81)
+    W = dev(weights(t, n_out, n_in, rng))
+    x = dev(synth.f32_normal(rng, n_in))
+    assert "fused-quantize" in qg.kernel_info(t, n_out, n_in, 1)
+    y1 = qg.qgemv(t, W, x, n_out, n_in, 1)
+    prev = qg.tune("QG_FUSED_MAX_MIB", 0)
+    try:
+        assert "fused-quantize" not in qg.kernel_info(t, n_out, n_in, 1)
+        y2 = qg.qgemv(t, W, x, n_out, n_in, 1)
+    finally:
+        qg.tune("QG_FUSED_MAX_MIB", prev)
+    assert torch.equal(y1, y2)
 
 
 # ---------------------------------------------------------------- edges
