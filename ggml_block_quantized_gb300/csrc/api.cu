@@ -286,6 +286,11 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
                     bp.stage_bytes = static_cast<int>(stage);
                     bp.act_bytes = static_cast<int>(act);
                     bp.red_bytes = static_cast<int>(red_bytes(S));
+                    // stages in flight while the consumers' first activation
+                    // loads travel: about 56 KiB (measured best for rows of
+                    // 1.3-3.4 KB)
+                    bp.pre_x = static_cast<int>(57344 / stage);
+                    bp.pre_x = bp.pre_x < 1 ? 1 : (bp.pre_x > S ? S : bp.pre_x);
                     best_smem = fixed0 + red_bytes(S) + S * stage;
                 }
             }

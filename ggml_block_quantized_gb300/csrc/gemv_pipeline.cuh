@@ -45,10 +45,14 @@ constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 16;
 constexpr int kRowsPerWarp = 2;  // most rows a warp group takes per stage (its items are flattened over them)
 constexpr int kMaxBatch = 256;   // matrices per batched launch (their table is a kernel parameter)
-// Shared memory: header (kMaxStages full + kMaxStages empty mbarriers) |
+// The producer issues only the first stages (GemvParams::pre_x, about 56 KiB)
+// before the consumers' first activation loads have arrived: behind a deep
+// queue of weight copies those loads wait for microseconds.
+// Shared memory: header (kMaxStages full + kMaxStages empty mbarriers, the
+// activations-arrived mbarrier, 8 bytes of padding) |
 // staged activations | cross-warp partial sums (split > 1:
 // [2 * n_stages][kConsumerWarps][kRowsPerWarp][NV] floats) | ring of stages.
-constexpr int kHeaderBytes = 2 * 8 * kMaxStages;
+constexpr int kHeaderBytes = 2 * 8 * kMaxStages + 16;
 
 // One matrix of a launch.
 struct GemvMat {
@@ -83,6 +87,7 @@ struct GemvParams {
     int stage_bytes;     // bytes per ring slot, multiple of 16
     int act_bytes;       // bytes of staged activations, multiple of 16
     int red_bytes;       // bytes of the cross-warp partial sums (split > 1), else 0
+    int pre_x;           // stages issued before the consumers' first activation loads arrive (>= 1)
 };
 
 // Walks a CTA's global rows [g, g1) as stages of at most R rows that never
@@ -161,7 +166,8 @@ __device__ __forceinline__ void finish_split_rows(const GemvParams &p, const flo
 
 template <int MAXB, int NV, bool ISUMS>
 __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBatch<MAXB> &b, uint8_t *ring,
-                                              const float *red, uint32_t bar_full0, uint32_t bar_empty0, int lane) {
+                                              const float *red, uint32_t bar_full0, uint32_t bar_empty0,
+                                              uint32_t bar_x, int lane) {
     const uint64_t policy = l2_evict_first_policy();
     const int S = p.n_stages;
     const bool reduce = !ISUMS && p.split > 1;
@@ -183,6 +189,16 @@ __device__ __forceinline__ void gemv_producer(const GemvParams &p, const GemvBat
     int n_out = 0;
     int64_t lim = 0;
     for (int k = 0; walk.next(b, p.n_mats, p.rows_per_stage, mat, r, rows); ++k) {
+        if (k == p.pre_x) {  // the rest after the consumers' first activation loads
+            bool got = true;
+            if (lane == 0) got = mbar_wait_bounded(bar_x, 0);
+            got = __shfl_sync(lanes, got, 0);
+            if (!got) {
+                if (lane == 0) record_error(p.err, kErrProducerWait);
+                ok = false;
+                break;
+            }
+        }
         if (k >= S) {
             const uint32_t parity = phase ^ 1u;
             bool got = true;
@@ -270,14 +286,23 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Activations of one matrix into shared memory (all consumer threads): f32
 // x quantized straight from global memory (each warp loads the blocks it
 // quantizes, two at a time), or records copied from byte-exact blocks.
+// With bar_x != 0 each consumer warp arrives on it once its first loads have
+// arrived (or at once when it has none), which lets the producer issue its
+// further stages.
 template <class T, int NV>
 __device__ __forceinline__ void stage_activations(const GemvParams &p, const GemvMat &mt, uint8_t *act, int warp,
-                                                  int lane) {
+                                                  int lane, uint32_t bar_x) {
+    bool told = bar_x == 0;
+    auto loaded = [&]() {
+        if (!told && lane == 0) mbar_arrive(bar_x);
+        told = true;
+    };
     if (mt.x) {
-        T::stage_x(mt.x, act, p.nb * NV, warp, kConsumerWarps, lane);
+        T::stage_x(mt.x, act, p.nb * NV, warp, kConsumerWarps, lane, loaded);
     } else {
         T::stage_act(mt.xq, act, p.nb, NV, threadIdx.x, kConsumerWarps * 32);
     }
+    loaded();
     named_barrier(1, kConsumerWarps * 32);
 }
 
@@ -292,6 +317,7 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t bar_full0 = smem_addr(smem);
     const uint32_t bar_empty0 = bar_full0 + 8 * kMaxStages;
+    const uint32_t bar_x = bar_full0 + 16 * kMaxStages;
     uint8_t *act = smem + kHeaderBytes;
     float *red = reinterpret_cast<float *>(act + p.act_bytes);
     uint8_t *ring = act + p.act_bytes + p.red_bytes;
@@ -306,6 +332,7 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
             mbar_init(bar_full0 + 8 * s, 1);
             mbar_init(bar_empty0 + 8 * s, kConsumerWarps);
         }
+        mbar_init(bar_x, kConsumerWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -313,7 +340,7 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
     pdl_allow_dependents();
 
     if (warp == kConsumerWarps) {
-        gemv_producer<MAXB, NV, ISUMS>(p, b, ring, red, bar_full0, bar_empty0, lane);
+        gemv_producer<MAXB, NV, ISUMS>(p, b, ring, red, bar_full0, bar_empty0, bar_x, lane);
         return;
     }
 
@@ -347,7 +374,7 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
         if (mat != cur) {  // this CTA reaches a new matrix: stage its activations
             if (cur >= 0) named_barrier(1, kConsumerWarps * 32);
             else pdl_wait_prior_grids();  // activations may come from the previous kernel
-            stage_activations<T, NV>(p, b.m[MAXB == 1 ? 0 : mat], act, warp, lane);
+            stage_activations<T, NV>(p, b.m[MAXB == 1 ? 0 : mat], act, warp, lane, cur < 0 ? bar_x : 0u);
             cur = mat;
             const GemvMat &mt = b.m[MAXB == 1 ? 0 : mat];  // constant index: no local copy of the table
             y = mt.y;

@@ -93,9 +93,11 @@ __device__ __forceinline__ uint32_t pack16(int lo, int hi) {
 // memory) inside the GEMV prologue: 4 lanes per block (lane l takes values
 // 8(l%4)..+7 of block base + l/4), 8 blocks per warp step, two steps at a
 // time so that their load round trips and reduction chains overlap.
-// emit(i, ok, part, w, sum, d) stores one lane's part of block i (ok: i < count).
-template <int LO, class Emit>
-__device__ __forceinline__ void stage_x_q8_0(const float *x, int count, int warp, int nwarps, int lane, Emit emit) {
+// emit(i, ok, part, w, sum, d) stores one lane's part of block i (ok: i < count);
+// loaded() runs once per warp, when its first loads have arrived.
+template <int LO, class Emit, class Loaded>
+__device__ __forceinline__ void stage_x_q8_0(const float *x, int count, int warp, int nwarps, int lane, Emit emit,
+                                             Loaded loaded) {
     const int part = lane & 3;
     for (int base = warp * 8; base < count; base += 2 * nwarps * 8) {
         int idx[2];
@@ -119,6 +121,7 @@ __device__ __forceinline__ void stage_x_q8_0(const float *x, int count, int warp
 #pragma unroll
             for (int k = 0; k < 8; ++k) a[n] = fmaxf(a[n], fabsf(v[n][k]));
         }
+        if (base == warp * 8 && a[0] >= 0.0f) loaded();  // (a >= 0 always: waits for the loads)
 #pragma unroll
         for (int m = 1; m < 4; m <<= 1)
 #pragma unroll
@@ -138,9 +141,11 @@ __device__ __forceinline__ void stage_x_q8_0(const float *x, int count, int warp
 // one warp per block, lane l owning values 8l..8l+7, two blocks at a time.
 // emit(i, w, sum16, d) stores block i's part of lane l: its codes (2 words),
 // the 16-value sum of lanes (2k, 2k+1) (in both lanes of the pair) and d.
-// emit is called by all lanes of the warp together (it may shuffle).
-template <class Emit>
-__device__ __forceinline__ void stage_x_q8_k(const float *x, int count, int warp, int nwarps, int lane, Emit emit) {
+// emit is called by all lanes of the warp together (it may shuffle);
+// loaded() runs once per warp, when its first loads have arrived.
+template <class Emit, class Loaded>
+__device__ __forceinline__ void stage_x_q8_k(const float *x, int count, int warp, int nwarps, int lane, Emit emit,
+                                             Loaded loaded) {
     for (int i = warp; i < count; i += 2 * nwarps) {
         const int j = i + nwarps;
         const bool two = j < count;  // warp-uniform
@@ -159,6 +164,7 @@ __device__ __forceinline__ void stage_x_q8_k(const float *x, int count, int warp
 #pragma unroll
             for (int k = 0; k < 8; ++k) a[n] = fmaxf(a[n], fabsf(v[n][k]));
         }
+        if (i == warp && a[0] >= 0.0f) loaded();  // (a >= 0 always: waits for the loads)
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1)
 #pragma unroll
@@ -178,9 +184,11 @@ __device__ __forceinline__ void stage_x_q8_k(const float *x, int count, int warp
 // ========================================================================
 // Staging interfaces shared by all types:
 //   stage_act(xq, act, nb, nv, tid, nthr): records from byte-exact blocks.
-//   stage_x(x, act, count, warp, nwarps, lane): records for activation
-//     blocks 0 .. count-1 (block index g = v * nb + b) quantized from their
-//     f32 values in global memory (x = value 0 of block 0).
+//   stage_x(x, act, count, warp, nwarps, lane, loaded): records for
+//     activation blocks 0 .. count-1 (block index g = v * nb + b) quantized
+//     from their f32 values in global memory (x = value 0 of block 0);
+//     loaded() is called once per warp that loads anything, when its first
+//     loads have arrived.
 // Item interface: item<NV, ISUMS>(rowa, b, sub, active, acta, nb, acc,
 //   isum_row, isum_vstride) adds the block's float terms of one weight row
 //   (shared address rowa) to acc[v], or writes its exact sums.
@@ -220,7 +228,9 @@ struct ActQ8_0 {
     }
 
     // From f32 x: 4 lanes per 32-value block (the Q8_0 rule).
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
         stage_x_q8_0<-128>(x, count, warp, nwarps, lane,
                            [&](int i, bool ok, int part, const uint32_t (&w)[2], int sum, float d) {
                                if (!ok) return;
@@ -231,7 +241,8 @@ struct ActQ8_0 {
                                    reinterpret_cast<uint4 *>(rec)[2] =
                                        make_uint4(__float_as_uint(dx), static_cast<uint32_t>(sum), 0u, 0u);
                                }
-                           });
+                           },
+                           loaded);
     }
 };
 
@@ -242,8 +253,10 @@ struct TypeQ8_0 {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
-        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane);
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
+        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane, loaded);
     }
 
     template <int NV, bool ISUMS>
@@ -282,8 +295,10 @@ struct TypeQ4_0 {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
-        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane);
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
+        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane, loaded);
     }
 
     template <int NV, bool ISUMS>
@@ -334,8 +349,10 @@ struct TypeQ5_0 {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_0::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
-        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane);
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
+        ActQ8_0::stage_x(x, act, count, warp, nwarps, lane, loaded);
     }
 
     template <int NV, bool ISUMS>
@@ -407,7 +424,9 @@ struct ActQ8_1 {
 
     // From f32 x (the Q8_0 rule, then s = f16(sum * d) from the f32 d): 4
     // lanes per block.
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
         stage_x_q8_0<-128>(x, count, warp, nwarps, lane,
                            [&](int i, bool ok, int part, const uint32_t (&w)[2], int sum, float d) {
                                if (!ok) return;
@@ -420,7 +439,8 @@ struct ActQ8_1 {
                                    reinterpret_cast<uint4 *>(rec)[2] = make_uint4(
                                        __float_as_uint(dx), static_cast<uint32_t>(sum), __float_as_uint(sx), 0u);
                                }
-                           });
+                           },
+                           loaded);
     }
 };
 
@@ -434,8 +454,10 @@ struct TypeQ4_1 {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         ActQ8_1::stage(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
-        ActQ8_1::stage_x(x, act, count, warp, nwarps, lane);
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
+        ActQ8_1::stage_x(x, act, count, warp, nwarps, lane, loaded);
     }
 
     template <int NV, bool ISUMS>
@@ -515,7 +537,9 @@ struct TypeQ4_K {
         }
     }
 
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
         const int h = lane >> 4;
         stage_x_q8_k(x, count, warp, nwarps, lane, [&](int i, const uint32_t (&w)[2], int s16, float d) {
             const int s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 2);  // sub-block lane/4
@@ -523,7 +547,7 @@ struct TypeQ4_K {
             reinterpret_cast<uint2 *>(rec)[lane & 15] = make_uint2(w[0], w[1]);
             if ((lane & 3) == 0) reinterpret_cast<int16_t *>(rec + 128)[(lane >> 2) & 3] = static_cast<int16_t>(s32);
             if ((lane & 15) == 0) reinterpret_cast<uint2 *>(rec + 136)[0] = make_uint2(__float_as_uint(d), 0u);
-        });
+        }, loaded);
     }
 
     template <int NV, bool ISUMS>
@@ -623,7 +647,9 @@ struct TypeQ6_K {
         }
     }
 
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
         // lane l holds values 8l..8l+7: half h = l/16
         const int h = lane >> 4;
         stage_x_q8_k(x, count, warp, nwarps, lane, [&](int i, const uint32_t (&w)[2], int s16, float d) {
@@ -631,7 +657,7 @@ struct TypeQ6_K {
             reinterpret_cast<uint2 *>(rec)[lane & 15] = make_uint2(w[0], w[1]);
             if ((lane & 1) == 0) reinterpret_cast<int16_t *>(rec + 128)[(lane & 15) >> 1] = static_cast<int16_t>(s16);
             if ((lane & 15) == 0) reinterpret_cast<float *>(rec + 144)[0] = d;
-        });
+        }, loaded);
     }
 
     // Lane part h: element e = 128h + 32k + 16m + lam (sub-block j = 8h + 2k + m)
@@ -722,7 +748,9 @@ struct TypeQ6_K4 {
         }
     }
 
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
         // lane l holds values 8l..8l+7: h = l/16, k = (l%16)/4, p = (l%4)/2
         const int h = lane >> 4, k = (lane >> 2) & 3, p = (lane >> 1) & 1;
         const int sub = 2 * h + p;
@@ -731,7 +759,7 @@ struct TypeQ6_K4 {
             reinterpret_cast<uint2 *>(rec + 16 * k)[lane & 1] = make_uint2(w[0], w[1]);
             if ((lane & 1) == 0) reinterpret_cast<int16_t *>(rec + 64)[k] = static_cast<int16_t>(s16);
             if (k == 0 && (lane & 1) == 0) reinterpret_cast<uint2 *>(rec + 72)[0] = make_uint2(__float_as_uint(d), 0u);
-        });
+        }, loaded);
     }
 
     template <int NV, bool ISUMS>
@@ -796,8 +824,10 @@ struct TypeQ5_K {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         TypeQ4_K::stage_act(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
-        TypeQ4_K::stage_x(x, act, count, warp, nwarps, lane);
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
+        TypeQ4_K::stage_x(x, act, count, warp, nwarps, lane, loaded);
     }
 
     template <int NV, bool ISUMS>
@@ -885,8 +915,10 @@ struct TypeQ2_K {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         TypeQ6_K::stage_act(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
-        TypeQ6_K::stage_x(x, act, count, warp, nwarps, lane);
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
+        TypeQ6_K::stage_x(x, act, count, warp, nwarps, lane, loaded);
     }
 
     template <int NV, bool ISUMS>
@@ -971,8 +1003,10 @@ struct TypeQ3_K {
     __device__ static void stage_act(const uint8_t *xq, uint8_t *act, int nb, int nv, int tid, int nthr) {
         TypeQ6_K::stage_act(xq, act, nb, nv, tid, nthr);
     }
-    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane) {
-        TypeQ6_K::stage_x(x, act, count, warp, nwarps, lane);
+    template <class Loaded>
+    __device__ static void stage_x(const float *x, uint8_t *act, int count, int warp, int nwarps, int lane,
+                                   Loaded loaded) {
+        TypeQ6_K::stage_x(x, act, count, warp, nwarps, lane, loaded);
     }
 
     template <int NV, bool ISUMS>
