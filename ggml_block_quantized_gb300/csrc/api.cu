@@ -596,7 +596,7 @@ int run_gemv_mats(int type, GemvMat *mats, int n, int64_t n_in, int64_t n_vec, s
             if (e != cudaSuccess) {
                 char where[160];
                 std::snprintf(where, sizeof where, "%s; tensor-core grid %d block %d smem %d stages %d", g_launch_step,
-                              ml.grid, (ml.warps + 1) * 32, ml.smem, mp.n_stages);
+                              ml.grid, mma_warps(ml.mode, ml.warps) * 32, ml.smem, mp.n_stages);
                 return cuda_fail(e, where);
             }
             return QG_OK;

@@ -46,10 +46,19 @@
 //  * Consumers (NW warps): warp w takes blocks w, w+NW, ... of each stage's
 //    chunk for all 16 rows and accumulates the tile's partial outputs in
 //    registers across the chunks. After the tile's last chunk every warp
-//    stores its partials and counts itself in; the last warp to arrive adds
-//    the NW partials in a fixed warp order (deterministic) and writes y. With
-//    the partial buffers doubled it first releases the ring slot, so the
-//    refill does not wait.
+//    stores its partials to the stage's partial buffer before releasing the
+//    ring slot.
+//  * Register mode (8 consumer warps): a reducer warp adds a tile's NW
+//    partials in a fixed warp order (deterministic) and writes y once the
+//    slot of its last chunk is released, then marks the stage's partial
+//    buffer free; the producer refills no slot whose stage would write a
+//    buffer the reducer has not read yet. The CTA's final tile is added up by
+//    the last consumer warp to store its partials (same warp order), so the
+//    end of a short launch waits for no other warp.
+//  * Panel modes (16 consumer warps; a 19th warp would leave too few
+//    registers): the last consumer warp to store its partials adds up every
+//    tile. With the partial buffers doubled it first releases the ring slot,
+//    so the refill does not wait.
 //  * Full/empty mbarriers with bounded waits (about 1 s), as in the __dp4a
 //    kernel; programmatic dependent launch: the producer streams W while the
 //    previous kernel finishes, the consumers wait for it before reading the
@@ -68,7 +77,8 @@ namespace qg {
 enum MmaBMode : int { kMmaPanel16 = 0, kMmaPanel8 = 1, kMmaRegs = 2 };
 constexpr int kMmaTileRows = 16;
 constexpr int kMmaMaxStages = 8;
-constexpr int kMmaHeaderBytes = 2 * 8 * kMmaMaxStages + 4 * 2 * kMmaMaxStages;  // mbarriers, partial-buffer counters
+// mbarriers full[8], empty[8] | the final-tile counter (64 bytes) | mbarriers reduced[16]
+constexpr int kMmaHeaderBytes = 2 * 8 * kMmaMaxStages + 4 * 2 * kMmaMaxStages + 8 * 2 * kMmaMaxStages;
 constexpr int kMmaRecords = 8;              // fragment records per block
 constexpr int kMmaTailBytes = 256 + 32 + 32;  // per block: correction operands, d_x[8], block sums[8]
 // Bytes of one partial-output buffer: every consumer lane's 4 partial outputs.
@@ -601,9 +611,6 @@ __device__ __forceinline__ void mma_load_regs(const uint8_t *xq, int nb, int nv,
 }
 
 // ------------------------------------------------------------------ producer
-// The whole producer warp runs this: lane 0 waits for free slots and issues
-// the copies; after each tile's last stage is consumed all lanes add the
-// consumer warps' partial outputs (fixed order) and store y.
 // The tile's output: the NW warps' partials of buffer ri added in warp
 // order, stored to y (lane (g, t) holds rows g and g+8, vectors 2t, 2t+1 of
 // the mma tile, i.e. stage rows mma_stage_row(g), mma_stage_row(g + 8)).
@@ -683,30 +690,35 @@ __device__ __forceinline__ void mma_issue_copy(const MmaCopy &c, const uint8_t *
     if (c.a1 > c.a0) bulk_copy_g2s(smem_addr(dst), W + c.a0, static_cast<uint32_t>(c.a1 - c.a0), bar, policy);
 }
 
-template <class T, int MAXB>
+// The whole producer warp: lane 0 waits for free slots (and for the reducer
+// to have read the partial buffer the stage will write) and issues the copies.
+template <class T, bool RED, int MAXB>
 __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<MAXB> &b, uint8_t *ring,
-                                             uint32_t full0, uint32_t empty0, int lane) {
+                                             uint32_t full0, uint32_t empty0, uint32_t reduced0, int lane) {
     const uint64_t policy = l2_evict_first_policy();
-    const int S = p.n_stages;
+    const int S = p.n_stages, R = RED ? p.red_slots : (1 << 30);  // (no reducer: no partial-buffer waits)
     int cur = -1;
     const uint8_t *W = nullptr;
     int n_out = 0;
     MmaWalk walk = mma_cta_walk(p, b);
     MmaStage st;
     int issued = 0;
-    // slot = k mod S and phase = (k / S) & 1, kept incrementally
-    int slot = 0;
-    uint32_t phase = 0;
+    // slot = k mod S, phase = (k / S) & 1, rk = k mod R, rphase = (k / R - 1) & 1, kept incrementally
+    int slot = 0, rk = 0;
+    uint32_t phase = 0, rphase = 1;
     for (int k = 0; walk.next(b, p, st); ++k) {
         if (st.mat != cur) {  // the matrix's fields, read from the parameter table once
             cur = st.mat;
-            W = b.m[cur].W;
-            n_out = b.m[cur].n_out;
+            W = b.m[MAXB == 1 ? 0 : cur].W;
+            n_out = b.m[MAXB == 1 ? 0 : cur].n_out;
         }
         const MmaCopy cp = mma_plan_copy<T>(p, n_out, st, lane);  // before the slot is free
-        if (k >= S) {
+        if (k >= S || k >= R) {
             bool got = true;
-            if (lane == 0) got = mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1u);
+            if (lane == 0) {
+                if (k >= S) got = mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1u);
+                if (got && k >= R) got = mbar_wait_bounded(reduced0 + 8 * rk, rphase);
+            }
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
                 if (lane == 0) record_error(p.err, kErrProducerWait);
@@ -719,12 +731,16 @@ __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<
             slot = 0;
             phase ^= 1u;
         }
+        if (RED && ++rk == R) {
+            rk = 0;
+            rphase ^= 1u;
+        }
     }
     // Leave no copy in flight into this CTA's shared memory.
     for (int k = max(0, issued - S); k < issued; ++k) {
-        const int slot = k % S;
+        const int sk = k % S;
         bool got = true;
-        if (lane == 0) got = mbar_wait_bounded(full0 + 8 * slot, static_cast<uint32_t>((k / S) & 1));
+        if (lane == 0) got = mbar_wait_bounded(full0 + 8 * sk, static_cast<uint32_t>((k / S) & 1));
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
             if (lane == 0) record_error(p.err, kErrDrainWait);
@@ -733,20 +749,61 @@ __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<
     }
 }
 
+// The reducer warp: for each stage but the CTA's final one, once the
+// consumers have released it, the tile's outputs when it is the tile's last
+// chunk; then the stage's partial buffer is marked free.
+template <int NW, int MAXB>
+__device__ __forceinline__ void mma_reducer(const MmaParams &p, const MmaBatch<MAXB> &b, const float4 *red,
+                                            uint32_t empty0, uint32_t reduced0, int lane) {
+    const int S = p.n_stages, R = p.red_slots;
+    MmaWalk walk = mma_cta_walk(p, b);
+    MmaStage st;
+    int slot = 0, ri = 0;
+    uint32_t phase = 0;
+    while (walk.next(b, p, st)) {
+        if (st.last && walk.t >= walk.t1) break;  // the final stage: the consumers add it up
+        bool got = true;
+        if (lane == 0) got = mbar_wait_bounded(empty0 + 8 * slot, phase);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        __syncwarp();  // the partials, released with the slot, are seen by every lane
+        if (!got) {
+            if (lane == 0) record_error(p.err, kErrConsumerWait);
+            return;
+        }
+        if (st.last) {
+            const MmaMat &m = b.m[MAXB == 1 ? 0 : st.mat];
+            mma_finish_tile<NW>(p, red, ri, m.y, m.n_out, st.tile, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(reduced0 + 8 * ri);
+        if (++ri == R) ri = 0;
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ kernel
 // Shared memory: mbarriers | panel | partial outputs [red_slots][warps][32]
 // float4 | ring of n_stages stages.
+// Warps of a launch: NW consumers, the producer and, in register mode, the reducer.
+__host__ __device__ constexpr int mma_warps(int bmode, int nw) { return nw + (bmode == kMmaRegs ? 2 : 1); }
+
 template <class T, int BMODE, int NW, int MAXB>
-__global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaParams p, const MmaBatch<MAXB> b) {
+__global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(const MmaParams p, const MmaBatch<MAXB> b) {
     constexpr bool B16 = BMODE == kMmaPanel16;
     constexpr bool REGS = BMODE == kMmaRegs;
+    constexpr bool RED = REGS;  // a reducer warp
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t full0 = smem_addr(smem);
     const uint32_t empty0 = full0 + 8 * kMmaMaxStages;
+    const uint32_t reduced0 = full0 + 2 * 8 * kMmaMaxStages + 4 * 2 * kMmaMaxStages;
     uint8_t *pan = smem + kMmaHeaderBytes;
     float4 *red = reinterpret_cast<float4 *>(pan + p.panel_bytes);
-    int *red_count = reinterpret_cast<int *>(smem + 2 * 8 * kMmaMaxStages);  // per partial buffer
     uint8_t *ring = pan + p.panel_bytes + p.red_slots * mma_red_bytes(NW);
+    // warps done with the tile of each partial buffer (without a reducer), or with the final tile ([0])
+    int *red_count = reinterpret_cast<int *>(smem + 2 * 8 * kMmaMaxStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -757,14 +814,21 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaPar
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, NW);
         }
-        for (int r = 0; r < 2 * kMmaMaxStages; ++r) red_count[r] = 0;
+        for (int r = 0; r < p.red_slots; ++r) {
+            mbar_init(reduced0 + 8 * r, 1);
+            red_count[r] = 0;
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     pdl_allow_dependents();
 
     if (warp == NW) {
-        mma_producer<T, MAXB>(p, b, ring, full0, empty0, lane);
+        mma_producer<T, RED, MAXB>(p, b, ring, full0, empty0, reduced0, lane);
+        return;
+    }
+    if (RED && warp == NW + 1) {
+        mma_reducer<NW, MAXB>(p, b, red, empty0, reduced0, lane);
         return;
     }
 
@@ -778,8 +842,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaPar
     MmaWalk walk = mma_cta_walk(p, b);
     MmaStage st;
     int cur = -1;
-    float *y = nullptr;
-    int n_out = 0;
+    MmaStage fin = {};
+    int fin_ri = -1;  // partial buffer of the CTA's final tile
     constexpr int RB = 2;  // REGS: blocks a warp keeps (warp, warp + NW)
     uint32_t breg[RB][kMmaRecords][4];
     uint2 bcorr[RB], bdx[RB], bbs[RB];
@@ -792,15 +856,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaPar
 #pragma unroll
                 for (int i = 0; i < RB; ++i)
                     if (warp + i * NW < p.nb)
-                        mma_load_regs<T>(b.m[st.mat].xq, p.nb, p.nv, warp + i * NW, lane, breg[i], bcorr[i], bdx[i],
-                                         bbs[i]);
+                        mma_load_regs<T>(b.m[MAXB == 1 ? 0 : st.mat].xq, p.nb, p.nv, warp + i * NW, lane, breg[i],
+                                         bcorr[i], bdx[i], bbs[i]);
             } else {
                 if (cur >= 0) named_barrier(1, NW * 32);
-                mma_build_panel<T, B16>(p, b.m[st.mat].xq, pan, threadIdx.x, NW * 32);
+                mma_build_panel<T, B16>(p, b.m[MAXB == 1 ? 0 : st.mat].xq, pan, threadIdx.x, NW * 32);
                 named_barrier(1, NW * 32);
             }
-            y = b.m[st.mat].y;
-            n_out = b.m[st.mat].n_out;
             cur = st.mat;
         }
         if (!failed) {
@@ -842,36 +904,61 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) gemv_mma_kernel(const MmaPar
         }
         bool last_warp = false;
         if (st.last) {
-            // this warp's share of the tile; the last of the NW warps adds them up
+            // this warp's share of the tile, added up by the reducer warp (the
+            // CTA's final tile: by the last consumer warp, after the loop) or,
+            // without a reducer, by the last warp to get here
             red[(ri * NW + warp) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                last = atomicAdd(red_count + ri, 1) == NW - 1;
-            }
-            last_warp = __shfl_sync(0xffffffffu, last, 0);
-            if (last_warp) {
-                __threadfence_block();
-                const bool doubled = p.red_slots > S;
-                if (doubled && lane == 0) mbar_arrive(empty0 + 8 * slot);  // the slot is free already
-                if (!failed) mma_finish_tile<NW>(p, red, ri, y, n_out, st.tile, lane);
+            if (RED) {
+                if (walk.t >= walk.t1) {
+                    fin = st;
+                    fin_ri = ri;
+                }
+            } else {
                 __syncwarp();
+                int last = 0;
                 if (lane == 0) {
-                    red_count[ri] = 0;
-                    if (!doubled) mbar_arrive(empty0 + 8 * slot);
+                    __threadfence_block();
+                    last = atomicAdd(red_count + ri, 1) == NW - 1;
+                }
+                last_warp = __shfl_sync(0xffffffffu, last, 0);
+                __syncwarp();  // orders lane 0's observation before every lane's reads
+                if (last_warp) {
+                    __threadfence_block();
+                    const bool doubled = p.red_slots > S;
+                    if (doubled && lane == 0) mbar_arrive(empty0 + 8 * slot);  // the slot is free already
+                    const MmaMat &m = b.m[MAXB == 1 ? 0 : st.mat];
+                    if (!failed) mma_finish_tile<NW>(p, red, ri, m.y, m.n_out, st.tile, lane);
+                    __syncwarp();
+                    if (lane == 0) {
+                        red_count[ri] = 0;
+                        if (!doubled) mbar_arrive(empty0 + 8 * slot);
+                    }
                 }
             }
         }
-        if (!(st.last && last_warp)) {
+        if (!last_warp) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);  // releases the slot (and the partials)
         }
         if (++ri == p.red_slots) ri = 0;
         if (++slot == S) {
             slot = 0;
             phase ^= 1u;
+        }
+    }
+    if (RED && fin_ri >= 0) {  // the last warp to get here adds up the final tile
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(red_count, 1) == NW - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();  // orders lane 0's observation before every lane's reads
+        if (last) {
+            __threadfence_block();
+            const MmaMat &m = b.m[MAXB == 1 ? 0 : fin.mat];
+            mma_finish_tile<NW>(p, red, fin_ri, m.y, m.n_out, fin.tile, lane);
         }
     }
 }

@@ -31,7 +31,7 @@ inline cudaError_t mma_launch_inst(const MmaParams &p, const MmaMat *mats, int n
     auto k = gemv_mma_kernel<T, BM, NW, MAXB>;
     cudaError_t e = mma_smem_attr<T, BM, NW, MAXB>(k, device, l.smem_optin);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, l.grid, (NW + 1) * 32, l.smem, s, p, b);
+    return launch_pdl(k, l.grid, mma_warps(BM, NW) * 32, l.smem, s, p, b);
 }
 
 template <class T, int BM, int NW>
