@@ -48,13 +48,14 @@
 //    registers across the chunks. After the tile's last chunk every warp
 //    stores its partials to the stage's partial buffer before releasing the
 //    ring slot.
-//  * Register mode (8 consumer warps): a reducer warp adds a tile's NW
-//    partials in a fixed warp order (deterministic) and writes y once the
-//    slot of its last chunk is released, then marks the stage's partial
-//    buffer free; the producer refills no slot whose stage would write a
-//    buffer the reducer has not read yet. The CTA's final tile is added up by
-//    the last consumer warp to store its partials (same warp order), so the
-//    end of a short launch waits for no other warp.
+//  * Register mode (8 consumer warps, one chunk per tile): a reducer warp
+//    waits for each stage's release (the consumers' partials are in), adds
+//    the tile's NW partials in a fixed warp order (deterministic), writes y
+//    and then frees the slot for the producer on a second mbarrier. Because
+//    the producer refills a slot only after the reducer has seen its
+//    previous release, no waiter can miss an mbarrier phase. The CTA's final
+//    tile is added up by the last consumer warp to store its partials (same
+//    warp order), so the end of a short launch waits for no other warp.
 //  * Panel modes (16 consumer warps; a 19th warp would leave too few
 //    registers): the last consumer warp to store its partials adds up every
 //    tile. With the partial buffers doubled it first releases the ring slot,
@@ -77,7 +78,7 @@ namespace qg {
 enum MmaBMode : int { kMmaPanel16 = 0, kMmaPanel8 = 1, kMmaRegs = 2 };
 constexpr int kMmaTileRows = 16;
 constexpr int kMmaMaxStages = 8;
-// mbarriers full[8], empty[8] | the final-tile counter (64 bytes) | mbarriers reduced[16]
+// mbarriers full[8], empty[8] | partial-buffer counters (64 bytes) | mbarriers reduced[8] | pad
 constexpr int kMmaHeaderBytes = 2 * 8 * kMmaMaxStages + 4 * 2 * kMmaMaxStages + 8 * 2 * kMmaMaxStages;
 constexpr int kMmaRecords = 8;              // fragment records per block
 constexpr int kMmaTailBytes = 256 + 32 + 32;  // per block: correction operands, d_x[8], block sums[8]
@@ -690,22 +691,23 @@ __device__ __forceinline__ void mma_issue_copy(const MmaCopy &c, const uint8_t *
     if (c.a1 > c.a0) bulk_copy_g2s(smem_addr(dst), W + c.a0, static_cast<uint32_t>(c.a1 - c.a0), bar, policy);
 }
 
-// The whole producer warp: lane 0 waits for free slots (and for the reducer
-// to have read the partial buffer the stage will write) and issues the copies.
+// The whole producer warp: lane 0 waits for free slots (with a reducer: slots
+// the reducer has freed) and issues the copies.
 template <class T, bool RED, int MAXB>
 __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<MAXB> &b, uint8_t *ring,
                                              uint32_t full0, uint32_t empty0, uint32_t reduced0, int lane) {
     const uint64_t policy = l2_evict_first_policy();
-    const int S = p.n_stages, R = RED ? p.red_slots : (1 << 30);  // (no reducer: no partial-buffer waits)
+    const int S = p.n_stages;
+    const uint32_t free0 = RED ? reduced0 : empty0;  // where a slot's release is announced
     int cur = -1;
     const uint8_t *W = nullptr;
     int n_out = 0;
     MmaWalk walk = mma_cta_walk(p, b);
     MmaStage st;
     int issued = 0;
-    // slot = k mod S, phase = (k / S) & 1, rk = k mod R, rphase = (k / R - 1) & 1, kept incrementally
-    int slot = 0, rk = 0;
-    uint32_t phase = 0, rphase = 1;
+    // slot = k mod S and phase = (k / S) & 1, kept incrementally
+    int slot = 0;
+    uint32_t phase = 0;
     for (int k = 0; walk.next(b, p, st); ++k) {
         if (st.mat != cur) {  // the matrix's fields, read from the parameter table once
             cur = st.mat;
@@ -713,12 +715,9 @@ __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<
             n_out = b.m[MAXB == 1 ? 0 : cur].n_out;
         }
         const MmaCopy cp = mma_plan_copy<T>(p, n_out, st, lane);  // before the slot is free
-        if (k >= S || k >= R) {
+        if (k >= S) {
             bool got = true;
-            if (lane == 0) {
-                if (k >= S) got = mbar_wait_bounded(empty0 + 8 * slot, phase ^ 1u);
-                if (got && k >= R) got = mbar_wait_bounded(reduced0 + 8 * rk, rphase);
-            }
+            if (lane == 0) got = mbar_wait_bounded(free0 + 8 * slot, phase ^ 1u);
             got = __shfl_sync(0xffffffffu, got, 0);
             if (!got) {
                 if (lane == 0) record_error(p.err, kErrProducerWait);
@@ -730,10 +729,6 @@ __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<
         if (++slot == S) {
             slot = 0;
             phase ^= 1u;
-        }
-        if (RED && ++rk == R) {
-            rk = 0;
-            rphase ^= 1u;
         }
     }
     // Leave no copy in flight into this CTA's shared memory.
@@ -750,8 +745,8 @@ __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<
 }
 
 // The reducer warp: for each stage but the CTA's final one, once the
-// consumers have released it, the tile's outputs when it is the tile's last
-// chunk; then the stage's partial buffer is marked free.
+// consumers have released it, the tile's outputs; then the slot (and its
+// partial buffer) is marked free for the producer.
 template <int NW, int MAXB>
 __device__ __forceinline__ void mma_reducer(const MmaParams &p, const MmaBatch<MAXB> &b, const float4 *red,
                                             uint32_t empty0, uint32_t reduced0, int lane) {
@@ -775,7 +770,7 @@ __device__ __forceinline__ void mma_reducer(const MmaParams &p, const MmaBatch<M
             mma_finish_tile<NW>(p, red, ri, m.y, m.n_out, st.tile, lane);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(reduced0 + 8 * ri);
+        if (lane == 0) mbar_arrive(reduced0 + 8 * slot);
         if (++ri == R) ri = 0;
         if (++slot == S) {
             slot = 0;
@@ -814,10 +809,8 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, NW);
         }
-        for (int r = 0; r < p.red_slots; ++r) {
-            mbar_init(reduced0 + 8 * r, 1);
-            red_count[r] = 0;
-        }
+        for (int r = 0; r < p.red_slots; ++r) red_count[r] = 0;
+        for (int r = 0; r < S; ++r) mbar_init(reduced0 + 8 * r, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
