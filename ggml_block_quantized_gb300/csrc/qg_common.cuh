@@ -86,8 +86,9 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Wait for the phase of `bar` with the given parity, giving up after about
-// one second (checked every 256 polls) or 2^26 polls. Returns false on
-// timeout; the caller records the error and winds down.
+// one second (the clock is read every 16 polls) or 2^26 polls. Each poll may
+// suspend the thread until the phase completes (at most 20 us). Returns
+// false on timeout; the caller records the error and winds down.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kWaitLimitPolls = 1u << 26;
 
@@ -118,14 +119,6 @@ __device__ __forceinline__ void bulk_copy_g2s_plain(uint32_t dst, const void *sr
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
-}
-
-// 16-byte asynchronous copy global -> shared through the load/store unit.
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 // L2 policy: weights are streamed once, so let them be evicted first.
