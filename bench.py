@@ -39,6 +39,32 @@ UNIT = "GB/s"
 
 
 # ----------------------------------------------------------------- helpers
+# Replicas under torchrun: each rank runs the whole workload on its own GPU;
+# the timed regions start together and the job's time is its slowest rank's.
+def rank_barrier(world):
+    """All ranks meet here (nothing to do with one process)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(t, world, device="cpu"):
+    """The slowest rank's time, returned on every rank."""
+    if world <= 1:
+        return t
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_rate(units_per_step, steps, world, seconds, scale=1e9):
+    """Units that all ranks processed per second, over the slowest rank's
+    time (every rank processes units_per_step per step)."""
+    return units_per_step * steps * world / seconds / scale
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -288,8 +314,7 @@ def run_ours(args, rank, world, local_rank):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if sampler:
             sampler.start()
-        if world > 1:
-            torch.distributed.barrier()
+        rank_barrier(world)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
@@ -308,11 +333,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank)
     t, clocks = time_graph(g_step, args.steps, sampler)
-    if world > 1:
-        tt = torch.tensor([t], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t = float(tt.item())
-    value = wbytes * args.steps * world / t / 1e9
+    t = max_over_ranks(t, world, device)
+    value = whole_job_rate(wbytes, args.steps, world, t)
     ms_per_step = t / args.steps * 1e3
     assert qg.device_error() == 0, "a kernel reported a bounded-wait timeout"
     fused = 4 * nv * max(c["n_in"] for c in calls) <= 48 * 1024
@@ -389,14 +411,15 @@ def run_ours(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         g.replay()
     torch.cuda.synchronize()
+    rank_barrier(world)
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(e2e_reps):
             g.replay()
     torch.cuda.synchronize()
-    te = time.perf_counter() - t0
+    te = max_over_ranks(time.perf_counter() - t0, world, device)
     del g
-    e2e = {"value": round(wbytes * e2e_reps * world / te / 1e9, 1), "unit": UNIT,
+    e2e = {"value": round(whole_job_rate(wbytes, e2e_reps, world, te), 1), "unit": UNIT,
            "h2d_bytes_per_step": HX.numel() * 4, "d2h_bytes_per_step": HY.numel() * 4,
            "timing": "host wall clock around CUDA-graph replays (copy in, step, copy out) and the final sync"}
 
@@ -488,6 +511,7 @@ def run_prefill(args, rank, world, local_rank):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if sampler:
             sampler.start()
+        rank_barrier(world)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
@@ -496,13 +520,13 @@ def run_prefill(args, rank, world, local_rank):
             e1.record(stream)
         torch.cuda.synchronize()
         clocks = sampler.stop() if sampler else None
-        return e0.elapsed_time(e1) / 1e3, clocks
+        return max_over_ranks(e0.elapsed_time(e1) / 1e3, world, device), clocks
 
     g = graph(step)
     sampler = ClockSampler(local_rank)
     tt, clocks = timed(g, args.steps, sampler)
     calls = args.steps * len(Ws)
-    value = flops * calls / tt / 1e12
+    value = whole_job_rate(flops * len(Ws), args.steps, world, tt, 1e12)
     del g
     gg = graph(gemm_only)
     tg, _ = timed(gg, args.steps)
@@ -529,12 +553,13 @@ def run_prefill(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         ge.replay()
     torch.cuda.synchronize()
+    rank_barrier(world)
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(reps):
             ge.replay()
     torch.cuda.synchronize()
-    te = time.perf_counter() - t0
+    te = max_over_ranks(time.perf_counter() - t0, world, device)
     del ge
 
     cpu = None
@@ -560,12 +585,12 @@ def run_prefill(args, rank, world, local_rank):
                    "timing": "CUDA graph of one step, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
         "us_per_call": round(tt / calls * 1e6, 3),
-        "roofline": {"bound": "tensor", "kernel": "gemm_f16_tc_kernel 128x128x64 tiles (qgemm_f16)",
+        "roofline": {"bound": "tensor", "kernel": "gemm_f16_tc_kernel, 128-row x 128- or 256-token tiles (qgemm_f16)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "algorithmic_flops_per_launch": int(flops), "avg_launch_us": round(gemm_us, 3), "launches": 1},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(flops * reps / te / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_rate(flops, reps, world, te, 1e12), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": HX.numel() * 4, "d2h_bytes_per_step": HY.numel() * 4,
                 "timing": "host wall clock around CUDA-graph replays (copy in, qgemm, copy out) and the final sync"},
         "gpu_launches": 3 * calls, "clocks": clocks,
