@@ -337,8 +337,14 @@ def run_ours(args, rank, world, local_rank):
     value = whole_job_rate(wbytes, args.steps, world, t)
     ms_per_step = t / args.steps * 1e3
     assert qg.device_error() == 0, "a kernel reported a bounded-wait timeout"
-    fused = 4 * nv * max(c["n_in"] for c in calls) <= 48 * 1024
-    launches_per_step = (len(plans) if batched else len(calls)) * (1 if fused else 2)
+    # a product whose plan quantizes x in its prologue is one launch, else two
+    def launches_of(t, rows, n_in, n_mats):
+        return 1 if "fused-quantize" in qg.kernel_info(t, rows, n_in, nv, n_mats) else 2
+    if batched:
+        launches_per_step = sum(launches_of(t, sum(c["n_out"] for c in part), part[0]["n_in"], len(part))
+                                for t, part, _ in plans)
+    else:
+        launches_per_step = sum(launches_of(c["type"], c["n_out"], c["n_in"], 1) for c in calls)
     del g_step
 
     # ---- one qgemv call per matrix (stream-ordered, each call may depend on the previous)
@@ -349,7 +355,8 @@ def run_ours(args, rank, world, local_rank):
         tc, _ = time_graph(g, reps)
         del g
         per_call = {"value": round(wbytes * reps / tc / 1e9, 1), "unit": UNIT,
-                    "ms_per_step": round(tc / reps * 1e3, 4), "launches_per_step": len(calls) * (1 if fused else 2)}
+                    "ms_per_step": round(tc / reps * 1e3, 4),
+                    "launches_per_step": sum(launches_of(c["type"], c["n_out"], c["n_in"], 1) for c in calls)}
 
     # ---- per-kind breakdown: each kind's calls alone, one qgemv call each
     breakdown = {}

@@ -155,7 +155,7 @@ struct KnobDef {
 };
 constexpr KnobDef kKnobs[kKnobCount] = {
     {"QG_CTAS_PER_SM", 2, 1, 4},          {"QG_RING_KIB", 96, 16, 200}, {"QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1},
-    {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 48, 0, 1024},
+    {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 16, 0, 1024},
     {"QG_TC", 0, 0, 1},                   {"QG_FUSED_MAX_MIB", 1 << 20, 0, 1 << 20}};
 std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
 
@@ -520,9 +520,12 @@ int launch_quantize_batched(int act_type, const QuantTable &t, int n, void *xq, 
 }
 
 // Activations of at most this many f32 bytes per call (QG_FUSED_QUANT_KIB,
-// default 48 KiB) are quantized inside the GEMV's prologue (every CTA reads
-// x once); larger ones go through the separate quantization launch into the
-// workspace.
+// default 16 KiB) are quantized inside the GEMV's prologue (every CTA
+// quantizes all of x); larger ones go through the separate quantization
+// launch into the workspace. Every CTA's share of that prologue grows with
+// the blocks of x: measured on this GPU, a 4096-element x (16 KiB) is
+// faster quantized in the prologue, an 11008-element one (43 KiB) or two
+// vectors of 4096 (32 KiB) through the separate launch.
 int64_t fused_quant_max_bytes() { return static_cast<int64_t>(knob(kKnobFusedQuantKib)) * 1024; }
 
 bool fused_quantization(int64_t n_in, int64_t n_vec) { return 4 * n_in * n_vec <= fused_quant_max_bytes(); }

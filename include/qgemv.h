@@ -264,8 +264,9 @@ typedef struct {
 
 /* Workspace bytes qgemv_batched needs for n_mats matrices: 16 when the
  * activations are small enough to be quantized inside the product (4 *
- * n_in * n_vec <= 48 KiB, and not a tensor-core product: Q4_K or Q6_K with
- * n_vec >= 3), else the quantized activations of every matrix,
+ * n_in * n_vec <= QG_FUSED_QUANT_KIB, 16 KiB by default, and not a
+ * tensor-core product: Q4_K or Q6_K with n_vec >= 3), else the quantized
+ * activations of every matrix,
  * n_mats * qgemv_workspace_bytes(type, n_in, n_vec). 0 on a bad argument. */
 size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int n_mats);
 
