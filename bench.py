@@ -358,6 +358,32 @@ def run_ours(args, rank, world, local_rank):
                     "ms_per_step": round(tc / reps * 1e3, 4),
                     "launches_per_step": sum(launches_of(c["type"], c["n_out"], c["n_in"], 1) for c in calls)}
 
+    # ---- dequantize_rows on the same weights (the Q4_K 4096 x 4096
+    # workload's second operation): read W, write every element as f32;
+    # the outputs rotate through buffers larger than L2 together
+    dequant = None
+    if args.workload == "q4_k_4096":
+        c0 = calls[0]
+        n_el = c0["n_out"] * c0["n_in"]
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        n_outs = max(2, int(np.ceil(2 * l2 / (4 * n_el))))
+        outs = [torch.empty((c0["n_out"], c0["n_in"]), dtype=torch.float32, device=device) for _ in range(n_outs)]
+        seq = [(c["W"], outs[i % n_outs]) for i, c in enumerate(calls)]
+
+        def deq_step():
+            for w, o in seq:
+                qg.dequantize_rows(c0["type"], w, c0["n_out"], c0["n_in"], out=o, stream=stream)
+        g = capture(deq_step)
+        reps = max(3, args.steps // 4)
+        td, _ = time_graph(g, reps)
+        td = max_over_ranks(td, world, device)
+        del g, outs
+        per = td / (reps * len(seq))
+        moved = c0["W"].numel() + 4 * n_el
+        dequant = {"us_per_call": round(per * 1e6, 3), "bytes_per_call": int(moved),
+                   "GB_s": round(moved / per / 1e9, 1), "hbm_frac": round(moved / per / 1e9 / measured_peaks()[0], 4),
+                   "note": "read + write bytes over the time; outputs rotate through buffers larger than L2"}
+
     # ---- per-kind breakdown: each kind's calls alone, one qgemv call each
     breakdown = {}
     kinds = sorted({(c["kind"] if c["kind"] not in ("q", "k", "v", "o") else "qkvo") for c in calls})
@@ -450,7 +476,7 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "hbm_frac": round(value / world / peak, 4), "hbm_peak_gbs": peak,
         "us_per_token": round(ms_per_step * 1e3, 2),
-        "per_call": per_call, "breakdown": breakdown, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "per_call": per_call, "breakdown": breakdown, "dequantize_rows": dequant, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
     return line

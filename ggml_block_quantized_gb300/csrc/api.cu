@@ -761,7 +761,9 @@ int dequantize_rows(int type, const void *W, float *out, int64_t n_rows, int64_t
     if (st != QG_OK) return st;
     const int threads = 256;
     int64_t grid = (groups + threads - 1) / threads;
-    if (grid > static_cast<int64_t>(dev.sms) * 16) grid = static_cast<int64_t>(dev.sms) * 16;
+    // 32 CTAs of 256 threads per SM (two waves of resident CTAs; measured
+    // faster than 16 for the write-bound Q4_K 4096 x 4096 case)
+    if (grid > static_cast<int64_t>(dev.sms) * 32) grid = static_cast<int64_t>(dev.sms) * 32;
     const uint8_t *w = static_cast<const uint8_t *>(W);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const unsigned g = static_cast<unsigned>(grid);
@@ -937,7 +939,7 @@ int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int6
                                            ((static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255)));
     const int64_t groups = n_out * n_in / 8;
     int64_t grid = (groups + 255) / 256;
-    if (grid > static_cast<int64_t>(dev.sms) * 16) grid = static_cast<int64_t>(dev.sms) * 16;
+    if (grid > static_cast<int64_t>(dev.sms) * 32) grid = static_cast<int64_t>(dev.sms) * 32;
     cudaError_t e = launch_dequant(type, static_cast<const uint8_t *>(W), A, groups, static_cast<unsigned>(grid), 256, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill: dequantize to f16");
     e = launch_f32_to_f16(x, B, n_tok * n_in, dev.sms, s);

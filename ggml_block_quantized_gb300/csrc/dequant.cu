@@ -134,29 +134,34 @@ template <class O>
 __global__ void dequant_q4_k_kernel(const uint8_t *__restrict__ W, O *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        // the block's d, dmin and scales in two 8-byte loads, the group's 8
+        // codes in one (the 144-byte blocks keep W's 16-byte alignment)
         const uint8_t *blk = W + (g >> 5) * 144;
         const int e0 = 8 * static_cast<int>(g & 31);
         const int j = e0 >> 5;                      // sub-block
-        const float d = f16_bits_to_f32(ldg_u16(blk));
-        const float dmin = f16_bits_to_f32(ldg_u16(blk + 2));
-        const uint8_t *s = blk + 4;
+        const uint2 h0 = __ldg(reinterpret_cast<const uint2 *>(blk));      // d | dmin | scales[0..3]
+        const uint2 h1 = __ldg(reinterpret_cast<const uint2 *>(blk + 8));  // scales[4..11]
+        const float d = f16_bits_to_f32(h0.x);
+        const float dmin = f16_bits_to_f32(h0.x >> 16);
+        const uint32_t sw[3] = {h0.y, h1.x, h1.y};
+        auto s8 = [&](int k) { return static_cast<int>((sw[k >> 2] >> (8 * (k & 3))) & 0xFFu); };
         int sc, m;
         if (j < 4) {
-            sc = __ldg(s + j) & 63;
-            m = __ldg(s + j + 4) & 63;
+            sc = s8(j) & 63;
+            m = s8(j + 4) & 63;
         } else {
-            sc = (__ldg(s + j + 4) & 0xF) | ((__ldg(s + j - 4) >> 6) << 4);
-            m = (__ldg(s + j + 4) >> 4) | ((__ldg(s + j) >> 6) << 4);
+            sc = (s8(j + 4) & 0xF) | ((s8(j - 4) >> 6) << 4);
+            m = (s8(j + 4) >> 4) | ((s8(j) >> 6) << 4);
         }
         const int p = e0 & 63;                       // position in the 64-element chunk
-        const uint8_t *qs = blk + 16 + 32 * (e0 >> 6) + (p & 31);
+        const uint2 qw = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 32 * (e0 >> 6) + (p & 31)));
         const int shift = p >= 32 ? 4 : 0;
         const float dsc = __fmul_rn(d, static_cast<float>(sc));
         const float off = __fmul_rn(dmin, static_cast<float>(m));
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int q = (__ldg(qs + i) >> shift) & 0xF;
+            const int q = ((i < 4 ? qw.x : qw.y) >> (8 * (i & 3) + shift)) & 0xF;
             v[i] = __fsub_rn(__fmul_rn(dsc, static_cast<float>(q)), off);
         }
         store8(out + g * 8, v);
