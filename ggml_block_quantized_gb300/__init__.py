@@ -20,7 +20,7 @@ __all__ = [
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes",
     "qgemv", "qgemv_xq", "qgemv_block_isums", "qgemv_noalloc", "qgemv_batched",
     "qgemv_batched_workspace_bytes", "BatchPlan", "device_error", "kernel_info", "EXPORTED_SYMBOLS",
-    "MAX_BATCH",
+    "MAX_BATCH", "tune", "qgemm_workspace_bytes", "qgemm", "qgemm_f16", "selftest_bounded_wait",
 ]
 
 F32, F16, Q4_0, Q4_1, Q5_0, Q8_0, Q8_1 = 0, 1, 2, 3, 6, 8, 9
