@@ -448,8 +448,19 @@ def run_ours(args, rank, world, local_rank):
         # the later group overlap the earlier group's compute (every byte
         # still crosses between host and device each step).
         copy_stream = torch.cuda.Stream(device)
+        # with several vectors the copies are large: launches of at most 48
+        # matrices, so that the inputs exposed before the first launch and
+        # the outputs after the last are small (with one vector a smaller
+        # launch costs more than the copy it hides)
+        per_launch = 48 if nv > 2 else qg.MAX_BATCH
+        e2e_plans = []
+        for (t, n_in), cs in sorted(groups.items()):
+            for i in range(0, len(cs), per_launch):
+                part = cs[i:i + per_launch]
+                e2e_plans.append((t, part, qg.BatchPlan(t, [(c["W"], c["x"], c["y"], c["n_out"]) for c in part],
+                                                        n_in, nv)))
         spans = []
-        for _, part, _ in plans:
+        for _, part, _ in e2e_plans:
             x0 = min(c["x_off"] for c in part)
             x1 = max(c["x_off"] + c["x"].numel() for c in part)
             y0 = min(c["y_off"] for c in part)
@@ -468,7 +479,7 @@ def run_ours(args, rank, world, local_rank):
                     e.record(copy_stream)
                     arrived.append(e)
             done = []
-            for (_, _, plan), e in zip(plans, arrived):
+            for (_, _, plan), e in zip(e2e_plans, arrived):
                 stream.wait_event(e)
                 plan.run(stream)
                 d = torch.cuda.Event()
