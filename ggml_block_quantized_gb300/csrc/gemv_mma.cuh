@@ -380,14 +380,16 @@ struct MmaQ6_K {
         c[3] = static_cast<float>(bs[2 * t + 9]);
     }
 
-    // The two f16 lanes (bytes 0,2 when odd == 0, bytes 1,3 otherwise) of
-    // codes q = low nibble(s) | 2 high bits << 4, as subnormal bits.
-    __device__ __forceinline__ static uint32_t codes(uint32_t ql, uint32_t qh, int k, int odd) {
-        const int n = k >> 1;
-        const uint32_t lo = (ql >> (8 * odd + 4 * n)) & 0x000F000Fu;
-        const uint32_t hi = ((qh >> (8 * odd + 2 * k)) & 0x00030003u) << 4;
-        return lo | hi;
+    // The 4 codes q = low nibble | 2 high bits << 4 of one word (one code a
+    // byte); the mma operands take bytes 0,2 and bytes 1,3 of it as the
+    // f16 subnormal bits of two lanes.
+    __device__ __forceinline__ static uint32_t codes(uint32_t ql, uint32_t qh, int k) {
+        const uint32_t lo = (ql >> (4 * (k >> 1))) & 0x0F0F0F0Fu;
+        const uint32_t hi = k < 2 ? qh << (4 - 2 * k) : qh >> (2 * k - 4);  // bits 2k, 2k+1 to 4, 5
+        return lo | (hi & 0x30303030u);
     }
+    __device__ __forceinline__ static uint32_t even(uint32_t c) { return c & 0x00FF00FFu; }
+    __device__ __forceinline__ static uint32_t odd(uint32_t c) { return __byte_perm(c, 0u, 0x4341u); }
 
     template <class BS>
     __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
@@ -435,10 +437,9 @@ struct MmaQ6_K {
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
                     const int j = 8 * h + 2 * k + m;
+                    const uint32_t ca = codes(qla[m][k & 1], qha[m], k), cb = codes(qlb[m][k & 1], qhb[m], k);
                     float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    mma_16816(C, codes(qla[m][k & 1], qha[m], k, 0), codes(qlb[m][k & 1], qhb[m], k, 0),
-                              codes(qla[m][k & 1], qha[m], k, 1), codes(qlb[m][k & 1], qhb[m], k, 1), bf[2 * m],
-                              bf[2 * m + 1]);
+                    mma_16816(C, even(ca), even(cb), odd(ca), odd(cb), bf[2 * m], bf[2 * m + 1]);
                     const float2 f = fadd2(
                         make_float2(__uint_as_float(__byte_perm(swa[j >> 2], 0x4B000000u, 0x7540u | (j & 3))),
                                     __uint_as_float(__byte_perm(swb[j >> 2], 0x4B000000u, 0x7540u | (j & 3)))),
