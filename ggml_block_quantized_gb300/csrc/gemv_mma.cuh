@@ -872,14 +872,14 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
             const uint32_t sb = ring_a + static_cast<uint32_t>(slot * p.stage_bytes);
             // row sr of the stage: group sr/4 at sr/4 * gpitch, row sr%4 of it at
             // (sr%4) * rpitch, plus the copy's offset from its 16-byte window
-            const int64_t row0 = static_cast<int64_t>(st.tile) * kMmaTileRows;
-            const int64_t koff = static_cast<int64_t>(st.kc) * p.kb * T::kBlockBytes;
-            const int64_t ca = (p.contig ? row0 + (sra & ~3) : row0 + sra) * p.row_bytes + koff;
-            const int64_t cb = (p.contig ? row0 + (srb & ~3) : row0 + srb) * p.row_bytes + koff;
-            const uint32_t ra = sb + static_cast<uint32_t>((sra >> 2) * p.gpitch + (sra & 3) * p.rpitch) +
-                                static_cast<uint32_t>(ca & 15);
-            const uint32_t rb = sb + static_cast<uint32_t>((srb >> 2) * p.gpitch + (srb & 3) * p.rpitch) +
-                                static_cast<uint32_t>(cb & 15);
+            // only the offset modulo 16 is needed, so 32-bit (wrapping) products suffice
+            const uint32_t row0 = static_cast<uint32_t>(st.tile) * kMmaTileRows;
+            const uint32_t rbytes = static_cast<uint32_t>(p.row_bytes);
+            const uint32_t koff = static_cast<uint32_t>(st.kc * p.kb * T::kBlockBytes);
+            const uint32_t ca = (p.contig ? row0 + (sra & ~3) : row0 + sra) * rbytes + koff;
+            const uint32_t cb = (p.contig ? row0 + (srb & ~3) : row0 + srb) * rbytes + koff;
+            const uint32_t ra = sb + static_cast<uint32_t>((sra >> 2) * p.gpitch + (sra & 3) * p.rpitch) + (ca & 15u);
+            const uint32_t rb = sb + static_cast<uint32_t>((srb >> 2) * p.gpitch + (srb & 3) * p.rpitch) + (cb & 15u);
             const int kbt = min(p.kb, p.nb - st.kc * p.kb);
             const uint32_t rec0 = pan_a + static_cast<uint32_t>(st.kc * p.kb * p.rec_bytes);
             if (REGS) {
