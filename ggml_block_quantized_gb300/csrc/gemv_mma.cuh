@@ -23,7 +23,7 @@
 // the Q8_K block sums (bsums), and only d_w, dmin_w and d_x are inexact
 // floats -- the same arithmetic as the scalar definition up to f32 rounding.
 //
-// Structure (one CTA = 1 producer warp + NW consumer warps, one CTA per SM):
+// Structure (one CTA = NW consumer warps + 1 or 2 producer warps, one CTA per SM):
 //  * Work unit: a tile of 16 consecutive rows of one matrix. A CTA owns a
 //    balanced contiguous range of the launch's tiles (matrices of a batch
 //    numbered consecutively). Each tile is streamed as one or more chunks of
@@ -34,7 +34,8 @@
 //    a stage spans whole rows, a group's 4 rows are contiguous in W and
 //    travel as one copy (4 requests a stage; each bulk request costs the
 //    issuing thread on the order of 100 cycles); otherwise each row segment
-//    is its own copy. gpitch is 32 modulo 128 bytes and the mma rows are
+//    is its own copy (16 requests: panel modes split them over two
+//    producer warps). gpitch is 32 modulo 128 bytes and the mma rows are
 //    mapped to stage rows so that the 4 rows read by one 16-lane phase of a
 //    64-bit load lie in 4 different groups: their banks are distinct. A copy
 //    takes the 16-byte aligned window covering its bytes; bytes of W past its
@@ -56,8 +57,8 @@
 //    previous release, no waiter can miss an mbarrier phase. The CTA's final
 //    tile is added up by the last consumer warp to store its partials (same
 //    warp order), so the end of a short launch waits for no other warp.
-//  * Panel modes (16 consumer warps; a 19th warp would leave too few
-//    registers): the last consumer warp to store its partials adds up every
+//  * Panel modes (16 consumer warps and 2 producer warps; a 19th warp would
+//    leave too few registers): the last consumer warp to store its partials adds up every
 //    tile. With the partial buffers doubled it first releases the ring slot,
 //    so the refill does not wait.
 //  * Full/empty mbarriers with bounded waits (about 1 s), as in the __dp4a
@@ -637,35 +638,40 @@ __device__ __forceinline__ void mma_finish_tile(const MmaParams &p, const float4
     }
 }
 
-// One stage's copies for the whole producer warp: lane q copies row group q
-// (whole rows) or lane i row segment i. mma_plan_copy works out this lane's
-// window (it does not touch the slot, so it runs before the slot is free);
-// mma_issue_copy stores the bytes past W's last 16-byte boundary, announces
-// the stage's bytes on its barrier and issues the copy.
+// One stage's copies, shared by the NP producer warps: copy i = lane * NP + pw
+// of producer warp pw is row group i (whole rows) or row segment i. Each
+// bulk request costs its issuing thread on the order of 100 cycles, so with
+// 16 row segments a stage two warps issue in parallel. mma_plan_copy works
+// out this lane's window (it does not touch the slot, so it runs before the
+// slot is free); mma_issue_copy stores the bytes past W's last 16-byte
+// boundary, announces the warp's bytes on the stage's barrier (one arrival
+// per producer warp) and issues the copy.
 struct MmaCopy {
     int64_t a0, a1, e;  // window [a0, a1) of W by bulk copy, [a1, e) by plain loads
     uint32_t dst;       // slot offset of the window
-    uint32_t total;     // bytes by bulk copy, whole stage (every lane)
+    uint32_t total;     // bytes by bulk copy, this warp's part of the stage (every lane)
 };
 
-template <class T>
-__device__ __forceinline__ MmaCopy mma_plan_copy(const MmaParams &p, int n_out, const MmaStage &st, int lane) {
+template <class T, int NP>
+__device__ __forceinline__ MmaCopy mma_plan_copy(const MmaParams &p, int n_out, const MmaStage &st, int lane,
+                                                 int pw) {
     const int rows = min(kMmaTileRows, n_out - st.tile * kMmaTileRows);
     const int64_t row0 = static_cast<int64_t>(st.tile) * kMmaTileRows;
+    const int i = lane * NP + pw;
     MmaCopy c;
     int64_t s;
     bool mine;
     if (p.contig) {
-        mine = 4 * lane < rows;
-        s = (row0 + 4 * lane) * p.row_bytes;
-        c.e = s + static_cast<int64_t>(min(4, rows - 4 * lane)) * p.row_bytes;
-        c.dst = static_cast<uint32_t>(lane * p.gpitch);
+        mine = 4 * i < rows;
+        s = (row0 + 4 * i) * p.row_bytes;
+        c.e = s + static_cast<int64_t>(min(4, rows - 4 * i)) * p.row_bytes;
+        c.dst = static_cast<uint32_t>(i * p.gpitch);
     } else {
-        mine = lane < rows;
+        mine = i < rows;
         const int kbt = min(p.kb, p.nb - st.kc * p.kb);
-        s = (row0 + lane) * p.row_bytes + static_cast<int64_t>(st.kc) * p.kb * T::kBlockBytes;
+        s = (row0 + i) * p.row_bytes + static_cast<int64_t>(st.kc) * p.kb * T::kBlockBytes;
         c.e = s + static_cast<int64_t>(kbt) * T::kBlockBytes;
-        c.dst = static_cast<uint32_t>((lane >> 2) * p.gpitch + (lane & 3) * p.rpitch);
+        c.dst = static_cast<uint32_t>((i >> 2) * p.gpitch + (i & 3) * p.rpitch);
     }
     c.a0 = c.a1 = c.e = mine ? c.e : 0;
     if (mine) {
@@ -692,11 +698,13 @@ __device__ __forceinline__ void mma_issue_copy(const MmaCopy &c, const uint8_t *
     if (c.a1 > c.a0) bulk_copy_g2s(smem_addr(dst), W + c.a0, static_cast<uint32_t>(c.a1 - c.a0), bar, policy);
 }
 
-// The whole producer warp: lane 0 waits for free slots (with a reducer: slots
-// the reducer has freed) and issues the copies.
-template <class T, bool RED, int MAXB>
+// One producer warp (pw of NP): lane 0 waits for free slots (with a reducer:
+// slots the reducer has freed) and the warp issues its copies. A producer
+// cannot get a phase ahead of another: a slot is released only after its
+// stage's full barrier has all NP arrivals.
+template <class T, bool RED, int NP, int MAXB>
 __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<MAXB> &b, uint8_t *ring,
-                                             uint32_t full0, uint32_t empty0, uint32_t reduced0, int lane) {
+                                             uint32_t full0, uint32_t empty0, uint32_t reduced0, int lane, int pw) {
     const uint64_t policy = l2_evict_first_policy();
     const int S = p.n_stages;
     const uint32_t free0 = RED ? reduced0 : empty0;  // where a slot's release is announced
@@ -715,7 +723,7 @@ __device__ __forceinline__ void mma_producer(const MmaParams &p, const MmaBatch<
             W = b.m[MAXB == 1 ? 0 : cur].W;
             n_out = b.m[MAXB == 1 ? 0 : cur].n_out;
         }
-        const MmaCopy cp = mma_plan_copy<T>(p, n_out, st, lane);  // before the slot is free
+        const MmaCopy cp = mma_plan_copy<T, NP>(p, n_out, st, lane, pw);  // before the slot is free
         if (k >= S) {
             bool got = true;
             if (lane == 0) got = mbar_wait_bounded(free0 + 8 * slot, phase ^ 1u);
@@ -783,14 +791,17 @@ __device__ __forceinline__ void mma_reducer(const MmaParams &p, const MmaBatch<M
 // ------------------------------------------------------------------ kernel
 // Shared memory: mbarriers | panel | partial outputs [red_slots][warps][32]
 // float4 | ring of n_stages stages.
-// Warps of a launch: NW consumers, the producer and, in register mode, the reducer.
-__host__ __device__ constexpr int mma_warps(int bmode, int nw) { return nw + (bmode == kMmaRegs ? 2 : 1); }
+// Warps of a launch: NW consumers, then the producers (one in register mode,
+// two with a panel) and, in register mode, the reducer.
+__host__ __device__ constexpr int mma_producers(int bmode) { return bmode == kMmaRegs ? 1 : 2; }
+__host__ __device__ constexpr int mma_warps(int bmode, int nw) { return nw + mma_producers(bmode) + (bmode == kMmaRegs ? 1 : 0); }
 
 template <class T, int BMODE, int NW, int MAXB>
 __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(const MmaParams p, const MmaBatch<MAXB> b) {
     constexpr bool B16 = BMODE == kMmaPanel16;
     constexpr bool REGS = BMODE == kMmaRegs;
     constexpr bool RED = REGS;  // a reducer warp
+    constexpr int NP = mma_producers(BMODE);
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t full0 = smem_addr(smem);
     const uint32_t empty0 = full0 + 8 * kMmaMaxStages;
@@ -807,7 +818,7 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, NP);
             mbar_init(empty0 + 8 * s, NW);
         }
         for (int r = 0; r < p.red_slots; ++r) red_count[r] = 0;
@@ -817,11 +828,11 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
     __syncthreads();
     pdl_allow_dependents();
 
-    if (warp == NW) {
-        mma_producer<T, RED, MAXB>(p, b, ring, full0, empty0, reduced0, lane);
+    if (warp >= NW && warp < NW + NP) {
+        mma_producer<T, RED, NP, MAXB>(p, b, ring, full0, empty0, reduced0, lane, warp - NW);
         return;
     }
-    if (RED && warp == NW + 1) {
+    if (RED && warp == NW + NP) {
         mma_reducer<NW, MAXB>(p, b, red, empty0, reduced0, lane);
         return;
     }
