@@ -894,12 +894,15 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
             const int kbt = min(p.kb, p.nb - st.kc * p.kb);
             const uint32_t rec0 = pan_a + static_cast<uint32_t>(st.kc * p.kb * p.rec_bytes);
             if (REGS) {
-#pragma unroll
-                for (int i = 0; i < RB; ++i) {
-                    const int kb = warp + i * NW;
-                    if (kb < kbt)
-                        T::tile_block(ra + kb * T::kBlockBytes, rb + kb * T::kBlockBytes,
-                                      MmaRegB{breg[i], bcorr[i], bdx[i], bbs[i]}, lane, acc);
+                // both blocks in one straight-line sequence when the warp has
+                // two, so the scheduler can interleave their dependency chains
+                const uint32_t o0 = static_cast<uint32_t>(warp * T::kBlockBytes);
+                const uint32_t o1 = static_cast<uint32_t>((warp + NW) * T::kBlockBytes);
+                if (warp + NW < kbt) {
+                    T::tile_block(ra + o0, rb + o0, MmaRegB{breg[0], bcorr[0], bdx[0], bbs[0]}, lane, acc);
+                    T::tile_block(ra + o1, rb + o1, MmaRegB{breg[1], bcorr[1], bdx[1], bbs[1]}, lane, acc);
+                } else if (warp < kbt) {
+                    T::tile_block(ra + o0, rb + o0, MmaRegB{breg[0], bcorr[0], bdx[0], bbs[0]}, lane, acc);
                 }
             } else {
                 for (int kb = warp; kb < kbt; kb += NW)
