@@ -389,13 +389,14 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
     if (!found) {
         constexpr int W = 16;
         long best = -1;
-        const int cands[6] = {nb, 32, 24, 16, 8, 4};
+        constexpr int kCands = 9;
+        const int cands[kCands] = {nb, 32, 24, 16, 12, 11, 10, 8, 4};
         for (int f = 0; f < 2; ++f) {
             const bool b16 = f == 0;
             if (b16 && force == 8) continue;
             const int rec = mma_rec_bytes(b16);
             const int64_t panel = static_cast<int64_t>(nb) * rec;
-            for (int ci = 0; ci < 6; ++ci) {
+            for (int ci = 0; ci < kCands; ++ci) {
                 const int kb = cands[ci];
                 if (kb > nb || (ci > 0 && kb == nb)) continue;
                 if (tune_mma_kb() > 0 && kb > tune_mma_kb()) continue;
@@ -999,8 +1000,8 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
         MmaLaunch ml = {};
         if (plan_gemv_mma(type, tiles, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &mp, &ml) == QG_OK) {
             const char *mode = ml.mode == kMmaRegs ? "regs" : ml.mode == kMmaPanel16 ? "panel16" : "panel8";
-            std::snprintf(buf, sizeof buf, "gemv_mma_kernel<%s,%s,%dw> grid=%d stages=%d kb=%d smem=%d", tn, mode,
-                          ml.warps, ml.grid, mp.n_stages, mp.kb, ml.smem);
+            std::snprintf(buf, sizeof buf, "gemv_mma_kernel<%s,%s,%dw> grid=%d stages=%d kb=%d smem=%d partials=%d", tn,
+                          mode, ml.warps, ml.grid, mp.n_stages, mp.kb, ml.smem, mp.red_slots);
             return buf;
         }
     }

@@ -123,6 +123,39 @@ def test_mma_batched_equals_single_calls(t):
     assert qg.device_error() == 0
 
 
+@pytest.mark.parametrize("t", K_TYPES)
+def test_mma_forced_plans(t):
+    """Plans the automatic choice does not take for these shapes, forced with
+    the QG_MMA_PANEL / QG_MMA_KB knobs: the f16 and the int8 panel for short
+    rows, and 43-block rows in chunks of at most 12, 11, 10, 8 and 4 blocks
+    (rings of 2 to 8 stages, plain and doubled partial-output buffers). All
+    rows against the oracle."""
+    rng = np.random.default_rng(4500 + t)
+    cases = [(1, 0, 40, 768), (8, 0, 40, 768), (1, 0, 33, 4096), (8, 0, 33, 4096),
+             (0, 12, 31, 11008), (0, 11, 31, 11008), (0, 10, 47, 11008), (0, 8, 31, 11008), (0, 4, 17, 11008)]
+    for panel, kb, n_out, n_in in cases:
+        p0 = qg.tune("QG_MMA_PANEL", panel)
+        k0 = qg.tune("QG_MMA_KB", kb)
+        try:
+            info = qg.kernel_info(t, n_out, n_in, 8)
+            assert info.startswith("gemv_mma_kernel<"), info
+            if panel == 8:
+                assert ",panel8," in info, info
+            elif panel == 1:
+                assert ",panel" in info, info
+            if kb:
+                assert int(info.split(" kb=")[1].split()[0]) <= kb, info
+            W = synth.k_blocks(t, n_out * n_in // 256, rng)
+            for n_vec in (3, 8):
+                x = synth.f32_normal(rng, n_vec * n_in)
+                y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
+                check_y(t, W, x, y, n_out, n_in, n_vec)
+        finally:
+            qg.tune("QG_MMA_PANEL", p0)
+            qg.tune("QG_MMA_KB", k0)
+    assert qg.device_error() == 0
+
+
 def test_kernel_choice_is_reported():
     """The tensor-core kernel is the one planned for Q4_K/Q6_K from 3 vectors,
     the __dp4a kernel below that and for Q8_0/Q4_0."""
