@@ -227,7 +227,7 @@ int item_lpbs(int type, int (&out)[2]) {
 int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int smem_limit, GemvParams *p,
               GemvLaunch *l) {
     int elems, bytes;
-    block_info(type, &elems, &bytes);
+    if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
     const int64_t nb = n_in / elems;
     const int64_t row_bytes = nb * bytes;
     const size_t ring_target = static_cast<size_t>(tune_ring_kib()) * 1024;
@@ -353,7 +353,7 @@ bool mma_ring(int64_t smem_limit, int64_t fixed, int64_t stage, int nw, int *S, 
 int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, int smem_limit, MmaParams *p,
                   MmaLaunch *l) {
     int elems, bytes;
-    block_info(type, &elems, &bytes);
+    if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
     const int64_t nb64 = n_in / elems;
     if (nb64 < 1 || nb64 > 4096 || total_tiles < 1) return QG_ERR_SHAPE;
     const int nb = static_cast<int>(nb64);
@@ -488,7 +488,7 @@ int check_weight_type(int type) {
 
 int check_gemv_shape(int type, int64_t n_out, int64_t n_in, int64_t n_vec) {
     int elems, bytes;
-    block_info(type, &elems, &bytes);
+    if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
     if (n_out < 0 || n_in < 0 || n_out > INT32_MAX) return QG_ERR_SHAPE;
     if (n_vec < 1 || n_vec > QG_MAX_NVEC) return QG_ERR_SHAPE;
     if (n_in % elems != 0 || n_in / elems > INT32_MAX / 4) return QG_ERR_SHAPE;
@@ -833,7 +833,7 @@ int qgemv(int type, const void *W, const float *x, float *y, int64_t n_out, int6
         return run_gemv(type, W, nullptr, y, nullptr, n_out, n_in, n_vec, dev, s, x);
     const int at = qtype_act_type(type);
     int elems, bytes;
-    block_info(at, &elems, &bytes);
+    if (!block_info(at, &elems, &bytes)) return QG_ERR_PAIR;
     st = launch_quantize(at, x, workspace, n_in / elems * n_vec, dev.sms, s);
     if (st != QG_OK) return st;
     return run_gemv(type, W, workspace, y, nullptr, n_out, n_in, n_vec, dev, s);
@@ -882,7 +882,7 @@ int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, i
     GemvMat gm[QG_MAX_BATCH];
     const int at = qtype_act_type(type);
     int elems, bytes;
-    block_info(at, &elems, &bytes);
+    if (!block_info(at, &elems, &bytes)) return QG_ERR_PAIR;
     const int64_t blocks_per_mat = n_in / elems * n_vec;
     if (!fused) {
         QuantTable t = {};
@@ -905,7 +905,7 @@ int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, i
 size_t qgemm_workspace_bytes(int type, int64_t n_out, int64_t n_in, int64_t n_tok) {
     if (check_weight_type(type) != QG_OK) return 0;
     int elems, bytes;
-    block_info(type, &elems, &bytes);
+    if (!block_info(type, &elems, &bytes)) return 0;
     if (n_out < 0 || n_in < 0 || n_tok < 0 || n_out > INT32_MAX || n_tok > INT32_MAX || n_in % elems != 0) return 0;
     const size_t a = (static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255);
     const size_t b = (static_cast<size_t>(2 * n_tok * n_in) + 255) & ~size_t(255);
@@ -917,7 +917,7 @@ int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     int st = check_weight_type(type);
     if (st != QG_OK) return st;
     int elems, bytes;
-    block_info(type, &elems, &bytes);
+    if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
     if (n_out < 0 || n_in < 0 || n_tok < 0 || n_out > INT32_MAX || n_tok > INT32_MAX || n_in % elems != 0 ||
         n_in > INT32_MAX)
         return QG_ERR_SHAPE;
@@ -972,7 +972,7 @@ int qgemm_f16(const void *A, const void *B, float *y, int64_t n_out, int64_t n_t
 }
 
 const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_t n_vec, int n_mats) {
-    static thread_local char buf[160];
+    static thread_local char buf[320];  // room for "cuda: " and a whole CUDA error string
     buf[0] = 0;
     if (check_weight_type(type) != QG_OK || check_gemv_shape(type, total_rows, n_in, n_vec) != QG_OK) return buf;
     if (n_mats < 1 || n_mats > QG_MAX_BATCH || total_rows < 1 || n_in < 1) return buf;
@@ -1109,7 +1109,7 @@ extern "C" int qgemv_noalloc(int type, const void *W, const float *x, float *y, 
     // quantization launched just before it, so nothing needs clearing.
     const int at = qtype_act_type(type);
     int elems, bytes;
-    block_info(at, &elems, &bytes);
+    if (!block_info(at, &elems, &bytes)) return QG_ERR_PAIR;
     st = launch_quantize(at, x, scratch, n_in / elems * n_vec, dev.sms, s);
     if (st != QG_OK) return st;
     return run_gemv(type, W, scratch, y, nullptr, n_out, n_in, n_vec, dev, s);
