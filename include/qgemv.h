@@ -324,7 +324,9 @@ int qgemm_f16(const void *A, const void *B, float *y, int64_t n_out, int64_t n_t
 /* Which kernel and launch plan a product over n_mats matrices with
  * total_rows rows in all (row length n_in, n_vec vectors) would use on the
  * current device, as one line of text for logs and benchmarks, e.g.
- * "gemv_mma_kernel<Q4_K,regs,8w> grid=152 stages=5 smem=226048". The string
+ * "gemv_mma_kernel<Q4_K,regs,8w> grid=152 stages=5 kb=16 smem=226240
+ * partials=10" (mode, consumer warps, CTAs, ring stages, blocks per stage
+ * row, shared memory, partial-output buffers). The string
  * belongs to the library (per host thread, overwritten by the next call).
  * Returns "" on a bad argument or when the shape has no plan; "cuda: ..." on
  * a CUDA error. Launches nothing. */
@@ -333,8 +335,10 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
 /* Sets a tuning knob for the rest of the process (the pages have no
  * counterpart; the knobs choose between kernels that compute the same
  * product). name is one of the environment variables the library reads once
- * at first use: QG_CTAS_PER_SM, QG_RING_KIB, QG_MMA_MIN_NVEC, QG_MMA_PANEL,
- * QG_MMA_KB, QG_FUSED_QUANT_KIB (f32 x of at most this many KiB is quantized
+ * at first use: QG_CTAS_PER_SM, QG_RING_KIB, QG_MMA_MIN_NVEC (vectors from
+ * which Q4_K/Q6_K use the tensor cores), QG_MMA_PANEL (0 automatic, 1 a
+ * shared-memory activation panel, 8 the int8 panel), QG_MMA_KB (longest
+ * chunk of blocks a panel-mode stage takes; 0 no limit), QG_FUSED_QUANT_KIB (f32 x of at most this many KiB is quantized
  * inside the GEMV), QG_FUSED_MAX_MIB (... for a single matrix of at most this
  * many MiB of blocks; default: no limit), QG_TC (the tcgen05 Q4_K kernel for three or
  * more vectors, rows of 2048 or 4096 elements: 0 never, the default; 1
