@@ -453,10 +453,15 @@ def run_ours(args, rank, world, local_rank):
         # the outputs after the last are small (with one vector a smaller
         # launch costs more than the copy it hides)
         per_launch = 48 if nv > 2 else qg.MAX_BATCH
+        # the step's first launch may be shorter (--e2e-head matrices), so that
+        # the compute starts after a small part of the inputs has arrived
         e2e_plans = []
-        for (t, n_in), cs in sorted(groups.items()):
-            for i in range(0, len(cs), per_launch):
-                part = cs[i:i + per_launch]
+        for gi, ((t, n_in), cs) in enumerate(sorted(groups.items())):
+            i = 0
+            while i < len(cs):
+                n = args.e2e_head if gi == 0 and i == 0 and args.e2e_head > 0 else per_launch
+                part = cs[i:i + n]
+                i += n
                 e2e_plans.append((t, part, qg.BatchPlan(t, [(c["W"], c["x"], c["y"], c["n_out"]) for c in part],
                                                         n_in, nv)))
         spans = []
@@ -736,6 +741,8 @@ def main():
                              "q4_1_32000", "q5_0_32000", "q2_k_32000", "q3_k_32000", "q5_k_32000",
                              "prefill_q4_k_4096"])
     ap.add_argument("--n-vec", type=int, default=1)
+    ap.add_argument("--e2e-head", type=int, default=8,
+                    help="matrices in the end-to-end step's first launch (0: as many as the others)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
     ap.add_argument("--layers", type=int, default=None,
                     help="decoder layers of the stack (default 32; fewer only for profiling captures)")
