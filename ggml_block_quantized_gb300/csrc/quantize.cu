@@ -31,6 +31,23 @@
 
 namespace qg {
 
+// Float to int as the lesson's Java code casts it: truncation toward zero,
+// 0 for NaN, the int range's end beyond it (a NaN element, or a scale so
+// small that 1/d overflows, reaches those cases). Written out rather than
+// left to the conversion instruction's own NaN and overflow rules.
+__device__ __forceinline__ int java_f2i(float t) {
+    if (t != t) return 0;
+    if (t >= 2147483648.0f) return 2147483647;
+    if (t <= -2147483648.0f) return -2147483647 - 1;
+    return static_cast<int>(t);
+}
+
+// Two 4-bit codes into one byte: the low 4 bits of each (a code below 0
+// comes only from -inf and keeps its low bits, 0).
+__device__ __forceinline__ uint8_t pack_nibbles(int lo, int hi) {
+    return static_cast<uint8_t>((static_cast<uint32_t>(lo) & 0xFu) | ((static_cast<uint32_t>(hi) & 0xFu) << 4));
+}
+
 __device__ __forceinline__ float warp_max_abs(float a) {
     // fmaxf ignores NaN, as the scalar rule's comparison does
 #pragma unroll
@@ -105,10 +122,10 @@ __device__ __forceinline__ void q4_0_block(const float *xb, uint8_t *ob, int lan
     const float d = mx / -8.0f;
     const float id = d != 0.0f ? 1.0f / d : 0.0f;
     const float t = __fadd_rn(__fmul_rn(v, id), 8.5f);
-    int code = static_cast<int>(t);  // truncation toward zero, t >= 0
+    int code = java_f2i(t);
     code = code < 15 ? code : 15;
     const int hi = __shfl_down_sync(0xffffffffu, code, 16);
-    if (lane < 16) ob[2 + lane] = static_cast<uint8_t>(code | (hi << 4));
+    if (lane < 16) ob[2 + lane] = pack_nibbles(code, hi);
     if (lane == 0) *reinterpret_cast<unsigned short *>(ob) = __half_as_ushort(__float2half_rn(d));
 }
 
@@ -149,10 +166,10 @@ __device__ __forceinline__ void q4_1_block(const float *xb, uint8_t *ob, int lan
     const float d = __fsub_rn(mx, mn) / 15.0f;
     const float id = d != 0.0f ? 1.0f / d : 0.0f;
     const float t = __fadd_rn(__fmul_rn(__fsub_rn(v, mn), id), 0.5f);
-    int code = t != t ? 0 : static_cast<int>(t);  // truncation toward zero, t >= 0
+    int code = java_f2i(t);
     code = code < 15 ? code : 15;
     const int hi = __shfl_down_sync(0xffffffffu, code, 16);
-    if (lane < 16) ob[4 + lane] = static_cast<uint8_t>(code | (hi << 4));
+    if (lane < 16) ob[4 + lane] = pack_nibbles(code, hi);
     if (lane == 0) {
         const uint32_t dbits = __half_as_ushort(__float2half_rn(d));
         const uint32_t mbits = __half_as_ushort(__float2half_rn(mn));
@@ -185,11 +202,11 @@ __device__ __forceinline__ void q5_0_block(const float *xb, uint8_t *ob, int lan
     const float d = signed_max(v, lane) / -16.0f;
     const float id = d != 0.0f ? 1.0f / d : 0.0f;
     const float t = __fadd_rn(__fmul_rn(v, id), 16.5f);
-    int code = t != t ? 0 : static_cast<int>(t);
+    int code = java_f2i(t);
     code = code < 31 ? code : 31;
-    const uint32_t qh = __ballot_sync(0xffffffffu, (code >> 4) & 1);
+    const uint32_t qh = __ballot_sync(0xffffffffu, (static_cast<uint32_t>(code) >> 4) & 1u);
     const int hi = __shfl_down_sync(0xffffffffu, code, 16);
-    if (lane < 16) ob[6 + lane] = static_cast<uint8_t>((code & 0xF) | ((hi & 0xF) << 4));
+    if (lane < 16) ob[6 + lane] = pack_nibbles(code, hi);
     if (lane == 0) {
         unsigned short *h = reinterpret_cast<unsigned short *>(ob);
         h[0] = __half_as_ushort(__float2half_rn(d));

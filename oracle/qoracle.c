@@ -251,6 +251,18 @@ void or_quantize_q8_0(const float *x, uint8_t *out, int64_t n) {
     }
 }
 
+/* The float-to-int cast of the lesson's Java code ([lesson21] Examples 5, 7
+ * and 8 are Java): truncation toward zero, 0 for NaN, and the int range's end
+ * for values beyond it. C leaves (int) undefined for NaN and out-of-range
+ * values, so the cast is written out. A NaN element, or a block whose scale
+ * is so small that 1/d overflows to infinity, reaches these cases. */
+static int or_java_f2i(float f) {
+    if (isnan(f)) return 0;
+    if (f >= 2147483648.0f) return INT32_MAX;
+    if (f <= -2147483648.0f) return INT32_MIN;
+    return (int)f;
+}
+
 /* Q4_0 ([lesson21] Example 5, [rml] A worked example: Q4_0): per block the
  * FIRST element of strictly largest magnitude gives max (a later tie does
  * not replace it), d = max / -8, id = 1/d (0 when d == 0), code =
@@ -272,13 +284,14 @@ void or_quantize_q4_0(const float *x, uint8_t *out, int64_t n) {
         for (int j = 0; j < 32; ++j) {
             float scaled = xb[j] * id;
             float shifted = scaled + 8.5f;
-            int c = (int)shifted; /* truncation toward zero; shifted >= 0 */
+            int c = or_java_f2i(shifted);
             code[j] = c < 15 ? c : 15;
         }
         or_block_q4_0 blk;
         blk.d = or_f32_to_f16(d);
+        /* low 4 bits of each code (a code below 0 comes only from -inf) */
         for (int j = 0; j < 16; ++j)
-            blk.qs[j] = (uint8_t)(code[j] | (code[j + 16] << 4));
+            blk.qs[j] = (uint8_t)((code[j] & 0x0F) | ((code[j + 16] & 0x0F) << 4));
         memcpy(out + b * 18, &blk, 18);
     }
 }
@@ -303,14 +316,14 @@ void or_quantize_q4_1(const float *x, uint8_t *out, int64_t n) {
             float diff = xb[j] - mn;
             float scaled = diff * id;
             float shifted = scaled + 0.5f;
-            int c = isnan(shifted) ? 0 : (int)shifted; /* truncation toward zero; shifted >= 0 */
+            int c = or_java_f2i(shifted);
             code[j] = c < 15 ? c : 15;
         }
         or_block_q4_1 blk;
         blk.d = or_f32_to_f16(d);
         blk.m = or_f32_to_f16(mn);
         for (int j = 0; j < 16; ++j)
-            blk.qs[j] = (uint8_t)(code[j] | (code[j + 16] << 4));
+            blk.qs[j] = (uint8_t)((code[j] & 0x0F) | ((code[j + 16] & 0x0F) << 4));
         memcpy(out + b * 20, &blk, 20);
     }
 }
@@ -336,13 +349,13 @@ void or_quantize_q5_0(const float *x, uint8_t *out, int64_t n) {
         for (int j = 0; j < 32; ++j) {
             float scaled = xb[j] * id;
             float shifted = scaled + 16.5f;
-            int c = isnan(shifted) ? 0 : (int)shifted;
+            int c = or_java_f2i(shifted);
             code[j] = c < 31 ? c : 31;
         }
         or_block_q5_0 blk;
         blk.d = or_f32_to_f16(d);
         uint32_t qh = 0;
-        for (int j = 0; j < 32; ++j) qh |= (uint32_t)((code[j] >> 4) & 1) << j;
+        for (int j = 0; j < 32; ++j) qh |= (((uint32_t)code[j] >> 4) & 1u) << j;
         for (int i = 0; i < 4; ++i) blk.qh[i] = (uint8_t)(qh >> (8 * i));
         for (int j = 0; j < 16; ++j)
             blk.qs[j] = (uint8_t)((code[j] & 0x0F) | ((code[j + 16] & 0x0F) << 4));

@@ -231,6 +231,38 @@ def test_lesson21_example5_q4_0_signed_max_and_nibbles():
         assert float(back[31]) == pytest.approx(float(g[f"ex5_{tag}_max"]), rel=1e-3)
 
 
+def test_q4_0_nan_and_overflowing_inverse_follow_the_java_cast():
+    """Lesson 21's Q4_0 quantizer (Example 5) is Java: its (int) cast truncates,
+    gives 0 for NaN and saturates at the int range; a NaN element is skipped
+    by the signed max (the comparison is false) and gets code 0, as candle's
+    special-value table ("一些边界值") also has it. Bytes derived by hand."""
+    # NaN first, then 1.0, then zeros: max = 1.0, d = -0.125 (f16 0xB000),
+    # id = -8; NaN -> 0, 1.0 -> (int)0.5 = 0, 0.0 -> (int)8.5 = 8.
+    x = np.zeros(32, np.float32)
+    x[0], x[1] = np.nan, 1.0
+    q = oracle.quantize(oracle.Q4_0, x).tobytes()
+    assert q == bytes([0x00, 0xB0, 0x80, 0x80] + [0x88] * 14)
+    # max = 2^-146 (a subnormal): d = -2^-149, 1/d overflows to -inf, so
+    # 2^-146 * id = -inf -> int minimum -> low nibble 0; -2^-147 * id = +inf
+    # -> int maximum -> min(15, .) = 15; 0 * id = NaN -> 0. d rounds to f16 -0.
+    x = np.zeros(32, np.float32)
+    x[0], x[1] = np.float32(2.0 ** -146), np.float32(-(2.0 ** -147))
+    q = oracle.quantize(oracle.Q4_0, x).tobytes()
+    assert q == bytes([0x00, 0x80, 0x00, 0x0F] + [0x00] * 14)
+
+
+def test_q4_1_nan_element_gets_code_0():
+    """Lesson 21's Q4_1 (Example 7, Java): NaN fails both the min and the max
+    comparison, so min = 0 and max = 1 here; its code is (int)NaN = 0."""
+    x = np.zeros(32, np.float32)
+    x[0], x[1] = np.nan, 1.0
+    q = oracle.quantize(oracle.Q4_1, x).tobytes()
+    d = np.float32(1.0) / np.float32(15.0)
+    assert q[0:2] == np.float16(d).tobytes() and q[2:4] == bytes(2)
+    # 1.0: (1 - 0) * id + 0.5 rounds to 15.5 -> 15; zeros: 0.5 -> 0
+    assert q[4] == 0x00 and q[5] == 0x0F and q[6:] == bytes(14)
+
+
 # --------------------------------------------- lesson 21 seeded Java examples
 def java_pairs(seed, n, scale_a=0.02):
     r = JavaRandom(seed)
