@@ -42,6 +42,12 @@ __global__ void selftest_wait_kernel(int32_t *err) {
     if (!mbar_wait_bounded(b, 0u)) record_error(err, kErrConsumerWait);
 }
 
+// Does nothing. quantize_rows launches it after the weight quantizer without
+// programmatic dependent launch, so it starts only once the weights are
+// written and visible; a product enqueued next, which may start streaming W
+// while the kernel before it finishes, then reads finished weights.
+__global__ void stream_order_kernel() {}
+
 namespace {
 
 thread_local char g_last_cuda_error[256] = "";
@@ -745,7 +751,14 @@ int quantize_rows(int type, const float *x, void *out, int64_t n_rows, int64_t n
     DeviceInfo dev;
     int st = current_device(&dev);
     if (st != QG_OK) return st;
-    return launch_quantize(type, x, out, n_blocks, dev.sms, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = launch_quantize(type, x, out, n_blocks, dev.sms, s);
+    if (st != QG_OK) return st;
+    // the products read W before waiting for the kernel ahead of them: end
+    // with a kernel that starts only after the weights are complete
+    stream_order_kernel<<<1, 32, 0, s>>>();
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? QG_OK : cuda_fail(e, "stream-order launch");
 }
 
 int dequantize_rows(int type, const void *W, float *out, int64_t n_rows, int64_t n_in, qg_stream_t stream) {
@@ -1102,6 +1115,10 @@ extern "C" int qgemv_noalloc(int type, const void *W, const float *x, float *y, 
     GemvLaunch pl = {};
     st = plan_gemv(type, n_out, n_in, static_cast<int>(n_vec), dev.sms, dev.smem_optin, &probe, &pl);
     if (st != QG_OK) return st;
+    // where qgemv quantizes x inside the product it needs no memory at all:
+    // the same single launch, and the array is not touched
+    if (fused_single(type, n_out, n_in, n_vec))
+        return run_gemv(type, W, nullptr, y, nullptr, n_out, n_in, n_vec, dev, s, x);
     void *scratch = nullptr;
     st = noalloc_scratch(dev.device, &scratch);
     if (st != QG_OK) return st;

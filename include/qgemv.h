@@ -27,11 +27,15 @@
  *     no call synchronizes. Argument errors are returned before anything is
  *     enqueued. A CUDA launch error is returned as QG_ERR_CUDA.
  *   - Kernels launched by these calls use programmatic dependent launch: a
- *     qgemv call may begin reading W while the previous call on the same
- *     stream is still finishing. W must therefore not be written by the call
- *     immediately before on the same stream (any other stream-ordered work
- *     in between, such as a copy or an ordinary kernel, restores full
- *     ordering). x, y and the workspace follow ordinary stream order.
+ *     product may begin streaming W while the kernel enqueued before it on
+ *     the same stream is still finishing. quantize_rows provides for this
+ *     (its last kernel starts only after the weights are written), so a
+ *     product may directly follow the quantize_rows call that writes its W.
+ *     A kernel of the caller's own that writes W must not be the last work
+ *     enqueued before the product on that stream; any other stream-ordered
+ *     work in between (another library call, a copy, an ordinary kernel)
+ *     restores full ordering. x, y and the workspace follow ordinary stream
+ *     order.
  *   - Inputs with NaN or inf are outside the contract of the product; the
  *     quantizers map NaN to code 0 and let an infinite scale through, as
  *     [candle] "一些边界值" (special values) shows.
@@ -141,7 +145,13 @@ int quantize_act(int act_type, const float *x, void *xq, int64_t n_in, int64_t n
  *   QG_Q5_0: Q4_0's signed max, d = max / -16, code = min(31, (int)(x * id +
  *     16.5f)); the low 4 bits in nibbles as Q4_0, bit 4 of code j in bit j of
  *     the little-endian 32-bit word qh.
- * x: f32 [n_rows][n_in]; out: n_rows * qtype_nbytes(type, n_in) bytes. */
+ *   (int) is the cast of the lesson's Java code: truncation toward zero, 0
+ *   for NaN, the int range's end beyond it; a code below 0 (only from -inf,
+ *   when 1/d overflows for a subnormal max) keeps its low bits, 0.
+ * x: f32 [n_rows][n_in]; out: n_rows * qtype_nbytes(type, n_in) bytes.
+ * Enqueues the quantizer and then one empty kernel launched without
+ * programmatic dependent launch, so that a product enqueued next on the
+ * stream, which starts streaming W early, sees the finished weights. */
 int quantize_rows(int type, const float *x, void *out, int64_t n_rows, int64_t n_in,
                   qg_stream_t stream);
 
@@ -237,6 +247,10 @@ int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, i
  * need more (qgemv_workspace_bytes(type, n_in, n_vec) > 262144) return
  * QG_ERR_WORKSPACE and enqueue nothing. The call allocates nothing.
  *
+ * Where qgemv would quantize x inside the product's own launch (small x,
+ * see QG_FUSED_QUANT_KIB) this call does the same and does not touch the
+ * array.
+ *
  * All calls on a device share that array. Calls ordered on one stream are
  * safe. Calls that may run at the same time on the GPU (different streams,
  * or different host threads without ordering between them) race on it and
@@ -244,9 +258,12 @@ int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, i
  * byte a call reads is written earlier in the same call, so nothing needs
  * clearing.
  *
- * The first call on each device, with that device current, looks up the
- * array's device address (cudaGetSymbolAddress) and keeps it. Make that
- * first call before any stream capture that includes this function. */
+ * The first call on each device that uses the array, with that device
+ * current, looks up the array's device address (cudaGetSymbolAddress) and
+ * keeps it for the life of the process. Make that first call before any
+ * stream capture that includes this function. A device reset
+ * (cudaDeviceReset, or a reset of the primary context) frees the array and
+ * leaves the kept address stale: do not call this function after one. */
 int qgemv_noalloc(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in,
                   int64_t n_vec, qg_stream_t stream);
 

@@ -132,14 +132,21 @@ def test_quantize_rows_bit_exact(t):
     x[::32] = -8.0
     assert np.array_equal(host(qg.quantize_rows(t, dev(x), 64)), oracle.quantize(t, x))
     if t in (qg.Q4_1, qg.Q5_0):
-        # off-centre blocks (Q4_1's min at work) and NaN / inf elements, which
-        # both sides define: NaN is skipped by min/max and gives code 0
+        # off-centre blocks (Q4_1's min at work)
         x = synth.f32_normal(rng, 32 * 64) + np.float32(3)
         assert np.array_equal(host(qg.quantize_rows(t, dev(x), 64)), oracle.quantize(t, x))
-        for bad in (np.nan, np.inf, -np.inf):
-            x = synth.f32_normal(rng, 32 * 8)
-            x[[3, 100, 101]] = bad
-            assert np.array_equal(host(qg.quantize_rows(t, dev(x), 8)), oracle.quantize(t, x)), bad
+    # NaN / inf elements, which both sides define (NaN is skipped by the max
+    # or min/max and gets code 0; the cast is Java's)
+    for bad in (np.nan, np.inf, -np.inf):
+        x = synth.f32_normal(rng, 32 * 8)
+        x[[3, 100, 101]] = bad
+        assert np.array_equal(host(qg.quantize_rows(t, dev(x), 8)), oracle.quantize(t, x)), bad
+    # subnormal blocks: for the smallest maxima d is tiny or 0 and 1/d may
+    # overflow to infinity (codes from +-inf and NaN through the Java cast)
+    k = np.arange(32 * 40)
+    x = (rng.integers(-12, 13, k.size) * np.exp2(-149.0 + (k // 32) % 20)).astype(np.float32)
+    x[::97] = np.nan
+    assert np.array_equal(host(qg.quantize_rows(t, dev(x), 40)), oracle.quantize(t, x))
 
 
 # ------------------------------------------------------------- dequantize
@@ -390,6 +397,48 @@ def test_chained_calls_keep_stream_order():
         return torch.stack(outs)
 
     assert torch.equal(run2(False), run2(True))
+
+
+@pytest.mark.parametrize("t", LEGACY)
+def test_quantize_rows_then_product_without_sync(t):
+    """quantize_rows writes W and the product that streams W is enqueued
+    directly behind it, with no sync in between (the product starts reading
+    W before the kernel ahead of it has finished): it must read the new
+    weights, not the bytes the buffer held before. One matrix of 32000 x 4096
+    with one vector (x quantized in the product's prologue) and with eight
+    (a separate activation launch in between), then a batched call over
+    three freshly written matrices."""
+    rng = np.random.default_rng(910 + t)
+    n_out, n_in = 32000, 4096
+    w = synth.f32_normal(rng, n_out * n_in, 0.02)
+    W_host = oracle.quantize(t, w)
+    wd = dev(w)
+    for n_vec in (1, 8):
+        x = synth.f32_normal(rng, n_vec * n_in)
+        xd = dev(x)
+        Wd = torch.full((W_host.size,), 0x7B, dtype=torch.uint8, device="cuda")  # stale bytes
+        torch.cuda.synchronize()
+        qg.quantize_rows(t, wd, n_out, out=Wd)
+        y = qg.qgemv(t, Wd, xd, n_out, n_in, n_vec)
+        torch.cuda.synchronize()
+        assert torch.equal(y, qg.qgemv(t, Wd, xd, n_out, n_in, n_vec)), n_vec
+        assert np.array_equal(host(Wd), W_host)
+        check_y(t, W_host, x, host(y), n_out, n_in, n_vec, sample_rows(n_out, rng, 64))
+    # batched: three matrices, each written by its own quantize_rows call
+    n_outs = [4096, 11008, 4096]
+    ws = [synth.f32_normal(rng, n * n_in, 0.02) for n in n_outs]
+    xs = [dev(synth.f32_normal(rng, n_in)) for _ in n_outs]
+    Wds = [torch.full((oracle.type_nbytes(t, n_in) * n,), 0x7B, dtype=torch.uint8, device="cuda")
+           for n in n_outs]
+    ys = [torch.full((1, n), np.nan, device="cuda") for n in n_outs]
+    wds = [dev(a) for a in ws]
+    torch.cuda.synchronize()
+    for wdm, Wd, n in zip(wds, Wds, n_outs):
+        qg.quantize_rows(t, wdm, n, out=Wd)
+    qg.qgemv_batched(t, list(zip(Wds, xs, ys, n_outs)), n_in, 1)
+    torch.cuda.synchronize()
+    for Wd, xd, y, n in zip(Wds, xs, ys, n_outs):
+        assert torch.equal(y, qg.qgemv(t, Wd, xd, n, n_in, 1))
 
 
 def test_graph_capture_replay_matches_eager():
