@@ -268,6 +268,9 @@ def qgemv_noalloc(t: int, W, x, n_out: int, n_in: int, n_vec: int = 1, y=None, s
     _dev_tensor(W, torch.uint8, "W")
     _dev_tensor(x, torch.float32, "x")
     _need(x, 4 * n_vec * n_in, "x")
+    if x.device.index != torch.cuda.current_device():
+        # the C call plans for and takes the array of the current device
+        raise ValueError("qgemv_noalloc: x is not on the current CUDA device")
     if y is None:
         y = torch.empty((n_vec, n_out), dtype=torch.float32, device=x.device)
     _dev_tensor(y, torch.float32, "y")
