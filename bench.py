@@ -263,6 +263,167 @@ def time_oracle(sample, n_vec, budget_s=12.0):
     return done_bytes / t_total / 1e9, cores, f"{ncalls} of the step's qgemv calls (first layers), n_vec={n_vec}"
 
 
+# ------------------------------------------------- every workload, one line
+SINGLE_CONFIGS = ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000"]   # the four single-matrix workloads
+OTHER_TYPES = ["q4_1_32000", "q5_0_32000", "q2_k_32000", "q3_k_32000", "q5_k_32000"]
+
+
+def time_single_calls(qg, timer, t, n_out, n_in, nv, W, x, peak, reps=10):
+    """One qgemv call per weight copy, the copies rotating through more than
+    4x L2 so every call streams W from HBM; returns the per-call figures."""
+    import torch
+    dev = W.device
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(1, int(np.ceil(4 * l2 / W.numel())))
+    Ws = [W] + [W.clone() for _ in range(copies - 1)]
+    y = torch.empty((nv, n_out), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, qg.qgemv_workspace_bytes(t, n_in, nv)), dtype=torch.uint8, device=dev)
+
+    def fn():
+        for Wc in Ws:
+            qg.qgemv(t, Wc, x, n_out, n_in, nv, y=y, workspace=ws, stream=timer.stream)
+    g = timer.capture(fn)
+    tt, _ = timer.time(g, reps)
+    del g, Ws
+    per = tt / (reps * copies)
+    gbs = W.numel() / per / 1e9
+    info = qg.kernel_info(t, n_out, n_in, nv, 1)
+    return {"us_per_call": round(per * 1e6, 3), "GB_s": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "launches_per_call": 1 if "fused-quantize" in info else 2, "kernel": info,
+            "weight_bytes": int(W.numel()), "copies_rotated": copies}
+
+
+def measure_single_workloads(qg, synth, timer, device, peak, names):
+    """Each single-matrix workload at one and eight vectors (same weights)."""
+    import torch
+    out = {}
+    for name in names:
+        m = synth.single_matrix(name, n_vec=8)
+        t, n_out, n_in = m["type"], m["n_out"], m["n_in"]
+        if "w_f32" in m:
+            W = qg.quantize_rows(t, torch.from_numpy(m["w_f32"]).to(device), n_out, stream=timer.stream)
+        else:
+            W = torch.from_numpy(m["w_blocks"]).to(device)
+        x8 = torch.from_numpy(m["x"]).to(device)
+        torch.cuda.synchronize()
+        row = {"shape": f"{qg.TYPE_NAMES[t]} {n_out}x{n_in}"}
+        for nv in (1, 8):
+            row[f"n_vec={nv}"] = time_single_calls(qg, timer, t, n_out, n_in, nv, W, x8[:nv * n_in], peak)
+        if name == "q4_k_4096":
+            row["dequantize_rows"] = time_dequantize(qg, timer, t, n_out, n_in, W, peak)
+        out[name] = row
+        del W, x8, m
+        torch.cuda.synchronize()
+    return out
+
+
+def time_dequantize(qg, timer, t, n_out, n_in, W, peak, reps=10):
+    """dequantize_rows, read + write bytes over the time; weight copies and
+    outputs rotate through buffers larger than L2."""
+    import torch
+    dev = W.device
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_el = n_out * n_in
+    n_outs = max(2, int(np.ceil(2 * l2 / (4 * n_el))))
+    outs = [torch.empty((n_out, n_in), dtype=torch.float32, device=dev) for _ in range(n_outs)]
+    Ws = [W] + [W.clone() for _ in range(max(1, int(np.ceil(2 * l2 / W.numel()))) - 1)]
+    seq = [(Ws[i % len(Ws)], outs[i % n_outs]) for i in range(max(len(Ws), n_outs))]
+
+    def fn():
+        for w, o in seq:
+            qg.dequantize_rows(t, w, n_out, n_in, out=o, stream=timer.stream)
+    g = timer.capture(fn)
+    td, _ = timer.time(g, reps)
+    del g, outs, Ws
+    per = td / (reps * len(seq))
+    moved = W.numel() + 4 * n_el
+    return {"us_per_call": round(per * 1e6, 3), "bytes_per_call": int(moved), "GB_s": round(moved / per / 1e9, 1),
+            "frac": round(moved / per / 1e9 / peak, 4),
+            "note": "read + write bytes over the time; weights and outputs rotate through buffers larger than L2"}
+
+
+def layer_groups(calls):
+    """One decoder layer's launches in dependency order: q/k/v batched, o,
+    gate/up batched, down (calls are in layer order, 7 per layer)."""
+    out = []
+    for base in range(0, len(calls), 7):
+        lc = calls[base:base + 7]
+        out += [lc[0:3], lc[3:4], lc[4:6], lc[6:7]]
+    return out
+
+
+def time_decode_chain(qg, timer, calls, nv, wbytes, peak, reps):
+    """The stack as a decoder runs it: every launch waits for the one before
+    it on the stream (q/k/v batched, o, gate/up batched, down per layer)."""
+    import torch
+    dev = calls[0]["W"].device
+    ws = torch.empty(max(qg.qgemv_workspace_bytes(c["type"], c["n_in"], nv) for c in calls) * 3,
+                     dtype=torch.uint8, device=dev)
+    steps, launches = [], 0
+    for grp in layer_groups(calls):
+        c0 = grp[0]
+        if len(grp) == 1:
+            steps.append(("one", c0))
+        else:
+            steps.append(("batch", qg.BatchPlan(c0["type"], [(c["W"], c["x"], c["y"], c["n_out"]) for c in grp],
+                                                c0["n_in"], nv, workspace=ws)))
+        info = qg.kernel_info(c0["type"], sum(c["n_out"] for c in grp), c0["n_in"], nv, len(grp))
+        launches += 1 if "fused-quantize" in info else 2
+
+    def fn():
+        for kind, v in steps:
+            if kind == "one":
+                qg.qgemv(v["type"], v["W"], v["x"], v["n_out"], v["n_in"], nv, y=v["y"], workspace=ws,
+                         stream=timer.stream)
+            else:
+                v.run(timer.stream)
+    g = timer.capture(fn)
+    tt, _ = timer.time(g, reps)
+    del g
+    gbs = wbytes * reps / tt / 1e9
+    return {"value": round(gbs, 1), "unit": "GB/s", "frac": round(gbs / peak, 4),
+            "ms_per_step": round(tt / reps * 1e3, 4), "launches_per_step": launches,
+            "api": "per layer: qgemv_batched(q, k, v), qgemv(o), qgemv_batched(gate, up), qgemv(down); "
+                   "stream-ordered, each launch after the previous one"}
+
+
+class GraphTimer:
+    """CUDA-graph capture and CUDA-event timing on one stream."""
+
+    def __init__(self, stream, world, device):
+        self.stream, self.world, self.device = stream, world, device
+
+    def capture(self, fn):
+        import torch
+        with torch.cuda.stream(self.stream):
+            fn()  # eager warm-up on the capture stream
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            fn()
+        return g
+
+    def time(self, g, reps, sampler=None):
+        import torch
+        with torch.cuda.stream(self.stream):
+            for _ in range(2):
+                g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if sampler:
+            sampler.start()
+        rank_barrier(self.world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(self.stream)
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        return max_over_ranks(e0.elapsed_time(e1) / 1e3, self.world, self.device), clocks
+
+
 # --------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -299,33 +460,8 @@ def run_ours(args, rank, world, local_rank):
         for c in (calls if sel is None else sel):
             qg.qgemv(c["type"], c["W"], c["x"], c["n_out"], c["n_in"], nv, y=c["y"], workspace=ws, stream=stream)
 
-    def capture(fn):
-        with torch.cuda.stream(stream):
-            fn()  # eager warm-up on the capture stream
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            fn()
-        return g
-
-    def time_graph(g, reps, sampler=None):
-        with torch.cuda.stream(stream):
-            for _ in range(2):
-                g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if sampler:
-            sampler.start()
-        rank_barrier(world)
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        clocks = sampler.stop() if sampler else None
-        return e0.elapsed_time(e1) / 1e3, clocks
+    timer = GraphTimer(stream, 1, device)  # per-rank times; the headline takes the max over ranks below
+    capture, time_graph = timer.capture, timer.time
 
     step = step_batched if batched else step_calls
     g_step = capture(step)
@@ -387,6 +523,7 @@ def run_ours(args, rank, world, local_rank):
                    "note": "read + write bytes over the time; outputs rotate through buffers larger than L2"}
 
     # ---- per-kind breakdown: each kind's calls alone, one qgemv call each
+    peak, peak_kind = measured_peaks()
     breakdown = {}
     kinds = sorted({(c["kind"] if c["kind"] not in ("q", "k", "v", "o") else "qkvo") for c in calls})
     for kind in kinds:
@@ -398,7 +535,8 @@ def run_ours(args, rank, world, local_rank):
         c0 = sel[0]
         breakdown[kind] = {"shape": f"{qg.TYPE_NAMES[c0['type']]} {c0['n_out']}x{c0['n_in']}",
                            "calls_per_step": len(sel), "us_per_call": round(tk / reps / len(sel) * 1e6, 3),
-                           "GB_s": round(b * reps / tk / 1e9, 1)}
+                           "GB_s": round(b * reps / tk / 1e9, 1), "frac": round(b * reps / tk / 1e9 / peak, 4),
+                           "kernel": qg.kernel_info(c0["type"], c0["n_out"], c0["n_in"], nv, 1)}
         del g
 
     # ---- roofline of the dominant kernel: the launch that streams the most
@@ -430,6 +568,68 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": committed_traffic(f"{kernel_key}@{args.workload}", kernel_family(desc)),
                 "algorithmic_bytes_per_launch": int(per_launch), "avg_launch_us": round(avg_dur * 1e6, 3),
                 "launches": launches}
+
+    # ---- every workload of the benchmark in the same line: the four
+    # single-matrix workloads and the other weight types at one and eight
+    # vectors, dequantize_rows, the stack at eight vectors, and the stack as
+    # a decoder runs it (dependency-ordered launches)
+    configs = None
+    if batched and args.configs:
+        import torch as _t
+        from ggml_block_quantized_gb300 import synth
+        t_cfg = time.perf_counter()
+        configs = {}
+        chain_reps = max(3, args.steps // 4)
+        configs["decode_chain"] = {f"n_vec={nv}": time_decode_chain(qg, timer, calls, nv, wbytes, peak, chain_reps)}
+        if nv == 1 and args.layers in (None, synth.N_LAYERS):
+            nv8 = 8
+            xs8 = [synth.layer_x(layer, m, nv8) for layer in range(synth.N_LAYERS)
+                   for m in range(len(synth.LAYER_MATRICES))]
+            X8 = _t.from_numpy(np.concatenate(xs8)).to(device)
+            Y8 = _t.empty(sum(nv8 * c["n_out"] for c in calls), dtype=_t.float32, device=device)
+            calls8, xo, yo = [], 0, 0
+            for c, xh in zip(calls, xs8):
+                c8 = dict(c)
+                c8["x"] = X8[xo:xo + xh.size]
+                c8["y"] = Y8[yo:yo + nv8 * c["n_out"]].view(nv8, c["n_out"])
+                xo += xh.size
+                yo += nv8 * c["n_out"]
+                calls8.append(c8)
+            del xs8
+            groups8 = {}
+            for c in calls8:
+                groups8.setdefault((c["type"], c["n_in"]), []).append(c)
+            plans8 = []
+            for (ty8, n_in8), cs in sorted(groups8.items()):
+                for i in range(0, len(cs), qg.MAX_BATCH):
+                    part = cs[i:i + qg.MAX_BATCH]
+                    plans8.append((ty8, part, qg.BatchPlan(ty8, [(c["W"], c["x"], c["y"], c["n_out"]) for c in part],
+                                                           n_in8, nv8)))
+            g = capture(lambda: [pl.run(stream) for _, _, pl in plans8])
+            t8, _ = time_graph(g, chain_reps)
+            del g
+            d_t, d_calls, d_plan = max(plans8, key=lambda pl: weight_bytes(pl[1]))
+            g = capture(lambda: d_plan.run(stream))
+            tg8, _ = time_graph(g, 10)
+            del g
+            alg8 = sum(c["W"].numel() + 4 * nv8 * (c["n_in"] + c["n_out"]) for c in d_calls)
+            desc8 = qg.kernel_info(d_t, sum(c["n_out"] for c in d_calls), d_calls[0]["n_in"], nv8, len(d_calls))
+            v8 = wbytes * chain_reps / t8 / 1e9
+            configs["layer_stack_n_vec=8"] = {
+                "value": round(v8, 1), "unit": UNIT, "frac": round(v8 / peak, 4),
+                "ms_per_step": round(t8 / chain_reps * 1e3, 4),
+                "api": "qgemv_batched (one launch per type and row length)",
+                "roofline": {"bound": "hbm", "kernel": desc8 + " (batched launch)",
+                             "achieved": round(alg8 / (tg8 / 10) / 1e9, 1), "peak": peak, "unit": "GB/s",
+                             "frac": round(alg8 / (tg8 / 10) / 1e9 / peak, 4),
+                             "traffic": committed_traffic(f"{desc8.split(' ')[0]}@layer_stack_nv8",
+                                                          kernel_family(desc8)),
+                             "algorithmic_bytes_per_launch": int(alg8), "avg_launch_us": round(tg8 / 10 * 1e6, 3)}}
+            configs["decode_chain"]["n_vec=8"] = time_decode_chain(qg, timer, calls8, nv8, wbytes, peak, chain_reps)
+            del plans8, calls8, groups8, X8, Y8
+            _t.cuda.synchronize()
+        configs.update(measure_single_workloads(qg, synth, timer, device, peak, SINGLE_CONFIGS + OTHER_TYPES))
+        configs["seconds"] = round(time.perf_counter() - t_cfg, 1)
 
     # ---- end to end through the public API with host buffers: each step
     # copies all of its x in from pinned host memory (one copy) and all of
@@ -536,7 +736,8 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "hbm_frac": round(value / world / peak, 4), "hbm_peak_gbs": peak,
         "us_per_token": round(ms_per_step * 1e3, 2),
-        "per_call": per_call, "breakdown": breakdown, "dequantize_rows": dequant, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "per_call": per_call, "breakdown": breakdown, "dequantize_rows": dequant, "configs": configs,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
     return line
@@ -744,6 +945,8 @@ def main():
     ap.add_argument("--e2e-head", type=int, default=8,
                     help="matrices in the end-to-end step's first launch (0: as many as the others)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the other workloads measured beside the stack (configs object)")
     ap.add_argument("--layers", type=int, default=None,
                     help="decoder layers of the stack (default 32; fewer only for profiling captures)")
     args = ap.parse_args()

@@ -139,14 +139,21 @@ def single_matrix(name: str, n_vec: int = 1, n_out: int = None, n_in: int = None
     return out
 
 
+def layer_x(layer: int, m: int, n_vec: int = 1) -> np.ndarray:
+    """The activations of matrix m of decoder layer `layer` alone (the first
+    n_in values are the same for every n_vec)."""
+    n_in = LAYER_MATRICES[m][3]
+    xr = np.random.default_rng([2000 + workload_index("layer_stack"), layer, m])
+    return f32_normal(xr, n_vec * n_in)
+
+
 def layer_matrix(layer: int, m: int, n_vec: int = 1):
     """Matrix m (index into LAYER_MATRICES) of decoder layer `layer`."""
     name, t, n_out, n_in = LAYER_MATRICES[m]
     idx = workload_index("layer_stack")
     wr = np.random.default_rng([1000 + idx, layer, m])
-    xr = np.random.default_rng([2000 + idx, layer, m])
     return dict(name=name, type=t, n_out=n_out, n_in=n_in, n_vec=n_vec,
-                w_blocks=k_blocks(t, n_out * n_in // 256, wr), x=f32_normal(xr, n_vec * n_in))
+                w_blocks=k_blocks(t, n_out * n_in // 256, wr), x=layer_x(layer, m, n_vec))
 
 
 def layer_stack_bytes() -> int:
