@@ -825,6 +825,17 @@ def run_prefill(args, rank, world, local_rank):
     gg = graph(gemm_only)
     tg, _ = timed(gg, args.steps)
     del gg
+    # the same calls with Q4_K dequantized inside the GEMM (no f16 copy of W)
+    prev = qg.tune("QG_FUSED_GEMM", 1)
+    try:
+        gf = graph(step)
+        tf, _ = timed(gf, args.steps)
+        del gf
+    finally:
+        qg.tune("QG_FUSED_GEMM", prev)
+    fused = {"us_per_call": round(tf / calls * 1e6, 3), "TFLOP_s": round(whole_job_rate(flops * len(Ws), args.steps,
+                                                                                          world, tf, 1e12), 2),
+             "note": "qgemm with QG_FUSED_GEMM=1: x to f16, then one GEMM that expands Q4_K blocks in shared memory"}
     gemm_us = tg / calls * 1e6
     achieved = flops / (tg / calls) / 1e12
     try:
@@ -878,7 +889,7 @@ def run_prefill(args, rank, world, local_rank):
                    "l2": "weights rotate through distinct buffers > 4x L2",
                    "timing": "CUDA graph of one step, CUDA events on the launching stream",
                    "parallelism": f"replicas x{world}"},
-        "us_per_call": round(tt / calls * 1e6, 3),
+        "us_per_call": round(tt / calls * 1e6, 3), "fused_dequant": fused,
         "roofline": {"bound": "tensor", "kernel": "gemm_f16_tc_kernel, 128-row x 128- or 256-token tiles (qgemm_f16)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None,

@@ -25,6 +25,8 @@ cudaError_t launch_dequant(int type, const uint8_t *w, O *out, int64_t groups, u
 cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, cudaStream_t s);
 cudaError_t launch_gemm_f16_tc(const __half *A, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
                                int32_t *err, int sms, int device, cudaStream_t s);
+cudaError_t launch_gemm_q4k_fused(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
+                                  int64_t K, int32_t *err, int sms, int device, cudaStream_t s);
 cudaError_t launch_gemv_tc_q4_k(const TcParams &p, const TcMat *mats, int n, int grid, int smem, int smem_optin,
                                 int device, cudaStream_t s);
 
@@ -143,7 +145,10 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 //    sets no limit: in-kernel quantization measured faster at every size);
 //  QG_TC: the tcgen05 Q4_K kernel for three or more vectors -- 0 never (the
 //    default: the mma.sync kernel measured faster on this GPU), 1 whenever its
-//    shared memory fits (rows of 8 or 16 blocks).
+//    shared memory fits (rows of 8 or 16 blocks);
+//  QG_FUSED_GEMM: qgemm on Q4_K weights dequantizes into an f16 copy in the
+//    workspace first (0, the default: measured as fast or faster at 512 to
+//    4096 tokens) or inside the GEMM's shared memory (1: no f16 copy of W).
 enum KnobId {
     kKnobCtasPerSm,
     kKnobRingKib,
@@ -153,6 +158,7 @@ enum KnobId {
     kKnobFusedQuantKib,
     kKnobTc,
     kKnobFusedMaxMib,
+    kKnobFusedGemm,
     kKnobCount
 };
 struct KnobDef {
@@ -162,7 +168,8 @@ struct KnobDef {
 constexpr KnobDef kKnobs[kKnobCount] = {
     {"QG_CTAS_PER_SM", 2, 1, 4},          {"QG_RING_KIB", 96, 16, 200}, {"QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1},
     {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 16, 0, 1024},
-    {"QG_TC", 0, 0, 1},                   {"QG_FUSED_MAX_MIB", 1 << 20, 0, 1 << 20}};
+    {"QG_TC", 0, 0, 1},                   {"QG_FUSED_MAX_MIB", 1 << 20, 0, 1 << 20},
+    {"QG_FUSED_GEMM", 0, 0, 1}};
 std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
 
 int knob(KnobId k) {
@@ -951,6 +958,15 @@ int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     __half *A = static_cast<__half *>(workspace);
     __half *B = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) +
                                            ((static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255)));
+    if (type == QG_Q4_K && knob(kKnobFusedGemm)) {
+        // W is dequantized inside the GEMM's shared memory: only x is converted first
+        cudaError_t e = launch_f32_to_f16(x, B, n_tok * n_in, dev.sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill: x to f16");
+        e = launch_gemm_q4k_fused(static_cast<const uint8_t *>(W), B, y, n_out, n_tok, n_in, dev.err, dev.sms,
+                                  dev.device, s);
+        if (e != cudaSuccess) return cuda_fail(e, g_launch_step);
+        return QG_OK;
+    }
     const int64_t groups = n_out * n_in / 8;
     int64_t grid = (groups + 255) / 256;
     if (grid > static_cast<int64_t>(dev.sms) * 32) grid = static_cast<int64_t>(dev.sms) * 32;

@@ -248,6 +248,297 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 1) tc_dealloc(tmem, kGemmTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// The prefill product for Q4_K weights with the dequantization fused into the
+// GEMM: no f16 copy of W in memory. Same tiles, mma issue and epilogue as
+// gemm_f16_tc_kernel; each stage of the ring holds, besides the f16 A tile
+// and the B tile of one 64-element k-block, the raw bytes that k-block needs:
+// for each of the tile's 128 rows the 16-byte header of its Q4_K block (d,
+// dmin, 12 scale bytes) and the 32 bytes of codes of the k-block (k-block q
+// of a block: qs[32 q .. 32 q + 31], low nibbles for its first 32 elements,
+// high nibbles for the other 32).
+//  * warp 0, lane 0: per k-block three 2-D tensor loads into the stage: the
+//    B tile as before, the headers (box 16 bytes x 128 rows) and the codes
+//    (32 bytes x 128 rows) of the raw blocks;
+//  * warps 6..13 (converters): thread c takes row c / 2 of the tile and half
+//    c % 2 of the k-block, i.e. one 32-element sub-block j = 2q + half: value
+//    d sc_j q - dmin m_j in f32 (the product d sc_j q is exact; the
+//    subtraction rounds once), rounded to f16 -- the values dequantize_rows
+//    gives, rounded as the unfused path rounds them -- written as four
+//    16-byte chunks into the 128-byte-swizzled K-major layout a tensor load
+//    would produce (chunk c of row r at (c ^ (r mod 8)) * 16). Each thread
+//    fences its generic-proxy stores for the tensor cores before its warp
+//    arrives on the stage's A-full barrier; the mma waits for both barriers.
+// ---------------------------------------------------------------------------
+constexpr int kFuseConvWarps = 8;
+constexpr int kFuseThreads = (6 + kFuseConvWarps) * 32;
+constexpr int kQ4kBlockBytes = 144;
+constexpr int kRawHdr = kGemmBM * 16, kRawCodes = kGemmBM * 32;  // raw bytes of one k-block
+
+template <int BN> struct FuseShape {
+    static constexpr int kBTile = BN * kGemmBK * 2;
+    static constexpr int kStage = kGemmTileBytes + kBTile + kRawHdr + kRawCodes;
+    static constexpr int kStages = BN == 128 ? 5 : 4;
+    static constexpr int kSmem = 1024 + kGemmHdrBytes + kStages * kStage;
+    static constexpr int kTmemCols = 2 * BN;
+};
+
+// 6-bit scale and min of Q4_K sub-block j from the 12 scale bytes (words
+// s0 = bytes 0..3, s1 = 4..7, s2 = 8..11) ("Quantization" (rml), Unpacking
+// the packed fields; "量化格式" (candle), block structure table).
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int &sc, int &m) {
+    auto byte = [&](int k) {
+        const uint32_t w = k < 4 ? s0 : (k < 8 ? s1 : s2);
+        return static_cast<int>((w >> (8 * (k & 3))) & 0xFFu);
+    };
+    if (j < 4) {
+        sc = byte(j) & 63;
+        m = byte(j + 4) & 63;
+    } else {
+        sc = (byte(j + 4) & 0xF) | ((byte(j - 4) >> 6) << 4);
+        m = (byte(j + 4) >> 4) | ((byte(j) >> 6) << 4);
+    }
+}
+
+// Two f32 values to one f16x2 word (round to nearest even), lo first.
+__device__ __forceinline__ uint32_t pack_f16x2(float2 v) {
+    const __half2 h = __floats2half2_rn(v.x, v.y);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kFuseThreads, 1)
+    gemm_q4k_fused_kernel(const __grid_constant__ CUtensorMap tma_hdr, const __grid_constant__ CUtensorMap tma_codes,
+                          const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+    using Sh = FuseShape<BN>;
+    constexpr int S = Sh::kStages;
+    constexpr int kOffB = kGemmTileBytes, kOffHdr = kGemmTileBytes + Sh::kBTile, kOffCodes = kOffHdr + kRawHdr;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_a = smem_addr(smem_raw);
+    const uint32_t base_a = (raw_a + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_a - raw_a);
+    // header: full[S] | afull[S] | empty[S] | tfull[2] | tempty[2] | mfinal | tmem | abort
+    const uint32_t full0 = base_a, afull0 = base_a + 64, empty0 = base_a + 128;
+    const uint32_t tfull0 = base_a + 192, tempty0 = base_a + 208, mfinal = base_a + 224;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + 232);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(base + 236);
+    const uint32_t stages_a = base_a + kGemmHdrBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.tiles_m * p.tiles_n;
+    const int nk = p.K / kGemmBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(afull0 + 8 * s, kFuseConvWarps);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int d = 0; d < 2; ++d) {
+            mbar_init(tfull0 + 8 * d, 1);
+            mbar_init(tempty0 + 8 * d, 4);
+        }
+        mbar_init(mfinal, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        tc_alloc(smem_addr(tmem_slot), Sh::kTmemCols);
+        tc_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_allow_dependents();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer: per k-block the B tile and the raw bytes
+        if (lane == 0) {
+            pdl_wait_prior_grids();  // B is written by the kernel before this one
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (issued >= S && !tc_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = stages_a + static_cast<uint32_t>(s * Sh::kStage);
+                    const int x0 = (kb >> 2) * kQ4kBlockBytes;  // the block column's first byte in a row
+                    mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(Sh::kBTile + kRawHdr + kRawCodes));
+                    tma_load_2d(st + kOffB, &tma_b, kb * kGemmBK, tn * BN, full0 + 8 * s);
+                    tma_load_2d(st + kOffHdr, &tma_hdr, x0, tm * kGemmBM, full0 + 8 * s);
+                    tma_load_2d(st + kOffCodes, &tma_codes, x0 + 16 + 32 * (kb & 3), tm * kGemmBM, full0 + 8 * s);
+                    ++issued;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                record_error(p.err, kErrProducerWait);
+                *abort_flag = 1;
+            }
+            // leave no copy in flight into this CTA's shared memory
+            for (int64_t k = issued > S ? issued - S : 0; k < issued; ++k) {
+                if (!mbar_wait_bounded(full0 + 8 * static_cast<int>(k % S), static_cast<uint32_t>((k / S) & 1))) {
+                    record_error(p.err, kErrDrainWait);
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- mma issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc_idesc_f16(kGemmBM, BN);
+            int s = 0, it = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+                const int d = it & 1;
+                if (it >= 2 && !tc_wait(tempty0 + 8 * d, static_cast<uint32_t>(((it - 2) >> 1) & 1), abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dt = tmem + static_cast<uint32_t>(d * BN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!tc_wait(full0 + 8 * s, ph, abort_flag) || !tc_wait(afull0 + 8 * s, ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = stages_a + static_cast<uint32_t>(s * Sh::kStage);
+                    const uint64_t da = tc_smem_desc(sa, 1024), db = tc_smem_desc(sa + kOffB, 1024);
+#pragma unroll
+                    for (int k = 0; k < kGemmBK / 16; ++k)
+                        tc_mma_ss(dt, da + static_cast<uint64_t>(2 * k), db + static_cast<uint64_t>(2 * k), idesc,
+                                  (kb | k) != 0 ? 1u : 0u);
+                    tc_commit(empty0 + 8 * s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok) tc_commit(tfull0 + 8 * d);
+            }
+            if (!ok) {
+                record_error(p.err, kErrConsumerWait);
+                *abort_flag = 1;
+            }
+            tc_commit(mfinal);
+            if (!mbar_wait_bounded(mfinal, 0u)) record_error(p.err, kErrDrainWait);
+        }
+        __syncwarp();
+    } else if (warp < 6) {
+        // ---------------- epilogue: warp w reads tensor-memory lanes 32 (w % 4) ..
+        const int q = warp & 3;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+            const int tm = t % p.tiles_m, tn = t / p.tiles_m, d = it & 1;
+            if (ok && !tc_wait(tfull0 + 8 * d, static_cast<uint32_t>((it >> 1) & 1), abort_flag)) {
+                if (lane == 0) {
+                    record_error(p.err, kErrConsumerWait);
+                    *abort_flag = 1;
+                }
+                ok = false;
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int row = tm * kGemmBM + 32 * q + lane;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t v[32];
+                tc_ld32_wait(tl + static_cast<uint32_t>(d * BN + c0), v);
+                const int tok0 = tn * BN + c0;
+                if (row < p.n_out) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (tok0 + j < p.n_tok)
+                            p.y[static_cast<int64_t>(tok0 + j) * p.n_out + row] = __uint_as_float(v[j]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * d);
+        }
+    } else {
+        // ---------------- converters
+        const int c = threadIdx.x - 6 * 32;
+        const int row = c >> 1, half = c & 1;
+        const uint32_t sw = static_cast<uint32_t>(row & 7);
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for (int kb = 0; kb < nk; ++kb) {
+                if (!tc_wait(full0 + 8 * s, ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t st = stages_a + static_cast<uint32_t>(s * Sh::kStage);
+                const uint4 hdr = ld_s128(st + kOffHdr + 16u * row);  // d | dmin | scales[0..11]
+                const uint4 w0 = ld_s128(st + kOffCodes + 32u * row), w1 = ld_s128(st + kOffCodes + 32u * row + 16u);
+                int sc, m;
+                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * (kb & 3) + half, sc, m);
+                const float dsc = __fmul_rn(f16_bits_to_f32(hdr.x), static_cast<float>(sc));
+                const float off = __fmul_rn(f16_bits_to_f32(hdr.x >> 16), static_cast<float>(m));
+                // Code q in the low byte of the float 2^23 (one byte permute
+                // after the word's nibbles are masked): the float is 2^23 + q
+                // exactly, and fma(d sc, 2^23 + q, -d sc 2^23) = d sc q is exact
+                // (d sc has at most 17 significant bits, q 4). The subtraction
+                // of dmin m then rounds once, as d sc q - dmin m does.
+                const float2 s2 = make_float2(dsc, dsc), c2 = make_float2(-dsc * 8388608.0f, -dsc * 8388608.0f);
+                const float2 off2 = make_float2(-off, -off);
+                const uint32_t qw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint32_t o[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t nib = (half ? qw[i] >> 4 : qw[i]) & 0x0F0F0F0Fu;
+#pragma unroll
+                    for (int b = 0; b < 4; b += 2) {
+                        const float2 mg = make_float2(__uint_as_float(__byte_perm(nib, 0x4B000000u, 0x7650u | b)),
+                                                      __uint_as_float(__byte_perm(nib, 0x4B000000u, 0x7651u | b)));
+                        o[2 * i + (b >> 1)] = pack_f16x2(fadd2(ffma2(s2, mg, c2), off2));
+                    }
+                }
+                // elements 32 half .. 32 half + 31 of the k-block: chunks 4 half .. 4 half + 3
+                const uint32_t arow = st + static_cast<uint32_t>(row * 128);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t chunk = (static_cast<uint32_t>(4 * half + i) ^ sw) << 4;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(arow + chunk), "r"(o[4 * i]),
+                                 "r"(o[4 * i + 1]), "r"(o[4 * i + 2]), "r"(o[4 * i + 3])
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull0 + 8 * s);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) record_error(p.err, kErrConsumerWait);
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tc_dealloc(tmem, Sh::kTmemCols);
+}
+
 // f32 -> f16 (round to nearest even), 8 elements per thread.
 __global__ void f32_to_f16_kernel(const float *__restrict__ x, __half *__restrict__ out, int64_t groups) {
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
@@ -292,6 +583,20 @@ bool encode_f16_map(CUtensorMap *tm, const void *base, int64_t rows, int64_t K, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The raw Q4_K blocks of W as a 2-D byte tensor [n_out][row_bytes] with a
+// box of `box_bytes` x 128 rows; rows past the matrix read as zeros.
+bool encode_q4k_map(CUtensorMap *tm, const void *W, int64_t n_out, int64_t row_bytes, int box_bytes) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(n_out)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes), static_cast<cuuint32_t>(kGemmBM)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, cudaStream_t s) {
@@ -331,6 +636,48 @@ cudaError_t launch_gemm_bn(const __half *A, const __half *B, float *y, int64_t n
         done.fetch_or(bit, std::memory_order_acq_rel);
     }
     return launch_pdl(gemm_f16_tc_kernel<BN>, grid, kGemmThreads, GemmShape<BN>::kSmem, s, ta, tb, p);
+}
+
+template <int BN>
+cudaError_t launch_fused_bn(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
+                            int32_t *err, int sms, int device, cudaStream_t s) {
+    CUtensorMap th, tc, tb;
+    const int64_t row_bytes = K / 256 * kQ4kBlockBytes;
+    if (!encode_q4k_map(&th, W, n_out, row_bytes, 16) || !encode_q4k_map(&tc, W, n_out, row_bytes, 32) ||
+        !encode_f16_map(&tb, B, n_tok, K, BN)) {
+        g_launch_step = "cuTensorMapEncodeTiled";
+        return cudaErrorInvalidValue;
+    }
+    GemmParams p = {};
+    p.y = y;
+    p.err = err;
+    p.n_out = static_cast<int>(n_out);
+    p.n_tok = static_cast<int>(n_tok);
+    p.K = static_cast<int>(K);
+    p.tiles_m = static_cast<int>((n_out + kGemmBM - 1) / kGemmBM);
+    p.tiles_n = static_cast<int>((n_tok + BN - 1) / BN);
+    const int64_t total = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    const int grid = static_cast<int>(total < sms ? total : sms);
+    static std::atomic<uint64_t> done{0};
+    const uint64_t bit = 1ull << (device & 63);
+    if (!(done.load(std::memory_order_acquire) & bit)) {
+        g_launch_step = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
+        cudaError_t e = cudaFuncSetAttribute(gemm_q4k_fused_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             FuseShape<BN>::kSmem);
+        if (e != cudaSuccess) return e;
+        done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    return launch_pdl(gemm_q4k_fused_kernel<BN>, grid, kFuseThreads, FuseShape<BN>::kSmem, s, th, tc, tb, p);
+}
+
+// Y[n_tok][n_out] = dequant(W)[n_out][K] . B[n_tok][K]^T for Q4_K W (K a
+// multiple of 256, rows 16-byte aligned) and f16 B, the dequantization done
+// in shared memory. Token tiles as launch_gemm_f16_tc chooses them.
+cudaError_t launch_gemm_q4k_fused(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
+                                  int64_t K, int32_t *err, int sms, int device, cudaStream_t s) {
+    const int64_t tiles256 = ((n_out + kGemmBM - 1) / kGemmBM) * ((n_tok + 255) / 256);
+    if (tiles256 >= sms) return launch_fused_bn<256>(W, B, y, n_out, n_tok, K, err, sms, device, s);
+    return launch_fused_bn<128>(W, B, y, n_out, n_tok, K, err, sms, device, s);
 }
 
 // Y[n_tok][n_out] = A[n_out][K] . B[n_tok][K]^T for f16 A, B (16-byte
