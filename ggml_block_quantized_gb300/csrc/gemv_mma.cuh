@@ -336,6 +336,95 @@ struct MmaQ4_K {
     }
 };
 
+// ------------------------------------------------------------------ Q5_K
+// Block: f16 d, f16 dmin, Q4_K's 12 scale/min bytes, qh[32], then Q4_K's 128
+// bytes of nibbles (176 bytes, 16-byte aligned). The fifth bit of element
+// e = 64c + 32n + l (sub-block j = 2c + n) is bit j of qh[l] ("量化格式"
+// (candle), block structure table: Q5_K carries Q4_K's fields plus qh).
+// Lane (g, t) reads the nibbles of Q4_K's lane and qh[8t .. 8t + 7], the
+// fifth bits of the same positions, so the activation panel, its runs and
+// the min term are Q4_K's. Both nibbles become plain 5-bit codes (the high
+// nibble shifted down, the fifth bit moved to bit 4 of each byte), so every
+// sub-block's scale takes the factor 2^23 and the sums stay exact: 32 codes
+// below 32 times activations of at most 127 is below 2^17 units of 2^-24.
+struct MmaQ5_K : MmaQ4_K {
+    static constexpr int kBlockBytes = 176;
+
+    // Bit j of each byte of w, moved to bit 4 of the byte.
+    template <int J>
+    __device__ __forceinline__ static uint32_t fifth(uint32_t w) {
+        return (J <= 4 ? (w << (4 - J)) : (w >> (J - 4))) & 0x10101010u;
+    }
+
+    template <int C, int N, class BS>
+    __device__ __forceinline__ static void sub_block(uint2 wa, uint2 wb, uint2 qa, uint2 qb, uint32_t swa,
+                                                     uint32_t swb, const BS &B, float2 &Ta, float2 &Tb) {
+        constexpr int J = 2 * C + N;
+        // 5-bit codes, one a byte: nibble N of each qs byte | fifth bit J of the qh byte
+        const uint32_t ca0 = ((N ? wa.x >> 4 : wa.x) & 0x0F0F0F0Fu) | fifth<J>(qa.x);
+        const uint32_t ca1 = ((N ? wa.y >> 4 : wa.y) & 0x0F0F0F0Fu) | fifth<J>(qa.y);
+        const uint32_t cb0 = ((N ? wb.x >> 4 : wb.x) & 0x0F0F0F0Fu) | fifth<J>(qb.x);
+        const uint32_t cb1 = ((N ? wb.y >> 4 : wb.y) & 0x0F0F0F0Fu) | fifth<J>(qb.y);
+        uint32_t bf[4];
+        B.b(J, bf);
+        float C4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // bytes 0,2 and bytes 1,3 of each word as the f16 subnormal bits of two lanes
+        mma_16816(C4, ca0 & 0x00FF00FFu, cb0 & 0x00FF00FFu, __byte_perm(ca0, 0u, 0x4341u),
+                  __byte_perm(cb0, 0u, 0x4341u), bf[0], bf[1]);
+        mma_16816(C4, ca1 & 0x00FF00FFu, cb1 & 0x00FF00FFu, __byte_perm(ca1, 0u, 0x4341u),
+                  __byte_perm(cb1, 0u, 0x4341u), bf[2], bf[3]);
+        // the two rows' scales of sub-block J: byte J&3 in the mantissa of 2^23
+        const float2 f = fadd2(make_float2(__uint_as_float(__byte_perm(swa, 0x4B000000u, 0x7540u | (J & 3))),
+                                           __uint_as_float(__byte_perm(swb, 0x4B000000u, 0x7540u | (J & 3)))),
+                               make_float2(-8388608.0f, -8388608.0f));
+        Ta = ffma2(make_float2(f.x, f.x), make_float2(C4[0], C4[1]), Ta);
+        Tb = ffma2(make_float2(f.y, f.y), make_float2(C4[2], C4[3]), Tb);
+    }
+
+    template <int C, class BS>
+    __device__ __forceinline__ static void chunk(uint32_t ra, uint32_t rb, int t, uint2 qa, uint2 qb, uint32_t sca0,
+                                                 uint32_t sca1, uint32_t scb0, uint32_t scb1, const BS &B, float2 &Ta,
+                                                 float2 &Tb) {
+        const uint2 wa = ld_s64(ra + 48 + 32 * C + 8 * t), wb = ld_s64(rb + 48 + 32 * C + 8 * t);
+        sub_block<C, 0>(wa, wb, qa, qb, C < 2 ? sca0 : sca1, C < 2 ? scb0 : scb1, B, Ta, Tb);
+        sub_block<C, 1>(wa, wb, qa, qb, C < 2 ? sca0 : sca1, C < 2 ? scb0 : scb1, B, Ta, Tb);
+    }
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        const uint4 ha = ld_s128(ra), hb = ld_s128(rb);
+        // scales and mins exactly as Q4_K
+        const uint32_t sca0 = ha.y & 0x3F3F3F3Fu, sca1 = (ha.w & 0x0F0F0F0Fu) | ((ha.y >> 2) & 0x30303030u);
+        const uint32_t scb0 = hb.y & 0x3F3F3F3Fu, scb1 = (hb.w & 0x0F0F0F0Fu) | ((hb.y >> 2) & 0x30303030u);
+        const uint32_t ma0 = ha.z & 0x3F3F3F3Fu, ma1 = ((ha.w >> 4) & 0x0F0F0F0Fu) | ((ha.z >> 2) & 0x30303030u);
+        const uint32_t mb0 = hb.z & 0x3F3F3F3Fu, mb1 = ((hb.w >> 4) & 0x0F0F0F0Fu) | ((hb.z >> 2) & 0x30303030u);
+        const uint32_t msel = (t & 1) ? 0x4342u : 0x4140u;
+        float m2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_1688(m2, __byte_perm(t < 2 ? ma0 : ma1, 0u, msel), __byte_perm(t < 2 ? mb0 : mb1, 0u, msel), B.corr32());
+        const uint2 qa = ld_s64(ra + 16 + 8 * t), qb = ld_s64(rb + 16 + 8 * t);  // qh[8t .. 8t + 7]
+        float2 Ta = make_float2(0.0f, 0.0f), Tb = make_float2(0.0f, 0.0f);  // rows g, g+8
+        chunk<0>(ra, rb, t, qa, qb, sca0, sca1, scb0, scb1, B, Ta, Tb);
+        chunk<1>(ra, rb, t, qa, qb, sca0, sca1, scb0, scb1, B, Ta, Tb);
+        chunk<2>(ra, rb, t, qa, qb, sca0, sca1, scb0, scb1, B, Ta, Tb);
+        chunk<3>(ra, rb, t, qa, qb, sca0, sca1, scb0, scb1, B, Ta, Tb);
+        // block value = d_x * 2^24 * (d * T - dmin * m2)
+        const float da = f16_bits_to_f32(ha.x) * 16777216.0f, dma = f16_bits_to_f32(ha.x >> 16) * -16777216.0f;
+        const float db = f16_bits_to_f32(hb.x) * 16777216.0f, dmb = f16_bits_to_f32(hb.x >> 16) * -16777216.0f;
+        const uint2 dxw = B.dxw(t);
+        const float2 dx = make_float2(__uint_as_float(dxw.x), __uint_as_float(dxw.y));
+        const float2 ua = ffma2(make_float2(da, da), Ta, make_float2(dma * m2[0], dma * m2[1]));
+        const float2 ub = ffma2(make_float2(db, db), Tb, make_float2(dmb * m2[2], dmb * m2[3]));
+        float2 acc01 = ffma2(dx, ua, make_float2(acc[0], acc[1]));
+        float2 acc23 = ffma2(dx, ub, make_float2(acc[2], acc[3]));
+        acc[0] = acc01.x;
+        acc[1] = acc01.y;
+        acc[2] = acc23.x;
+        acc[3] = acc23.y;
+    }
+};
+
 // ------------------------------------------------------------------ Q6_K
 // Block: ql[128], qh[64], int8 scales[16], f16 d (the 210 bytes start
 // 2-byte aligned). Element e = 128h + 32k + 16m + lam (sub-block
