@@ -538,6 +538,91 @@ struct MmaQ6_K {
     }
 };
 
+// ------------------------------------------------------------------ Q2_K
+// Block: scales[16] (sub-block s: scale in the low nibble of byte s, min in
+// the high one), qs[64], f16 d, f16 dmin (84 bytes, 4-byte aligned). Element
+// e = 128n + 32j + 16h + l takes bits 2j, 2j+1 of qs[32n + 16h + l] and lies
+// in the 16-element sub-block s = 8n + 2j + h = e / 16; its value is
+// d sc_s q - dmin m_s ("量化格式" (candle), block structure table; the
+// library's reading of the ggml layout). The 16-element sub-blocks line up
+// with Q6_K's, so the activation panel, its runs and the correction operand
+// (bsums of the 16 sub-blocks) are Q6_K's: lane (g, t) takes positions
+// l = 4t..4t+3 of every sub-block, i.e. the word qs[32n + 16h + 4t ..] of
+// each row, whose bit pair 2j gives sub-block 8n + 2j + h. The min term
+// sum_s m_s bsum_s is one k = 16 mma over the mins; the codes (0..3) and
+// the sums (16 codes times activations of at most 127) stay exact.
+struct MmaQ2_K : MmaQ6_K {
+    static constexpr int kBlockBytes = 84;
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        uint32_t swa[4], swb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            swa[i] = ld_s32(ra + 4 * i);
+            swb[i] = ld_s32(rb + 4 * i);
+        }
+        // min term: sum_s m_s * bsum16_s (mins as subnormal f16 bits: m * 2^-24)
+        const uint32_t ssel = (t & 1) ? 0x4342u : 0x4140u;
+        auto mins = [](uint32_t w) { return (w >> 4) & 0x0F0F0F0Fu; };
+        const uint2 cw = B.corr64();
+        float mq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_16816(mq, __byte_perm(mins(t < 2 ? swa[0] : swa[1]), 0u, ssel),
+                  __byte_perm(mins(t < 2 ? swb[0] : swb[1]), 0u, ssel),
+                  __byte_perm(mins(t < 2 ? swa[2] : swa[3]), 0u, ssel),
+                  __byte_perm(mins(t < 2 ? swb[2] : swb[3]), 0u, ssel), cw.x, cw.y);
+        float2 Ta = make_float2(0.0f, 0.0f), Tb = make_float2(0.0f, 0.0f);  // rows g, g+8
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            uint32_t qa[2], qb[2];  // [h]: qs[32n + 16h + 4t ..]
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                qa[h] = ld_s32(ra + 16 + 32 * n + 16 * h + 4 * t);
+                qb[h] = ld_s32(rb + 16 + 32 * n + 16 * h + 4 * t);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t bf[4];
+                B.b(4 * n + j, bf);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int sb = 8 * n + 2 * j + h;
+                    const uint32_t ca = (qa[h] >> (2 * j)) & 0x03030303u, cb = (qb[h] >> (2 * j)) & 0x03030303u;
+                    float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    mma_16816(C, ca & 0x00FF00FFu, cb & 0x00FF00FFu, __byte_perm(ca, 0u, 0x4341u),
+                              __byte_perm(cb, 0u, 0x4341u), bf[2 * h], bf[2 * h + 1]);
+                    // the two rows' scales of sub-block sb: the low nibble of byte
+                    // sb placed in the mantissa of 2^23, then 2^23 subtracted
+                    const float2 f = fadd2(
+                        make_float2(__uint_as_float(__byte_perm(swa[sb >> 2] & 0x0F0F0F0Fu, 0x4B000000u,
+                                                                0x7540u | (sb & 3))),
+                                    __uint_as_float(__byte_perm(swb[sb >> 2] & 0x0F0F0F0Fu, 0x4B000000u,
+                                                                0x7540u | (sb & 3)))),
+                        make_float2(-8388608.0f, -8388608.0f));
+                    Ta = ffma2(make_float2(f.x, f.x), make_float2(C[0], C[1]), Ta);
+                    Tb = ffma2(make_float2(f.y, f.y), make_float2(C[2], C[3]), Tb);
+                }
+            }
+        }
+        // block value = d_x * 2^24 * (d * T - dmin * mq)
+        const uint32_t dda = ld_s32(ra + 80), ddb = ld_s32(rb + 80);
+        const float da = f16_bits_to_f32(dda) * 16777216.0f, dma = f16_bits_to_f32(dda >> 16) * -16777216.0f;
+        const float db = f16_bits_to_f32(ddb) * 16777216.0f, dmb = f16_bits_to_f32(ddb >> 16) * -16777216.0f;
+        const uint2 dxw = B.dxw(t);
+        const float2 dx = make_float2(__uint_as_float(dxw.x), __uint_as_float(dxw.y));
+        const float2 ua = ffma2(make_float2(da, da), Ta, make_float2(dma * mq[0], dma * mq[1]));
+        const float2 ub = ffma2(make_float2(db, db), Tb, make_float2(dmb * mq[2], dmb * mq[3]));
+        float2 acc01 = ffma2(dx, ua, make_float2(acc[0], acc[1]));
+        float2 acc23 = ffma2(dx, ub, make_float2(acc[2], acc[3]));
+        acc[0] = acc01.x;
+        acc[1] = acc01.y;
+        acc[2] = acc23.x;
+        acc[3] = acc23.y;
+    }
+};
+
 // ------------------------------------------------------------------ panel
 // Activations of one matrix (Q8_K blocks [nv][nb] at xq) into the panel:
 // per block, fragment record r of lane (g, t) = codes of vector g at the
