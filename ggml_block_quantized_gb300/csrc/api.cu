@@ -133,7 +133,7 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 // process with qg_tune():
 //  QG_CTAS_PER_SM, QG_RING_KIB: CTAs per SM the __dp4a GEMV grid aims at, and
 //    its shared-memory ring budget per CTA in KiB;
-//  QG_MMA_MIN_NVEC: vectors from which Q2_K / Q4_K / Q5_K / Q6_K products run on the
+//  QG_MMA_MIN_NVEC: vectors from which K-quant (Q2_K .. Q6_K) products run on the
 //    tensor cores;
 //  QG_MMA_PANEL, QG_MMA_KB: mma.sync plan overrides (activation source: 0
 //    automatic, 1 a shared-memory panel, 8 the biased-int8 panel; an upper
@@ -190,7 +190,7 @@ int tune_mma_panel() { return knob(kKnobMmaPanel); }
 int tune_mma_kb() { return knob(kKnobMmaKb); }
 int tune_tc() { return knob(kKnobTc); }
 
-bool mma_type(int type) { return type == QG_Q2_K || type == QG_Q4_K || type == QG_Q5_K || type == QG_Q6_K; }
+bool mma_type(int type) { return type >= QG_Q2_K && type <= QG_Q6_K; }  // every K-quant weight type
 
 // Whether a product (not the exact-block-sum diagnostic) takes the tensor-core
 // kernel; it reads activations from the workspace, so such calls never

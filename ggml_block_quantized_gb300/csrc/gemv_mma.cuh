@@ -623,6 +623,107 @@ struct MmaQ2_K : MmaQ6_K {
     }
 };
 
+// ------------------------------------------------------------------ Q3_K
+// Block: hmask[32], qs[64], 12 bytes of packed 6-bit scales, f16 d (110
+// bytes, 2-byte aligned). Element e = 128n + 32j + 16h + l: 2-bit value from
+// bits 2j, 2j+1 of qs[32n + 16h + l], third bit from bit 4n + j of
+// hmask[16h + l], q = value + 4 * bit - 4 (-4..3); sub-block s = 8n + 2j + h
+// with scale sc_s = v_s - 32, v_s 6 bits (low 4 in the nibbles of bytes
+// 0..7, high 2 in bytes 8..11) (the library's reading of the ggml layout).
+// As for Q2_K, the activation panel, runs and correction operand are Q6_K's.
+// The mma takes the unsigned codes c = q + 4 (0..7) and the scales biased by
+// 32, so S = sum_s sc_s sum c a - 4 sum_s sc_s bsum_s, with
+// sum_s sc_s bsum_s = sum_s v_s bsum_s - 32 (block sum): one k = 16 mma over
+// the biased scales gives sum_s v_s bsum_s.
+struct MmaQ3_K : MmaQ6_K {
+    static constexpr int kBlockBytes = 110;
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        // biased 6-bit scales v_s, one a byte: word k holds s = 4k .. 4k+3
+        uint32_t sa[3], sb[3];
+        ld_words_a2<3>(ra + 96, sa);
+        ld_words_a2<3>(rb + 96, sb);
+        uint32_t va[4], vb[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            va[k] = (((k & 2) ? sa[k & 1] >> 4 : sa[k & 1]) & 0x0F0F0F0Fu) | (((sa[2] >> (2 * k)) & 0x03030303u) << 4);
+            vb[k] = (((k & 2) ? sb[k & 1] >> 4 : sb[k & 1]) & 0x0F0F0F0Fu) | (((sb[2] >> (2 * k)) & 0x03030303u) << 4);
+        }
+        const uint32_t ssel = (t & 1) ? 0x4342u : 0x4140u;
+        const uint2 cw = B.corr64();
+        float mq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_16816(mq, __byte_perm(t < 2 ? va[0] : va[1], 0u, ssel), __byte_perm(t < 2 ? vb[0] : vb[1], 0u, ssel),
+                  __byte_perm(t < 2 ? va[2] : va[3], 0u, ssel), __byte_perm(t < 2 ? vb[2] : vb[3], 0u, ssel), cw.x,
+                  cw.y);
+        uint32_t hma[2], hmb[2];  // [h]: hmask[16h + 4t ..]
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w[1];
+            ld_words_a2<1>(ra + 16 * h + 4 * t, w);
+            hma[h] = w[0];
+            ld_words_a2<1>(rb + 16 * h + 4 * t, w);
+            hmb[h] = w[0];
+        }
+        float2 Ta = make_float2(0.0f, 0.0f), Tb = make_float2(0.0f, 0.0f);  // rows g, g+8
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            uint32_t qa[2], qb[2];  // [h]: qs[32n + 16h + 4t ..]
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t w[1];
+                ld_words_a2<1>(ra + 32 + 32 * n + 16 * h + 4 * t, w);
+                qa[h] = w[0];
+                ld_words_a2<1>(rb + 32 + 32 * n + 16 * h + 4 * t, w);
+                qb[h] = w[0];
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t bf[4];
+                B.b(4 * n + j, bf);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int sb = 8 * n + 2 * j + h;
+                    const int hb = 4 * n + j;  // the hmask bit, moved to bit 2 of each byte
+                    const uint32_t ha3 = (hb >= 2 ? hma[h] >> (hb - 2) : hma[h] << (2 - hb)) & 0x04040404u;
+                    const uint32_t hb3 = (hb >= 2 ? hmb[h] >> (hb - 2) : hmb[h] << (2 - hb)) & 0x04040404u;
+                    const uint32_t ca = ((qa[h] >> (2 * j)) & 0x03030303u) | ha3;
+                    const uint32_t cb = ((qb[h] >> (2 * j)) & 0x03030303u) | hb3;
+                    float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                    mma_16816(C, ca & 0x00FF00FFu, cb & 0x00FF00FFu, __byte_perm(ca, 0u, 0x4341u),
+                              __byte_perm(cb, 0u, 0x4341u), bf[2 * h], bf[2 * h + 1]);
+                    // sc_s = v_s - 32: byte s of the biased words in the mantissa
+                    // of 2^23, then 2^23 + 32 subtracted
+                    const float2 f = fadd2(
+                        make_float2(__uint_as_float(__byte_perm(va[sb >> 2], 0x4B000000u, 0x7540u | (sb & 3))),
+                                    __uint_as_float(__byte_perm(vb[sb >> 2], 0x4B000000u, 0x7540u | (sb & 3)))),
+                        make_float2(-8388640.0f, -8388640.0f));
+                    Ta = ffma2(make_float2(f.x, f.x), make_float2(C[0], C[1]), Ta);
+                    Tb = ffma2(make_float2(f.y, f.y), make_float2(C[2], C[3]), Tb);
+                }
+            }
+        }
+        // block value = d * d_x * 2^24 * (T - 4 mq + 2^-17 * block sum)
+        const float da = f16_bits_to_f32(ld_s16(ra + 108)) * 16777216.0f;
+        const float db = f16_bits_to_f32(ld_s16(rb + 108)) * 16777216.0f;
+        const uint2 dxw = B.dxw(t);
+        const uint2 bsw = B.bsw(t);
+        const float dx0 = __uint_as_float(dxw.x), dx1 = __uint_as_float(dxw.y);
+        const float2 bs = make_float2(__uint_as_float(bsw.x), __uint_as_float(bsw.y));
+        const float2 q17 = make_float2(0.00000762939453125f, 0.00000762939453125f), m4 = make_float2(-4.0f, -4.0f);
+        const float2 ea = ffma2(q17, bs, ffma2(m4, make_float2(mq[0], mq[1]), Ta));
+        const float2 eb = ffma2(q17, bs, ffma2(m4, make_float2(mq[2], mq[3]), Tb));
+        const float2 acc01 = ffma2(make_float2(da * dx0, da * dx1), ea, make_float2(acc[0], acc[1]));
+        const float2 acc23 = ffma2(make_float2(db * dx0, db * dx1), eb, make_float2(acc[2], acc[3]));
+        acc[0] = acc01.x;
+        acc[1] = acc01.y;
+        acc[2] = acc23.x;
+        acc[3] = acc23.y;
+    }
+};
+
 // ------------------------------------------------------------------ panel
 // Activations of one matrix (Q8_K blocks [nv][nb] at xq) into the panel:
 // per block, fragment record r of lane (g, t) = codes of vector g at the

@@ -60,6 +60,8 @@ cudaError_t launch_gemv_mma_q4_k(const MmaParams &p, const MmaMat *mats, int n, 
                                  cudaStream_t s);
 cudaError_t launch_gemv_mma_q2_k(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
                                  cudaStream_t s);
+cudaError_t launch_gemv_mma_q3_k(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
+                                 cudaStream_t s);
 cudaError_t launch_gemv_mma_q5_k(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
                                  cudaStream_t s);
 cudaError_t launch_gemv_mma_q6_k(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
@@ -69,6 +71,7 @@ inline cudaError_t launch_gemv_mma(int type, const MmaParams &p, const MmaMat *m
                                    int device, cudaStream_t s) {
     switch (type) {
     case QG_Q2_K: return launch_gemv_mma_q2_k(p, mats, n, l, device, s);
+    case QG_Q3_K: return launch_gemv_mma_q3_k(p, mats, n, l, device, s);
     case QG_Q4_K: return launch_gemv_mma_q4_k(p, mats, n, l, device, s);
     case QG_Q5_K: return launch_gemv_mma_q5_k(p, mats, n, l, device, s);
     case QG_Q6_K: return launch_gemv_mma_q6_k(p, mats, n, l, device, s);

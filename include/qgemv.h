@@ -198,7 +198,7 @@ size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec);
  *   Q2_K, Q4_K, Q5_K:             d_x * (d_w * S_q - dmin_w * S_m)
  * in f32. The f32 order of these few float operations is not fixed by the
  * pages; results agree with an f64 accumulation to about 1e-5 relative.
- * For Q2_K, Q4_K, Q5_K and Q6_K with n_vec >= 3 the sums are formed on the tensor cores
+ * For the K-quant weight types (Q2_K .. Q6_K) with n_vec >= 3 the sums are formed on the tensor cores
  * (mma.sync, f16 operands that hold the integer codes exactly, f32
  * accumulation per sub-block, which is exact) and the sub-block scales are
  * applied in f32 per sub-block -- the same tolerance holds. The vector count
@@ -282,7 +282,7 @@ typedef struct {
 /* Workspace bytes qgemv_batched needs for n_mats matrices: 16 when the
  * activations are small enough to be quantized inside the product (4 *
  * n_in * n_vec <= QG_FUSED_QUANT_KIB, 16 KiB by default, and not a
- * tensor-core product: Q2_K, Q4_K, Q5_K or Q6_K with n_vec >= 3), else the quantized
+ * tensor-core product: a K-quant weight type with n_vec >= 3), else the quantized
  * activations of every matrix,
  * n_mats * qgemv_workspace_bytes(type, n_in, n_vec). 0 on a bad argument. */
 size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int n_mats);
@@ -356,7 +356,7 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
  * counterpart; the knobs choose between kernels that compute the same
  * product). name is one of the environment variables the library reads once
  * at first use: QG_CTAS_PER_SM, QG_RING_KIB, QG_MMA_MIN_NVEC (vectors from
- * which Q2_K/Q4_K/Q5_K/Q6_K use the tensor cores), QG_MMA_PANEL (0 automatic, 1 a
+ * which the K-quant types use the tensor cores), QG_MMA_PANEL (0 automatic, 1 a
  * shared-memory activation panel, 8 the int8 panel), QG_MMA_KB (longest
  * chunk of blocks a panel-mode stage takes; 0 no limit), QG_FUSED_QUANT_KIB (f32 x of at most this many KiB is quantized
  * inside the GEMV), QG_FUSED_MAX_MIB (... for a single matrix of at most this

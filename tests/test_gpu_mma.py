@@ -1,5 +1,5 @@
-"""The tensor-core GEMV (Q2_K / Q4_K / Q5_K / Q6_K weights, three or more
-vectors) against the oracle, through the C ABI.
+"""The tensor-core GEMV (Q2_K / Q3_K / Q4_K / Q5_K / Q6_K weights, three or
+more vectors) against the oracle, through the C ABI.
 
 The kernel tiles 16 rows and streams each tile as chunks of whole blocks, so
 the shapes here cover a ragged last tile (n_out not a multiple of 16), rows of
@@ -21,7 +21,7 @@ from ggml_block_quantized_gb300 import synth  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
-K_TYPES = [qg.Q2_K, qg.Q4_K, qg.Q5_K, qg.Q6_K]
+K_TYPES = [qg.Q2_K, qg.Q3_K, qg.Q4_K, qg.Q5_K, qg.Q6_K]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -156,10 +156,11 @@ def test_mma_forced_plans(t):
     assert qg.device_error() == 0
 
 
-@pytest.mark.parametrize("t,nbytes,dpos", [(qg.Q5_K, 176, (0, 2)), (qg.Q2_K, 84, (80, 82))])
+@pytest.mark.parametrize("t,nbytes,dpos", [(qg.Q5_K, 176, (0, 2)), (qg.Q2_K, 84, (80, 82)), (qg.Q3_K, 110, (108,))])
 def test_mma_extreme_codes(t, nbytes, dpos):
     """Every code at its largest (Q5_K 31: nibbles 15 and every fifth bit set;
-    Q2_K 3), every scale and min at its largest, activations at the Q8_K
+    Q2_K 3; Q3_K 3 with every hmask bit set), every scale and min at its
+    largest, activations at the Q8_K
     extreme 127: the exact sub-block sums stay exact in the f32
     accumulators."""
     rng = np.random.default_rng(4600 + t)
@@ -184,6 +185,7 @@ def test_kernel_choice_is_reported():
     assert qg.kernel_info(qg.Q5_K, 32000, 4096, 8).startswith("gemv_mma_kernel<Q5_K,")
     assert qg.kernel_info(qg.Q5_K, 32000, 4096, 2).startswith("gemv_kernel<Q5_K,NV=2>")
     assert qg.kernel_info(qg.Q2_K, 32000, 4096, 8).startswith("gemv_mma_kernel<Q2_K,")
+    assert qg.kernel_info(qg.Q3_K, 32000, 4096, 8).startswith("gemv_mma_kernel<Q3_K,")
     assert qg.kernel_info(qg.Q4_K, 4096, 4096, 2).startswith("gemv_kernel<Q4_K,NV=2>")
     assert qg.kernel_info(qg.Q4_0, 4096, 4096, 8).startswith("gemv_kernel<Q4_0,NV=8>")
     # the __dp4a kernel's two Q6_K items: two lanes per block where their
