@@ -135,6 +135,13 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 //    its shared-memory ring budget per CTA in KiB;
 //  QG_MMA_MIN_NVEC: vectors from which K-quant (Q2_K .. Q6_K) products run on the
 //    tensor cores;
+//  QG_MMA_GROUP_MELEM: the 32-element types (Q4_0, Q4_1, Q5_0, Q8_0) take the
+//    tensor cores from QG_MMA_MIN_NVEC vectors when a matrix's elements
+//    n_out * n_in times (vectors - 3) reach this many Mi (2^20): the __dp4a
+//    kernel's time grows with the vectors, the tensor-core kernel's barely,
+//    but the latter pays a fixed activation-panel prologue. Measured on this
+//    GPU, all four types at 32000 x 4096 win from 4 vectors, at 11008 x 4096
+//    from 5, at 4096 x 4096 from 8 (7 is within 5% either way);
 //  QG_MMA_PANEL, QG_MMA_KB: mma.sync plan overrides (activation source: 0
 //    automatic, 1 a shared-memory panel, 8 the biased-int8 panel; an upper
 //    bound on blocks per chunk, 0 none);
@@ -159,6 +166,7 @@ enum KnobId {
     kKnobTc,
     kKnobFusedMaxMib,
     kKnobFusedGemm,
+    kKnobMmaGroupMelem,
     kKnobCount
 };
 struct KnobDef {
@@ -169,7 +177,7 @@ constexpr KnobDef kKnobs[kKnobCount] = {
     {"QG_CTAS_PER_SM", 2, 1, 4},          {"QG_RING_KIB", 96, 16, 200}, {"QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1},
     {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 16, 0, 1024},
     {"QG_TC", 0, 0, 1},                   {"QG_FUSED_MAX_MIB", 1 << 20, 0, 1 << 20},
-    {"QG_FUSED_GEMM", 0, 0, 1}};
+    {"QG_FUSED_GEMM", 0, 0, 1},           {"QG_MMA_GROUP_MELEM", 65, 0, 1 << 20}};
 std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
 
 int knob(KnobId k) {
@@ -190,12 +198,21 @@ int tune_mma_panel() { return knob(kKnobMmaPanel); }
 int tune_mma_kb() { return knob(kKnobMmaKb); }
 int tune_tc() { return knob(kKnobTc); }
 
-bool mma_type(int type) { return type >= QG_Q2_K && type <= QG_Q6_K; }  // every K-quant weight type
+// The weight types with a tensor-core item: every K-quant type, and the
+// 32-element types taken eight blocks at a time (rows of whole groups).
+bool mma_grouped(int type) { return type == QG_Q4_0 || type == QG_Q4_1 || type == QG_Q5_0 || type == QG_Q8_0; }
+bool mma_type(int type) { return (type >= QG_Q2_K && type <= QG_Q6_K) || mma_grouped(type); }
 
-// Whether a product (not the exact-block-sum diagnostic) takes the tensor-core
-// kernel; it reads activations from the workspace, so such calls never
-// quantize x inside the GEMV prologue.
+// Whether a product (not the exact-block-sum diagnostic) may take the
+// tensor-core kernel; it reads activations from the workspace, so such calls
+// never quantize x inside the GEMV prologue.
 bool mma_preferred(int type, int64_t n_vec) { return mma_type(type) && n_vec >= tune_mma_min_nvec(); }
+
+// ... and whether it does, for a matrix of n_out x n_in.
+bool mma_wins(int type, int64_t n_vec, int64_t n_out, int64_t n_in) {
+    if (!mma_preferred(type, n_vec)) return false;
+    return !mma_grouped(type) || n_out * n_in * (n_vec - 3) >= (static_cast<int64_t>(knob(kKnobMmaGroupMelem)) << 20);
+}
 
 size_t act_smem_bytes(int type, int lpb, int nb, int nv) {
     switch (type) {
@@ -367,6 +384,12 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
                   MmaLaunch *l) {
     int elems, bytes;
     if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
+    const bool grouped = mma_grouped(type);
+    if (grouped) {  // eight 32-element blocks per panel block: rows of whole groups only
+        if (n_in % 256 != 0) return QG_ERR_SHAPE;
+        elems = 256;
+        bytes *= 8;
+    }
     const int64_t nb64 = n_in / elems;
     if (nb64 < 1 || nb64 > 4096 || total_tiles < 1) return QG_ERR_SHAPE;
     const int nb = static_cast<int>(nb64);
@@ -379,7 +402,7 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
     bool found = false;
     const int force = tune_mma_panel();  // 0 automatic, 1 a panel, 8 the int8 panel
     constexpr int rw = 8;  // consumer warps of the register kernel: blocks w and w + 8 each
-    if (force == 0 && nb <= 2 * rw) {
+    if (force == 0 && nb <= 2 * rw && !grouped) {
         int rp, gp, S, R;
         mma_slot_layout(nb, nb, bytes, &rp, &gp);
         if (mma_ring(smem_limit, kMmaHeaderBytes, 4 * static_cast<int64_t>(gp), rw, &S, &R)) {
@@ -407,7 +430,8 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
         for (int f = 0; f < 2; ++f) {
             const bool b16 = f == 0;
             if (b16 && force == 8) continue;
-            const int rec = mma_rec_bytes(b16);
+            // grouped types: per record and vector d_x and a sum (512 bytes) for the Q8_K tail
+            const int rec = mma_rec_bytes(b16) + (grouped ? 512 - kMmaTailBytes : 0);
             const int64_t panel = static_cast<int64_t>(nb) * rec;
             for (int ci = 0; ci < kCands; ++ci) {
                 const int kb = cands[ci];
@@ -548,7 +572,7 @@ bool fused_quantization(int64_t n_in, int64_t n_vec) { return 4 * n_in * n_vec <
 // QG_FUSED_MAX_MIB of blocks (by default any matrix); above that the separate
 // quantization launch, overlapped with the GEMV's weight prefetch, is taken.
 bool fused_single(int type, int64_t n_out, int64_t n_in, int64_t n_vec) {
-    return fused_quantization(n_in, n_vec) && !mma_preferred(type, n_vec) &&
+    return fused_quantization(n_in, n_vec) && !mma_wins(type, n_vec, n_out, n_in) &&
            qtype_nbytes(type, n_in) * n_out <= (static_cast<int64_t>(knob(kKnobFusedMaxMib)) << 20);
 }
 
@@ -563,7 +587,27 @@ int run_gemv_mats(int type, GemvMat *mats, int n, int64_t n_in, int64_t n_vec, s
         total += mats[i].n_out;
     }
     if (total == 0) return QG_OK;
-    if (!isums && x_bytes == 0 && mma_preferred(type, n_vec)) {
+    bool use_mma = !isums && x_bytes == 0 && mma_preferred(type, n_vec);
+    if (use_mma && mma_grouped(type)) {
+        // each matrix takes the kernel a call on it alone would take (the
+        // choice depends on its size), so a batch gives the same bits as
+        // single calls: the matrices the tensor cores win on in one launch,
+        // the others in a second
+        GemvMat win[QG_MAX_BATCH], rest[QG_MAX_BATCH];
+        int nw = 0, nr = 0;
+        for (int i = 0; i < n; ++i) {
+            if (mma_wins(type, n_vec, mats[i].n_out, n_in))
+                win[nw++] = mats[i];
+            else
+                rest[nr++] = mats[i];
+        }
+        if (nw > 0 && nr > 0) {
+            int st = run_gemv_mats(type, win, nw, n_in, n_vec, x_bytes, isums, dev, s);
+            return st != QG_OK ? st : run_gemv_mats(type, rest, nr, n_in, n_vec, x_bytes, isums, dev, s);
+        }
+        use_mma = nw > 0;
+    }
+    if (use_mma) {
         // several vectors: the tcgen05 kernel (Q4_K, launches of many 16-row
         // tiles), else the mma.sync kernel, when their shapes fit
         int64_t tiles16 = 0;
@@ -1013,7 +1057,7 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
     const char *tn = type == QG_Q4_K ? "Q4_K" : type == QG_Q6_K ? "Q6_K" : type == QG_Q8_0 ? "Q8_0"
                    : type == QG_Q4_1 ? "Q4_1" : type == QG_Q5_0 ? "Q5_0" : type == QG_Q2_K ? "Q2_K"
                    : type == QG_Q3_K ? "Q3_K" : type == QG_Q5_K ? "Q5_K" : "Q4_0";
-    if (mma_preferred(type, n_vec)) {
+    if (mma_wins(type, n_vec, total_rows / n_mats, n_in)) {
         // tiles: a batch of equal matrices is assumed for the tile count
         const int64_t per = total_rows / n_mats;
         TcParams tp = {};

@@ -236,6 +236,14 @@ struct MmaSmemB {
     __device__ __forceinline__ uint2 corr64() const { return ld_s64(rec + mma_frag_bytes(B16) + 8 * lane); }
     __device__ __forceinline__ uint2 dxw(int t) const { return ld_s64(rec + mma_frag_bytes(B16) + 256 + 8 * t); }
     __device__ __forceinline__ uint2 bsw(int t) const { return ld_s64(rec + mma_frag_bytes(B16) + 288 + 8 * t); }
+    // groups of 32-element blocks: d_x and (Q8_1) s of record r, vectors 2t
+    // and 2t+1
+    __device__ __forceinline__ uint2 dxr(int r, int t) const {
+        return ld_s64(rec + mma_frag_bytes(B16) + static_cast<uint32_t>(4 * (8 * r + 2 * t)));
+    }
+    __device__ __forceinline__ uint2 axr(int r, int t) const {
+        return ld_s64(rec + mma_frag_bytes(B16) + 256 + static_cast<uint32_t>(4 * (8 * r + 2 * t)));
+    }
 };
 
 // ... or held in registers (f16 fragments).
@@ -264,6 +272,7 @@ struct MmaRegB {
 // codes 32j + 8t + {0,2,1,3, 4,6,5,7} of vector g.
 struct MmaQ4_K {
     static constexpr int kBlockBytes = 144;
+    static constexpr int kActBytes = 0;  // activations: Q8_K blocks (the panel's bsums tail)
 
     // Element offsets (within the block) of the two 4-code runs of record r
     // for lane t; the run is permuted to slots {0,2,1,3}.
@@ -437,6 +446,7 @@ struct MmaQ5_K : MmaQ4_K {
 // (sub-block 2i+1) of vector g.
 struct MmaQ6_K {
     static constexpr int kBlockBytes = 210;
+    static constexpr int kActBytes = 0;  // activations: Q8_K blocks (the panel's bsums tail)
 
     __device__ static int run0(int r, int t) { return 32 * r + 4 * t; }
     __device__ static int run1(int r, int t) { return 32 * r + 16 + 4 * t; }
@@ -724,6 +734,197 @@ struct MmaQ3_K : MmaQ6_K {
     }
 };
 
+// ------------------------------------------------------- 32-element blocks
+// Q4_0, Q5_0, Q4_1 and Q8_0 rows are taken eight blocks (256 elements) at a
+// time: one panel block per group, record r = block r of the group
+// ("Building Q8_0 and Q4_0 Like ggml", Examples 1, 5, 7 and 8; "量化格式"
+// (candle), block structure table). Lane (g, t) takes elements 4t..4t+3 and
+// 16 + 4t..16 + 4t + 3 of each block of rows g and g + 8 (the runs of the
+// records); block sums are exact in the mma's f32 accumulators (integer
+// codes times activations of at most 127, 32 of them), then each block's
+// float step is applied per row and vector: d_w d_x S (+ m_w s_x for Q4_1).
+
+// Four codes (one per byte, c + bias in 0..255) of a word as the mma's two A
+// registers of one row, exact f16 integers c: bytes 0,2 (k-slots 2t, 2t+1)
+// and bytes 1,3 (slots 2t+8, 2t+9) each placed under 0x64 (the f16 1024 + c
+// + bias), then 1024 + bias subtracted -- so a signed code needs no offset
+// term and no activation sums.
+__device__ __forceinline__ uint32_t hsub2c(uint32_t h, uint32_t c) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(c));
+    return r;
+}
+template <uint32_t BIASED_1024>
+__device__ __forceinline__ uint32_t mma_even_s(uint32_t c) {
+    return hsub2c(__byte_perm(c, 0x64646464u, 0x4240), BIASED_1024);
+}
+template <uint32_t BIASED_1024>
+__device__ __forceinline__ uint32_t mma_odd_s(uint32_t c) {
+    return hsub2c(__byte_perm(c, 0x64646464u, 0x4341), BIASED_1024);
+}
+
+// One block's float step for rows g, g+8 and vectors 2t, 2t+1, from the
+// exact block sums C (integers in f32).
+__device__ __forceinline__ void mma_block_step(const float (&C)[4], float dwa, float dwb, uint2 dxw, float (&acc)[4]) {
+    const float2 dx = make_float2(__uint_as_float(dxw.x), __uint_as_float(dxw.y));
+    const float2 a01 = ffma2(make_float2(dwa * dx.x, dwa * dx.y), make_float2(C[0], C[1]), make_float2(acc[0], acc[1]));
+    const float2 a23 = ffma2(make_float2(dwb * dx.x, dwb * dx.y), make_float2(C[2], C[3]), make_float2(acc[2], acc[3]));
+    acc[0] = a01.x;
+    acc[1] = a01.y;
+    acc[2] = a23.x;
+    acc[3] = a23.y;
+}
+
+// Q4_0: 18-byte blocks (f16 d, qs[16]: byte k = code k | code k+16 << 4),
+// value (code - 8) d, paired with Q8_0 activations. The mma takes the signed
+// values code - 8 (f16 1024 + code minus 1032).
+struct MmaQ4_0 {
+    static constexpr int kBlockBytes = 8 * 18;
+    static constexpr int kActBytes = 34;
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        constexpr uint32_t k1032 = 0x64086408u;
+#pragma unroll 2
+        for (int r = 0; r < 8; ++r) {
+            const uint32_t a = ra + 18u * r, b = rb + 18u * r;  // 2-byte aligned blocks
+            uint32_t wa[1], wb[1];
+            ld_words_a2<1>(a + 2 + 4 * t, wa);  // qs[4t..4t+3]: codes 4t.. (low), 16 + 4t.. (high)
+            ld_words_a2<1>(b + 2 + 4 * t, wb);
+            const float dwa = f16_bits_to_f32(ld_s16(a)), dwb = f16_bits_to_f32(ld_s16(b));
+            uint32_t bf[4];
+            B.b(r, bf);
+            float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint32_t la = wa[0] & 0x0F0F0F0Fu, lb = wb[0] & 0x0F0F0F0Fu;
+            const uint32_t ha = (wa[0] >> 4) & 0x0F0F0F0Fu, hb = (wb[0] >> 4) & 0x0F0F0F0Fu;
+            mma_16816(C, mma_even_s<k1032>(la), mma_even_s<k1032>(lb), mma_odd_s<k1032>(la), mma_odd_s<k1032>(lb),
+                      bf[0], bf[1]);
+            mma_16816(C, mma_even_s<k1032>(ha), mma_even_s<k1032>(hb), mma_odd_s<k1032>(ha), mma_odd_s<k1032>(hb),
+                      bf[2], bf[3]);
+            mma_block_step(C, dwa, dwb, B.dxr(r, t), acc);
+        }
+    }
+};
+
+// Q8_0: 34-byte blocks (f16 d, 32 int8 codes), value q d, paired with Q8_0
+// activations. The mma takes q as f16 (1024 + (q + 128) minus 1152).
+struct MmaQ8_0 {
+    static constexpr int kBlockBytes = 8 * 34;
+    static constexpr int kActBytes = 34;
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        constexpr uint32_t k1152 = 0x64806480u;
+#pragma unroll 2
+        for (int r = 0; r < 8; ++r) {
+            const uint32_t a = ra + 34u * r, b = rb + 34u * r;
+            uint32_t wa[1], wb[1], va[1], vb[1];
+            ld_words_a2<1>(a + 2 + 4 * t, wa);  // codes 4t .. 4t+3
+            ld_words_a2<1>(b + 2 + 4 * t, wb);
+            ld_words_a2<1>(a + 18 + 4 * t, va);  // codes 16 + 4t ..
+            ld_words_a2<1>(b + 18 + 4 * t, vb);
+            const float dwa = f16_bits_to_f32(ld_s16(a)), dwb = f16_bits_to_f32(ld_s16(b));
+            uint32_t bf[4];
+            B.b(r, bf);
+            float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint32_t la = wa[0] ^ 0x80808080u, lb = wb[0] ^ 0x80808080u;
+            const uint32_t ha = va[0] ^ 0x80808080u, hb = vb[0] ^ 0x80808080u;
+            mma_16816(C, mma_even_s<k1152>(la), mma_even_s<k1152>(lb), mma_odd_s<k1152>(la), mma_odd_s<k1152>(lb),
+                      bf[0], bf[1]);
+            mma_16816(C, mma_even_s<k1152>(ha), mma_even_s<k1152>(hb), mma_odd_s<k1152>(ha), mma_odd_s<k1152>(hb),
+                      bf[2], bf[3]);
+            mma_block_step(C, dwa, dwb, B.dxr(r, t), acc);
+        }
+    }
+};
+
+// Four bits (bit i of n, n < 16) to bit 0 of byte i: the four shifted copies
+// of n do not overlap, so the product carries nothing between them.
+__device__ __forceinline__ uint32_t spread4(uint32_t n) { return (n * 0x00204081u) & 0x01010101u; }
+
+// Q5_0: 22-byte blocks (f16 d, u32 qh: bit j = fifth bit of code j, qs[16]
+// as in Q4_0), value (code - 16) d, paired with Q8_0 activations. The mma
+// takes code - 16 (f16 1024 + code minus 1040).
+struct MmaQ5_0 {
+    static constexpr int kBlockBytes = 8 * 22;
+    static constexpr int kActBytes = 34;
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        constexpr uint32_t k1040 = 0x64106410u;
+#pragma unroll 2
+        for (int r = 0; r < 8; ++r) {
+            const uint32_t a = ra + 22u * r, b = rb + 22u * r;
+            uint32_t wa[1], wb[1], qa[1], qb[1];
+            ld_words_a2<1>(a + 2, qa);
+            ld_words_a2<1>(b + 2, qb);
+            ld_words_a2<1>(a + 6 + 4 * t, wa);
+            ld_words_a2<1>(b + 6 + 4 * t, wb);
+            const float dwa = f16_bits_to_f32(ld_s16(a)), dwb = f16_bits_to_f32(ld_s16(b));
+            uint32_t bf[4];
+            B.b(r, bf);
+            float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint32_t la = (wa[0] & 0x0F0F0F0Fu) | (spread4((qa[0] >> (4 * t)) & 0xFu) << 4);
+            const uint32_t lb = (wb[0] & 0x0F0F0F0Fu) | (spread4((qb[0] >> (4 * t)) & 0xFu) << 4);
+            const uint32_t ha = ((wa[0] >> 4) & 0x0F0F0F0Fu) | (spread4((qa[0] >> (16 + 4 * t)) & 0xFu) << 4);
+            const uint32_t hb = ((wb[0] >> 4) & 0x0F0F0F0Fu) | (spread4((qb[0] >> (16 + 4 * t)) & 0xFu) << 4);
+            mma_16816(C, mma_even_s<k1040>(la), mma_even_s<k1040>(lb), mma_odd_s<k1040>(la), mma_odd_s<k1040>(lb),
+                      bf[0], bf[1]);
+            mma_16816(C, mma_even_s<k1040>(ha), mma_even_s<k1040>(hb), mma_odd_s<k1040>(ha), mma_odd_s<k1040>(hb),
+                      bf[2], bf[3]);
+            mma_block_step(C, dwa, dwb, B.dxr(r, t), acc);
+        }
+    }
+};
+
+// Q4_1: 20-byte blocks (f16 d, f16 m, qs[16] as in Q4_0), value code d + m,
+// paired with Q8_1 activations (d_x, s = d_x sum q): per block
+// d d_x sum(code q) + m s. The mma takes the unsigned codes (f16 1024 + code
+// minus 1024).
+struct MmaQ4_1 {
+    static constexpr int kBlockBytes = 8 * 20;
+    static constexpr int kActBytes = 36;
+
+    template <class BS>
+    __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
+                                                      float (&acc)[4]) {
+        const int t = lane & 3;
+        constexpr uint32_t k1024 = 0x64006400u;
+#pragma unroll 2
+        for (int r = 0; r < 8; ++r) {
+            const uint32_t a = ra + 20u * r, b = rb + 20u * r;
+            uint32_t wa[1], wb[1];
+            ld_words_a2<1>(a + 4 + 4 * t, wa);
+            ld_words_a2<1>(b + 4 + 4 * t, wb);
+            const float dwa = f16_bits_to_f32(ld_s16(a)), dwb = f16_bits_to_f32(ld_s16(b));
+            const float ma = f16_bits_to_f32(ld_s16(a + 2)), mb = f16_bits_to_f32(ld_s16(b + 2));
+            uint32_t bf[4];
+            B.b(r, bf);
+            float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint32_t la = wa[0] & 0x0F0F0F0Fu, lb = wb[0] & 0x0F0F0F0Fu;
+            const uint32_t ha = (wa[0] >> 4) & 0x0F0F0F0Fu, hb = (wb[0] >> 4) & 0x0F0F0F0Fu;
+            mma_16816(C, mma_even_s<k1024>(la), mma_even_s<k1024>(lb), mma_odd_s<k1024>(la), mma_odd_s<k1024>(lb),
+                      bf[0], bf[1]);
+            mma_16816(C, mma_even_s<k1024>(ha), mma_even_s<k1024>(hb), mma_odd_s<k1024>(ha), mma_odd_s<k1024>(hb),
+                      bf[2], bf[3]);
+            const uint2 sw = B.axr(r, t);
+            const float2 s = make_float2(__uint_as_float(sw.x), __uint_as_float(sw.y));
+            float m4[4] = {ma * s.x + acc[0], ma * s.y + acc[1], mb * s.x + acc[2], mb * s.y + acc[3]};
+            mma_block_step(C, dwa, dwb, B.dxr(r, t), m4);
+            acc[0] = m4[0];
+            acc[1] = m4[1];
+            acc[2] = m4[2];
+            acc[3] = m4[3];
+        }
+    }
+};
+
 // ------------------------------------------------------------------ panel
 // Activations of one matrix (Q8_K blocks [nv][nb] at xq) into the panel:
 // per block, fragment record r of lane (g, t) = codes of vector g at the
@@ -804,6 +1005,72 @@ __device__ __forceinline__ void mma_build_panel(const MmaParams &p, const uint8_
         }
         reinterpret_cast<float *>(tail + 256)[v] = dx;
         reinterpret_cast<float *>(tail + 288)[v] = static_cast<float>(sum);
+    }
+}
+
+// Activations of one matrix from Q8_0 (34-byte) or Q8_1 (36-byte) blocks
+// [nv][8 nb] into the panel, for weights in groups of eight 32-element blocks
+// (one panel block per group): record r = activation block r of the group,
+// its two 4-code runs at codes 4t and 16 + 4t permuted to slots {0,2,1,3}
+// (the layout of the Q6_K records); then per record and vector d_x (f32)
+// and, for Q8_1, its s, as [record][vector] floats. Vectors g >= nv are
+// zero.
+template <class T, bool B16>
+__device__ __forceinline__ void mma_build_panel_q8(const MmaParams &p, const uint8_t *xq, uint8_t *pan, int tid,
+                                                   int nthr) {
+    constexpr int AB = T::kActBytes, CO = AB - 32;  // block bytes; offset of the codes
+    const int nb = p.nb, nv = p.nv, nb32 = 8 * nb;
+    const int n_rec = nb * kMmaRecords * 32;
+    auto ld4 = [](const uint8_t *a) {  // 4 bytes at a 2-byte aligned address
+        const uint16_t *h = reinterpret_cast<const uint16_t *>(a);
+        return static_cast<uint32_t>(__ldg(h)) | (static_cast<uint32_t>(__ldg(h + 1)) << 16);
+    };
+    constexpr int kBatch = 8;
+    for (int u0 = tid; u0 < n_rec; u0 += kBatch * nthr) {
+        uint32_t w0[kBatch], w1[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int u = u0 + i * nthr;
+            const int b = u / (kMmaRecords * 32), r = (u / 32) % kMmaRecords, L = u % 32;
+            const int g = L >> 2, t = L & 3;
+            w0[i] = w1[i] = 0u;
+            if (u < n_rec && g < nv) {
+                const uint8_t *qs = xq + (static_cast<size_t>(g) * nb32 + 8 * b + r) * AB + CO;
+                w0[i] = ld4(qs + 4 * t);
+                w1[i] = ld4(qs + 16 + 4 * t);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int u = u0 + i * nthr;
+            if (u >= n_rec) break;
+            const int b = u / (kMmaRecords * 32), r = (u / 32) % kMmaRecords, L = u % 32;
+            const uint32_t x0 = __byte_perm(w0[i], 0u, 0x3120), x1 = __byte_perm(w1[i], 0u, 0x3120);
+            uint8_t *dst = pan + static_cast<size_t>(b) * p.rec_bytes;
+            if (B16) {
+                uint4 o;
+                o.x = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x0, 0))), __half_as_ushort(__int2half_rn(sbyte(x0, 1))));
+                o.y = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x0, 2))), __half_as_ushort(__int2half_rn(sbyte(x0, 3))));
+                o.z = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x1, 0))), __half_as_ushort(__int2half_rn(sbyte(x1, 1))));
+                o.w = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x1, 2))), __half_as_ushort(__int2half_rn(sbyte(x1, 3))));
+                reinterpret_cast<uint4 *>(dst)[r * 32 + L] = o;
+            } else {
+                reinterpret_cast<uint2 *>(dst)[r * 32 + L] = make_uint2(x0 ^ 0x80808080u, x1 ^ 0x80808080u);
+            }
+        }
+    }
+    // per (group, record, vector): d_x and (Q8_1) s
+    for (int u = tid; u < nb * kMmaRecords * kMmaNvec; u += nthr) {
+        const int b = u / (kMmaRecords * kMmaNvec), r = (u / kMmaNvec) % kMmaRecords, v = u % kMmaNvec;
+        float dx = 0.0f, aux = 0.0f;
+        if (v < nv) {
+            const uint8_t *blk = xq + (static_cast<size_t>(v) * nb32 + 8 * b + r) * AB;
+            dx = f16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t *>(blk)));
+            if (AB == 36) aux = f16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t *>(blk + 2)));  // Q8_1 s
+        }
+        float *tail = reinterpret_cast<float *>(pan + static_cast<size_t>(b) * p.rec_bytes + mma_frag_bytes(B16));
+        tail[8 * r + v] = dx;
+        tail[64 + 8 * r + v] = aux;
     }
 }
 
@@ -1112,7 +1379,7 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
     uint32_t phase = 0;
     for (int k = 0; walk.next(b, p, st); ++k) {
         if (st.mat != cur) {  // a new matrix: its activations
-            if (REGS) {
+            if constexpr (REGS) {
 #pragma unroll
                 for (int i = 0; i < RB; ++i)
                     if (warp + i * NW < p.nb)
@@ -1120,7 +1387,10 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
                                          bcorr[i], bdx[i], bbs[i]);
             } else {
                 if (cur >= 0) named_barrier(1, NW * 32);
-                mma_build_panel<T, B16>(p, b.m[MAXB == 1 ? 0 : st.mat].xq, pan, threadIdx.x, NW * 32);
+                if constexpr (T::kActBytes == 0)
+                    mma_build_panel<T, B16>(p, b.m[MAXB == 1 ? 0 : st.mat].xq, pan, threadIdx.x, NW * 32);
+                else
+                    mma_build_panel_q8<T, B16>(p, b.m[MAXB == 1 ? 0 : st.mat].xq, pan, threadIdx.x, NW * 32);
                 named_barrier(1, NW * 32);
             }
             cur = st.mat;
@@ -1148,7 +1418,7 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
             const uint32_t rb = sb + static_cast<uint32_t>((srb >> 2) * p.gpitch + (srb & 3) * p.rpitch) + (cb & 15u);
             const int kbt = min(p.kb, p.nb - st.kc * p.kb);
             const uint32_t rec0 = pan_a + static_cast<uint32_t>(st.kc * p.kb * p.rec_bytes);
-            if (REGS) {
+            if constexpr (REGS) {
                 // both blocks in one straight-line sequence when the warp has
                 // two, so the scheduler can interleave their dependency chains
                 const uint32_t o0 = static_cast<uint32_t>(warp * T::kBlockBytes);

@@ -46,7 +46,10 @@ template <class T>
 inline cudaError_t mma_launch_type(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
                                    cudaStream_t s) {
     switch (l.mode) {
-    case kMmaRegs: return l.warps == 8 ? mma_launch_mode<T, kMmaRegs, 8>(p, mats, n, l, device, s) : cudaErrorInvalidValue;
+    case kMmaRegs:
+        // activation fragments in registers: Q8_K-paired types only
+        if constexpr (T::kActBytes != 0) return cudaErrorInvalidValue;
+        else return l.warps == 8 ? mma_launch_mode<T, kMmaRegs, 8>(p, mats, n, l, device, s) : cudaErrorInvalidValue;
     case kMmaPanel16:
         return l.warps == 16 ? mma_launch_mode<T, kMmaPanel16, 16>(p, mats, n, l, device, s) : cudaErrorInvalidValue;
     case kMmaPanel8:
@@ -57,6 +60,14 @@ inline cudaError_t mma_launch_type(const MmaParams &p, const MmaMat *mats, int n
 
 // One definition per weight type, each in its own translation unit.
 cudaError_t launch_gemv_mma_q4_k(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
+                                 cudaStream_t s);
+cudaError_t launch_gemv_mma_q4_0(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
+                                 cudaStream_t s);
+cudaError_t launch_gemv_mma_q4_1(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
+                                 cudaStream_t s);
+cudaError_t launch_gemv_mma_q5_0(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
+                                 cudaStream_t s);
+cudaError_t launch_gemv_mma_q8_0(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
                                  cudaStream_t s);
 cudaError_t launch_gemv_mma_q2_k(const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l, int device,
                                  cudaStream_t s);
@@ -70,6 +81,10 @@ cudaError_t launch_gemv_mma_q6_k(const MmaParams &p, const MmaMat *mats, int n, 
 inline cudaError_t launch_gemv_mma(int type, const MmaParams &p, const MmaMat *mats, int n, const MmaLaunch &l,
                                    int device, cudaStream_t s) {
     switch (type) {
+    case QG_Q4_0: return launch_gemv_mma_q4_0(p, mats, n, l, device, s);
+    case QG_Q4_1: return launch_gemv_mma_q4_1(p, mats, n, l, device, s);
+    case QG_Q5_0: return launch_gemv_mma_q5_0(p, mats, n, l, device, s);
+    case QG_Q8_0: return launch_gemv_mma_q8_0(p, mats, n, l, device, s);
     case QG_Q2_K: return launch_gemv_mma_q2_k(p, mats, n, l, device, s);
     case QG_Q3_K: return launch_gemv_mma_q3_k(p, mats, n, l, device, s);
     case QG_Q4_K: return launch_gemv_mma_q4_k(p, mats, n, l, device, s);

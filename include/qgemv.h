@@ -201,9 +201,13 @@ size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec);
  * For the K-quant weight types (Q2_K .. Q6_K) with n_vec >= 3 the sums are formed on the tensor cores
  * (mma.sync, f16 operands that hold the integer codes exactly, f32
  * accumulation per sub-block, which is exact) and the sub-block scales are
- * applied in f32 per sub-block -- the same tolerance holds. The vector count
- * from which this path is taken can be changed with the environment
- * variable QG_MMA_MIN_NVEC (read once per process).
+ * applied in f32 per sub-block -- the same tolerance holds. So are those of
+ * the 32-element types (eight blocks at a time, n_in a multiple of 256) when
+ * n_out * n_in * (n_vec - 3) >= 65 * 2^20, the size from which that kernel
+ * measured faster; the block's float step is then the one above. The vector
+ * count from which this path is taken can be changed with the environment
+ * variable QG_MMA_MIN_NVEC, the size with QG_MMA_GROUP_MELEM (in 2^20
+ * elements; both read once per process).
  * workspace: device buffer of at least qgemv_workspace_bytes(type, n_in,
  * n_vec) bytes (workspace_bytes gives its size). Limits: n_out <=
  * 2^31 - 1; n_vec * n_in must be small enough for the activations of one
@@ -226,9 +230,8 @@ int qgemv_xq(int type, const void *W, const void *xq, float *y, int64_t n_out, i
  * sum qw qx; Q4_0: sum (code - 8) qx; Q5_0: sum (code - 16) qx; Q4_1:
  * sum code qx, its min term m_w s_x being float; Q6_K: sum_j sc_j
  * sum_{i in j} (q_i - 32) a_i) ([rml] Quantized dot products, Kernels and
- * references). Runs the __dp4a kernel that qgemv_xq runs for the 32-element
- * types and for fewer
- * than 3 vectors (the tensor-core kernel accumulates the same exact sums,
+ * references). Runs the __dp4a kernel that qgemv_xq runs for fewer than 3
+ * vectors (the tensor-core kernel accumulates the same exact sums, some
  * scaled by 2^-24, but does not write them out). */
 int qgemv_block_isums(int type, const void *W, const void *xq, int32_t *isums, int64_t n_out,
                       int64_t n_in, int64_t n_vec, qg_stream_t stream);
@@ -282,7 +285,7 @@ typedef struct {
 /* Workspace bytes qgemv_batched needs for n_mats matrices: 16 when the
  * activations are small enough to be quantized inside the product (4 *
  * n_in * n_vec <= QG_FUSED_QUANT_KIB, 16 KiB by default, and not a
- * tensor-core product: a K-quant weight type with n_vec >= 3), else the quantized
+ * product that may take the tensor cores, n_vec >= 3), else the quantized
  * activations of every matrix,
  * n_mats * qgemv_workspace_bytes(type, n_in, n_vec). 0 on a bad argument. */
 size_t qgemv_batched_workspace_bytes(int type, int64_t n_in, int64_t n_vec, int n_mats);
@@ -356,7 +359,9 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
  * counterpart; the knobs choose between kernels that compute the same
  * product). name is one of the environment variables the library reads once
  * at first use: QG_CTAS_PER_SM, QG_RING_KIB, QG_MMA_MIN_NVEC (vectors from
- * which the K-quant types use the tensor cores), QG_MMA_PANEL (0 automatic, 1 a
+ * which the K-quant types use the tensor cores), QG_MMA_GROUP_MELEM (the
+ * 32-element types do from n_out * n_in * (n_vec - 3) >= this many 2^20
+ * elements; 0: from QG_MMA_MIN_NVEC vectors), QG_MMA_PANEL (0 automatic, 1 a
  * shared-memory activation panel, 8 the int8 panel), QG_MMA_KB (longest
  * chunk of blocks a panel-mode stage takes; 0 no limit), QG_FUSED_QUANT_KIB (f32 x of at most this many KiB is quantized
  * inside the GEMV), QG_FUSED_MAX_MIB (... for a single matrix of at most this

@@ -1,5 +1,8 @@
-"""The tensor-core GEMV (Q2_K / Q3_K / Q4_K / Q5_K / Q6_K weights, three or
-more vectors) against the oracle, through the C ABI.
+"""The tensor-core GEMV (the K-quant weight types, and Q4_0 / Q4_1 / Q5_0 /
+Q8_0 taken eight blocks at a time; three or more vectors) against the oracle,
+through the C ABI. The 32-element types take that kernel by default only for
+matrices of enough elements; here QG_MMA_GROUP_MELEM = 0 routes every
+product of whole 8-block groups to it.
 
 The kernel tiles 16 rows and streams each tile as chunks of whole blocks, so
 the shapes here cover a ragged last tile (n_out not a multiple of 16), rows of
@@ -21,7 +24,17 @@ from ggml_block_quantized_gb300 import synth  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
-K_TYPES = [qg.Q2_K, qg.Q3_K, qg.Q4_K, qg.Q5_K, qg.Q6_K]
+GROUPED = (qg.Q4_0, qg.Q4_1, qg.Q5_0, qg.Q8_0)  # 32-element blocks, eight to a panel block
+K_TYPES = [qg.Q2_K, qg.Q3_K, qg.Q4_K, qg.Q5_K, qg.Q6_K, *GROUPED]
+_GROUP_MELEM = {}  # the knob's value outside this module
+
+
+def wblocks(t, n_out, n_in, rng):
+    """Random weight blocks: K-quant super-blocks, or 32-element blocks of
+    uniform bytes with an f16 d of either sign (every code pattern)."""
+    if t in GROUPED:
+        return synth.legacy_blocks(t, n_out * n_in // 32, rng)
+    return synth.k_blocks(t, n_out * n_in // 256, rng)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -31,6 +44,9 @@ def _built():
     import __graft_entry__
     __graft_entry__.build()
     torch.cuda.set_device(0)
+    _GROUP_MELEM["v"] = qg.tune("QG_MMA_GROUP_MELEM", 0)
+    yield
+    qg.tune("QG_MMA_GROUP_MELEM", _GROUP_MELEM["v"])
 
 
 def dev(a):
@@ -68,7 +84,7 @@ SHAPES = [(33, 256), (40, 768), (100, 2816), (16, 4096), (257, 4096), (17, 11008
 def test_mma_shapes_all_rows(t):
     rng = np.random.default_rng(4100 + t)
     for n_out, n_in in SHAPES:
-        W = synth.k_blocks(t, n_out * n_in // 256, rng)
+        W = wblocks(t, n_out, n_in, rng)
         for n_vec in (3, 5, 8):
             x = synth.f32_normal(rng, n_vec * n_in)
             y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
@@ -79,7 +95,7 @@ def test_mma_shapes_all_rows(t):
 def test_mma_every_vector_count(t):
     rng = np.random.default_rng(4200 + t)
     n_out, n_in = 48, 2048
-    W = synth.k_blocks(t, n_out * n_in // 256, rng)
+    W = wblocks(t, n_out, n_in, rng)
     for n_vec in range(3, 9):
         x = synth.f32_normal(rng, n_vec * n_in)
         y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
@@ -90,7 +106,7 @@ def test_mma_every_vector_count(t):
 def test_mma_is_deterministic(t):
     rng = np.random.default_rng(4300 + t)
     n_out, n_in, n_vec = 1000, 11008 if t == qg.Q6_K else 4096, 8
-    Wd = dev(synth.k_blocks(t, n_out * n_in // 256, rng))
+    Wd = dev(wblocks(t, n_out, n_in, rng))
     xd = dev(synth.f32_normal(rng, n_vec * n_in))
     a = host(qg.qgemv(t, Wd, xd, n_out, n_in, n_vec))
     b = host(qg.qgemv(t, Wd, xd, n_out, n_in, n_vec))
@@ -107,7 +123,7 @@ def test_mma_batched_equals_single_calls(t):
     n_outs = [1, 15, 16, 17, 100, 700, 4096]
     mats, hw, hx = [], [], []
     for n_out in n_outs:
-        W = synth.k_blocks(t, n_out * n_in // 256, rng)
+        W = wblocks(t, n_out, n_in, rng)
         x = synth.f32_normal(rng, n_vec * n_in)
         hw.append(W)
         hx.append(x)
@@ -145,7 +161,7 @@ def test_mma_forced_plans(t):
                 assert ",panel" in info, info
             if kb:
                 assert int(info.split(" kb=")[1].split()[0]) <= kb, info
-            W = synth.k_blocks(t, n_out * n_in // 256, rng)
+            W = wblocks(t, n_out, n_in, rng)
             for n_vec in (3, 8):
                 x = synth.f32_normal(rng, n_vec * n_in)
                 y = host(qg.qgemv(t, dev(W), dev(x), n_out, n_in, n_vec))
@@ -156,16 +172,18 @@ def test_mma_forced_plans(t):
     assert qg.device_error() == 0
 
 
-@pytest.mark.parametrize("t,nbytes,dpos", [(qg.Q5_K, 176, (0, 2)), (qg.Q2_K, 84, (80, 82)), (qg.Q3_K, 110, (108,))])
-def test_mma_extreme_codes(t, nbytes, dpos):
+@pytest.mark.parametrize("t,nbytes,dpos,fill", [(qg.Q5_K, 176, (0, 2), 0xFF), (qg.Q2_K, 84, (80, 82), 0xFF),
+                                                (qg.Q3_K, 110, (108,), 0xFF), (qg.Q4_0, 18, (0,), 0xFF),
+                                                (qg.Q4_1, 20, (0, 2), 0xFF), (qg.Q5_0, 22, (0,), 0xFF),
+                                                (qg.Q8_0, 34, (0,), 0x80)])
+def test_mma_extreme_codes(t, nbytes, dpos, fill):
     """Every code at its largest (Q5_K 31: nibbles 15 and every fifth bit set;
-    Q2_K 3; Q3_K 3 with every hmask bit set), every scale and min at its
-    largest, activations at the Q8_K
-    extreme 127: the exact sub-block sums stay exact in the f32
-    accumulators."""
+    Q2_K 3; Q3_K 3 with every hmask bit set; Q4_0 / Q4_1 15; Q5_0 31; Q8_0
+    -128), every scale and min at its largest, activations at the int8
+    extreme 127: the exact block sums stay exact in the f32 accumulators."""
     rng = np.random.default_rng(4600 + t)
     n_out, n_in = 40, 4096
-    W = np.full((n_out * n_in // 256, nbytes), 0xFF, np.uint8)
+    W = np.full((n_out * n_in // (32 if t in GROUPED else 256), nbytes), fill, np.uint8)
     for p in dpos:  # d, dmin: f16 of |N(0,1)| * 1e-3
         W[:, p:p + 2] = (np.abs(rng.standard_normal((W.shape[0], 1))) * 1e-3).astype(np.float16).view(np.uint8)
     W = W.reshape(-1)
@@ -177,8 +195,17 @@ def test_mma_extreme_codes(t, nbytes, dpos):
 
 
 def test_kernel_choice_is_reported():
-    """The tensor-core kernel is the one planned for Q4_K/Q6_K from 3 vectors,
-    the __dp4a kernel below that and for Q8_0/Q4_0."""
+    """The tensor-core kernel is the one planned for the K-quant types from 3
+    vectors, the __dp4a kernel below that; the 32-element types take it by
+    default for large launches with several vectors only."""
+    qg.tune("QG_MMA_GROUP_MELEM", _GROUP_MELEM["v"])
+    try:
+        _kernel_choice()
+    finally:
+        qg.tune("QG_MMA_GROUP_MELEM", 0)
+
+
+def _kernel_choice():
     assert qg.kernel_info(qg.Q4_K, 4096, 4096, 8).startswith("gemv_mma_kernel<Q4_K,regs,8w>")
     assert qg.kernel_info(qg.Q6_K, 4096, 11008, 8).startswith("gemv_mma_kernel<Q6_K,panel8,16w>")
     assert qg.kernel_info(qg.Q4_K, 4096, 4096, 3).startswith("gemv_mma_kernel<")
@@ -187,7 +214,13 @@ def test_kernel_choice_is_reported():
     assert qg.kernel_info(qg.Q2_K, 32000, 4096, 8).startswith("gemv_mma_kernel<Q2_K,")
     assert qg.kernel_info(qg.Q3_K, 32000, 4096, 8).startswith("gemv_mma_kernel<Q3_K,")
     assert qg.kernel_info(qg.Q4_K, 4096, 4096, 2).startswith("gemv_kernel<Q4_K,NV=2>")
-    assert qg.kernel_info(qg.Q4_0, 4096, 4096, 8).startswith("gemv_kernel<Q4_0,NV=8>")
+    for t in GROUPED:
+        assert qg.kernel_info(t, 32000, 4096, 8).startswith("gemv_mma_kernel<"), t
+        assert qg.kernel_info(t, 11008, 4096, 5).startswith("gemv_mma_kernel<"), t
+        assert qg.kernel_info(t, 11008, 4096, 4).startswith("gemv_kernel<"), t
+        assert qg.kernel_info(t, 4096, 4096, 8).startswith("gemv_mma_kernel<"), t
+        assert qg.kernel_info(t, 4096, 4096, 7).startswith("gemv_kernel<"), t
+        assert qg.kernel_info(t, 4096, 96, 8).startswith("gemv_kernel<"), t  # not whole groups
     # the __dp4a kernel's two Q6_K items: two lanes per block where their
     # 16-block iterations fill (16 blocks a row), four where they would not
     # (43 blocks a row); the parity tests cover both row lengths
