@@ -140,8 +140,10 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 //    n_out * n_in times (vectors - 3) reach this many Mi (2^20): the __dp4a
 //    kernel's time grows with the vectors, the tensor-core kernel's barely,
 //    but the latter pays a fixed activation-panel prologue. Measured on this
-//    GPU, all four types at 32000 x 4096 win from 4 vectors, at 11008 x 4096
-//    from 5, at 4096 x 4096 from 8 (7 is within 5% either way);
+//    GPU, all four types win at 32000 x 4096 and 11008 x 4096 from 4 vectors
+//    (Q5_0 at 11008 ties), at 4096 x 4096 from 5 to 7 depending on the type
+//    (the default, 40, takes the tensor cores from 6 there: within 8% of
+//    the faster kernel for every type);
 //  QG_MMA_PANEL, QG_MMA_KB: mma.sync plan overrides (activation source: 0
 //    automatic, 1 a shared-memory panel, 8 the biased-int8 panel; an upper
 //    bound on blocks per chunk, 0 none);
@@ -177,7 +179,7 @@ constexpr KnobDef kKnobs[kKnobCount] = {
     {"QG_CTAS_PER_SM", 2, 1, 4},          {"QG_RING_KIB", 96, 16, 200}, {"QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1},
     {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 16, 0, 1024},
     {"QG_TC", 0, 0, 1},                   {"QG_FUSED_MAX_MIB", 1 << 20, 0, 1 << 20},
-    {"QG_FUSED_GEMM", 0, 0, 1},           {"QG_MMA_GROUP_MELEM", 65, 0, 1 << 20}};
+    {"QG_FUSED_GEMM", 0, 0, 1},           {"QG_MMA_GROUP_MELEM", 40, 0, 1 << 20}};
 std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
 
 int knob(KnobId k) {
@@ -355,7 +357,15 @@ int plan_gemv(int type, int64_t total_rows, int64_t n_in, int nv, int sms, int s
 namespace {
 
 // Slot layout for kb blocks per chunk of a row of nb blocks of `bytes` each.
-void mma_slot_layout(int nb, int kb, int bytes, int *rpitch, int *gpitch) {
+void mma_slot_layout(int nb, int kb, int bytes, int *rpitch, int *gpitch, bool apart = false) {
+    if (apart) {
+        // one copy per row, rows 16 mod 128 bytes apart and groups 32 mod
+        // 128: the 8 rows a 32-bit warp load touches (2 in each group) start
+        // on 8 different 4-bank sets
+        *rpitch = static_cast<int>((static_cast<int64_t>(kb) * bytes + 32 + 111) / 128 * 128 + 16);
+        *gpitch = (4 * *rpitch + 95) / 128 * 128 + 32;
+        return;
+    }
     const bool contig = kb == nb;
     const int64_t row = static_cast<int64_t>(nb) * bytes;
     *rpitch = contig ? static_cast<int>(row) : static_cast<int>(round16(static_cast<size_t>(kb) * bytes + 32));
@@ -430,7 +440,7 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
         for (int f = 0; f < 2; ++f) {
             const bool b16 = f == 0;
             if (b16 && force == 8) continue;
-            // grouped types: per record and vector d_x and a sum (512 bytes) for the Q8_K tail
+            // grouped types: per record and lane a float4 (512 bytes) for the Q8_K tail
             const int rec = mma_rec_bytes(b16) + (grouped ? 512 - kMmaTailBytes : 0);
             const int64_t panel = static_cast<int64_t>(nb) * rec;
             for (int ci = 0; ci < kCands; ++ci) {
@@ -438,7 +448,7 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
                 if (kb > nb || (ci > 0 && kb == nb)) continue;
                 if (tune_mma_kb() > 0 && kb > tune_mma_kb()) continue;
                 int rp, gp, S, R;
-                mma_slot_layout(nb, kb, bytes, &rp, &gp);
+                mma_slot_layout(nb, kb, bytes, &rp, &gp, grouped);
                 const int64_t stage = 4 * static_cast<int64_t>(gp);
                 const int64_t fixed = kMmaHeaderBytes + panel;
                 if (!mma_ring(smem_limit, fixed, stage, W, &S, &R)) continue;
@@ -453,7 +463,7 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
                 bp.n_chunks = n_chunks;
                 bp.rpitch = rp;
                 bp.gpitch = gp;
-                bp.contig = kb == nb ? 1 : 0;
+                bp.contig = kb == nb && !grouped ? 1 : 0;
                 bp.stage_bytes = static_cast<int>(stage);
                 bp.n_stages = S;
                 bp.red_slots = R;

@@ -185,11 +185,26 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// D = A x B + C with C given apart from D.
+__device__ __forceinline__ void mma_16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1, float c0, float c1, float c2, float c3) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
 // The k = 8 form: a0/a1 = rows g/g+8, columns 2t,2t+1; b0 = rows 2t,2t+1 of column g.
 __device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
     asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Two f16 lanes minus the two f16 lanes of c.
+__device__ __forceinline__ uint32_t hsub2c(uint32_t h, uint32_t c) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(c));
+    return r;
 }
 
 // Two f16 lanes minus 1152 each (exact for the integers used here).
@@ -200,8 +215,8 @@ __device__ __forceinline__ uint32_t hsub1152(uint32_t h) {
 }
 
 // The B fragments of record r for this lane: b[0], b[1] for the record's
-// first mma, b[2], b[3] for its second.
-template <bool B16>
+// first mma, b[2], b[3] for its second (HI: the second run divided by 16).
+template <bool B16, bool HI = false>
 __device__ __forceinline__ void mma_load_b(uint32_t rec, int r, int lane, uint32_t (&b)[4]) {
     if (B16) {
         const uint4 v = ld_s128(rec + static_cast<uint32_t>((r * 32 + lane) * 16));
@@ -215,8 +230,15 @@ __device__ __forceinline__ void mma_load_b(uint32_t rec, int r, int lane, uint32
         const uint2 v = ld_s64(rec + static_cast<uint32_t>((r * 32 + lane) * 8));
         b[0] = hsub1152(__byte_perm(v.x, 0x64646464u, 0x4140));
         b[1] = hsub1152(__byte_perm(v.x, 0x64646464u, 0x4342));
-        b[2] = hsub1152(__byte_perm(v.y, 0x64646464u, 0x4140));
-        b[3] = hsub1152(__byte_perm(v.y, 0x64646464u, 0x4342));
+        if constexpr (HI) {
+            // under 0x54 a byte c is the f16 64 + c/16 (steps of 1/16 in
+            // [64, 128)); minus 72 gives (c - 128)/16
+            b[2] = hsub2c(__byte_perm(v.y, 0x54545454u, 0x4140), 0x54805480u);
+            b[3] = hsub2c(__byte_perm(v.y, 0x54545454u, 0x4342), 0x54805480u);
+        } else {
+            b[2] = hsub1152(__byte_perm(v.y, 0x64646464u, 0x4140));
+            b[3] = hsub1152(__byte_perm(v.y, 0x64646464u, 0x4342));
+        }
     }
 }
 
@@ -227,22 +249,18 @@ __device__ __forceinline__ uint32_t mma_pack(unsigned short lo, unsigned short h
 // A warp's B operands for one weight block: the fragments of record r
 // (b(r, .)), the correction operand of the lane and d_x / block sums of
 // vectors 2t, 2t+1 -- read from the shared-memory panel ...
-template <bool B16>
+template <bool B16, bool HI = false>
 struct MmaSmemB {
     uint32_t rec;
     int lane;
-    __device__ __forceinline__ void b(int r, uint32_t (&bf)[4]) const { mma_load_b<B16>(rec, r, lane, bf); }
+    __device__ __forceinline__ void b(int r, uint32_t (&bf)[4]) const { mma_load_b<B16, HI>(rec, r, lane, bf); }
     __device__ __forceinline__ uint32_t corr32() const { return ld_s32(rec + mma_frag_bytes(B16) + 8 * lane); }
     __device__ __forceinline__ uint2 corr64() const { return ld_s64(rec + mma_frag_bytes(B16) + 8 * lane); }
     __device__ __forceinline__ uint2 dxw(int t) const { return ld_s64(rec + mma_frag_bytes(B16) + 256 + 8 * t); }
     __device__ __forceinline__ uint2 bsw(int t) const { return ld_s64(rec + mma_frag_bytes(B16) + 288 + 8 * t); }
-    // groups of 32-element blocks: d_x and (Q8_1) s of record r, vectors 2t
-    // and 2t+1
-    __device__ __forceinline__ uint2 dxr(int r, int t) const {
-        return ld_s64(rec + mma_frag_bytes(B16) + static_cast<uint32_t>(4 * (8 * r + 2 * t)));
-    }
-    __device__ __forceinline__ uint2 axr(int r, int t) const {
-        return ld_s64(rec + mma_frag_bytes(B16) + 256 + static_cast<uint32_t>(4 * (8 * r + 2 * t)));
+    // groups of 32-element blocks: the tail float4 of record r and lane t
+    __device__ __forceinline__ uint4 tail(int r, int t) const {
+        return ld_s128(rec + mma_frag_bytes(B16) + static_cast<uint32_t>(64 * r + 16 * t));
     }
 };
 
@@ -273,6 +291,7 @@ struct MmaRegB {
 struct MmaQ4_K {
     static constexpr int kBlockBytes = 144;
     static constexpr int kActBytes = 0;  // activations: Q8_K blocks (the panel's bsums tail)
+    static constexpr bool kHiScaled = false;
 
     // Element offsets (within the block) of the two 4-code runs of record r
     // for lane t; the run is permuted to slots {0,2,1,3}.
@@ -447,6 +466,7 @@ struct MmaQ5_K : MmaQ4_K {
 struct MmaQ6_K {
     static constexpr int kBlockBytes = 210;
     static constexpr int kActBytes = 0;  // activations: Q8_K blocks (the panel's bsums tail)
+    static constexpr bool kHiScaled = false;
 
     __device__ static int run0(int r, int t) { return 32 * r + 4 * t; }
     __device__ static int run1(int r, int t) { return 32 * r + 16 + 4 * t; }
@@ -738,190 +758,238 @@ struct MmaQ3_K : MmaQ6_K {
 // Q4_0, Q5_0, Q4_1 and Q8_0 rows are taken eight blocks (256 elements) at a
 // time: one panel block per group, record r = block r of the group
 // ("Building Q8_0 and Q4_0 Like ggml", Examples 1, 5, 7 and 8; "量化格式"
-// (candle), block structure table). Lane (g, t) takes elements 4t..4t+3 and
-// 16 + 4t..16 + 4t + 3 of each block of rows g and g + 8 (the runs of the
-// records); block sums are exact in the mma's f32 accumulators (integer
-// codes times activations of at most 127, 32 of them), then each block's
-// float step is applied per row and vector: d_w d_x S (+ m_w s_x for Q4_1).
+// (candle), block structure table). Lane (g, t) takes elements 4t..4t+3 (the
+// record's first run: the block's first mma) and 16 + 4t..16 + 4t + 3 (the
+// second run: its second mma) of each block of rows g and g + 8.
+//  * Codes enter unsigned, as f16 subnormal bit patterns cut from the block
+//    bytes by one mask: code c (Q8_0: q + 128) is c 2^-24. Where a code's
+//    low bits sit at bits 4..7 of a byte (the second run of Q4_0, Q4_1 and
+//    Q5_0) the mask leaves them there, giving 16 c 2^-24, and the panel holds
+//    that run's activations divided by 16 (exact in f16): every product is
+//    c a 2^-24 exactly.
+//  * The offset of the signed types (value (c - bias) d) is the mma
+//    accumulator's initial value -bias S 2^-24, S = the block's activation
+//    code sum, which the panel holds per block and vector. The block's
+//    exact sum of (c - bias) a, times 2^-24, is then the mma's result (every
+//    partial sum an integer times 2^-24 of magnitude below 1: exact in f32).
+//  * A group's rows start 16-byte aligned in the ring (eight blocks are a
+//    multiple of 16 bytes and so is every row and chunk offset), so the
+//    alignment of each field is fixed by its block index; a 2-byte aligned
+//    word is read as its two aligned neighbours, whose bytes one permute per
+//    operand sorts into even and odd bytes.
+// The panel's tail holds per record r and lane t the float4 {d_x 2^24 of
+// vectors 2t, 2t+1; the accumulator's initial value for the same vectors
+// (Q4_1: s_x)}.
 
-// Four codes (one per byte, c + bias in 0..255) of a word as the mma's two A
-// registers of one row, exact f16 integers c: bytes 0,2 (k-slots 2t, 2t+1)
-// and bytes 1,3 (slots 2t+8, 2t+9) each placed under 0x64 (the f16 1024 + c
-// + bias), then 1024 + bias subtracted -- so a signed code needs no offset
-// term and no activation sums.
-__device__ __forceinline__ uint32_t hsub2c(uint32_t h, uint32_t c) {
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(c));
-    return r;
-}
-template <uint32_t BIASED_1024>
-__device__ __forceinline__ uint32_t mma_even_s(uint32_t c) {
-    return hsub2c(__byte_perm(c, 0x64646464u, 0x4240), BIASED_1024);
-}
-template <uint32_t BIASED_1024>
-__device__ __forceinline__ uint32_t mma_odd_s(uint32_t c) {
-    return hsub2c(__byte_perm(c, 0x64646464u, 0x4341), BIASED_1024);
+// The 4-byte word at base + 4t + OFF (base 16-byte aligned, OFF a constant)
+// as E = its bytes 0 and 2 in the low byte of each 16-bit lane and O = its
+// bytes 1 and 3 likewise; the high byte of each lane is unspecified.
+template <int OFF>
+__device__ __forceinline__ void mma_eo(uint32_t base_t, uint32_t &E, uint32_t &O) {
+    if constexpr (OFF % 4 == 0) {
+        E = ld_s32(base_t + OFF);
+        O = E >> 8;
+    } else {
+        static_assert(OFF % 4 == 2, "block fields are 2-byte aligned");
+        const uint32_t w0 = ld_s32(base_t + OFF - 2), w1 = ld_s32(base_t + OFF + 2);
+        E = __byte_perm(w0, w1, 0x0402);
+        O = __byte_perm(w0, w1, 0x0503);
+    }
 }
 
-// One block's float step for rows g, g+8 and vectors 2t, 2t+1, from the
-// exact block sums C (integers in f32).
-__device__ __forceinline__ void mma_block_step(const float (&C)[4], float dwa, float dwb, uint2 dxw, float (&acc)[4]) {
-    const float2 dx = make_float2(__uint_as_float(dxw.x), __uint_as_float(dxw.y));
-    const float2 a01 = ffma2(make_float2(dwa * dx.x, dwa * dx.y), make_float2(C[0], C[1]), make_float2(acc[0], acc[1]));
-    const float2 a23 = ffma2(make_float2(dwb * dx.x, dwb * dx.y), make_float2(C[2], C[3]), make_float2(acc[2], acc[3]));
+// The 4 bytes at base + OFF (same alignment rule), as one word.
+template <int OFF>
+__device__ __forceinline__ uint32_t mma_word(uint32_t base) {
+    if constexpr (OFF % 4 == 0) {
+        return ld_s32(base + OFF);
+    } else {
+        static_assert(OFF % 4 == 2, "block fields are 2-byte aligned");
+        return __byte_perm(ld_s32(base + OFF - 2), ld_s32(base + OFF + 2), 0x5432);
+    }
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// The first mma of a block, its accumulator starting from the tail's
+// initial values (rows g, g+8; vectors 2t, 2t+1).
+__device__ __forceinline__ void mma_group_first(float (&C)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t b0, uint32_t b1, uint4 tl) {
+    const float c0 = __uint_as_float(tl.z), c1 = __uint_as_float(tl.w);
+    mma_16816_c(C, a0, a1, a2, a3, b0, b1, c0, c1, c0, c1);
+}
+
+// acc += d_w (d_x 2^24) C for rows g, g+8 and vectors 2t, 2t+1.
+__device__ __forceinline__ void mma_group_step(const float (&C)[4], float dwa, float dwb, uint4 tl, float (&acc)[4]) {
+    const float2 dx = make_float2(__uint_as_float(tl.x), __uint_as_float(tl.y));
+    const float2 a01 = ffma2(fmul2(make_float2(dwa, dwa), dx), make_float2(C[0], C[1]), make_float2(acc[0], acc[1]));
+    const float2 a23 = ffma2(fmul2(make_float2(dwb, dwb), dx), make_float2(C[2], C[3]), make_float2(acc[2], acc[3]));
     acc[0] = a01.x;
     acc[1] = a01.y;
     acc[2] = a23.x;
     acc[3] = a23.y;
 }
 
+// The eight blocks of a group, unrolled (each block's field offsets, and so
+// their alignment, are constants).
+template <class T, class BS, int R = 0>
+__device__ __forceinline__ void mma_group_blocks(uint32_t ra, uint32_t rb, const BS &B, int t, float (&acc)[4]) {
+    T::template block<R>(ra, rb, B, t, acc);
+    if constexpr (R + 1 < kMmaRecords) mma_group_blocks<T, BS, R + 1>(ra, rb, B, t, acc);
+}
+
 // Q4_0: 18-byte blocks (f16 d, qs[16]: byte k = code k | code k+16 << 4),
-// value (code - 8) d, paired with Q8_0 activations. The mma takes the signed
-// values code - 8 (f16 1024 + code minus 1032).
+// value (code - 8) d, paired with Q8_0 activations.
 struct MmaQ4_0 {
     static constexpr int kBlockBytes = 8 * 18;
     static constexpr int kActBytes = 34;
+    static constexpr int kBias = 8;
+    static constexpr bool kHiScaled = true;
 
+    template <int R, class BS>
+    __device__ __forceinline__ static void block(uint32_t ra, uint32_t rb, const BS &B, int t, float (&acc)[4]) {
+        uint32_t Ea, Oa, Eb, Ob;
+        mma_eo<18 * R + 2>(ra + 4 * t, Ea, Oa);  // qs[4t..4t+3]
+        mma_eo<18 * R + 2>(rb + 4 * t, Eb, Ob);
+        const float dwa = f16_bits_to_f32(ld_s16(ra + 18 * R)), dwb = f16_bits_to_f32(ld_s16(rb + 18 * R));
+        uint32_t bf[4];
+        B.b(R, bf);
+        const uint4 tl = B.tail(R, t);
+        float C[4];
+        mma_group_first(C, Ea & 0x000F000Fu, Eb & 0x000F000Fu, Oa & 0x000F000Fu, Ob & 0x000F000Fu, bf[0], bf[1], tl);
+        mma_16816(C, Ea & 0x00F000F0u, Eb & 0x00F000F0u, Oa & 0x00F000F0u, Ob & 0x00F000F0u, bf[2], bf[3]);
+        mma_group_step(C, dwa, dwb, tl, acc);
+    }
     template <class BS>
     __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
                                                       float (&acc)[4]) {
-        const int t = lane & 3;
-        constexpr uint32_t k1032 = 0x64086408u;
-#pragma unroll 2
-        for (int r = 0; r < 8; ++r) {
-            const uint32_t a = ra + 18u * r, b = rb + 18u * r;  // 2-byte aligned blocks
-            uint32_t wa[1], wb[1];
-            ld_words_a2<1>(a + 2 + 4 * t, wa);  // qs[4t..4t+3]: codes 4t.. (low), 16 + 4t.. (high)
-            ld_words_a2<1>(b + 2 + 4 * t, wb);
-            const float dwa = f16_bits_to_f32(ld_s16(a)), dwb = f16_bits_to_f32(ld_s16(b));
-            uint32_t bf[4];
-            B.b(r, bf);
-            float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint32_t la = wa[0] & 0x0F0F0F0Fu, lb = wb[0] & 0x0F0F0F0Fu;
-            const uint32_t ha = (wa[0] >> 4) & 0x0F0F0F0Fu, hb = (wb[0] >> 4) & 0x0F0F0F0Fu;
-            mma_16816(C, mma_even_s<k1032>(la), mma_even_s<k1032>(lb), mma_odd_s<k1032>(la), mma_odd_s<k1032>(lb),
-                      bf[0], bf[1]);
-            mma_16816(C, mma_even_s<k1032>(ha), mma_even_s<k1032>(hb), mma_odd_s<k1032>(ha), mma_odd_s<k1032>(hb),
-                      bf[2], bf[3]);
-            mma_block_step(C, dwa, dwb, B.dxr(r, t), acc);
-        }
+        mma_group_blocks<MmaQ4_0>(ra, rb, B, lane & 3, acc);
     }
 };
 
 // Q8_0: 34-byte blocks (f16 d, 32 int8 codes), value q d, paired with Q8_0
-// activations. The mma takes q as f16 (1024 + (q + 128) minus 1152).
+// activations; the mma takes q + 128.
 struct MmaQ8_0 {
     static constexpr int kBlockBytes = 8 * 34;
     static constexpr int kActBytes = 34;
+    static constexpr int kBias = 128;
+    static constexpr bool kHiScaled = false;
 
+    __device__ __forceinline__ static uint32_t u(uint32_t e) { return (e ^ 0x00800080u) & 0x00FF00FFu; }
+
+    template <int R, class BS>
+    __device__ __forceinline__ static void block(uint32_t ra, uint32_t rb, const BS &B, int t, float (&acc)[4]) {
+        uint32_t Ea, Oa, Eb, Ob, Fa, Pa, Fb, Pb;
+        mma_eo<34 * R + 2>(ra + 4 * t, Ea, Oa);  // codes 4t..4t+3
+        mma_eo<34 * R + 2>(rb + 4 * t, Eb, Ob);
+        mma_eo<34 * R + 18>(ra + 4 * t, Fa, Pa);  // codes 16 + 4t..
+        mma_eo<34 * R + 18>(rb + 4 * t, Fb, Pb);
+        const float dwa = f16_bits_to_f32(ld_s16(ra + 34 * R)), dwb = f16_bits_to_f32(ld_s16(rb + 34 * R));
+        uint32_t bf[4];
+        B.b(R, bf);
+        const uint4 tl = B.tail(R, t);
+        float C[4];
+        mma_group_first(C, u(Ea), u(Eb), u(Oa), u(Ob), bf[0], bf[1], tl);
+        mma_16816(C, u(Fa), u(Fb), u(Pa), u(Pb), bf[2], bf[3]);
+        mma_group_step(C, dwa, dwb, tl, acc);
+    }
     template <class BS>
     __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
                                                       float (&acc)[4]) {
-        const int t = lane & 3;
-        constexpr uint32_t k1152 = 0x64806480u;
-#pragma unroll 2
-        for (int r = 0; r < 8; ++r) {
-            const uint32_t a = ra + 34u * r, b = rb + 34u * r;
-            uint32_t wa[1], wb[1], va[1], vb[1];
-            ld_words_a2<1>(a + 2 + 4 * t, wa);  // codes 4t .. 4t+3
-            ld_words_a2<1>(b + 2 + 4 * t, wb);
-            ld_words_a2<1>(a + 18 + 4 * t, va);  // codes 16 + 4t ..
-            ld_words_a2<1>(b + 18 + 4 * t, vb);
-            const float dwa = f16_bits_to_f32(ld_s16(a)), dwb = f16_bits_to_f32(ld_s16(b));
-            uint32_t bf[4];
-            B.b(r, bf);
-            float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint32_t la = wa[0] ^ 0x80808080u, lb = wb[0] ^ 0x80808080u;
-            const uint32_t ha = va[0] ^ 0x80808080u, hb = vb[0] ^ 0x80808080u;
-            mma_16816(C, mma_even_s<k1152>(la), mma_even_s<k1152>(lb), mma_odd_s<k1152>(la), mma_odd_s<k1152>(lb),
-                      bf[0], bf[1]);
-            mma_16816(C, mma_even_s<k1152>(ha), mma_even_s<k1152>(hb), mma_odd_s<k1152>(ha), mma_odd_s<k1152>(hb),
-                      bf[2], bf[3]);
-            mma_block_step(C, dwa, dwb, B.dxr(r, t), acc);
-        }
+        mma_group_blocks<MmaQ8_0>(ra, rb, B, lane & 3, acc);
     }
 };
 
-// Four bits (bit i of n, n < 16) to bit 0 of byte i: the four shifted copies
-// of n do not overlap, so the product carries nothing between them.
-__device__ __forceinline__ uint32_t spread4(uint32_t n) { return (n * 0x00204081u) & 0x01010101u; }
-
 // Q5_0: 22-byte blocks (f16 d, u32 qh: bit j = fifth bit of code j, qs[16]
-// as in Q4_0), value (code - 16) d, paired with Q8_0 activations. The mma
-// takes code - 16 (f16 1024 + code minus 1040).
+// as in Q4_0), value (code - 16) d, paired with Q8_0 activations. A lane's
+// nibble n of qh (the fifth bits of its 4 codes of one run) is spread to
+// bits 0, 8, 16, 24 by one multiply (the four shifted copies of n do not
+// overlap), then each pair is shifted under its code: bits 4 and 20 in the
+// first run, 8 and 24 in the second (where the code is 16 c).
 struct MmaQ5_0 {
     static constexpr int kBlockBytes = 8 * 22;
     static constexpr int kActBytes = 34;
+    static constexpr int kBias = 16;
+    static constexpr bool kHiScaled = true;
 
+    __device__ __forceinline__ static void ops(uint32_t E, uint32_t O, uint32_t n0, uint32_t n1, uint32_t (&a)[4]) {
+        const uint32_t x0 = ((n0 & 15u) * 0x00204081u) & 0x01010101u;
+        const uint32_t x1 = ((n1 & 15u) * 0x00204081u) & 0x01010101u;
+        a[0] = (E & 0x000F000Fu) | ((x0 << 4) & 0x00100010u);
+        a[1] = (O & 0x000F000Fu) | ((x0 >> 4) & 0x00100010u);
+        a[2] = (E & 0x00F000F0u) | ((x1 << 8) & 0x01000100u);
+        a[3] = (O & 0x00F000F0u) | (x1 & 0x01000100u);
+    }
+
+    template <int R, class BS>
+    __device__ __forceinline__ static void block(uint32_t ra, uint32_t rb, const BS &B, int t, float (&acc)[4]) {
+        uint32_t Ea, Oa, Eb, Ob;
+        mma_eo<22 * R + 6>(ra + 4 * t, Ea, Oa);  // qs[4t..4t+3]
+        mma_eo<22 * R + 6>(rb + 4 * t, Eb, Ob);
+        const uint32_t qa = mma_word<22 * R + 2>(ra), qb = mma_word<22 * R + 2>(rb);
+        const float dwa = f16_bits_to_f32(ld_s16(ra + 22 * R)), dwb = f16_bits_to_f32(ld_s16(rb + 22 * R));
+        uint32_t xa[4], xb[4];
+        ops(Ea, Oa, qa >> (4 * t), qa >> (16 + 4 * t), xa);
+        ops(Eb, Ob, qb >> (4 * t), qb >> (16 + 4 * t), xb);
+        uint32_t bf[4];
+        B.b(R, bf);
+        const uint4 tl = B.tail(R, t);
+        float C[4];
+        mma_group_first(C, xa[0], xb[0], xa[1], xb[1], bf[0], bf[1], tl);
+        mma_16816(C, xa[2], xb[2], xa[3], xb[3], bf[2], bf[3]);
+        mma_group_step(C, dwa, dwb, tl, acc);
+    }
     template <class BS>
     __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
                                                       float (&acc)[4]) {
-        const int t = lane & 3;
-        constexpr uint32_t k1040 = 0x64106410u;
-#pragma unroll 2
-        for (int r = 0; r < 8; ++r) {
-            const uint32_t a = ra + 22u * r, b = rb + 22u * r;
-            uint32_t wa[1], wb[1], qa[1], qb[1];
-            ld_words_a2<1>(a + 2, qa);
-            ld_words_a2<1>(b + 2, qb);
-            ld_words_a2<1>(a + 6 + 4 * t, wa);
-            ld_words_a2<1>(b + 6 + 4 * t, wb);
-            const float dwa = f16_bits_to_f32(ld_s16(a)), dwb = f16_bits_to_f32(ld_s16(b));
-            uint32_t bf[4];
-            B.b(r, bf);
-            float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint32_t la = (wa[0] & 0x0F0F0F0Fu) | (spread4((qa[0] >> (4 * t)) & 0xFu) << 4);
-            const uint32_t lb = (wb[0] & 0x0F0F0F0Fu) | (spread4((qb[0] >> (4 * t)) & 0xFu) << 4);
-            const uint32_t ha = ((wa[0] >> 4) & 0x0F0F0F0Fu) | (spread4((qa[0] >> (16 + 4 * t)) & 0xFu) << 4);
-            const uint32_t hb = ((wb[0] >> 4) & 0x0F0F0F0Fu) | (spread4((qb[0] >> (16 + 4 * t)) & 0xFu) << 4);
-            mma_16816(C, mma_even_s<k1040>(la), mma_even_s<k1040>(lb), mma_odd_s<k1040>(la), mma_odd_s<k1040>(lb),
-                      bf[0], bf[1]);
-            mma_16816(C, mma_even_s<k1040>(ha), mma_even_s<k1040>(hb), mma_odd_s<k1040>(ha), mma_odd_s<k1040>(hb),
-                      bf[2], bf[3]);
-            mma_block_step(C, dwa, dwb, B.dxr(r, t), acc);
-        }
+        mma_group_blocks<MmaQ5_0>(ra, rb, B, lane & 3, acc);
     }
 };
 
 // Q4_1: 20-byte blocks (f16 d, f16 m, qs[16] as in Q4_0), value code d + m,
 // paired with Q8_1 activations (d_x, s = d_x sum q): per block
-// d d_x sum(code q) + m s. The mma takes the unsigned codes (f16 1024 + code
-// minus 1024).
+// d d_x sum(code q) + m s.
 struct MmaQ4_1 {
     static constexpr int kBlockBytes = 8 * 20;
     static constexpr int kActBytes = 36;
+    static constexpr int kBias = 0;
+    static constexpr bool kHiScaled = true;
 
+    template <int R, class BS>
+    __device__ __forceinline__ static void block(uint32_t ra, uint32_t rb, const BS &B, int t, float (&acc)[4]) {
+        uint32_t Ea, Oa, Eb, Ob;
+        mma_eo<20 * R + 4>(ra + 4 * t, Ea, Oa);
+        mma_eo<20 * R + 4>(rb + 4 * t, Eb, Ob);
+        const uint32_t ha = ld_s32(ra + 20 * R), hb = ld_s32(rb + 20 * R);  // d | m << 16
+        const float dwa = f16_bits_to_f32(ha & 0xFFFFu), dwb = f16_bits_to_f32(hb & 0xFFFFu);
+        const float ma = f16_bits_to_f32(ha >> 16), mb = f16_bits_to_f32(hb >> 16);
+        uint32_t bf[4];
+        B.b(R, bf);
+        const uint4 tl = B.tail(R, t);
+        float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_16816(C, Ea & 0x000F000Fu, Eb & 0x000F000Fu, Oa & 0x000F000Fu, Ob & 0x000F000Fu, bf[0], bf[1]);
+        mma_16816(C, Ea & 0x00F000F0u, Eb & 0x00F000F0u, Oa & 0x00F000F0u, Ob & 0x00F000F0u, bf[2], bf[3]);
+        const float2 sx = make_float2(__uint_as_float(tl.z), __uint_as_float(tl.w));
+        const float2 m01 = ffma2(make_float2(ma, ma), sx, make_float2(acc[0], acc[1]));
+        const float2 m23 = ffma2(make_float2(mb, mb), sx, make_float2(acc[2], acc[3]));
+        float m4[4] = {m01.x, m01.y, m23.x, m23.y};
+        mma_group_step(C, dwa, dwb, tl, m4);
+        acc[0] = m4[0];
+        acc[1] = m4[1];
+        acc[2] = m4[2];
+        acc[3] = m4[3];
+    }
     template <class BS>
     __device__ __forceinline__ static void tile_block(uint32_t ra, uint32_t rb, const BS &B, int lane,
                                                       float (&acc)[4]) {
-        const int t = lane & 3;
-        constexpr uint32_t k1024 = 0x64006400u;
-#pragma unroll 2
-        for (int r = 0; r < 8; ++r) {
-            const uint32_t a = ra + 20u * r, b = rb + 20u * r;
-            uint32_t wa[1], wb[1];
-            ld_words_a2<1>(a + 4 + 4 * t, wa);
-            ld_words_a2<1>(b + 4 + 4 * t, wb);
-            const float dwa = f16_bits_to_f32(ld_s16(a)), dwb = f16_bits_to_f32(ld_s16(b));
-            const float ma = f16_bits_to_f32(ld_s16(a + 2)), mb = f16_bits_to_f32(ld_s16(b + 2));
-            uint32_t bf[4];
-            B.b(r, bf);
-            float C[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint32_t la = wa[0] & 0x0F0F0F0Fu, lb = wb[0] & 0x0F0F0F0Fu;
-            const uint32_t ha = (wa[0] >> 4) & 0x0F0F0F0Fu, hb = (wb[0] >> 4) & 0x0F0F0F0Fu;
-            mma_16816(C, mma_even_s<k1024>(la), mma_even_s<k1024>(lb), mma_odd_s<k1024>(la), mma_odd_s<k1024>(lb),
-                      bf[0], bf[1]);
-            mma_16816(C, mma_even_s<k1024>(ha), mma_even_s<k1024>(hb), mma_odd_s<k1024>(ha), mma_odd_s<k1024>(hb),
-                      bf[2], bf[3]);
-            const uint2 sw = B.axr(r, t);
-            const float2 s = make_float2(__uint_as_float(sw.x), __uint_as_float(sw.y));
-            float m4[4] = {ma * s.x + acc[0], ma * s.y + acc[1], mb * s.x + acc[2], mb * s.y + acc[3]};
-            mma_block_step(C, dwa, dwb, B.dxr(r, t), m4);
-            acc[0] = m4[0];
-            acc[1] = m4[1];
-            acc[2] = m4[2];
-            acc[3] = m4[3];
-        }
+        mma_group_blocks<MmaQ4_1>(ra, rb, B, lane & 3, acc);
     }
 };
 
@@ -1012,9 +1080,10 @@ __device__ __forceinline__ void mma_build_panel(const MmaParams &p, const uint8_
 // [nv][8 nb] into the panel, for weights in groups of eight 32-element blocks
 // (one panel block per group): record r = activation block r of the group,
 // its two 4-code runs at codes 4t and 16 + 4t permuted to slots {0,2,1,3}
-// (the layout of the Q6_K records); then per record and vector d_x (f32)
-// and, for Q8_1, its s, as [record][vector] floats. Vectors g >= nv are
-// zero.
+// (the layout of the Q6_K records; the second run divided by 16 in the f16
+// panel when T::kHiScaled); then per record and lane t the float4 {d_x 2^24,
+// d_x 2^24, c, c} of vectors 2t, 2t+1, c = -T::kBias * (sum of the block's
+// codes) * 2^-24 (Q8_1: its s). Vectors g >= nv are zero.
 template <class T, bool B16>
 __device__ __forceinline__ void mma_build_panel_q8(const MmaParams &p, const uint8_t *xq, uint8_t *pan, int tid,
                                                    int nthr) {
@@ -1047,30 +1116,47 @@ __device__ __forceinline__ void mma_build_panel_q8(const MmaParams &p, const uin
             const int b = u / (kMmaRecords * 32), r = (u / 32) % kMmaRecords, L = u % 32;
             const uint32_t x0 = __byte_perm(w0[i], 0u, 0x3120), x1 = __byte_perm(w1[i], 0u, 0x3120);
             uint8_t *dst = pan + static_cast<size_t>(b) * p.rec_bytes;
+            if constexpr (T::kBias != 0) {
+                // the block's code sum S: the 4 lanes t of vector g hold its
+                // 32 codes (lanes 4g..4g+3 of this warp, the same u / 32);
+                // lane t = 0 stores the accumulator's start -bias S 2^-24
+                // (exact: |bias S| < 2^24)
+                int sum = __dp4a(static_cast<int>(w0[i]), 0x01010101, __dp4a(static_cast<int>(w1[i]), 0x01010101, 0));
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                if ((L & 3) == 0) {
+                    const int g = L >> 2;
+                    reinterpret_cast<float *>(dst + mma_frag_bytes(B16))[16 * r + 4 * (g >> 1) + 2 + (g & 1)] =
+                        static_cast<float>(-T::kBias * sum) * 5.9604644775390625e-8f;
+                }
+            }
             if (B16) {
                 uint4 o;
                 o.x = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x0, 0))), __half_as_ushort(__int2half_rn(sbyte(x0, 1))));
                 o.y = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x0, 2))), __half_as_ushort(__int2half_rn(sbyte(x0, 3))));
-                o.z = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x1, 0))), __half_as_ushort(__int2half_rn(sbyte(x1, 1))));
-                o.w = mma_pack(__half_as_ushort(__int2half_rn(sbyte(x1, 2))), __half_as_ushort(__int2half_rn(sbyte(x1, 3))));
+                constexpr float hs = T::kHiScaled ? 0.0625f : 1.0f;  // exact: a power of two
+                o.z = mma_pack(__half_as_ushort(__float2half_rn(hs * sbyte(x1, 0))),
+                               __half_as_ushort(__float2half_rn(hs * sbyte(x1, 1))));
+                o.w = mma_pack(__half_as_ushort(__float2half_rn(hs * sbyte(x1, 2))),
+                               __half_as_ushort(__float2half_rn(hs * sbyte(x1, 3))));
                 reinterpret_cast<uint4 *>(dst)[r * 32 + L] = o;
             } else {
                 reinterpret_cast<uint2 *>(dst)[r * 32 + L] = make_uint2(x0 ^ 0x80808080u, x1 ^ 0x80808080u);
             }
         }
     }
-    // per (group, record, vector): d_x and (Q8_1) s
+    // per (group, record, vector): d_x 2^24 and (Q8_1) s
     for (int u = tid; u < nb * kMmaRecords * kMmaNvec; u += nthr) {
         const int b = u / (kMmaRecords * kMmaNvec), r = (u / kMmaNvec) % kMmaRecords, v = u % kMmaNvec;
-        float dx = 0.0f, aux = 0.0f;
+        float dx = 0.0f, sx = 0.0f;
         if (v < nv) {
             const uint8_t *blk = xq + (static_cast<size_t>(v) * nb32 + 8 * b + r) * AB;
-            dx = f16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t *>(blk)));
-            if (AB == 36) aux = f16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t *>(blk + 2)));  // Q8_1 s
+            dx = f16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t *>(blk))) * 16777216.0f;
+            if constexpr (AB == 36) sx = f16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t *>(blk + 2)));
         }
         float *tail = reinterpret_cast<float *>(pan + static_cast<size_t>(b) * p.rec_bytes + mma_frag_bytes(B16));
-        tail[8 * r + v] = dx;
-        tail[64 + 8 * r + v] = aux;
+        tail[16 * r + 4 * (v >> 1) + (v & 1)] = dx;
+        if constexpr (T::kBias == 0) tail[16 * r + 4 * (v >> 1) + 2 + (v & 1)] = sx;
     }
 }
 
@@ -1432,7 +1518,8 @@ __global__ void __launch_bounds__(mma_warps(BMODE, NW) * 32, 1) gemv_mma_kernel(
             } else {
                 for (int kb = warp; kb < kbt; kb += NW)
                     T::tile_block(ra + kb * T::kBlockBytes, rb + kb * T::kBlockBytes,
-                                  MmaSmemB<B16>{rec0 + static_cast<uint32_t>(kb * p.rec_bytes), lane}, lane, acc);
+                                  MmaSmemB<B16, T::kHiScaled>{rec0 + static_cast<uint32_t>(kb * p.rec_bytes), lane},
+                                  lane, acc);
             }
         }
         bool last_warp = false;

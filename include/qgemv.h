@@ -203,7 +203,7 @@ size_t qgemv_workspace_bytes(int type, int64_t n_in, int64_t n_vec);
  * accumulation per sub-block, which is exact) and the sub-block scales are
  * applied in f32 per sub-block -- the same tolerance holds. So are those of
  * the 32-element types (eight blocks at a time, n_in a multiple of 256) when
- * n_out * n_in * (n_vec - 3) >= 65 * 2^20, the size from which that kernel
+ * n_out * n_in * (n_vec - 3) >= 40 * 2^20, the size from which that kernel
  * measured faster; the block's float step is then the one above. The vector
  * count from which this path is taken can be changed with the environment
  * variable QG_MMA_MIN_NVEC, the size with QG_MMA_GROUP_MELEM (in 2^20

@@ -216,10 +216,9 @@ def _kernel_choice():
     assert qg.kernel_info(qg.Q4_K, 4096, 4096, 2).startswith("gemv_kernel<Q4_K,NV=2>")
     for t in GROUPED:
         assert qg.kernel_info(t, 32000, 4096, 8).startswith("gemv_mma_kernel<"), t
-        assert qg.kernel_info(t, 11008, 4096, 5).startswith("gemv_mma_kernel<"), t
-        assert qg.kernel_info(t, 11008, 4096, 4).startswith("gemv_kernel<"), t
-        assert qg.kernel_info(t, 4096, 4096, 8).startswith("gemv_mma_kernel<"), t
-        assert qg.kernel_info(t, 4096, 4096, 7).startswith("gemv_kernel<"), t
+        assert qg.kernel_info(t, 11008, 4096, 4).startswith("gemv_mma_kernel<"), t
+        assert qg.kernel_info(t, 4096, 4096, 6).startswith("gemv_mma_kernel<"), t
+        assert qg.kernel_info(t, 4096, 4096, 5).startswith("gemv_kernel<"), t
         assert qg.kernel_info(t, 4096, 96, 8).startswith("gemv_kernel<"), t  # not whole groups
     # the __dp4a kernel's two Q6_K items: two lanes per block where their
     # 16-block iterations fill (16 blocks a row), four where they would not
