@@ -395,6 +395,10 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
     int elems, bytes;
     if (!block_info(type, &elems, &bytes)) return QG_ERR_TYPE;
     const bool grouped = mma_grouped(type);
+    // rows of 32-bit lane loads: one copy per row, pitches that spread a warp
+    // load's 8 rows over the banks (the K-quant items' loads measured no
+    // faster with it)
+    const bool apart = grouped;
     if (grouped) {  // eight 32-element blocks per panel block: rows of whole groups only
         if (n_in % 256 != 0) return QG_ERR_SHAPE;
         elems = 256;
@@ -414,13 +418,13 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
     constexpr int rw = 8;  // consumer warps of the register kernel: blocks w and w + 8 each
     if (force == 0 && nb <= 2 * rw && !grouped) {
         int rp, gp, S, R;
-        mma_slot_layout(nb, nb, bytes, &rp, &gp);
+        mma_slot_layout(nb, nb, bytes, &rp, &gp, apart);
         if (mma_ring(smem_limit, kMmaHeaderBytes, 4 * static_cast<int64_t>(gp), rw, &S, &R)) {
             bp.kb = nb;
             bp.n_chunks = 1;
             bp.rpitch = rp;
             bp.gpitch = gp;
-            bp.contig = 1;
+            bp.contig = apart ? 0 : 1;
             bp.stage_bytes = 4 * gp;
             bp.n_stages = S;
             bp.red_slots = R;
@@ -448,7 +452,7 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
                 if (kb > nb || (ci > 0 && kb == nb)) continue;
                 if (tune_mma_kb() > 0 && kb > tune_mma_kb()) continue;
                 int rp, gp, S, R;
-                mma_slot_layout(nb, kb, bytes, &rp, &gp, grouped);
+                mma_slot_layout(nb, kb, bytes, &rp, &gp, apart);
                 const int64_t stage = 4 * static_cast<int64_t>(gp);
                 const int64_t fixed = kMmaHeaderBytes + panel;
                 if (!mma_ring(smem_limit, fixed, stage, W, &S, &R)) continue;
@@ -463,7 +467,7 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
                 bp.n_chunks = n_chunks;
                 bp.rpitch = rp;
                 bp.gpitch = gp;
-                bp.contig = kb == nb && !grouped ? 1 : 0;
+                bp.contig = kb == nb && !apart ? 1 : 0;
                 bp.stage_bytes = static_cast<int>(stage);
                 bp.n_stages = S;
                 bp.red_slots = R;
