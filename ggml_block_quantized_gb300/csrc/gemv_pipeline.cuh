@@ -44,6 +44,8 @@ constexpr int kConsumerWarps = 8;
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxStages = 16;
 constexpr int kRowsPerWarp = 2;  // most rows a warp group takes per stage (its items are flattened over them)
+// Vector counts whose two-row straight-line form fits the registers (no spills).
+constexpr int kStraightNv = 1;
 constexpr int kMaxBatch = 256;   // matrices per batched launch (their table is a kernel parameter)
 // The producer issues only the first stages (GemvParams::pre_x, about 56 KiB)
 // before the consumers' first activation loads have arrived: behind a deep
@@ -405,7 +407,27 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
         for (int i = 0; i < kRowsPerWarp; ++i)
 #pragma unroll
             for (int v = 0; v < NV; ++v) acc[i][v] = 0.0f;
-        if (!failed && has[0]) {
+        if (NV <= kStraightNv && !failed && has[0] && nbw == kBlocksPerIter) {
+            // One iteration per row (the common row lengths): the warp's rows
+            // as one straight-line sequence, so the scheduler can interleave
+            // their loads and dependency chains. Each row's block sum is
+            // formed from zero and then added, as in the loop below, so the
+            // result does not depend on which of the two forms ran.
+            const int blk = b0 + lane_blk;
+            float part0[NV], part1[NV];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) part0[v] = part1[v] = 0.0f;
+            T::template item<NV, ISUMS>(smem_addr(rowp[0]), blk, sub, true, acta, p.nb, part0, isum_row[0],
+                                        isum_vstride);
+            if (has[1])
+                T::template item<NV, ISUMS>(smem_addr(rowp[1]), blk, sub, true, acta, p.nb, part1, isum_row[1],
+                                            isum_vstride);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                acc[0][v] += part0[v];
+                acc[1][v] += part1[v];
+            }
+        } else if (!failed && has[0]) {
             // The warp's blocks over its rows, flattened (virtual block vb:
             // row vb / nbw, block vb % nbw), so the lanes stay busy whatever
             // the row length. A lane always takes the same part `sub` of its
