@@ -408,11 +408,11 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
 #pragma unroll
             for (int v = 0; v < NV; ++v) acc[i][v] = 0.0f;
         if (NV <= kStraightNv && !failed && has[0] && nbw == kBlocksPerIter) {
-            // One iteration per row (the common row lengths): the warp's rows
-            // as one straight-line sequence, so the scheduler can interleave
-            // their loads and dependency chains. Each row's block sum is
-            // formed from zero and then added, as in the loop below, so the
-            // result does not depend on which of the two forms ran.
+            // One iteration per row (K-quant rows of 4096 elements): the
+            // warp's two rows as one straight-line sequence, so the scheduler
+            // can interleave their loads and dependency chains. Each row's
+            // block sum is formed from zero and then added, as in the loop at
+            // the end, so the result does not depend on which form ran.
             const int blk = b0 + lane_blk;
             float part0[NV], part1[NV];
 #pragma unroll
@@ -426,6 +426,25 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
             for (int v = 0; v < NV; ++v) {
                 acc[0][v] += part0[v];
                 acc[1][v] += part1[v];
+            }
+        } else if (NV <= kStraightNv && !failed && has[0] && nbw % kBlocksPerIter == 0) {
+            // Several whole iterations per row (32-element rows of 4096
+            // elements): the same pairing of the two rows per iteration, each
+            // iteration's sum added to its row in the loop's order.
+            const uint32_t ra0 = smem_addr(rowp[0]), ra1 = smem_addr(rowp[1]);
+            for (int vb = lane_blk; vb < nbw; vb += kBlocksPerIter) {
+                const int blk = b0 + vb;
+                float part0[NV], part1[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v) part0[v] = part1[v] = 0.0f;
+                T::template item<NV, ISUMS>(ra0, blk, sub, true, acta, p.nb, part0, isum_row[0], isum_vstride);
+                if (has[1])
+                    T::template item<NV, ISUMS>(ra1, blk, sub, true, acta, p.nb, part1, isum_row[1], isum_vstride);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    acc[0][v] += part0[v];
+                    acc[1][v] += part1[v];
+                }
             }
         } else if (!failed && has[0]) {
             // The warp's blocks over its rows, flattened (virtual block vb:
