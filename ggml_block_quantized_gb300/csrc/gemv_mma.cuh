@@ -1,8 +1,10 @@
 // gemv_mma.cuh - the block-quantized GEMV for several vectors on the tensor
 // cores: Y[v][o] = sum over the blocks of row o of (exact sub-block sums) x
-// (block scales), for Q4_K and Q6_K weights with Q8_K activations
-// ("Quantization" (rml), Quantized dot products, K-quants; "How to Read
-// ggml/GGUF" (sh), block layouts).
+// (block scales), for the K-quant weights (Q2_K .. Q6_K) with Q8_K
+// activations and the 32-element types (Q4_0, Q4_1, Q5_0, Q8_0) with Q8_0 /
+// Q8_1 activations, the latter eight blocks at a time ("Quantization" (rml),
+// Quantized dot products, K-quants; "How to Read ggml/GGUF" (sh), block
+// layouts).
 //
 // Why tensor cores here. With n_vec vectors every weight code meets n_vec
 // activation codes: the product is the dense contraction
@@ -16,8 +18,9 @@
 //  * an activation code (-127..127) is an exact f16;
 //  * every product and every partial sum of one sub-block is an integer
 //    times 2^-24 below 2^0, exact in the f32 accumulator;
-// so the accumulator of a sub-block (32 codes for Q4_K, 16 for Q6_K) is its
-// exact int32 sum times 2^-24 (times 16 for Q4_K odd sub-blocks). The
+// so the accumulator of a sub-block (32 codes for Q4_K, 16 for Q6_K, one
+// block of a 32-element type) is its exact int32 sum times 2^-24 (times 16
+// for Q4_K odd sub-blocks). The
 // sub-block scales are then applied in f32 (an exact small integer times the
 // accumulator), the minimum / offset terms come from one more small mma over
 // the Q8_K block sums (bsums), and only d_w, dmin_w and d_x are inexact
