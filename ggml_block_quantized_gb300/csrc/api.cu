@@ -418,13 +418,13 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
     constexpr int rw = 8;  // consumer warps of the register kernel: blocks w and w + 8 each
     if (force == 0 && nb <= 2 * rw && !grouped) {
         int rp, gp, S, R;
-        mma_slot_layout(nb, nb, bytes, &rp, &gp, apart);
+        mma_slot_layout(nb, nb, bytes, &rp, &gp);
         if (mma_ring(smem_limit, kMmaHeaderBytes, 4 * static_cast<int64_t>(gp), rw, &S, &R)) {
             bp.kb = nb;
             bp.n_chunks = 1;
             bp.rpitch = rp;
             bp.gpitch = gp;
-            bp.contig = apart ? 0 : 1;
+            bp.contig = 1;
             bp.stage_bytes = 4 * gp;
             bp.n_stages = S;
             bp.red_slots = R;
@@ -444,7 +444,7 @@ int plan_gemv_mma(int type, int64_t total_tiles, int64_t n_in, int nv, int sms, 
         for (int f = 0; f < 2; ++f) {
             const bool b16 = f == 0;
             if (b16 && force == 8) continue;
-            // grouped types: per record and lane a float4 (512 bytes) for the Q8_K tail
+            // grouped types: per record and lane a float4 (512 bytes) in place of the Q8_K tail
             const int rec = mma_rec_bytes(b16) + (grouped ? 512 - kMmaTailBytes : 0);
             const int64_t panel = static_cast<int64_t>(nb) * rec;
             for (int ci = 0; ci < kCands; ++ci) {

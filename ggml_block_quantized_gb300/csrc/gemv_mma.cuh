@@ -811,6 +811,7 @@ __device__ __forceinline__ uint32_t mma_word(uint32_t base) {
     }
 }
 
+// Packed two-lane f32 product (one instruction for both lanes).
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
     float2 d;
     asm("{\n\t.reg .b64 ra, rb;\n\t"
