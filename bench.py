@@ -265,17 +265,20 @@ def time_oracle(sample, n_vec, budget_s=12.0):
 
 # ------------------------------------------------- every workload, one line
 SINGLE_CONFIGS = ["q8_0_256x1024", "q4_0_4096", "q4_k_4096", "q6_k_32000"]   # the four single-matrix workloads
+L2_HOT = ("q8_0_256x1024", "q4_0_4096", "q4_k_4096")  # small enough to also time with W resident in L2
 OTHER_TYPES = ["q4_1_32000", "q5_0_32000", "q2_k_32000", "q3_k_32000", "q5_k_32000"]
 
 
-def time_single_calls(qg, timer, t, n_out, n_in, nv, W, x, peak, reps=10):
+def time_single_calls(qg, timer, t, n_out, n_in, nv, W, x, peak, reps=10, l2_hot=False):
     """One qgemv call per weight copy, the copies rotating through more than
-    4x L2 so every call streams W from HBM; returns the per-call figures."""
+    4x L2 so every call streams W from HBM; returns the per-call figures.
+    With l2_hot the same number of calls all use W itself, which stays in L2
+    after the first call (a latency figure, not a bandwidth one)."""
     import torch
     dev = W.device
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     copies = max(1, int(np.ceil(4 * l2 / W.numel())))
-    Ws = [W] + [W.clone() for _ in range(copies - 1)]
+    Ws = [W] * copies if l2_hot else [W] + [W.clone() for _ in range(copies - 1)]
     y = torch.empty((nv, n_out), dtype=torch.float32, device=dev)
     ws = torch.empty(max(16, qg.qgemv_workspace_bytes(t, n_in, nv)), dtype=torch.uint8, device=dev)
 
@@ -309,6 +312,10 @@ def measure_single_workloads(qg, synth, timer, device, peak, names):
         row = {"shape": f"{qg.TYPE_NAMES[t]} {n_out}x{n_in}"}
         for nv in (1, 8):
             row[f"n_vec={nv}"] = time_single_calls(qg, timer, t, n_out, n_in, nv, W, x8[:nv * n_in], peak)
+            if name in L2_HOT:
+                hot = time_single_calls(qg, timer, t, n_out, n_in, nv, W, x8[:nv * n_in], peak, l2_hot=True)
+                row[f"n_vec={nv}"]["l2_hot"] = {"us_per_call": hot["us_per_call"],
+                                                "note": "one weight copy, resident in L2 after the first call"}
         if name == "q4_k_4096":
             row["dequantize_rows"] = time_dequantize(qg, timer, t, n_out, n_in, W, peak)
         out[name] = row
