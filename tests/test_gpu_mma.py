@@ -225,3 +225,35 @@ def _kernel_choice():
     # (43 blocks a row); the parity tests cover both row lengths
     assert "lanes_per_block=2" in qg.kernel_info(qg.Q6_K, 32000, 4096, 1)
     assert "lanes_per_block=4" in qg.kernel_info(qg.Q6_K, 4096, 11008, 1, 32)
+
+
+@pytest.mark.parametrize("t", GROUPED)
+def test_batch_split_by_routing(t):
+    """With the default size rule a batch whose matrices fall on both sides
+    of it runs as two launches (tensor cores for the large matrix, __dp4a for
+    the small ones); every matrix gives the bits of its own single call, and
+    the large one matches the oracle on sampled rows."""
+    prev = qg.tune("QG_MMA_GROUP_MELEM", _GROUP_MELEM["v"])
+    try:
+        rng = np.random.default_rng(4700 + t)
+        n_in, n_vec = 4096, 8
+        n_outs = [100, 11008, 17, 513]
+        kinds = [qg.kernel_info(t, n, n_in, n_vec).split("<")[0] for n in n_outs]
+        assert kinds == ["gemv_kernel", "gemv_mma_kernel", "gemv_kernel", "gemv_kernel"], kinds
+        mats, hw, hx = [], [], []
+        for n_out in n_outs:
+            W = wblocks(t, n_out, n_in, rng)
+            x = synth.f32_normal(rng, n_vec * n_in)
+            hw.append(W)
+            hx.append(x)
+            mats.append((dev(W), dev(x), torch.full((n_vec, n_out), np.nan, device="cuda"), n_out))
+        qg.qgemv_batched(t, mats, n_in, n_vec)
+        torch.cuda.synchronize()
+        for W, x, y, n_out in mats:
+            ref = qg.qgemv(t, W, x, n_out, n_in, n_vec)
+            assert np.array_equal(host(y).view(np.uint32), host(ref).view(np.uint32)), n_out
+        rows = np.random.default_rng(1).choice(n_outs[1], 48, replace=False)
+        check_y(t, hw[1], hx[1], host(mats[1][2]), n_outs[1], n_in, n_vec, rows=rows)
+        assert qg.device_error() == 0
+    finally:
+        qg.tune("QG_MMA_GROUP_MELEM", prev)
