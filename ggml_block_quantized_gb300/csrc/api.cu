@@ -25,7 +25,7 @@ cudaError_t launch_dequant(int type, const uint8_t *w, O *out, int64_t groups, u
 cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, cudaStream_t s);
 cudaError_t launch_gemm_f16_tc(const __half *A, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
                                int32_t *err, int sms, int device, cudaStream_t s);
-cudaError_t launch_gemm_q4k_fused(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
+cudaError_t launch_gemm_q4k_tmem(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
                                   int64_t K, int32_t *err, int sms, int device, cudaStream_t s);
 cudaError_t launch_gemv_tc_q4_k(const TcParams &p, const TcMat *mats, int n, int grid, int smem, int smem_optin,
                                 int device, cudaStream_t s);
@@ -156,8 +156,9 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 //    default: the mma.sync kernel measured faster on this GPU), 1 whenever its
 //    shared memory fits (rows of 8 or 16 blocks);
 //  QG_FUSED_GEMM: qgemm on Q4_K weights dequantizes into an f16 copy in the
-//    workspace first (0, the default: measured as fast or faster at 512 to
-//    4096 tokens) or inside the GEMM's shared memory (1: no f16 copy of W).
+//    workspace first (0, the default: measured faster at 1024 and 4096
+//    tokens, as fast at 2048) or inside the GEMM, into tensor memory (1: no
+//    f16 copy of W; measured faster at 512 tokens).
 enum KnobId {
     kKnobCtasPerSm,
     kKnobRingKib,
@@ -1017,11 +1018,11 @@ int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     __half *B = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) +
                                            ((static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255)));
     if (type == QG_Q4_K && knob(kKnobFusedGemm)) {
-        // W is dequantized inside the GEMM's shared memory: only x is converted first
+        // W is dequantized inside the GEMM (into tensor memory): only x is converted first
         cudaError_t e = launch_f32_to_f16(x, B, n_tok * n_in, dev.sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "prefill: x to f16");
-        e = launch_gemm_q4k_fused(static_cast<const uint8_t *>(W), B, y, n_out, n_tok, n_in, dev.err, dev.sms,
-                                  dev.device, s);
+        e = launch_gemm_q4k_tmem(static_cast<const uint8_t *>(W), B, y, n_out, n_tok, n_in, dev.err, dev.sms,
+                                 dev.device, s);
         if (e != cudaSuccess) return cuda_fail(e, g_launch_step);
         return QG_OK;
     }

@@ -248,40 +248,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 1) tc_dealloc(tmem, kGemmTmemCols);
 }
 
-// ---------------------------------------------------------------------------
-// The prefill product for Q4_K weights with the dequantization fused into the
-// GEMM: no f16 copy of W in memory. Same tiles, mma issue and epilogue as
-// gemm_f16_tc_kernel; each stage of the ring holds, besides the f16 A tile
-// and the B tile of one 64-element k-block, the raw bytes that k-block needs:
-// for each of the tile's 128 rows the 16-byte header of its Q4_K block (d,
-// dmin, 12 scale bytes) and the 32 bytes of codes of the k-block (k-block q
-// of a block: qs[32 q .. 32 q + 31], low nibbles for its first 32 elements,
-// high nibbles for the other 32).
-//  * warp 0, lane 0: per k-block three 2-D tensor loads into the stage: the
-//    B tile as before, the headers (box 16 bytes x 128 rows) and the codes
-//    (32 bytes x 128 rows) of the raw blocks;
-//  * warps 6..13 (converters): thread c takes row c / 2 of the tile and half
-//    c % 2 of the k-block, i.e. one 32-element sub-block j = 2q + half: value
-//    d sc_j q - dmin m_j in f32 (the product d sc_j q is exact; the
-//    subtraction rounds once), rounded to f16 -- the values dequantize_rows
-//    gives, rounded as the unfused path rounds them -- written as four
-//    16-byte chunks into the 128-byte-swizzled K-major layout a tensor load
-//    would produce (chunk c of row r at (c ^ (r mod 8)) * 16). Each thread
-//    fences its generic-proxy stores for the tensor cores before its warp
-//    arrives on the stage's A-full barrier; the mma waits for both barriers.
-// ---------------------------------------------------------------------------
-constexpr int kFuseConvWarps = 8;
-constexpr int kFuseThreads = (6 + kFuseConvWarps) * 32;
 constexpr int kQ4kBlockBytes = 144;
 constexpr int kRawHdr = kGemmBM * 16, kRawCodes = kGemmBM * 32;  // raw bytes of one k-block
-
-template <int BN> struct FuseShape {
-    static constexpr int kBTile = BN * kGemmBK * 2;
-    static constexpr int kStage = kGemmTileBytes + kBTile + kRawHdr + kRawCodes;
-    static constexpr int kStages = BN == 128 ? 5 : 4;
-    static constexpr int kSmem = 1024 + kGemmHdrBytes + kStages * kStage;
-    static constexpr int kTmemCols = 2 * BN;
-};
 
 // 6-bit scale and min of Q4_K sub-block j from the 12 scale bytes (words
 // s0 = bytes 0..3, s1 = 4..7, s2 = 8..11) ("Quantization" (rml), Unpacking
@@ -306,13 +274,78 @@ __device__ __forceinline__ uint32_t pack_f16x2(float2 v) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// ---------------------------------------------------------------------------
+// The prefill product for Q4_K weights with the dequantization fused into the
+// GEMM: no f16 copy of W in memory. Same tiles, mma issue and epilogue as
+// gemm_f16_tc_kernel, but tcgen05.mma reads its A operand (the dequantized
+// weights) from tensor memory: lane m = row m of the tile, two f16 per
+// 32-bit column, the even k in the low half.
+//  * warp 0, lane 0: per 64-element k-block three 2-D tensor loads into a
+//    ring stage: the B tile as in gemm_f16_tc_kernel, and the raw bytes the
+//    k-block needs for each of the tile's 128 rows -- the 16-byte header of
+//    its Q4_K block (d, dmin, 12 scale bytes; box 16 bytes x 128 rows) and
+//    the 32 bytes of codes (box 32 x 128; k-block q of a block uses
+//    qs[32 q .. 32 q + 31], low nibbles for its first 32 elements, high
+//    nibbles for the other 32);
+//  * tensor memory: kND accumulators of BN columns (one when BN = 256, so
+//    the mma waits for the epilogue to drain it before a tile's first mma),
+//    then one 32-column A slot per ring stage;
+//  * warps 6..13 (converters): warp w serves tensor-memory lanes 32 (w % 4)
+//    .. (the only lanes it may access) and half (w - 6) / 4 of each k-block,
+//    i.e. thread = (row, one 32-element sub-block j = 2 q + half): value
+//    d sc_j q - dmin m_j in f32 (the product d sc_j q is exact; the
+//    subtraction rounds once), rounded to f16 -- the values dequantize_rows
+//    gives, rounded as the f16-copy path rounds them -- 16 columns with one
+//    tcgen05.st; then tcgen05.wait::st and the before-thread-sync fence, and
+//    the warp arrives on the stage's A-full barrier; the mma waits for that
+//    barrier and the stage's full barrier;
+//  * the A slot of stage s is rewritten only after the producer has reused
+//    stage s, i.e. after the mmas that read it completed (their commit to the
+//    stage's empty barrier).
+// Writing A to tensor memory leaves shared memory to the tensor loads and
+// the mma's B reads: the ring holds only the B tile and the raw bytes.
+// ---------------------------------------------------------------------------
+constexpr int kTmemConvWarps = 8;
+constexpr int kTmemThreads = (6 + kTmemConvWarps) * 32;
+
+template <int BN> struct TmemFuseShape {
+    static constexpr int kBTile = BN * kGemmBK * 2;
+    static constexpr int kStage = kBTile + kRawHdr + kRawCodes;  // a multiple of 1024
+    static constexpr int kND = BN == 256 ? 1 : 2;                 // accumulators
+    static constexpr int kStages = BN == 256 ? 5 : 8;
+    static constexpr int kACol0 = kND * BN;                       // first A column
+    static constexpr int kSmem = 1024 + kGemmHdrBytes + kStages * kStage;
+    static constexpr int kTmemCols = 512;
+    static_assert(kStage % 1024 == 0, "swizzled B tiles start 1024-byte aligned");
+    static_assert(kACol0 + 32 * kStages <= kTmemCols, "tensor-memory columns");
+};
+
+// D (tensor memory) = A (tensor memory) x B (shared memory) (+ D).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_t, uint32_t a_t, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_t),
+        "r"(a_t), "l"(b_desc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 32 lanes x 16 columns from this warp's 16 registers each.
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 template <int BN>
-__global__ void __launch_bounds__(kFuseThreads, 1)
-    gemm_q4k_fused_kernel(const __grid_constant__ CUtensorMap tma_hdr, const __grid_constant__ CUtensorMap tma_codes,
-                          const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
-    using Sh = FuseShape<BN>;
-    constexpr int S = Sh::kStages;
-    constexpr int kOffB = kGemmTileBytes, kOffHdr = kGemmTileBytes + Sh::kBTile, kOffCodes = kOffHdr + kRawHdr;
+__global__ void __launch_bounds__(kTmemThreads, 1)
+    gemm_q4k_tmem_kernel(const __grid_constant__ CUtensorMap tma_hdr, const __grid_constant__ CUtensorMap tma_codes,
+                         const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+    using Sh = TmemFuseShape<BN>;
+    constexpr int S = Sh::kStages, ND = Sh::kND;
+    constexpr int kOffHdr = Sh::kBTile, kOffCodes = kOffHdr + kRawHdr;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_a = smem_addr(smem_raw);
     const uint32_t base_a = (raw_a + 1023u) & ~1023u;
@@ -330,7 +363,7 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(afull0 + 8 * s, kFuseConvWarps);
+            mbar_init(afull0 + 8 * s, kTmemConvWarps);
             mbar_init(empty0 + 8 * s, 1);
         }
         for (int d = 0; d < 2; ++d) {
@@ -368,8 +401,8 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
                     }
                     const uint32_t st = stages_a + static_cast<uint32_t>(s * Sh::kStage);
                     const int x0 = (kb >> 2) * kQ4kBlockBytes;  // the block column's first byte in a row
-                    mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(Sh::kBTile + kRawHdr + kRawCodes));
-                    tma_load_2d(st + kOffB, &tma_b, kb * kGemmBK, tn * BN, full0 + 8 * s);
+                    mbar_arrive_expect_tx(full0 + 8 * s, static_cast<uint32_t>(Sh::kStage));
+                    tma_load_2d(st, &tma_b, kb * kGemmBK, tn * BN, full0 + 8 * s);
                     tma_load_2d(st + kOffHdr, &tma_hdr, x0, tm * kGemmBM, full0 + 8 * s);
                     tma_load_2d(st + kOffCodes, &tma_codes, x0 + 16 + 32 * (kb & 3), tm * kGemmBM, full0 + 8 * s);
                     ++issued;
@@ -400,8 +433,8 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
-                const int d = it & 1;
-                if (it >= 2 && !tc_wait(tempty0 + 8 * d, static_cast<uint32_t>(((it - 2) >> 1) & 1), abort_flag)) {
+                const int d = it % ND;
+                if (it >= ND && !tc_wait(tempty0 + 8 * d, static_cast<uint32_t>(((it - ND) / ND) & 1), abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -413,13 +446,14 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = stages_a + static_cast<uint32_t>(s * Sh::kStage);
-                    const uint64_t da = tc_smem_desc(sa, 1024), db = tc_smem_desc(sa + kOffB, 1024);
+                    const uint32_t st = stages_a + static_cast<uint32_t>(s * Sh::kStage);
+                    const uint64_t db = tc_smem_desc(st, 1024);
+                    const uint32_t at = tmem + static_cast<uint32_t>(Sh::kACol0 + 32 * s);
 #pragma unroll
                     for (int k = 0; k < kGemmBK / 16; ++k)
-                        tc_mma_ss(dt, da + static_cast<uint64_t>(2 * k), db + static_cast<uint64_t>(2 * k), idesc,
+                        tc_mma_ts(dt, at + static_cast<uint32_t>(8 * k), db + static_cast<uint64_t>(2 * k), idesc,
                                   (kb | k) != 0 ? 1u : 0u);
-                    tc_commit(empty0 + 8 * s);
+                    tc_commit(empty0 + 8 * s);  // stage s and its A slot are free once these mmas are done
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -442,8 +476,8 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-            const int tm = t % p.tiles_m, tn = t / p.tiles_m, d = it & 1;
-            if (ok && !tc_wait(tfull0 + 8 * d, static_cast<uint32_t>((it >> 1) & 1), abort_flag)) {
+            const int tm = t % p.tiles_m, tn = t / p.tiles_m, d = it % ND;
+            if (ok && !tc_wait(tfull0 + 8 * d, static_cast<uint32_t>((it / ND) & 1), abort_flag)) {
                 if (lane == 0) {
                     record_error(p.err, kErrConsumerWait);
                     *abort_flag = 1;
@@ -471,16 +505,17 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
             if (lane == 0) mbar_arrive(tempty0 + 8 * d);
         }
     } else {
-        // ---------------- converters
-        const int c = threadIdx.x - 6 * 32;
-        const int row = c >> 1, half = c & 1;
-        const uint32_t sw = static_cast<uint32_t>(row & 7);
+        // ---------------- converters: lanes 32 q .. of tensor memory, sub-block `half` of each k-block
+        const int q = warp & 3, half = (warp - 6) >> 2;
+        const int row = 32 * q + lane;
+        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(Sh::kACol0 + 16 * half);
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             for (int kb = 0; kb < nk; ++kb) {
-                if (!tc_wait(full0 + 8 * s, ph, abort_flag)) {
+                // the tensor-memory store below is warp-collective: the warp goes on or stops as one
+                if (!__all_sync(0xffffffffu, tc_wait(full0 + 8 * s, ph, abort_flag))) {
                     ok = false;
                     break;
                 }
@@ -495,7 +530,8 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
                 // after the word's nibbles are masked): the float is 2^23 + q
                 // exactly, and fma(d sc, 2^23 + q, -d sc 2^23) = d sc q is exact
                 // (d sc has at most 17 significant bits, q 4). The subtraction
-                // of dmin m then rounds once, as d sc q - dmin m does.
+                // of dmin m then rounds once, as d sc q - dmin m does in
+                // dequantize_rows.
                 const float2 s2 = make_float2(dsc, dsc), c2 = make_float2(-dsc * 8388608.0f, -dsc * 8388608.0f);
                 const float2 off2 = make_float2(-off, -off);
                 const uint32_t qw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -510,16 +546,9 @@ __global__ void __launch_bounds__(kFuseThreads, 1)
                         o[2 * i + (b >> 1)] = pack_f16x2(fadd2(ffma2(s2, mg, c2), off2));
                     }
                 }
-                // elements 32 half .. 32 half + 31 of the k-block: chunks 4 half .. 4 half + 3
-                const uint32_t arow = st + static_cast<uint32_t>(row * 128);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t chunk = (static_cast<uint32_t>(4 * half + i) ^ sw) << 4;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(arow + chunk), "r"(o[4 * i]),
-                                 "r"(o[4 * i + 1]), "r"(o[4 * i + 2]), "r"(o[4 * i + 3])
-                                 : "memory");
-                }
-                fence_proxy_async_smem();
+                tc_st16(ta + static_cast<uint32_t>(32 * s), o);
+                tc_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(afull0 + 8 * s);
                 if (++s == S) {
@@ -639,8 +668,8 @@ cudaError_t launch_gemm_bn(const __half *A, const __half *B, float *y, int64_t n
 }
 
 template <int BN>
-cudaError_t launch_fused_bn(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
-                            int32_t *err, int sms, int device, cudaStream_t s) {
+cudaError_t launch_tmem_bn(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
+                           int32_t *err, int sms, int device, cudaStream_t s) {
     CUtensorMap th, tc, tb;
     const int64_t row_bytes = K / 256 * kQ4kBlockBytes;
     if (!encode_q4k_map(&th, W, n_out, row_bytes, 16) || !encode_q4k_map(&tc, W, n_out, row_bytes, 32) ||
@@ -662,22 +691,23 @@ cudaError_t launch_fused_bn(const uint8_t *W, const __half *B, float *y, int64_t
     const uint64_t bit = 1ull << (device & 63);
     if (!(done.load(std::memory_order_acquire) & bit)) {
         g_launch_step = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)";
-        cudaError_t e = cudaFuncSetAttribute(gemm_q4k_fused_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             FuseShape<BN>::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(gemm_q4k_tmem_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             TmemFuseShape<BN>::kSmem);
         if (e != cudaSuccess) return e;
         done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    return launch_pdl(gemm_q4k_fused_kernel<BN>, grid, kFuseThreads, FuseShape<BN>::kSmem, s, th, tc, tb, p);
+    return launch_pdl(gemm_q4k_tmem_kernel<BN>, grid, kTmemThreads, TmemFuseShape<BN>::kSmem, s, th, tc, tb, p);
 }
 
 // Y[n_tok][n_out] = dequant(W)[n_out][K] . B[n_tok][K]^T for Q4_K W (K a
 // multiple of 256, rows 16-byte aligned) and f16 B, the dequantization done
-// in shared memory. Token tiles as launch_gemm_f16_tc chooses them.
-cudaError_t launch_gemm_q4k_fused(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
-                                  int64_t K, int32_t *err, int sms, int device, cudaStream_t s) {
+// on the way into tensor memory. Token tiles as launch_gemm_f16_tc chooses
+// them.
+cudaError_t launch_gemm_q4k_tmem(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
+                                 int64_t K, int32_t *err, int sms, int device, cudaStream_t s) {
     const int64_t tiles256 = ((n_out + kGemmBM - 1) / kGemmBM) * ((n_tok + 255) / 256);
-    if (tiles256 >= sms) return launch_fused_bn<256>(W, B, y, n_out, n_tok, K, err, sms, device, s);
-    return launch_fused_bn<128>(W, B, y, n_out, n_tok, K, err, sms, device, s);
+    if (tiles256 >= sms) return launch_tmem_bn<256>(W, B, y, n_out, n_tok, K, err, sms, device, s);
+    return launch_tmem_bn<128>(W, B, y, n_out, n_tok, K, err, sms, device, s);
 }
 
 // Y[n_tok][n_out] = A[n_out][K] . B[n_tok][K]^T for f16 A, B (16-byte

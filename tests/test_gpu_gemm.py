@@ -109,18 +109,20 @@ def test_gemm_wide_token_tiles():
 @pytest.mark.parametrize("shape", [(1, 256, 1), (100, 512, 37), (129, 1024, 130), (4352, 4096, 640),
                                    (4096, 2048, 1300), (300, 11008, 257)])
 def test_fused_q4_k_equals_the_f16_copy_path(shape):
-    """Q4_K blocks expanded to f16 inside the GEMM's shared memory give the
-    same bits as dequantizing W to an f16 copy first (the same f16 values,
-    the same mma order): ragged row tiles (rows past the matrix are zeros),
-    ragged token tiles, 128- and 256-token tiles, long rows."""
+    """Q4_K blocks expanded to f16 inside the GEMM (into tensor memory, where
+    the mma reads its A operand) give the same bits as dequantizing W to an
+    f16 copy first (the same f16 values, the same mma order): ragged row
+    tiles (rows past the matrix are zeros), ragged token tiles, 128- and
+    256-token tiles, long rows."""
     n_out, n_in, n_tok = shape
     rng = np.random.default_rng(7700 + n_out)
     Wd = dev(weights(qg.Q4_K, n_out, n_in, rng))
     xd = dev(synth.f32_normal(rng, n_tok * n_in))
-    copy = host(qg.qgemm(qg.Q4_K, Wd, xd, n_out, n_in, n_tok))
     old = qg.tune("QG_FUSED_GEMM", 1)
     try:
         fused = host(qg.qgemm(qg.Q4_K, Wd, xd, n_out, n_in, n_tok))
+        qg.tune("QG_FUSED_GEMM", 0)
+        copy = host(qg.qgemm(qg.Q4_K, Wd, xd, n_out, n_in, n_tok))
     finally:
         qg.tune("QG_FUSED_GEMM", old)
     assert np.array_equal(fused.view(np.uint32), copy.view(np.uint32))
