@@ -446,6 +446,22 @@ __global__ void __launch_bounds__(kGemvThreads, NV <= 2 ? 2 : 1)
                     acc[1][v] += part1[v];
                 }
             }
+        } else if (!failed && has[0] && !has[1]) {
+            // One row for this warp in the stage (rows split over warps, or
+            // the stage's last rows): its blocks in 32 / lanes-per-block
+            // steps, lanes past the row's end inactive.
+            const uint32_t rowa0 = smem_addr(rowp[0]);
+            const int lim = (nbw + kBlocksPerIter - 1) / kBlocksPerIter * kBlocksPerIter;
+            for (int vb = lane_blk; vb < lim; vb += kBlocksPerIter) {
+                const bool active = vb < nbw;
+                float part[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v) part[v] = 0.0f;
+                T::template item<NV, ISUMS>(rowa0, b0 + (active ? vb : 0), sub, active, acta, p.nb, part, isum_row[0],
+                                            isum_vstride);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) acc[0][v] += part[v];
+            }
         } else if (!failed && has[0]) {
             // The warp's blocks over its rows, flattened (virtual block vb:
             // row vb / nbw, block vb % nbw), so the lanes stay busy whatever
