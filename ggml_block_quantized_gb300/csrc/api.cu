@@ -156,9 +156,9 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 //    default: the mma.sync kernel measured faster on this GPU), 1 whenever its
 //    shared memory fits (rows of 8 or 16 blocks);
 //  QG_FUSED_GEMM: qgemm on Q4_K weights dequantizes into an f16 copy in the
-//    workspace first (0, the default: measured faster at 1024 and 4096
-//    tokens, as fast at 2048) or inside the GEMM, into tensor memory (1: no
-//    f16 copy of W; measured faster at 512 tokens).
+//    workspace first (0) or inside the GEMM, into tensor memory (1: no f16
+//    copy of W); 2, the default, fuses up to kFusedGemmMaxTok tokens (measured
+//    5-6% faster from 64 to 512 tokens, 12% slower at 768, 11% at 1024).
 enum KnobId {
     kKnobCtasPerSm,
     kKnobRingKib,
@@ -180,8 +180,9 @@ constexpr KnobDef kKnobs[kKnobCount] = {
     {"QG_CTAS_PER_SM", 2, 1, 4},          {"QG_RING_KIB", 96, 16, 200}, {"QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1},
     {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 16, 0, 1024},
     {"QG_TC", 0, 0, 1},                   {"QG_FUSED_MAX_MIB", 1 << 20, 0, 1 << 20},
-    {"QG_FUSED_GEMM", 0, 0, 1},           {"QG_MMA_GROUP_MELEM", 40, 0, 1 << 20}};
+    {"QG_FUSED_GEMM", 2, 0, 2},           {"QG_MMA_GROUP_MELEM", 40, 0, 1 << 20}};
 std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
+constexpr int64_t kFusedGemmMaxTok = 512;  // QG_FUSED_GEMM = 2: the fused prefill up to this many tokens
 
 int knob(KnobId k) {
     int v = g_knob_val[k].load(std::memory_order_relaxed);
@@ -1017,7 +1018,8 @@ int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     __half *A = static_cast<__half *>(workspace);
     __half *B = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) +
                                            ((static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255)));
-    if (type == QG_Q4_K && knob(kKnobFusedGemm)) {
+    const int fuse = knob(kKnobFusedGemm);
+    if (type == QG_Q4_K && (fuse == 1 || (fuse == 2 && n_tok <= kFusedGemmMaxTok))) {
         // W is dequantized inside the GEMM (into tensor memory): only x is converted first
         cudaError_t e = launch_f32_to_f16(x, B, n_tok * n_in, dev.sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "prefill: x to f16");

@@ -314,11 +314,11 @@ size_t qgemm_workspace_bytes(int type, int64_t n_out, int64_t n_in, int64_t n_to
  * it with f32 x; here the whole product is one dense GEMM). Steps, all on
  * `stream`: dequantize W to f16 (round to nearest even) into the workspace,
  * round x to f16 into the workspace, then a tcgen05 tensor-core GEMM with
- * f32 accumulation. With the knob QG_FUSED_GEMM set (see qg_tune), Q4_K
- * weights are instead dequantized inside the GEMM (raw blocks are loaded
- * into shared memory and expanded to the same f16 values in tensor memory,
- * where the mma reads them; no f16 copy of W is written), with the same
- * result bit for bit. The result differs from the f32 product by the f16
+ * f32 accumulation. For Q4_K weights and at most 512 tokens (by default;
+ * see the knob QG_FUSED_GEMM of qg_tune) W is instead dequantized inside the
+ * GEMM (raw blocks are loaded into shared memory and expanded to the same
+ * f16 values in tensor memory, where the mma reads them; no f16 copy of W is
+ * written), with the same result bit for bit. The result differs from the f32 product by the f16
  * rounding of each weight and activation (at most 2^-11 relative each) and
  * the f32 accumulation: |y - y_exact| <= (2^-10 + n_in 2^-24) sum_i
  * |W[o][i] x[t][i]| (values beyond f16's range, 65504, become inf).
@@ -368,9 +368,9 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
  * inside the GEMV), QG_FUSED_MAX_MIB (... for a single matrix of at most this
  * many MiB of blocks; default: no limit), QG_TC (the tcgen05 Q4_K kernel for three or
  * more vectors, rows of 2048 or 4096 elements: 0 never, the default; 1
- * whenever it fits), QG_FUSED_GEMM (qgemm on Q4_K weights: 0, the default,
- * writes the f16 copy of W to the workspace first; 1 dequantizes inside the
- * GEMM, into tensor memory, instead). value is clamped to the knob's range; the old
+ * whenever it fits), QG_FUSED_GEMM (qgemm on Q4_K weights: 0 writes the f16
+ * copy of W to the workspace first; 1 dequantizes inside the GEMM, into
+ * tensor memory, instead; 2, the default, does so up to 512 tokens). value is clamped to the knob's range; the old
  * value goes to *previous when that is not NULL. Returns QG_OK, QG_ERR_NULL
  * or QG_ERR_TYPE (unknown name). Host-only; affects launches planned after
  * it returns. */

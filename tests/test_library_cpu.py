@@ -184,6 +184,9 @@ def test_tune_knobs(L):
     assert L.qg_tune(b"QG_TC", 7, ctypes.byref(prev)) == OK and prev.value == 1
     assert L.qg_tune(b"QG_TC", old, ctypes.byref(prev)) == OK and prev.value == 1  # clamped to 1
     assert qg.tune("QG_MMA_MIN_NVEC", 3) in range(1, 10)
+    old = qg.tune("QG_FUSED_GEMM", 9)  # 0, 1 or 2 (the default: fused up to 512 tokens)
+    assert old in (0, 1, 2)
+    assert qg.tune("QG_FUSED_GEMM", old) == 2  # clamped to 2
 
 
 def test_batched_validation(L):
