@@ -26,7 +26,9 @@ cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, c
 cudaError_t launch_gemm_f16_tc(const __half *A, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
                                int32_t *err, int sms, int device, cudaStream_t s);
 cudaError_t launch_gemm_q4k_tmem(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
-                                  int64_t K, int32_t *err, int sms, int device, cudaStream_t s);
+                                 int64_t K, int ksplit, float *part, int32_t *err, int sms, int device,
+                                 cudaStream_t s);
+int gemm_q4k_tmem_ksplit(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes);
 cudaError_t launch_gemv_tc_q4_k(const TcParams &p, const TcMat *mats, int n, int grid, int smem, int smem_optin,
                                 int device, cudaStream_t s);
 
@@ -158,7 +160,9 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 //  QG_FUSED_GEMM: qgemm on Q4_K weights dequantizes into an f16 copy in the
 //    workspace first (0) or inside the GEMM, into tensor memory (1: no f16
 //    copy of W); 2, the default, fuses up to kFusedGemmMaxTok tokens (measured
-//    5-6% faster from 64 to 512 tokens, 12% slower at 768, 11% at 1024).
+//    5-6% faster from 64 to 512 tokens, 12% slower at 768, 11% at 1024);
+//  QG_GEMM_KSPLIT: the fused GEMM splits each tile's k-blocks into at most this
+//    many parts when its tiles leave SMs idle (1: no split).
 enum KnobId {
     kKnobCtasPerSm,
     kKnobRingKib,
@@ -170,6 +174,7 @@ enum KnobId {
     kKnobFusedMaxMib,
     kKnobFusedGemm,
     kKnobMmaGroupMelem,
+    kKnobGemmKsplit,
     kKnobCount
 };
 struct KnobDef {
@@ -180,7 +185,8 @@ constexpr KnobDef kKnobs[kKnobCount] = {
     {"QG_CTAS_PER_SM", 2, 1, 4},          {"QG_RING_KIB", 96, 16, 200}, {"QG_MMA_MIN_NVEC", 3, 1, QG_MAX_NVEC + 1},
     {"QG_MMA_PANEL", 0, 0, 16},           {"QG_MMA_KB", 0, 0, 4096},    {"QG_FUSED_QUANT_KIB", 16, 0, 1024},
     {"QG_TC", 0, 0, 1},                   {"QG_FUSED_MAX_MIB", 1 << 20, 0, 1 << 20},
-    {"QG_FUSED_GEMM", 2, 0, 2},           {"QG_MMA_GROUP_MELEM", 40, 0, 1 << 20}};
+    {"QG_FUSED_GEMM", 2, 0, 2},           {"QG_MMA_GROUP_MELEM", 40, 0, 1 << 20},
+    {"QG_GEMM_KSPLIT", 8, 1, 8}};
 std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
 constexpr int64_t kFusedGemmMaxTok = 512;  // QG_FUSED_GEMM = 2: the fused prefill up to this many tokens
 
@@ -1020,11 +1026,15 @@ int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int6
                                            ((static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255)));
     const int fuse = knob(kKnobFusedGemm);
     if (type == QG_Q4_K && (fuse == 1 || (fuse == 2 && n_tok <= kFusedGemmMaxTok))) {
-        // W is dequantized inside the GEMM (into tensor memory): only x is converted first
+        // W is dequantized inside the GEMM (into tensor memory): only x is converted first.
+        // With few tiles the GEMM splits k; the workspace's f16-weight part, unused
+        // here, holds the partial products of the parts after the first.
+        const int ks = gemm_q4k_tmem_ksplit(n_out, n_tok, n_in, dev.sms, knob(kKnobGemmKsplit),
+                                            static_cast<size_t>(2 * n_out * n_in));
         cudaError_t e = launch_f32_to_f16(x, B, n_tok * n_in, dev.sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "prefill: x to f16");
-        e = launch_gemm_q4k_tmem(static_cast<const uint8_t *>(W), B, y, n_out, n_tok, n_in, dev.err, dev.sms,
-                                 dev.device, s);
+        e = launch_gemm_q4k_tmem(static_cast<const uint8_t *>(W), B, y, n_out, n_tok, n_in, ks,
+                                 reinterpret_cast<float *>(A), dev.err, dev.sms, dev.device, s);
         if (e != cudaSuccess) return cuda_fail(e, g_launch_step);
         return QG_OK;
     }

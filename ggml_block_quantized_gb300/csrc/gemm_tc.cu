@@ -16,12 +16,18 @@
 //    and B from shared memory), four per k-block, commits each k-block to
 //    the stage's empty barrier and each tile to its accumulator's barrier.
 //  * warps 2..5: epilogue. Each reads its 32 tensor-memory lanes (rows) of
-//    the finished accumulator, 32 columns (tokens) at a time, and stores
-//    them: for one token, 32 lanes write 32 consecutive rows of Y.
+//    the finished accumulator, 32 columns (tokens) at a time, writes them to
+//    a 4 KB shared-memory buffer as [token][row] and sends the buffer to Y
+//    with one TMA tensor store (two buffers per warp, so the next chunk is
+//    written while the store reads the last). Plain stores replace them when
+//    Y is not 16-byte aligned or n_out is not a multiple of 4: measured, the
+//    32 scalar stores of a chunk took about 0.65 us, a 128 x 128 tile about
+//    3 us, at the end of every CTA's last tile.
 // All waits are bounded and give up when another thread has recorded an
 // error; tensor memory is freed on every path.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "tc_common.cuh"
@@ -32,6 +38,9 @@ constexpr int kGemmBM = 128, kGemmBK = 64;
 constexpr int kGemmThreads = 6 * 32;
 constexpr int kGemmTileBytes = kGemmBM * kGemmBK * 2;  // the A tile, f16
 constexpr int kGemmHdrBytes = 1024;
+// Epilogue staging: two 4 KB buffers (32 tokens x 32 rows of f32) for each of
+// the four epilogue warps, after the ring.
+constexpr int kEpiBytes = 4 * 2 * 4096;
 // Per token-tile width BN (128 or 256): B tile bytes, stage bytes, ring
 // depth (what fits next to the header), shared memory, tensor-memory columns
 // (two accumulators).
@@ -39,8 +48,9 @@ template <int BN> struct GemmShape {
     static constexpr int kBTile = BN * kGemmBK * 2;
     static constexpr int kStage = kGemmTileBytes + kBTile;
     static constexpr int kStages = BN == 128 ? 6 : 4;
-    static constexpr int kSmem = 1024 /* base alignment */ + kGemmHdrBytes + kStages * kStage;
+    static constexpr int kSmem = 1024 /* base alignment */ + kGemmHdrBytes + kStages * kStage + kEpiBytes;
     static constexpr int kTmemCols = 2 * BN;
+    static_assert(kSmem <= 232448, "shared memory");
 };
 
 struct GemmParams {
@@ -48,6 +58,14 @@ struct GemmParams {
     int32_t *err;
     int n_out, n_tok, K;
     int tiles_m, tiles_n;
+    // k split (tensor-memory prefill kernel): each tile's k-blocks in ksplit
+    // parts, run as separate work items; part 0 writes y, part k > 0 writes the
+    // same layout at part + (k - 1) n_tok n_out, and gemm_ksum adds them after
+    int ksplit;
+    float *part;
+    // 1: tiles leave through shared memory and TMA tensor stores (the output
+    // maps); 0: plain stores (y not 16-byte aligned or n_out not a multiple of 4)
+    int tma_out;
 };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int c0, int c1, uint32_t bar) {
@@ -79,10 +97,71 @@ __device__ __forceinline__ void tc_ld32_wait(uint32_t taddr, uint32_t (&v)[32]) 
         : "memory");
 }
 
+// TMA tensor store of a shared-memory box into a 3-D f32 tensor, in the
+// issuing thread's bulk group; the parts of the box past the tensor's extent
+// are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *tm, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most one of this thread's bulk groups still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Wait until this thread's bulk groups are complete (their writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_b32(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Epilogue of one warp's 32 rows of an accumulator tile: tensor-memory
+// columns tcol .. tcol + BN (this warp's lanes) to out[z][tok0 + c][row0 + r].
+// Each 32-column chunk goes from registers into one of the warp's two 4 KB
+// buffers as [token][row] (for one token the 32 lanes write 128 consecutive
+// bytes, no bank conflict) and leaves with one TMA tensor store, which clips
+// rows and tokens past the tensor. Lane 0 issues the stores; a buffer is
+// rewritten only after the store from it two chunks earlier has read it.
+template <int BN>
+__device__ __forceinline__ void epilogue_tma(uint32_t tcol, const CUtensorMap *out, int row0, int tok0, int z,
+                                             uint32_t buf, int lane) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tc_ld32_wait(tcol + static_cast<uint32_t>(c0), v);
+        const uint32_t b = buf + static_cast<uint32_t>((c0 >> 5) & 1) * 4096u;
+        if (lane == 0) bulk_wait_read1();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st_shared_b32(b + 128u * j + 4u * lane, v[j]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(out, b, row0, tok0 + c0, z);
+            bulk_commit();
+        }
+    }
+}
+
+// The same with plain stores to out[tok][n_out] (row = this lane's row).
+template <int BN>
+__device__ __forceinline__ void epilogue_plain(uint32_t tcol, float *out, int n_out, int n_tok, int row, int tok0) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tc_ld32_wait(tcol + static_cast<uint32_t>(c0), v);
+        if (row < n_out) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (tok0 + c0 + j < n_tok) out[static_cast<int64_t>(tok0 + c0 + j) * n_out + row] = __uint_as_float(v[j]);
+        }
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_f16_tc_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                       const GemmParams p) {
+                       const __grid_constant__ CUtensorMap tma_y, const GemmParams p) {
     using Sh = GemmShape<BN>;
     constexpr int kGemmStages = Sh::kStages, kGemmStageBytes = Sh::kStage, kGemmTmemCols = Sh::kTmemCols;
     constexpr int kGemmBN = BN;
@@ -210,6 +289,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ---------------- epilogue: warp w reads tensor-memory lanes 32 (w % 4) ..
         const int q = warp & 3;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const uint32_t epi_buf = stages_a + static_cast<uint32_t>(kGemmStages * kGemmStageBytes + q * 8192);
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -224,23 +304,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const int row = tm * kGemmBM + 32 * q + lane;
-#pragma unroll 1
-            for (int c0 = 0; c0 < kGemmBN; c0 += 32) {
-                uint32_t v[32];
-                tc_ld32_wait(tl + static_cast<uint32_t>(d * kGemmBN + c0), v);
-                const int tok0 = tn * kGemmBN + c0;
-                if (row < p.n_out) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (tok0 + j < p.n_tok)
-                            p.y[static_cast<int64_t>(tok0 + j) * p.n_out + row] = __uint_as_float(v[j]);
-                }
-            }
+            const uint32_t tcol = tl + static_cast<uint32_t>(d * kGemmBN);
+            if (p.tma_out)
+                epilogue_tma<kGemmBN>(tcol, &tma_y, tm * kGemmBM + 32 * q, tn * kGemmBN, 0, epi_buf, lane);
+            else
+                epilogue_plain<kGemmBN>(tcol, p.y, p.n_out, p.n_tok, tm * kGemmBM + 32 * q + lane, tn * kGemmBN);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8 * d);
         }
+        if (lane == 0) bulk_wait_all();  // the stores have read shared memory and written y
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -314,10 +388,11 @@ template <int BN> struct TmemFuseShape {
     static constexpr int kND = BN == 256 ? 1 : 2;                 // accumulators
     static constexpr int kStages = BN == 256 ? 5 : 8;
     static constexpr int kACol0 = kND * BN;                       // first A column
-    static constexpr int kSmem = 1024 + kGemmHdrBytes + kStages * kStage;
+    static constexpr int kSmem = 1024 + kGemmHdrBytes + kStages * kStage + kEpiBytes;
     static constexpr int kTmemCols = 512;
     static_assert(kStage % 1024 == 0, "swizzled B tiles start 1024-byte aligned");
     static_assert(kACol0 + 32 * kStages <= kTmemCols, "tensor-memory columns");
+    static_assert(kSmem <= 232448, "shared memory");
 };
 
 // D (tensor memory) = A (tensor memory) x B (shared memory) (+ D).
@@ -342,7 +417,8 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16])
 template <int BN>
 __global__ void __launch_bounds__(kTmemThreads, 1)
     gemm_q4k_tmem_kernel(const __grid_constant__ CUtensorMap tma_hdr, const __grid_constant__ CUtensorMap tma_codes,
-                         const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+                         const __grid_constant__ CUtensorMap tma_b, const __grid_constant__ CUtensorMap tma_y,
+                         const __grid_constant__ CUtensorMap tma_part, const GemmParams p) {
     using Sh = TmemFuseShape<BN>;
     constexpr int S = Sh::kStages, ND = Sh::kND;
     constexpr int kOffHdr = Sh::kBTile, kOffCodes = kOffHdr + kRawHdr;
@@ -357,8 +433,15 @@ __global__ void __launch_bounds__(kTmemThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(base + 236);
     const uint32_t stages_a = base_a + kGemmHdrBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int total = p.tiles_m * p.tiles_n;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const int total = tiles * p.ksplit;  // work items: (tile, k part), the tile fastest
     const int nk = p.K / kGemmBK;
+    // item t: tile t % tiles, k-blocks [kb0, kb1) of part t / tiles
+    auto kb_range = [&](int t, int &kb0, int &kb1) {
+        const int ks = t / tiles;
+        kb0 = ks * nk / p.ksplit;
+        kb1 = (ks + 1) * nk / p.ksplit;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -393,8 +476,10 @@ __global__ void __launch_bounds__(kTmemThreads, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const int tm = t % p.tiles_m, tn = t / p.tiles_m;
-                for (int kb = 0; kb < nk; ++kb) {
+                const int tile = t % tiles, tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+                int kb0, kb1;
+                kb_range(t, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (issued >= S && !tc_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) {
                         ok = false;
                         break;
@@ -440,7 +525,9 @@ __global__ void __launch_bounds__(kTmemThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t dt = tmem + static_cast<uint32_t>(d * BN);
-                for (int kb = 0; kb < nk; ++kb) {
+                int kb0, kb1;
+                kb_range(t, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!tc_wait(full0 + 8 * s, ph, abort_flag) || !tc_wait(afull0 + 8 * s, ph, abort_flag)) {
                         ok = false;
                         break;
@@ -452,7 +539,7 @@ __global__ void __launch_bounds__(kTmemThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kGemmBK / 16; ++k)
                         tc_mma_ts(dt, at + static_cast<uint32_t>(8 * k), db + static_cast<uint64_t>(2 * k), idesc,
-                                  (kb | k) != 0 ? 1u : 0u);
+                                  (kb != kb0 || k != 0) ? 1u : 0u);
                     tc_commit(empty0 + 8 * s);  // stage s and its A slot are free once these mmas are done
                     if (++s == S) {
                         s = 0;
@@ -473,10 +560,11 @@ __global__ void __launch_bounds__(kTmemThreads, 1)
         // ---------------- epilogue: warp w reads tensor-memory lanes 32 (w % 4) ..
         const int q = warp & 3;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const uint32_t epi_buf = stages_a + static_cast<uint32_t>(S * Sh::kStage + q * 8192);
         int it = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-            const int tm = t % p.tiles_m, tn = t / p.tiles_m, d = it % ND;
+            const int tile = t % tiles, tm = tile % p.tiles_m, tn = tile / p.tiles_m, d = it % ND;
             if (ok && !tc_wait(tfull0 + 8 * d, static_cast<uint32_t>((it / ND) & 1), abort_flag)) {
                 if (lane == 0) {
                     record_error(p.err, kErrConsumerWait);
@@ -487,23 +575,21 @@ __global__ void __launch_bounds__(kTmemThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const int row = tm * kGemmBM + 32 * q + lane;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t v[32];
-                tc_ld32_wait(tl + static_cast<uint32_t>(d * BN + c0), v);
-                const int tok0 = tn * BN + c0;
-                if (row < p.n_out) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (tok0 + j < p.n_tok)
-                            p.y[static_cast<int64_t>(tok0 + j) * p.n_out + row] = __uint_as_float(v[j]);
-                }
+            const int ks = t / tiles;
+            const uint32_t tcol = tl + static_cast<uint32_t>(d * BN);
+            if (p.tma_out) {
+                epilogue_tma<BN>(tcol, ks == 0 ? &tma_y : &tma_part, tm * kGemmBM + 32 * q, tn * BN,
+                                 ks == 0 ? 0 : ks - 1, epi_buf, lane);
+            } else {
+                float *out = ks == 0 ? p.y : p.part + static_cast<int64_t>(ks - 1) * p.n_tok * p.n_out;
+                epilogue_plain<BN>(tcol, out, p.n_out, p.n_tok, tm * kGemmBM + 32 * q + lane, tn * BN);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty0 + 8 * d);
         }
+        if (lane == 0) bulk_wait_all();  // the stores have read shared memory and written their tensor
+        __syncwarp();
     } else {
         // ---------------- converters: lanes 32 q .. of tensor memory, sub-block `half` of each k-block
         const int q = warp & 3, half = (warp - 6) >> 2;
@@ -513,7 +599,9 @@ __global__ void __launch_bounds__(kTmemThreads, 1)
         uint32_t ph = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            for (int kb = 0; kb < nk; ++kb) {
+            int kb0, kb1;
+            kb_range(t, kb0, kb1);
+            for (int kb = kb0; kb < kb1; ++kb) {
                 // the tensor-memory store below is warp-collective: the warp goes on or stops as one
                 if (!__all_sync(0xffffffffu, tc_wait(full0 + 8 * s, ph, abort_flag))) {
                     ok = false;
@@ -626,6 +714,27 @@ bool encode_q4k_map(CUtensorMap *tm, const void *W, int64_t n_out, int64_t row_b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An f32 output [depth][n_tok][n_out] as a 3-D tensor with a box of 32 rows x
+// 32 tokens x 1 (the epilogue's TMA stores). Needs base 16-byte aligned and
+// n_out a multiple of 4 (16-byte row pitch).
+bool encode_out_map(CUtensorMap *tm, void *base, int64_t n_out, int64_t n_tok, int64_t depth) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(n_out), static_cast<cuuint64_t>(n_tok),
+                                static_cast<cuuint64_t>(depth)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(n_out) * 4, static_cast<cuuint64_t>(n_out * n_tok) * 4};
+    const cuuint32_t box[3] = {32u, 32u, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Whether y (and the k-split partials) can leave through TMA stores.
+bool out_tma_ok(const float *y, int64_t n_out) {
+    return (reinterpret_cast<uintptr_t>(y) & 15u) == 0 && n_out % 4 == 0;
+}
+
 }  // namespace
 
 cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, cudaStream_t s) {
@@ -637,16 +746,37 @@ cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, c
     return cudaGetLastError();
 }
 
+// y[i] += part[0][i] + ... + part[n_parts - 1][i], added in that order (part k
+// at part + k n), after the GEMM that wrote them has finished.
+__global__ void gemm_ksum_kernel(float *__restrict__ y, const float *__restrict__ part, int64_t n, int n_parts) {
+    pdl_wait_prior_grids();
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float v[7];
+#pragma unroll
+        for (int k = 0; k < 7; ++k) v[k] = k < n_parts ? __ldcg(part + k * n + i) : 0.0f;
+        float acc = y[i];
+#pragma unroll
+        for (int k = 0; k < 7; ++k)
+            if (k < n_parts) acc += v[k];
+        y[i] = acc;
+    }
+}
+
 template <int BN>
 cudaError_t launch_gemm_bn(const __half *A, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
                            int32_t *err, int sms, int device, cudaStream_t s) {
-    CUtensorMap ta, tb;
-    if (!encode_f16_map(&ta, A, n_out, K, kGemmBM) || !encode_f16_map(&tb, B, n_tok, K, BN)) {
+    CUtensorMap ta, tb, ty;
+    const bool tma_out = out_tma_ok(y, n_out);
+    if (!encode_f16_map(&ta, A, n_out, K, kGemmBM) || !encode_f16_map(&tb, B, n_tok, K, BN) ||
+        (tma_out && !encode_out_map(&ty, y, n_out, n_tok, 1))) {
         g_launch_step = "cuTensorMapEncodeTiled";
         return cudaErrorInvalidValue;
     }
+    if (!tma_out) ty = tb;  // unused
     GemmParams p = {};
     p.y = y;
+    p.tma_out = tma_out ? 1 : 0;
     p.err = err;
     p.n_out = static_cast<int>(n_out);
     p.n_tok = static_cast<int>(n_tok);
@@ -664,28 +794,35 @@ cudaError_t launch_gemm_bn(const __half *A, const __half *B, float *y, int64_t n
         if (e != cudaSuccess) return e;
         done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    return launch_pdl(gemm_f16_tc_kernel<BN>, grid, kGemmThreads, GemmShape<BN>::kSmem, s, ta, tb, p);
+    return launch_pdl(gemm_f16_tc_kernel<BN>, grid, kGemmThreads, GemmShape<BN>::kSmem, s, ta, tb, ty, p);
 }
 
 template <int BN>
 cudaError_t launch_tmem_bn(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
-                           int32_t *err, int sms, int device, cudaStream_t s) {
-    CUtensorMap th, tc, tb;
+                           int ksplit, float *part, int32_t *err, int sms, int device, cudaStream_t s) {
+    CUtensorMap th, tc, tb, ty, tp;
     const int64_t row_bytes = K / 256 * kQ4kBlockBytes;
+    const bool tma_out = out_tma_ok(y, n_out);
     if (!encode_q4k_map(&th, W, n_out, row_bytes, 16) || !encode_q4k_map(&tc, W, n_out, row_bytes, 32) ||
-        !encode_f16_map(&tb, B, n_tok, K, BN)) {
+        !encode_f16_map(&tb, B, n_tok, K, BN) || (tma_out && !encode_out_map(&ty, y, n_out, n_tok, 1)) ||
+        (tma_out && ksplit > 1 && !encode_out_map(&tp, part, n_out, n_tok, ksplit - 1))) {
         g_launch_step = "cuTensorMapEncodeTiled";
         return cudaErrorInvalidValue;
     }
+    if (!tma_out) ty = tb;  // unused
+    if (!tma_out || ksplit == 1) tp = ty;
     GemmParams p = {};
     p.y = y;
+    p.tma_out = tma_out ? 1 : 0;
     p.err = err;
     p.n_out = static_cast<int>(n_out);
     p.n_tok = static_cast<int>(n_tok);
     p.K = static_cast<int>(K);
     p.tiles_m = static_cast<int>((n_out + kGemmBM - 1) / kGemmBM);
     p.tiles_n = static_cast<int>((n_tok + BN - 1) / BN);
-    const int64_t total = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+    p.ksplit = ksplit;
+    p.part = part;
+    const int64_t total = static_cast<int64_t>(p.tiles_m) * p.tiles_n * ksplit;
     const int grid = static_cast<int>(total < sms ? total : sms);
     static std::atomic<uint64_t> done{0};
     const uint64_t bit = 1ull << (device & 63);
@@ -696,7 +833,8 @@ cudaError_t launch_tmem_bn(const uint8_t *W, const __half *B, float *y, int64_t 
         if (e != cudaSuccess) return e;
         done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    return launch_pdl(gemm_q4k_tmem_kernel<BN>, grid, kTmemThreads, TmemFuseShape<BN>::kSmem, s, th, tc, tb, p);
+    return launch_pdl(gemm_q4k_tmem_kernel<BN>, grid, kTmemThreads, TmemFuseShape<BN>::kSmem, s, th, tc, tb, ty, tp,
+                      p);
 }
 
 // Y[n_tok][n_out] = dequant(W)[n_out][K] . B[n_tok][K]^T for Q4_K W (K a
@@ -704,10 +842,42 @@ cudaError_t launch_tmem_bn(const uint8_t *W, const __half *B, float *y, int64_t 
 // on the way into tensor memory. Token tiles as launch_gemm_f16_tc chooses
 // them.
 cudaError_t launch_gemm_q4k_tmem(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
-                                 int64_t K, int32_t *err, int sms, int device, cudaStream_t s) {
+                                 int64_t K, int ksplit, float *part, int32_t *err, int sms, int device,
+                                 cudaStream_t s) {
     const int64_t tiles256 = ((n_out + kGemmBM - 1) / kGemmBM) * ((n_tok + 255) / 256);
-    if (tiles256 >= sms) return launch_tmem_bn<256>(W, B, y, n_out, n_tok, K, err, sms, device, s);
-    return launch_tmem_bn<128>(W, B, y, n_out, n_tok, K, err, sms, device, s);
+    if (tiles256 >= sms) return launch_tmem_bn<256>(W, B, y, n_out, n_tok, K, 1, part, err, sms, device, s);
+    cudaError_t e = launch_tmem_bn<128>(W, B, y, n_out, n_tok, K, ksplit, part, err, sms, device, s);
+    if (e != cudaSuccess || ksplit == 1) return e;
+    g_launch_step = "k-split sum";
+    const int64_t n = n_out * n_tok;
+    const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(sms) * 8);
+    return launch_pdl(gemm_ksum_kernel, static_cast<int>(grid), 256, 0, s, y, static_cast<const float *>(part), n,
+                      ksplit - 1);
+}
+
+// The k split launch_gemm_q4k_tmem takes for these sizes: 1 with 256-token
+// tiles; else the part count ks (at most max_parts and 8, at least 4 k-blocks a
+// part, the parts after the first -- f32 [n_tok][n_out] each -- within
+// scratch_bytes) that minimizes the k-blocks of the busiest CTA,
+// ceil(tiles ks / sms) ceil(nk / ks), plus the split's own cost in k-block
+// times: about 4 for the sum launch and one per 2^19 partial values it reads.
+int gemm_q4k_tmem_ksplit(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes) {
+    const int64_t tm = (n_out + kGemmBM - 1) / kGemmBM;
+    if (tm * ((n_tok + 255) / 256) >= sms) return 1;
+    const int64_t tiles = tm * ((n_tok + 127) / 128), nk = K / kGemmBK;
+    if (tiles == 0 || nk == 0) return 1;
+    int best = 1;
+    int64_t best_cost = ((tiles + sms - 1) / sms) * nk;
+    for (int ks = 2; ks <= std::min(max_parts, 8); ++ks) {
+        if (nk / ks < 4 || static_cast<size_t>(ks - 1) * n_tok * n_out * 4 > scratch_bytes) break;
+        const int64_t cost = ((tiles * ks + sms - 1) / sms) * ((nk + ks - 1) / ks) + 4 +
+                             ((ks - 1) * n_tok * n_out >> 19);
+        if (cost < best_cost) {
+            best = ks;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 // Y[n_tok][n_out] = A[n_out][K] . B[n_tok][K]^T for f16 A, B (16-byte

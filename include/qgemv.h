@@ -318,7 +318,11 @@ size_t qgemm_workspace_bytes(int type, int64_t n_out, int64_t n_in, int64_t n_to
  * see the knob QG_FUSED_GEMM of qg_tune) W is instead dequantized inside the
  * GEMM (raw blocks are loaded into shared memory and expanded to the same
  * f16 values in tensor memory, where the mma reads them; no f16 copy of W is
- * written), with the same result bit for bit. The result differs from the f32 product by the f16
+ * written), with the same result bit for bit; when its 128 x 128 tiles are
+ * fewer than the SMs it also splits each tile's k-range into parts (knob
+ * QG_GEMM_KSPLIT), whose f32 partial products go to the workspace and are
+ * added to y in part order by one more launch: deterministic, and within
+ * n_in 2^-23 sum_i |W[o][i] x[t][i]| of the unsplit result. The result differs from the f32 product by the f16
  * rounding of each weight and activation (at most 2^-11 relative each) and
  * the f32 accumulation: |y - y_exact| <= (2^-10 + n_in 2^-24) sum_i
  * |W[o][i] x[t][i]| (values beyond f16's range, 65504, become inf).
@@ -370,7 +374,11 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
  * more vectors, rows of 2048 or 4096 elements: 0 never, the default; 1
  * whenever it fits), QG_FUSED_GEMM (qgemm on Q4_K weights: 0 writes the f16
  * copy of W to the workspace first; 1 dequantizes inside the GEMM, into
- * tensor memory, instead; 2, the default, does so up to 512 tokens). value is clamped to the knob's range; the old
+ * tensor memory, instead; 2, the default, does so up to 512 tokens),
+ * QG_GEMM_KSPLIT (that fused GEMM, when its 128 x 128 tiles are fewer than the
+ * SMs, splits each tile's k-blocks into at most this many parts, 1 to 8, the
+ * default 8, at least 4 k-blocks a part; the parts' f32 sums are added in part
+ * order, so results stay deterministic). value is clamped to the knob's range; the old
  * value goes to *previous when that is not NULL. Returns QG_OK, QG_ERR_NULL
  * or QG_ERR_TYPE (unknown name). Host-only; affects launches planned after
  * it returns. */

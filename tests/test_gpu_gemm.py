@@ -107,25 +107,36 @@ def test_gemm_wide_token_tiles():
 
 
 @pytest.mark.parametrize("shape", [(1, 256, 1), (100, 512, 37), (129, 1024, 130), (4352, 4096, 640),
-                                   (4096, 2048, 1300), (300, 11008, 257)])
+                                   (4096, 2048, 1300), (300, 11008, 257), (4096, 4096, 64), (4096, 11008, 200)])
 def test_fused_q4_k_equals_the_f16_copy_path(shape):
     """Q4_K blocks expanded to f16 inside the GEMM (into tensor memory, where
     the mma reads its A operand) give the same bits as dequantizing W to an
     f16 copy first (the same f16 values, the same mma order): ragged row
     tiles (rows past the matrix are zeros), ragged token tiles, 128- and
-    256-token tiles, long rows."""
+    256-token tiles, long rows. With the k-blocks split into parts (few tiles)
+    only the f32 additions differ: each part's sum, then the parts in order,
+    so the two agree within n_in 2^-23 of sum_i |W[o][i] x[t][i]|."""
     n_out, n_in, n_tok = shape
-    rng = np.random.default_rng(7700 + n_out)
-    Wd = dev(weights(qg.Q4_K, n_out, n_in, rng))
-    xd = dev(synth.f32_normal(rng, n_tok * n_in))
+    rng = np.random.default_rng(7700 + n_out + n_tok)
+    W = weights(qg.Q4_K, n_out, n_in, rng)
+    x = synth.f32_normal(rng, n_tok * n_in)
+    Wd, xd = dev(W), dev(x)
     old = qg.tune("QG_FUSED_GEMM", 1)
+    old_ks = qg.tune("QG_GEMM_KSPLIT", 1)
     try:
         fused = host(qg.qgemm(qg.Q4_K, Wd, xd, n_out, n_in, n_tok))
+        qg.tune("QG_GEMM_KSPLIT", old_ks)
+        split = host(qg.qgemm(qg.Q4_K, Wd, xd, n_out, n_in, n_tok))
         qg.tune("QG_FUSED_GEMM", 0)
         copy = host(qg.qgemm(qg.Q4_K, Wd, xd, n_out, n_in, n_tok))
     finally:
         qg.tune("QG_FUSED_GEMM", old)
+        qg.tune("QG_GEMM_KSPLIT", old_ks)
     assert np.array_equal(fused.view(np.uint32), copy.view(np.uint32))
+    wd = np.abs(oracle.dequantize(qg.Q4_K, W, n_out * n_in).reshape(n_out, n_in).astype(np.float64))
+    mag = np.abs(x.reshape(n_tok, n_in).astype(np.float64)) @ wd.T
+    err = np.abs(split.astype(np.float64) - copy.astype(np.float64)).reshape(n_tok, n_out)
+    assert np.all(err <= n_in * 2.0 ** -23 * mag)
     assert qg.device_error() == 0
 
 

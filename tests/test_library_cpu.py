@@ -187,6 +187,8 @@ def test_tune_knobs(L):
     old = qg.tune("QG_FUSED_GEMM", 9)  # 0, 1 or 2 (the default: fused up to 512 tokens)
     assert old in (0, 1, 2)
     assert qg.tune("QG_FUSED_GEMM", old) == 2  # clamped to 2
+    old = qg.tune("QG_GEMM_KSPLIT", 0)  # 1 .. 8 parts (the default: at most 8)
+    assert old == 8 and qg.tune("QG_GEMM_KSPLIT", old) == 1  # clamped to 1
 
 
 def test_batched_validation(L):
