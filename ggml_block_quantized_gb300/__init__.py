@@ -21,6 +21,7 @@ __all__ = [
     "qgemv", "qgemv_xq", "qgemv_block_isums", "qgemv_noalloc", "qgemv_batched",
     "qgemv_batched_workspace_bytes", "BatchPlan", "device_error", "kernel_info", "EXPORTED_SYMBOLS",
     "MAX_BATCH", "tune", "qgemm_workspace_bytes", "qgemm", "qgemm_f16", "selftest_bounded_wait",
+    "gemm_kernel_info",
 ]
 
 F32, F16, Q4_0, Q4_1, Q5_0, Q8_0, Q8_1 = 0, 1, 2, 3, 6, 8, 9
@@ -36,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "quantize_act", "quantize_rows", "dequantize_rows", "qgemv_workspace_bytes", "qgemv",
     "qgemv_xq", "qgemv_block_isums", "qg_device_error", "qgemv_noalloc",
     "qgemv_batched_workspace_bytes", "qgemv_batched", "qgemv_kernel_info", "qg_tune",
-    "qgemm_workspace_bytes", "qgemm", "qgemm_f16", "qg_selftest_bounded_wait",
+    "qgemm_workspace_bytes", "qgemm", "qgemm_f16", "qg_selftest_bounded_wait", "qgemm_kernel_info",
 )
 MAX_BATCH = 256
 
@@ -93,6 +94,8 @@ def lib():
         L.qgemv_batched.restype = i32
         L.qgemv_kernel_info.argtypes = [i32, i64, i64, i64, i32]
         L.qgemv_kernel_info.restype = ctypes.c_char_p
+        L.qgemm_kernel_info.argtypes = [i32, i64, i64, i64]
+        L.qgemm_kernel_info.restype = ctypes.c_char_p
         L.qg_tune.argtypes, L.qg_tune.restype = [ctypes.c_char_p, i32, ctypes.POINTER(i32)], i32
         L.qgemm_workspace_bytes.argtypes, L.qgemm_workspace_bytes.restype = [i32, i64, i64, i64], sz
         L.qgemm.argtypes, L.qgemm.restype = [i32, vp, vp, vp, i64, i64, i64, vp, sz, vp], i32
@@ -366,6 +369,11 @@ def qgemm_f16(A, B, n_out: int, n_tok: int, K: int, y=None, stream=None):
 def kernel_info(t: int, total_rows: int, n_in: int, n_vec: int = 1, n_mats: int = 1) -> str:
     """Which kernel and plan a product would use on the current device."""
     return lib().qgemv_kernel_info(t, total_rows, n_in, n_vec, n_mats).decode()
+
+
+def gemm_kernel_info(t: int, n_out: int, n_in: int, n_tok: int) -> str:
+    """Which GEMM kernel, tiles and launches qgemm would use on the current device."""
+    return lib().qgemm_kernel_info(t, n_out, n_in, n_tok).decode()
 
 
 def tune(name: str, value: int) -> int:

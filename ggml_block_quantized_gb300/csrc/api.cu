@@ -25,10 +25,14 @@ cudaError_t launch_dequant(int type, const uint8_t *w, O *out, int64_t groups, u
 cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, cudaStream_t s);
 cudaError_t launch_gemm_f16_tc(const __half *A, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
                                int32_t *err, int sms, int device, cudaStream_t s);
+struct GemmPlan {
+    int bn, ks;
+};
 cudaError_t launch_gemm_q4k_tmem(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
-                                 int64_t K, int ksplit, float *part, int32_t *err, int sms, int device,
+                                 int64_t K, GemmPlan plan, float *part, int32_t *err, int sms, int device,
                                  cudaStream_t s);
-int gemm_q4k_tmem_ksplit(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes);
+GemmPlan gemm_q4k_tmem_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes);
+GemmPlan gemm_f16_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms);
 cudaError_t launch_gemv_tc_q4_k(const TcParams &p, const TcMat *mats, int n, int grid, int smem, int smem_optin,
                                 int device, cudaStream_t s);
 
@@ -159,8 +163,9 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 //    shared memory fits (rows of 8 or 16 blocks);
 //  QG_FUSED_GEMM: qgemm on Q4_K weights dequantizes into an f16 copy in the
 //    workspace first (0) or inside the GEMM, into tensor memory (1: no f16
-//    copy of W); 2, the default, fuses up to kFusedGemmMaxTok tokens (measured
-//    5-6% faster from 64 to 512 tokens, 12% slower at 768, 11% at 1024);
+//    copy of W); 2, the default, fuses while the fused GEMM has at most two
+//    256-token tiles per SM (fused_gemm_default: measured as fast or faster
+//    from 16 to 2048 tokens on 4096 x 4096, 10% slower at 4096 tokens);
 //  QG_GEMM_KSPLIT: the fused GEMM splits each tile's k-blocks into at most this
 //    many parts when its tiles leave SMs idle (1: no split).
 enum KnobId {
@@ -188,7 +193,6 @@ constexpr KnobDef kKnobs[kKnobCount] = {
     {"QG_FUSED_GEMM", 2, 0, 2},           {"QG_MMA_GROUP_MELEM", 40, 0, 1 << 20},
     {"QG_GEMM_KSPLIT", 8, 1, 8}};
 std::atomic<int> g_knob_val[kKnobCount];  // value + 1; 0 = not read yet
-constexpr int64_t kFusedGemmMaxTok = 512;  // QG_FUSED_GEMM = 2: the fused prefill up to this many tokens
 
 int knob(KnobId k) {
     int v = g_knob_val[k].load(std::memory_order_relaxed);
@@ -998,6 +1002,13 @@ size_t qgemm_workspace_bytes(int type, int64_t n_out, int64_t n_in, int64_t n_to
     return a + b > 0 ? a + b : 16;
 }
 
+// Whether qgemm routes Q4_K weights to the fused GEMM (QG_FUSED_GEMM).
+bool fused_gemm(int type, int64_t n_out, int64_t n_tok, int sms) {
+    if (type != QG_Q4_K) return false;
+    const int fuse = knob(kKnobFusedGemm);
+    return fuse == 1 || (fuse == 2 && ((n_out + 127) / 128) * ((n_tok + 255) / 256) <= 2 * static_cast<int64_t>(sms));
+}
+
 int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int64_t n_in, int64_t n_tok,
           void *workspace, size_t workspace_bytes, qg_stream_t stream) {
     int st = check_weight_type(type);
@@ -1024,16 +1035,15 @@ int qgemm(int type, const void *W, const float *x, float *y, int64_t n_out, int6
     __half *A = static_cast<__half *>(workspace);
     __half *B = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) +
                                            ((static_cast<size_t>(2 * n_out * n_in) + 255) & ~size_t(255)));
-    const int fuse = knob(kKnobFusedGemm);
-    if (type == QG_Q4_K && (fuse == 1 || (fuse == 2 && n_tok <= kFusedGemmMaxTok))) {
+    if (fused_gemm(type, n_out, n_tok, dev.sms)) {
         // W is dequantized inside the GEMM (into tensor memory): only x is converted first.
         // With few tiles the GEMM splits k; the workspace's f16-weight part, unused
         // here, holds the partial products of the parts after the first.
-        const int ks = gemm_q4k_tmem_ksplit(n_out, n_tok, n_in, dev.sms, knob(kKnobGemmKsplit),
-                                            static_cast<size_t>(2 * n_out * n_in));
+        const GemmPlan plan = gemm_q4k_tmem_plan(n_out, n_tok, n_in, dev.sms, knob(kKnobGemmKsplit),
+                                                 static_cast<size_t>(2 * n_out * n_in));
         cudaError_t e = launch_f32_to_f16(x, B, n_tok * n_in, dev.sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "prefill: x to f16");
-        e = launch_gemm_q4k_tmem(static_cast<const uint8_t *>(W), B, y, n_out, n_tok, n_in, ks,
+        e = launch_gemm_q4k_tmem(static_cast<const uint8_t *>(W), B, y, n_out, n_tok, n_in, plan,
                                  reinterpret_cast<float *>(A), dev.err, dev.sms, dev.device, s);
         if (e != cudaSuccess) return cuda_fail(e, g_launch_step);
         return QG_OK;
@@ -1114,6 +1124,34 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
     std::snprintf(buf, sizeof buf, "gemv_kernel<%s,NV=%d> grid=%d stages=%d split=%d rows_per_stage=%d lanes_per_block=%d smem=%d%s",
                   tn, static_cast<int>(n_vec), gl.grid, gp.n_stages, gp.split, gp.rows_per_stage, gl.lpb, gl.smem,
                   fused ? " fused-quantize" : "");
+    return buf;
+}
+
+const char *qgemm_kernel_info(int type, int64_t n_out, int64_t n_in, int64_t n_tok) {
+    static thread_local char buf[320];
+    buf[0] = 0;
+    int elems, bytes;
+    if (check_weight_type(type) != QG_OK || !block_info(type, &elems, &bytes)) return buf;
+    if (n_out < 1 || n_tok < 1 || n_in < 1 || n_out > INT32_MAX || n_tok > INT32_MAX || n_in > INT32_MAX ||
+        n_in % elems != 0)
+        return buf;
+    DeviceInfo dev;
+    if (current_device(&dev) != QG_OK) {
+        std::snprintf(buf, sizeof buf, "cuda: %s", g_last_cuda_error);
+        return buf;
+    }
+    if (fused_gemm(type, n_out, n_tok, dev.sms)) {
+        const GemmPlan p = gemm_q4k_tmem_plan(n_out, n_tok, n_in, dev.sms, knob(kKnobGemmKsplit),
+                                              static_cast<size_t>(2 * n_out * n_in));
+        const int64_t items = ((n_out + 127) / 128) * ((n_tok + p.bn - 1) / p.bn) * p.ks;
+        std::snprintf(buf, sizeof buf, "gemm_q4k_tmem_kernel<%d> grid=%d ksplit=%d launches=%d", p.bn,
+                      static_cast<int>(std::min<int64_t>(items, dev.sms)), p.ks, p.ks > 1 ? 3 : 2);
+        return buf;
+    }
+    const GemmPlan p = gemm_f16_plan(n_out, n_tok, n_in, dev.sms);
+    const int64_t tiles = ((n_out + 127) / 128) * ((n_tok + p.bn - 1) / p.bn);
+    std::snprintf(buf, sizeof buf, "gemm_f16_tc_kernel<%d> grid=%d ksplit=1 launches=3", p.bn,
+                  static_cast<int>(std::min<int64_t>(tiles, dev.sms)));
     return buf;
 }
 

@@ -53,6 +53,11 @@ template <int BN> struct GemmShape {
     static_assert(kSmem <= 232448, "shared memory");
 };
 
+// Token-tile width (128 or 256) and k-split parts of the fused GEMM.
+struct GemmPlan {
+    int bn, ks;
+};
+
 struct GemmParams {
     float *y;  // [n_tok][n_out]
     int32_t *err;
@@ -839,55 +844,69 @@ cudaError_t launch_tmem_bn(const uint8_t *W, const __half *B, float *y, int64_t 
 
 // Y[n_tok][n_out] = dequant(W)[n_out][K] . B[n_tok][K]^T for Q4_K W (K a
 // multiple of 256, rows 16-byte aligned) and f16 B, the dequantization done
-// on the way into tensor memory. Token tiles as launch_gemm_f16_tc chooses
-// them.
+// on the way into tensor memory, with the tile width and k split of `plan`
+// (gemm_q4k_tmem_plan); a split's partials go to `part`.
 cudaError_t launch_gemm_q4k_tmem(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
-                                 int64_t K, int ksplit, float *part, int32_t *err, int sms, int device,
+                                 int64_t K, GemmPlan plan, float *part, int32_t *err, int sms, int device,
                                  cudaStream_t s) {
-    const int64_t tiles256 = ((n_out + kGemmBM - 1) / kGemmBM) * ((n_tok + 255) / 256);
-    if (tiles256 >= sms) return launch_tmem_bn<256>(W, B, y, n_out, n_tok, K, 1, part, err, sms, device, s);
-    cudaError_t e = launch_tmem_bn<128>(W, B, y, n_out, n_tok, K, ksplit, part, err, sms, device, s);
-    if (e != cudaSuccess || ksplit == 1) return e;
+    cudaError_t e = plan.bn == 256 ? launch_tmem_bn<256>(W, B, y, n_out, n_tok, K, plan.ks, part, err, sms, device, s)
+                                   : launch_tmem_bn<128>(W, B, y, n_out, n_tok, K, plan.ks, part, err, sms, device, s);
+    if (e != cudaSuccess || plan.ks == 1) return e;
     g_launch_step = "k-split sum";
     const int64_t n = n_out * n_tok;
     const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(sms) * 8);
     return launch_pdl(gemm_ksum_kernel, static_cast<int>(grid), 256, 0, s, y, static_cast<const float *>(part), n,
-                      ksplit - 1);
+                      plan.ks - 1);
 }
 
-// The k split launch_gemm_q4k_tmem takes for these sizes: 1 with 256-token
-// tiles; else the part count ks (at most max_parts and 8, at least 4 k-blocks a
-// part, the parts after the first -- f32 [n_tok][n_out] each -- within
-// scratch_bytes) that minimizes the k-blocks of the busiest CTA,
-// ceil(tiles ks / sms) ceil(nk / ks), plus the split's own cost in k-block
-// times: about 4 for the sum launch and one per 2^19 partial values it reads.
-int gemm_q4k_tmem_ksplit(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes) {
-    const int64_t tm = (n_out + kGemmBM - 1) / kGemmBM;
-    if (tm * ((n_tok + 255) / 256) >= sms) return 1;
-    const int64_t tiles = tm * ((n_tok + 127) / 128), nk = K / kGemmBK;
-    if (tiles == 0 || nk == 0) return 1;
-    int best = 1;
-    int64_t best_cost = ((tiles + sms - 1) / sms) * nk;
-    for (int ks = 2; ks <= std::min(max_parts, 8); ++ks) {
-        if (nk / ks < 4 || static_cast<size_t>(ks - 1) * n_tok * n_out * 4 > scratch_bytes) break;
-        const int64_t cost = ((tiles * ks + sms - 1) / sms) * ((nk + ks - 1) / ks) + 4 +
-                             ((ks - 1) * n_tok * n_out >> 19);
-        if (cost < best_cost) {
-            best = ks;
-            best_cost = cost;
+// Token-tile width and k split for a GEMM of these sizes: the pair that
+// minimizes the busiest CTA's time, ceil(tiles ks / sms) ceil(nk / ks)
+// k-blocks at 10 units each with 128-token tiles and unit256 with 256-token
+// tiles, plus the split's own cost: about 4 k-blocks for the sum launch and one
+// per 2^19 partial values it reads. Splits keep at least 4 k-blocks a part, at
+// most max_parts (and 8) parts, the parts after the first (f32 [n_tok][n_out]
+// each) within scratch_bytes, and with 256-token tiles at most one item per
+// CTA. Ties keep the narrower tile and fewer parts.
+GemmPlan gemm_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes,
+                   int unit256) {
+    GemmPlan best = {128, 1};
+    const int64_t tm = (n_out + kGemmBM - 1) / kGemmBM, nk = (K + kGemmBK - 1) / kGemmBK;
+    if (tm == 0 || n_tok == 0 || nk == 0 || sms < 1) return best;
+    int64_t best_cost = -1;
+    for (int bn : {128, 256}) {
+        const int64_t tiles = tm * ((n_tok + bn - 1) / bn), unit = bn == 256 ? unit256 : 10;
+        for (int ks = 1; ks <= std::min(max_parts, 8); ++ks) {
+            if (ks > 1 && (nk / ks < 4 || static_cast<size_t>(ks - 1) * n_tok * n_out * 4 > scratch_bytes)) break;
+            if (bn == 256 && ks > 1 && tiles * ks > sms) break;
+            int64_t cost = ((tiles * ks + sms - 1) / sms) * ((nk + ks - 1) / ks) * unit;
+            if (ks > 1) cost += 10 * (4 + ((ks - 1) * n_tok * n_out >> 19));
+            if (best_cost < 0 || cost < best_cost) {
+                best = {bn, ks};
+                best_cost = cost;
+            }
         }
     }
     return best;
 }
 
+// The fused Q4_K GEMM's plan: measured 0.39 us a k-block with 128-token tiles
+// and about 0.5 with 256 (its converters' work grows with the tile), so 13 units.
+GemmPlan gemm_q4k_tmem_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes) {
+    return gemm_plan(n_out, n_tok, K, sms, max_parts, scratch_bytes, 13);
+}
+
+// The f16 GEMM's plan (no split: qgemm_f16 has no scratch): measured 0.37 us
+// a k-block with 128-token tiles and 0.38 with 256, so 11 units.
+GemmPlan gemm_f16_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms) {
+    return gemm_plan(n_out, n_tok, K, sms, 1, 0, 11);
+}
+
 // Y[n_tok][n_out] = A[n_out][K] . B[n_tok][K]^T for f16 A, B (16-byte
-// aligned, K a multiple of 8). Token tiles of 256 (an mma of N = 256 does
-// twice the work of N = 128 for about 1.35 times the cycles) when they still
-// give every SM a tile, else 128.
+// aligned, K a multiple of 8), token tiles as gemm_f16_plan chooses them.
 cudaError_t launch_gemm_f16_tc(const __half *A, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
                                int32_t *err, int sms, int device, cudaStream_t s) {
-    const int64_t tiles256 = ((n_out + kGemmBM - 1) / kGemmBM) * ((n_tok + 255) / 256);
-    if (tiles256 >= sms) return launch_gemm_bn<256>(A, B, y, n_out, n_tok, K, err, sms, device, s);
+    if (gemm_f16_plan(n_out, n_tok, K, sms).bn == 256)
+        return launch_gemm_bn<256>(A, B, y, n_out, n_tok, K, err, sms, device, s);
     return launch_gemm_bn<128>(A, B, y, n_out, n_tok, K, err, sms, device, s);
 }
 

@@ -314,8 +314,8 @@ size_t qgemm_workspace_bytes(int type, int64_t n_out, int64_t n_in, int64_t n_to
  * it with f32 x; here the whole product is one dense GEMM). Steps, all on
  * `stream`: dequantize W to f16 (round to nearest even) into the workspace,
  * round x to f16 into the workspace, then a tcgen05 tensor-core GEMM with
- * f32 accumulation. For Q4_K weights and at most 512 tokens (by default;
- * see the knob QG_FUSED_GEMM of qg_tune) W is instead dequantized inside the
+ * f32 accumulation. For Q4_K weights and up to 2048 tokens for 4096 rows (by
+ * default; see the knob QG_FUSED_GEMM of qg_tune) W is instead dequantized inside the
  * GEMM (raw blocks are loaded into shared memory and expanded to the same
  * f16 values in tensor memory, where the mma reads them; no f16 copy of W is
  * written), with the same result bit for bit; when its 128 x 128 tiles are
@@ -360,6 +360,14 @@ int qgemm_f16(const void *A, const void *B, float *y, int64_t n_out, int64_t n_t
  * a CUDA error. Launches nothing. */
 const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_t n_vec, int n_mats);
 
+/* The same for qgemm on these sizes: the GEMM kernel with its token-tile
+ * width, CTAs, k-split parts and the launches one call makes, e.g.
+ * "gemm_q4k_tmem_kernel<256> grid=128 ksplit=2 launches=3" (x to f16, the
+ * fused GEMM, the sum of the k-split parts) or "gemm_f16_tc_kernel<128>
+ * grid=152 ksplit=1 launches=3" (W to f16, x to f16, the GEMM). Same
+ * ownership and errors as qgemv_kernel_info; launches nothing. */
+const char *qgemm_kernel_info(int type, int64_t n_out, int64_t n_in, int64_t n_tok);
+
 /* Sets a tuning knob for the rest of the process (the pages have no
  * counterpart; the knobs choose between kernels that compute the same
  * product). name is one of the environment variables the library reads once
@@ -374,7 +382,8 @@ const char *qgemv_kernel_info(int type, int64_t total_rows, int64_t n_in, int64_
  * more vectors, rows of 2048 or 4096 elements: 0 never, the default; 1
  * whenever it fits), QG_FUSED_GEMM (qgemm on Q4_K weights: 0 writes the f16
  * copy of W to the workspace first; 1 dequantizes inside the GEMM, into
- * tensor memory, instead; 2, the default, does so up to 512 tokens),
+ * tensor memory, instead; 2, the default, does so while that GEMM has at
+ * most two 256-token tiles per SM: up to 2048 tokens for 4096 rows),
  * QG_GEMM_KSPLIT (that fused GEMM, when its 128 x 128 tiles are fewer than the
  * SMs, splits each tile's k-blocks into at most this many parts, 1 to 8, the
  * default 8, at least 4 k-blocks a part; the parts' f32 sums are added in part

@@ -107,13 +107,14 @@ def test_gemm_wide_token_tiles():
 
 
 @pytest.mark.parametrize("shape", [(1, 256, 1), (100, 512, 37), (129, 1024, 130), (4352, 4096, 640),
-                                   (4096, 2048, 1300), (300, 11008, 257), (4096, 4096, 64), (4096, 11008, 200)])
+                                   (4096, 2048, 1300), (300, 11008, 257), (4096, 4096, 64), (4096, 11008, 200),
+                                   (4096, 4096, 384)])
 def test_fused_q4_k_equals_the_f16_copy_path(shape):
     """Q4_K blocks expanded to f16 inside the GEMM (into tensor memory, where
     the mma reads its A operand) give the same bits as dequantizing W to an
     f16 copy first (the same f16 values, the same mma order): ragged row
     tiles (rows past the matrix are zeros), ragged token tiles, 128- and
-    256-token tiles, long rows. With the k-blocks split into parts (few tiles)
+    256-token tiles (both also with a k split), long rows. With the k-blocks split into parts (few tiles)
     only the f32 additions differ: each part's sum, then the parts in order,
     so the two agree within n_in 2^-23 of sum_i |W[o][i] x[t][i]|."""
     n_out, n_in, n_tok = shape
@@ -138,6 +139,24 @@ def test_fused_q4_k_equals_the_f16_copy_path(shape):
     err = np.abs(split.astype(np.float64) - copy.astype(np.float64)).reshape(n_tok, n_out)
     assert np.all(err <= n_in * 2.0 ** -23 * mag)
     assert qg.device_error() == 0
+
+
+def test_gemm_plans():
+    """The plan qgemm reports: Q4_K fused with a k split when its tiles are
+    few, 256-token tiles when they pay, the f16-copy GEMM for the other types
+    and past two fused tiles per SM; a split adds the sum launch."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    info = qg.gemm_kernel_info(qg.Q4_K, 4096, 4096, 64)
+    assert info.startswith("gemm_q4k_tmem_kernel<128>") and "launches=3" in info and "ksplit=1 " not in info
+    assert qg.gemm_kernel_info(qg.Q4_K, 4096, 4096, 1024).startswith("gemm_q4k_tmem_kernel<256>")
+    big = qg.gemm_kernel_info(qg.Q4_K, 4096, 4096, 256 * (2 * sms // 32 + 1))
+    assert big.startswith("gemm_f16_tc_kernel<256>") and big.endswith("launches=3")
+    assert qg.gemm_kernel_info(qg.Q6_K, 4096, 4096, 64).startswith("gemm_f16_tc_kernel<128>")
+    old = qg.tune("QG_GEMM_KSPLIT", 1)
+    try:
+        assert qg.gemm_kernel_info(qg.Q4_K, 4096, 4096, 64).endswith("ksplit=1 launches=2")
+    finally:
+        qg.tune("QG_GEMM_KSPLIT", old)
 
 
 def test_gemm_is_deterministic_and_edges():

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declarations_are_exported(L):
     names = declared_functions()
-    assert len(names) == 22
+    assert len(names) == 23
     assert sorted(qg.EXPORTED_SYMBOLS) == names
     for n in names:
         assert hasattr(L, n), n
@@ -170,6 +170,10 @@ def test_other_entry_points_validate(L):
     assert L.qgemv_kernel_info(qg.Q4_K, 16, 250, 1, 1) == b""
     assert L.qgemv_kernel_info(qg.Q4_K, 16, 256, 9, 1) == b""
     assert L.qgemv_kernel_info(qg.Q4_K, 16, 256, 1, 0) == b""
+    assert L.qgemm_kernel_info(qg.Q8_K, 16, 256, 4) == b""
+    assert L.qgemm_kernel_info(qg.Q4_K, 16, 250, 4) == b""
+    assert L.qgemm_kernel_info(qg.Q4_K, 0, 256, 4) == b""
+    assert L.qgemm_kernel_info(qg.Q4_K, 16, 256, 0) == b""
 
 
 def test_tune_knobs(L):
