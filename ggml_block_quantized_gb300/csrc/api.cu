@@ -7,6 +7,7 @@
 
 #include <atomic>
 
+#include "gemm_tc.cuh"
 #include "gemv_launch.cuh"
 #include "gemv_tc.cuh"
 
@@ -21,18 +22,6 @@ cudaError_t launch_quantize_batched_kernel(int type, int grid, int block, cudaSt
 template <class O>
 cudaError_t launch_dequant(int type, const uint8_t *w, O *out, int64_t groups, unsigned grid, int threads,
                            cudaStream_t s);
-// gemm_tc.cu: f32 -> f16 and the tcgen05 f16 GEMM of the prefill product.
-cudaError_t launch_f32_to_f16(const float *x, __half *out, int64_t n, int sms, cudaStream_t s);
-cudaError_t launch_gemm_f16_tc(const __half *A, const __half *B, float *y, int64_t n_out, int64_t n_tok, int64_t K,
-                               int32_t *err, int sms, int device, cudaStream_t s);
-struct GemmPlan {
-    int bn, ks;
-};
-cudaError_t launch_gemm_q4k_tmem(const uint8_t *W, const __half *B, float *y, int64_t n_out, int64_t n_tok,
-                                 int64_t K, GemmPlan plan, float *part, int32_t *err, int sms, int device,
-                                 cudaStream_t s);
-GemmPlan gemm_q4k_tmem_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes);
-GemmPlan gemm_f16_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms);
 cudaError_t launch_gemv_tc_q4_k(const TcParams &p, const TcMat *mats, int n, int grid, int smem, int smem_optin,
                                 int device, cudaStream_t s);
 

@@ -30,6 +30,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "gemm_tc.cuh"
 #include "tc_common.cuh"
 
 namespace qg {
@@ -51,11 +52,6 @@ template <int BN> struct GemmShape {
     static constexpr int kSmem = 1024 /* base alignment */ + kGemmHdrBytes + kStages * kStage + kEpiBytes;
     static constexpr int kTmemCols = 2 * BN;
     static_assert(kSmem <= 232448, "shared memory");
-};
-
-// Token-tile width (128 or 256) and k-split parts of the fused GEMM.
-struct GemmPlan {
-    int bn, ks;
 };
 
 struct GemmParams {
