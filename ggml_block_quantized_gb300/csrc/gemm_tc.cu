@@ -886,7 +886,8 @@ GemmPlan gemm_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_par
 }
 
 // The fused Q4_K GEMM's plan: measured 0.39 us a k-block with 128-token tiles
-// and about 0.5 with 256 (its converters' work grows with the tile), so 13 units.
+// and about 0.5 with 256 (five ring stages instead of eight, one accumulator,
+// an mma twice as large), so 13 units.
 GemmPlan gemm_q4k_tmem_plan(int64_t n_out, int64_t n_tok, int64_t K, int sms, int max_parts, size_t scratch_bytes) {
     return gemm_plan(n_out, n_tok, K, sms, max_parts, scratch_bytes, 13);
 }
