@@ -88,7 +88,9 @@ def kernel_source_hash(family):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ggml_block_quantized_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if family in ("mma", "tc"):
+        if family == "gemm":  # the prefill GEMMs
+            mine = name.startswith("gemm") or name == "tc_common.cuh"
+        elif family in ("mma", "tc"):
             mine = name.startswith("gemv_" + family)
         else:
             mine = name.startswith("gemv") and not name.startswith(("gemv_mma", "gemv_tc"))
@@ -920,7 +922,8 @@ def run_prefill(args, rank, world, local_rank):
         # (conversion included, an underestimate); the f16 GEMM is timed alone
         "roofline": ({"bound": "tensor", "kernel": plan.split()[0] + " with the x conversion before it (one qgemm call)",
                       "achieved": round(flops / (call_us * 1e-6) / 1e12, 1), "peak": peak, "peak_kind": peak_kind,
-                      "unit": "TFLOP/s", "frac": round(flops / (call_us * 1e-6) / 1e12 / peak, 4), "traffic": None,
+                      "unit": "TFLOP/s", "frac": round(flops / (call_us * 1e-6) / 1e12 / peak, 4),
+                      "traffic": committed_traffic(f"{plan.split()[0]}@{args.workload}@{n_tok}", "gemm"),
                       "algorithmic_flops_per_launch": int(flops), "avg_launch_us": round(call_us, 3),
                       "launches": launches_per_call} if fused_default else
                      {"bound": "tensor", "kernel": "gemm_f16_tc_kernel, 128-row x 128- or 256-token tiles (qgemm_f16)",
