@@ -305,7 +305,10 @@ int qgemv_batched(int type, const qg_gemv_mat *mats, int n_mats, int64_t n_in, i
 /* ---- Prefill: many tokens ------------------------------------------------ */
 
 /* Workspace bytes qgemm needs: the f16 copy of W (2 * n_out * n_in) and of x
- * (2 * n_tok * n_in), each rounded up to 256 bytes. 0 on a bad argument. */
+ * (2 * n_tok * n_in), each rounded up to 256 bytes. 0 on a bad argument.
+ * When qgemm expands Q4_K blocks inside the GEMM, the W part holds the
+ * f32 partial products of a k split instead (never more than it has room
+ * for: the split is chosen to fit). */
 size_t qgemm_workspace_bytes(int type, int64_t n_out, int64_t n_in, int64_t n_tok);
 
 /* The product for many tokens at once (prefill): y[t][o] = sum_i
